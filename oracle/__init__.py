@@ -1,0 +1,229 @@
+"""CPU oracle for broadcasting elementwise binary ops — TEST INFRASTRUCTURE.
+
+Plain C++ (``zr_oracle.cpp``, single thread, binary64 accumulation, built with
+``-O2 -ffp-contract=off``), wrapped here with ctypes.  Only ``tests/``,
+``__graft_entry__.smoke()`` and the CPU-baseline / reference legs of
+``bench.py`` may import this package.  The product library never does, and the
+two share no code.
+
+What it computes follows the "Zero" book (ismantic.github.io/zero):
+Operator page, sections "逐元素算子" (elementwise ops) and "广播"
+(broadcasting, sum back to shape); Tensor page, section "形状与步长"
+(shape and strides); GPU page, section "OpAdd" (add's local derivative).
+sub/div backward use the calculus rules (g, -g) and (g/b, -g*a/b^2), which
+the pages leave unstated.
+
+Pins (tests/test_oracle_pins.py, all CPU): the pages' printed broadcast,
+stride and transposed-view examples, the worked gradient z = x*y + x at
+x=3, y=2, NumPy broadcasting and float32 arithmetic, float64 central
+finite differences, closed forms of sum-to-shape, and scatter-vs-gather
+agreement.  Every function here is pinned by at least one of them.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "zr_oracle.cpp")
+_LIB = os.path.join(_HERE, "_build", "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+ADD, SUB, MUL, DIV = 0, 1, 2, 3
+OPS = {"add": ADD, "sub": SUB, "mul": MUL, "div": DIV}
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle to ``oracle/_build/liboracle.so`` (g++, -O2, no FP contraction)."""
+    os.makedirs(os.path.dirname(_LIB), exist_ok=True)
+    if (not force and os.path.exists(_LIB)
+            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
+        return _LIB
+    tmp = f"{_LIB}.{os.getpid()}.tmp"
+    cmd = ["g++", "-std=c++17", "-O2", "-ffp-contract=off", "-fno-fast-math",
+           "-fPIC", "-shared", "-o", tmp, _SRC]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            _lib = ctypes.CDLL(build())
+            i64p = ctypes.POINTER(ctypes.c_int64)
+            vp = ctypes.c_void_p
+            ci = ctypes.c_int
+            ten = [vp, ci, i64p, i64p]
+            _lib.orc_contiguous_strides.argtypes = [ci, i64p, i64p]
+            _lib.orc_broadcast_shape.argtypes = [ci, i64p, ci, i64p, ctypes.POINTER(ci), i64p]
+            _lib.orc_binary_fwd.argtypes = [ci] + ten + ten + [vp]
+            _lib.orc_binary_fwd_at.argtypes = [ci] + ten + ten + [ctypes.c_int64, i64p, vp]
+            _lib.orc_binary_bwd.argtypes = [ci] + ten + ten + ten + [vp, vp, vp, vp]
+            _lib.orc_binary_bwd_at.argtypes = [ci, ci] + ten + ten + ten + [ctypes.c_int64, i64p, vp, vp]
+            _lib.orc_sum_to_shape.argtypes = ten + [ci, i64p, vp, vp]
+            _lib.orc_sum_to_shape_at.argtypes = ten + [ci, i64p, ctypes.c_int64, i64p, vp, vp]
+            for f in ("orc_contiguous_strides", "orc_broadcast_shape", "orc_binary_fwd",
+                      "orc_binary_fwd_at", "orc_binary_bwd", "orc_binary_bwd_at",
+                      "orc_sum_to_shape", "orc_sum_to_shape_at"):
+                getattr(_lib, f).restype = ci
+    return _lib
+
+
+class OracleError(RuntimeError):
+    pass
+
+
+def _check(rc: int, what: str) -> None:
+    if rc != 0:
+        raise OracleError(f"{what}: oracle returned {rc}")
+
+
+def _i64(seq):
+    arr = (ctypes.c_int64 * max(1, len(seq)))(*[int(s) for s in seq])
+    return arr
+
+
+class _T:
+    """A strided float32 host view: (base pointer, sizes, element strides).
+
+    Accepts a torch CPU tensor (any strides, storage offset included in
+    ``data_ptr()``), a NumPy array, or ``None`` with an explicit shape (for
+    operands whose data the op does not read).
+    """
+
+    def __init__(self, x, shape=None):
+        self.keep = x
+        if x is None:
+            self.ptr = None
+            self.sizes = list(shape)
+            self.strides = None
+        elif hasattr(x, "data_ptr"):  # torch tensor
+            import torch
+            if x.dtype != torch.float32 or x.device.type != "cpu":
+                raise TypeError("oracle takes float32 CPU tensors")
+            self.ptr = x.data_ptr() if x.numel() > 0 else None
+            self.sizes = list(x.shape)
+            self.strides = list(x.stride())
+        else:
+            x = np.asarray(x)
+            if x.dtype != np.float32:
+                raise TypeError("oracle takes float32 arrays")
+            self.keep = x
+            self.ptr = x.ctypes.data if x.size > 0 else None
+            self.sizes = list(x.shape)
+            self.strides = [s // 4 for s in x.strides]
+        self._sz = _i64(self.sizes)
+        self._st = _i64(self.strides) if self.strides is not None else None
+
+    def args(self):
+        return [self.ptr, len(self.sizes), self._sz, self._st]
+
+
+def contiguous_strides(shape):
+    lib = _load()
+    out = (ctypes.c_int64 * max(1, len(shape)))()
+    _check(lib.orc_contiguous_strides(len(shape), _i64(shape), out), "contiguous_strides")
+    return tuple(out[i] for i in range(len(shape)))
+
+
+def broadcast_shape(shape_a, shape_b):
+    """Broadcast shape, or raise OracleError if incompatible."""
+    lib = _load()
+    nd = ctypes.c_int(0)
+    out = (ctypes.c_int64 * 8)()
+    _check(lib.orc_broadcast_shape(len(shape_a), _i64(shape_a), len(shape_b), _i64(shape_b),
+                                   ctypes.byref(nd), out), "broadcast_shape")
+    return tuple(out[i] for i in range(nd.value))
+
+
+def binary_fwd(op, a, b):
+    """out = a op b, dense row-major float32 of the broadcast shape."""
+    lib = _load()
+    op = OPS.get(op, op)
+    ta, tb = _T(a), _T(b)
+    shape = broadcast_shape(ta.sizes, tb.sizes)
+    out = np.empty(shape, dtype=np.float32)
+    _check(lib.orc_binary_fwd(op, *ta.args(), *tb.args(), out.ctypes.data if out.size else None),
+           "binary_fwd")
+    return out
+
+
+def binary_fwd_at(op, a, b, idx):
+    """Forward values at output linear indices ``idx`` (row-major)."""
+    lib = _load()
+    op = OPS.get(op, op)
+    ta, tb = _T(a), _T(b)
+    idx = np.ascontiguousarray(idx, dtype=np.int64)
+    vals = np.empty(idx.shape, dtype=np.float32)
+    _check(lib.orc_binary_fwd_at(op, *ta.args(), *tb.args(), idx.size,
+                                 idx.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
+                                 vals.ctypes.data if vals.size else None), "binary_fwd_at")
+    return vals
+
+
+def binary_bwd(op, g, a, b, want_a=True, want_b=True, shape_a=None, shape_b=None):
+    """(grad_a, grad_b, abs_a, abs_b): gradients dense in each input's shape,
+    plus sum|term| per gradient element (float64).  Pass ``a``/``b`` as None
+    with ``shape_a``/``shape_b`` when the op does not read them."""
+    lib = _load()
+    op = OPS.get(op, op)
+    tg, ta, tb = _T(g), _T(a, shape_a), _T(b, shape_b)
+    ga = np.empty(ta.sizes, dtype=np.float32) if want_a else None
+    gb = np.empty(tb.sizes, dtype=np.float32) if want_b else None
+    sa = np.empty(ta.sizes, dtype=np.float64) if want_a else None
+    sb = np.empty(tb.sizes, dtype=np.float64) if want_b else None
+
+    def p(x):
+        return None if x is None else x.ctypes.data
+
+    _check(lib.orc_binary_bwd(op, *tg.args(), *ta.args(), *tb.args(), p(ga), p(gb), p(sa), p(sb)),
+           "binary_bwd")
+    return ga, gb, sa, sb
+
+
+def binary_bwd_at(op, which, g, a, b, idx, shape_a=None, shape_b=None):
+    """Gradient values (and sum|term|) of grad_a (which=0) or grad_b (which=1)
+    at linear indices ``idx`` of that input's dense row-major shape."""
+    lib = _load()
+    op = OPS.get(op, op)
+    tg, ta, tb = _T(g), _T(a, shape_a), _T(b, shape_b)
+    idx = np.ascontiguousarray(idx, dtype=np.int64)
+    vals = np.empty(idx.shape, dtype=np.float32)
+    sabs = np.empty(idx.shape, dtype=np.float64)
+    _check(lib.orc_binary_bwd_at(op, which, *tg.args(), *ta.args(), *tb.args(), idx.size,
+                                 idx.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
+                                 vals.ctypes.data if vals.size else None,
+                                 sabs.ctypes.data if sabs.size else None), "binary_bwd_at")
+    return vals, sabs
+
+
+def sum_to_shape(x, shape):
+    """(out, abs): binary64 sums of x down to ``shape`` rounded once, and sum|x|."""
+    lib = _load()
+    tx = _T(x)
+    out = np.empty(shape, dtype=np.float32)
+    sabs = np.empty(shape, dtype=np.float64)
+    _check(lib.orc_sum_to_shape(*tx.args(), len(shape), _i64(shape),
+                                out.ctypes.data if out.size else None,
+                                sabs.ctypes.data if sabs.size else None), "sum_to_shape")
+    return out, sabs
+
+
+def sum_to_shape_at(x, shape, idx):
+    lib = _load()
+    tx = _T(x)
+    idx = np.ascontiguousarray(idx, dtype=np.int64)
+    vals = np.empty(idx.shape, dtype=np.float32)
+    sabs = np.empty(idx.shape, dtype=np.float64)
+    _check(lib.orc_sum_to_shape_at(*tx.args(), len(shape), _i64(shape), idx.size,
+                                   idx.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
+                                   vals.ctypes.data if vals.size else None,
+                                   sabs.ctypes.data if sabs.size else None), "sum_to_shape_at")
+    return vals, sabs
