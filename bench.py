@@ -1,0 +1,565 @@
+#!/usr/bin/env python
+"""Benchmark of broadcasting elementwise binary ops (forward + fused
+backward) on GB300: effective HBM GB/s against the HBM roofline.
+
+One step = every op of the five seeded synthetic workloads (forward chain,
+then fused backward with sum-to-shape), issued through the C ABI on
+device-resident inputs:
+
+  c1  mul      [32,64,128] * [64,1]
+  c2  bias add [4096,1024] + [1024]
+  c3  affine   ([16,1024,768] * [768]) + [768]
+  c4  scores   ([8,12,1024,1024] + causal mask [1,1,1024,1024]) / [8.0]
+  c5a sub      transposed view [128,256,512] - [1,256,1]
+  c5b div      [4,1,8,1,16,1,32,64] / [1,6,1,12,1,10,1,64]
+
+value = algorithmic bytes of the step (each op reads every input once and
+writes every output once) / device time of the step (CUDA events, L2
+flushed before each step).  ``--impl reference`` times the CPU oracle on a
+bounded sample of the same workload instead.
+
+Launch: ``python bench.py --gpus N --steps K --warmup W``; for N > 1 under
+torchrun, every rank runs its own replica of the step (weak scaling, no
+collective on the data path) and rank 0 prints the line.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "effective HBM GB/s (and % of GB300 peak) for broadcast binary fwd+bwd"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+SUITE = ["c1", "c2", "c3", "c4", "c5a", "c5b"]
+WORKLOAD_DESC = ("five-workload suite c1..c5b (c1 mul [32,64,128]x[64,1]; c2 bias add "
+                 "[4096,1024]+[1024]; c3 affine [16,1024,768]; c4 causal-mask add + /8 on "
+                 "[8,12,1024,1024]; c5a transposed-view sub [128,256,512]-[1,256,1]; c5b 8-d div "
+                 "to [4,6,8,12,16,10,32,64]) fwd+bwd")
+KERNEL_SOURCES = ["broadcast_elementwise_shape_gb300/csrc/zr_kernels.cuh",
+                  "broadcast_elementwise_shape_gb300/csrc/zr_internal.h",
+                  "broadcast_elementwise_shape_gb300/csrc/zr_plan.cpp"]
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["zr", "reference"], default="zr")
+    p.add_argument("--workload", default="suite", help="suite or one of " + ",".join(SUITE))
+    p.add_argument("--e2e-steps", type=int, default=3)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    a = p.parse_args()
+    if a.warmup < 3:
+        p.error("--warmup must be >= 3")
+    return a
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def kernel_hash():
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ------------------------------------------------------------------ op list
+
+def op_bytes(step, shapes):
+    """Algorithmic bytes of one op: read each input once, write each output once."""
+    if step[0] == "fwd":
+        _, op, an, bn, on = step
+        return 4 * (shapes[an] + shapes[bn] + shapes[on])
+    _, op, gn, an, bn, gan, gbn = step
+    reads_a = op in ("mul", "div")
+    reads_b = op in ("mul", "div")
+    return 4 * (shapes[gn] + (shapes[an] if reads_a else 0) + (shapes[bn] if reads_b else 0)
+                + shapes[gan] + shapes[gbn])
+
+
+def numel(shape):
+    n = 1
+    for s in shape:
+        n *= int(s)
+    return n
+
+
+def shape_table(name, host):
+    """Element counts of every tensor named in a workload's steps."""
+    sizes = {k: v.numel() for k, v in host.items()}
+    shapes = {k: tuple(v.shape) for k, v in host.items()}
+    for step in workloads.STEPS[name]:
+        if step[0] == "fwd":
+            _, op, an, bn, on = step
+            import numpy as np
+            shapes[on] = tuple(np.broadcast_shapes(shapes[an], shapes[bn]))
+            sizes[on] = numel(shapes[on])
+        else:
+            _, op, gn, an, bn, gan, gbn = step
+            shapes[gan], shapes[gbn] = shapes[an], shapes[bn]
+            sizes[gan], sizes[gbn] = sizes[an], sizes[bn]
+    return sizes, shapes
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi sampling (every 100 ms) stamped with host time."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid=None):
+        self.samples = []
+        self.proc = None
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "100"]
+        if uuid:
+            cmd += ["-i", uuid]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.th = threading.Thread(target=self._read, daemon=True)
+        self.th.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.monotonic(), [x.strip() for x in line.split(",")]))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+        win = [s for t, s in self.samples if t0 <= t <= t1]
+        if not win:  # very short timed region: nearest samples
+            win = [min(self.samples, key=lambda ts: abs(ts[0] - (t0 + t1) / 2))[1]]
+        sm = [float(s[1]) for s in win if s[1].replace(".", "").isdigit()]
+        smax = [float(s[2]) for s in win if s[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for s in win for i in range(4)
+                          if len(s) > 5 + i and s[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
+                "samples": len(win)}
+
+
+# ------------------------------------------------------------------ zr arm
+
+class Suite:
+    """Device tensors, preallocated outputs/workspaces and prepared C-ABI
+    calls for the chosen workloads."""
+
+    def __init__(self, names, device):
+        import torch
+        import broadcast_elementwise_shape_gb300 as zr
+        from broadcast_elementwise_shape_gb300 import ZrTensor
+        self.zr = zr
+        self.L = zr.lib()
+        self.torch = torch
+        self.device = device
+        self.calls = []       # (config, kind, op, bytes, launches, fn)
+        self.host = {}
+        self.dev = {}
+        self.in_names = {}
+        self.out_names = {}
+        self._keep = []
+        i64p = ctypes.POINTER(ctypes.c_int64)
+        L = self.L
+        L.zr_test_describe_bwd.argtypes = [ctypes.c_int, ZrTensor, ZrTensor, ZrTensor,
+                                           ctypes.c_void_p, ctypes.c_void_p, ctypes.c_char_p,
+                                           ctypes.c_size_t]
+        L.zr_test_describe_fwd.argtypes = [ctypes.c_int, ZrTensor, ZrTensor, ctypes.c_void_p,
+                                           i64p, ctypes.c_char_p, ctypes.c_size_t]
+        for name in names:
+            host = workloads.make_inputs(name)
+            sizes, shapes = shape_table(name, host)
+            env = {}
+            for k, v in host.items():
+                env[k] = self._to_dev(v)
+            outs = []
+            for step in workloads.STEPS[name]:
+                if step[0] == "fwd":
+                    on = step[4]
+                    env[on] = torch.empty(shapes[on], dtype=torch.float32, device=device)
+                    outs.append(on)
+                else:
+                    for gname in step[5:7]:
+                        env[gname] = torch.empty(shapes[gname], dtype=torch.float32, device=device)
+                        outs.append(gname)
+            self.host[name] = host
+            self.dev[name] = env
+            self.in_names[name] = list(host)
+            self.out_names[name] = outs
+            for step in workloads.STEPS[name]:
+                self.calls.append(self._prepare(name, step, env, sizes))
+
+    def _to_dev(self, v):
+        torch = self.torch
+        if v.is_contiguous():
+            return v.to(self.device)
+        base = v._base if v._base is not None else v
+        d = base.contiguous().to(self.device)
+        return d.as_strided(v.shape, v.stride(), v.storage_offset() - base.storage_offset())
+
+    def _desc(self, t):
+        d, keep = self.zr._desc(t)
+        self._keep.append(keep)
+        return d
+
+    def _prepare(self, name, step, env, sizes):
+        zr, L, torch = self.zr, self.L, self.torch
+        stream_of = lambda: ctypes.c_void_p(torch.cuda.current_stream(self.device).cuda_stream)
+        opc = zr.OPS[step[1]]
+        nbytes = op_bytes(step, sizes)
+        if step[0] == "fwd":
+            _, op, an, bn, on = step
+            da, db = self._desc(env[an]), self._desc(env[bn])
+            out = env[on]
+            ost = zr._i64(out.stride())
+            self._keep.append(ost)
+            ptr = out.data_ptr()
+            buf = ctypes.create_string_buffer(2048)
+            assert L.zr_test_describe_fwd(opc, da, db, ptr, ost, buf, 2048) == 0
+            launches = 0 if json.loads(buf.value.decode()).get("kernel") == "none" else 1
+
+            def fn(da=da, db=db, ptr=ptr, ost=ost):
+                rc = L.zr_binary_fwd(opc, da, db, ptr, ost, stream_of())
+                if rc:
+                    raise zr.ZrError(rc, f"{name} fwd {op}")
+            return (name, "fwd", op, nbytes, launches, fn)
+        _, op, gn, an, bn, gan, gbn = step
+        dg, da, db = self._desc(env[gn]), self._desc(env[an]), self._desc(env[bn])
+        pa, pb = env[gan].data_ptr(), env[gbn].data_ptr()
+        need = ctypes.c_size_t(0)
+        rc = L.zr_binary_bwd(opc, dg, da, db, pa, pb, None, ctypes.byref(need), None)
+        assert rc == 0, rc
+        ws = torch.empty(max(16, need.value), dtype=torch.uint8, device=self.device)
+        self._keep.append(ws)
+        buf = ctypes.create_string_buffer(8192)
+        assert L.zr_test_describe_bwd(opc, dg, da, db, pa, pb, buf, 8192) == 0
+        desc = json.loads(buf.value.decode())
+        launches = sum(1 + (p.get("nslots", 1) > 1) for p in desc.get("plans", []))
+        wsz = ws.numel()
+
+        def fn(dg=dg, da=da, db=db, pa=pa, pb=pb, wsp=ws.data_ptr(), wsz=wsz):
+            n = ctypes.c_size_t(wsz)
+            rc = L.zr_binary_bwd(opc, dg, da, db, pa, pb, wsp, ctypes.byref(n), stream_of())
+            if rc:
+                raise zr.ZrError(rc, f"{name} bwd {op}")
+        return (name, "bwd", op, nbytes, launches, fn)
+
+    def step_bytes(self):
+        return sum(c[3] for c in self.calls)
+
+    def launches(self):
+        return sum(c[4] for c in self.calls)
+
+
+def run_zr(args, rank, world, local):
+    import torch
+    import torch.distributed as dist
+
+    import __graft_entry__
+    __graft_entry__.build()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (no CPU fallback)")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=device)
+    names = SUITE if args.workload == "suite" else [args.workload]
+    suite = Suite(names, device)
+    nbytes = suite.step_bytes()
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def one_step(events=None):
+        for i, c in enumerate(suite.calls):
+            if events is not None:
+                events[i][0].record(stream)
+            c[5]()
+            if events is not None:
+                events[i][1].record(stream)
+
+    for _ in range(args.warmup):
+        flush.fill_(0.0)
+        one_step()
+    torch.cuda.synchronize()
+
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(device).uuid)
+        if not uuid.startswith("GPU-"):
+            uuid = "GPU-" + uuid
+    except Exception:
+        uuid = None
+    sampler = ClockSampler(uuid) if rank == 0 else None
+    if sampler:
+        time.sleep(0.35)
+        if not sampler.samples and uuid:
+            sampler.stop()
+            sampler = ClockSampler(None)
+            time.sleep(0.35)
+    ncalls = len(suite.calls)
+    steps_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(args.steps)]
+    op_ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(ncalls)] for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.monotonic()
+    for k in range(args.steps):
+        flush.fill_(0.0)
+        steps_ev[k][0].record(stream)
+        one_step(op_ev[k])
+        steps_ev[k][1].record(stream)
+    torch.cuda.synchronize()
+    t1 = time.monotonic()
+    if world > 1:
+        dist.barrier()
+    step_ms = [s.elapsed_time(e) for s, e in steps_ev]
+    total_ms = sum(step_ms)
+    op_ms = [[op_ev[k][i][0].elapsed_time(op_ev[k][i][1]) for k in range(args.steps)]
+             for i in range(ncalls)]
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    clocks = sampler.summary(t0, t1) if sampler else None
+
+    e2e = None
+    if not args.no_e2e and rank == 0:
+        e2e = run_e2e(args, suite, flush, stream, nbytes)
+    if sampler:
+        sampler.stop()
+
+    if rank == 0:
+        peak, peak_kind = measured_peak()
+        value = world * nbytes * args.steps / (total_ms * 1e-3) / 1e9
+        per_op = []
+        for i, c in enumerate(suite.calls):
+            mean = statistics.fmean(op_ms[i])
+            med = statistics.median(op_ms[i])
+            per_op.append({"config": c[0], "kind": c[1], "op": c[2], "bytes": c[3],
+                           "launches": c[4], "ms_mean": round(mean, 5), "ms_median": round(med, 5),
+                           "gbs": round(c[3] / (mean * 1e-3) / 1e9, 1)})
+        dom = max(range(ncalls), key=lambda i: statistics.fmean(op_ms[i]))
+        dom_gbs = suite.calls[dom][3] / (statistics.fmean(op_ms[dom]) * 1e-3) / 1e9
+        traffic = read_traffic(suite.calls[dom])
+        roofline = {"bound": "hbm", "achieved": round(dom_gbs, 1), "peak": peak, "unit": "GB/s",
+                    "frac": round(dom_gbs / peak, 4), "traffic": traffic,
+                    "kernel": f"{suite.calls[dom][0]} {suite.calls[dom][1]} {suite.calls[dom][2]}",
+                    "peak_kind": peak_kind}
+        cpu = None
+        if not args.no_cpu_baseline and world == 1:
+            cpu = cpu_baseline()
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(total_ms / args.steps, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": WORKLOAD_DESC if args.workload == "suite" else args.workload,
+                       "bytes_per_step": nbytes,
+                       "l2": "flushed before every step (2x L2 write, outside the timed events)",
+                       "pct_of_measured_hbm": round(value / world / peak, 4),
+                       "pct_of_nominal_8000": round(value / world / NOMINAL_HBM_GBS, 4)},
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": suite.launches() * args.steps, "clocks": clocks, "per_op": per_op,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_e2e(args, suite, flush, stream, nbytes):
+    """Same metric with host buffers: every step copies the inputs from pinned
+    host memory, runs the ops and copies every output back."""
+    import torch
+    pinned_in, pinned_out = [], []
+    h2d = d2h = 0
+    for name in suite.dev:
+        env = suite.dev[name]
+        for k in suite.in_names[name]:
+            t = env[k]
+            src = suite.host[name][k]
+            hp = torch.empty_like(src, device="cpu").pin_memory() if src.is_contiguous() else None
+            if hp is None:  # a view: copy its storage
+                base = src._base if src._base is not None else src
+                hb = base.contiguous().pin_memory()
+                db = t._base if t._base is not None else t
+                pinned_in.append((db, hb))
+                h2d += hb.numel() * 4
+            else:
+                hp.copy_(src)
+                pinned_in.append((t, hp))
+                h2d += hp.numel() * 4
+        for k in suite.out_names[name]:
+            t = env[k]
+            hp = torch.empty(t.shape, dtype=torch.float32).pin_memory()
+            pinned_out.append((hp, t))
+            d2h += hp.numel() * 4
+    ev = []
+    steps = max(1, args.e2e_steps)
+    for k in range(steps + 1):  # first iteration is a warm-up
+        flush.fill_(0.0)
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        for dst, src in pinned_in:
+            dst.copy_(src, non_blocking=True)
+        for c in suite.calls:
+            c[5]()
+        for dst, src in pinned_out:
+            dst.copy_(src, non_blocking=True)
+        e.record(stream)
+        if k > 0:
+            ev.append((s, e))
+    torch.cuda.synchronize()
+    ms = statistics.fmean(s.elapsed_time(e) for s, e in ev)
+    return {"value": round(nbytes / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 3),
+            "steps": steps}
+
+
+def read_traffic(call):
+    """DRAM bytes per launch of the dominant op from the committed ncu
+    summary, if it was taken on the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)
+    except Exception:
+        return None
+    if t.get("kernel_hash") != kernel_hash():
+        return None
+    key = f"{call[0]} {call[1]} {call[2]}"
+    v = t.get("per_op_dram_bytes", {}).get(key)
+    return v
+
+
+# ------------------------------------------------------------------ oracle (CPU)
+
+def oracle_sample(names):
+    """Run the oracle over the complete fwd+bwd of the named workloads;
+    returns (seconds, algorithmic bytes, output elements)."""
+    import oracle
+    oracle.build()
+    total_bytes = 0
+    elems = 0
+    t_total = 0.0
+    for name in names:
+        host = workloads.make_inputs(name)
+        sizes, _ = shape_table(name, host)
+        env = dict(host)
+        t = time.perf_counter()
+        for step in workloads.STEPS[name]:
+            total_bytes += op_bytes(step, sizes)
+            if step[0] == "fwd":
+                _, op, an, bn, on = step
+                env[on] = oracle.binary_fwd(op, env[an], env[bn])
+                elems += sizes[on]
+            else:
+                _, op, gn, an, bn, gan, gbn = step
+                ga, gb, _, _ = oracle.binary_bwd(op, env[gn], env[an], env[bn])
+                env[gan], env[gbn] = ga, gb
+                elems += sizes[gn]
+        t_total += time.perf_counter() - t
+    return t_total, total_bytes, elems
+
+
+def cpu_baseline():
+    names = ["c1", "c2", "c3"]
+    secs, nbytes, elems = oracle_sample(names)
+    return {"value": round(nbytes / secs / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": "complete fwd+bwd of c1, c2 and c3 (single-thread C++ oracle, binary64 "
+                      f"accumulation); {elems} op-elements in {secs:.2f} s",
+            "seconds": round(secs, 3)}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    # Each step is a bounded sample of the suite, sized so that K + W steps
+    # stay within a few minutes of CPU time.
+    names = ["c1", "c2"] if args.steps + args.warmup <= 40 else ["c1"]
+    for _ in range(args.warmup):
+        oracle_sample(names)
+    times, nbytes = [], 0
+    for _ in range(args.steps):
+        s, b, _ = oracle_sample(names)
+        times.append(s)
+        nbytes = b
+    total = sum(times)
+    value = nbytes * len(times) / total / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * total / len(times), 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "bounded sample of the suite per step: complete fwd+bwd of "
+                               + " and ".join(names)},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": "complete fwd+bwd of " + " and ".join(names)
+                                   + " per step (single-thread C++ oracle)"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    if args.gpus > 1 and world == 1:
+        raise SystemExit("--gpus > 1 needs torchrun (one process per GPU)")
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    run_zr(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,699 @@
+// zr_api.cu — the C ABI (include/zr.h): argument checks, planning and
+// launches.  Every check runs on the host before the first launch (Zero book,
+// Operator page, section 逐元素算子: shape and broadcast checks belong to the
+// operator layer), so an error never leaves a partial write.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstring>
+#include <string>
+
+#include "../../include/zr.h"
+#include "../../include/zr_testing.h"
+#include "zr_launch.h"
+#include "zr_plan.h"
+
+namespace zr {
+namespace {
+
+bool op_ok(int op) { return op >= OP_ADD && op <= OP_DIV; }
+
+// Which inputs a gradient's local term reads (mul: the other input; div:
+// b for grad_a, a and b for grad_b).
+bool needs_a(int op, int which) { return which == 1 && (op == OP_MUL || op == OP_DIV); }
+bool needs_b(int op, int which) {
+  return (which == 0 && (op == OP_MUL || op == OP_DIV)) || (which == 1 && op == OP_DIV);
+}
+
+// Byte interval [lo, hi) touched by a tensor (empty when numel == 0).
+struct Span {
+  uintptr_t lo = 0, hi = 0;
+};
+Span span_of(const void* p, int64_t extent) {
+  Span s;
+  if (p && extent > 0) {
+    s.lo = reinterpret_cast<uintptr_t>(p);
+    s.hi = s.lo + uintptr_t(extent) * sizeof(float);
+  }
+  return s;
+}
+bool overlaps(const Span& x, const Span& y) {
+  return x.hi > x.lo && y.hi > y.lo && x.lo < y.hi && y.lo < x.hi;
+}
+
+// Sufficient condition for a strided view to address every element once:
+// sorted by stride, each stride exceeds the extent of all smaller dims.
+bool non_overlapping(const TDesc& t) {
+  int idx[kMaxDims];
+  int m = 0;
+  for (int i = 0; i < t.nd; ++i)
+    if (t.size[i] > 1) idx[m++] = i;
+  std::sort(idx, idx + m, [&](int x, int y) { return t.stride[x] < t.stride[y]; });
+  int64_t reach = 0;  // largest offset reachable with the dims seen so far
+  for (int i = 0; i < m; ++i) {
+    const int d = idx[i];
+    if (t.stride[d] <= reach) return false;
+    reach += (t.size[d] - 1) * t.stride[d];
+  }
+  return true;
+}
+
+bool same_layout(const TDesc& x, const TDesc& y) {
+  if (x.ptr != y.ptr || x.nd != y.nd) return false;
+  for (int i = 0; i < x.nd; ++i) {
+    if (x.size[i] != y.size[i]) return false;
+    if (x.size[i] > 1 && x.stride[i] != y.stride[i]) return false;
+  }
+  return true;
+}
+
+bool is_reduced(const TDesc& x, int n, const int64_t* out_size) {
+  for (int od = 0; od < n; ++od) {
+    const int d = od - (n - x.nd);
+    if (out_size[od] != 1 && (d < 0 || x.size[d] == 1)) return true;
+  }
+  return false;
+}
+
+TDesc dense_desc(const float* p, int nd, const int64_t* size) {
+  TDesc t;
+  t.ptr = p;
+  t.nd = nd;
+  int64_t n = 1;
+  for (int i = 0; i < nd; ++i) {
+    t.size[i] = size[i];
+    n *= size[i];
+  }
+  t.numel = n;
+  contiguous_strides(nd, t.size, t.stride);
+  t.extent = n;
+  return t;
+}
+
+int check_device_ptr(const void* p) {
+  if (p == nullptr) return ZR_ERR_NULL;
+  cudaPointerAttributes at;
+  const cudaError_t e = cudaPointerGetAttributes(&at, p);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return ZR_ERR_DEVICE;
+  }
+  if (at.type == cudaMemoryTypeUnregistered) return ZR_ERR_DEVICE;
+  if (at.type == cudaMemoryTypeHost && at.devicePointer == nullptr) return ZR_ERR_DEVICE;
+  if (at.type == cudaMemoryTypeDevice) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+      cudaGetLastError();
+      return ZR_ERR_DEVICE;
+    }
+    if (at.device != dev) return ZR_ERR_DEVICE;
+  }
+  return ZR_OK;
+}
+
+// ------------------------------------------------------------------ forward
+
+struct FwdSet {
+  int op = 0;
+  bool empty = false;
+  EwBuild eb;
+  TDesc a, b, out;
+};
+
+int plan_fwd(int op, const zr_tensor& ta, const zr_tensor& tb, const float* out,
+             const int64_t* out_strides, FwdSet* S) {
+  if (!op_ok(op)) return ZR_ERR_NULL;
+  S->op = op;
+  int rc = read_tensor(ta, &S->a);
+  if (rc) return rc;
+  rc = read_tensor(tb, &S->b);
+  if (rc) return rc;
+  int n = 0;
+  int64_t osz[kMaxDims];
+  rc = broadcast_sizes(S->a.nd, S->a.size, S->b.nd, S->b.size, &n, osz);
+  if (rc) return rc;
+  zr_tensor to{out, n, osz, out_strides};
+  rc = read_tensor(to, &S->out);
+  if (rc) return rc;
+  if (S->out.numel == 0) {
+    S->empty = true;
+    return ZR_OK;
+  }
+  if (!S->a.ptr || !S->b.ptr || !out) return ZR_ERR_NULL;
+  if (!non_overlapping(S->out)) return ZR_ERR_LAYOUT;
+  const Span so = span_of(out, S->out.extent);
+  for (const TDesc* x : {&S->a, &S->b}) {
+    if (overlaps(so, span_of(x->ptr, x->extent)) && !same_layout(*x, S->out)) return ZR_ERR_LAYOUT;
+  }
+  int64_t st[kProbSlots][kMaxDims] = {};
+  align_strides(S->a, n, osz, st[0]);
+  align_strides(S->b, n, osz, st[1]);
+  for (int d = 0; d < n; ++d) st[kSlotOut][d] = osz[d] == 1 ? 0 : S->out.stride[d];
+  Prob P;
+  rc = coalesce(n, osz, st, (1u << 0) | (1u << 1) | (1u << kSlotOut), kSlotOut, &P);
+  if (rc) return rc;
+  const float* in[3] = {S->a.ptr, S->b.ptr, nullptr};
+  float* outs[2] = {const_cast<float*>(out), nullptr};
+  const uint32_t stream_mask = (S->a.numel == S->out.numel ? 1u : 0u) |
+                               (S->b.numel == S->out.numel ? 2u : 0u);
+  return build_ew(P, in, outs, 0x3u, stream_mask, &S->eb);
+}
+
+// ------------------------------------------------------------------ backward
+
+struct BwdSet {
+  int op = 0;
+  bool nothing = false;          // no gradient requested
+  bool empty = false;            // grad_out empty: only zero fills
+  bool direct = false;           // elementwise plan (no reduction)
+  int want = 0;                  // bit 0 grad_a, bit 1 grad_b
+  EwBuild eb;
+  int nred = 0;
+  int which[2] = {0, 0};
+  RedBuild rb[2];
+  size_t ws_off[2] = {0, 0};
+  size_t ws_run = 0;             // bytes this call uses
+  size_t ws_query = 0;           // bytes reported by a workspace query
+  float* zero_ptr[2] = {nullptr, nullptr};
+  size_t zero_bytes[2] = {0, 0};
+  TDesc g, a, b, ga, gb;
+};
+
+int plan_bwd(int op, const zr_tensor& tg, const zr_tensor& ta, const zr_tensor& tb, float* grad_a,
+             float* grad_b, BwdSet* S) {
+  if (!op_ok(op)) return ZR_ERR_NULL;
+  S->op = op;
+  int rc = read_tensor(tg, &S->g);
+  if (rc) return rc;
+  rc = read_tensor(ta, &S->a);
+  if (rc) return rc;
+  rc = read_tensor(tb, &S->b);
+  if (rc) return rc;
+  int n = 0;
+  int64_t osz[kMaxDims];
+  rc = broadcast_sizes(S->a.nd, S->a.size, S->b.nd, S->b.size, &n, osz);
+  if (rc) return rc;
+  if (S->g.nd != n) return ZR_ERR_SHAPE;
+  for (int d = 0; d < n; ++d)
+    if (S->g.size[d] != osz[d]) return ZR_ERR_SHAPE;
+  S->want = (grad_a ? 1 : 0) | (grad_b ? 2 : 0);
+  if (S->want == 0) {
+    S->nothing = true;
+    return ZR_OK;
+  }
+  S->ga = dense_desc(grad_a, S->a.nd, S->a.size);
+  S->gb = dense_desc(grad_b, S->b.nd, S->b.size);
+  const bool red_a = grad_a && is_reduced(S->a, n, osz);
+  const bool red_b = grad_b && is_reduced(S->b, n, osz);
+  const bool read_a = (grad_a && needs_a(op, 0)) || (grad_b && needs_a(op, 1));
+  const bool read_b = (grad_a && needs_b(op, 0)) || (grad_b && needs_b(op, 1));
+
+  // Layout: the two gradients are disjoint; a gradient may alias grad_out
+  // exactly only when it has grad_out's shape and grad_out is dense (then each
+  // element is read and written by the same thread); any other overlap with
+  // an input is refused.
+  const Span sga = span_of(grad_a, S->ga.extent);
+  const Span sgb = span_of(grad_b, S->gb.extent);
+  if (overlaps(sga, sgb)) return ZR_ERR_LAYOUT;
+  struct In { const TDesc* t; bool read; };
+  const In ins[3] = {{&S->g, true}, {&S->a, read_a}, {&S->b, read_b}};
+  for (int w = 0; w < 2; ++w) {
+    const TDesc& gd = w == 0 ? S->ga : S->gb;
+    const Span& sp = w == 0 ? sga : sgb;
+    const bool reduced = w == 0 ? red_a : red_b;
+    if (!gd.ptr) continue;
+    for (int i = 0; i < 3; ++i) {
+      if (!ins[i].read || !ins[i].t->ptr) continue;
+      if (!overlaps(sp, span_of(ins[i].t->ptr, ins[i].t->extent))) continue;
+      const bool ok = i == 0 && !reduced && same_layout(gd, S->g);
+      if (!ok) return ZR_ERR_LAYOUT;
+    }
+  }
+
+  if (S->g.numel == 0) {
+    S->empty = true;
+    if (grad_a && S->ga.numel > 0) { S->zero_ptr[0] = grad_a; S->zero_bytes[0] = S->ga.numel * 4; }
+    if (grad_b && S->gb.numel > 0) { S->zero_ptr[1] = grad_b; S->zero_bytes[1] = S->gb.numel * 4; }
+    return ZR_OK;
+  }
+  if (!S->g.ptr || (read_a && !S->a.ptr) || (read_b && !S->b.ptr)) return ZR_ERR_NULL;
+
+  int64_t st[kProbSlots][kMaxDims] = {};
+  align_strides(S->g, n, osz, st[0]);
+  if (read_a) align_strides(S->a, n, osz, st[1]);
+  if (read_b) align_strides(S->b, n, osz, st[2]);
+  int64_t dense[kMaxDims];
+  contiguous_strides(n, osz, dense);
+  for (int d = 0; d < n; ++d) st[kSlotOut][d] = osz[d] == 1 ? 0 : dense[d];
+  if (grad_a) grad_index_strides(S->a, n, osz, st[kSlotXA]);
+  if (grad_b) grad_index_strides(S->b, n, osz, st[kSlotXB]);
+  const uint32_t read_mask = 1u | (read_a ? 2u : 0u) | (read_b ? 4u : 0u);
+  const uint32_t stream_mask = 1u | (S->a.numel == S->g.numel ? 2u : 0u) |
+                               (S->b.numel == S->g.numel ? 4u : 0u);
+
+  if (!red_a && !red_b) {
+    S->direct = true;
+    Prob P;
+    rc = coalesce(n, osz, st, read_mask | (1u << kSlotOut), -1, &P);
+    if (rc) return rc;
+    const float* in[3] = {S->g.ptr, S->a.ptr, S->b.ptr};
+    float* outs[2] = {grad_a, grad_b};
+    return build_ew(P, in, outs, read_mask, stream_mask, &S->eb);
+  }
+
+  // One reduced gradient, the other written densely in the same pass (or
+  // not requested); or both reduced, one reduction pass each.
+  const bool dense_other = (red_a != red_b) && ((red_a && grad_b) || (red_b && grad_a));
+  uint32_t active = read_mask;
+  if (dense_other) active |= 1u << kSlotOut;
+  if (red_a) active |= 1u << kSlotXA;
+  if (red_b) active |= 1u << kSlotXB;
+  Prob P;
+  rc = coalesce(n, osz, st, active, -1, &P);
+  if (rc) return rc;
+  size_t off = 0, off_q = 0;
+  for (int w = 0; w < 2; ++w) {
+    const bool red = w == 0 ? red_a : red_b;
+    if (!red) continue;
+    float* xo = w == 0 ? grad_a : grad_b;
+    float* d_out = dense_other ? (w == 0 ? grad_b : grad_a) : nullptr;
+    const int xslot = w == 0 ? kSlotXA : kSlotXB;
+    // Only the operands this gradient's terms need are read in its pass.
+    const bool ra = needs_a(op, w) || (d_out && needs_a(op, 1 - w));
+    const bool rbb = needs_b(op, w) || (d_out && needs_b(op, 1 - w));
+    const uint32_t rm = 1u | (ra ? 2u : 0u) | (rbb ? 4u : 0u);
+    RedBuild& rb = S->rb[S->nred];
+    rc = build_red(P, xslot, S->g.ptr, ra ? S->a.ptr : nullptr, rbb ? S->b.ptr : nullptr, rm,
+                   stream_mask & rm, xo, d_out, 0, &rb);
+    if (rc) return rc;
+    size_t q = rb.ws_bytes;
+    for (int v : {1, 4}) {
+      RedBuild tmp;
+      rc = build_red(P, xslot, S->g.ptr, nullptr, nullptr, rm, 0, xo, d_out, v, &tmp);
+      if (rc) return rc;
+      q = std::max(q, tmp.ws_bytes);
+    }
+    S->ws_off[S->nred] = off;
+    off += rb.ws_bytes;
+    off_q += q;
+    S->which[S->nred] = w;
+    ++S->nred;
+  }
+  S->ws_run = off;
+  S->ws_query = off_q;
+  return ZR_OK;
+}
+
+// ------------------------------------------------------------------ sum to shape
+
+struct SumSet {
+  bool empty = false;
+  bool copy = false;
+  EwBuild eb;
+  RedBuild rb;
+  size_t ws_query = 0;
+  float* zero_ptr = nullptr;
+  size_t zero_bytes = 0;
+  TDesc in, out;
+};
+
+int plan_sum(const zr_tensor& tin, int32_t ndo, const int64_t* so, float* out, SumSet* S) {
+  int rc = read_tensor(tin, &S->in);
+  if (rc) return rc;
+  zr_tensor to{out, ndo, so, nullptr};
+  if (ndo > 0 && so == nullptr) return ZR_ERR_NULL;
+  rc = read_tensor(to, &S->out);
+  if (rc) return rc;
+  int n = 0;
+  int64_t bsz[kMaxDims];
+  rc = broadcast_sizes(S->in.nd, S->in.size, S->out.nd, S->out.size, &n, bsz);
+  if (rc) return rc;
+  if (n != S->in.nd) return ZR_ERR_SHAPE;
+  for (int d = 0; d < n; ++d)
+    if (bsz[d] != S->in.size[d]) return ZR_ERR_SHAPE;
+  const bool reduced = is_reduced(S->out, n, S->in.size);
+  const Span sout = span_of(out, S->out.extent);
+  if (overlaps(sout, span_of(S->in.ptr, S->in.extent)) &&
+      (reduced || !same_layout(S->out, S->in)))
+    return ZR_ERR_LAYOUT;
+  if (S->in.numel == 0) {
+    S->empty = true;
+    if (S->out.numel > 0) { S->zero_ptr = out; S->zero_bytes = S->out.numel * 4; }
+    return ZR_OK;
+  }
+  if (!S->in.ptr || !out) return ZR_ERR_NULL;
+  int64_t st[kProbSlots][kMaxDims] = {};
+  align_strides(S->in, n, S->in.size, st[0]);
+  Prob P;
+  if (!reduced) {
+    S->copy = true;
+    int64_t dense[kMaxDims];
+    contiguous_strides(n, S->in.size, dense);
+    for (int d = 0; d < n; ++d) st[kSlotOut][d] = S->in.size[d] == 1 ? 0 : dense[d];
+    rc = coalesce(n, S->in.size, st, 1u | (1u << kSlotOut), -1, &P);
+    if (rc) return rc;
+    const float* in[3] = {S->in.ptr, nullptr, nullptr};
+    float* outs[2] = {out, nullptr};
+    return build_ew(P, in, outs, 1u, 1u, &S->eb);
+  }
+  grad_index_strides(S->out, n, S->in.size, st[kSlotXA]);
+  rc = coalesce(n, S->in.size, st, 1u | (1u << kSlotXA), -1, &P);
+  if (rc) return rc;
+  rc = build_red(P, kSlotXA, S->in.ptr, nullptr, nullptr, 1u, 1u, out, nullptr, 0, &S->rb);
+  if (rc) return rc;
+  S->ws_query = S->rb.ws_bytes;
+  for (int v : {1, 4}) {
+    RedBuild tmp;
+    rc = build_red(P, kSlotXA, S->in.ptr, nullptr, nullptr, 1u, 0, out, nullptr, v, &tmp);
+    if (rc) return rc;
+    S->ws_query = std::max(S->ws_query, tmp.ws_bytes);
+  }
+  return ZR_OK;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? ZR_OK : ZR_ERR_CUDA; }
+
+int copy_json(const std::string& s, char* buf, size_t len) {
+  if (!buf || len == 0) return ZR_ERR_NULL;
+  const size_t m = std::min(len - 1, s.size());
+  std::memcpy(buf, s.data(), m);
+  buf[m] = '\0';
+  return ZR_OK;
+}
+
+}  // namespace
+}  // namespace zr
+
+using namespace zr;
+
+extern "C" {
+
+int zr_broadcast_shape(int32_t ndim_a, const int64_t* sizes_a, int32_t ndim_b,
+                       const int64_t* sizes_b, int32_t* ndim_out, int64_t sizes_out[ZR_MAX_DIMS]) {
+  if (!ndim_out || !sizes_out) return ZR_ERR_NULL;
+  if (ndim_a < 0 || ndim_a > kMaxDims || ndim_b < 0 || ndim_b > kMaxDims) return ZR_ERR_RANK;
+  if ((ndim_a > 0 && !sizes_a) || (ndim_b > 0 && !sizes_b)) return ZR_ERR_NULL;
+  int n = 0;
+  int64_t so[kMaxDims];
+  const int rc = broadcast_sizes(ndim_a, sizes_a, ndim_b, sizes_b, &n, so);
+  if (rc) return rc;
+  *ndim_out = n;
+  for (int i = 0; i < n; ++i) sizes_out[i] = so[i];
+  return ZR_OK;
+}
+
+int zr_binary_fwd(zr_op op, zr_tensor a, zr_tensor b, float* out, const int64_t* out_strides,
+                  zr_stream_t stream) {
+  FwdSet S;
+  int rc = plan_fwd(op, a, b, out, out_strides, &S);
+  if (rc) return rc;
+  if (S.empty) return ZR_OK;
+  for (const void* p : {static_cast<const void*>(S.a.ptr), static_cast<const void*>(S.b.ptr),
+                        static_cast<const void*>(out)}) {
+    rc = check_device_ptr(p);
+    if (rc) return rc;
+  }
+  return cuda_status(launch_fwd(op, S.eb, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int zr_binary_bwd(zr_op op, zr_tensor grad_out, zr_tensor a, zr_tensor b, float* grad_a,
+                  float* grad_b, void* workspace, size_t* workspace_bytes, zr_stream_t stream) {
+  if (!workspace_bytes) return ZR_ERR_NULL;
+  BwdSet S;
+  int rc = plan_bwd(op, grad_out, a, b, grad_a, grad_b, &S);
+  if (rc) return rc;
+  if (workspace == nullptr) {
+    *workspace_bytes = S.ws_query;
+    return ZR_OK;
+  }
+  if (S.nothing) return ZR_OK;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (S.empty) {
+    for (int w = 0; w < 2; ++w) {
+      if (!S.zero_ptr[w]) continue;
+      rc = check_device_ptr(S.zero_ptr[w]);
+      if (rc) return rc;
+    }
+    for (int w = 0; w < 2; ++w)
+      if (S.zero_ptr[w] && cudaMemsetAsync(S.zero_ptr[w], 0, S.zero_bytes[w], st) != cudaSuccess)
+        return ZR_ERR_CUDA;
+    return ZR_OK;
+  }
+  if (S.ws_run > 0) {
+    if (*workspace_bytes < S.ws_run) return ZR_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(workspace) % 16 != 0) return ZR_ERR_WORKSPACE;
+  }
+  // Device checks on every pointer that will be touched.
+  const void* ptrs[6] = {S.g.ptr, nullptr, nullptr, grad_a, grad_b,
+                         S.ws_run > 0 ? workspace : nullptr};
+  const bool ra = (grad_a && needs_a(op, 0)) || (grad_b && needs_a(op, 1));
+  const bool rb = (grad_a && needs_b(op, 0)) || (grad_b && needs_b(op, 1));
+  if (ra) ptrs[1] = S.a.ptr;
+  if (rb) ptrs[2] = S.b.ptr;
+  for (const void* p : ptrs) {
+    if (!p) continue;
+    rc = check_device_ptr(p);
+    if (rc) return rc;
+  }
+  if (S.direct) return cuda_status(launch_bwd_direct(op, S.want, S.eb, st));
+  for (int i = 0; i < S.nred; ++i) {
+    RedBuild rbi = S.rb[i];
+    rbi.plan.partial = reinterpret_cast<float*>(static_cast<char*>(workspace) + S.ws_off[i]);
+    rbi.comb.partial = rbi.plan.partial;
+    rc = cuda_status(launch_reduce(op, S.which[i], rbi, st));
+    if (rc) return rc;
+  }
+  return ZR_OK;
+}
+
+int zr_sum_to_shape(zr_tensor in, int32_t ndim_out, const int64_t* sizes_out, float* out,
+                    void* workspace, size_t* workspace_bytes, zr_stream_t stream) {
+  if (!workspace_bytes) return ZR_ERR_NULL;
+  SumSet S;
+  int rc = plan_sum(in, ndim_out, sizes_out, out, &S);
+  if (rc) return rc;
+  if (workspace == nullptr) {
+    *workspace_bytes = S.ws_query;
+    return ZR_OK;
+  }
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (S.empty) {
+    if (!S.zero_ptr) return ZR_OK;
+    rc = check_device_ptr(S.zero_ptr);
+    if (rc) return rc;
+    return cuda_status(cudaMemsetAsync(S.zero_ptr, 0, S.zero_bytes, st));
+  }
+  const size_t need = S.copy ? 0 : S.rb.ws_bytes;
+  if (need > 0) {
+    if (*workspace_bytes < need) return ZR_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(workspace) % 16 != 0) return ZR_ERR_WORKSPACE;
+  }
+  for (const void* p : {static_cast<const void*>(S.in.ptr), static_cast<const void*>(out),
+                        need > 0 ? static_cast<const void*>(workspace) : nullptr}) {
+    if (!p) continue;
+    rc = check_device_ptr(p);
+    if (rc) return rc;
+  }
+  if (S.copy) return cuda_status(launch_copy(S.eb, st));
+  RedBuild rb = S.rb;
+  rb.plan.partial = static_cast<float*>(workspace);
+  rb.comb.partial = rb.plan.partial;
+  return cuda_status(launch_reduce(OP_ADD, 2, rb, st));
+}
+
+const char* zr_status_string(int status) {
+  switch (status) {
+    case ZR_OK: return "ZR_OK";
+    case ZR_ERR_NULL: return "ZR_ERR_NULL: required pointer is NULL or op code unknown";
+    case ZR_ERR_RANK: return "ZR_ERR_RANK: ndim < 0 or ndim > 8";
+    case ZR_ERR_SHAPE: return "ZR_ERR_SHAPE: shapes not broadcastable or wrong grad_out shape";
+    case ZR_ERR_SIZE: return "ZR_ERR_SIZE: negative size or stride, or index range overflow";
+    case ZR_ERR_LAYOUT: return "ZR_ERR_LAYOUT: output overlaps itself, an input or another output";
+    case ZR_ERR_DEVICE: return "ZR_ERR_DEVICE: pointer not addressable by the current device";
+    case ZR_ERR_WORKSPACE: return "ZR_ERR_WORKSPACE: workspace too small or misaligned";
+    case ZR_ERR_CUDA: return "ZR_ERR_CUDA: CUDA call or kernel launch failed";
+    default: return "unknown zr status";
+  }
+}
+
+// ------------------------------------------------------------------ test hooks
+
+int zr_test_fastdiv(uint32_t d, uint32_t n, uint32_t* q) {
+  if (!q || d == 0) return ZR_ERR_NULL;
+  *q = fd_div(make_fastdiv(d), n);
+  return ZR_OK;
+}
+
+int zr_test_describe_fwd(zr_op op, zr_tensor a, zr_tensor b, const float* out,
+                         const int64_t* out_strides, char* buf, size_t len) {
+  FwdSet S;
+  const int rc = plan_fwd(op, a, b, out, out_strides, &S);
+  if (rc) return rc;
+  return copy_json(S.empty ? std::string("{\"kernel\":\"none\"}") : describe_ew(S.eb), buf, len);
+}
+
+int zr_test_describe_bwd(zr_op op, zr_tensor grad_out, zr_tensor a, zr_tensor b,
+                         const float* grad_a, const float* grad_b, char* buf, size_t len) {
+  BwdSet S;
+  const int rc = plan_bwd(op, grad_out, a, b, const_cast<float*>(grad_a),
+                          const_cast<float*>(grad_b), &S);
+  if (rc) return rc;
+  std::string s;
+  if (S.nothing || S.empty) {
+    s = "{\"kernel\":\"none\",\"ws_query\":" + std::to_string(S.ws_query) + "}";
+  } else if (S.direct) {
+    s = "{\"plans\":[" + describe_ew(S.eb) + "],\"ws_run\":0,\"ws_query\":" +
+        std::to_string(S.ws_query) + "}";
+  } else {
+    s = "{\"plans\":[";
+    for (int i = 0; i < S.nred; ++i) {
+      if (i) s += ",";
+      s += describe_red(S.rb[i]);
+    }
+    s += "],\"which\":[" + std::to_string(S.which[0]) +
+         (S.nred > 1 ? "," + std::to_string(S.which[1]) : std::string()) +
+         "],\"ws_run\":" + std::to_string(S.ws_run) + ",\"ws_query\":" + std::to_string(S.ws_query) + "}";
+  }
+  return copy_json(s, buf, len);
+}
+
+int zr_test_describe_sum(zr_tensor in, int32_t ndim_out, const int64_t* sizes_out,
+                         const float* out, char* buf, size_t len) {
+  SumSet S;
+  const int rc = plan_sum(in, ndim_out, sizes_out, const_cast<float*>(out), &S);
+  if (rc) return rc;
+  std::string s;
+  if (S.empty) s = "{\"kernel\":\"none\"}";
+  else if (S.copy) s = "{\"plans\":[" + describe_ew(S.eb) + "],\"ws_query\":0}";
+  else s = "{\"plans\":[" + describe_red(S.rb) + "],\"ws_query\":" + std::to_string(S.ws_query) + "}";
+  return copy_json(s, buf, len);
+}
+
+}  // extern "C"
+
+namespace zr {
+namespace {
+
+// Host walk of k_elementwise's (CTA, item, lane) space.
+template <class Rec>
+void walk_ew(const EwBuild& eb, Rec rec) {
+  const EwPlan& p = eb.plan;
+  for (uint32_t cta = 0; cta < p.n_cta; ++cta) {
+    const EwTile t = ew_tile(p, cta);
+    for (uint32_t item = 0; item < p.items_per_cta; ++item) {
+      const uint32_t ri = fd_div(p.tile_vcols_div, item);
+      const uint32_t vc = item - ri * p.tile_vcols;
+      if (!(ri < t.nrows && vc < t.nvcols)) continue;
+      int64_t off[kMaxOperands];
+      decomp_offsets(p.rows, t.row0 + ri, off);
+      for (int i = 0; i < eb.vec; ++i) {
+        const int64_t c = int64_t(t.vcol0 + vc) * eb.vec + i;
+        if (c >= p.ncol) continue;
+        int64_t o[kMaxOperands];
+        for (int k = 0; k < kMaxOperands; ++k) o[k] = off[k] + c * p.inner_stride[k];
+        rec(o);
+      }
+    }
+  }
+}
+
+// Host walk of k_reduce's (CTA, row, column, lane) space.
+template <class Rec>
+void walk_red(const RedBuild& rb, Rec rec) {
+  const RedPlan& p = rb.plan;
+  for (uint32_t cta = 0; cta < p.n_cta; ++cta) {
+    const RedCta c = red_cta(p, cta);
+    int64_t base[kMaxOperands];
+    decomp_offsets(p.kept, c.kidx, base);
+    const uint32_t row0 = c.rblk * p.rows_per_blk;
+    const uint32_t nrows = std::min(p.rows_per_blk, p.n_red - row0);
+    const uint32_t vb = c.cblk * p.vcols_per_blk;
+    const uint32_t ve = std::min(vb + p.vcols_per_blk, p.nvcol);
+    for (uint32_t r = 0; r < nrows; ++r) {
+      int64_t off[kMaxOperands];
+      decomp_offsets(p.red, row0 + r, off);
+      for (uint32_t vc = vb; vc < ve; ++vc) {
+        for (int i = 0; i < rb.vec; ++i) {
+          const int64_t col = int64_t(vc) * rb.vec + i;
+          if (col >= p.ncol) continue;
+          int64_t o[kMaxOperands];
+          for (int k = 0; k < kMaxOperands; ++k) o[k] = base[k] + off[k] + col * p.inner_stride[k];
+          const int64_t x = p.inner_kept ? int64_t(c.kidx) * p.ncol + col : int64_t(c.kidx);
+          const int64_t slot = p.inner_kept ? c.rblk : int64_t(c.rblk) * p.n_cblk + c.cblk;
+          rec(o, x, slot);
+        }
+      }
+    }
+  }
+}
+
+}  // namespace
+}  // namespace zr
+
+extern "C" {
+
+int zr_test_emulate_fwd(zr_tensor a, zr_tensor b, const float* out, const int64_t* out_strides,
+                        int64_t cap, int64_t* rec, int64_t* nrec) {
+  if (!rec || !nrec) return ZR_ERR_NULL;
+  FwdSet S;
+  const int rc = plan_fwd(OP_ADD, a, b, out, out_strides, &S);
+  if (rc) return rc;
+  int64_t m = 0;
+  bool over = false;
+  if (!S.empty) {
+    walk_ew(S.eb, [&](const int64_t* o) {
+      if (m >= cap) { over = true; return; }
+      rec[3 * m + 0] = o[kSlotOut];
+      rec[3 * m + 1] = o[0];
+      rec[3 * m + 2] = o[1];
+      ++m;
+    });
+  }
+  *nrec = m;
+  return over ? ZR_ERR_SIZE : ZR_OK;
+}
+
+int zr_test_emulate_bwd(zr_op op, zr_tensor grad_out, zr_tensor a, zr_tensor b,
+                        const float* grad_a, const float* grad_b, int64_t cap, int64_t* rec,
+                        int64_t* nrec) {
+  if (!rec || !nrec) return ZR_ERR_NULL;
+  BwdSet S;
+  const int rc = plan_bwd(op, grad_out, a, b, const_cast<float*>(grad_a),
+                          const_cast<float*>(grad_b), &S);
+  if (rc) return rc;
+  int64_t m = 0;
+  bool over = false;
+  auto put = [&](int64_t plan, const int64_t* o, uint32_t rmask, int64_t x, int64_t slot,
+                 bool has_d) {
+    if (m >= cap) { over = true; return; }
+    int64_t* r = rec + 7 * m;
+    r[0] = plan;
+    r[1] = o[0];
+    r[2] = (rmask & 2) ? o[1] : -1;
+    r[3] = (rmask & 4) ? o[2] : -1;
+    r[4] = x;
+    r[5] = slot;
+    r[6] = has_d ? o[kSlotOut] : -1;
+    ++m;
+  };
+  if (!S.nothing && !S.empty) {
+    if (S.direct) {
+      const uint32_t rm = 1u | (S.eb.plan.in[1] && ((S.want & 2) && needs_a(op, 1)) ? 2u : 0u) |
+                          (S.eb.plan.in[2] && (((S.want & 1) && needs_b(op, 0)) ||
+                                               ((S.want & 2) && needs_b(op, 1))) ? 4u : 0u);
+      walk_ew(S.eb, [&](const int64_t* o) { put(0, o, rm, -1, -1, true); });
+    } else {
+      for (int i = 0; i < S.nred; ++i) {
+        const RedPlan& p = S.rb[i].plan;
+        const uint32_t rm = 1u | (p.a ? 2u : 0u) | (p.b ? 4u : 0u);
+        walk_red(S.rb[i], [&](const int64_t* o, int64_t x, int64_t slot) {
+          put(i, o, rm, x, slot, p.d_out != nullptr);
+        });
+      }
+    }
+  }
+  *nrec = m;
+  return over ? ZR_ERR_SIZE : ZR_OK;
+}
+
+}  // extern "C"

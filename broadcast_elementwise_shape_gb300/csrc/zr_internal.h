@@ -1,0 +1,192 @@
+// zr_internal.h — plan structures shared by the host planner and the CUDA
+// kernels.  Everything here is plain data passed to kernels by value (the
+// "DimsArg" idea of the Zero book's GPU page, section Kernel 派发: up to eight
+// dimensions travel as kernel parameters, with no metadata copies), plus the
+// integer fast-divmod used to turn a linear index into coordinates, and the
+// block/item index maps that both the kernels and the host-side plan checker
+// use.
+#pragma once
+
+#include <stdint.h>
+#include <stddef.h>
+
+#if defined(__CUDACC__)
+#define ZR_HD __host__ __device__ __forceinline__
+#else
+#define ZR_HD inline
+#endif
+
+namespace zr {
+
+constexpr int kMaxDims = 8;
+// Operand slots of a plan.  Slots 0..2 are inputs, slot 3 the output offset.
+// Forward: A, B, -, OUT.  Backward: G (grad_out), A, B, D (a gradient that
+// has the output's shape, written densely).
+constexpr int kMaxOperands = 4;
+constexpr int kSlotOut = 3;
+
+enum OpCode : int32_t { OP_ADD = 0, OP_SUB = 1, OP_MUL = 2, OP_DIV = 3 };
+
+// ---------------------------------------------------------------------------
+// Division by an invariant unsigned 32-bit integer with one multiply-high,
+// one add and one shift (T. Granlund and P. L. Montgomery, "Division by
+// invariant integers using multiplication", PLDI 1994, section 4): with
+// l = ceil(log2 d) and m = floor(2^32 * (2^l - d) / d) + 1,
+// floor(n / d) = (mulhi(m, n) + n) >> l for every 0 <= n < 2^32.  The sum is
+// formed in 64 bits, so no overflow correction is needed, and d = 1 works
+// with l = 0, m = 1 (mulhi gives 0).
+struct FastDiv {
+  uint32_t d;  // divisor, >= 1
+  uint32_t m;  // magic multiplier
+  uint32_t l;  // shift
+};
+
+inline FastDiv make_fastdiv(uint32_t d) {
+  FastDiv f;
+  f.d = d == 0 ? 1 : d;
+  uint32_t l = 0;
+  while (l < 32 && (uint64_t(1) << l) < f.d) ++l;
+  f.l = l;
+  // (2^l - d) < d <= 2^32, so the product fits in 64 bits and m < 2^32.
+  const uint64_t two32 = uint64_t(1) << 32;
+  f.m = static_cast<uint32_t>((two32 * ((uint64_t(1) << l) - f.d)) / f.d + 1);
+  return f;
+}
+
+ZR_HD uint32_t fd_div(const FastDiv& f, uint32_t n) {
+#if defined(__CUDA_ARCH__)
+  const uint32_t t = __umulhi(n, f.m);
+#else
+  const uint32_t t = static_cast<uint32_t>((uint64_t(n) * f.m) >> 32);
+#endif
+  return static_cast<uint32_t>((uint64_t(t) + n) >> f.l);
+}
+
+// Decomposition of a row-major linear index over up to eight dimensions,
+// innermost first, accumulating per-operand element offsets.
+struct Decomp {
+  int32_t n;                                  // number of dims (0 = none)
+  FastDiv div[kMaxDims];                      // sizes, innermost first
+  int64_t stride[kMaxOperands][kMaxDims];     // per operand, innermost first
+};
+
+ZR_HD void decomp_offsets(const Decomp& dc, uint32_t idx, int64_t* off) {
+  for (int k = 0; k < kMaxOperands; ++k) off[k] = 0;
+  for (int i = 0; i < dc.n; ++i) {
+    const uint32_t q = fd_div(dc.div[i], idx);
+    const uint32_t c = idx - q * dc.div[i].d;
+    idx = q;
+#if defined(__CUDA_ARCH__)
+#pragma unroll
+#endif
+    for (int k = 0; k < kMaxOperands; ++k) off[k] += int64_t(c) * dc.stride[k][i];
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Elementwise tile plan (forward; backward when no gradient is reduced;
+// sum-to-shape without reduction).  The coalesced output is viewed as
+// rows x columns: columns = the innermost coalesced dim (ncol), rows = all
+// outer dims (nrow, row-major).  A CTA covers tile_rows consecutive rows and
+// tile_vcols vectors of VEC columns; a per-CTA table in shared memory holds
+// each row's operand offsets, so index decomposition runs once per row, not
+// once per element.
+struct EwPlan {
+  const float* in[3];       // forward: a, b; backward: g, a, b
+  float* out[2];            // forward: out; backward: grad_a, grad_b
+  Decomp rows;              // decomposition of the row index (outer dims)
+  int64_t inner_stride[kMaxOperands];
+  uint32_t stream_mask;     // bit k: input k is full-size (read once)
+  uint32_t nrow;            // number of rows
+  uint32_t ncol;            // columns per row
+  uint32_t nvcol;           // column vectors per row = ceil(ncol / VEC)
+  uint32_t tile_rows;       // rows per CTA tile (<= kMaxTileRows)
+  uint32_t tile_vcols;      // column vectors per CTA tile
+  uint32_t col_tiles;       // tiles along a row
+  FastDiv col_tiles_div;    // blockIdx -> (row tile, column tile)
+  FastDiv tile_vcols_div;   // item -> (row in tile, column vector)
+  uint32_t items_per_cta;   // tile_rows * tile_vcols
+  uint32_t n_cta;
+};
+
+constexpr uint32_t kMaxTileRows = 512;
+constexpr int kThreads = 256;
+
+// CTA -> (first row, first column vector, rows in tile, vectors in tile).
+struct EwTile {
+  uint32_t row0, vcol0, nrows, nvcols;
+};
+ZR_HD EwTile ew_tile(const EwPlan& p, uint32_t cta) {
+  EwTile t;
+  const uint32_t rt = fd_div(p.col_tiles_div, cta);
+  const uint32_t ct = cta - rt * p.col_tiles;
+  t.row0 = rt * p.tile_rows;
+  t.vcol0 = ct * p.tile_vcols;
+  const uint32_t rleft = p.nrow - t.row0;
+  const uint32_t vleft = p.nvcol - t.vcol0;
+  t.nrows = rleft < p.tile_rows ? rleft : p.tile_rows;
+  t.nvcols = vleft < p.tile_vcols ? vleft : p.tile_vcols;
+  return t;
+}
+
+// ---------------------------------------------------------------------------
+// Reduction plan: one gradient X (or the output of sum-to-shape) that sums
+// terms over its broadcast dims, optionally writing one dense gradient D in
+// the same pass.  Outer dims split into kept dims K' (X has them) and
+// reduced dims R'.  The innermost dim is either kept by X (threads own
+// columns and add rows) or reduced (all threads of a CTA add into one value
+// per kept index).  Each CTA writes one partial per output it touches, to a
+// fixed slot; a second pass adds the slots in order.  No atomics anywhere.
+struct RedPlan {
+  const float* g;           // grad_out (or sum-to-shape input)
+  const float* a;
+  const float* b;
+  float* x_final;           // X, dense in its own shape (when nslots == 1)
+  float* partial;           // workspace partials [nslots][nout] (nslots > 1)
+  float* d_out;             // dense gradient written in the same pass, or null
+  Decomp kept;              // kept outer dims; operands G, A, B, D
+  Decomp red;               // reduced outer dims; operands G, A, B, D
+  int64_t inner_stride[kMaxOperands];  // G, A, B, D strides along the inner dim
+  uint32_t stream_mask;     // bit k: input k is full-size (read once)
+  uint32_t n_kept;          // product of kept outer sizes
+  uint32_t n_red;           // product of reduced outer sizes (rows)
+  uint32_t ncol;            // inner dim size
+  uint32_t nvcol;           // ceil(ncol / VEC)
+  uint32_t inner_kept;      // 1: inner dim kept by X; 0: reduced
+  uint32_t tx, ty;          // thread layout: tx column lanes x ty row lanes
+  uint32_t rows_per_blk;    // rows of the reduced range per CTA (<= kMaxTileRows)
+  uint32_t vcols_per_blk;   // column vectors per CTA (multiple of tx)
+  uint32_t n_rblk;          // row blocks
+  uint32_t n_cblk;          // column blocks
+  FastDiv n_cblk_div;
+  FastDiv n_rblk_div;
+  uint64_t nout;            // elements of X
+  uint32_t nslots;          // partial slots per output (1 = final write)
+  uint32_t n_cta;
+  float scale;              // multiplies X's final value (1 except as noted)
+};
+
+struct RedCta {
+  uint32_t kidx, rblk, cblk;
+};
+// CTA order: column blocks fastest, then row blocks, then kept index.
+ZR_HD RedCta red_cta(const RedPlan& p, uint32_t cta) {
+  RedCta c;
+  const uint32_t t = fd_div(p.n_cblk_div, cta);
+  c.cblk = cta - t * p.n_cblk;
+  c.kidx = fd_div(p.n_rblk_div, t);
+  c.rblk = t - c.kidx * p.n_rblk;
+  return c;
+}
+
+// Second pass: out[j] = sum over s of partial[s * nout + j], s in order.
+struct CombinePlan {
+  const float* partial;
+  float* out;
+  uint64_t nout;
+  uint32_t nslots;
+  uint32_t jx, sy;          // thread layout: jx outputs x sy slot lanes
+  float scale;
+};
+
+}  // namespace zr

@@ -1,0 +1,398 @@
+// zr_kernels.cuh — CUDA kernels (sm_103a) for broadcasting elementwise
+// binary ops, their fused backward and deterministic sum-to-shape.
+//
+// Arithmetic is explicit: __fadd_rn/__fsub_rn/__fmul_rn/__fdiv_rn are IEEE
+// binary32 operations with round-to-nearest-even that the compiler never
+// contracts into FMAs, and the library is built with -ftz=false, so a
+// forward element is exactly the one IEEE operation the Zero book's
+// Operator page (section 逐元素算子) names for it.
+#pragma once
+
+#include <cuda_runtime.h>
+#include "zr_internal.h"
+
+namespace zr {
+
+// ---------------------------------------------------------------- arithmetic
+
+template <int OP>
+__device__ __forceinline__ float fwd_op(float x, float y) {
+  if (OP == OP_ADD) return __fadd_rn(x, y);
+  if (OP == OP_SUB) return __fsub_rn(x, y);
+  if (OP == OP_MUL) return __fmul_rn(x, y);
+  return __fdiv_rn(x, y);
+}
+
+// Local gradient terms.  add (g, g) — GPU page, section OpAdd; mul (g*b, g*a)
+// — Operator page, section 逐元素算子; sub (g, -g) and div (g/b, -g*a/b^2) by
+// calculus (the pages do not write them out).  Every single-operation term
+// (all but div's grad_b) is the exact IEEE result.
+template <int OP>
+__device__ __forceinline__ float term_a(float g, float a, float b) {
+  (void)a;
+  if (OP == OP_ADD || OP == OP_SUB) return g;
+  if (OP == OP_MUL) return __fmul_rn(g, b);
+  return __fdiv_rn(g, b);
+}
+template <int OP>
+__device__ __forceinline__ float term_b(float g, float a, float b) {
+  if (OP == OP_ADD) return g;
+  if (OP == OP_SUB) return -g;
+  if (OP == OP_MUL) return __fmul_rn(g, a);
+  return -__fmul_rn(__fdiv_rn(g, b), __fdiv_rn(a, b));
+}
+
+// Which inputs a gradient reads.  WHICH: 0 = grad_a, 1 = grad_b.
+template <int OP, int WHICH>
+struct Needs {
+  static constexpr bool a = (WHICH == 1) && (OP == OP_MUL || OP == OP_DIV);
+  static constexpr bool b = (WHICH == 0 && (OP == OP_MUL || OP == OP_DIV)) ||
+                            (WHICH == 1 && OP == OP_DIV);
+};
+
+// Compensated (Kahan) summation: error <= (2u + O(n u^2)) * sum|x_i| whatever
+// the number of terms (N. J. Higham, "Accuracy and Stability of Numerical
+// Algorithms", 2nd ed., section 4.3).  Explicit _rn intrinsics keep the
+// compiler from reassociating or contracting the compensation away.
+struct Kahan {
+  float s, c;
+  __device__ __forceinline__ void init() { s = 0.f; c = 0.f; }
+  __device__ __forceinline__ void add(float x) {
+    const float y = __fsub_rn(x, c);
+    const float t = __fadd_rn(s, y);
+    c = __fsub_rn(__fsub_rn(t, s), y);
+    s = t;
+  }
+};
+
+// ---------------------------------------------------------------- loads/stores
+
+template <int VEC>
+struct Vec { float v[VEC]; };
+
+// Load VEC consecutive columns of one operand in one row.  inner == 1:
+// contiguous (128-bit load when VEC == 4; the planner guarantees alignment);
+// inner == 0: the column is broadcast, one load; otherwise a strided gather.
+template <int VEC>
+__device__ __forceinline__ Vec<VEC> load_cols(const float* __restrict__ base, int64_t row_off,
+                                              int64_t inner, uint32_t c, bool streaming) {
+  Vec<VEC> r;
+  if (inner == 1) {
+    const float* p = base + row_off + c;
+    if (VEC == 4) {
+      const float4 q = streaming ? __ldcs(reinterpret_cast<const float4*>(p))
+                                 : __ldg(reinterpret_cast<const float4*>(p));
+      r.v[0] = q.x; r.v[1] = q.y; r.v[2] = q.z; r.v[VEC - 1] = q.w;
+    } else {
+      r.v[0] = streaming ? __ldcs(p) : __ldg(p);
+    }
+  } else if (inner == 0) {
+    const float s = __ldg(base + row_off);
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) r.v[i] = s;
+  } else {
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) r.v[i] = __ldg(base + row_off + int64_t(c + i) * inner);
+  }
+  return r;
+}
+
+template <int VEC>
+__device__ __forceinline__ void store_cols(float* __restrict__ base, int64_t row_off, int64_t inner,
+                                           uint32_t c, const Vec<VEC>& x) {
+  if (inner == 1) {
+    float* p = base + row_off + c;
+    if (VEC == 4) {
+      *reinterpret_cast<float4*>(p) = make_float4(x.v[0], x.v[1], x.v[2], x.v[VEC - 1]);
+    } else {
+      *p = x.v[0];
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) base[row_off + int64_t(c + i) * inner] = x.v[i];
+  }
+}
+
+// ---------------------------------------------------------------- functors
+
+// Forward: out = a op b.
+template <int OP>
+struct FwdF {
+  static constexpr bool kR1 = true, kR2 = false;  // slot 0 = a, slot 1 = b
+  template <int VEC>
+  __device__ __forceinline__ void operator()(const Vec<VEC> (&x)[3], Vec<VEC> (&y)[2]) const {
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) y[0].v[i] = fwd_op<OP>(x[0].v[i], x[1].v[i]);
+  }
+};
+
+// Backward with no reduction: grad_a and/or grad_b elementwise.
+// Inputs: slot 0 = g, 1 = a, 2 = b.  WANT: bit 0 grad_a, bit 1 grad_b.
+template <int OP, int WANT>
+struct BwdDirectF {
+  static constexpr bool kR1 = ((WANT & 1) && Needs<OP, 0>::a) || ((WANT & 2) && Needs<OP, 1>::a);
+  static constexpr bool kR2 = ((WANT & 1) && Needs<OP, 0>::b) || ((WANT & 2) && Needs<OP, 1>::b);
+  template <int VEC>
+  __device__ __forceinline__ void operator()(const Vec<VEC> (&x)[3], Vec<VEC> (&y)[2]) const {
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) {
+      if (WANT & 1) y[0].v[i] = term_a<OP>(x[0].v[i], x[1].v[i], x[2].v[i]);
+      if (WANT & 2) y[1].v[i] = term_b<OP>(x[0].v[i], x[1].v[i], x[2].v[i]);
+    }
+  }
+};
+
+// Copy (sum-to-shape onto the same shape).
+struct CopyF {
+  static constexpr bool kR1 = false, kR2 = false;
+  template <int VEC>
+  __device__ __forceinline__ void operator()(const Vec<VEC> (&x)[3], Vec<VEC> (&y)[2]) const {
+    y[0] = x[0];
+  }
+};
+
+// ---------------------------------------------------------------- elementwise
+
+// One CTA = one tile of rows x column vectors.  Each thread takes items
+// threadIdx.x + k * 256; items are processed in batches of U so that U
+// independent loads per operand are in flight before any result is stored.
+template <class F, int VEC, int NOUT>
+__global__ void __launch_bounds__(kThreads)
+k_elementwise(const __grid_constant__ EwPlan p) {
+  extern __shared__ int64_t s_off[];  // [tile_rows][kMaxOperands]
+  const EwTile t = ew_tile(p, blockIdx.x);
+  for (uint32_t i = threadIdx.x; i < t.nrows; i += blockDim.x) {
+    int64_t off[kMaxOperands];
+    decomp_offsets(p.rows, t.row0 + i, off);
+#pragma unroll
+    for (int k = 0; k < kMaxOperands; ++k) s_off[i * kMaxOperands + k] = off[k];
+  }
+  __syncthreads();
+
+  constexpr int U = 4;
+  const F f;
+  for (uint32_t it0 = 0; it0 < p.items_per_cta; it0 += U * blockDim.x) {
+    Vec<VEC> x[U][3];
+    int64_t doff[U];
+    uint32_t col[U];
+    bool ok[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const uint32_t item = it0 + u * blockDim.x + threadIdx.x;
+      const uint32_t ri = fd_div(p.tile_vcols_div, item);
+      const uint32_t vc = item - ri * p.tile_vcols;
+      ok[u] = ri < t.nrows && vc < t.nvcols;
+      col[u] = (t.vcol0 + vc) * VEC;
+      doff[u] = 0;
+      if (ok[u]) {
+        const int64_t* ro = s_off + ri * kMaxOperands;
+        x[u][0] = load_cols<VEC>(p.in[0], ro[0], p.inner_stride[0], col[u], p.stream_mask & 1);
+        if (F::kR1) x[u][1] = load_cols<VEC>(p.in[1], ro[1], p.inner_stride[1], col[u], p.stream_mask & 2);
+        if (F::kR2) x[u][2] = load_cols<VEC>(p.in[2], ro[2], p.inner_stride[2], col[u], p.stream_mask & 4);
+        doff[u] = ro[kSlotOut];
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (!ok[u]) continue;
+      Vec<VEC> y[2];
+      f(x[u], y);
+      if (p.out[0]) store_cols<VEC>(p.out[0], doff[u], p.inner_stride[kSlotOut], col[u], y[0]);
+      if (NOUT > 1 && p.out[1]) store_cols<VEC>(p.out[1], doff[u], p.inner_stride[kSlotOut], col[u], y[1]);
+    }
+  }
+}
+
+// ---------------------------------------------------------------- reduction
+
+// Term of the reduced gradient X (WHICH: 0 = a, 1 = b; 2 = sum-to-shape
+// identity) and, when the other gradient is written densely in the same pass,
+// the other term.
+template <int OP, int WHICH>
+struct RedTerms {
+  static constexpr bool kReadA = (WHICH < 2) && (Needs<OP, 0>::a || Needs<OP, 1>::a);
+  static constexpr bool kReadB = (WHICH < 2) && (Needs<OP, 0>::b || Needs<OP, 1>::b);
+  __device__ __forceinline__ static float x(float g, float a, float b) {
+    if (WHICH == 0) return term_a<OP>(g, a, b);
+    if (WHICH == 1) return term_b<OP>(g, a, b);
+    return g;
+  }
+  __device__ __forceinline__ static float d(float g, float a, float b) {
+    if (WHICH == 0) return term_b<OP>(g, a, b);
+    return term_a<OP>(g, a, b);
+  }
+};
+
+// Reduction pass.  CTA = (kept index, row block, column block).  Rows of
+// the block come from a shared-memory offset table (reduced outer dims,
+// refilled every kMaxTileRows rows), the kept index adds a CTA-wide base
+// offset.  INNER_KEPT: thread (tx, ty) owns column vector tx of the block and
+// adds rows ty, ty + ty_n, ...; then a fixed tree over ty.  Otherwise every
+// thread adds its rows and columns into one value and the CTA reduces them
+// with a fixed tree.  Per-thread sums are Kahan-compensated, so the error
+// bound does not grow with the number of rows a thread adds.
+template <int OP, int WHICH, int VEC, bool INNER_KEPT>
+__global__ void __launch_bounds__(kThreads)
+k_reduce(const __grid_constant__ RedPlan p) {
+  using T = RedTerms<OP, WHICH>;
+  extern __shared__ int64_t s_dyn[];
+  const uint32_t table_rows = p.rows_per_blk < kMaxTileRows ? p.rows_per_blk : kMaxTileRows;
+  int64_t* s_off = s_dyn;  // [table_rows][kMaxOperands]
+  float* s_red = reinterpret_cast<float*>(s_dyn + kMaxOperands * table_rows);
+
+  const RedCta cta = red_cta(p, blockIdx.x);
+  int64_t base[kMaxOperands];
+  decomp_offsets(p.kept, cta.kidx, base);
+  const uint32_t row0 = cta.rblk * p.rows_per_blk;
+  const uint32_t rleft = p.n_red - row0;
+  const uint32_t nrows = rleft < p.rows_per_blk ? rleft : p.rows_per_blk;
+
+  const uint32_t tx = threadIdx.x % p.tx;
+  const uint32_t ty = threadIdx.x / p.tx;
+  const bool has_d = p.d_out != nullptr;
+  const uint32_t vcol_begin = cta.cblk * p.vcols_per_blk;
+  const uint32_t vcol_end_raw = vcol_begin + p.vcols_per_blk;
+  const uint32_t vcol_end = vcol_end_raw < p.nvcol ? vcol_end_raw : p.nvcol;
+
+  Kahan acc[VEC];
+#pragma unroll
+  for (int i = 0; i < VEC; ++i) acc[i].init();
+
+  for (uint32_t ch0 = 0; ch0 < nrows; ch0 += kMaxTileRows) {
+    const uint32_t cleft = nrows - ch0;
+    const uint32_t nch = cleft < kMaxTileRows ? cleft : kMaxTileRows;
+    if (ch0 > 0) __syncthreads();
+    for (uint32_t i = threadIdx.x; i < nch; i += blockDim.x) {
+      int64_t off[kMaxOperands];
+      decomp_offsets(p.red, row0 + ch0 + i, off);
+#pragma unroll
+      for (int k = 0; k < kMaxOperands; ++k) s_off[i * kMaxOperands + k] = off[k] + base[k];
+    }
+    __syncthreads();
+
+    for (uint32_t vc = vcol_begin + tx; vc < vcol_end; vc += p.tx) {
+      const uint32_t c = vc * VEC;
+      constexpr int U = 4;
+      for (uint32_t r0 = ty; r0 < nch; r0 += U * p.ty) {
+        Vec<VEC> gv[U], av[U], bv[U];
+        bool ok[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const uint32_t ri = r0 + u * p.ty;
+          ok[u] = ri < nch;
+          if (ok[u]) {
+            const int64_t* ro = s_off + ri * kMaxOperands;
+            gv[u] = load_cols<VEC>(p.g, ro[0], p.inner_stride[0], c, p.stream_mask & 1);
+            if (T::kReadA) av[u] = load_cols<VEC>(p.a, ro[1], p.inner_stride[1], c, p.stream_mask & 2);
+            if (T::kReadB) bv[u] = load_cols<VEC>(p.b, ro[2], p.inner_stride[2], c, p.stream_mask & 4);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          if (!ok[u]) continue;
+          Vec<VEC> dv;
+#pragma unroll
+          for (int i = 0; i < VEC; ++i) {
+            const float gg = gv[u].v[i];
+            const float aa = T::kReadA ? av[u].v[i] : 0.f;
+            const float bb = T::kReadB ? bv[u].v[i] : 0.f;
+            if (INNER_KEPT) acc[i].add(T::x(gg, aa, bb));
+            else acc[0].add(T::x(gg, aa, bb));
+            if (has_d) dv.v[i] = T::d(gg, aa, bb);
+          }
+          if (has_d) {
+            const uint32_t ri = r0 + u * p.ty;
+            store_cols<VEC>(p.d_out, s_off[ri * kMaxOperands + kSlotOut], 1, c, dv);
+          }
+        }
+      }
+      if (INNER_KEPT) break;  // one column vector per thread
+    }
+  }
+
+  if (INNER_KEPT) {
+    // Fixed tree over the ty row lanes of each column vector (ty = 256/tx is
+    // a power of two).
+    const uint32_t lanes = p.tx * VEC;
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) s_red[ty * lanes + tx * VEC + i] = acc[i].s;
+    for (uint32_t h = p.ty >> 1; h > 0; h >>= 1) {
+      __syncthreads();
+      if (ty < h) {
+#pragma unroll
+        for (int i = 0; i < VEC; ++i)
+          s_red[ty * lanes + tx * VEC + i] =
+              __fadd_rn(s_red[ty * lanes + tx * VEC + i], s_red[(ty + h) * lanes + tx * VEC + i]);
+      }
+    }
+    __syncthreads();
+    const uint32_t vc = vcol_begin + tx;
+    if (ty == 0 && vc < vcol_end) {
+      Vec<VEC> r;
+      const uint64_t j = uint64_t(cta.kidx) * p.ncol + uint64_t(vc) * VEC;
+      float* dst;
+      if (p.nslots == 1) {
+#pragma unroll
+        for (int i = 0; i < VEC; ++i) r.v[i] = __fmul_rn(s_red[tx * VEC + i], p.scale);
+        dst = p.x_final + j;
+      } else {
+#pragma unroll
+        for (int i = 0; i < VEC; ++i) r.v[i] = s_red[tx * VEC + i];
+        dst = p.partial + uint64_t(cta.rblk) * p.nout + j;
+      }
+      store_cols<VEC>(dst, 0, 1, 0, r);
+    }
+  } else {
+    // Whole-CTA fixed tree: one value per kept index.
+    __syncthreads();
+    s_red[threadIdx.x] = acc[0].s;
+    for (uint32_t h = blockDim.x >> 1; h > 0; h >>= 1) {
+      __syncthreads();
+      if (threadIdx.x < h) s_red[threadIdx.x] = __fadd_rn(s_red[threadIdx.x], s_red[threadIdx.x + h]);
+    }
+    if (threadIdx.x == 0) {
+      const float r = s_red[0];
+      if (p.nslots == 1) {
+        p.x_final[cta.kidx] = __fmul_rn(r, p.scale);
+      } else {
+        const uint64_t slot = uint64_t(cta.rblk) * p.n_cblk + cta.cblk;
+        p.partial[slot * p.nout + cta.kidx] = r;
+      }
+    }
+  }
+}
+
+// Second pass: for each output j, add its nslots partials in slot order.
+// Thread (jx lane, sy lane) adds slots sy, sy + sy_n, ... (Kahan), then a
+// fixed tree over the sy lanes.
+static __global__ void __launch_bounds__(kThreads)
+k_combine(const __grid_constant__ CombinePlan p) {
+  __shared__ float s_red[kThreads];
+  const uint32_t jl = threadIdx.x % p.jx;
+  const uint32_t sl = threadIdx.x / p.jx;
+  const uint64_t j = uint64_t(blockIdx.x) * p.jx + jl;
+  Kahan acc;
+  acc.init();
+  if (j < p.nout && sl < p.sy) {
+    uint32_t s = sl;
+    for (; s + 3 * p.sy < p.nslots; s += 4 * p.sy) {
+      const float v0 = __ldg(p.partial + uint64_t(s) * p.nout + j);
+      const float v1 = __ldg(p.partial + uint64_t(s + p.sy) * p.nout + j);
+      const float v2 = __ldg(p.partial + uint64_t(s + 2 * p.sy) * p.nout + j);
+      const float v3 = __ldg(p.partial + uint64_t(s + 3 * p.sy) * p.nout + j);
+      acc.add(v0); acc.add(v1); acc.add(v2); acc.add(v3);
+    }
+    for (; s < p.nslots; s += p.sy) acc.add(__ldg(p.partial + uint64_t(s) * p.nout + j));
+  }
+  const uint32_t syn = blockDim.x / p.jx;  // power of two
+  s_red[sl * p.jx + jl] = (sl < p.sy) ? acc.s : 0.f;
+  for (uint32_t h = syn >> 1; h > 0; h >>= 1) {
+    __syncthreads();
+    if (sl < h) s_red[sl * p.jx + jl] = __fadd_rn(s_red[sl * p.jx + jl], s_red[(sl + h) * p.jx + jl]);
+  }
+  __syncthreads();
+  if (sl == 0 && j < p.nout) p.out[j] = __fmul_rn(s_red[jl], p.scale);
+}
+
+}  // namespace zr

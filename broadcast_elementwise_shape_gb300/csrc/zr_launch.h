@@ -1,0 +1,18 @@
+// zr_launch.h — kernel launchers (one translation unit per kernel family so
+// the library builds in parallel).
+#pragma once
+
+#include <cuda_runtime.h>
+#include "zr_plan.h"
+
+namespace zr {
+
+cudaError_t launch_fwd(int op, const EwBuild& eb, cudaStream_t s);
+// want: bit 0 grad_a, bit 1 grad_b (no reduction).
+cudaError_t launch_bwd_direct(int op, int want, const EwBuild& eb, cudaStream_t s);
+cudaError_t launch_copy(const EwBuild& eb, cudaStream_t s);
+// which: 0 = grad_a, 1 = grad_b, 2 = sum-to-shape.  Launches the reduction
+// pass and, when it writes partials, the combine pass.
+cudaError_t launch_reduce(int op, int which, const RedBuild& rb, cudaStream_t s);
+
+}  // namespace zr

@@ -1,0 +1,48 @@
+// zr_launch_red.cu — instantiations and launches of the reduction and
+// combine kernels.
+#include "zr_launch.h"
+#include "zr_kernels.cuh"
+
+namespace zr {
+
+namespace {
+
+template <int OP, int WHICH>
+cudaError_t launch_red_t(const RedBuild& rb, cudaStream_t s) {
+  const RedPlan& p = rb.plan;
+  const uint32_t table_rows = p.rows_per_blk < kMaxTileRows ? p.rows_per_blk : kMaxTileRows;
+  const size_t red_floats = p.inner_kept ? size_t(kThreads) * rb.vec : size_t(kThreads);
+  const size_t smem = size_t(table_rows) * kMaxOperands * sizeof(int64_t) + red_floats * sizeof(float);
+  if (p.inner_kept) {
+    if (rb.vec == 4) k_reduce<OP, WHICH, 4, true><<<p.n_cta, kThreads, smem, s>>>(p);
+    else k_reduce<OP, WHICH, 1, true><<<p.n_cta, kThreads, smem, s>>>(p);
+  } else {
+    if (rb.vec == 4) k_reduce<OP, WHICH, 4, false><<<p.n_cta, kThreads, smem, s>>>(p);
+    else k_reduce<OP, WHICH, 1, false><<<p.n_cta, kThreads, smem, s>>>(p);
+  }
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || p.nslots <= 1) return e;
+  const CombinePlan& c = rb.comb;
+  const uint64_t nblk = (c.nout + c.jx - 1) / c.jx;
+  k_combine<<<static_cast<unsigned>(nblk), kThreads, 0, s>>>(c);
+  return cudaGetLastError();
+}
+
+template <int OP>
+cudaError_t launch_red_op(int which, const RedBuild& rb, cudaStream_t s) {
+  return which == 0 ? launch_red_t<OP, 0>(rb, s) : launch_red_t<OP, 1>(rb, s);
+}
+
+}  // namespace
+
+cudaError_t launch_reduce(int op, int which, const RedBuild& rb, cudaStream_t s) {
+  if (which == 2) return launch_red_t<OP_ADD, 2>(rb, s);
+  switch (op) {
+    case OP_ADD: return launch_red_op<OP_ADD>(which, rb, s);
+    case OP_SUB: return launch_red_op<OP_SUB>(which, rb, s);
+    case OP_MUL: return launch_red_op<OP_MUL>(which, rb, s);
+    default: return launch_red_op<OP_DIV>(which, rb, s);
+  }
+}
+
+}  // namespace zr

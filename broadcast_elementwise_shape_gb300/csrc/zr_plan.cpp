@@ -1,0 +1,419 @@
+// zr_plan.cpp — host planner (see zr_plan.h).
+//
+// Broadcast rule: Zero book, Operator page, section 广播 — compare from the
+// last dim; equal, or one side 1, or one side missing.  A size-1 input dim
+// reads coordinate 0, which is a stride of 0 here, so no broadcast operand is
+// ever materialised.  Strides: Tensor page, section 形状与步长.
+#include "zr_plan.h"
+
+#include <algorithm>
+#include <cstdio>
+#include <limits>
+
+namespace zr {
+
+namespace {
+
+constexpr int64_t kI64Max = std::numeric_limits<int64_t>::max();
+
+bool mul_overflows(int64_t a, int64_t b) { return a != 0 && b > kI64Max / a; }
+
+uint32_t pow2_ceil(uint64_t v) {
+  uint32_t p = 1;
+  while (p < v && p < (1u << 31)) p *= 2;
+  return p;
+}
+uint64_t ceil_div(uint64_t a, uint64_t b) { return (a + b - 1) / b; }
+
+// Target elements per CTA: enough CTAs to fill 152 SMs several times over,
+// and enough bytes per thread to keep loads in flight.
+uint64_t elems_per_cta_target(uint64_t total) {
+  uint64_t e = total / 1216;
+  if (e < 4096) e = 4096;
+  if (e > 32768) e = 32768;
+  return e;
+}
+
+// Column lanes for a row of nvcol vectors: a power of two <= 256 with the
+// least padding, preferring wider.
+uint32_t pick_tx(uint64_t nvcol) {
+  if (nvcol <= 32) return pow2_ceil(nvcol);
+  uint32_t best = 32;
+  uint64_t best_waste = ceil_div(nvcol, 32) * 32 - nvcol;
+  for (uint32_t tx = 64; tx <= 256; tx *= 2) {
+    const uint64_t waste = ceil_div(nvcol, tx) * tx - nvcol;
+    if (waste <= best_waste) { best = tx; best_waste = waste; }
+  }
+  return best;
+}
+
+void fill_decomp(Decomp* dc, const Prob& P, const int* dims, int nd) {
+  // dims: outer dims in row-major order; the decomposition is innermost first.
+  dc->n = nd;
+  for (int i = 0; i < nd; ++i) {
+    const int d = dims[nd - 1 - i];
+    dc->div[i] = make_fastdiv(static_cast<uint32_t>(P.size[d]));
+    for (int k = 0; k < kMaxOperands; ++k) dc->stride[k][i] = P.st[k][d];
+  }
+  for (int i = nd; i < kMaxDims; ++i) {
+    dc->div[i] = make_fastdiv(1);
+    for (int k = 0; k < kMaxOperands; ++k) dc->stride[k][i] = 0;
+  }
+}
+
+// VEC = 4 is allowed when every slot that is read or written with unit inner
+// stride starts 16-byte aligned and every row start stays aligned.
+bool vec4_ok(const Prob& P, uint32_t slots, const void* const* ptrs) {
+  const int n = P.n;
+  if (P.size[n - 1] % 4 != 0) return false;
+  bool any_unit = false;
+  for (int k = 0; k < kMaxOperands; ++k) {
+    if (!(slots & (1u << k))) continue;
+    if (P.st[k][n - 1] != 1) continue;
+    any_unit = true;
+    if (reinterpret_cast<uintptr_t>(ptrs[k]) % 16 != 0) return false;
+    for (int d = 0; d < n - 1; ++d)
+      if (P.st[k][d] % 4 != 0) return false;
+  }
+  return any_unit;
+}
+
+}  // namespace
+
+int read_tensor(const zr_tensor& t, TDesc* d) {
+  if (t.ndim < 0 || t.ndim > kMaxDims) return ZR_ERR_RANK;
+  if (t.ndim > 0 && t.sizes == nullptr) return ZR_ERR_NULL;
+  d->ptr = static_cast<const float*>(t.data);
+  d->nd = t.ndim;
+  int64_t n = 1;
+  for (int i = 0; i < t.ndim; ++i) {
+    const int64_t s = t.sizes[i];
+    if (s < 0) return ZR_ERR_SIZE;
+    if (mul_overflows(n, s) && s != 0) return ZR_ERR_SIZE;
+    d->size[i] = s;
+    n *= s;
+  }
+  d->numel = n;
+  if (t.strides) {
+    for (int i = 0; i < t.ndim; ++i) {
+      if (t.strides[i] < 0) return ZR_ERR_SIZE;
+      d->stride[i] = t.strides[i];
+    }
+  } else {
+    contiguous_strides(t.ndim, d->size, d->stride);
+  }
+  d->extent = 0;
+  if (n > 0) {
+    int64_t e = 0;
+    for (int i = 0; i < t.ndim; ++i) {
+      if (mul_overflows(d->size[i] - 1, d->stride[i])) return ZR_ERR_SIZE;
+      const int64_t span = (d->size[i] - 1) * d->stride[i];
+      if (e > kI64Max - span) return ZR_ERR_SIZE;
+      e += span;
+    }
+    if (e > kI64Max / 4 - 1) return ZR_ERR_SIZE;
+    d->extent = e + 1;
+  }
+  return ZR_OK;
+}
+
+void contiguous_strides(int nd, const int64_t* size, int64_t* stride) {
+  int64_t s = 1;
+  for (int i = nd - 1; i >= 0; --i) {
+    stride[i] = s;
+    s *= size[i] > 0 ? size[i] : 1;
+  }
+}
+
+int broadcast_sizes(int nda, const int64_t* sa, int ndb, const int64_t* sb, int* nd,
+                    int64_t* so) {
+  if (nda < 0 || nda > kMaxDims || ndb < 0 || ndb > kMaxDims) return ZR_ERR_RANK;
+  const int n = nda > ndb ? nda : ndb;
+  for (int k = 0; k < n; ++k) {
+    const int64_t x = k < nda ? sa[nda - 1 - k] : 1;
+    const int64_t y = k < ndb ? sb[ndb - 1 - k] : 1;
+    if (x < 0 || y < 0) return ZR_ERR_SIZE;
+    int64_t o;
+    if (x == y) o = x;
+    else if (x == 1) o = y;
+    else if (y == 1) o = x;
+    else return ZR_ERR_SHAPE;
+    so[n - 1 - k] = o;
+  }
+  *nd = n;
+  return ZR_OK;
+}
+
+void align_strides(const TDesc& x, int n, const int64_t* out_size, int64_t* st) {
+  for (int od = 0; od < n; ++od) {
+    const int d = od - (n - x.nd);
+    st[od] = (d < 0 || x.size[d] == 1 || out_size[od] == 1) ? 0 : x.stride[d];
+  }
+}
+
+void grad_index_strides(const TDesc& x, int n, const int64_t* out_size, int64_t* st) {
+  int64_t cs[kMaxDims];
+  contiguous_strides(x.nd, x.size, cs);
+  for (int od = 0; od < n; ++od) {
+    const int d = od - (n - x.nd);
+    st[od] = (d < 0 || x.size[d] == 1 || out_size[od] == 1) ? 0 : cs[d];
+  }
+}
+
+int coalesce(int n, const int64_t* size, const int64_t (*st)[kMaxDims], uint32_t active,
+             int order_slot, Prob* P) {
+  int dims[kMaxDims];
+  int nd = 0;
+  for (int d = 0; d < n; ++d)
+    if (size[d] != 1) dims[nd++] = d;
+  if (order_slot >= 0) {
+    std::stable_sort(dims, dims + nd, [&](int x, int y) {
+      return st[order_slot][x] > st[order_slot][y];
+    });
+  }
+  // Merge from the innermost dim outwards: dim d folds into the current
+  // outermost merged dim c when every active slot has st[d] == st[c] * size[c].
+  int64_t msize[kMaxDims];
+  int64_t mst[kProbSlots][kMaxDims];
+  int m = 0;  // merged dims stored innermost first
+  for (int i = nd - 1; i >= 0; --i) {
+    const int d = dims[i];
+    bool merge = m > 0;
+    if (merge) {
+      for (int k = 0; k < kProbSlots && merge; ++k) {
+        if (!(active & (1u << k))) continue;
+        if (mul_overflows(mst[k][m - 1], msize[m - 1])) merge = false;
+        else if (st[k][d] != mst[k][m - 1] * msize[m - 1]) merge = false;
+      }
+    }
+    if (merge) {
+      msize[m - 1] *= size[d];
+    } else {
+      msize[m] = size[d];
+      for (int k = 0; k < kProbSlots; ++k) mst[k][m] = (active & (1u << k)) ? st[k][d] : 0;
+      ++m;
+    }
+  }
+  if (m == 0) {  // every dim is 1: one element
+    msize[0] = 1;
+    for (int k = 0; k < kProbSlots; ++k) mst[k][0] = 0;
+    m = 1;
+  }
+  // An innermost dim of 2^31 or more elements is split into [size / W, W]
+  // with W a power of two, so that column indices fit 32 bits.
+  if (msize[0] >= (int64_t(1) << 31)) {
+    if (m >= kMaxDims) return ZR_ERR_SIZE;
+    int64_t w = int64_t(1) << 24;
+    while (w > 1 && msize[0] % w != 0) w >>= 1;
+    if (msize[0] / w >= (int64_t(1) << 31) || w == 1) return ZR_ERR_SIZE;
+    for (int j = m; j > 0; --j) {
+      msize[j] = msize[j - 1];
+      for (int k = 0; k < kProbSlots; ++k) mst[k][j] = mst[k][j - 1];
+    }
+    msize[1] = msize[0] / w;
+    msize[0] = w;
+    for (int k = 0; k < kProbSlots; ++k) mst[k][1] = mst[k][0] * w;
+    ++m;
+  }
+  P->n = m;
+  P->active = active;
+  for (int i = 0; i < m; ++i) {
+    P->size[i] = msize[m - 1 - i];
+    for (int k = 0; k < kProbSlots; ++k) P->st[k][i] = mst[k][m - 1 - i];
+  }
+  for (int i = 0; i + 1 < m; ++i)
+    if (P->size[i] >= (int64_t(1) << 32)) return ZR_ERR_SIZE;
+  return ZR_OK;
+}
+
+int build_ew(const Prob& P, const float* const in[3], float* const out[2], uint32_t read_mask,
+             uint32_t stream_mask, EwBuild* eb) {
+  EwPlan& p = eb->plan;
+  p = EwPlan{};
+  const int n = P.n;
+  for (int k = 0; k < 3; ++k) p.in[k] = in[k];
+  p.out[0] = out[0];
+  p.out[1] = out[1];
+  int dims[kMaxDims];
+  for (int i = 0; i < n - 1; ++i) dims[i] = i;
+  fill_decomp(&p.rows, P, dims, n - 1);
+  for (int k = 0; k < kMaxOperands; ++k) p.inner_stride[k] = P.st[k][n - 1];
+  p.stream_mask = stream_mask;
+
+  uint64_t nrow = 1;
+  for (int i = 0; i < n - 1; ++i) nrow *= uint64_t(P.size[i]);
+  const uint64_t ncol = uint64_t(P.size[n - 1]);
+  if (nrow >= (uint64_t(1) << 32) || ncol >= (uint64_t(1) << 31)) return ZR_ERR_SIZE;
+
+  const void* ptrs[kMaxOperands] = {in[0], in[1], in[2], out[0] ? out[0] : out[1]};
+  uint32_t slots = read_mask | (1u << kSlotOut);
+  bool v4 = vec4_ok(P, slots, ptrs);
+  if (v4 && out[0] && out[1] && reinterpret_cast<uintptr_t>(out[1]) % 16 != 0) v4 = false;
+  eb->vec = v4 ? 4 : 1;
+
+  const uint64_t nvcol = ceil_div(ncol, eb->vec);
+  const uint64_t items = nrow * nvcol;
+  uint64_t ipc = items / 1216;
+  ipc = std::max<uint64_t>(256, std::min<uint64_t>(2048, ipc));
+  ipc = ceil_div(ipc, 256) * 256;
+  const uint64_t tvc = std::min<uint64_t>(nvcol, ipc);
+  uint64_t trows = std::max<uint64_t>(1, ipc / tvc);
+  trows = std::min<uint64_t>(trows, std::min<uint64_t>(nrow, kMaxTileRows));
+  p.nrow = uint32_t(nrow);
+  p.ncol = uint32_t(ncol);
+  p.nvcol = uint32_t(nvcol);
+  p.tile_vcols = uint32_t(tvc);
+  p.tile_rows = uint32_t(trows);
+  p.col_tiles = uint32_t(ceil_div(nvcol, tvc));
+  p.col_tiles_div = make_fastdiv(p.col_tiles);
+  p.tile_vcols_div = make_fastdiv(p.tile_vcols);
+  p.items_per_cta = uint32_t(trows * tvc);
+  const uint64_t ncta = ceil_div(nrow, trows) * p.col_tiles;
+  if (ncta >= (uint64_t(1) << 31)) return ZR_ERR_SIZE;
+  p.n_cta = uint32_t(ncta);
+  return ZR_OK;
+}
+
+int build_red(const Prob& P, int xslot, const float* g, const float* a, const float* b,
+              uint32_t read_mask, uint32_t stream_mask, float* x_out, float* d_out,
+              int vec_override, RedBuild* rb) {
+  RedPlan& p = rb->plan;
+  p = RedPlan{};
+  const int n = P.n;
+  p.g = g;
+  p.a = a;
+  p.b = b;
+  p.x_final = x_out;
+  p.d_out = d_out;
+  p.stream_mask = stream_mask;
+  p.scale = 1.0f;
+  int kd[kMaxDims], rd[kMaxDims];
+  int nk = 0, nr = 0;
+  uint64_t n_kept = 1, n_red = 1;
+  for (int d = 0; d < n - 1; ++d) {
+    if (P.st[xslot][d] != 0) { kd[nk++] = d; n_kept *= uint64_t(P.size[d]); }
+    else { rd[nr++] = d; n_red *= uint64_t(P.size[d]); }
+  }
+  fill_decomp(&p.kept, P, kd, nk);
+  fill_decomp(&p.red, P, rd, nr);
+  for (int k = 0; k < kMaxOperands; ++k) p.inner_stride[k] = P.st[k][n - 1];
+  const uint64_t ncol = uint64_t(P.size[n - 1]);
+  p.inner_kept = P.st[xslot][n - 1] != 0 ? 1 : 0;
+  if (n_kept >= (uint64_t(1) << 32) || n_red >= (uint64_t(1) << 32) ||
+      ncol >= (uint64_t(1) << 31))
+    return ZR_ERR_SIZE;
+  p.n_kept = uint32_t(n_kept);
+  p.n_red = uint32_t(n_red);
+  p.ncol = uint32_t(ncol);
+  p.nout = p.inner_kept ? n_kept * ncol : n_kept;
+
+  const void* ptrs[kMaxOperands] = {g, a, b, d_out};
+  uint32_t slots = (read_mask & 7u) | (d_out ? (1u << kSlotOut) : 0u);
+  bool v4 = vec4_ok(P, slots, ptrs);
+  if (v4 && p.inner_kept && reinterpret_cast<uintptr_t>(x_out) % 16 != 0) v4 = false;
+  // The reduced gradient's kept outer strides are multiples of ncol, so its
+  // rows stay aligned; the workspace is 16-byte aligned by contract.
+  rb->vec = vec_override ? vec_override : (v4 ? 4 : 1);
+  const uint32_t vec = uint32_t(rb->vec);
+  const uint64_t nvcol = ceil_div(ncol, vec);
+  p.nvcol = uint32_t(nvcol);
+
+  const uint64_t total = n_kept * n_red * ncol;
+  const uint64_t E = elems_per_cta_target(total);
+  // Partial slots are capped so that their write + read stays within about
+  // 3% of the input stream, and at 4096 for the second pass.
+  uint64_t cap = total / (64 * std::max<uint64_t>(1, p.nout));
+  cap = std::max<uint64_t>(1, std::min<uint64_t>(4096, cap));
+
+  uint32_t tx = pick_tx(nvcol);
+  uint64_t rows, vcols;
+  if (p.inner_kept) {
+    // Narrow the column lanes while that adds CTAs the slot cap would
+    // otherwise forbid.
+    while (tx > 32) {
+      const uint64_t ty = kThreads / tx;
+      const uint64_t ctas = n_kept * ceil_div(nvcol, tx) * std::min<uint64_t>(cap, ceil_div(n_red, ty));
+      if (ctas >= 1216) break;
+      tx /= 2;
+    }
+    vcols = tx;
+    rows = ceil_div(E, uint64_t(tx) * vec);
+    rows = std::max<uint64_t>(rows, ceil_div(n_red, cap));
+    rows = std::min<uint64_t>(rows, n_red);
+  } else {
+    if (nvcol * vec >= E) {
+      vcols = ceil_div(ceil_div(E, vec), tx) * tx;
+      rows = 1;
+    } else {
+      vcols = ceil_div(nvcol, tx) * tx;
+      rows = std::max<uint64_t>(1, E / (nvcol * vec));
+      rows = std::min<uint64_t>(rows, n_red);
+    }
+    for (;;) {
+      const uint64_t slots_now = ceil_div(n_red, rows) * ceil_div(nvcol, vcols);
+      if (slots_now <= cap) break;
+      if (rows < n_red) rows = std::min<uint64_t>(n_red, rows * 2);
+      else vcols *= 2;
+    }
+  }
+  p.tx = tx;
+  p.ty = kThreads / tx;
+  p.rows_per_blk = uint32_t(rows);
+  p.vcols_per_blk = uint32_t(vcols);
+  p.n_rblk = uint32_t(ceil_div(n_red, rows));
+  p.n_cblk = uint32_t(ceil_div(nvcol, vcols));
+  p.n_cblk_div = make_fastdiv(p.n_cblk);
+  p.n_rblk_div = make_fastdiv(p.n_rblk);
+  p.nslots = p.inner_kept ? p.n_rblk : p.n_rblk * p.n_cblk;
+  const uint64_t ncta = n_kept * p.n_rblk * uint64_t(p.n_cblk);
+  if (ncta >= (uint64_t(1) << 31)) return ZR_ERR_SIZE;
+  p.n_cta = uint32_t(ncta);
+  rb->ws_bytes = p.nslots > 1 ? ((p.nslots * p.nout * sizeof(float) + 255) / 256) * 256 : 0;
+
+  CombinePlan& c = rb->comb;
+  c = CombinePlan{};
+  c.nout = p.nout;
+  c.nslots = p.nslots;
+  c.out = x_out;
+  c.scale = 1.0f;
+  uint32_t sy = std::min<uint32_t>(kThreads, pow2_ceil(p.nslots));
+  if (p.nout >= 64 * 1024) sy = std::min<uint32_t>(sy, 4);
+  else if (p.nout >= 4096) sy = std::min<uint32_t>(sy, 32);
+  uint32_t jx = kThreads / sy;
+  if (p.nout < jx) {
+    jx = pow2_ceil(p.nout);
+    sy = kThreads / jx;
+  }
+  c.jx = jx;
+  c.sy = std::min<uint32_t>(sy, pow2_ceil(p.nslots));
+  return ZR_OK;
+}
+
+std::string describe_ew(const EwBuild& eb) {
+  const EwPlan& p = eb.plan;
+  char buf[1024];
+  std::snprintf(buf, sizeof(buf),
+                "{\"kernel\":\"elementwise\",\"vec\":%d,\"nrow\":%u,\"ncol\":%u,\"row_dims\":%d,"
+                "\"inner_stride\":[%lld,%lld,%lld,%lld],\"tile_rows\":%u,\"tile_vcols\":%u,"
+                "\"ctas\":%u,\"stream_mask\":%u}",
+                eb.vec, p.nrow, p.ncol, p.rows.n, (long long)p.inner_stride[0],
+                (long long)p.inner_stride[1], (long long)p.inner_stride[2],
+                (long long)p.inner_stride[3], p.tile_rows, p.tile_vcols, p.n_cta, p.stream_mask);
+  return buf;
+}
+
+std::string describe_red(const RedBuild& rb) {
+  const RedPlan& p = rb.plan;
+  char buf[1024];
+  std::snprintf(buf, sizeof(buf),
+                "{\"kernel\":\"reduce\",\"vec\":%d,\"inner_kept\":%u,\"n_kept\":%u,\"n_red\":%u,"
+                "\"ncol\":%u,\"kept_dims\":%d,\"red_dims\":%d,\"tx\":%u,\"ty\":%u,"
+                "\"rows_per_blk\":%u,\"vcols_per_blk\":%u,\"n_rblk\":%u,\"n_cblk\":%u,"
+                "\"nslots\":%u,\"nout\":%llu,\"ctas\":%u,\"ws_bytes\":%zu,\"dense_out\":%d}",
+                rb.vec, p.inner_kept, p.n_kept, p.n_red, p.ncol, p.kept.n, p.red.n, p.tx, p.ty,
+                p.rows_per_blk, p.vcols_per_blk, p.n_rblk, p.n_cblk, p.nslots,
+                (unsigned long long)p.nout, p.n_cta, rb.ws_bytes, p.d_out ? 1 : 0);
+  return buf;
+}
+
+}  // namespace zr

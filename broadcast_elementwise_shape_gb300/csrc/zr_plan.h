@@ -1,0 +1,83 @@
+// zr_plan.h — host planner: validation, broadcast, dimension coalescing and
+// construction of the by-value kernel plans.  Pure host C++; the launches
+// live in the .cu files.
+#pragma once
+
+#include <stdint.h>
+#include <stddef.h>
+#include <string>
+
+#include "../../include/zr.h"
+#include "zr_internal.h"
+
+namespace zr {
+
+// A validated tensor view with explicit strides.
+struct TDesc {
+  const float* ptr = nullptr;
+  int nd = 0;
+  int64_t size[kMaxDims] = {};
+  int64_t stride[kMaxDims] = {};
+  int64_t numel = 1;
+  int64_t extent = 0;  // largest element offset + 1 (0 when empty)
+};
+
+int read_tensor(const zr_tensor& t, TDesc* d);
+int broadcast_sizes(int nda, const int64_t* sa, int ndb, const int64_t* sb, int* nd,
+                    int64_t* so);
+void contiguous_strides(int nd, const int64_t* size, int64_t* stride);
+
+// Operand slots while coalescing: G/A/B/D as in zr_internal.h plus the two
+// gradient index maps (dense in a's / b's shape, 0 on broadcast dims).
+constexpr int kSlotXA = 4;
+constexpr int kSlotXB = 5;
+constexpr int kProbSlots = 6;
+
+// The output index space after dropping size-1 dims and merging adjacent
+// dims that every active operand walks contiguously; row-major, dims[0]
+// outermost.
+struct Prob {
+  int n = 0;
+  int64_t size[kMaxDims] = {};
+  int64_t st[kProbSlots][kMaxDims] = {};
+  uint32_t active = 0;  // bit k: slot k takes part
+};
+
+// Strides of x against an output of rank n: 0 where x is missing or 1.
+void align_strides(const TDesc& x, int n, const int64_t* out_size, int64_t* st);
+// Row-major strides of x's own shape against the output: 0 on broadcast dims.
+void grad_index_strides(const TDesc& x, int n, const int64_t* out_size, int64_t* st);
+
+// Drop size-1 dims, optionally sort by descending stride of `order_slot`
+// (-1 = keep order), and merge.  Splits an innermost dim that is too long for
+// 32-bit column indexing.  Returns ZR_OK or ZR_ERR_SIZE.
+int coalesce(int n, const int64_t* size, const int64_t (*st)[kMaxDims], uint32_t active,
+             int order_slot, Prob* P);
+
+struct EwBuild {
+  EwPlan plan;
+  int vec;
+};
+// Elementwise plan over P with input slots 0..2 and output slot 3.
+int build_ew(const Prob& P, const float* const in[3], float* const out[2], uint32_t read_mask,
+             uint32_t stream_mask, EwBuild* eb);
+
+struct RedBuild {
+  RedPlan plan;
+  CombinePlan comb;
+  int vec;
+  size_t ws_bytes;  // partial workspace (0 when nslots == 1)
+};
+// Reduction plan over P for the gradient whose index map is slot `xslot`.
+// `d_out` (may be null) is written densely from slot 3 offsets.
+// vec_override: 0 = choose VEC from alignment; 1 or 4 = size the tiling as if
+// VEC were that value (used to report a workspace size that holds whatever
+// the alignment of the run-time pointers turns out to be).
+int build_red(const Prob& P, int xslot, const float* g, const float* a, const float* b,
+              uint32_t read_mask, uint32_t stream_mask, float* x_out, float* d_out,
+              int vec_override, RedBuild* rb);
+
+std::string describe_ew(const EwBuild& eb);
+std::string describe_red(const RedBuild& rb);
+
+}  // namespace zr

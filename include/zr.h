@@ -1,0 +1,170 @@
+/*
+ * zr.h — C ABI of a GB300 (sm_103a) library of broadcasting elementwise
+ * binary operators on strided fp32 tensors: forward, fused backward and
+ * deterministic sum-to-shape.
+ *
+ * Semantics follow the "Zero" book (ismantic.github.io/zero):
+ *   - Tensor page, section 形状与步长 (shape and strides): a tensor is a base
+ *     pointer plus per-dimension sizes and element strides; element
+ *     (i0, i1, ...) lives at base + sum_d i_d * stride_d.  Default strides are
+ *     row-major, built from the last dimension ([2,3,4] -> [12,4,1]).
+ *   - Operator page, section 广播 (broadcasting): shapes are compared from the
+ *     last dimension; each pair must be equal, or one side 1, or one side
+ *     missing (treated as 1).  A size-1 input dimension always reads
+ *     coordinate 0.  Repetition in the forward pass is summation in the
+ *     backward pass: dL/dx_j = sum over all outputs i that read x_j.
+ *   - Operator page, section 逐元素算子 (elementwise ops): add, sub, mul, div;
+ *     mul backward is (g*b, g*a).  GPU page, section OpAdd: add backward
+ *     passes g to both inputs.  sub and div backward are not written out on
+ *     the pages; this library uses the calculus rules (g, -g) and
+ *     (g/b, -g*a/b^2).
+ *   - Operator page, section 逐元素算子: shape and broadcast checks belong to
+ *     the operator layer, not the kernels — every check here runs on the host
+ *     before anything is launched.
+ *   - GPU page, section Kernel 派发 (kernel dispatch): all operands of one op
+ *     are on one device; up to eight dimensions are passed by value to the
+ *     kernels (no metadata copies).
+ *   - GPU page, section 异步执行 (asynchronous execution): every call only
+ *     enqueues work on the caller's stream; success means "enqueued".
+ *
+ * Numerics.  Forward results are one IEEE binary32 operation per element,
+ * round-to-nearest-even, no contraction, subnormals kept: bit-identical to
+ * the same scalar C expression.  Gradients that receive exactly one term and
+ * are one operation (add/sub copy or negation, mul g*b and g*a, div g/b) are
+ * bit-identical too.  Reduced gradients, and div's -g*a/b^2, are within
+ * 1e-5 * sum|terms| of the exact value per element; reductions use a fixed,
+ * shape-determined order (no atomics), so results are bitwise reproducible
+ * run to run on the same GPU model.
+ *
+ * Memory.  The library never allocates, frees or retains caller memory and
+ * keeps no state between calls.  All pointers given for data must be device
+ * memory (or host memory the device can address: registered/pinned or
+ * managed) on the current device; the caller owns them and the stream.
+ */
+#ifndef ZR_H_
+#define ZR_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as CUDA's cudaStream_t; NULL is the legacy default stream. */
+struct CUstream_st;
+typedef struct CUstream_st* zr_stream_t;
+
+/* Maximum rank of any operand (DimsArg-style, passed by value). */
+#define ZR_MAX_DIMS 8
+
+typedef enum { ZR_ADD = 0, ZR_SUB = 1, ZR_MUL = 2, ZR_DIV = 3 } zr_op;
+
+typedef enum {
+  ZR_OK = 0,
+  ZR_ERR_NULL = -1,      /* required pointer is NULL, or op code unknown      */
+  ZR_ERR_RANK = -2,      /* ndim < 0 or ndim > 8                               */
+  ZR_ERR_SHAPE = -3,     /* shapes not broadcastable / wrong grad_out shape    */
+  ZR_ERR_SIZE = -4,      /* negative size or stride, or index range overflow   */
+  ZR_ERR_LAYOUT = -5,    /* output overlaps itself, or partially overlaps an
+                            input or another output                           */
+  ZR_ERR_DEVICE = -6,    /* pointer not addressable by the current device      */
+  ZR_ERR_WORKSPACE = -7, /* workspace smaller than required                    */
+  ZR_ERR_CUDA = -8       /* a CUDA call or kernel launch failed                */
+} zr_status;
+
+/*
+ * A strided fp32 tensor view (Tensor page, 形状与步长).
+ *   data    : address of element (0, ..., 0); may be NULL only when the
+ *             tensor is empty or the call does not read it (see below).
+ *   ndim    : 0..8; ndim == 0 is a scalar (one element).
+ *   sizes   : ndim sizes, each >= 0 (may be NULL when ndim == 0).
+ *   strides : ndim element strides, each >= 0 (0 = expanded/broadcast view),
+ *             or NULL for row-major contiguous.
+ * The arrays are read during the call only.
+ */
+typedef struct {
+  const void* data;
+  int32_t ndim;
+  const int64_t* sizes;
+  const int64_t* strides;
+} zr_tensor;
+
+/*
+ * zr_broadcast_shape — the broadcast rule (Operator page, 广播).
+ * Writes the broadcast shape of (sizes_a[ndim_a]) and (sizes_b[ndim_b]) to
+ * sizes_out[0 .. *ndim_out-1]; *ndim_out = max(ndim_a, ndim_b).  A size-0
+ * dimension pairs with 0 or 1 (NumPy reading; the pages are silent).
+ * Host only, launches nothing.  Errors: ZR_ERR_NULL, ZR_ERR_RANK,
+ * ZR_ERR_SIZE (negative size), ZR_ERR_SHAPE (incompatible).
+ */
+int zr_broadcast_shape(int32_t ndim_a, const int64_t* sizes_a,
+                       int32_t ndim_b, const int64_t* sizes_b,
+                       int32_t* ndim_out, int64_t sizes_out[ZR_MAX_DIMS]);
+
+/*
+ * zr_binary_fwd — out = a op b with broadcasting (Operator page, 逐元素算子
+ * and 广播).
+ *   a, b        : inputs, any non-negative strides.
+ *   out         : device buffer of the broadcast shape.
+ *   out_strides : element strides of out (rank = broadcast rank), or NULL
+ *                 for row-major contiguous.  out must not overlap itself.
+ *                 out may alias an input exactly (same base, same shape as
+ *                 out, same strides: in place); any other overlap with an
+ *                 input is ZR_ERR_LAYOUT.
+ * Empty outputs launch nothing.  Errors: ZR_ERR_NULL, ZR_ERR_RANK,
+ * ZR_ERR_SHAPE, ZR_ERR_SIZE, ZR_ERR_LAYOUT, ZR_ERR_DEVICE, ZR_ERR_CUDA.
+ * All checks happen before any launch: an error never writes to out.
+ */
+int zr_binary_fwd(zr_op op, zr_tensor a, zr_tensor b, float* out,
+                  const int64_t* out_strides, zr_stream_t stream);
+
+/*
+ * zr_binary_bwd — fused backward of out = a op b (Operator page, 逐元素算子
+ * and 广播; GPU page, OpAdd): one pass over grad_out computes
+ *   grad_a = sum_to_shape(dL/da local terms, shape of a)
+ *   grad_b = sum_to_shape(dL/db local terms, shape of b)
+ * with local terms add (g, g), sub (g, -g), mul (g*b, g*a),
+ * div (g/b, -g*a/b^2).
+ *   grad_out : tensor of the broadcast shape, any strides.
+ *   a, b     : the forward inputs; their sizes are always required.  Their
+ *              data is read only where a term needs it (mul: b for grad_a, a
+ *              for grad_b; div: b for grad_a, a and b for grad_b) and may be
+ *              NULL otherwise.
+ *   grad_a, grad_b : outputs, dense row-major in a's / b's own shape; either
+ *              may be NULL to skip it.  They are written, not accumulated.
+ *              An output may alias grad_out exactly (same shape, grad_out
+ *              row-major); other overlaps are ZR_ERR_LAYOUT.
+ *   workspace, workspace_bytes : scratch device memory for the two-pass
+ *              reduction.  With workspace == NULL the call only stores the
+ *              required size in *workspace_bytes and launches nothing.
+ *              Otherwise *workspace_bytes is the size provided; if the
+ *              required size is 0 any non-NULL pointer may be passed (it is
+ *              not touched).  Workspace must be 16-byte aligned.
+ * A reduced gradient of an empty grad_out is filled with zeros.
+ * Errors: as zr_binary_fwd, plus ZR_ERR_WORKSPACE.
+ */
+int zr_binary_bwd(zr_op op, zr_tensor grad_out, zr_tensor a, zr_tensor b,
+                  float* grad_a, float* grad_b,
+                  void* workspace, size_t* workspace_bytes, zr_stream_t stream);
+
+/*
+ * zr_sum_to_shape — OpSumToSize (Operator page, 广播): out[j] = sum of every
+ * element of `in` whose coordinate maps to j when sizes_out is broadcast to
+ * in's shape.  sizes_out must broadcast with in's shape to exactly in's shape
+ * (else ZR_ERR_SHAPE).  out is dense row-major of sizes_out and must not
+ * overlap `in` unless it aliases it exactly with no reduction.
+ * Workspace protocol as zr_binary_bwd.
+ */
+int zr_sum_to_shape(zr_tensor in, int32_t ndim_out, const int64_t* sizes_out,
+                    float* out, void* workspace, size_t* workspace_bytes,
+                    zr_stream_t stream);
+
+/* Static, human-readable name of a status code. */
+const char* zr_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ZR_H_ */

@@ -1,0 +1,48 @@
+/*
+ * zr_testing.h — host-only introspection hooks of the zr library, for tests
+ * of the planner on machines without a GPU.  None of these touch device
+ * memory or launch anything; data pointers are only inspected for alignment.
+ * Return values are zr_status codes.
+ */
+#ifndef ZR_TESTING_H_
+#define ZR_TESTING_H_
+
+#include "zr.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* q = floor(n / d) through the kernels' multiply-high division (d >= 1). */
+int zr_test_fastdiv(uint32_t d, uint32_t n, uint32_t* q);
+
+/* JSON description of the plan zr_binary_fwd / zr_binary_bwd /
+ * zr_sum_to_shape would launch for these arguments (NUL-terminated, up to
+ * len bytes). */
+int zr_test_describe_fwd(zr_op op, zr_tensor a, zr_tensor b, const float* out,
+                         const int64_t* out_strides, char* buf, size_t len);
+int zr_test_describe_bwd(zr_op op, zr_tensor grad_out, zr_tensor a, zr_tensor b,
+                         const float* grad_a, const float* grad_b, char* buf, size_t len);
+int zr_test_describe_sum(zr_tensor in, int32_t ndim_out, const int64_t* sizes_out,
+                         const float* out, char* buf, size_t len);
+
+/* Walk every (CTA, thread item) of the planned forward kernel on the host and
+ * record, per element visited, {out_offset, a_offset, b_offset} (element
+ * units).  rec holds cap records of 3 int64; *nrec receives the count. */
+int zr_test_emulate_fwd(zr_tensor a, zr_tensor b, const float* out, const int64_t* out_strides,
+                        int64_t cap, int64_t* rec, int64_t* nrec);
+
+/* Same for the backward plans: per element visited, 7 int64
+ * {plan, g_offset, a_offset, b_offset, x_index, slot, d_offset}: plan is the
+ * launch index; x_index the reduced gradient's element (-1 if none); slot its
+ * partial slot; d_offset the densely written gradient's element (-1 if
+ * none).  Offsets of operands the plan does not read are -1. */
+int zr_test_emulate_bwd(zr_op op, zr_tensor grad_out, zr_tensor a, zr_tensor b,
+                        const float* grad_a, const float* grad_b, int64_t cap, int64_t* rec,
+                        int64_t* nrec);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ZR_TESTING_H_ */

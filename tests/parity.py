@@ -1,0 +1,119 @@
+"""Helpers shared by the GPU parity tests: run a workload's op steps through
+the CUDA library and through the CPU oracle on the same seeded host inputs,
+and compare.
+
+Acceptance (the operators' contract):
+* forward outputs, and gradients that are one exact IEEE operation of their
+  inputs (add/sub copy or negation, mul g*b / g*a, div g/b when nothing is
+  summed), must be bit-identical, any NaN matching any NaN;
+* every summed gradient, and div's -g*a/b^2, must be within
+  1e-5 * sum|terms| of the oracle's binary64 result, per element.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import broadcast_elementwise_shape_gb300 as zr
+import oracle
+import workloads
+
+TOL = 1e-5
+
+
+def bitexact(gpu: np.ndarray, ref: np.ndarray, what: str = ""):
+    gpu = np.asarray(gpu, np.float32)
+    ref = np.asarray(ref, np.float32)
+    assert gpu.shape == ref.shape, (what, gpu.shape, ref.shape)
+    gn, rn = np.isnan(gpu), np.isnan(ref)
+    assert np.array_equal(gn, rn), f"{what}: NaN positions differ"
+    gb, rb = gpu.view(np.uint32)[~gn], ref.view(np.uint32)[~rn]
+    bad = np.nonzero(gb != rb)[0]
+    assert bad.size == 0, (f"{what}: {bad.size} elements differ; first at flat {bad[0]}: "
+                           f"gpu {gpu[~gn][bad[0]]!r} ref {ref[~rn][bad[0]]!r}")
+
+
+def within(gpu: np.ndarray, ref: np.ndarray, abs_sum: np.ndarray, what: str = "", tol=TOL):
+    gpu = np.asarray(gpu, np.float64)
+    ref = np.asarray(ref, np.float64)
+    abs_sum = np.asarray(abs_sum, np.float64)
+    assert gpu.shape == ref.shape == abs_sum.shape, (what, gpu.shape, ref.shape, abs_sum.shape)
+    gn, rn = np.isnan(gpu), np.isnan(ref)
+    assert np.array_equal(gn, rn), f"{what}: NaN positions differ"
+    fin = ~gn & np.isfinite(ref) & np.isfinite(abs_sum)
+    inf = ~gn & ~fin
+    assert np.array_equal(gpu[inf], ref[inf]) or not inf.any(), f"{what}: infinities differ"
+    err = np.abs(gpu[fin] - ref[fin])
+    bound = tol * abs_sum[fin]
+    bad = np.nonzero(err > bound)[0]
+    assert bad.size == 0, (f"{what}: {bad.size} elements beyond {tol}*sum|terms|; worst ratio "
+                           f"{np.max(err / np.maximum(bound, 1e-300)):.3g}")
+
+
+def is_single_op_grad(op: str, which: int, reduced: bool) -> bool:
+    """True if a gradient element is exactly one IEEE op of the inputs."""
+    if reduced:
+        return False
+    return not (op == "div" and which == 1)
+
+
+def to_gpu(x: torch.Tensor) -> torch.Tensor:
+    """Device copy keeping the view's strides (e.g. a transposed view)."""
+    if x.is_contiguous():
+        return x.cuda()
+    # Rebuild the same view over a device copy of its storage.
+    base = x
+    while base._base is not None:
+        base = base._base
+    dev_base = base.contiguous().cuda()
+    return dev_base.as_strided(x.shape, x.stride(), x.storage_offset() - base.storage_offset())
+
+
+def run_gpu(name: str, host: dict) -> dict:
+    """All step outputs of workload ``name`` computed by the CUDA library."""
+    env = {k: to_gpu(v) for k, v in host.items()}
+    for step in workloads.STEPS[name]:
+        if step[0] == "fwd":
+            _, op, an, bn, on = step
+            env[on] = zr.zr_binary_fwd(op, env[an], env[bn])
+        else:
+            _, op, gn, an, bn, gan, gbn = step
+            ga, gb = zr.zr_binary_bwd(op, env[gn], env[an], env[bn])
+            env[gan], env[gbn] = ga, gb
+    torch.cuda.synchronize()
+    return {k: v.cpu() for k, v in env.items()}
+
+
+def run_oracle(name: str, host: dict) -> tuple[dict, dict]:
+    """(values, abs_sums) of every step output, computed by the oracle."""
+    env = {k: v for k, v in host.items()}
+    sums = {}
+    for step in workloads.STEPS[name]:
+        if step[0] == "fwd":
+            _, op, an, bn, on = step
+            env[on] = torch.from_numpy(oracle.binary_fwd(op, env[an], env[bn]))
+        else:
+            _, op, gn, an, bn, gan, gbn = step
+            ga, gb, sa, sb = oracle.binary_bwd(op, env[gn], env[an], env[bn])
+            env[gan], env[gbn] = torch.from_numpy(ga), torch.from_numpy(gb)
+            sums[gan], sums[gbn] = sa, sb
+    return env, sums
+
+
+def compare_workload(name: str, host: dict, gpu: dict, ref: dict, sums: dict):
+    out_shapes = {}
+    for step in workloads.STEPS[name]:
+        if step[0] == "fwd":
+            _, op, an, bn, on = step
+            bitexact(gpu[on].numpy(), ref[on].numpy(), f"{name} fwd {op} -> {on}")
+            out_shapes[on] = tuple(ref[on].shape)
+        else:
+            _, op, gn, an, bn, gan, gbn = step
+            out_numel = ref[gn].numel()
+            for which, gname, src in ((0, gan, an), (1, gbn, bn)):
+                reduced = ref[gname].numel() != out_numel
+                what = f"{name} bwd {op} -> {gname}"
+                if is_single_op_grad(op, which, reduced):
+                    bitexact(gpu[gname].numpy(), ref[gname].numpy(), what)
+                else:
+                    within(gpu[gname].numpy(), ref[gname].numpy(), sums[gname], what)

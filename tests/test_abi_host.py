@@ -1,0 +1,335 @@
+"""Host-side checks of the C ABI library (no GPU needed).
+
+* the library loads and exports every function declared in include/*.h;
+* zr_broadcast_shape agrees with the book's printed examples and NumPy;
+* the multiply-high division used by the kernels is exact;
+* a host walk of every planned kernel (the same CTA/item/row/column loops the
+  kernels run, via zr_test_emulate_*) visits each output element exactly
+  once and computes the same operand offsets and gradient indices as naive
+  strided index arithmetic written here with NumPy;
+* argument errors are reported before anything touches a device.
+"""
+import ctypes
+import json
+import os
+import re
+
+import numpy as np
+import pytest
+
+import broadcast_elementwise_shape_gb300 as zr
+from broadcast_elementwise_shape_gb300 import ZrTensor
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+INCLUDE = os.path.join(ROOT, "include")
+
+
+@pytest.fixture(scope="module")
+def L():
+    zr.build()
+    lib = zr.lib()
+    i64p = ctypes.POINTER(ctypes.c_int64)
+    vp = ctypes.c_void_p
+    lib.zr_test_fastdiv.argtypes = [ctypes.c_uint32, ctypes.c_uint32, ctypes.POINTER(ctypes.c_uint32)]
+    lib.zr_test_describe_fwd.argtypes = [ctypes.c_int, ZrTensor, ZrTensor, vp, i64p, ctypes.c_char_p, ctypes.c_size_t]
+    lib.zr_test_describe_bwd.argtypes = [ctypes.c_int, ZrTensor, ZrTensor, ZrTensor, vp, vp, ctypes.c_char_p, ctypes.c_size_t]
+    lib.zr_test_describe_sum.argtypes = [ZrTensor, ctypes.c_int32, i64p, vp, ctypes.c_char_p, ctypes.c_size_t]
+    lib.zr_test_emulate_fwd.argtypes = [ZrTensor, ZrTensor, vp, i64p, ctypes.c_int64, i64p, i64p]
+    lib.zr_test_emulate_bwd.argtypes = [ctypes.c_int, ZrTensor, ZrTensor, ZrTensor, vp, vp, ctypes.c_int64, i64p, i64p]
+    return lib
+
+
+def _i64(seq):
+    return (ctypes.c_int64 * max(1, len(seq)))(*[int(v) for v in seq])
+
+
+class FakeT:
+    """A descriptor with a fake (never dereferenced) base address."""
+
+    def __init__(self, addr, shape, strides=None):
+        self.shape = tuple(shape)
+        self.strides = tuple(strides) if strides is not None else tuple(
+            s // 4 for s in np.empty(self.shape, np.float32).strides) if self.shape else ()
+        self._sz = _i64(self.shape)
+        self._st = _i64(self.strides)
+        self.desc = ZrTensor(addr, len(self.shape), self._sz, self._st)
+
+
+def declared_functions():
+    names = []
+    for f in os.listdir(INCLUDE):
+        if f.endswith(".h"):
+            text = open(os.path.join(INCLUDE, f)).read()
+            names += re.findall(r"^\s*(?:int|const char\*)\s+(zr_\w+)\s*\(", text, re.M)
+    return sorted(set(names))
+
+
+def test_exports_every_declared_symbol(L):
+    names = declared_functions()
+    assert {"zr_broadcast_shape", "zr_binary_fwd", "zr_binary_bwd", "zr_sum_to_shape",
+            "zr_status_string"} <= set(names)
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_status_strings(L):
+    for code in range(0, -9, -1):
+        assert L.zr_status_string(code).decode().startswith("ZR_")
+
+
+def test_broadcast_shape_examples_and_numpy(L):
+    assert zr.zr_broadcast_shape((2, 3, 4), (3, 1)) == (2, 3, 4)
+    with pytest.raises(zr.ZrError) as e:
+        zr.zr_broadcast_shape((2, 3, 4), (2, 4, 5))
+    assert e.value.status == -3
+    rng = np.random.default_rng(0)
+    for _ in range(2000):
+        na, nb = rng.integers(0, 9, 2)
+        sa = tuple(int(v) for v in rng.choice([0, 1, 1, 2, 3, 5], na))
+        sb = tuple(int(v) for v in rng.choice([0, 1, 1, 2, 3, 5], nb))
+        try:
+            ref = tuple(np.broadcast_shapes(sa, sb))
+        except ValueError:
+            ref = None
+        if ref is None:
+            with pytest.raises(zr.ZrError):
+                zr.zr_broadcast_shape(sa, sb)
+        else:
+            assert zr.zr_broadcast_shape(sa, sb) == ref
+    with pytest.raises(zr.ZrError) as e:
+        zr.zr_broadcast_shape((1,) * 9, (1,))
+    assert e.value.status == -2
+
+
+def test_fastdiv_exact(L):
+    rng = np.random.default_rng(1)
+    q = ctypes.c_uint32()
+    ds = [1, 2, 3, 5, 7, 10, 12, 64, 96, 255, 256, 641, 65535, 65536, 2**31 - 1, 2**31,
+          2**31 + 1, 2**32 - 1] + [int(v) for v in rng.integers(1, 2**32, 300)]
+    ns = [0, 1, 2, 2**31 - 1, 2**31, 2**32 - 2, 2**32 - 1]
+    for d in ds:
+        for n in ns + [int(v) for v in rng.integers(0, 2**32, 40)] + [d - 1, d, d + 1, 2 * d - 1]:
+            if not 0 <= n < 2**32:
+                continue
+            assert L.zr_test_fastdiv(d, n, ctypes.byref(q)) == 0
+            assert q.value == n // d, (d, n)
+
+
+# ------------------------------------------------------------- naive index maps
+
+def naive_offsets(out_shape, x_shape, x_strides):
+    """Element offset of x for every output coordinate (row-major), with
+    coordinate 0 on x's size-1 or missing dims."""
+    n = len(out_shape)
+    off = np.zeros(out_shape, np.int64)
+    for od in range(n):
+        d = od - (n - len(x_shape))
+        if d < 0 or x_shape[d] == 1:
+            continue
+        shape = [1] * n
+        shape[od] = out_shape[od]
+        off = off + np.arange(out_shape[od], dtype=np.int64).reshape(shape) * x_strides[d]
+    return off
+
+
+def dense_strides(shape):
+    return tuple(s // 4 for s in np.empty(shape, np.float32).strides) if shape else ()
+
+
+def rand_view(rng, shape, addr):
+    """Fake view of `shape`: contiguous, permuted or stepped strides; some
+    base addresses are misaligned by one element."""
+    kind = rng.integers(0, 3)
+    if kind == 0 or len(shape) == 0:
+        st = dense_strides(shape)
+    elif kind == 1:
+        perm = rng.permutation(len(shape))
+        base = dense_strides(tuple(shape[p] for p in perm))
+        st = [0] * len(shape)
+        for i, p in enumerate(perm):
+            st[p] = base[i]
+        st = tuple(st)
+    else:
+        big = tuple(2 * s + 1 for s in shape)
+        st = tuple(2 * s for s in dense_strides(big))
+    return FakeT(addr, shape, st)
+
+
+def rand_shapes(rng, max_nd=6):
+    n = int(rng.integers(0, max_nd + 1))
+    out = [int(v) for v in rng.choice([1, 2, 3, 4, 5, 8, 12], n)]
+    sa = [s if rng.random() < 0.6 else 1 for s in out]
+    sb = [s if rng.random() < 0.6 else 1 for s in out]
+    sa = sa[int(rng.integers(0, n + 1)) if n else 0:]
+    sb = sb[int(rng.integers(0, n + 1)) if n else 0:]
+    return tuple(sa), tuple(sb)
+
+
+def test_emulated_forward_matches_naive(L):
+    rng = np.random.default_rng(2)
+    checked = 0
+    for it in range(400):
+        sa, sb = rand_shapes(rng)
+        out_shape = np.broadcast_shapes(sa, sb)
+        n_out = int(np.prod(out_shape))
+        if n_out == 0:
+            continue
+        a = rand_view(rng, sa, 0x100000 + 4 * int(rng.integers(0, 2)))
+        b = rand_view(rng, sb, 0x900000)
+        if rng.random() < 0.5:
+            ost = dense_strides(out_shape)
+        else:
+            ost = rand_view(rng, out_shape, 0).strides
+        outp = 0x4000000 + (4 if rng.random() < 0.2 else 0)
+        cap = n_out + 8
+        rec = (ctypes.c_int64 * (3 * cap))()
+        nrec = ctypes.c_int64()
+        rc = L.zr_test_emulate_fwd(a.desc, b.desc, outp, _i64(ost), cap, rec, ctypes.byref(nrec))
+        assert rc == 0, (sa, sb, rc)
+        r = np.frombuffer(rec, np.int64)[: 3 * nrec.value].reshape(-1, 3)
+        assert r.shape[0] == n_out
+        o = naive_offsets(out_shape, out_shape, ost).ravel()
+        ao = naive_offsets(out_shape, sa, a.strides).ravel()
+        bo = naive_offsets(out_shape, sb, b.strides).ravel()
+        order = np.argsort(r[:, 0])
+        ref_order = np.argsort(o)
+        np.testing.assert_array_equal(r[order, 0], o[ref_order])
+        np.testing.assert_array_equal(r[order, 1], ao[ref_order])
+        np.testing.assert_array_equal(r[order, 2], bo[ref_order])
+        checked += 1
+    assert checked > 250
+
+
+def grad_index(out_shape, x_shape):
+    """Index into x's dense row-major layout for every output coordinate."""
+    return naive_offsets(out_shape, x_shape, dense_strides(x_shape))
+
+
+@pytest.mark.parametrize("op", [0, 1, 2, 3])
+def test_emulated_backward_matches_naive(L, op):
+    rng = np.random.default_rng(10 + op)
+    checked = 0
+    for it in range(250):
+        sa, sb = rand_shapes(rng)
+        out_shape = np.broadcast_shapes(sa, sb)
+        n_out = int(np.prod(out_shape))
+        if n_out == 0:
+            continue
+        g = rand_view(rng, out_shape, 0x100000 + 4 * int(rng.integers(0, 2)))
+        a = rand_view(rng, sa, 0x2000000)
+        b = rand_view(rng, sb, 0x3000000)
+        want = int(rng.integers(1, 4))
+        pa = 0x5000000 if want & 1 else None
+        pb = 0x6000000 if want & 2 else None
+        buf = ctypes.create_string_buffer(8192)
+        assert L.zr_test_describe_bwd(op, g.desc, a.desc, b.desc, pa, pb, buf, 8192) == 0
+        desc = json.loads(buf.value.decode())
+        cap = 2 * n_out + 8
+        rec = (ctypes.c_int64 * (7 * cap))()
+        nrec = ctypes.c_int64()
+        rc = L.zr_test_emulate_bwd(op, g.desc, a.desc, b.desc, pa, pb, cap, rec, ctypes.byref(nrec))
+        assert rc == 0
+        r = np.frombuffer(rec, np.int64)[: 7 * nrec.value].reshape(-1, 7)
+        go = naive_offsets(out_shape, out_shape, g.strides).ravel()
+        ao = naive_offsets(out_shape, sa, a.strides).ravel()
+        bo = naive_offsets(out_shape, sb, b.strides).ravel()
+        xa = grad_index(out_shape, sa).ravel()
+        xb = grad_index(out_shape, sb).ravel()
+        dense = np.arange(n_out, dtype=np.int64)
+        ref_by_g = np.argsort(go)
+        plans = desc["plans"]
+        for pi, plan in enumerate(plans):
+            rp = r[r[:, 0] == pi]
+            assert rp.shape[0] == n_out, (sa, sb, plan)
+            order = np.argsort(rp[:, 1])
+            np.testing.assert_array_equal(rp[order, 1], go[ref_by_g])
+            rows = rp[order]
+            ref = ref_by_g
+            if rows[0, 2] != -1:
+                np.testing.assert_array_equal(rows[:, 2], ao[ref])
+            if rows[0, 3] != -1:
+                np.testing.assert_array_equal(rows[:, 3], bo[ref])
+            if plan["kernel"] == "reduce":
+                which = desc["which"][pi]
+                np.testing.assert_array_equal(rows[:, 4], (xa if which == 0 else xb)[ref])
+                assert rows[:, 5].min() >= 0 and rows[:, 5].max() < plan["nslots"]
+                if plan["dense_out"]:
+                    np.testing.assert_array_equal(rows[:, 6], dense[ref])
+            else:
+                np.testing.assert_array_equal(rows[:, 6], dense[ref])
+        checked += 1
+    assert checked > 150
+
+
+def test_plan_dispatch_for_workloads(L):
+    """The five workloads coalesce the way the design expects."""
+    T = 1 << 40  # fake base addresses far apart
+
+    def fwd(sa, sb, sta=None):
+        a, b = FakeT(T, sa, sta), FakeT(2 * T, sb)
+        buf = ctypes.create_string_buffer(4096)
+        assert L.zr_test_describe_fwd(2, a.desc, b.desc, 3 * T, None, buf, 4096) == 0
+        return json.loads(buf.value.decode())
+
+    def bwd(op, sa, sb, sta=None):
+        out = np.broadcast_shapes(sa, sb)
+        g, a, b = FakeT(T, out), FakeT(2 * T, sa, sta), FakeT(3 * T, sb)
+        buf = ctypes.create_string_buffer(4096)
+        assert L.zr_test_describe_bwd(op, g.desc, a.desc, b.desc, 4 * T, 5 * T, buf, 4096) == 0
+        return json.loads(buf.value.decode())
+
+    d = fwd((4096, 1024), (1024,))
+    assert (d["nrow"], d["ncol"], d["vec"], d["inner_stride"][1]) == (4096, 1024, 4, 1)
+    d = fwd((8, 12, 1024, 1024), (1,))
+    assert (d["nrow"], d["ncol"], d["inner_stride"][1]) == (1, 8 * 12 * 1024 * 1024, 0)
+    d = fwd((8, 12, 1024, 1024), (1, 1, 1024, 1024))
+    assert (d["nrow"], d["ncol"]) == (96, 1024 * 1024)
+    d = fwd((128, 256, 512), (1, 256, 1), sta=(131072, 1, 256))
+    assert d["row_dims"] == 2 and d["inner_stride"][0] == 256
+    d = fwd((4, 1, 8, 1, 16, 1, 32, 64), (1, 6, 1, 12, 1, 10, 1, 64))
+    assert d["row_dims"] == 7 and d["ncol"] == 64 and d["vec"] == 4
+    d = bwd(0, (4096, 1024), (1024,))
+    (p,) = d["plans"]
+    assert p["kernel"] == "reduce" and p["inner_kept"] == 1 and p["dense_out"] == 1
+    assert (p["n_kept"], p["n_red"], p["ncol"]) == (1, 4096, 1024)
+    d = bwd(1, (128, 256, 512), (1, 256, 1), sta=(131072, 1, 256))
+    (p,) = d["plans"]
+    assert p["inner_kept"] == 0 and (p["n_kept"], p["n_red"], p["ncol"]) == (256, 128, 512)
+    d = bwd(3, (100663296,), (1,))
+    (p,) = d["plans"]
+    assert p["inner_kept"] == 0 and p["n_kept"] == 1 and p["nout"] == 1
+
+
+def test_errors_before_any_device_access(L):
+    a = FakeT(0x100000, (2, 3, 4))
+    b = FakeT(0x200000, (2, 4, 5))
+    out = 0x300000
+    assert L.zr_binary_fwd(0, a.desc, b.desc, out, None, None) == -3
+    bad = ZrTensor(0x100000, 9, _i64([1] * 9), None)
+    assert L.zr_binary_fwd(0, bad, b.desc, out, None, None) == -2
+    neg = FakeT(0x100000, (2, -1), (1, 1))
+    assert L.zr_binary_fwd(0, neg.desc, b.desc, out, None, None) == -4
+    assert L.zr_binary_fwd(7, a.desc, a.desc, out, None, None) == -1
+    # Output overlapping an input partially.
+    x = FakeT(0x100000, (4, 4))
+    assert L.zr_binary_fwd(0, x.desc, x.desc, 0x100000 + 4, None, None) == -5
+    # Output with a zero stride overlaps itself.
+    assert L.zr_binary_fwd(0, x.desc, x.desc, 0x900000, _i64([0, 1]), None) == -5
+    # Workspace query is host-only and sizes the partials.
+    T = 1 << 40
+    g = FakeT(T, (4096, 1024))
+    xx = FakeT(2 * T, (4096, 1024))
+    bias = FakeT(3 * T, (1024,))
+    nbytes = ctypes.c_size_t(0)
+    assert L.zr_binary_bwd(0, g.desc, xx.desc, bias.desc, 4 * T, 5 * T, None,
+                           ctypes.byref(nbytes), None) == 0
+    assert nbytes.value > 0
+    # grad_out of the wrong shape.
+    g2 = FakeT(T, (4096, 1023))
+    assert L.zr_binary_bwd(0, g2.desc, xx.desc, bias.desc, 4 * T, 5 * T, None,
+                           ctypes.byref(nbytes), None) == -3
+    # Gradients overlapping each other.
+    assert L.zr_binary_bwd(0, g.desc, xx.desc, bias.desc, 4 * T, 4 * T + 64, None,
+                           ctypes.byref(nbytes), None) == -5
+    # sum_to_shape onto a shape that does not broadcast back.
+    assert L.zr_sum_to_shape(xx.desc, 1, _i64([1023]), 6 * T, None, ctypes.byref(nbytes), None) == -3
