@@ -56,7 +56,7 @@ KERNEL_SOURCES = ["broadcast_elementwise_shape_gb300/csrc/zr_kernels.cuh",
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--steps", type=int, default=300)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["zr", "reference"], default="zr")
     p.add_argument("--workload", default="suite", help="suite or one of " + ",".join(SUITE))
@@ -236,12 +236,11 @@ class Suite:
                 self.calls.append(self._prepare(name, step, env, sizes))
 
     def _to_dev(self, v):
+        """Device copy keeping strides and storage offset (views included)."""
         torch = self.torch
-        if v.is_contiguous():
-            return v.to(self.device)
-        base = v._base if v._base is not None else v
-        d = base.contiguous().to(self.device)
-        return d.as_strided(v.shape, v.stride(), v.storage_offset() - base.storage_offset())
+        st = v.untyped_storage()
+        flat = torch.empty(0, dtype=v.dtype).set_(st, 0, (st.nbytes() // v.element_size(),), (1,))
+        return flat.to(self.device).as_strided(v.shape, v.stride(), v.storage_offset())
 
     def _desc(self, t):
         d, keep = self.zr._desc(t)
@@ -426,17 +425,14 @@ def run_e2e(args, suite, flush, stream, nbytes):
         for k in suite.in_names[name]:
             t = env[k]
             src = suite.host[name][k]
-            hp = torch.empty_like(src, device="cpu").pin_memory() if src.is_contiguous() else None
-            if hp is None:  # a view: copy its storage
-                base = src._base if src._base is not None else src
-                hb = base.contiguous().pin_memory()
-                db = t._base if t._base is not None else t
-                pinned_in.append((db, hb))
-                h2d += hb.numel() * 4
-            else:
-                hp.copy_(src)
-                pinned_in.append((t, hp))
-                h2d += hp.numel() * 4
+            # Copy the whole storage (views keep their layout).
+            st = src.untyped_storage()
+            hs = torch.empty(0, dtype=src.dtype).set_(st, 0, (st.nbytes() // 4,), (1,))
+            hp = hs.pin_memory()
+            ds = t.untyped_storage()
+            dflat = torch.empty(0, dtype=t.dtype, device=t.device).set_(ds, 0, (ds.nbytes() // 4,), (1,))
+            pinned_in.append((dflat, hp))
+            h2d += hp.numel() * 4
         for k in suite.out_names[name]:
             t = env[k]
             hp = torch.empty(t.shape, dtype=torch.float32).pin_memory()

@@ -373,6 +373,27 @@ int plan_sum(const zr_tensor& tin, int32_t ndo, const int64_t* so, float* out, S
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? ZR_OK : ZR_ERR_CUDA; }
 
+// Launch (or, with dry, only guard-check) the kernels of a backward plan.
+int launch_bwd_set(const BwdSet& S, int op, void* workspace, cudaStream_t st, bool dry) {
+  if (S.direct) return cuda_status(launch_bwd_direct(op, S.want, S.eb, st, dry));
+  for (int i = 0; i < S.nred; ++i) {
+    RedBuild rbi = S.rb[i];
+    rbi.plan.partial = reinterpret_cast<float*>(static_cast<char*>(workspace) + S.ws_off[i]);
+    rbi.comb.partial = rbi.plan.partial;
+    const int rc = cuda_status(launch_reduce(op, S.which[i], rbi, st, dry));
+    if (rc) return rc;
+  }
+  return ZR_OK;
+}
+
+int launch_sum_set(const SumSet& S, void* workspace, cudaStream_t st, bool dry) {
+  if (S.copy) return cuda_status(launch_copy(S.eb, st, dry));
+  RedBuild rb = S.rb;
+  rb.plan.partial = static_cast<float*>(workspace);
+  rb.comb.partial = rb.plan.partial;
+  return cuda_status(launch_reduce(OP_ADD, 2, rb, st, dry));
+}
+
 int copy_json(const std::string& s, char* buf, size_t len) {
   if (!buf || len == 0) return ZR_ERR_NULL;
   const size_t m = std::min(len - 1, s.size());
@@ -455,15 +476,7 @@ int zr_binary_bwd(zr_op op, zr_tensor grad_out, zr_tensor a, zr_tensor b, float*
     rc = check_device_ptr(p);
     if (rc) return rc;
   }
-  if (S.direct) return cuda_status(launch_bwd_direct(op, S.want, S.eb, st));
-  for (int i = 0; i < S.nred; ++i) {
-    RedBuild rbi = S.rb[i];
-    rbi.plan.partial = reinterpret_cast<float*>(static_cast<char*>(workspace) + S.ws_off[i]);
-    rbi.comb.partial = rbi.plan.partial;
-    rc = cuda_status(launch_reduce(op, S.which[i], rbi, st));
-    if (rc) return rc;
-  }
-  return ZR_OK;
+  return launch_bwd_set(S, op, workspace, st, false);
 }
 
 int zr_sum_to_shape(zr_tensor in, int32_t ndim_out, const int64_t* sizes_out, float* out,
@@ -494,11 +507,7 @@ int zr_sum_to_shape(zr_tensor in, int32_t ndim_out, const int64_t* sizes_out, fl
     rc = check_device_ptr(p);
     if (rc) return rc;
   }
-  if (S.copy) return cuda_status(launch_copy(S.eb, st));
-  RedBuild rb = S.rb;
-  rb.plan.partial = static_cast<float*>(workspace);
-  rb.comb.partial = rb.plan.partial;
-  return cuda_status(launch_reduce(OP_ADD, 2, rb, st));
+  return launch_sum_set(S, workspace, st, false);
 }
 
 const char* zr_status_string(int status) {
@@ -522,6 +531,32 @@ int zr_test_fastdiv(uint32_t d, uint32_t n, uint32_t* q) {
   if (!q || d == 0) return ZR_ERR_NULL;
   *q = fd_div(make_fastdiv(d), n);
   return ZR_OK;
+}
+
+int zr_test_dry_run_fwd(zr_op op, zr_tensor a, zr_tensor b, const float* out,
+                        const int64_t* out_strides) {
+  FwdSet S;
+  const int rc = plan_fwd(op, a, b, out, out_strides, &S);
+  if (rc || S.empty) return rc;
+  return cuda_status(launch_fwd(op, S.eb, nullptr, true));
+}
+
+int zr_test_dry_run_bwd(zr_op op, zr_tensor grad_out, zr_tensor a, zr_tensor b,
+                        const float* grad_a, const float* grad_b) {
+  BwdSet S;
+  const int rc = plan_bwd(op, grad_out, a, b, const_cast<float*>(grad_a),
+                          const_cast<float*>(grad_b), &S);
+  if (rc || S.nothing || S.empty) return rc;
+  // A stand-in workspace address: only checked for presence, never touched.
+  return launch_bwd_set(S, op, reinterpret_cast<void*>(uintptr_t(1) << 40), nullptr, true);
+}
+
+int zr_test_dry_run_sum(zr_tensor in, int32_t ndim_out, const int64_t* sizes_out,
+                        const float* out) {
+  SumSet S;
+  const int rc = plan_sum(in, ndim_out, sizes_out, const_cast<float*>(out), &S);
+  if (rc || S.empty) return rc;
+  return launch_sum_set(S, reinterpret_cast<void*>(uintptr_t(1) << 40), nullptr, true);
 }
 
 int zr_test_describe_fwd(zr_op op, zr_tensor a, zr_tensor b, const float* out,

@@ -210,8 +210,12 @@ k_elementwise(const __grid_constant__ EwPlan p) {
 // the other term.
 template <int OP, int WHICH>
 struct RedTerms {
-  static constexpr bool kReadA = (WHICH < 2) && (Needs<OP, 0>::a || Needs<OP, 1>::a);
-  static constexpr bool kReadB = (WHICH < 2) && (Needs<OP, 0>::b || Needs<OP, 1>::b);
+  // Inputs read by X's term, and by the dense gradient's term (only when a
+  // dense gradient is written in the same pass).
+  static constexpr bool kXa = Needs<OP, WHICH>::a;
+  static constexpr bool kXb = Needs<OP, WHICH>::b;
+  static constexpr bool kDa = WHICH < 2 && Needs<OP, 1 - WHICH>::a;
+  static constexpr bool kDb = WHICH < 2 && Needs<OP, 1 - WHICH>::b;
   __device__ __forceinline__ static float x(float g, float a, float b) {
     if (WHICH == 0) return term_a<OP>(g, a, b);
     if (WHICH == 1) return term_b<OP>(g, a, b);
@@ -221,6 +225,9 @@ struct RedTerms {
     if (WHICH == 0) return term_b<OP>(g, a, b);
     return term_a<OP>(g, a, b);
   }
+  // The same rule on the host: which pointers the kernel dereferences.
+  static bool reads_a(bool has_d) { return kXa || (has_d && kDa); }
+  static bool reads_b(bool has_d) { return kXb || (has_d && kDb); }
 };
 
 // Reduction pass.  CTA = (kept index, row block, column block).  Rows of
@@ -250,6 +257,8 @@ k_reduce(const __grid_constant__ RedPlan p) {
   const uint32_t tx = threadIdx.x % p.tx;
   const uint32_t ty = threadIdx.x / p.tx;
   const bool has_d = p.d_out != nullptr;
+  const bool read_a = T::kXa || (has_d && T::kDa);
+  const bool read_b = T::kXb || (has_d && T::kDb);
   const uint32_t vcol_begin = cta.cblk * p.vcols_per_blk;
   const uint32_t vcol_end_raw = vcol_begin + p.vcols_per_blk;
   const uint32_t vcol_end = vcol_end_raw < p.nvcol ? vcol_end_raw : p.nvcol;
@@ -283,8 +292,10 @@ k_reduce(const __grid_constant__ RedPlan p) {
           if (ok[u]) {
             const int64_t* ro = s_off + ri * kMaxOperands;
             gv[u] = load_cols<VEC>(p.g, ro[0], p.inner_stride[0], c, p.stream_mask & 1);
-            if (T::kReadA) av[u] = load_cols<VEC>(p.a, ro[1], p.inner_stride[1], c, p.stream_mask & 2);
-            if (T::kReadB) bv[u] = load_cols<VEC>(p.b, ro[2], p.inner_stride[2], c, p.stream_mask & 4);
+            if ((T::kXa || T::kDa) && read_a)
+              av[u] = load_cols<VEC>(p.a, ro[1], p.inner_stride[1], c, p.stream_mask & 2);
+            if ((T::kXb || T::kDb) && read_b)
+              bv[u] = load_cols<VEC>(p.b, ro[2], p.inner_stride[2], c, p.stream_mask & 4);
           }
         }
 #pragma unroll
@@ -294,8 +305,8 @@ k_reduce(const __grid_constant__ RedPlan p) {
 #pragma unroll
           for (int i = 0; i < VEC; ++i) {
             const float gg = gv[u].v[i];
-            const float aa = T::kReadA ? av[u].v[i] : 0.f;
-            const float bb = T::kReadB ? bv[u].v[i] : 0.f;
+            const float aa = ((T::kXa || T::kDa) && read_a) ? av[u].v[i] : 0.f;
+            const float bb = ((T::kXb || T::kDb) && read_b) ? bv[u].v[i] : 0.f;
             if (INNER_KEPT) acc[i].add(T::x(gg, aa, bb));
             else acc[0].add(T::x(gg, aa, bb));
             if (has_d) dv.v[i] = T::d(gg, aa, bb);

@@ -7,12 +7,15 @@
 
 namespace zr {
 
-cudaError_t launch_fwd(int op, const EwBuild& eb, cudaStream_t s);
+// Every launcher first checks that the plan provides each operand its kernel
+// dereferences (cudaErrorInvalidValue otherwise); with dry == true it stops
+// there and launches nothing.
+cudaError_t launch_fwd(int op, const EwBuild& eb, cudaStream_t s, bool dry = false);
 // want: bit 0 grad_a, bit 1 grad_b (no reduction).
-cudaError_t launch_bwd_direct(int op, int want, const EwBuild& eb, cudaStream_t s);
-cudaError_t launch_copy(const EwBuild& eb, cudaStream_t s);
+cudaError_t launch_bwd_direct(int op, int want, const EwBuild& eb, cudaStream_t s, bool dry = false);
+cudaError_t launch_copy(const EwBuild& eb, cudaStream_t s, bool dry = false);
 // which: 0 = grad_a, 1 = grad_b, 2 = sum-to-shape.  Launches the reduction
 // pass and, when it writes partials, the combine pass.
-cudaError_t launch_reduce(int op, int which, const RedBuild& rb, cudaStream_t s);
+cudaError_t launch_reduce(int op, int which, const RedBuild& rb, cudaStream_t s, bool dry = false);
 
 }  // namespace zr

@@ -7,7 +7,12 @@ namespace zr {
 namespace {
 
 template <class F, int NOUT>
-cudaError_t launch_ew_t(const EwBuild& eb, cudaStream_t s) {
+cudaError_t launch_ew_t(const EwBuild& eb, cudaStream_t s, bool dry) {
+  // Refuse a launch whose kernel would dereference a missing operand.
+  if (!eb.plan.in[0] || (F::kR1 && !eb.plan.in[1]) || (F::kR2 && !eb.plan.in[2]) ||
+      (!eb.plan.out[0] && !eb.plan.out[1]))
+    return cudaErrorInvalidValue;
+  if (dry) return cudaSuccess;
   const size_t smem = size_t(eb.plan.tile_rows) * kMaxOperands * sizeof(int64_t);
   if (eb.vec == 4)
     k_elementwise<F, 4, NOUT><<<eb.plan.n_cta, kThreads, smem, s>>>(eb.plan);
@@ -17,36 +22,36 @@ cudaError_t launch_ew_t(const EwBuild& eb, cudaStream_t s) {
 }
 
 template <int OP>
-cudaError_t launch_direct_op(int want, const EwBuild& eb, cudaStream_t s) {
+cudaError_t launch_direct_op(int want, const EwBuild& eb, cudaStream_t s, bool dry) {
   switch (want) {
-    case 1: return launch_ew_t<BwdDirectF<OP, 1>, 2>(eb, s);
-    case 2: return launch_ew_t<BwdDirectF<OP, 2>, 2>(eb, s);
-    default: return launch_ew_t<BwdDirectF<OP, 3>, 2>(eb, s);
+    case 1: return launch_ew_t<BwdDirectF<OP, 1>, 2>(eb, s, dry);
+    case 2: return launch_ew_t<BwdDirectF<OP, 2>, 2>(eb, s, dry);
+    default: return launch_ew_t<BwdDirectF<OP, 3>, 2>(eb, s, dry);
   }
 }
 
 }  // namespace
 
-cudaError_t launch_fwd(int op, const EwBuild& eb, cudaStream_t s) {
+cudaError_t launch_fwd(int op, const EwBuild& eb, cudaStream_t s, bool dry) {
   switch (op) {
-    case OP_ADD: return launch_ew_t<FwdF<OP_ADD>, 1>(eb, s);
-    case OP_SUB: return launch_ew_t<FwdF<OP_SUB>, 1>(eb, s);
-    case OP_MUL: return launch_ew_t<FwdF<OP_MUL>, 1>(eb, s);
-    default: return launch_ew_t<FwdF<OP_DIV>, 1>(eb, s);
+    case OP_ADD: return launch_ew_t<FwdF<OP_ADD>, 1>(eb, s, dry);
+    case OP_SUB: return launch_ew_t<FwdF<OP_SUB>, 1>(eb, s, dry);
+    case OP_MUL: return launch_ew_t<FwdF<OP_MUL>, 1>(eb, s, dry);
+    default: return launch_ew_t<FwdF<OP_DIV>, 1>(eb, s, dry);
   }
 }
 
-cudaError_t launch_bwd_direct(int op, int want, const EwBuild& eb, cudaStream_t s) {
+cudaError_t launch_bwd_direct(int op, int want, const EwBuild& eb, cudaStream_t s, bool dry) {
   switch (op) {
-    case OP_ADD: return launch_direct_op<OP_ADD>(want, eb, s);
-    case OP_SUB: return launch_direct_op<OP_SUB>(want, eb, s);
-    case OP_MUL: return launch_direct_op<OP_MUL>(want, eb, s);
-    default: return launch_direct_op<OP_DIV>(want, eb, s);
+    case OP_ADD: return launch_direct_op<OP_ADD>(want, eb, s, dry);
+    case OP_SUB: return launch_direct_op<OP_SUB>(want, eb, s, dry);
+    case OP_MUL: return launch_direct_op<OP_MUL>(want, eb, s, dry);
+    default: return launch_direct_op<OP_DIV>(want, eb, s, dry);
   }
 }
 
-cudaError_t launch_copy(const EwBuild& eb, cudaStream_t s) {
-  return launch_ew_t<CopyF, 1>(eb, s);
+cudaError_t launch_copy(const EwBuild& eb, cudaStream_t s, bool dry) {
+  return launch_ew_t<CopyF, 1>(eb, s, dry);
 }
 
 }  // namespace zr

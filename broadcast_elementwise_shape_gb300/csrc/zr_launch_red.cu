@@ -8,8 +8,16 @@ namespace zr {
 namespace {
 
 template <int OP, int WHICH>
-cudaError_t launch_red_t(const RedBuild& rb, cudaStream_t s) {
+cudaError_t launch_red_t(const RedBuild& rb, cudaStream_t s, bool dry) {
   const RedPlan& p = rb.plan;
+  // Refuse a launch whose kernel would dereference an operand the plan did
+  // not provide.
+  const bool has_d = p.d_out != nullptr;
+  if (!p.g || (RedTerms<OP, WHICH>::reads_a(has_d) && !p.a) ||
+      (RedTerms<OP, WHICH>::reads_b(has_d) && !p.b) || !p.x_final ||
+      (p.nslots > 1 && !p.partial))
+    return cudaErrorInvalidValue;
+  if (dry) return cudaSuccess;
   const uint32_t table_rows = p.rows_per_blk < kMaxTileRows ? p.rows_per_blk : kMaxTileRows;
   const size_t red_floats = p.inner_kept ? size_t(kThreads) * rb.vec : size_t(kThreads);
   const size_t smem = size_t(table_rows) * kMaxOperands * sizeof(int64_t) + red_floats * sizeof(float);
@@ -29,19 +37,19 @@ cudaError_t launch_red_t(const RedBuild& rb, cudaStream_t s) {
 }
 
 template <int OP>
-cudaError_t launch_red_op(int which, const RedBuild& rb, cudaStream_t s) {
-  return which == 0 ? launch_red_t<OP, 0>(rb, s) : launch_red_t<OP, 1>(rb, s);
+cudaError_t launch_red_op(int which, const RedBuild& rb, cudaStream_t s, bool dry) {
+  return which == 0 ? launch_red_t<OP, 0>(rb, s, dry) : launch_red_t<OP, 1>(rb, s, dry);
 }
 
 }  // namespace
 
-cudaError_t launch_reduce(int op, int which, const RedBuild& rb, cudaStream_t s) {
-  if (which == 2) return launch_red_t<OP_ADD, 2>(rb, s);
+cudaError_t launch_reduce(int op, int which, const RedBuild& rb, cudaStream_t s, bool dry) {
+  if (which == 2) return launch_red_t<OP_ADD, 2>(rb, s, dry);
   switch (op) {
-    case OP_ADD: return launch_red_op<OP_ADD>(which, rb, s);
-    case OP_SUB: return launch_red_op<OP_SUB>(which, rb, s);
-    case OP_MUL: return launch_red_op<OP_MUL>(which, rb, s);
-    default: return launch_red_op<OP_DIV>(which, rb, s);
+    case OP_ADD: return launch_red_op<OP_ADD>(which, rb, s, dry);
+    case OP_SUB: return launch_red_op<OP_SUB>(which, rb, s, dry);
+    case OP_MUL: return launch_red_op<OP_MUL>(which, rb, s, dry);
+    default: return launch_red_op<OP_DIV>(which, rb, s, dry);
   }
 }
 

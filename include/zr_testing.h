@@ -26,6 +26,16 @@ int zr_test_describe_bwd(zr_op op, zr_tensor grad_out, zr_tensor a, zr_tensor b,
 int zr_test_describe_sum(zr_tensor in, int32_t ndim_out, const int64_t* sizes_out,
                          const float* out, char* buf, size_t len);
 
+/* Plan a call and run the launch-time operand checks without launching:
+ * ZR_OK, an argument error, or ZR_ERR_CUDA if a kernel would read an operand
+ * the plan does not provide. */
+int zr_test_dry_run_fwd(zr_op op, zr_tensor a, zr_tensor b, const float* out,
+                        const int64_t* out_strides);
+int zr_test_dry_run_bwd(zr_op op, zr_tensor grad_out, zr_tensor a, zr_tensor b,
+                        const float* grad_a, const float* grad_b);
+int zr_test_dry_run_sum(zr_tensor in, int32_t ndim_out, const int64_t* sizes_out,
+                        const float* out);
+
 /* Walk every (CTA, thread item) of the planned forward kernel on the host and
  * record, per element visited, {out_offset, a_offset, b_offset} (element
  * units).  rec holds cap records of 3 int64; *nrec receives the count. */

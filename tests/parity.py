@@ -58,15 +58,14 @@ def is_single_op_grad(op: str, which: int, reduced: bool) -> bool:
 
 
 def to_gpu(x: torch.Tensor) -> torch.Tensor:
-    """Device copy keeping the view's strides (e.g. a transposed view)."""
-    if x.is_contiguous():
-        return x.cuda()
-    # Rebuild the same view over a device copy of its storage.
-    base = x
-    while base._base is not None:
-        base = base._base
-    dev_base = base.contiguous().cuda()
-    return dev_base.as_strided(x.shape, x.stride(), x.storage_offset() - base.storage_offset())
+    """Device copy with the same strides and storage offset: the whole
+    underlying storage is copied and the view rebuilt over it, so transposed,
+    stepped and misaligned views keep their layout on the GPU."""
+    st = x.untyped_storage()
+    n = st.nbytes() // x.element_size()
+    flat = torch.empty(0, dtype=x.dtype).set_(st, 0, (n,), (1,))
+    dev = flat.cuda()
+    return dev.as_strided(x.shape, x.stride(), x.storage_offset())
 
 
 def run_gpu(name: str, host: dict) -> dict:

@@ -333,3 +333,47 @@ def test_errors_before_any_device_access(L):
                            ctypes.byref(nbytes), None) == -5
     # sum_to_shape onto a shape that does not broadcast back.
     assert L.zr_sum_to_shape(xx.desc, 1, _i64([1023]), 6 * T, None, ctypes.byref(nbytes), None) == -3
+
+
+def _dry_lib(L):
+    vp = ctypes.c_void_p
+    i64p = ctypes.POINTER(ctypes.c_int64)
+    L.zr_test_dry_run_fwd.argtypes = [ctypes.c_int, ZrTensor, ZrTensor, vp, i64p]
+    L.zr_test_dry_run_bwd.argtypes = [ctypes.c_int, ZrTensor, ZrTensor, ZrTensor, vp, vp]
+    L.zr_test_dry_run_sum.argtypes = [ZrTensor, ctypes.c_int32, i64p, vp]
+    return L
+
+
+NEEDS_A = {0: (False, False), 1: (False, False), 2: (False, True), 3: (False, True)}
+NEEDS_B = {0: (False, False), 1: (False, False), 2: (True, False), 3: (True, True)}
+
+
+@pytest.mark.parametrize("op", [0, 1, 2, 3])
+def test_every_plan_provides_what_its_kernels_read(L, op):
+    """Plans built with a/b data NULL whenever no requested gradient needs
+    them must pass the launch-time operand checks (a kernel that would read a
+    missing operand is refused before launch)."""
+    L = _dry_lib(L)
+    T = 1 << 40
+    rng = np.random.default_rng(50 + op)
+    shapes = [((4, 1, 8, 1, 16, 1, 32, 64), (1, 6, 1, 12, 1, 10, 1, 64)),
+              ((4096, 1024), (1024,)), ((16, 1024, 768), (768,)), ((32, 64, 128), (64, 1)),
+              ((8, 12, 1024, 1024), (1, 1, 1024, 1024)), ((100663296,), (1,))]
+    for _ in range(150):
+        shapes.append(rand_shapes(rng))
+    for sa, sb in shapes:
+        out_shape = tuple(np.broadcast_shapes(sa, sb))
+        if int(np.prod(out_shape)) == 0:
+            continue
+        for want in (1, 2, 3):
+            need_a = (want & 1 and NEEDS_A[op][0]) or (want & 2 and NEEDS_A[op][1])
+            need_b = (want & 1 and NEEDS_B[op][0]) or (want & 2 and NEEDS_B[op][1])
+            g = FakeT(T, out_shape)
+            a = FakeT(2 * T if need_a else None, sa)
+            b = FakeT(3 * T if need_b else None, sb)
+            pa = 4 * T if want & 1 else None
+            pb = 5 * T if want & 2 else None
+            assert L.zr_test_dry_run_bwd(op, g.desc, a.desc, b.desc, pa, pb) == 0, (op, want, sa, sb)
+        a, b = FakeT(2 * T, sa), FakeT(3 * T, sb)
+        assert L.zr_test_dry_run_fwd(op, a.desc, b.desc, 4 * T, None) == 0
+        assert L.zr_test_dry_run_sum(g.desc, len(sb), _i64(sb), 6 * T) in (0, -3)
