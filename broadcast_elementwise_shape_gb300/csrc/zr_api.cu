@@ -6,6 +6,7 @@
 
 #include <algorithm>
 #include <cstring>
+#include <mutex>
 #include <string>
 
 #include "../../include/zr.h"
@@ -477,6 +478,88 @@ int zr_binary_bwd(zr_op op, zr_tensor grad_out, zr_tensor a, zr_tensor b, float*
     if (rc) return rc;
   }
   return launch_bwd_set(S, op, workspace, st, false);
+}
+
+}  // extern "C"
+
+// ------------------------------------------------------------------ no-allocation backward
+//
+// Scratch for zr_binary_bwd_noalloc: the partial sums of its two-pass
+// reduction live here instead of in a caller-provided workspace.  The array
+// exists once per device that loads this library and stays until the process
+// exits.  Host code cannot use the array's name as a device address, so the
+// address is looked up with cudaGetSymbolAddress, once per device, with that
+// device current, on the first call made on it.
+static __device__ __align__(256) unsigned char zr_noalloc_scratch[ZR_STATIC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int kScratchDevices = 256;
+std::mutex g_scratch_mu;
+void* g_scratch_addr[kScratchDevices] = {};
+
+// Device address of the scratch array on the current device.
+int noalloc_scratch(void** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return ZR_ERR_CUDA;
+  }
+  if (dev < 0 || dev >= kScratchDevices) return ZR_ERR_DEVICE;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (g_scratch_addr[dev] == nullptr) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, zr_noalloc_scratch);
+    if (e != cudaSuccess || p == nullptr) {
+      cudaGetLastError();
+      return ZR_ERR_CUDA;
+    }
+    g_scratch_addr[dev] = p;
+  }
+  *out = g_scratch_addr[dev];
+  return ZR_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int zr_binary_bwd_noalloc(zr_op op, zr_tensor grad_out, zr_tensor a, zr_tensor b, float* grad_a,
+                          float* grad_b, zr_stream_t stream) {
+  BwdSet S;
+  int rc = plan_bwd(op, grad_out, a, b, grad_a, grad_b, &S);
+  if (rc) return rc;
+  if (S.nothing) return ZR_OK;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (S.empty) {
+    for (int w = 0; w < 2; ++w) {
+      if (!S.zero_ptr[w]) continue;
+      rc = check_device_ptr(S.zero_ptr[w]);
+      if (rc) return rc;
+    }
+    for (int w = 0; w < 2; ++w)
+      if (S.zero_ptr[w] && cudaMemsetAsync(S.zero_ptr[w], 0, S.zero_bytes[w], st) != cudaSuccess)
+        return ZR_ERR_CUDA;
+    return ZR_OK;
+  }
+  // The plan's partials must fit the fixed scratch array.
+  if (S.ws_run > size_t(ZR_STATIC_SCRATCH_BYTES)) return ZR_ERR_WORKSPACE;
+  const bool ra = (grad_a && needs_a(op, 0)) || (grad_b && needs_a(op, 1));
+  const bool rb = (grad_a && needs_b(op, 0)) || (grad_b && needs_b(op, 1));
+  const void* ptrs[5] = {S.g.ptr, ra ? S.a.ptr : nullptr, rb ? S.b.ptr : nullptr, grad_a, grad_b};
+  for (const void* p : ptrs) {
+    if (!p) continue;
+    rc = check_device_ptr(p);
+    if (rc) return rc;
+  }
+  void* scratch = nullptr;
+  if (S.ws_run > 0) {
+    rc = noalloc_scratch(&scratch);
+    if (rc) return rc;
+  }
+  // Every partial slot the plan uses is written by the first pass before the
+  // second pass reads it, so the scratch needs no clearing between calls.
+  return launch_bwd_set(S, op, scratch, st, false);
 }
 
 int zr_sum_to_shape(zr_tensor in, int32_t ndim_out, const int64_t* sizes_out, float* out,

@@ -149,6 +149,45 @@ int zr_binary_bwd(zr_op op, zr_tensor grad_out, zr_tensor a, zr_tensor b,
                   void* workspace, size_t* workspace_bytes, zr_stream_t stream);
 
 /*
+ * Size of the scratch array behind zr_binary_bwd_noalloc, in bytes.  Every
+ * device that loads this library holds one such array until the process
+ * exits.
+ */
+#define ZR_STATIC_SCRATCH_BYTES (8u << 20)
+
+/*
+ * zr_binary_bwd_noalloc — the same fused backward as zr_binary_bwd, for
+ * callers that cannot hand the library a workspace.  The pages have no
+ * counterpart: this is an interface convenience, not part of the method.
+ *
+ * Who needs it: code that must not, or cannot, request device memory while
+ * it runs — for example a callback inside a host framework that owns every
+ * device allocation through its own pool and gives a library only the
+ * tensors themselves, or a latency-critical path where cudaMalloc could
+ * synchronise the device or fail under memory pressure.  This entry point
+ * calls no allocator of any kind (no cudaMalloc, cudaFree, or allocating
+ * library routine): the reduction's partial sums go to a fixed array of
+ * ZR_STATIC_SCRATCH_BYTES bytes compiled into the library.
+ *
+ * Arguments, layout and results are those of zr_binary_bwd, without the
+ * workspace.  A problem whose partial sums need more than
+ * ZR_STATIC_SCRATCH_BYTES is rejected with ZR_ERR_WORKSPACE before anything
+ * is launched (use zr_binary_bwd with a workspace for it; its workspace query
+ * reports the size).
+ *
+ * The array is shared by every call on a device and keeps whatever the last
+ * call left in it; nothing in it needs to start at zero, since each call
+ * writes every partial it later reads.  Two calls whose work overlaps on the
+ * GPU (e.g. on two streams without ordering between them) race on the array
+ * and may return wrong gradients: order them, for instance by issuing them on
+ * one stream.  The first call on each device looks up the array's device
+ * address (cudaGetSymbolAddress, with that device current); make that first
+ * call before any stream capture.
+ */
+int zr_binary_bwd_noalloc(zr_op op, zr_tensor grad_out, zr_tensor a, zr_tensor b,
+                          float* grad_a, float* grad_b, zr_stream_t stream);
+
+/*
  * zr_sum_to_shape — OpSumToSize (Operator page, 广播): out[j] = sum of every
  * element of `in` whose coordinate maps to j when sizes_out is broadcast to
  * in's shape.  sizes_out must broadcast with in's shape to exactly in's shape
