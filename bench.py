@@ -60,6 +60,9 @@ def parse():
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["zr", "reference"], default="zr")
     p.add_argument("--workload", default="suite", help="suite or one of " + ",".join(SUITE))
+    p.add_argument("--dims", default=None,
+                   help="JSON size overrides for a single --workload (see workloads.DEFAULT_DIMS), "
+                        "e.g. for a smaller profiling case")
     p.add_argument("--e2e-steps", type=int, default=3)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
@@ -191,7 +194,7 @@ class Suite:
     """Device tensors, preallocated outputs/workspaces and prepared C-ABI
     calls for the chosen workloads."""
 
-    def __init__(self, names, device):
+    def __init__(self, names, device, dims=None):
         import torch
         import broadcast_elementwise_shape_gb300 as zr
         from broadcast_elementwise_shape_gb300 import ZrTensor
@@ -213,7 +216,7 @@ class Suite:
         L.zr_test_describe_fwd.argtypes = [ctypes.c_int, ZrTensor, ZrTensor, ctypes.c_void_p,
                                            i64p, ctypes.c_char_p, ctypes.c_size_t]
         for name in names:
-            host = workloads.make_inputs(name)
+            host = workloads.make_inputs(name, **(dims or {}))
             sizes, shapes = shape_table(name, host)
             env = {}
             for k, v in host.items():
@@ -309,7 +312,10 @@ def run_zr(args, rank, world, local):
     if world > 1:
         dist.init_process_group("nccl", device_id=device)
     names = SUITE if args.workload == "suite" else [args.workload]
-    suite = Suite(names, device)
+    dims = json.loads(args.dims) if args.dims else None
+    if dims and args.workload == "suite":
+        raise SystemExit("--dims needs a single --workload")
+    suite = Suite(names, device, dims)
     nbytes = suite.step_bytes()
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
     flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=device)
@@ -401,7 +407,8 @@ def run_zr(args, rank, world, local):
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(total_ms / args.steps, 5), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": WORKLOAD_DESC if args.workload == "suite" else args.workload,
+            "config": {"workload": WORKLOAD_DESC if args.workload == "suite" else
+                       (args.workload + (" " + json.dumps(dims) if dims else "")),
                        "bytes_per_step": nbytes,
                        "l2": "flushed before every step (2x L2 write, outside the timed events)",
                        "pct_of_measured_hbm": round(value / world / peak, 4),
