@@ -8,6 +8,7 @@
 #include <cstring>
 #include <mutex>
 #include <string>
+#include <vector>
 
 #include "../../include/zr.h"
 #include "../../include/zr_testing.h"
@@ -172,6 +173,8 @@ struct BwdSet {
   int nred = 0;
   int which[2] = {0, 0};
   RedBuild rb[2];
+  bool sab = false;              // fused both-reduced pass (k_sab)
+  SabBuild sb;
   size_t ws_off[2] = {0, 0};
   size_t ws_run = 0;             // bytes this call uses
   size_t ws_query = 0;           // bytes reported by a workspace query
@@ -302,6 +305,21 @@ int plan_bwd(int op, const zr_tensor& tg, const zr_tensor& ta, const zr_tensor& 
   }
   S->ws_run = off;
   S->ws_query = off_q;
+  // Both gradients reduced: one fused pass when the shape allows it.
+  if (red_a && red_b) {
+    const int r = build_sab(P, S->g.ptr, S->a.ptr, S->b.ptr, grad_a, grad_b, read_mask, &S->sb);
+    if (r == ZR_OK) {
+      S->sab = true;
+      S->ws_run = S->sb.ws_a_bytes + S->sb.ws_b_bytes;
+    } else if (r != 1) {
+      return r;
+    }
+    // The query covers whichever route the run-time pointers select.
+    SabBuild any;
+    const float* fake = reinterpret_cast<const float*>(uintptr_t(256));
+    if (build_sab(P, fake, fake, fake, grad_a, grad_b, read_mask, &any) == ZR_OK)
+      S->ws_query = std::max(S->ws_query, any.ws_a_bytes + any.ws_b_bytes);
+  }
   return ZR_OK;
 }
 
@@ -377,6 +395,12 @@ int cuda_status(cudaError_t e) { return e == cudaSuccess ? ZR_OK : ZR_ERR_CUDA; 
 // Launch (or, with dry, only guard-check) the kernels of a backward plan.
 int launch_bwd_set(const BwdSet& S, int op, void* workspace, cudaStream_t st, bool dry) {
   if (S.direct) return cuda_status(launch_bwd_direct(op, S.want, S.eb, st, dry));
+  if (S.sab) {
+    SabBuild sb = S.sb;
+    sb.plan.ws_a = static_cast<float*>(workspace);
+    sb.plan.ws_b = reinterpret_cast<float*>(static_cast<char*>(workspace) + sb.ws_a_bytes);
+    return cuda_status(launch_sab(op, sb, st, dry));
+  }
   for (int i = 0; i < S.nred; ++i) {
     RedBuild rbi = S.rb[i];
     rbi.plan.partial = reinterpret_cast<float*>(static_cast<char*>(workspace) + S.ws_off[i]);
@@ -662,6 +686,12 @@ int zr_test_describe_bwd(zr_op op, zr_tensor grad_out, zr_tensor a, zr_tensor b,
   } else if (S.direct) {
     s = "{\"plans\":[" + describe_ew(S.eb) + "],\"ws_run\":0,\"ws_query\":" +
         std::to_string(S.ws_query) + "}";
+  } else if (S.sab) {
+    const std::string d = describe_sab(S.sb);
+    s = "{\"plans\":[" + d.substr(0, d.size() - 1) + ",\"nslots\":" +
+        std::to_string(S.sb.plan.slots_a) + "}," + d.substr(0, d.size() - 1) + ",\"nslots\":" +
+        std::to_string(S.sb.plan.n_tiles) + "}],\"which\":[0,1],\"ws_run\":" +
+        std::to_string(S.ws_run) + ",\"ws_query\":" + std::to_string(S.ws_query) + "}";
   } else {
     s = "{\"plans\":[";
     for (int i = 0; i < S.nred; ++i) {
@@ -745,6 +775,55 @@ void walk_red(const RedBuild& rb, Rec rec) {
   }
 }
 
+// Host walk of k_sab's (CTA, step, row, column) space.  rec(o, x_a, slot_a,
+// x_b, slot_b).  Also replays the grad_a flushes and zero fills and returns
+// false unless every (slot, tile) pair is written exactly once.
+template <class Rec>
+bool walk_sab(const SabBuild& sb, Rec rec) {
+  const SabPlan& p = sb.plan;
+  std::vector<int> writes(size_t(p.n_tiles) * p.slots_a, 0);
+  std::vector<int64_t> row_g(p.ta), row_a(p.ta), beta_g(p.n_beta), beta_b(p.n_beta);
+  for (uint32_t i = 0; i < p.ta; ++i) {
+    int64_t off[kMaxOperands];
+    decomp_offsets(p.a_inner, i, off);
+    row_g[i] = off[0];
+    row_a[i] = off[1];
+  }
+  for (uint32_t i = 0; i < p.n_beta; ++i) {
+    int64_t off[kMaxOperands];
+    decomp_offsets(p.beta, i, off);
+    beta_g[i] = off[0];
+    beta_b[i] = off[2];
+  }
+  for (uint32_t c = 0; c < p.grid; ++c) {
+    const uint64_t s0 = sab_start(p, c), s1 = sab_start(p, c + 1);
+    for (uint64_t step = s0; step < s1; ++step) {
+      const uint32_t tile = fd_div(p.n_beta_div, uint32_t(step));
+      const uint32_t beta = uint32_t(step) - tile * p.n_beta;
+      int64_t ob[kMaxOperands];
+      decomp_offsets(p.a_outer, tile, ob);
+      const uint32_t slot = c - sab_owner(p, uint64_t(tile) * p.n_beta);
+      for (uint32_t r = 0; r < p.ta; ++r) {
+        for (uint32_t col = 0; col < p.ncol; ++col) {
+          int64_t o[kMaxOperands] = {ob[0] + row_g[r] + beta_g[beta] + col,
+                                     ob[1] + row_a[r] + col, beta_b[beta] + col, -1};
+          rec(o, (int64_t(tile) * p.ta + r) * p.ncol + col, int64_t(slot),
+              int64_t(beta) * p.ncol + col, int64_t(tile));
+        }
+      }
+      if (beta == p.n_beta - 1 || step == s1 - 1) {
+        if (slot >= p.slots_a) return false;
+        writes[size_t(tile) * p.slots_a + slot]++;
+        if (beta == p.n_beta - 1)
+          for (uint32_t s = slot + 1; s < p.slots_a; ++s) writes[size_t(tile) * p.slots_a + s]++;
+      }
+    }
+  }
+  for (int w : writes)
+    if (w != 1) return false;
+  return true;
+}
+
 }  // namespace
 }  // namespace zr
 
@@ -795,7 +874,15 @@ int zr_test_emulate_bwd(zr_op op, zr_tensor grad_out, zr_tensor a, zr_tensor b,
     ++m;
   };
   if (!S.nothing && !S.empty) {
-    if (S.direct) {
+    if (S.sab) {
+      const uint32_t rm = 1u | (S.sb.plan.a ? 2u : 0u) | (S.sb.plan.b ? 4u : 0u);
+      const bool ok = walk_sab(S.sb, [&](const int64_t* o, int64_t xa, int64_t sa, int64_t xb,
+                                         int64_t sbs) {
+        put(0, o, rm, xa, sa, false);
+        put(1, o, rm, xb, sbs, false);
+      });
+      if (!ok) return ZR_ERR_CUDA;
+    } else if (S.direct) {
       const uint32_t rm = 1u | (S.eb.plan.in[1] && ((S.want & 2) && needs_a(op, 1)) ? 2u : 0u) |
                           (S.eb.plan.in[2] && (((S.want & 1) && needs_b(op, 0)) ||
                                                ((S.want & 2) && needs_b(op, 1))) ? 4u : 0u);

@@ -179,6 +179,50 @@ ZR_HD RedCta red_cta(const RedPlan& p, uint32_t cta) {
   return c;
 }
 
+// ---------------------------------------------------------------------------
+// Fused backward when BOTH gradients are reduced and the innermost dim is
+// kept by both (every other dim is kept by exactly one input).  Writing
+// A = the dims only a keeps and B = the dims only b keeps, grad_out is a
+// family of matrices g[alpha, beta, col]: grad_a = sum over beta, grad_b =
+// sum over alpha.  alpha = (A-outer tile, A-inner row), beta = all B dims.
+// A persistent grid of `grid` CTAs splits the step sequence
+// (tile, beta), tile-major, into equal contiguous ranges; each step streams
+// one tile of ta rows x ncol columns through a shared-memory pipeline.
+// grad_a partials are flushed when a CTA leaves a tile (slot = the CTA's
+// position among the CTAs covering that tile); grad_b partials are written
+// per step (slot = tile).  A second pass adds the slots in order.
+struct SabPlan {
+  const float* g;
+  const float* a;
+  const float* b;
+  float* ws_a;              // [slots_a][n_a]
+  float* ws_b;              // [n_tiles][n_b]
+  Decomp a_outer;           // tile -> offsets (slot 0: g, slot 1: a)
+  Decomp a_inner;           // row  -> offsets (slot 0: g, slot 1: a)
+  Decomp beta;              // beta -> offsets (slot 0: g, slot 2: b)
+  uint32_t ncol, nvc;       // inner dim, its float4 count (power of two <= 32)
+  uint32_t ta;              // rows per tile
+  uint32_t n_tiles, n_beta;
+  FastDiv n_beta_div;
+  uint64_t total_steps;     // n_tiles * n_beta
+  uint32_t grid;            // CTAs (persistent)
+  uint32_t slots_a;         // grad_a partial slots (max CTAs covering a tile)
+  uint64_t n_a, n_b;        // elements of grad_a / grad_b
+  uint32_t smem_bytes;
+};
+
+constexpr int kSabStages = 4;
+constexpr uint32_t kSabGrid = 152;  // one CTA per SM of a GB300; fixed so that
+                                    // the partition depends on the shape only
+
+// First step of CTA c, and the CTA that owns a step.
+ZR_HD uint64_t sab_start(const SabPlan& p, uint32_t c) {
+  return (uint64_t(c) * p.total_steps) / p.grid;
+}
+ZR_HD uint32_t sab_owner(const SabPlan& p, uint64_t step) {
+  return static_cast<uint32_t>(((step + 1) * p.grid - 1) / p.total_steps);
+}
+
 // Second pass: out[j] = sum over s of partial[s * nout + j], s in order.
 struct CombinePlan {
   const float* partial;

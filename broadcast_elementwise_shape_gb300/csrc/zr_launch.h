@@ -18,4 +18,8 @@ cudaError_t launch_copy(const EwBuild& eb, cudaStream_t s, bool dry = false);
 // pass and, when it writes partials, the combine pass.
 cudaError_t launch_reduce(int op, int which, const RedBuild& rb, cudaStream_t s, bool dry = false);
 
+// Fused backward with both gradients reduced: the k_sab pass, then one
+// combine pass per gradient.  sb.plan.ws_a / ws_b must be set.
+cudaError_t launch_sab(int op, const SabBuild& sb, cudaStream_t s, bool dry = false);
+
 }  // namespace zr

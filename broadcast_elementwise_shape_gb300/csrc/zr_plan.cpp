@@ -417,3 +417,179 @@ std::string describe_red(const RedBuild& rb) {
 }
 
 }  // namespace zr
+
+namespace zr {
+
+namespace {
+
+// Fill a decomposition from an explicit dim list (outer to inner), each with
+// a size and up to three operand strides.
+struct DimSpec {
+  uint64_t size;
+  int64_t st[3];  // operand slots 0..2
+};
+void fill_from_specs(Decomp* dc, const DimSpec* dims, int nd) {
+  dc->n = nd;
+  for (int i = 0; i < kMaxDims; ++i) {
+    dc->div[i] = make_fastdiv(1);
+    for (int k = 0; k < kMaxOperands; ++k) dc->stride[k][i] = 0;
+  }
+  for (int i = 0; i < nd; ++i) {
+    const DimSpec& d = dims[nd - 1 - i];
+    dc->div[i] = make_fastdiv(static_cast<uint32_t>(d.size));
+    for (int k = 0; k < 3; ++k) dc->stride[k][i] = d.st[k];
+  }
+}
+
+}  // namespace
+
+int build_sab(const Prob& P, const float* g, const float* a, const float* b, float* grad_a,
+              float* grad_b, uint32_t read_mask, SabBuild* sb) {
+  const int n = P.n;
+  if (n < 2 || !grad_a || !grad_b) return 1;
+  const int I = n - 1;
+  // Inner dim kept by both, unit stride for every operand read.
+  if (P.st[kSlotXA][I] == 0 || P.st[kSlotXB][I] == 0) return 1;
+  for (int k = 0; k < 3; ++k)
+    if ((read_mask & (1u << k)) && P.st[k][I] != 1) return 1;
+  const uint64_t ncol = uint64_t(P.size[I]);
+  if (ncol % 4 != 0) return 1;
+  const uint64_t nvc = ncol / 4;
+  if (nvc > 32 || (nvc & (nvc - 1)) != 0) return 1;
+  const void* ptrs[3] = {g, a, b};
+  for (int k = 0; k < 3; ++k) {
+    if (!(read_mask & (1u << k))) continue;
+    if (reinterpret_cast<uintptr_t>(ptrs[k]) % 16 != 0) return 1;
+    for (int d = 0; d < I; ++d)
+      if (P.st[k][d] % 4 != 0) return 1;
+  }
+  // Every outer dim is kept by exactly one input.
+  int adims[kMaxDims], bdims[kMaxDims];
+  int na = 0, nb = 0;
+  uint64_t n_alpha = 1, n_beta = 1;
+  for (int d = 0; d < I; ++d) {
+    const bool ka = P.st[kSlotXA][d] != 0, kb = P.st[kSlotXB][d] != 0;
+    if (ka == kb) return 1;
+    if (ka) { adims[na++] = d; n_alpha *= uint64_t(P.size[d]); }
+    else { bdims[nb++] = d; n_beta *= uint64_t(P.size[d]); }
+  }
+  if (na == 0 || nb == 0 || n_beta > 4096) return 1;
+  // Rows per tile: from the innermost A dims outwards, at most 2048/nvc rows,
+  // splitting one dim by its largest fitting divisor.
+  const uint64_t ta_max = 2048 / nvc;
+  DimSpec inner[kMaxDims + 1], outer[kMaxDims + 1];
+  int n_in = 0, n_out = 0;
+  uint64_t ta = 1;
+  int i = na - 1;
+  for (; i >= 0; --i) {
+    const int d = adims[i];
+    const uint64_t s = uint64_t(P.size[d]);
+    if (ta * s <= ta_max) {
+      inner[n_in++] = {s, {P.st[0][d], P.st[1][d], P.st[2][d]}};
+      ta *= s;
+      continue;
+    }
+    uint64_t f = ta_max / ta;
+    while (f > 1 && s % f != 0) --f;
+    if (f > 1) {
+      inner[n_in++] = {f, {P.st[0][d], P.st[1][d], P.st[2][d]}};
+      outer[n_out++] = {s / f, {P.st[0][d] * int64_t(f), P.st[1][d] * int64_t(f),
+                                P.st[2][d] * int64_t(f)}};
+      ta *= f;
+    } else {
+      outer[n_out++] = {s, {P.st[0][d], P.st[1][d], P.st[2][d]}};
+    }
+    --i;
+    break;
+  }
+  for (; i >= 0; --i) {
+    const int d = adims[i];
+    outer[n_out++] = {uint64_t(P.size[d]), {P.st[0][d], P.st[1][d], P.st[2][d]}};
+  }
+  const uint64_t rows_x_vec = ta * nvc;
+  if (rows_x_vec < 256 || rows_x_vec > 2048 || (rows_x_vec & (rows_x_vec - 1)) != 0) return 1;
+  if (n_in > kMaxDims || n_out > kMaxDims) return 1;
+  // inner[] / outer[] were collected inner-to-outer; reverse into row-major.
+  std::reverse(inner, inner + n_in);
+  std::reverse(outer, outer + n_out);
+  DimSpec beta[kMaxDims];
+  for (int j = 0; j < nb; ++j) {
+    const int d = bdims[j];
+    beta[j] = {uint64_t(P.size[d]), {P.st[0][d], P.st[1][d], P.st[2][d]}};
+  }
+  const uint64_t n_tiles = n_alpha / ta;
+  // Steps are indexed in 32 bits; the slot count is found by a walk over tiles.
+  if (n_tiles > (uint64_t(1) << 22) || n_tiles * n_beta >= (uint64_t(1) << 32)) return 1;
+
+  SabPlan& p = sb->plan;
+  p = SabPlan{};
+  p.g = g;
+  p.a = (read_mask & 2) ? a : nullptr;
+  p.b = (read_mask & 4) ? b : nullptr;
+  fill_from_specs(&p.a_outer, outer, n_out);
+  fill_from_specs(&p.a_inner, inner, n_in);
+  fill_from_specs(&p.beta, beta, nb);
+  p.ncol = uint32_t(ncol);
+  p.nvc = uint32_t(nvc);
+  p.ta = uint32_t(ta);
+  p.n_tiles = uint32_t(n_tiles);
+  p.n_beta = uint32_t(n_beta);
+  p.n_beta_div = make_fastdiv(p.n_beta);
+  p.total_steps = n_tiles * n_beta;
+  p.grid = uint32_t(std::min<uint64_t>(kSabGrid, p.total_steps));
+  p.n_a = n_alpha * ncol;
+  p.n_b = n_beta * ncol;
+  uint32_t smax = 1;
+  for (uint64_t t = 0; t < n_tiles; ++t) {
+    const uint32_t c0 = sab_owner(p, t * n_beta);
+    const uint32_t c1 = sab_owner(p, t * n_beta + n_beta - 1);
+    smax = std::max(smax, c1 - c0 + 1);
+  }
+  p.slots_a = smax;
+  const uint64_t smem = uint64_t(kSabStages) * ta * ncol * 4 + 2 * ta * 8 + 2 * n_beta * 8 +
+                        2 * 8 * ncol * 4;
+  if (smem > 220 * 1024) return 1;
+  p.smem_bytes = uint32_t(smem);
+  sb->rpt = int(rows_x_vec / 256);
+  sb->ws_a_bytes = ((uint64_t(p.slots_a) * p.n_a * 4 + 255) / 256) * 256;
+  sb->ws_b_bytes = ((uint64_t(p.n_tiles) * p.n_b * 4 + 255) / 256) * 256;
+  CombinePlan* cs[2] = {&sb->comb_a, &sb->comb_b};
+  const uint64_t nouts[2] = {p.n_a, p.n_b};
+  const uint32_t nsl[2] = {p.slots_a, p.n_tiles};
+  float* outs[2] = {grad_a, grad_b};
+  for (int w = 0; w < 2; ++w) {
+    CombinePlan& c = *cs[w];
+    c = CombinePlan{};
+    c.nout = nouts[w];
+    c.nslots = nsl[w];
+    c.out = outs[w];
+    c.scale = 1.0f;
+    uint32_t sy = std::min<uint32_t>(kThreads, pow2_ceil(c.nslots));
+    if (c.nout >= 64 * 1024) sy = std::min<uint32_t>(sy, 4);
+    else if (c.nout >= 4096) sy = std::min<uint32_t>(sy, 32);
+    uint32_t jx = kThreads / sy;
+    if (c.nout < jx) {
+      jx = pow2_ceil(c.nout);
+      sy = kThreads / jx;
+    }
+    c.jx = jx;
+    c.sy = std::min<uint32_t>(sy, pow2_ceil(c.nslots));
+  }
+  return ZR_OK;
+}
+
+std::string describe_sab(const SabBuild& sb) {
+  const SabPlan& p = sb.plan;
+  char buf[1024];
+  std::snprintf(buf, sizeof(buf),
+                "{\"kernel\":\"sab\",\"ncol\":%u,\"ta\":%u,\"rpt\":%d,\"n_tiles\":%u,"
+                "\"n_beta\":%u,\"grid\":%u,\"slots_a\":%u,\"slots_b\":%u,\"n_a\":%llu,"
+                "\"n_b\":%llu,\"ws_bytes\":%zu,\"smem\":%u,\"outer_dims\":%d,\"inner_dims\":%d,"
+                "\"beta_dims\":%d}",
+                p.ncol, p.ta, sb.rpt, p.n_tiles, p.n_beta, p.grid, p.slots_a, p.n_tiles,
+                (unsigned long long)p.n_a, (unsigned long long)p.n_b,
+                sb.ws_a_bytes + sb.ws_b_bytes, p.smem_bytes, p.a_outer.n, p.a_inner.n, p.beta.n);
+  return buf;
+}
+
+}  // namespace zr

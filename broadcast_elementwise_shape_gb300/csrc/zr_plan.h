@@ -77,7 +77,20 @@ int build_red(const Prob& P, int xslot, const float* g, const float* a, const fl
               uint32_t read_mask, uint32_t stream_mask, float* x_out, float* d_out,
               int vec_override, RedBuild* rb);
 
+struct SabBuild {
+  SabPlan plan;
+  CombinePlan comb_a, comb_b;
+  int rpt;                  // rows per thread (ta * nvc / 256)
+  size_t ws_a_bytes, ws_b_bytes;
+};
+// Fused both-reduced plan; returns ZR_OK when the shape qualifies, 1 when it
+// does not (the caller then runs one reduction pass per gradient), or an
+// error code.
+int build_sab(const Prob& P, const float* g, const float* a, const float* b, float* grad_a,
+              float* grad_b, uint32_t read_mask, SabBuild* sb);
+
 std::string describe_ew(const EwBuild& eb);
+std::string describe_sab(const SabBuild& sb);
 std::string describe_red(const RedBuild& rb);
 
 }  // namespace zr

@@ -249,11 +249,11 @@ def test_emulated_backward_matches_naive(L, op):
                 np.testing.assert_array_equal(rows[:, 2], ao[ref])
             if rows[0, 3] != -1:
                 np.testing.assert_array_equal(rows[:, 3], bo[ref])
-            if plan["kernel"] == "reduce":
+            if plan["kernel"] in ("reduce", "sab"):
                 which = desc["which"][pi]
                 np.testing.assert_array_equal(rows[:, 4], (xa if which == 0 else xb)[ref])
                 assert rows[:, 5].min() >= 0 and rows[:, 5].max() < plan["nslots"]
-                if plan["dense_out"]:
+                if plan.get("dense_out"):
                     np.testing.assert_array_equal(rows[:, 6], dense[ref])
             else:
                 np.testing.assert_array_equal(rows[:, 6], dense[ref])
@@ -377,3 +377,52 @@ def test_every_plan_provides_what_its_kernels_read(L, op):
         a, b = FakeT(2 * T, sa), FakeT(3 * T, sb)
         assert L.zr_test_dry_run_fwd(op, a.desc, b.desc, 4 * T, None) == 0
         assert L.zr_test_dry_run_sum(g.desc, len(sb), _i64(sb), 6 * T) in (0, -3)
+
+
+SAB_CASES = [
+    ((2, 1, 256, 4), (1, 3, 1, 4)),            # one tile, three steps
+    ((8, 1, 64, 1, 32), (1, 5, 1, 7, 32)),     # split A dim, 2 tiles, many CTAs per tile
+    ((3, 1, 16, 1, 8, 1, 64), (1, 4, 1, 5, 1, 3, 64)),
+]
+
+
+@pytest.mark.parametrize("op", [0, 1, 2, 3])
+def test_emulated_sab_backward(L, op):
+    """Shapes where both gradients are reduced take the fused pass; its host
+    walk must visit every grad_out element once with naive offsets and
+    gradient indices, and fill every grad_a partial slot exactly once."""
+    T = 1 << 40
+    for sa, sb in SAB_CASES:
+        out_shape = tuple(np.broadcast_shapes(sa, sb))
+        n_out = int(np.prod(out_shape))
+        g, a, b = FakeT(T, out_shape), FakeT(2 * T, sa), FakeT(3 * T, sb)
+        buf = ctypes.create_string_buffer(8192)
+        assert L.zr_test_describe_bwd(op, g.desc, a.desc, b.desc, 4 * T, 5 * T, buf, 8192) == 0
+        desc = json.loads(buf.value.decode())
+        assert [p["kernel"] for p in desc["plans"]] == ["sab", "sab"], desc
+        cap = 2 * n_out + 8
+        rec = (ctypes.c_int64 * (7 * cap))()
+        nrec = ctypes.c_int64()
+        assert L.zr_test_emulate_bwd(op, g.desc, a.desc, b.desc, 4 * T, 5 * T, cap, rec,
+                                     ctypes.byref(nrec)) == 0
+        r = np.frombuffer(rec, np.int64)[: 7 * nrec.value].reshape(-1, 7)
+        go = naive_offsets(out_shape, out_shape, g.strides).ravel()
+        ao = naive_offsets(out_shape, sa, a.strides).ravel()
+        bo = naive_offsets(out_shape, sb, b.strides).ravel()
+        xs = (grad_index(out_shape, sa).ravel(), grad_index(out_shape, sb).ravel())
+        ref = np.argsort(go)
+        for pi in (0, 1):
+            rows = r[r[:, 0] == pi]
+            assert rows.shape[0] == n_out
+            rows = rows[np.argsort(rows[:, 1])]
+            np.testing.assert_array_equal(rows[:, 1], go[ref])
+            np.testing.assert_array_equal(rows[:, 4], xs[pi][ref])
+            if op >= 2:
+                np.testing.assert_array_equal(rows[:, 2], ao[ref])
+                np.testing.assert_array_equal(rows[:, 3], bo[ref])
+            assert rows[:, 5].min() >= 0 and rows[:, 5].max() < desc["plans"][pi]["nslots"]
+        L2 = _dry_lib(L)
+        need_ab = op >= 2
+        a2 = FakeT(2 * T if need_ab else None, sa)
+        b2 = FakeT(3 * T if need_ab else None, sb)
+        assert L2.zr_test_dry_run_bwd(op, g.desc, a2.desc, b2.desc, 4 * T, 5 * T) == 0
