@@ -118,6 +118,8 @@ int check_device_ptr(const void* p) {
 struct FwdSet {
   int op = 0;
   bool empty = false;
+  bool tr = false;               // transposed-input tile path
+  TrPlan tp;
   EwBuild eb;
   TDesc a, b, out;
 };
@@ -158,6 +160,11 @@ int plan_fwd(int op, const zr_tensor& ta, const zr_tensor& tb, const float* out,
   float* outs[2] = {const_cast<float*>(out), nullptr};
   const uint32_t stream_mask = (S->a.numel == S->out.numel ? 1u : 0u) |
                                (S->b.numel == S->out.numel ? 2u : 0u);
+  rc = build_tr(P, S->a.ptr, S->b.ptr, const_cast<float*>(out), &S->tp);
+  if (rc == ZR_OK) {
+    S->tr = true;
+    return ZR_OK;
+  }
   return build_ew(P, in, outs, 0x3u, stream_mask, &S->eb);
 }
 
@@ -459,6 +466,7 @@ int zr_binary_fwd(zr_op op, zr_tensor a, zr_tensor b, float* out, const int64_t*
     rc = check_device_ptr(p);
     if (rc) return rc;
   }
+  if (S.tr) return cuda_status(launch_fwd_tr(op, S.tp, reinterpret_cast<cudaStream_t>(stream)));
   return cuda_status(launch_fwd(op, S.eb, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -645,6 +653,7 @@ int zr_test_dry_run_fwd(zr_op op, zr_tensor a, zr_tensor b, const float* out,
   FwdSet S;
   const int rc = plan_fwd(op, a, b, out, out_strides, &S);
   if (rc || S.empty) return rc;
+  if (S.tr) return cuda_status(launch_fwd_tr(op, S.tp, nullptr, true));
   return cuda_status(launch_fwd(op, S.eb, nullptr, true));
 }
 
@@ -671,7 +680,8 @@ int zr_test_describe_fwd(zr_op op, zr_tensor a, zr_tensor b, const float* out,
   FwdSet S;
   const int rc = plan_fwd(op, a, b, out, out_strides, &S);
   if (rc) return rc;
-  return copy_json(S.empty ? std::string("{\"kernel\":\"none\"}") : describe_ew(S.eb), buf, len);
+  return copy_json(S.empty ? std::string("{\"kernel\":\"none\"}")
+                           : (S.tr ? describe_tr(S.tp) : describe_ew(S.eb)), buf, len);
 }
 
 int zr_test_describe_bwd(zr_op op, zr_tensor grad_out, zr_tensor a, zr_tensor b,
@@ -726,19 +736,49 @@ namespace {
 template <class Rec>
 void walk_ew(const EwBuild& eb, Rec rec) {
   const EwPlan& p = eb.plan;
+  const uint32_t ty_n = kThreads >> p.tx_shift;
   for (uint32_t cta = 0; cta < p.n_cta; ++cta) {
     const EwTile t = ew_tile(p, cta);
-    for (uint32_t item = 0; item < p.items_per_cta; ++item) {
-      const uint32_t ri = fd_div(p.tile_vcols_div, item);
-      const uint32_t vc = item - ri * p.tile_vcols;
-      if (!(ri < t.nrows && vc < t.nvcols)) continue;
-      int64_t off[kMaxOperands];
-      decomp_offsets(p.rows, t.row0 + ri, off);
-      for (int i = 0; i < eb.vec; ++i) {
-        const int64_t c = int64_t(t.vcol0 + vc) * eb.vec + i;
-        if (c >= p.ncol) continue;
-        int64_t o[kMaxOperands];
-        for (int k = 0; k < kMaxOperands; ++k) o[k] = off[k] + c * p.inner_stride[k];
+    for (uint32_t thr = 0; thr < uint32_t(kThreads); ++thr) {
+      const uint32_t tx = thr & (p.tx - 1), ty = thr >> p.tx_shift;
+      const uint32_t ncs = t.nvcols > tx ? (t.nvcols - tx + p.tx - 1) >> p.tx_shift : 0;
+      const uint32_t nrs = t.nrows > ty ? (t.nrows - ty + ty_n - 1) / ty_n : 0;
+      uint32_t rm = 0, cm = 0;
+      for (uint32_t m = 0; m < ncs * nrs; ++m) {
+        const uint32_t row = ty + rm * ty_n;
+        const uint32_t vc = tx + cm * p.tx;
+        if (++cm == ncs) { cm = 0; ++rm; }
+        int64_t off[kMaxOperands];
+        decomp_offsets(p.rows, t.row0 + row, off);
+        for (int i = 0; i < eb.vec; ++i) {
+          const int64_t c = int64_t(t.vcol0 + vc) * eb.vec + i;
+          if (c >= p.ncol) continue;
+          int64_t o[kMaxOperands];
+          for (int k = 0; k < kMaxOperands; ++k) o[k] = off[k] + c * p.inner_stride[k];
+          rec(o);
+        }
+      }
+    }
+  }
+}
+
+// Host walk of k_transpose's (CTA, p, q) space; o[0] = x, o[1] = y, o[3] = out.
+template <class Rec>
+void walk_tr(const TrPlan& p, Rec rec) {
+  for (uint32_t cta = 0; cta < p.n_cta; ++cta) {
+    const uint32_t t1 = fd_div(p.n_qt_div, cta);
+    const uint32_t qt = cta - t1 * p.n_qt;
+    const uint32_t bidx = fd_div(p.n_pt_div, t1);
+    const uint32_t pt = t1 - bidx * p.n_pt;
+    int64_t base[kMaxOperands];
+    decomp_offsets(p.batch, bidx, base);
+    for (uint32_t i = 0; i < kTrTile; ++i) {
+      for (uint32_t l = 0; l < kTrTile; ++l) {
+        const uint32_t pp = pt * kTrTile + i, q = qt * kTrTile + l;
+        if (q >= p.nq || pp >= p.np) continue;
+        int64_t o[kMaxOperands] = {base[0] + pp + int64_t(q) * p.xs_q,
+                                   base[1] + int64_t(pp) * p.ys_p + int64_t(q) * p.ys_q, 0,
+                                   base[kSlotOut] + int64_t(pp) * p.os_p + q};
         rec(o);
       }
     }
@@ -837,7 +877,15 @@ int zr_test_emulate_fwd(zr_tensor a, zr_tensor b, const float* out, const int64_
   if (rc) return rc;
   int64_t m = 0;
   bool over = false;
-  if (!S.empty) {
+  if (!S.empty && S.tr) {
+    walk_tr(S.tp, [&](const int64_t* o) {
+      if (m >= cap) { over = true; return; }
+      rec[3 * m + 0] = o[kSlotOut];
+      rec[3 * m + 1] = S.tp.x_is_a ? o[0] : o[1];
+      rec[3 * m + 2] = S.tp.x_is_a ? o[1] : o[0];
+      ++m;
+    });
+  } else if (!S.empty) {
     walk_ew(S.eb, [&](const int64_t* o) {
       if (m >= cap) { over = true; return; }
       rec[3 * m + 0] = o[kSlotOut];

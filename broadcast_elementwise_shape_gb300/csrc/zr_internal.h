@@ -107,7 +107,28 @@ struct EwPlan {
   FastDiv tile_vcols_div;   // item -> (row in tile, column vector)
   uint32_t items_per_cta;   // tile_rows * tile_vcols
   uint32_t n_cta;
+  uint32_t tx, tx_shift;    // column lanes per CTA (power of two) and log2
 };
+
+// Forward with one input read transposed: that input (X) walks the output's
+// innermost dim q with a large stride but has unit stride along another dim
+// p.  A CTA moves a 32 x 32 (p, q) tile of X through shared memory so that
+// X is read along p and the output written along q, both coalesced.
+struct TrPlan {
+  const float* x;           // the transposed input
+  const float* y;           // the other input
+  float* out;
+  uint32_t x_is_a;          // 1: out = x op y; 0: out = y op x
+  Decomp batch;             // all dims but p and q; slots 0: x, 1: y, 3: out
+  int64_t xs_q;             // x stride along q (x stride along p is 1)
+  int64_t ys_p, ys_q;       // y strides
+  int64_t os_p;             // out stride along p (out stride along q is 1)
+  uint32_t np, nq;          // sizes of p and q
+  uint32_t n_pt, n_qt;      // tiles along p and q
+  FastDiv n_qt_div, n_pt_div;
+  uint32_t n_cta;
+};
+constexpr uint32_t kTrTile = 32;
 
 constexpr uint32_t kMaxTileRows = 512;
 constexpr int kThreads = 256;
@@ -211,7 +232,8 @@ struct SabPlan {
   uint32_t smem_bytes;
 };
 
-constexpr int kSabStages = 4;
+constexpr int kSabStages = 5;
+constexpr int kSabThreads = 512;
 constexpr uint32_t kSabGrid = 152;  // one CTA per SM of a GB300; fixed so that
                                     // the partition depends on the shape only
 

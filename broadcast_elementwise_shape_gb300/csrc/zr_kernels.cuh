@@ -153,9 +153,12 @@ struct CopyF {
 
 // ---------------------------------------------------------------- elementwise
 
-// One CTA = one tile of rows x column vectors.  Each thread takes items
-// threadIdx.x + k * 256; items are processed in batches of U so that U
-// independent loads per operand are in flight before any result is stored.
+// One CTA = one tile of rows x column vectors.  Thread (tx, ty) owns column
+// vectors vcol0 + tx, + tx_n, ... and rows ty, ty + ty_n, ... of the tile and
+// walks them columns-fastest with counters; a row's operand offsets are
+// read from the shared table only when the row changes.  Items are loaded U
+// at a time so that U independent loads per operand are in flight before
+// any result is stored.
 template <class F, int VEC, int NOUT>
 __global__ void __launch_bounds__(kThreads)
 k_elementwise(const __grid_constant__ EwPlan p) {
@@ -169,27 +172,45 @@ k_elementwise(const __grid_constant__ EwPlan p) {
   }
   __syncthreads();
 
+  const uint32_t tx = threadIdx.x & (p.tx - 1);
+  const uint32_t ty = threadIdx.x >> p.tx_shift;
+  const uint32_t ty_n = kThreads >> p.tx_shift;
+  const uint32_t ncs = t.nvcols > tx ? (t.nvcols - tx + p.tx - 1) >> p.tx_shift : 0;
+  const uint32_t nrs = t.nrows > ty ? (t.nrows - ty + ty_n - 1) / ty_n : 0;
+  const uint32_t items = ncs * nrs;
+  const int64_t in0 = p.inner_stride[0], in1 = p.inner_stride[1], in2 = p.inner_stride[2];
+  const int64_t ino = p.inner_stride[kSlotOut];
+
   constexpr int U = 4;
   const F f;
-  for (uint32_t it0 = 0; it0 < p.items_per_cta; it0 += U * blockDim.x) {
+  uint32_t rm = 0, cm = 0;
+  uint32_t row = ty;
+  int64_t ro[kMaxOperands];
+#pragma unroll
+  for (int k = 0; k < kMaxOperands; ++k) ro[k] = row < t.nrows ? s_off[row * kMaxOperands + k] : 0;
+  for (uint32_t m0 = 0; m0 < items; m0 += U) {
     Vec<VEC> x[U][3];
     int64_t doff[U];
     uint32_t col[U];
     bool ok[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      const uint32_t item = it0 + u * blockDim.x + threadIdx.x;
-      const uint32_t ri = fd_div(p.tile_vcols_div, item);
-      const uint32_t vc = item - ri * p.tile_vcols;
-      ok[u] = ri < t.nrows && vc < t.nvcols;
-      col[u] = (t.vcol0 + vc) * VEC;
-      doff[u] = 0;
+      ok[u] = m0 + u < items;
+      col[u] = (t.vcol0 + tx + cm * p.tx) * VEC;
+      doff[u] = ro[kSlotOut];
       if (ok[u]) {
-        const int64_t* ro = s_off + ri * kMaxOperands;
-        x[u][0] = load_cols<VEC>(p.in[0], ro[0], p.inner_stride[0], col[u], p.stream_mask & 1);
-        if (F::kR1) x[u][1] = load_cols<VEC>(p.in[1], ro[1], p.inner_stride[1], col[u], p.stream_mask & 2);
-        if (F::kR2) x[u][2] = load_cols<VEC>(p.in[2], ro[2], p.inner_stride[2], col[u], p.stream_mask & 4);
-        doff[u] = ro[kSlotOut];
+        x[u][0] = load_cols<VEC>(p.in[0], ro[0], in0, col[u], p.stream_mask & 1);
+        if (F::kR1) x[u][1] = load_cols<VEC>(p.in[1], ro[1], in1, col[u], p.stream_mask & 2);
+        if (F::kR2) x[u][2] = load_cols<VEC>(p.in[2], ro[2], in2, col[u], p.stream_mask & 4);
+        if (++cm == ncs) {
+          cm = 0;
+          ++rm;
+          row += ty_n;
+          if (row < t.nrows) {
+#pragma unroll
+            for (int k = 0; k < kMaxOperands; ++k) ro[k] = s_off[row * kMaxOperands + k];
+          }
+        }
       }
     }
 #pragma unroll
@@ -197,8 +218,38 @@ k_elementwise(const __grid_constant__ EwPlan p) {
       if (!ok[u]) continue;
       Vec<VEC> y[2];
       f(x[u], y);
-      if (p.out[0]) store_cols<VEC>(p.out[0], doff[u], p.inner_stride[kSlotOut], col[u], y[0]);
-      if (NOUT > 1 && p.out[1]) store_cols<VEC>(p.out[1], doff[u], p.inner_stride[kSlotOut], col[u], y[1]);
+      if (p.out[0]) store_cols<VEC>(p.out[0], doff[u], ino, col[u], y[0]);
+      if (NOUT > 1 && p.out[1]) store_cols<VEC>(p.out[1], doff[u], ino, col[u], y[1]);
+    }
+  }
+}
+
+// Forward with a transposed input (TrPlan): X's tile is read along its
+// unit-stride dim p into shared memory (one 128-byte row per warp access),
+// then read back along q to write the output along its unit-stride dim.
+template <int OP>
+__global__ void __launch_bounds__(kThreads)
+k_transpose(const __grid_constant__ TrPlan p) {
+  __shared__ float tile[kTrTile][kTrTile + 1];  // [q][p], padded: no bank conflicts
+  const uint32_t t1 = fd_div(p.n_qt_div, blockIdx.x);
+  const uint32_t qt = blockIdx.x - t1 * p.n_qt;
+  const uint32_t bidx = fd_div(p.n_pt_div, t1);
+  const uint32_t pt = t1 - bidx * p.n_pt;
+  int64_t base[kMaxOperands];
+  decomp_offsets(p.batch, bidx, base);
+  const uint32_t lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const uint32_t p0 = pt * kTrTile, q0 = qt * kTrTile;
+  for (uint32_t j = w; j < kTrTile; j += kThreads / 32) {
+    const uint32_t q = q0 + j, pp = p0 + lane;
+    if (q < p.nq && pp < p.np) tile[j][lane] = __ldcs(p.x + base[0] + pp + int64_t(q) * p.xs_q);
+  }
+  __syncthreads();
+  for (uint32_t i = w; i < kTrTile; i += kThreads / 32) {
+    const uint32_t pp = p0 + i, q = q0 + lane;
+    if (q < p.nq && pp < p.np) {
+      const float xv = tile[lane][i];
+      const float yv = __ldg(p.y + base[1] + int64_t(pp) * p.ys_p + int64_t(q) * p.ys_q);
+      p.out[base[kSlotOut] + int64_t(pp) * p.os_p + q] = p.x_is_a ? fwd_op<OP>(xv, yv) : fwd_op<OP>(yv, xv);
     }
   }
 }
@@ -210,24 +261,41 @@ k_elementwise(const __grid_constant__ EwPlan p) {
 // the other term.
 template <int OP, int WHICH>
 struct RedTerms {
-  // Inputs read by X's term, and by the dense gradient's term (only when a
-  // dense gradient is written in the same pass).
+  // div with grad_b reduced: b is constant along the reduction (it is the
+  // broadcast operand), so sum(-g*a/b^2) = -(1/b^2) * sum(g*a): the kernel adds
+  // g*a and applies post(b) once per output.
+  static constexpr bool kPost = OP == OP_DIV && WHICH == 1;
+  // Inputs read per element by X's term, and by the dense gradient's term
+  // (only when a dense gradient is written in the same pass).
   static constexpr bool kXa = Needs<OP, WHICH>::a;
-  static constexpr bool kXb = Needs<OP, WHICH>::b;
+  static constexpr bool kXb = Needs<OP, WHICH>::b && !kPost;
   static constexpr bool kDa = WHICH < 2 && Needs<OP, 1 - WHICH>::a;
   static constexpr bool kDb = WHICH < 2 && Needs<OP, 1 - WHICH>::b;
+  // Summed terms need not be single IEEE operations (the sum is within
+  // tolerance, not bit-exact): div's g/b is taken as g * (1/b).
   __device__ __forceinline__ static float x(float g, float a, float b) {
-    if (WHICH == 0) return term_a<OP>(g, a, b);
-    if (WHICH == 1) return term_b<OP>(g, a, b);
+    if (WHICH == 0) {
+      if (OP == OP_DIV) return __fmul_rn(g, __frcp_rn(b));
+      return term_a<OP>(g, a, b);
+    }
+    if (WHICH == 1) {
+      if (OP == OP_DIV) return __fmul_rn(g, a);
+      return term_b<OP>(g, a, b);
+    }
     return g;
   }
+  __device__ __forceinline__ static float post(float b) {
+    const float r = __frcp_rn(b);
+    return -__fmul_rn(r, r);
+  }
+  // Dense gradient terms stay exact single operations (bit-identical).
   __device__ __forceinline__ static float d(float g, float a, float b) {
     if (WHICH == 0) return term_b<OP>(g, a, b);
     return term_a<OP>(g, a, b);
   }
   // The same rule on the host: which pointers the kernel dereferences.
   static bool reads_a(bool has_d) { return kXa || (has_d && kDa); }
-  static bool reads_b(bool has_d) { return kXb || (has_d && kDb); }
+  static bool reads_b(bool has_d) { return kXb || (has_d && kDb) || kPost; }
 };
 
 // Reduction pass.  CTA = (kept index, row block, column block).  Rows of
@@ -266,6 +334,9 @@ k_reduce(const __grid_constant__ RedPlan p) {
   Kahan acc[VEC];
 #pragma unroll
   for (int i = 0; i < VEC; ++i) acc[i].init();
+  // Column vectors this thread owns in the block (one when the inner dim is
+  // kept: vcols_per_blk == tx).
+  const uint32_t ncs = vcol_end > vcol_begin + tx ? (vcol_end - vcol_begin - tx + p.tx - 1) / p.tx : 0;
 
   for (uint32_t ch0 = 0; ch0 < nrows; ch0 += kMaxTileRows) {
     const uint32_t cleft = nrows - ch0;
@@ -279,45 +350,48 @@ k_reduce(const __grid_constant__ RedPlan p) {
     }
     __syncthreads();
 
-    for (uint32_t vc = vcol_begin + tx; vc < vcol_end; vc += p.tx) {
-      const uint32_t c = vc * VEC;
-      constexpr int U = 4;
-      for (uint32_t r0 = ty; r0 < nch; r0 += U * p.ty) {
-        Vec<VEC> gv[U], av[U], bv[U];
-        bool ok[U];
+    // This thread's items are (row, column vector) pairs: rows ty, ty + ty_n,
+    // ... of the chunk, columns vcol_begin + tx, + tx_n, ... of the block,
+    // walked columns-fastest and loaded U at a time so that U independent
+    // loads per operand are in flight whichever of the two is longer.
+    const uint32_t nrs = nch > ty ? (nch - ty + p.ty - 1) / p.ty : 0;
+    const uint32_t items = ncs * nrs;
+    uint32_t rm = 0, cm = 0;
+    constexpr int U = 4;
+    for (uint32_t m0 = 0; m0 < items; m0 += U) {
+      Vec<VEC> gv[U], av[U], bv[U];
+      uint32_t ri[U], cc[U];
+      bool ok[U];
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-          const uint32_t ri = r0 + u * p.ty;
-          ok[u] = ri < nch;
-          if (ok[u]) {
-            const int64_t* ro = s_off + ri * kMaxOperands;
-            gv[u] = load_cols<VEC>(p.g, ro[0], p.inner_stride[0], c, p.stream_mask & 1);
-            if ((T::kXa || T::kDa) && read_a)
-              av[u] = load_cols<VEC>(p.a, ro[1], p.inner_stride[1], c, p.stream_mask & 2);
-            if ((T::kXb || T::kDb) && read_b)
-              bv[u] = load_cols<VEC>(p.b, ro[2], p.inner_stride[2], c, p.stream_mask & 4);
-          }
-        }
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-          if (!ok[u]) continue;
-          Vec<VEC> dv;
-#pragma unroll
-          for (int i = 0; i < VEC; ++i) {
-            const float gg = gv[u].v[i];
-            const float aa = ((T::kXa || T::kDa) && read_a) ? av[u].v[i] : 0.f;
-            const float bb = ((T::kXb || T::kDb) && read_b) ? bv[u].v[i] : 0.f;
-            if (INNER_KEPT) acc[i].add(T::x(gg, aa, bb));
-            else acc[0].add(T::x(gg, aa, bb));
-            if (has_d) dv.v[i] = T::d(gg, aa, bb);
-          }
-          if (has_d) {
-            const uint32_t ri = r0 + u * p.ty;
-            store_cols<VEC>(p.d_out, s_off[ri * kMaxOperands + kSlotOut], 1, c, dv);
-          }
+      for (int u = 0; u < U; ++u) {
+        ok[u] = m0 + u < items;
+        ri[u] = ty + rm * p.ty;
+        cc[u] = (vcol_begin + tx + cm * p.tx) * VEC;
+        if (ok[u]) {
+          const int64_t* ro = s_off + ri[u] * kMaxOperands;
+          gv[u] = load_cols<VEC>(p.g, ro[0], p.inner_stride[0], cc[u], p.stream_mask & 1);
+          if ((T::kXa || T::kDa) && read_a)
+            av[u] = load_cols<VEC>(p.a, ro[1], p.inner_stride[1], cc[u], p.stream_mask & 2);
+          if ((T::kXb || T::kDb) && read_b)
+            bv[u] = load_cols<VEC>(p.b, ro[2], p.inner_stride[2], cc[u], p.stream_mask & 4);
+          if (++cm == ncs) { cm = 0; ++rm; }
         }
       }
-      if (INNER_KEPT) break;  // one column vector per thread
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        if (!ok[u]) continue;
+        Vec<VEC> dv;
+#pragma unroll
+        for (int i = 0; i < VEC; ++i) {
+          const float gg = gv[u].v[i];
+          const float aa = ((T::kXa || T::kDa) && read_a) ? av[u].v[i] : 0.f;
+          const float bb = ((T::kXb || T::kDb) && read_b) ? bv[u].v[i] : 0.f;
+          if (INNER_KEPT) acc[i].add(T::x(gg, aa, bb));
+          else acc[0].add(T::x(gg, aa, bb));
+          if (has_d) dv.v[i] = T::d(gg, aa, bb);
+        }
+        if (has_d) store_cols<VEC>(p.d_out, s_off[ri[u] * kMaxOperands + kSlotOut], 1, cc[u], dv);
+      }
     }
   }
 
@@ -342,14 +416,19 @@ k_reduce(const __grid_constant__ RedPlan p) {
     if (ty == 0 && vc < vcol_end) {
       Vec<VEC> r;
       const uint64_t j = uint64_t(cta.kidx) * p.ncol + uint64_t(vc) * VEC;
+#pragma unroll
+      for (int i = 0; i < VEC; ++i) r.v[i] = s_red[tx * VEC + i];
+      if (T::kPost) {
+        const Vec<VEC> bv = load_cols<VEC>(p.b, base[2], p.inner_stride[2], vc * VEC, false);
+#pragma unroll
+        for (int i = 0; i < VEC; ++i) r.v[i] = __fmul_rn(r.v[i], T::post(bv.v[i]));
+      }
       float* dst;
       if (p.nslots == 1) {
 #pragma unroll
-        for (int i = 0; i < VEC; ++i) r.v[i] = __fmul_rn(s_red[tx * VEC + i], p.scale);
+        for (int i = 0; i < VEC; ++i) r.v[i] = __fmul_rn(r.v[i], p.scale);
         dst = p.x_final + j;
       } else {
-#pragma unroll
-        for (int i = 0; i < VEC; ++i) r.v[i] = s_red[tx * VEC + i];
         dst = p.partial + uint64_t(cta.rblk) * p.nout + j;
       }
       store_cols<VEC>(dst, 0, 1, 0, r);
@@ -363,7 +442,8 @@ k_reduce(const __grid_constant__ RedPlan p) {
       if (threadIdx.x < h) s_red[threadIdx.x] = __fadd_rn(s_red[threadIdx.x], s_red[threadIdx.x + h]);
     }
     if (threadIdx.x == 0) {
-      const float r = s_red[0];
+      float r = s_red[0];
+      if (T::kPost) r = __fmul_rn(r, T::post(__ldg(p.b + base[2])));
       if (p.nslots == 1) {
         p.x_final[cta.kidx] = __fmul_rn(r, p.scale);
       } else {

@@ -41,6 +41,18 @@ cudaError_t launch_fwd(int op, const EwBuild& eb, cudaStream_t s, bool dry) {
   }
 }
 
+cudaError_t launch_fwd_tr(int op, const TrPlan& tp, cudaStream_t s, bool dry) {
+  if (!tp.x || !tp.y || !tp.out) return cudaErrorInvalidValue;
+  if (dry) return cudaSuccess;
+  switch (op) {
+    case OP_ADD: k_transpose<OP_ADD><<<tp.n_cta, kThreads, 0, s>>>(tp); break;
+    case OP_SUB: k_transpose<OP_SUB><<<tp.n_cta, kThreads, 0, s>>>(tp); break;
+    case OP_MUL: k_transpose<OP_MUL><<<tp.n_cta, kThreads, 0, s>>>(tp); break;
+    default: k_transpose<OP_DIV><<<tp.n_cta, kThreads, 0, s>>>(tp); break;
+  }
+  return cudaGetLastError();
+}
+
 cudaError_t launch_bwd_direct(int op, int want, const EwBuild& eb, cudaStream_t s, bool dry) {
   switch (op) {
     case OP_ADD: return launch_direct_op<OP_ADD>(want, eb, s, dry);

@@ -18,7 +18,7 @@ cudaError_t launch_sab_t(const SabBuild& sb, cudaStream_t s, bool dry) {
   cudaError_t e = cudaFuncSetAttribute(k_sab<OP, RPT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        int(p.smem_bytes));
   if (e != cudaSuccess) return e;
-  k_sab<OP, RPT><<<p.grid, kThreads, p.smem_bytes, s>>>(p);
+  k_sab<OP, RPT><<<p.grid, kSabThreads, p.smem_bytes, s>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   CombinePlan ca = sb.comb_a, cb = sb.comb_b;
@@ -35,7 +35,6 @@ cudaError_t launch_sab_op(const SabBuild& sb, cudaStream_t s, bool dry) {
     case 1: return launch_sab_t<OP, 1>(sb, s, dry);
     case 2: return launch_sab_t<OP, 2>(sb, s, dry);
     case 4: return launch_sab_t<OP, 4>(sb, s, dry);
-    case 8: return launch_sab_t<OP, 8>(sb, s, dry);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -271,6 +271,9 @@ int build_ew(const Prob& P, const float* const in[3], float* const out[2], uint3
   const uint64_t ncta = ceil_div(nrow, trows) * p.col_tiles;
   if (ncta >= (uint64_t(1) << 31)) return ZR_ERR_SIZE;
   p.n_cta = uint32_t(ncta);
+  p.tx = std::min<uint32_t>(kThreads, pick_tx(tvc));
+  p.tx_shift = 0;
+  while ((1u << p.tx_shift) < p.tx) ++p.tx_shift;
   return ZR_OK;
 }
 
@@ -387,6 +390,68 @@ int build_red(const Prob& P, int xslot, const float* g, const float* a, const fl
   c.jx = jx;
   c.sy = std::min<uint32_t>(sy, pow2_ceil(p.nslots));
   return ZR_OK;
+}
+
+int build_tr(const Prob& P, const float* a, const float* b, float* out, TrPlan* tp) {
+  const int n = P.n;
+  const int q = n - 1;
+  if (n < 2 || P.st[kSlotOut][q] != 1) return 1;
+  int xs = -1, pd = -1;
+  for (int k = 0; k < 2 && xs < 0; ++k) {
+    if (P.st[k][q] == 0 || P.st[k][q] == 1) continue;
+    for (int d = 0; d < q; ++d)
+      if (P.st[k][d] == 1) { xs = k; pd = d; break; }
+  }
+  if (xs < 0) return 1;
+  const int ys = 1 - xs;
+  if (P.size[pd] >= (int64_t(1) << 31) || P.size[q] >= (int64_t(1) << 31)) return 1;
+  TrPlan& p = *tp;
+  p = TrPlan{};
+  p.x = xs == 0 ? a : b;
+  p.y = xs == 0 ? b : a;
+  p.out = out;
+  p.x_is_a = xs == 0 ? 1 : 0;
+  // Batch dims in row-major order, remapped to slots x=0, y=1, out=3.
+  int dims[kMaxDims];
+  int nd = 0;
+  uint64_t nbatch = 1;
+  for (int d = 0; d < q; ++d)
+    if (d != pd) { dims[nd++] = d; nbatch *= uint64_t(P.size[d]); }
+  p.batch.n = nd;
+  for (int i = 0; i < kMaxDims; ++i) {
+    p.batch.div[i] = make_fastdiv(1);
+    for (int k = 0; k < kMaxOperands; ++k) p.batch.stride[k][i] = 0;
+  }
+  for (int i = 0; i < nd; ++i) {
+    const int d = dims[nd - 1 - i];
+    p.batch.div[i] = make_fastdiv(uint32_t(P.size[d]));
+    p.batch.stride[0][i] = P.st[xs][d];
+    p.batch.stride[1][i] = P.st[ys][d];
+    p.batch.stride[kSlotOut][i] = P.st[kSlotOut][d];
+  }
+  p.xs_q = P.st[xs][q];
+  p.ys_p = P.st[ys][pd];
+  p.ys_q = P.st[ys][q];
+  p.os_p = P.st[kSlotOut][pd];
+  p.np = uint32_t(P.size[pd]);
+  p.nq = uint32_t(P.size[q]);
+  p.n_pt = uint32_t(ceil_div(p.np, kTrTile));
+  p.n_qt = uint32_t(ceil_div(p.nq, kTrTile));
+  p.n_qt_div = make_fastdiv(p.n_qt);
+  p.n_pt_div = make_fastdiv(p.n_pt);
+  const uint64_t ncta = nbatch * p.n_pt * p.n_qt;
+  if (nbatch >= (uint64_t(1) << 32) || ncta >= (uint64_t(1) << 31)) return 1;
+  p.n_cta = uint32_t(ncta);
+  return ZR_OK;
+}
+
+std::string describe_tr(const TrPlan& p) {
+  char buf[512];
+  std::snprintf(buf, sizeof(buf),
+                "{\"kernel\":\"transpose\",\"x_is_a\":%u,\"np\":%u,\"nq\":%u,\"batch_dims\":%d,"
+                "\"xs_q\":%lld,\"ctas\":%u}",
+                p.x_is_a, p.np, p.nq, p.batch.n, (long long)p.xs_q, p.n_cta);
+  return buf;
 }
 
 std::string describe_ew(const EwBuild& eb) {
@@ -507,7 +572,9 @@ int build_sab(const Prob& P, const float* g, const float* a, const float* b, flo
     outer[n_out++] = {uint64_t(P.size[d]), {P.st[0][d], P.st[1][d], P.st[2][d]}};
   }
   const uint64_t rows_x_vec = ta * nvc;
-  if (rows_x_vec < 256 || rows_x_vec > 2048 || (rows_x_vec & (rows_x_vec - 1)) != 0) return 1;
+  if (rows_x_vec < uint64_t(kSabThreads) || rows_x_vec > 2048 ||
+      (rows_x_vec & (rows_x_vec - 1)) != 0)
+    return 1;
   if (n_in > kMaxDims || n_out > kMaxDims) return 1;
   // inner[] / outer[] were collected inner-to-outer; reverse into row-major.
   std::reverse(inner, inner + n_in);
@@ -546,11 +613,11 @@ int build_sab(const Prob& P, const float* g, const float* a, const float* b, flo
     smax = std::max(smax, c1 - c0 + 1);
   }
   p.slots_a = smax;
-  const uint64_t smem = uint64_t(kSabStages) * ta * ncol * 4 + 2 * ta * 8 + 2 * n_beta * 8 +
-                        2 * 8 * ncol * 4;
+  const uint64_t smem = uint64_t(kSabStages) * (ta + 1) * ncol * 4 + 2 * ta * 8 +
+                        2 * n_beta * 8 + 2 * (kSabThreads / 32) * ncol * 4;
   if (smem > 220 * 1024) return 1;
   p.smem_bytes = uint32_t(smem);
-  sb->rpt = int(rows_x_vec / 256);
+  sb->rpt = int(rows_x_vec / kSabThreads);
   sb->ws_a_bytes = ((uint64_t(p.slots_a) * p.n_a * 4 + 255) / 256) * 256;
   sb->ws_b_bytes = ((uint64_t(p.n_tiles) * p.n_b * 4 + 255) / 256) * 256;
   CombinePlan* cs[2] = {&sb->comb_a, &sb->comb_b};

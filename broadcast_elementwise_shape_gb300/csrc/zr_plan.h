@@ -62,6 +62,10 @@ struct EwBuild {
 int build_ew(const Prob& P, const float* const in[3], float* const out[2], uint32_t read_mask,
              uint32_t stream_mask, EwBuild* eb);
 
+// Transposed-input forward plan; ZR_OK when the layout qualifies, 1 if not.
+int build_tr(const Prob& P, const float* a, const float* b, float* out, TrPlan* tp);
+std::string describe_tr(const TrPlan& tp);
+
 struct RedBuild {
   RedPlan plan;
   CombinePlan comb;

@@ -15,9 +15,10 @@
 // with b's factor taken out of the alpha sum.
 //
 // Persistent grid; each CTA walks a contiguous range of steps (tile, beta).
-// A step's tile (ta rows x ncol floats, typically 32 KB) is staged into
-// shared memory by cp.async through a kSabStages-deep pipeline, so several
-// tiles' loads are in flight while the previous one is summed.
+// A step's tile (ta rows x ncol floats, typically 32 KB) and b's row for
+// that beta are staged into shared memory by cp.async through a
+// kSabStages-deep pipeline, so several tiles' loads are in flight while the
+// previous one is summed and no load sits on the per-step critical path.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -38,35 +39,36 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
 }
 
-// b's factor in grad_a's term, per lane.
+// The factor of b applied per element to grad_a's term is staged as a row
+// of shared memory one step ahead: for div the row holds 1/b (so the per
+// element work is one multiply), for mul it holds b.
 template <int OP>
-__device__ __forceinline__ float sab_ca(float bv) {
-  if (OP == OP_MUL) return bv;
-  if (OP == OP_DIV) return __frcp_rn(bv);
-  return 1.0f;
+__device__ __forceinline__ float sab_row(float bv) {
+  return OP == OP_DIV ? __frcp_rn(bv) : bv;
 }
-// b's factor applied to grad_b's alpha sum.
+// Factor applied to grad_b's alpha sum, from the staged row value.
 template <int OP>
-__device__ __forceinline__ float sab_sb(float bv) {
+__device__ __forceinline__ float sab_scale(float rv) {
   if (OP == OP_SUB) return -1.0f;
-  if (OP == OP_DIV) {
-    const float r = __frcp_rn(bv);
-    return -__fmul_rn(r, r);
-  }
+  if (OP == OP_DIV) return -__fmul_rn(rv, rv);
   return 1.0f;
 }
 
 template <int OP, int RPT>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kSabThreads, 1)
 k_sab(const __grid_constant__ SabPlan p) {
   constexpr bool kUsesA = OP == OP_MUL || OP == OP_DIV;
   constexpr bool kUsesB = OP == OP_MUL || OP == OP_DIV;
+  constexpr uint32_t kWarps = kSabThreads / 32;
   extern __shared__ float4 s_raw[];
+  // Stage = tile [ta][ncol] followed by b's row [ncol] (converted in place
+  // to the per-element factor one step before use).
   const uint32_t tile_floats = p.ta * p.ncol;
+  const uint32_t stage_floats = tile_floats + p.ncol;
   float* s_stage = reinterpret_cast<float*>(s_raw);
-  int64_t* s_row = reinterpret_cast<int64_t*>(s_stage + kSabStages * tile_floats);  // [ta][2]
-  int64_t* s_beta = s_row + 2 * p.ta;                                                // [n_beta][2]
-  float* s_sb = reinterpret_cast<float*>(s_beta + 2 * p.n_beta);                     // [2][8][ncol]
+  int64_t* s_row = reinterpret_cast<int64_t*>(s_stage + kSabStages * stage_floats);  // [ta][2]
+  int64_t* s_beta = s_row + 2 * p.ta;                                                 // [n_beta][2]
+  float* s_sb = reinterpret_cast<float*>(s_beta + 2 * p.n_beta);                      // [2][warps][ncol]
 
   const uint32_t tid = threadIdx.x;
   for (uint32_t i = tid; i < p.ta; i += blockDim.x) {
@@ -88,52 +90,70 @@ k_sab(const __grid_constant__ SabPlan p) {
   const uint64_t s1 = sab_start(p, cta + 1);
   const uint32_t nvc = p.nvc;  // power of two
   const uint32_t nvc_shift = __ffs(nvc) - 1;
-  const uint32_t lanes = kThreads >> nvc_shift;  // row lanes
+  const uint32_t lanes = kSabThreads >> nvc_shift;  // row lanes
   const uint32_t tx = tid & (nvc - 1);
   const uint32_t ty = tid >> nvc_shift;
   const uint32_t warp = tid >> 5, lane = tid & 31;
 
-  // Stage the tile of step `step` (if in range) and close one copy group.
+  // This thread's RPT 16-byte chunks of every tile: fixed rows and columns,
+  // so their source offsets (within a tile) and destinations are fixed too.
+  int64_t chunk_src[RPT];
+  uint32_t chunk_dst[RPT];
+#pragma unroll
+  for (int k = 0; k < RPT; ++k) {
+    const uint32_t id = tid + k * kSabThreads;
+    const uint32_t row = id >> nvc_shift;
+    const uint32_t c4 = id & (nvc - 1);
+    chunk_src[k] = s_row[2 * row] + c4 * 4;
+    chunk_dst[k] = row * p.ncol + c4 * 4;
+  }
+  uint32_t iss_tile = 0xffffffffu;
+  int64_t iss_base = 0;
+
+  // Stage the tile (and b's row) of `step` if in range; close one group.
   auto issue = [&](uint64_t step, uint32_t stage) {
     if (step < s1) {
       const uint32_t tile = fd_div(p.n_beta_div, static_cast<uint32_t>(step));
       const uint32_t beta = static_cast<uint32_t>(step) - tile * p.n_beta;
-      int64_t ob[kMaxOperands];
-      decomp_offsets(p.a_outer, tile, ob);
-      const float* src = p.g + ob[0] + s_beta[2 * beta];
-      float* dst = s_stage + stage * tile_floats;
-#pragma unroll
-      for (int k = 0; k < RPT; ++k) {
-        const uint32_t id = tid + k * kThreads;
-        const uint32_t row = id >> nvc_shift;
-        const uint32_t c4 = id & (nvc - 1);
-        cp_async16(dst + row * p.ncol + c4 * 4, src + s_row[2 * row] + c4 * 4);
+      if (tile != iss_tile) {
+        int64_t ob[kMaxOperands];
+        decomp_offsets(p.a_outer, tile, ob);
+        iss_tile = tile;
+        iss_base = ob[0];
       }
+      const float* src = p.g + iss_base + s_beta[2 * beta];
+      float* dst = s_stage + stage * stage_floats;
+      if (kUsesB && tid < nvc) cp_async16(dst + tile_floats + tid * 4, p.b + s_beta[2 * beta + 1] + tid * 4);
+#pragma unroll
+      for (int k = 0; k < RPT; ++k) cp_async16(dst + chunk_dst[k], src + chunk_src[k]);
     }
     cp_async_commit();
   };
-
-  // grad_b of one finished step: add the 8 warps' partials in warp order,
-  // apply b's factor, store to slot `tile` of the workspace.
-  auto finish_b = [&](uint64_t step, uint32_t buf, float4 bv) {
-    if (tid < nvc) {
+  // Turn a landed stage's b row into the per-element factor.
+  auto convert_row = [&](uint32_t stage) {
+    if (kUsesB && tid < p.ncol) {
+      float* r = s_stage + stage * stage_floats + tile_floats;
+      r[tid] = sab_row<OP>(r[tid]);
+    }
+  };
+  // grad_b of a finished step: per column, the warps' partials in warp order,
+  // times b's factor; stored to slot `tile` of the workspace.
+  auto finish_b = [&](uint64_t step, uint32_t buf, float rv) {
+    if (tid < p.ncol) {
       const uint32_t tile = fd_div(p.n_beta_div, static_cast<uint32_t>(step));
       const uint32_t beta = static_cast<uint32_t>(step) - tile * p.n_beta;
-      const float* src = s_sb + buf * 8 * p.ncol + tid * 4;
-      float4 v = *reinterpret_cast<const float4*>(src);
-      for (int w = 1; w < 8; ++w) {
-        const float4 u = *reinterpret_cast<const float4*>(src + w * p.ncol);
-        v.x = __fadd_rn(v.x, u.x); v.y = __fadd_rn(v.y, u.y);
-        v.z = __fadd_rn(v.z, u.z); v.w = __fadd_rn(v.w, u.w);
-      }
-      v.x = __fmul_rn(v.x, sab_sb<OP>(bv.x)); v.y = __fmul_rn(v.y, sab_sb<OP>(bv.y));
-      v.z = __fmul_rn(v.z, sab_sb<OP>(bv.z)); v.w = __fmul_rn(v.w, sab_sb<OP>(bv.w));
-      float* dst = p.ws_b + uint64_t(tile) * p.n_b + uint64_t(beta) * p.ncol + tid * 4;
-      *reinterpret_cast<float4*>(dst) = v;
+      const float* src = s_sb + buf * kWarps * p.ncol + tid;
+      float v = src[0];
+#pragma unroll
+      for (uint32_t w = 1; w < kWarps; ++w) v = __fadd_rn(v, src[w * p.ncol]);
+      p.ws_b[uint64_t(tile) * p.n_b + uint64_t(beta) * p.ncol + tid] = __fmul_rn(v, sab_scale<OP>(rv));
     }
   };
 
   for (int k = 0; k < kSabStages - 1; ++k) issue(s0 + k, k);
+  cp_async_wait<kSabStages - 2>();
+  __syncthreads();
+  convert_row(0);
 
   Kahan acc[RPT][4];
 #pragma unroll
@@ -144,13 +164,16 @@ k_sab(const __grid_constant__ SabPlan p) {
 #pragma unroll
   for (int j = 0; j < RPT; ++j) areg[j] = make_float4(1.f, 1.f, 1.f, 1.f);
   uint32_t cur_tile = 0xffffffffu;
-  float4 bcur = make_float4(1.f, 1.f, 1.f, 1.f), bprev = bcur;
+  float rprev = 1.0f;  // factor of column tid at the previous step (tid < ncol)
 
   for (uint64_t step = s0; step < s1; ++step) {
     const uint32_t k = static_cast<uint32_t>(step - s0);
-    cp_async_wait<kSabStages - 2>();
+    // Steps k and k+1 have landed (for this thread's copies); the barrier
+    // makes every thread's copies visible and frees stage (k-1).
+    cp_async_wait<kSabStages - 3>();
     __syncthreads();
-    if (k > 0) finish_b(step - 1, (k - 1) & 1, bprev);
+    if (step + 1 < s1) convert_row((k + 1) % kSabStages);
+    if (k > 0) finish_b(step - 1, (k - 1) & 1, rprev);
     issue(step + kSabStages - 1, (k + kSabStages - 1) % kSabStages);
 
     const uint32_t tile = fd_div(p.n_beta_div, static_cast<uint32_t>(step));
@@ -165,11 +188,13 @@ k_sab(const __grid_constant__ SabPlan p) {
       }
     }
     cur_tile = tile;
-    if (kUsesB) bcur = __ldg(reinterpret_cast<const float4*>(p.b + s_beta[2 * beta + 1] + tx * 4));
-    const float4 ca = make_float4(sab_ca<OP>(bcur.x), sab_ca<OP>(bcur.y), sab_ca<OP>(bcur.z),
-                                  sab_ca<OP>(bcur.w));
+    const float* st = s_stage + (k % kSabStages) * stage_floats;
+    float4 ca = make_float4(1.f, 1.f, 1.f, 1.f);
+    if (kUsesB) {
+      ca = *reinterpret_cast<const float4*>(st + tile_floats + tx * 4);
+      if (tid < p.ncol) rprev = st[tile_floats + tid];
+    }
 
-    const float* st = s_stage + (k % kSabStages) * tile_floats;
     float4 sb = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int j = 0; j < RPT; ++j) {
@@ -196,7 +221,7 @@ k_sab(const __grid_constant__ SabPlan p) {
       sb.w = __fadd_rn(sb.w, __shfl_xor_sync(0xffffffffu, sb.w, off));
     }
     if (lane < nvc)
-      *reinterpret_cast<float4*>(s_sb + (k & 1) * 8 * p.ncol + warp * p.ncol + tx * 4) = sb;
+      *reinterpret_cast<float4*>(s_sb + (k & 1) * kWarps * p.ncol + warp * p.ncol + tx * 4) = sb;
 
     // Leaving this tile (its last beta, or the end of this CTA's range):
     // write grad_a's partial to this CTA's slot for the tile.
@@ -219,11 +244,10 @@ k_sab(const __grid_constant__ SabPlan p) {
         for (int i = 0; i < 4; ++i) acc[j][i].init();
       }
     }
-    bprev = bcur;
   }
   cp_async_wait<0>();
   __syncthreads();
-  if (s1 > s0) finish_b(s1 - 1, static_cast<uint32_t>(s1 - s0 - 1) & 1, bprev);
+  if (s1 > s0) finish_b(s1 - 1, static_cast<uint32_t>(s1 - s0 - 1) & 1, rprev);
 }
 
 }  // namespace zr

@@ -285,7 +285,7 @@ def test_plan_dispatch_for_workloads(L):
     d = fwd((8, 12, 1024, 1024), (1, 1, 1024, 1024))
     assert (d["nrow"], d["ncol"]) == (96, 1024 * 1024)
     d = fwd((128, 256, 512), (1, 256, 1), sta=(131072, 1, 256))
-    assert d["row_dims"] == 2 and d["inner_stride"][0] == 256
+    assert d["kernel"] == "transpose" and d["xs_q"] == 256 and (d["np"], d["nq"]) == (256, 512)
     d = fwd((4, 1, 8, 1, 16, 1, 32, 64), (1, 6, 1, 12, 1, 10, 1, 64))
     assert d["row_dims"] == 7 and d["ncol"] == 64 and d["vec"] == 4
     d = bwd(0, (4096, 1024), (1024,))
