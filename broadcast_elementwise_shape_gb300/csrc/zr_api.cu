@@ -739,17 +739,19 @@ void walk_ew(const EwBuild& eb, Rec rec) {
   const uint32_t ty_n = kThreads >> p.tx_shift;
   for (uint32_t cta = 0; cta < p.n_cta; ++cta) {
     const EwTile t = ew_tile(p, cta);
+    const uint32_t rpt = (t.nrows + ty_n - 1) / ty_n;
     for (uint32_t thr = 0; thr < uint32_t(kThreads); ++thr) {
       const uint32_t tx = thr & (p.tx - 1), ty = thr >> p.tx_shift;
+      const uint32_t r_begin = ty * rpt;
       const uint32_t ncs = t.nvcols > tx ? (t.nvcols - tx + p.tx - 1) >> p.tx_shift : 0;
-      const uint32_t nrs = t.nrows > ty ? (t.nrows - ty + ty_n - 1) / ty_n : 0;
-      uint32_t rm = 0, cm = 0;
+      const uint32_t nrs = t.nrows > r_begin ? std::min(rpt, t.nrows - r_begin) : 0;
+      uint32_t row = r_begin, cm = 0;
       for (uint32_t m = 0; m < ncs * nrs; ++m) {
-        const uint32_t row = ty + rm * ty_n;
+        const uint32_t r = row;
         const uint32_t vc = tx + cm * p.tx;
-        if (++cm == ncs) { cm = 0; ++rm; }
+        if (++cm == ncs) { cm = 0; ++row; }
         int64_t off[kMaxOperands];
-        decomp_offsets(p.rows, t.row0 + row, off);
+        decomp_offsets(p.rows, t.row0 + r, off);
         for (int i = 0; i < eb.vec; ++i) {
           const int64_t c = int64_t(t.vcol0 + vc) * eb.vec + i;
           if (c >= p.ncol) continue;

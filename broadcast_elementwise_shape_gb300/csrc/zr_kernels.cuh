@@ -23,6 +23,30 @@ __device__ __forceinline__ float fwd_op(float x, float y) {
   return __fdiv_rn(x, y);
 }
 
+// Correctly rounded x / y given r = RN(1/y) (the binary32 reciprocal from
+// __frcp_rn), for a divisor that repeats across many elements so that its
+// reciprocal is computed once.  q = RN(x*r) is within a few ulps of x/y; one
+// step q + r*(x - y*q), with the remainder x - y*q exact under FMA, makes it
+// faithful, and a second identical step then yields RN(x/y) (P. Markstein,
+// "Computation of elementary functions on the IBM RISC System/6000
+// processor", IBM J. Res. Dev. 34(1), 1990; J.-M. Muller et al., "Handbook of
+// Floating-Point Arithmetic", 2nd ed., 2018, ch. 4).  The theorem needs every
+// intermediate to stay normal: operands outside [2^-60, 2^60] in magnitude
+// (zeros, subnormals, infinities, huge values) take the IEEE division, and
+// NaNs propagate through either path.
+__device__ __forceinline__ float div_rn_rcp(float x, float y, float r) {
+  const float ax = fabsf(x), ay = fabsf(y);
+  if (!(ax >= 0x1p-60f && ax <= 0x1p60f && ay >= 0x1p-60f && ay <= 0x1p60f)) {
+    if (x != x || y != y) return __fadd_rn(x, y);  // NaN in, NaN out
+    return __fdiv_rn(x, y);
+  }
+  float q = __fmul_rn(x, r);
+  float e = __fmaf_rn(-y, q, x);
+  q = __fmaf_rn(e, r, q);
+  e = __fmaf_rn(-y, q, x);
+  return __fmaf_rn(e, r, q);
+}
+
 // Local gradient terms.  add (g, g) — GPU page, section OpAdd; mul (g*b, g*a)
 // — Operator page, section 逐元素算子; sub (g, -g) and div (g/b, -g*a/b^2) by
 // calculus (the pages do not write them out).  Every single-operation term
@@ -115,14 +139,18 @@ __device__ __forceinline__ void store_cols(float* __restrict__ base, int64_t row
 
 // ---------------------------------------------------------------- functors
 
-// Forward: out = a op b.
+// Forward: out = a op b.  For div, r holds RN(1/b) per lane.
 template <int OP>
 struct FwdF {
   static constexpr bool kR1 = true, kR2 = false;  // slot 0 = a, slot 1 = b
+  static constexpr int kDivSlot = OP == OP_DIV ? 1 : -1;  // input that divides
   template <int VEC>
-  __device__ __forceinline__ void operator()(const Vec<VEC> (&x)[3], Vec<VEC> (&y)[2]) const {
+  __device__ __forceinline__ void operator()(const Vec<VEC> (&x)[3], const Vec<VEC>& r,
+                                             Vec<VEC> (&y)[2]) const {
 #pragma unroll
-    for (int i = 0; i < VEC; ++i) y[0].v[i] = fwd_op<OP>(x[0].v[i], x[1].v[i]);
+    for (int i = 0; i < VEC; ++i)
+      y[0].v[i] = OP == OP_DIV ? div_rn_rcp(x[0].v[i], x[1].v[i], r.v[i])
+                               : fwd_op<OP>(x[0].v[i], x[1].v[i]);
   }
 };
 
@@ -132,8 +160,10 @@ template <int OP, int WANT>
 struct BwdDirectF {
   static constexpr bool kR1 = ((WANT & 1) && Needs<OP, 0>::a) || ((WANT & 2) && Needs<OP, 1>::a);
   static constexpr bool kR2 = ((WANT & 1) && Needs<OP, 0>::b) || ((WANT & 2) && Needs<OP, 1>::b);
+  static constexpr int kDivSlot = -1;  // exact IEEE division per element
   template <int VEC>
-  __device__ __forceinline__ void operator()(const Vec<VEC> (&x)[3], Vec<VEC> (&y)[2]) const {
+  __device__ __forceinline__ void operator()(const Vec<VEC> (&x)[3], const Vec<VEC>& r,
+                                             Vec<VEC> (&y)[2]) const {
 #pragma unroll
     for (int i = 0; i < VEC; ++i) {
       if (WANT & 1) y[0].v[i] = term_a<OP>(x[0].v[i], x[1].v[i], x[2].v[i]);
@@ -145,8 +175,10 @@ struct BwdDirectF {
 // Copy (sum-to-shape onto the same shape).
 struct CopyF {
   static constexpr bool kR1 = false, kR2 = false;
+  static constexpr int kDivSlot = -1;
   template <int VEC>
-  __device__ __forceinline__ void operator()(const Vec<VEC> (&x)[3], Vec<VEC> (&y)[2]) const {
+  __device__ __forceinline__ void operator()(const Vec<VEC> (&x)[3], const Vec<VEC>& r,
+                                             Vec<VEC> (&y)[2]) const {
     y[0] = x[0];
   }
 };
@@ -160,7 +192,7 @@ struct CopyF {
 // at a time so that U independent loads per operand are in flight before
 // any result is stored.
 template <class F, int VEC, int NOUT>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 4)
 k_elementwise(const __grid_constant__ EwPlan p) {
   extern __shared__ int64_t s_off[];  // [tile_rows][kMaxOperands]
   const EwTile t = ew_tile(p, blockIdx.x);
@@ -172,25 +204,36 @@ k_elementwise(const __grid_constant__ EwPlan p) {
   }
   __syncthreads();
 
+  // Thread (tx, ty): column vectors vcol0 + tx, + tx_n, ... and a contiguous
+  // run of rows [ty * rpt, ty * rpt + rpt), walked columns-fastest.
   const uint32_t tx = threadIdx.x & (p.tx - 1);
   const uint32_t ty = threadIdx.x >> p.tx_shift;
   const uint32_t ty_n = kThreads >> p.tx_shift;
+  const uint32_t rpt = (t.nrows + ty_n - 1) / ty_n;
+  const uint32_t r_begin = ty * rpt;
   const uint32_t ncs = t.nvcols > tx ? (t.nvcols - tx + p.tx - 1) >> p.tx_shift : 0;
-  const uint32_t nrs = t.nrows > ty ? (t.nrows - ty + ty_n - 1) / ty_n : 0;
+  const uint32_t nrs = t.nrows > r_begin ? min(rpt, t.nrows - r_begin) : 0;
   const uint32_t items = ncs * nrs;
   const int64_t in0 = p.inner_stride[0], in1 = p.inner_stride[1], in2 = p.inner_stride[2];
   const int64_t ino = p.inner_stride[kSlotOut];
+  constexpr int kDiv = F::kDivSlot;
+  const int64_t ind = kDiv == 1 ? in1 : in2;
 
   constexpr int U = 4;
   const F f;
-  uint32_t rm = 0, cm = 0;
-  uint32_t row = ty;
+  uint32_t cm = 0;
+  uint32_t row = r_begin;
   int64_t ro[kMaxOperands];
 #pragma unroll
-  for (int k = 0; k < kMaxOperands; ++k) ro[k] = row < t.nrows ? s_off[row * kMaxOperands + k] : 0;
+  for (int k = 0; k < kMaxOperands; ++k) ro[k] = nrs ? s_off[row * kMaxOperands + k] : 0;
+  // Reciprocal of the divisor, recomputed only when its element changes.
+  int64_t rkey = -1;
+  Vec<VEC> rcp;
+#pragma unroll
+  for (int i = 0; i < VEC; ++i) rcp.v[i] = 1.0f;
   for (uint32_t m0 = 0; m0 < items; m0 += U) {
     Vec<VEC> x[U][3];
-    int64_t doff[U];
+    int64_t doff[U], dkey[U];
     uint32_t col[U];
     bool ok[U];
 #pragma unroll
@@ -198,15 +241,15 @@ k_elementwise(const __grid_constant__ EwPlan p) {
       ok[u] = m0 + u < items;
       col[u] = (t.vcol0 + tx + cm * p.tx) * VEC;
       doff[u] = ro[kSlotOut];
+      dkey[u] = kDiv >= 0 ? ro[kDiv] + int64_t(col[u]) * ind : 0;
       if (ok[u]) {
         x[u][0] = load_cols<VEC>(p.in[0], ro[0], in0, col[u], p.stream_mask & 1);
         if (F::kR1) x[u][1] = load_cols<VEC>(p.in[1], ro[1], in1, col[u], p.stream_mask & 2);
         if (F::kR2) x[u][2] = load_cols<VEC>(p.in[2], ro[2], in2, col[u], p.stream_mask & 4);
         if (++cm == ncs) {
           cm = 0;
-          ++rm;
-          row += ty_n;
-          if (row < t.nrows) {
+          ++row;
+          if (row < r_begin + nrs) {
 #pragma unroll
             for (int k = 0; k < kMaxOperands; ++k) ro[k] = s_off[row * kMaxOperands + k];
           }
@@ -216,8 +259,13 @@ k_elementwise(const __grid_constant__ EwPlan p) {
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       if (!ok[u]) continue;
+      if (kDiv >= 0 && dkey[u] != rkey) {
+        rkey = dkey[u];
+#pragma unroll
+        for (int i = 0; i < VEC; ++i) rcp.v[i] = __frcp_rn(x[u][kDiv > 0 ? kDiv : 0].v[i]);
+      }
       Vec<VEC> y[2];
-      f(x[u], y);
+      f(x[u], rcp, y);
       if (p.out[0]) store_cols<VEC>(p.out[0], doff[u], ino, col[u], y[0]);
       if (NOUT > 1 && p.out[1]) store_cols<VEC>(p.out[1], doff[u], ino, col[u], y[1]);
     }

@@ -374,3 +374,33 @@ def test_both_reduced_fused_pass(op):
         ga2, gb2 = zr.zr_binary_bwd(op, g.cuda(), a.cuda(), b.cuda())
         assert torch.equal(ga.view(torch.int32), ga2.view(torch.int32))
         assert torch.equal(gb.view(torch.int32), gb2.view(torch.int32))
+
+
+def _rand_bits(rng, shape):
+    return rng.integers(0, 2 ** 32, size=shape, dtype=np.uint64).astype(np.uint32).view(np.float32)
+
+
+def _log_uniform(rng, shape, lo=-60, hi=60):
+    mag = np.exp2(rng.uniform(lo, hi, size=shape)).astype(np.float32)
+    return np.where(rng.random(shape) < 0.5, -mag, mag).astype(np.float32)
+
+
+def test_division_is_ieee_bit_exact():
+    """The forward div computes each quotient from the divisor's reciprocal
+    with remainder corrections; it must equal IEEE division bit for bit
+    (any NaN matching any NaN), including every binade, subnormals,
+    infinities and zeros (random bit patterns) and the reciprocal reuse
+    across rows of a broadcast divisor."""
+    rng = np.random.default_rng(2024)
+    cases = []
+    cases.append((_rand_bits(rng, (4096, 256)), _rand_bits(rng, (256,))))         # row divisor
+    cases.append((_log_uniform(rng, (4096, 256)), _log_uniform(rng, (256,))))     # fast path
+    cases.append((_log_uniform(rng, (2048, 512)), _log_uniform(rng, (2048, 1))))  # column divisor
+    cases.append((_rand_bits(rng, (1 << 20,)), _rand_bits(rng, (1 << 20,))))      # no reuse
+    cases.append((_log_uniform(rng, (1 << 20,), -126, 127), _log_uniform(rng, (1 << 20,), -126, 127)))
+    for s in (8.0, 3.0, 1e-40, 3e38, -7.5, 0.0, float("inf")):
+        cases.append((_log_uniform(rng, (1 << 18,), -80, 80), np.array([s], np.float32)))
+    for a, b in cases:
+        ta, tb = torch.from_numpy(a), torch.from_numpy(b)
+        got = zr.zr_binary_fwd("div", ta.cuda(), tb.cuda()).cpu().numpy()
+        bitexact(got, oracle.binary_fwd("div", ta, tb), f"div {a.shape} / {b.shape}")
