@@ -120,6 +120,9 @@ struct FwdSet {
   bool empty = false;
   bool tr = false;               // transposed-input tile path
   TrPlan tp;
+  bool sabf = false;             // split forward path
+  SabFPlan sp;
+  int sp_rpt = 0;
   EwBuild eb;
   TDesc a, b, out;
 };
@@ -163,6 +166,11 @@ int plan_fwd(int op, const zr_tensor& ta, const zr_tensor& tb, const float* out,
   rc = build_tr(P, S->a.ptr, S->b.ptr, const_cast<float*>(out), &S->tp);
   if (rc == ZR_OK) {
     S->tr = true;
+    return ZR_OK;
+  }
+  rc = build_sabf(P, S->a.ptr, S->b.ptr, const_cast<float*>(out), &S->sp, &S->sp_rpt);
+  if (rc == ZR_OK) {
+    S->sabf = true;
     return ZR_OK;
   }
   return build_ew(P, in, outs, 0x3u, stream_mask, &S->eb);
@@ -467,6 +475,8 @@ int zr_binary_fwd(zr_op op, zr_tensor a, zr_tensor b, float* out, const int64_t*
     if (rc) return rc;
   }
   if (S.tr) return cuda_status(launch_fwd_tr(op, S.tp, reinterpret_cast<cudaStream_t>(stream)));
+  if (S.sabf)
+    return cuda_status(launch_fwd_sabf(op, S.sp_rpt, S.sp, reinterpret_cast<cudaStream_t>(stream)));
   return cuda_status(launch_fwd(op, S.eb, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -654,6 +664,7 @@ int zr_test_dry_run_fwd(zr_op op, zr_tensor a, zr_tensor b, const float* out,
   const int rc = plan_fwd(op, a, b, out, out_strides, &S);
   if (rc || S.empty) return rc;
   if (S.tr) return cuda_status(launch_fwd_tr(op, S.tp, nullptr, true));
+  if (S.sabf) return cuda_status(launch_fwd_sabf(op, S.sp_rpt, S.sp, nullptr, true));
   return cuda_status(launch_fwd(op, S.eb, nullptr, true));
 }
 
@@ -681,7 +692,9 @@ int zr_test_describe_fwd(zr_op op, zr_tensor a, zr_tensor b, const float* out,
   const int rc = plan_fwd(op, a, b, out, out_strides, &S);
   if (rc) return rc;
   return copy_json(S.empty ? std::string("{\"kernel\":\"none\"}")
-                           : (S.tr ? describe_tr(S.tp) : describe_ew(S.eb)), buf, len);
+                           : (S.tr ? describe_tr(S.tp)
+                                   : (S.sabf ? describe_sabf(S.sp, S.sp_rpt) : describe_ew(S.eb))),
+                   buf, len);
 }
 
 int zr_test_describe_bwd(zr_op op, zr_tensor grad_out, zr_tensor a, zr_tensor b,
@@ -736,29 +749,20 @@ namespace {
 template <class Rec>
 void walk_ew(const EwBuild& eb, Rec rec) {
   const EwPlan& p = eb.plan;
-  const uint32_t ty_n = kThreads >> p.tx_shift;
   for (uint32_t cta = 0; cta < p.n_cta; ++cta) {
     const EwTile t = ew_tile(p, cta);
-    const uint32_t rpt = (t.nrows + ty_n - 1) / ty_n;
-    for (uint32_t thr = 0; thr < uint32_t(kThreads); ++thr) {
-      const uint32_t tx = thr & (p.tx - 1), ty = thr >> p.tx_shift;
-      const uint32_t r_begin = ty * rpt;
-      const uint32_t ncs = t.nvcols > tx ? (t.nvcols - tx + p.tx - 1) >> p.tx_shift : 0;
-      const uint32_t nrs = t.nrows > r_begin ? std::min(rpt, t.nrows - r_begin) : 0;
-      uint32_t row = r_begin, cm = 0;
-      for (uint32_t m = 0; m < ncs * nrs; ++m) {
-        const uint32_t r = row;
-        const uint32_t vc = tx + cm * p.tx;
-        if (++cm == ncs) { cm = 0; ++row; }
-        int64_t off[kMaxOperands];
-        decomp_offsets(p.rows, t.row0 + r, off);
-        for (int i = 0; i < eb.vec; ++i) {
-          const int64_t c = int64_t(t.vcol0 + vc) * eb.vec + i;
-          if (c >= p.ncol) continue;
-          int64_t o[kMaxOperands];
-          for (int k = 0; k < kMaxOperands; ++k) o[k] = off[k] + c * p.inner_stride[k];
-          rec(o);
-        }
+    for (uint32_t item = 0; item < p.items_per_cta; ++item) {
+      const uint32_t ri = fd_div(p.tile_vcols_div, item);
+      const uint32_t vc = item - ri * p.tile_vcols;
+      if (!(ri < t.nrows && vc < t.nvcols)) continue;
+      int64_t off[kMaxOperands];
+      decomp_offsets(p.rows, t.row0 + ri, off);
+      for (int i = 0; i < eb.vec; ++i) {
+        const int64_t c = int64_t(t.vcol0 + vc) * eb.vec + i;
+        if (c >= p.ncol) continue;
+        int64_t o[kMaxOperands];
+        for (int k = 0; k < kMaxOperands; ++k) o[k] = off[k] + c * p.inner_stride[k];
+        rec(o);
       }
     }
   }
@@ -774,14 +778,39 @@ void walk_tr(const TrPlan& p, Rec rec) {
     const uint32_t pt = t1 - bidx * p.n_pt;
     int64_t base[kMaxOperands];
     decomp_offsets(p.batch, bidx, base);
-    for (uint32_t i = 0; i < kTrTile; ++i) {
+    for (uint32_t i = 0; i < kTrP; ++i) {
       for (uint32_t l = 0; l < kTrTile; ++l) {
-        const uint32_t pp = pt * kTrTile + i, q = qt * kTrTile + l;
+        const uint32_t pp = pt * kTrP + i, q = qt * kTrTile + l;
         if (q >= p.nq || pp >= p.np) continue;
         int64_t o[kMaxOperands] = {base[0] + pp + int64_t(q) * p.xs_q,
                                    base[1] + int64_t(pp) * p.ys_p + int64_t(q) * p.ys_q, 0,
                                    base[kSlotOut] + int64_t(pp) * p.os_p + q};
         rec(o);
+      }
+    }
+  }
+}
+
+// Host walk of k_sabf's (CTA, row, beta, column) space; o[0] = a, o[1] = b,
+// o[3] = out.
+template <class Rec>
+void walk_sabf(const SabFPlan& p, Rec rec) {
+  for (uint32_t cta = 0; cta < p.n_cta; ++cta) {
+    const uint32_t tile = fd_div(p.n_bc_div, cta);
+    const uint32_t bc = cta - tile * p.n_bc;
+    int64_t ob[kMaxOperands];
+    decomp_offsets(p.a_outer, tile, ob);
+    const uint32_t b0 = bc * p.beta_chunk, b1 = std::min(p.n_beta, b0 + p.beta_chunk);
+    for (uint32_t r = 0; r < p.ta; ++r) {
+      int64_t ri[kMaxOperands];
+      decomp_offsets(p.a_inner, r, ri);
+      for (uint32_t beta = b0; beta < b1; ++beta) {
+        int64_t bo[kMaxOperands];
+        decomp_offsets(p.beta, beta, bo);
+        for (uint32_t c = 0; c < p.ncol; ++c) {
+          int64_t o[kMaxOperands] = {ob[1] + ri[1] + c, bo[2] + c, 0, ob[0] + ri[0] + bo[0] + c};
+          rec(o);
+        }
       }
     }
   }
@@ -885,6 +914,14 @@ int zr_test_emulate_fwd(zr_tensor a, zr_tensor b, const float* out, const int64_
       rec[3 * m + 0] = o[kSlotOut];
       rec[3 * m + 1] = S.tp.x_is_a ? o[0] : o[1];
       rec[3 * m + 2] = S.tp.x_is_a ? o[1] : o[0];
+      ++m;
+    });
+  } else if (!S.empty && S.sabf) {
+    walk_sabf(S.sp, [&](const int64_t* o) {
+      if (m >= cap) { over = true; return; }
+      rec[3 * m + 0] = o[kSlotOut];
+      rec[3 * m + 1] = o[0];
+      rec[3 * m + 2] = o[1];
       ++m;
     });
   } else if (!S.empty) {

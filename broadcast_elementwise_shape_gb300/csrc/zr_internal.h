@@ -107,7 +107,6 @@ struct EwPlan {
   FastDiv tile_vcols_div;   // item -> (row in tile, column vector)
   uint32_t items_per_cta;   // tile_rows * tile_vcols
   uint32_t n_cta;
-  uint32_t tx, tx_shift;    // column lanes per CTA (power of two) and log2
 };
 
 // Forward with one input read transposed: that input (X) walks the output's
@@ -127,8 +126,10 @@ struct TrPlan {
   uint32_t n_pt, n_qt;      // tiles along p and q
   FastDiv n_qt_div, n_pt_div;
   uint32_t n_cta;
+  uint32_t vec_ok;          // x's rows start 16-byte aligned: 16-byte loads
 };
-constexpr uint32_t kTrTile = 32;
+constexpr uint32_t kTrTile = 32;   // tile extent along q
+constexpr uint32_t kTrP = 128;     // tile extent along p
 
 constexpr uint32_t kMaxTileRows = 512;
 constexpr int kThreads = 256;
@@ -230,6 +231,25 @@ struct SabPlan {
   uint32_t slots_a;         // grad_a partial slots (max CTAs covering a tile)
   uint64_t n_a, n_b;        // elements of grad_a / grad_b
   uint32_t smem_bytes;
+};
+
+// Forward for the same split (every outer dim varies in exactly one input,
+// the innermost in both): out[alpha, beta, col] = a[alpha, col] op
+// b[beta, col].  A CTA holds one tile of a's rows in registers and writes
+// them against a chunk of betas, one b row per step.
+struct SabFPlan {
+  const float* a;
+  const float* b;
+  float* out;
+  Decomp a_outer;           // tile -> offsets (slot 0: out, 1: a)
+  Decomp a_inner;           // row  -> offsets (slot 0: out, 1: a)
+  Decomp beta;              // beta -> offsets (slot 0: out, 2: b)
+  uint32_t ncol, nvc;       // inner dim, float4 count (power of two <= 32)
+  uint32_t ta;              // rows per tile
+  uint32_t n_tiles, n_beta;
+  uint32_t beta_chunk, n_bc;  // betas per CTA, chunks
+  FastDiv n_bc_div;
+  uint32_t n_cta;
 };
 
 constexpr int kSabStages = 5;

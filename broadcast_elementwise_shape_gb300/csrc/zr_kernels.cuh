@@ -23,30 +23,6 @@ __device__ __forceinline__ float fwd_op(float x, float y) {
   return __fdiv_rn(x, y);
 }
 
-// Correctly rounded x / y given r = RN(1/y) (the binary32 reciprocal from
-// __frcp_rn), for a divisor that repeats across many elements so that its
-// reciprocal is computed once.  q = RN(x*r) is within a few ulps of x/y; one
-// step q + r*(x - y*q), with the remainder x - y*q exact under FMA, makes it
-// faithful, and a second identical step then yields RN(x/y) (P. Markstein,
-// "Computation of elementary functions on the IBM RISC System/6000
-// processor", IBM J. Res. Dev. 34(1), 1990; J.-M. Muller et al., "Handbook of
-// Floating-Point Arithmetic", 2nd ed., 2018, ch. 4).  The theorem needs every
-// intermediate to stay normal: operands outside [2^-60, 2^60] in magnitude
-// (zeros, subnormals, infinities, huge values) take the IEEE division, and
-// NaNs propagate through either path.
-__device__ __forceinline__ float div_rn_rcp(float x, float y, float r) {
-  const float ax = fabsf(x), ay = fabsf(y);
-  if (!(ax >= 0x1p-60f && ax <= 0x1p60f && ay >= 0x1p-60f && ay <= 0x1p60f)) {
-    if (x != x || y != y) return __fadd_rn(x, y);  // NaN in, NaN out
-    return __fdiv_rn(x, y);
-  }
-  float q = __fmul_rn(x, r);
-  float e = __fmaf_rn(-y, q, x);
-  q = __fmaf_rn(e, r, q);
-  e = __fmaf_rn(-y, q, x);
-  return __fmaf_rn(e, r, q);
-}
-
 // Local gradient terms.  add (g, g) — GPU page, section OpAdd; mul (g*b, g*a)
 // — Operator page, section 逐元素算子; sub (g, -g) and div (g/b, -g*a/b^2) by
 // calculus (the pages do not write them out).  Every single-operation term
@@ -139,18 +115,14 @@ __device__ __forceinline__ void store_cols(float* __restrict__ base, int64_t row
 
 // ---------------------------------------------------------------- functors
 
-// Forward: out = a op b.  For div, r holds RN(1/b) per lane.
+// Forward: out = a op b.
 template <int OP>
 struct FwdF {
   static constexpr bool kR1 = true, kR2 = false;  // slot 0 = a, slot 1 = b
-  static constexpr int kDivSlot = OP == OP_DIV ? 1 : -1;  // input that divides
   template <int VEC>
-  __device__ __forceinline__ void operator()(const Vec<VEC> (&x)[3], const Vec<VEC>& r,
-                                             Vec<VEC> (&y)[2]) const {
+  __device__ __forceinline__ void operator()(const Vec<VEC> (&x)[3], Vec<VEC> (&y)[2]) const {
 #pragma unroll
-    for (int i = 0; i < VEC; ++i)
-      y[0].v[i] = OP == OP_DIV ? div_rn_rcp(x[0].v[i], x[1].v[i], r.v[i])
-                               : fwd_op<OP>(x[0].v[i], x[1].v[i]);
+    for (int i = 0; i < VEC; ++i) y[0].v[i] = fwd_op<OP>(x[0].v[i], x[1].v[i]);
   }
 };
 
@@ -160,10 +132,8 @@ template <int OP, int WANT>
 struct BwdDirectF {
   static constexpr bool kR1 = ((WANT & 1) && Needs<OP, 0>::a) || ((WANT & 2) && Needs<OP, 1>::a);
   static constexpr bool kR2 = ((WANT & 1) && Needs<OP, 0>::b) || ((WANT & 2) && Needs<OP, 1>::b);
-  static constexpr int kDivSlot = -1;  // exact IEEE division per element
   template <int VEC>
-  __device__ __forceinline__ void operator()(const Vec<VEC> (&x)[3], const Vec<VEC>& r,
-                                             Vec<VEC> (&y)[2]) const {
+  __device__ __forceinline__ void operator()(const Vec<VEC> (&x)[3], Vec<VEC> (&y)[2]) const {
 #pragma unroll
     for (int i = 0; i < VEC; ++i) {
       if (WANT & 1) y[0].v[i] = term_a<OP>(x[0].v[i], x[1].v[i], x[2].v[i]);
@@ -175,24 +145,19 @@ struct BwdDirectF {
 // Copy (sum-to-shape onto the same shape).
 struct CopyF {
   static constexpr bool kR1 = false, kR2 = false;
-  static constexpr int kDivSlot = -1;
   template <int VEC>
-  __device__ __forceinline__ void operator()(const Vec<VEC> (&x)[3], const Vec<VEC>& r,
-                                             Vec<VEC> (&y)[2]) const {
+  __device__ __forceinline__ void operator()(const Vec<VEC> (&x)[3], Vec<VEC> (&y)[2]) const {
     y[0] = x[0];
   }
 };
 
 // ---------------------------------------------------------------- elementwise
 
-// One CTA = one tile of rows x column vectors.  Thread (tx, ty) owns column
-// vectors vcol0 + tx, + tx_n, ... and rows ty, ty + ty_n, ... of the tile and
-// walks them columns-fastest with counters; a row's operand offsets are
-// read from the shared table only when the row changes.  Items are loaded U
-// at a time so that U independent loads per operand are in flight before
-// any result is stored.
+// One CTA = one tile of rows x column vectors.  Each thread takes items
+// threadIdx.x + k * 256; items are processed in batches of U so that U
+// independent loads per operand are in flight before any result is stored.
 template <class F, int VEC, int NOUT>
-__global__ void __launch_bounds__(kThreads, 4)
+__global__ void __launch_bounds__(kThreads)
 k_elementwise(const __grid_constant__ EwPlan p) {
   extern __shared__ int64_t s_off[];  // [tile_rows][kMaxOperands]
   const EwTile t = ew_tile(p, blockIdx.x);
@@ -204,81 +169,48 @@ k_elementwise(const __grid_constant__ EwPlan p) {
   }
   __syncthreads();
 
-  // Thread (tx, ty): column vectors vcol0 + tx, + tx_n, ... and a contiguous
-  // run of rows [ty * rpt, ty * rpt + rpt), walked columns-fastest.
-  const uint32_t tx = threadIdx.x & (p.tx - 1);
-  const uint32_t ty = threadIdx.x >> p.tx_shift;
-  const uint32_t ty_n = kThreads >> p.tx_shift;
-  const uint32_t rpt = (t.nrows + ty_n - 1) / ty_n;
-  const uint32_t r_begin = ty * rpt;
-  const uint32_t ncs = t.nvcols > tx ? (t.nvcols - tx + p.tx - 1) >> p.tx_shift : 0;
-  const uint32_t nrs = t.nrows > r_begin ? min(rpt, t.nrows - r_begin) : 0;
-  const uint32_t items = ncs * nrs;
-  const int64_t in0 = p.inner_stride[0], in1 = p.inner_stride[1], in2 = p.inner_stride[2];
-  const int64_t ino = p.inner_stride[kSlotOut];
-  constexpr int kDiv = F::kDivSlot;
-  const int64_t ind = kDiv == 1 ? in1 : in2;
-
   constexpr int U = 4;
   const F f;
-  uint32_t cm = 0;
-  uint32_t row = r_begin;
-  int64_t ro[kMaxOperands];
-#pragma unroll
-  for (int k = 0; k < kMaxOperands; ++k) ro[k] = nrs ? s_off[row * kMaxOperands + k] : 0;
-  // Reciprocal of the divisor, recomputed only when its element changes.
-  int64_t rkey = -1;
-  Vec<VEC> rcp;
-#pragma unroll
-  for (int i = 0; i < VEC; ++i) rcp.v[i] = 1.0f;
-  for (uint32_t m0 = 0; m0 < items; m0 += U) {
+  for (uint32_t it0 = 0; it0 < p.items_per_cta; it0 += U * blockDim.x) {
     Vec<VEC> x[U][3];
-    int64_t doff[U], dkey[U];
+    int64_t doff[U];
     uint32_t col[U];
     bool ok[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      ok[u] = m0 + u < items;
-      col[u] = (t.vcol0 + tx + cm * p.tx) * VEC;
-      doff[u] = ro[kSlotOut];
-      dkey[u] = kDiv >= 0 ? ro[kDiv] + int64_t(col[u]) * ind : 0;
+      const uint32_t item = it0 + u * blockDim.x + threadIdx.x;
+      const uint32_t ri = fd_div(p.tile_vcols_div, item);
+      const uint32_t vc = item - ri * p.tile_vcols;
+      ok[u] = ri < t.nrows && vc < t.nvcols;
+      col[u] = (t.vcol0 + vc) * VEC;
+      doff[u] = 0;
       if (ok[u]) {
-        x[u][0] = load_cols<VEC>(p.in[0], ro[0], in0, col[u], p.stream_mask & 1);
-        if (F::kR1) x[u][1] = load_cols<VEC>(p.in[1], ro[1], in1, col[u], p.stream_mask & 2);
-        if (F::kR2) x[u][2] = load_cols<VEC>(p.in[2], ro[2], in2, col[u], p.stream_mask & 4);
-        if (++cm == ncs) {
-          cm = 0;
-          ++row;
-          if (row < r_begin + nrs) {
-#pragma unroll
-            for (int k = 0; k < kMaxOperands; ++k) ro[k] = s_off[row * kMaxOperands + k];
-          }
-        }
+        const int64_t* ro = s_off + ri * kMaxOperands;
+        x[u][0] = load_cols<VEC>(p.in[0], ro[0], p.inner_stride[0], col[u], p.stream_mask & 1);
+        if (F::kR1) x[u][1] = load_cols<VEC>(p.in[1], ro[1], p.inner_stride[1], col[u], p.stream_mask & 2);
+        if (F::kR2) x[u][2] = load_cols<VEC>(p.in[2], ro[2], p.inner_stride[2], col[u], p.stream_mask & 4);
+        doff[u] = ro[kSlotOut];
       }
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       if (!ok[u]) continue;
-      if (kDiv >= 0 && dkey[u] != rkey) {
-        rkey = dkey[u];
-#pragma unroll
-        for (int i = 0; i < VEC; ++i) rcp.v[i] = __frcp_rn(x[u][kDiv > 0 ? kDiv : 0].v[i]);
-      }
       Vec<VEC> y[2];
-      f(x[u], rcp, y);
-      if (p.out[0]) store_cols<VEC>(p.out[0], doff[u], ino, col[u], y[0]);
-      if (NOUT > 1 && p.out[1]) store_cols<VEC>(p.out[1], doff[u], ino, col[u], y[1]);
+      f(x[u], y);
+      if (p.out[0]) store_cols<VEC>(p.out[0], doff[u], p.inner_stride[kSlotOut], col[u], y[0]);
+      if (NOUT > 1 && p.out[1]) store_cols<VEC>(p.out[1], doff[u], p.inner_stride[kSlotOut], col[u], y[1]);
     }
   }
 }
 
-// Forward with a transposed input (TrPlan): X's tile is read along its
-// unit-stride dim p into shared memory (one 128-byte row per warp access),
-// then read back along q to write the output along its unit-stride dim.
+// Forward with a transposed input (TrPlan): X's tile (kTrP values along its
+// unit-stride dim p x kTrTile along the output's dim q) is read along p with
+// 16-byte loads into shared memory, then read back along q to write the
+// output along its unit-stride dim, both coalesced.
 template <int OP>
 __global__ void __launch_bounds__(kThreads)
 k_transpose(const __grid_constant__ TrPlan p) {
-  __shared__ float tile[kTrTile][kTrTile + 1];  // [q][p], padded: no bank conflicts
+  __shared__ float tile[kTrTile][kTrP + 1];  // [q][p], padded: no bank conflicts
   const uint32_t t1 = fd_div(p.n_qt_div, blockIdx.x);
   const uint32_t qt = blockIdx.x - t1 * p.n_qt;
   const uint32_t bidx = fd_div(p.n_pt_div, t1);
@@ -286,18 +218,83 @@ k_transpose(const __grid_constant__ TrPlan p) {
   int64_t base[kMaxOperands];
   decomp_offsets(p.batch, bidx, base);
   const uint32_t lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  const uint32_t p0 = pt * kTrTile, q0 = qt * kTrTile;
-  for (uint32_t j = w; j < kTrTile; j += kThreads / 32) {
-    const uint32_t q = q0 + j, pp = p0 + lane;
-    if (q < p.nq && pp < p.np) tile[j][lane] = __ldcs(p.x + base[0] + pp + int64_t(q) * p.xs_q);
+  constexpr uint32_t kWarps = kThreads / 32;
+  const uint32_t p0 = pt * kTrP, q0 = qt * kTrTile;
+  const bool full_p = p0 + kTrP <= p.np;
+  if (full_p && p.vec_ok) {
+    float4 v[kTrTile / kWarps];
+#pragma unroll
+    for (uint32_t k = 0; k < kTrTile / kWarps; ++k) {
+      const uint32_t q = q0 + w + k * kWarps;
+      if (q < p.nq)
+        v[k] = __ldcs(reinterpret_cast<const float4*>(p.x + base[0] + p0 + 4 * lane + int64_t(q) * p.xs_q));
+    }
+#pragma unroll
+    for (uint32_t k = 0; k < kTrTile / kWarps; ++k) {
+      const uint32_t j = w + k * kWarps;
+      tile[j][4 * lane + 0] = v[k].x;
+      tile[j][4 * lane + 1] = v[k].y;
+      tile[j][4 * lane + 2] = v[k].z;
+      tile[j][4 * lane + 3] = v[k].w;
+    }
+  } else {
+    for (uint32_t j = w; j < kTrTile; j += kWarps) {
+      const uint32_t q = q0 + j;
+      for (uint32_t l = lane; l < kTrP; l += 32) {
+        const uint32_t pp = p0 + l;
+        if (q < p.nq && pp < p.np) tile[j][l] = __ldcs(p.x + base[0] + pp + int64_t(q) * p.xs_q);
+      }
+    }
   }
   __syncthreads();
-  for (uint32_t i = w; i < kTrTile; i += kThreads / 32) {
-    const uint32_t pp = p0 + i, q = q0 + lane;
-    if (q < p.nq && pp < p.np) {
+  const uint32_t q = q0 + lane;
+  if (q < p.nq) {
+    for (uint32_t i = w; i < kTrP; i += kWarps) {
+      const uint32_t pp = p0 + i;
+      if (pp >= p.np) break;
       const float xv = tile[lane][i];
       const float yv = __ldg(p.y + base[1] + int64_t(pp) * p.ys_p + int64_t(q) * p.ys_q);
       p.out[base[kSlotOut] + int64_t(pp) * p.os_p + q] = p.x_is_a ? fwd_op<OP>(xv, yv) : fwd_op<OP>(yv, xv);
+    }
+  }
+}
+
+// Split forward (SabFPlan): CTA = (tile of a's rows, chunk of betas).
+// Thread (tx, ty) holds a's float4 at column tx for rows ty, ty + lanes, ...
+// and writes them against each beta's b row: one load of b per beta, one
+// operation and one 16-byte store per four outputs.
+template <int OP, int RPT>
+__global__ void __launch_bounds__(kThreads)
+k_sabf(const __grid_constant__ SabFPlan p) {
+  const uint32_t tile = fd_div(p.n_bc_div, blockIdx.x);
+  const uint32_t bc = blockIdx.x - tile * p.n_bc;
+  const uint32_t nvc = p.nvc;
+  const uint32_t nvc_shift = __ffs(nvc) - 1;
+  const uint32_t lanes = kThreads >> nvc_shift;
+  const uint32_t tx = threadIdx.x & (nvc - 1);
+  const uint32_t ty = threadIdx.x >> nvc_shift;
+  int64_t ob[kMaxOperands];
+  decomp_offsets(p.a_outer, tile, ob);
+  float4 areg[RPT];
+  int64_t ooff[RPT];
+#pragma unroll
+  for (int j = 0; j < RPT; ++j) {
+    int64_t ri[kMaxOperands];
+    decomp_offsets(p.a_inner, ty + j * lanes, ri);
+    areg[j] = __ldg(reinterpret_cast<const float4*>(p.a + ob[1] + ri[1] + tx * 4));
+    ooff[j] = ob[0] + ri[0] + tx * 4;
+  }
+  const uint32_t b0 = bc * p.beta_chunk;
+  const uint32_t b1 = min(p.n_beta, b0 + p.beta_chunk);
+  for (uint32_t beta = b0; beta < b1; ++beta) {
+    int64_t bo[kMaxOperands];
+    decomp_offsets(p.beta, beta, bo);
+    const float4 b4 = __ldg(reinterpret_cast<const float4*>(p.b + bo[2] + tx * 4));
+#pragma unroll
+    for (int j = 0; j < RPT; ++j) {
+      const float4 r = make_float4(fwd_op<OP>(areg[j].x, b4.x), fwd_op<OP>(areg[j].y, b4.y),
+                                   fwd_op<OP>(areg[j].z, b4.z), fwd_op<OP>(areg[j].w, b4.w));
+      *reinterpret_cast<float4*>(p.out + ooff[j] + bo[0]) = r;
     }
   }
 }

@@ -11,6 +11,8 @@ namespace zr {
 // dereferences (cudaErrorInvalidValue otherwise); with dry == true it stops
 // there and launches nothing.
 cudaError_t launch_fwd(int op, const EwBuild& eb, cudaStream_t s, bool dry = false);
+// Split forward (each outer dim varies in exactly one input).
+cudaError_t launch_fwd_sabf(int op, int rpt, const SabFPlan& sp, cudaStream_t s, bool dry = false);
 // Forward with a transposed input (shared-memory tile transpose).
 cudaError_t launch_fwd_tr(int op, const TrPlan& tp, cudaStream_t s, bool dry = false);
 // want: bit 0 grad_a, bit 1 grad_b (no reduction).

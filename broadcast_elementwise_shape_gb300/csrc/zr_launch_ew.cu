@@ -41,6 +41,32 @@ cudaError_t launch_fwd(int op, const EwBuild& eb, cudaStream_t s, bool dry) {
   }
 }
 
+namespace {
+template <int OP>
+cudaError_t launch_sabf_op(int rpt, const SabFPlan& sp, cudaStream_t s) {
+  switch (rpt) {
+    case 1: k_sabf<OP, 1><<<sp.n_cta, kThreads, 0, s>>>(sp); break;
+    case 2: k_sabf<OP, 2><<<sp.n_cta, kThreads, 0, s>>>(sp); break;
+    case 4: k_sabf<OP, 4><<<sp.n_cta, kThreads, 0, s>>>(sp); break;
+    case 8: k_sabf<OP, 8><<<sp.n_cta, kThreads, 0, s>>>(sp); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_fwd_sabf(int op, int rpt, const SabFPlan& sp, cudaStream_t s, bool dry) {
+  if (!sp.a || !sp.b || !sp.out || (rpt != 1 && rpt != 2 && rpt != 4 && rpt != 8))
+    return cudaErrorInvalidValue;
+  if (dry) return cudaSuccess;
+  switch (op) {
+    case OP_ADD: return launch_sabf_op<OP_ADD>(rpt, sp, s);
+    case OP_SUB: return launch_sabf_op<OP_SUB>(rpt, sp, s);
+    case OP_MUL: return launch_sabf_op<OP_MUL>(rpt, sp, s);
+    default: return launch_sabf_op<OP_DIV>(rpt, sp, s);
+  }
+}
+
 cudaError_t launch_fwd_tr(int op, const TrPlan& tp, cudaStream_t s, bool dry) {
   if (!tp.x || !tp.y || !tp.out) return cudaErrorInvalidValue;
   if (dry) return cudaSuccess;

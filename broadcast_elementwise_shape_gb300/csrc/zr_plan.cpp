@@ -271,9 +271,6 @@ int build_ew(const Prob& P, const float* const in[3], float* const out[2], uint3
   const uint64_t ncta = ceil_div(nrow, trows) * p.col_tiles;
   if (ncta >= (uint64_t(1) << 31)) return ZR_ERR_SIZE;
   p.n_cta = uint32_t(ncta);
-  p.tx = std::min<uint32_t>(kThreads, pick_tx(tvc));
-  p.tx_shift = 0;
-  while ((1u << p.tx_shift) < p.tx) ++p.tx_shift;
   return ZR_OK;
 }
 
@@ -435,13 +432,16 @@ int build_tr(const Prob& P, const float* a, const float* b, float* out, TrPlan* 
   p.os_p = P.st[kSlotOut][pd];
   p.np = uint32_t(P.size[pd]);
   p.nq = uint32_t(P.size[q]);
-  p.n_pt = uint32_t(ceil_div(p.np, kTrTile));
+  p.n_pt = uint32_t(ceil_div(p.np, kTrP));
   p.n_qt = uint32_t(ceil_div(p.nq, kTrTile));
   p.n_qt_div = make_fastdiv(p.n_qt);
   p.n_pt_div = make_fastdiv(p.n_pt);
   const uint64_t ncta = nbatch * p.n_pt * p.n_qt;
   if (nbatch >= (uint64_t(1) << 32) || ncta >= (uint64_t(1) << 31)) return 1;
   p.n_cta = uint32_t(ncta);
+  bool v = reinterpret_cast<uintptr_t>(p.x) % 16 == 0 && p.xs_q % 4 == 0;
+  for (int i = 0; i < nd; ++i) v = v && p.batch.stride[0][i] % 4 == 0;
+  p.vec_ok = v ? 1 : 0;
   return ZR_OK;
 }
 
@@ -643,6 +643,107 @@ int build_sab(const Prob& P, const float* g, const float* a, const float* b, flo
     c.sy = std::min<uint32_t>(sy, pow2_ceil(c.nslots));
   }
   return ZR_OK;
+}
+
+int build_sabf(const Prob& P, const float* a, const float* b, float* out, SabFPlan* sp, int* rpt) {
+  const int n = P.n;
+  if (n < 2) return 1;
+  const int I = n - 1;
+  // Slots in P: a = 0, b = 1, out = 3.
+  if (P.st[0][I] != 1 || P.st[1][I] != 1 || P.st[kSlotOut][I] != 1) return 1;
+  const uint64_t ncol = uint64_t(P.size[I]);
+  if (ncol % 4 != 0) return 1;
+  const uint64_t nvc = ncol / 4;
+  if (nvc > 32 || (nvc & (nvc - 1)) != 0) return 1;
+  const void* ptrs[3] = {a, b, out};
+  const int slots[3] = {0, 1, kSlotOut};
+  for (int k = 0; k < 3; ++k) {
+    if (reinterpret_cast<uintptr_t>(ptrs[k]) % 16 != 0) return 1;
+    for (int d = 0; d < I; ++d)
+      if (P.st[slots[k]][d] % 4 != 0) return 1;
+  }
+  int adims[kMaxDims], bdims[kMaxDims];
+  int na = 0, nb = 0;
+  uint64_t n_alpha = 1, n_beta = 1;
+  for (int d = 0; d < I; ++d) {
+    const bool va = P.st[0][d] != 0, vb = P.st[1][d] != 0;
+    if (va == vb) return 1;
+    if (va) { adims[na++] = d; n_alpha *= uint64_t(P.size[d]); }
+    else { bdims[nb++] = d; n_beta *= uint64_t(P.size[d]); }
+  }
+  if (na == 0 || nb == 0) return 1;
+  // Rows per tile from the innermost A dims (one of them possibly split),
+  // at most 2048/nvc rows: 256 threads x up to 8 float4 rows each.
+  const uint64_t ta_max = 2048 / nvc;
+  DimSpec inner[kMaxDims + 1], outer[kMaxDims + 1];
+  int n_in = 0, n_out = 0;
+  uint64_t ta = 1;
+  auto spec = [&](int d, uint64_t size, int64_t mult) {
+    return DimSpec{size, {P.st[kSlotOut][d] * mult, P.st[0][d] * mult, P.st[1][d] * mult}};
+  };
+  int i = na - 1;
+  for (; i >= 0; --i) {
+    const int d = adims[i];
+    const uint64_t s = uint64_t(P.size[d]);
+    if (ta * s <= ta_max) { inner[n_in++] = spec(d, s, 1); ta *= s; continue; }
+    uint64_t f = ta_max / ta;
+    while (f > 1 && s % f != 0) --f;
+    if (f > 1) {
+      inner[n_in++] = spec(d, f, 1);
+      outer[n_out++] = spec(d, s / f, int64_t(f));
+      ta *= f;
+    } else {
+      outer[n_out++] = spec(d, s, 1);
+    }
+    --i;
+    break;
+  }
+  for (; i >= 0; --i) outer[n_out++] = spec(adims[i], uint64_t(P.size[adims[i]]), 1);
+  const uint64_t rows_x_vec = ta * nvc;
+  if (rows_x_vec < 256 || rows_x_vec > 2048 || (rows_x_vec & (rows_x_vec - 1)) != 0) return 1;
+  if (n_in > kMaxDims || n_out > kMaxDims) return 1;
+  std::reverse(inner, inner + n_in);
+  std::reverse(outer, outer + n_out);
+  DimSpec beta[kMaxDims];
+  for (int j = 0; j < nb; ++j) {
+    const int d = bdims[j];
+    beta[j] = {uint64_t(P.size[d]), {P.st[kSlotOut][d], 0, P.st[1][d]}};
+  }
+  const uint64_t n_tiles = n_alpha / ta;
+  if (n_tiles >= (uint64_t(1) << 31) || n_beta >= (uint64_t(1) << 31)) return 1;
+  SabFPlan& p = *sp;
+  p = SabFPlan{};
+  p.a = a;
+  p.b = b;
+  p.out = out;
+  fill_from_specs(&p.a_outer, outer, n_out);
+  fill_from_specs(&p.a_inner, inner, n_in);
+  fill_from_specs(&p.beta, beta, nb);
+  p.ncol = uint32_t(ncol);
+  p.nvc = uint32_t(nvc);
+  p.ta = uint32_t(ta);
+  p.n_tiles = uint32_t(n_tiles);
+  p.n_beta = uint32_t(n_beta);
+  // About 512 KB written per CTA, and at least ~8 CTAs per SM in total.
+  uint64_t chunk = std::max<uint64_t>(1, (512 * 1024) / (ta * ncol * 4));
+  while (chunk > 1 && n_tiles * ceil_div(n_beta, chunk) < 1216) chunk /= 2;
+  p.beta_chunk = uint32_t(std::min<uint64_t>(chunk, n_beta));
+  p.n_bc = uint32_t(ceil_div(n_beta, p.beta_chunk));
+  p.n_bc_div = make_fastdiv(p.n_bc);
+  const uint64_t ncta = n_tiles * p.n_bc;
+  if (ncta >= (uint64_t(1) << 31)) return 1;
+  p.n_cta = uint32_t(ncta);
+  *rpt = int(rows_x_vec / 256);
+  return ZR_OK;
+}
+
+std::string describe_sabf(const SabFPlan& p, int rpt) {
+  char buf[512];
+  std::snprintf(buf, sizeof(buf),
+                "{\"kernel\":\"sab_fwd\",\"ncol\":%u,\"ta\":%u,\"rpt\":%d,\"n_tiles\":%u,"
+                "\"n_beta\":%u,\"beta_chunk\":%u,\"ctas\":%u}",
+                p.ncol, p.ta, rpt, p.n_tiles, p.n_beta, p.beta_chunk, p.n_cta);
+  return buf;
 }
 
 std::string describe_sab(const SabBuild& sb) {

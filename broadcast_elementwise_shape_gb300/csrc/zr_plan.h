@@ -93,6 +93,11 @@ struct SabBuild {
 int build_sab(const Prob& P, const float* g, const float* a, const float* b, float* grad_a,
               float* grad_b, uint32_t read_mask, SabBuild* sb);
 
+// Split forward plan (SabFPlan); ZR_OK when the layout qualifies, 1 if not.
+// Slots of P: 0 = a, 1 = b, 3 = out.
+int build_sabf(const Prob& P, const float* a, const float* b, float* out, SabFPlan* sp, int* rpt);
+std::string describe_sabf(const SabFPlan& sp, int rpt);
+
 std::string describe_ew(const EwBuild& eb);
 std::string describe_sab(const SabBuild& sb);
 std::string describe_red(const RedBuild& rb);

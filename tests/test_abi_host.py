@@ -287,7 +287,7 @@ def test_plan_dispatch_for_workloads(L):
     d = fwd((128, 256, 512), (1, 256, 1), sta=(131072, 1, 256))
     assert d["kernel"] == "transpose" and d["xs_q"] == 256 and (d["np"], d["nq"]) == (256, 512)
     d = fwd((4, 1, 8, 1, 16, 1, 32, 64), (1, 6, 1, 12, 1, 10, 1, 64))
-    assert d["row_dims"] == 7 and d["ncol"] == 64 and d["vec"] == 4
+    assert d["kernel"] == "sab_fwd" and (d["ta"], d["n_tiles"], d["n_beta"]) == (128, 128, 720)
     d = bwd(0, (4096, 1024), (1024,))
     (p,) = d["plans"]
     assert p["kernel"] == "reduce" and p["inner_kept"] == 1 and p["dense_out"] == 1
@@ -384,6 +384,32 @@ SAB_CASES = [
     ((8, 1, 64, 1, 32), (1, 5, 1, 7, 32)),     # split A dim, 2 tiles, many CTAs per tile
     ((3, 1, 16, 1, 8, 1, 64), (1, 4, 1, 5, 1, 3, 64)),
 ]
+
+
+def test_emulated_split_forward(L):
+    """Forward shapes whose outer dims each vary in one input take the split
+    kernel; its host walk must write every output once from the right a and b."""
+    T = 1 << 40
+    for sa, sb in SAB_CASES + [((2, 1, 4, 1, 8, 1, 32, 64), (1, 3, 1, 4, 1, 5, 1, 64))]:
+        out_shape = tuple(np.broadcast_shapes(sa, sb))
+        n_out = int(np.prod(out_shape))
+        a, b = FakeT(T, sa), FakeT(2 * T, sb)
+        buf = ctypes.create_string_buffer(4096)
+        assert L.zr_test_describe_fwd(3, a.desc, b.desc, 3 * T, None, buf, 4096) == 0
+        assert json.loads(buf.value.decode())["kernel"] == "sab_fwd"
+        cap = n_out + 8
+        rec = (ctypes.c_int64 * (3 * cap))()
+        nrec = ctypes.c_int64()
+        assert L.zr_test_emulate_fwd(a.desc, b.desc, 3 * T, None, cap, rec, ctypes.byref(nrec)) == 0
+        r = np.frombuffer(rec, np.int64)[: 3 * nrec.value].reshape(-1, 3)
+        assert r.shape[0] == n_out
+        o = naive_offsets(out_shape, out_shape, dense_strides(out_shape)).ravel()
+        ao = naive_offsets(out_shape, sa, a.strides).ravel()
+        bo = naive_offsets(out_shape, sb, b.strides).ravel()
+        order, ref = np.argsort(r[:, 0]), np.argsort(o)
+        np.testing.assert_array_equal(r[order, 0], o[ref])
+        np.testing.assert_array_equal(r[order, 1], ao[ref])
+        np.testing.assert_array_equal(r[order, 2], bo[ref])
 
 
 @pytest.mark.parametrize("op", [0, 1, 2, 3])

@@ -366,6 +366,8 @@ def test_both_reduced_fused_pass(op):
         a = torch.from_numpy(rng.standard_normal(sa).astype(np.float32))
         b = torch.from_numpy((np.sign(rng.standard_normal(sb)) * (0.5 + rng.random(sb))).astype(np.float32))
         g = torch.from_numpy(rng.standard_normal(np.broadcast_shapes(sa, sb)).astype(np.float32))
+        out = zr.zr_binary_fwd(op, a.cuda(), b.cuda()).cpu().numpy()
+        bitexact(out, oracle.binary_fwd(op, a, b), f"split fwd {op} {sa} {sb}")
         ga, gb = zr.zr_binary_bwd(op, g.cuda(), a.cuda(), b.cuda())
         ra, rb, s1, s2 = oracle.binary_bwd(op, g, a, b)
         within(ga.cpu().numpy(), ra, s1, f"fused {op} grad_a {sa} {sb}")
