@@ -63,6 +63,14 @@ struct Kahan {
     c = __fsub_rn(__fsub_rn(t, s), y);
     s = t;
   }
+  // Adds the exact product u*v: the FMA forms u*v - c with one rounding, so
+  // the summed term carries no product rounding error.
+  __device__ __forceinline__ void add_prod(float u, float v) {
+    const float y = __fmaf_rn(u, v, -c);
+    const float t = __fadd_rn(s, y);
+    c = __fsub_rn(__fsub_rn(t, s), y);
+    s = t;
+  }
 };
 
 // ---------------------------------------------------------------- loads/stores
@@ -318,16 +326,19 @@ struct RedTerms {
   static constexpr bool kDb = WHICH < 2 && Needs<OP, 1 - WHICH>::b;
   // Summed terms need not be single IEEE operations (the sum is within
   // tolerance, not bit-exact): div's g/b is taken as g * (1/b).
-  __device__ __forceinline__ static float x(float g, float a, float b) {
+  // X's term is g * m(a, b); the kernel adds the product through an FMA.
+  __device__ __forceinline__ static float m(float a, float b) {
     if (WHICH == 0) {
-      if (OP == OP_DIV) return __fmul_rn(g, __frcp_rn(b));
-      return term_a<OP>(g, a, b);
+      if (OP == OP_MUL) return b;
+      if (OP == OP_DIV) return __frcp_rn(b);
+      return 1.0f;
     }
     if (WHICH == 1) {
-      if (OP == OP_DIV) return __fmul_rn(g, a);
-      return term_b<OP>(g, a, b);
+      if (OP == OP_SUB) return -1.0f;
+      if (OP == OP_MUL || OP == OP_DIV) return a;
+      return 1.0f;
     }
-    return g;
+    return 1.0f;
   }
   __device__ __forceinline__ static float post(float b) {
     const float r = __frcp_rn(b);
@@ -431,8 +442,8 @@ k_reduce(const __grid_constant__ RedPlan p) {
           const float gg = gv[u].v[i];
           const float aa = ((T::kXa || T::kDa) && read_a) ? av[u].v[i] : 0.f;
           const float bb = ((T::kXb || T::kDb) && read_b) ? bv[u].v[i] : 0.f;
-          if (INNER_KEPT) acc[i].add(T::x(gg, aa, bb));
-          else acc[0].add(T::x(gg, aa, bb));
+          if (INNER_KEPT) acc[i].add_prod(gg, T::m(aa, bb));
+          else acc[0].add_prod(gg, T::m(aa, bb));
           if (has_d) dv.v[i] = T::d(gg, aa, bb);
         }
         if (has_d) store_cols<VEC>(p.d_out, s_off[ri[u] * kMaxOperands + kSlotOut], 1, cc[u], dv);

@@ -9,6 +9,8 @@
 // b's, grad_out is g[alpha, beta, col] and
 //   grad_a[alpha, col] = sum_beta  g * ca(beta, col)
 //   grad_b[beta, col]  = sb(beta, col) * sum_alpha g * cb(alpha, col)
+// (each product enters its sum through an FMA, so it is never rounded on
+// its own)
 // where (ca, cb, sb) = (1, 1, 1) add, (1, 1, -1) sub, (b, a, 1) mul,
 // (1/b, a, -1/b^2) div — the local terms of add (GPU page, section OpAdd),
 // mul (Operator page, section 逐元素算子) and the calculus rules for sub/div,
@@ -205,12 +207,12 @@ k_sab(const __grid_constant__ SabPlan p) {
         sb.x = __fadd_rn(sb.x, g4.x); sb.y = __fadd_rn(sb.y, g4.y);
         sb.z = __fadd_rn(sb.z, g4.z); sb.w = __fadd_rn(sb.w, g4.w);
       } else {
-        acc[j][0].add(__fmul_rn(g4.x, ca.x)); acc[j][1].add(__fmul_rn(g4.y, ca.y));
-        acc[j][2].add(__fmul_rn(g4.z, ca.z)); acc[j][3].add(__fmul_rn(g4.w, ca.w));
-        sb.x = __fadd_rn(sb.x, __fmul_rn(g4.x, areg[j].x));
-        sb.y = __fadd_rn(sb.y, __fmul_rn(g4.y, areg[j].y));
-        sb.z = __fadd_rn(sb.z, __fmul_rn(g4.z, areg[j].z));
-        sb.w = __fadd_rn(sb.w, __fmul_rn(g4.w, areg[j].w));
+        acc[j][0].add_prod(g4.x, ca.x); acc[j][1].add_prod(g4.y, ca.y);
+        acc[j][2].add_prod(g4.z, ca.z); acc[j][3].add_prod(g4.w, ca.w);
+        sb.x = __fmaf_rn(g4.x, areg[j].x, sb.x);
+        sb.y = __fmaf_rn(g4.y, areg[j].y, sb.y);
+        sb.z = __fmaf_rn(g4.z, areg[j].z, sb.z);
+        sb.w = __fmaf_rn(g4.w, areg[j].w, sb.w);
       }
     }
     // Lanes of a warp that share tx hold different rows: butterfly over them.
