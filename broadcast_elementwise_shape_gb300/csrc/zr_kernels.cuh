@@ -127,6 +127,7 @@ __device__ __forceinline__ void store_cols(float* __restrict__ base, int64_t row
 template <int OP>
 struct FwdF {
   static constexpr bool kR1 = true, kR2 = false;  // slot 0 = a, slot 1 = b
+  static constexpr int kMinBlocks = 4;  // CTAs per SM the register budget targets
   template <int VEC>
   __device__ __forceinline__ void operator()(const Vec<VEC> (&x)[3], Vec<VEC> (&y)[2]) const {
 #pragma unroll
@@ -140,6 +141,7 @@ template <int OP, int WANT>
 struct BwdDirectF {
   static constexpr bool kR1 = ((WANT & 1) && Needs<OP, 0>::a) || ((WANT & 2) && Needs<OP, 1>::a);
   static constexpr bool kR2 = ((WANT & 1) && Needs<OP, 0>::b) || ((WANT & 2) && Needs<OP, 1>::b);
+  static constexpr int kMinBlocks = 3;
   template <int VEC>
   __device__ __forceinline__ void operator()(const Vec<VEC> (&x)[3], Vec<VEC> (&y)[2]) const {
 #pragma unroll
@@ -153,6 +155,7 @@ struct BwdDirectF {
 // Copy (sum-to-shape onto the same shape).
 struct CopyF {
   static constexpr bool kR1 = false, kR2 = false;
+  static constexpr int kMinBlocks = 4;
   template <int VEC>
   __device__ __forceinline__ void operator()(const Vec<VEC> (&x)[3], Vec<VEC> (&y)[2]) const {
     y[0] = x[0];
@@ -165,7 +168,7 @@ struct CopyF {
 // threadIdx.x + k * 256; items are processed in batches of U so that U
 // independent loads per operand are in flight before any result is stored.
 template <class F, int VEC, int NOUT>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, F::kMinBlocks)
 k_elementwise(const __grid_constant__ EwPlan p) {
   extern __shared__ int64_t s_off[];  // [tile_rows][kMaxOperands]
   const EwTile t = ew_tile(p, blockIdx.x);
@@ -363,7 +366,7 @@ struct RedTerms {
 // with a fixed tree.  Per-thread sums are Kahan-compensated, so the error
 // bound does not grow with the number of rows a thread adds.
 template <int OP, int WHICH, int VEC, bool INNER_KEPT>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 3)
 k_reduce(const __grid_constant__ RedPlan p) {
   using T = RedTerms<OP, WHICH>;
   extern __shared__ int64_t s_dyn[];
@@ -393,6 +396,19 @@ k_reduce(const __grid_constant__ RedPlan p) {
   // Column vectors this thread owns in the block (one when the inner dim is
   // kept: vcols_per_blk == tx).
   const uint32_t ncs = vcol_end > vcol_begin + tx ? (vcol_end - vcol_begin - tx + p.tx - 1) / p.tx : 0;
+  // The input of the gradient being reduced (a for grad_a, b for grad_b) is
+  // broadcast along every reduced dim, so its value depends only on the kept
+  // index and, when the inner dim is kept, the column: load it once.
+  Vec<VEC> own;
+#pragma unroll
+  for (int i = 0; i < VEC; ++i) own.v[i] = 0.f;
+  if (WHICH < 2 && ncs > 0) {
+    const int slot = WHICH == 0 ? 1 : 2;
+    const bool needed = WHICH == 0 ? ((T::kXa || T::kDa) && read_a) : ((T::kXb || T::kDb) && read_b);
+    if (needed)
+      own = load_cols<VEC>(WHICH == 0 ? p.a : p.b, base[slot], p.inner_stride[slot],
+                           (vcol_begin + tx) * VEC, false);
+  }
 
   for (uint32_t ch0 = 0; ch0 < nrows; ch0 += kMaxTileRows) {
     const uint32_t cleft = nrows - ch0;
@@ -426,9 +442,9 @@ k_reduce(const __grid_constant__ RedPlan p) {
         if (ok[u]) {
           const int64_t* ro = s_off + ri[u] * kMaxOperands;
           gv[u] = load_cols<VEC>(p.g, ro[0], p.inner_stride[0], cc[u], p.stream_mask & 1);
-          if ((T::kXa || T::kDa) && read_a)
+          if ((T::kXa || T::kDa) && read_a && WHICH != 0)
             av[u] = load_cols<VEC>(p.a, ro[1], p.inner_stride[1], cc[u], p.stream_mask & 2);
-          if ((T::kXb || T::kDb) && read_b)
+          if ((T::kXb || T::kDb) && read_b && WHICH != 1)
             bv[u] = load_cols<VEC>(p.b, ro[2], p.inner_stride[2], cc[u], p.stream_mask & 4);
           if (++cm == ncs) { cm = 0; ++rm; }
         }
@@ -440,8 +456,8 @@ k_reduce(const __grid_constant__ RedPlan p) {
 #pragma unroll
         for (int i = 0; i < VEC; ++i) {
           const float gg = gv[u].v[i];
-          const float aa = ((T::kXa || T::kDa) && read_a) ? av[u].v[i] : 0.f;
-          const float bb = ((T::kXb || T::kDb) && read_b) ? bv[u].v[i] : 0.f;
+          const float aa = ((T::kXa || T::kDa) && read_a) ? (WHICH == 0 ? own.v[i] : av[u].v[i]) : 0.f;
+          const float bb = ((T::kXb || T::kDb) && read_b) ? (WHICH == 1 ? own.v[i] : bv[u].v[i]) : 0.f;
           if (INNER_KEPT) acc[i].add_prod(gg, T::m(aa, bb));
           else acc[0].add_prod(gg, T::m(aa, bb));
           if (has_d) dv.v[i] = T::d(gg, aa, bb);
