@@ -49,6 +49,7 @@ WORKLOAD_DESC = ("five-workload suite c1..c5b (c1 mul [32,64,128]x[64,1]; c2 bia
                  "[8,12,1024,1024]; c5a transposed-view sub [128,256,512]-[1,256,1]; c5b 8-d div "
                  "to [4,6,8,12,16,10,32,64]) fwd+bwd")
 KERNEL_SOURCES = ["broadcast_elementwise_shape_gb300/csrc/zr_kernels.cuh",
+                  "broadcast_elementwise_shape_gb300/csrc/zr_sab.cuh",
                   "broadcast_elementwise_shape_gb300/csrc/zr_internal.h",
                   "broadcast_elementwise_shape_gb300/csrc/zr_plan.cpp"]
 
@@ -468,8 +469,9 @@ def run_e2e(args, suite, flush, stream, nbytes):
 
 
 def read_traffic(call):
-    """DRAM bytes per launch of the dominant op from the committed ncu
-    summary, if it was taken on the current kernel sources."""
+    """DRAM bytes (read + write, summed over the op's launches) of the
+    dominant op from the committed ncu summary (profiles/traffic.json), if
+    it was taken on the current kernel sources; otherwise None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:

@@ -366,7 +366,7 @@ struct RedTerms {
 // with a fixed tree.  Per-thread sums are Kahan-compensated, so the error
 // bound does not grow with the number of rows a thread adds.
 template <int OP, int WHICH, int VEC, bool INNER_KEPT>
-__global__ void __launch_bounds__(kThreads, 3)
+__global__ void __launch_bounds__(kThreads, (OP == OP_MUL || OP == OP_DIV) ? 3 : 4)
 k_reduce(const __grid_constant__ RedPlan p) {
   using T = RedTerms<OP, WHICH>;
   extern __shared__ int64_t s_dyn[];

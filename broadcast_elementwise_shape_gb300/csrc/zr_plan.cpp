@@ -47,6 +47,22 @@ uint32_t pick_tx(uint64_t nvcol) {
   return best;
 }
 
+// Thread layout of the combine pass: jx outputs x sy slot lanes (powers of
+// two, jx * sy = 256).  Few slots: one output per thread, summed serially
+// (no tree).  Many slots: 32 consecutive outputs per row of lanes (coalesced
+// 128-byte loads) and 8 slot lanes, unless there are fewer than 32 outputs,
+// where the lanes go to the slots.
+void combine_layout(CombinePlan* c) {
+  uint32_t jx;
+  if (c->nslots <= 16) jx = kThreads;
+  else if (c->nout >= 32) jx = 32;
+  else jx = pow2_ceil(c->nout);
+  if (jx > kThreads) jx = kThreads;
+  const uint32_t sy_max = kThreads / jx;
+  c->jx = jx;
+  c->sy = std::min<uint32_t>(sy_max, pow2_ceil(c->nslots));
+}
+
 void fill_decomp(Decomp* dc, const Prob& P, const int* dims, int nd) {
   // dims: outer dims in row-major order; the decomposition is innermost first.
   dc->n = nd;
@@ -376,16 +392,7 @@ int build_red(const Prob& P, int xslot, const float* g, const float* a, const fl
   c.nslots = p.nslots;
   c.out = x_out;
   c.scale = 1.0f;
-  uint32_t sy = std::min<uint32_t>(kThreads, pow2_ceil(p.nslots));
-  if (p.nout >= 64 * 1024) sy = std::min<uint32_t>(sy, 4);
-  else if (p.nout >= 4096) sy = std::min<uint32_t>(sy, 32);
-  uint32_t jx = kThreads / sy;
-  if (p.nout < jx) {
-    jx = pow2_ceil(p.nout);
-    sy = kThreads / jx;
-  }
-  c.jx = jx;
-  c.sy = std::min<uint32_t>(sy, pow2_ceil(p.nslots));
+  combine_layout(&c);
   return ZR_OK;
 }
 
@@ -631,16 +638,7 @@ int build_sab(const Prob& P, const float* g, const float* a, const float* b, flo
     c.nslots = nsl[w];
     c.out = outs[w];
     c.scale = 1.0f;
-    uint32_t sy = std::min<uint32_t>(kThreads, pow2_ceil(c.nslots));
-    if (c.nout >= 64 * 1024) sy = std::min<uint32_t>(sy, 4);
-    else if (c.nout >= 4096) sy = std::min<uint32_t>(sy, 32);
-    uint32_t jx = kThreads / sy;
-    if (c.nout < jx) {
-      jx = pow2_ceil(c.nout);
-      sy = kThreads / jx;
-    }
-    c.jx = jx;
-    c.sy = std::min<uint32_t>(sy, pow2_ceil(c.nslots));
+    combine_layout(&c);
   }
   return ZR_OK;
 }
