@@ -414,9 +414,6 @@ int launch_bwd_set(const BwdSet& S, int op, void* workspace, cudaStream_t st, bo
     SabBuild sb = S.sb;
     sb.plan.ws_a = static_cast<float*>(workspace);
     sb.plan.ws_b = reinterpret_cast<float*>(static_cast<char*>(workspace) + sb.ws_a_bytes);
-    // The last 256 bytes of grad_b's region hold the pipeline status word.
-    sb.plan.status = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + sb.ws_a_bytes +
-                                                sb.ws_b_bytes - 256);
     return cuda_status(launch_sab(op, sb, st, dry));
   }
   for (int i = 0; i < S.nred; ++i) {

@@ -231,8 +231,6 @@ struct SabPlan {
   uint32_t slots_a;         // grad_a partial slots (max CTAs covering a tile)
   uint64_t n_a, n_b;        // elements of grad_a / grad_b
   uint32_t smem_bytes;
-  uint32_t run_rows;        // tile rows that are contiguous in g (one bulk copy each run)
-  int32_t* status;          // set to 1 by a CTA whose pipeline wait timed out
 };
 
 // Forward for the same split (every outer dim varies in exactly one input,
@@ -254,9 +252,8 @@ struct SabFPlan {
   uint32_t n_cta;
 };
 
-constexpr int kSabStages = 4;
+constexpr int kSabStages = 5;
 constexpr int kSabThreads = 512;
-constexpr int kSabFold = 16;  // steps between folds of the plain sums into Kahan totals
 constexpr uint32_t kSabGrid = 152;  // one CTA per SM of a GB300; fixed so that
                                     // the partition depends on the shape only
 

@@ -11,12 +11,10 @@ template <int OP, int RPT>
 cudaError_t launch_sab_t(const SabBuild& sb, cudaStream_t s, bool dry) {
   const SabPlan& p = sb.plan;
   constexpr bool kUses = OP == OP_MUL || OP == OP_DIV;
-  if (!p.g || (kUses && (!p.a || !p.b)) || !p.ws_a || !p.ws_b || !p.status || !sb.comb_a.out ||
+  if (!p.g || (kUses && (!p.a || !p.b)) || !p.ws_a || !p.ws_b || !sb.comb_a.out ||
       !sb.comb_b.out)
     return cudaErrorInvalidValue;
   if (dry) return cudaSuccess;
-  cudaError_t z = cudaMemsetAsync(p.status, 0, sizeof(int32_t), s);
-  if (z != cudaSuccess) return z;
   cudaError_t e = cudaFuncSetAttribute(k_sab<OP, RPT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        int(p.smem_bytes));
   if (e != cudaSuccess) return e;

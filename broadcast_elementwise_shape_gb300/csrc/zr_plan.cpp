@@ -620,28 +620,13 @@ int build_sab(const Prob& P, const float* g, const float* a, const float* b, flo
     smax = std::max(smax, c1 - c0 + 1);
   }
   p.slots_a = smax;
-  // Rows of a tile that sit back to back in g: the innermost A-inner dims
-  // whose g stride continues the previous run.  Each run is one bulk copy.
-  uint64_t run = 1;
-  int64_t want = int64_t(ncol);
-  for (int j = n_in - 1; j >= 0; --j) {
-    if (inner[j].st[0] != want) break;
-    run *= inner[j].size;
-    want *= int64_t(inner[j].size);
-  }
-  p.run_rows = uint32_t(run);
-  const uint64_t rpt_n = rows_x_vec / kSabThreads;
-  const uint64_t smem = uint64_t(kSabStages) * (ta + 1) * ncol * 4   // stages: tile + b row
-                        + uint64_t(kSabThreads) * rpt_n * 4 * 2 * 4  // Kahan sums + compensations
-                        + 2 * ta * 8 + 2 * n_beta * 8                  // row and beta offsets
-                        + 2 * (kSabThreads / 32) * ncol * 4            // grad_b warp partials
-                        + kSabStages * 8;                              // stage barriers
-  if (smem > 225 * 1024) return 1;
+  const uint64_t smem = uint64_t(kSabStages) * (ta + 1) * ncol * 4 + 2 * ta * 8 +
+                        2 * n_beta * 8 + 2 * (kSabThreads / 32) * ncol * 4;
+  if (smem > 220 * 1024) return 1;
   p.smem_bytes = uint32_t(smem);
   sb->rpt = int(rows_x_vec / kSabThreads);
   sb->ws_a_bytes = ((uint64_t(p.slots_a) * p.n_a * 4 + 255) / 256) * 256;
-  // grad_b's partials, then 256 bytes holding the pipeline status word.
-  sb->ws_b_bytes = ((uint64_t(p.n_tiles) * p.n_b * 4 + 255) / 256) * 256 + 256;
+  sb->ws_b_bytes = ((uint64_t(p.n_tiles) * p.n_b * 4 + 255) / 256) * 256;
   CombinePlan* cs[2] = {&sb->comb_a, &sb->comb_b};
   const uint64_t nouts[2] = {p.n_a, p.n_b};
   const uint32_t nsl[2] = {p.slots_a, p.n_tiles};
@@ -766,11 +751,10 @@ std::string describe_sab(const SabBuild& sb) {
                 "{\"kernel\":\"sab\",\"ncol\":%u,\"ta\":%u,\"rpt\":%d,\"n_tiles\":%u,"
                 "\"n_beta\":%u,\"grid\":%u,\"slots_a\":%u,\"slots_b\":%u,\"n_a\":%llu,"
                 "\"n_b\":%llu,\"ws_bytes\":%zu,\"smem\":%u,\"outer_dims\":%d,\"inner_dims\":%d,"
-                "\"beta_dims\":%d,\"run_rows\":%u}",
+                "\"beta_dims\":%d}",
                 p.ncol, p.ta, sb.rpt, p.n_tiles, p.n_beta, p.grid, p.slots_a, p.n_tiles,
                 (unsigned long long)p.n_a, (unsigned long long)p.n_b,
-                sb.ws_a_bytes + sb.ws_b_bytes, p.smem_bytes, p.a_outer.n, p.a_inner.n, p.beta.n,
-                p.run_rows);
+                sb.ws_a_bytes + sb.ws_b_bytes, p.smem_bytes, p.a_outer.n, p.a_inner.n, p.beta.n);
   return buf;
 }
 

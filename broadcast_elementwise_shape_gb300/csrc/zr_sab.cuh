@@ -18,10 +18,9 @@
 //
 // Persistent grid; each CTA walks a contiguous range of steps (tile, beta).
 // A step's tile (ta rows x ncol floats, typically 32 KB) and b's row for
-// that beta are staged into shared memory by TMA bulk copies (one per run of
-// rows contiguous in g) through a kSabStages-deep ring of stage barriers,
-// so several tiles' loads are in flight while the previous one is summed and
-// no load sits on the per-step critical path.
+// that beta are staged into shared memory by cp.async through a
+// kSabStages-deep pipeline, so several tiles' loads are in flight while the
+// previous one is summed and no load sits on the per-step critical path.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -30,57 +29,21 @@
 
 namespace zr {
 
-// ---- TMA bulk copies and stage barriers (inline PTX, sm_90 and later) ----
-
-__device__ __forceinline__ uint32_t smem_addr(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc) {
+  const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gsrc) : "memory");
 }
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_addr(bar)), "r"(count)
-               : "memory");
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;\n" ::: "memory");
 }
-// Make barrier initialisation visible to the async (bulk copy) proxy.
-__device__ __forceinline__ void mbar_init_fence() {
-  asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
-}
-// Order this thread's earlier generic shared-memory accesses before later
-// bulk copies into the same memory.
-__device__ __forceinline__ void fence_proxy_async() {
-  asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-}
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
-  uint64_t state;
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 %0, [%1], %2;\n"
-               : "=l"(state) : "r"(smem_addr(bar)), "r"(bytes) : "memory");
-  (void)state;
-}
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t done;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-      " selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(done) : "r"(smem_addr(bar)), "r"(parity) : "memory");
-  return done != 0;
-}
-// Bounded wait for the phase of parity `parity` to complete.  Returns false
-// if it did not within the limit (each try_wait may itself suspend a while),
-// so a broken pipeline ends the kernel instead of hanging the GPU.
-constexpr uint32_t kWaitLimit = 1u << 22;
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kWaitLimit; ++i)
-    if (mbar_try_wait(bar, parity)) return true;
-  return false;
-}
-// Bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned)
-// from global to this CTA's shared memory, completing on `bar`.
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n"
-      ::"r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar)) : "memory");
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
 }
 
-// The factor of b applied per element to grad_a's term, staged as a row of
-// shared memory one step ahead: 1/b for div, b for mul.
+// The factor of b applied per element to grad_a's term is staged as a row
+// of shared memory one step ahead: for div the row holds 1/b (so the per
+// element work is one multiply), for mul it holds b.
 template <int OP>
 __device__ __forceinline__ float sab_row(float bv) {
   return OP == OP_DIV ? __frcp_rn(bv) : bv;
@@ -91,28 +54,6 @@ __device__ __forceinline__ float sab_scale(float rv) {
   if (OP == OP_SUB) return -1.0f;
   if (OP == OP_DIV) return -__fmul_rn(rv, rv);
   return 1.0f;
-}
-
-// grad_a accumulation: each thread adds one term per step per element into
-// a plain register sum (an FMA), and every kSabFold steps folds those sums
-// into Kahan totals kept in shared memory; error <= (kSabFold + 2) u
-// sum|terms|, however many steps a thread covers.
-template <int RPT>
-__device__ __forceinline__ void sab_fold(float4 (&blk)[RPT], float* ks, float* kc, uint32_t tid) {
-#pragma unroll
-  for (int j = 0; j < RPT; ++j) {
-    const float v[4] = {blk[j].x, blk[j].y, blk[j].z, blk[j].w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint32_t idx = (j * 4 + i) * kSabThreads + tid;
-      const float c = kc[idx], s = ks[idx];
-      const float y = __fsub_rn(v[i], c);
-      const float t = __fadd_rn(s, y);
-      kc[idx] = __fsub_rn(__fsub_rn(t, s), y);
-      ks[idx] = t;
-    }
-    blk[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-  }
 }
 
 template <int OP, int RPT>
@@ -127,13 +68,9 @@ k_sab(const __grid_constant__ SabPlan p) {
   const uint32_t tile_floats = p.ta * p.ncol;
   const uint32_t stage_floats = tile_floats + p.ncol;
   float* s_stage = reinterpret_cast<float*>(s_raw);
-  float* s_ks = s_stage + kSabStages * stage_floats;               // [RPT*4][threads]
-  float* s_kc = s_ks + RPT * 4 * kSabThreads;                      // [RPT*4][threads]
-  int64_t* s_row = reinterpret_cast<int64_t*>(s_kc + RPT * 4 * kSabThreads);  // [ta][2]
-  int64_t* s_beta = s_row + 2 * p.ta;                                         // [n_beta][2]
-  float* s_sb = reinterpret_cast<float*>(s_beta + 2 * p.n_beta);              // [2][warps][ncol]
-  uint64_t* s_bar = reinterpret_cast<uint64_t*>(s_sb + 2 * kWarps * p.ncol);  // [stages]
-  __shared__ int s_abort;
+  int64_t* s_row = reinterpret_cast<int64_t*>(s_stage + kSabStages * stage_floats);  // [ta][2]
+  int64_t* s_beta = s_row + 2 * p.ta;                                                 // [n_beta][2]
+  float* s_sb = reinterpret_cast<float*>(s_beta + 2 * p.n_beta);                      // [2][warps][ncol]
 
   const uint32_t tid = threadIdx.x;
   for (uint32_t i = tid; i < p.ta; i += blockDim.x) {
@@ -148,15 +85,6 @@ k_sab(const __grid_constant__ SabPlan p) {
     s_beta[2 * i] = off[0];
     s_beta[2 * i + 1] = off[2];
   }
-  for (uint32_t i = tid; i < RPT * 4 * kSabThreads; i += blockDim.x) {
-    s_ks[i] = 0.f;
-    s_kc[i] = 0.f;
-  }
-  if (tid == 0) {
-    for (int st = 0; st < kSabStages; ++st) mbar_init(&s_bar[st], 1);
-    mbar_init_fence();
-    s_abort = 0;
-  }
   __syncthreads();
 
   const uint32_t cta = blockIdx.x;
@@ -168,38 +96,41 @@ k_sab(const __grid_constant__ SabPlan p) {
   const uint32_t tx = tid & (nvc - 1);
   const uint32_t ty = tid >> nvc_shift;
   const uint32_t warp = tid >> 5, lane = tid & 31;
-  const uint32_t run_bytes = p.run_rows * p.ncol * 4;
-  const uint32_t n_runs = p.ta / p.run_rows;
-  const uint32_t step_bytes = tile_floats * 4 + (kUsesB ? p.ncol * 4 : 0);
 
-  // Warp 0 stages step `step` into `stage`: lane 0 arms the stage barrier
-  // with the byte count, then the lanes issue one bulk copy per row run and
-  // one for b's row.
+  // This thread's RPT 16-byte chunks of every tile: fixed rows and columns,
+  // so their source offsets (within a tile) and destinations are fixed too.
+  int64_t chunk_src[RPT];
+  uint32_t chunk_dst[RPT];
+#pragma unroll
+  for (int k = 0; k < RPT; ++k) {
+    const uint32_t id = tid + k * kSabThreads;
+    const uint32_t row = id >> nvc_shift;
+    const uint32_t c4 = id & (nvc - 1);
+    chunk_src[k] = s_row[2 * row] + c4 * 4;
+    chunk_dst[k] = row * p.ncol + c4 * 4;
+  }
   uint32_t iss_tile = 0xffffffffu;
   int64_t iss_base = 0;
+
+  // Stage the tile (and b's row) of `step` if in range; close one group.
   auto issue = [&](uint64_t step, uint32_t stage) {
-    if (warp != 0 || step >= s1) return;
-    const uint32_t tile = fd_div(p.n_beta_div, static_cast<uint32_t>(step));
-    const uint32_t beta = static_cast<uint32_t>(step) - tile * p.n_beta;
-    if (tile != iss_tile) {
-      int64_t ob[kMaxOperands];
-      decomp_offsets(p.a_outer, tile, ob);
-      iss_tile = tile;
-      iss_base = ob[0];
+    if (step < s1) {
+      const uint32_t tile = fd_div(p.n_beta_div, static_cast<uint32_t>(step));
+      const uint32_t beta = static_cast<uint32_t>(step) - tile * p.n_beta;
+      if (tile != iss_tile) {
+        int64_t ob[kMaxOperands];
+        decomp_offsets(p.a_outer, tile, ob);
+        iss_tile = tile;
+        iss_base = ob[0];
+      }
+      const float* src = p.g + iss_base + s_beta[2 * beta];
+      float* dst = s_stage + stage * stage_floats;
+      if (kUsesB && tid < nvc) cp_async16(dst + tile_floats + tid * 4, p.b + s_beta[2 * beta + 1] + tid * 4);
+#pragma unroll
+      for (int k = 0; k < RPT; ++k) cp_async16(dst + chunk_dst[k], src + chunk_src[k]);
     }
-    const float* src = p.g + iss_base + s_beta[2 * beta];
-    float* dst = s_stage + stage * stage_floats;
-    if (lane == 0) {
-      fence_proxy_async();
-      mbar_arrive_expect_tx(&s_bar[stage], step_bytes);
-    }
-    __syncwarp();
-    for (uint32_t r = lane; r < n_runs; r += 32)
-      bulk_g2s(dst + r * p.run_rows * p.ncol, src + s_row[2 * r * p.run_rows], run_bytes, &s_bar[stage]);
-    if (kUsesB && lane == 0)
-      bulk_g2s(dst + tile_floats, p.b + s_beta[2 * beta + 1], p.ncol * 4, &s_bar[stage]);
+    cp_async_commit();
   };
-  auto parity_of = [&](uint32_t k) { return (k / kSabStages) & 1u; };
   // Turn a landed stage's b row into the per-element factor.
   auto convert_row = [&](uint32_t stage) {
     if (kUsesB && tid < p.ncol) {
@@ -221,40 +152,31 @@ k_sab(const __grid_constant__ SabPlan p) {
     }
   };
 
-  for (uint32_t k = 0; k + 1 < kSabStages; ++k) issue(s0 + k, k);
-  // Step 0's b row must be converted before anyone computes step 0.
-  if (kUsesB && tid < p.ncol && s0 < s1) {
-    if (mbar_wait(&s_bar[0], 0)) convert_row(0);
-    else s_abort = 1;
-  }
+  for (int k = 0; k < kSabStages - 1; ++k) issue(s0 + k, k);
+  cp_async_wait<kSabStages - 2>();
+  __syncthreads();
+  convert_row(0);
 
-  float4 blk[RPT];
+  Kahan acc[RPT][4];
 #pragma unroll
-  for (int j = 0; j < RPT; ++j) blk[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int j = 0; j < RPT; ++j)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[j][i].init();
   float4 areg[RPT];
 #pragma unroll
   for (int j = 0; j < RPT; ++j) areg[j] = make_float4(1.f, 1.f, 1.f, 1.f);
   uint32_t cur_tile = 0xffffffffu;
-  uint32_t since_fold = 0;
   float rprev = 1.0f;  // factor of column tid at the previous step (tid < ncol)
-  uint32_t k = 0;
 
-  for (uint64_t step = s0; step < s1; ++step, ++k) {
-    // Everyone is done with step k-1: its stage may be refilled and its
-    // grad_b partials summed.
+  for (uint64_t step = s0; step < s1; ++step) {
+    const uint32_t k = static_cast<uint32_t>(step - s0);
+    // Steps k and k+1 have landed (for this thread's copies); the barrier
+    // makes every thread's copies visible and frees stage (k-1).
+    cp_async_wait<kSabStages - 3>();
     __syncthreads();
-    if (s_abort) break;
-    issue(step + kSabStages - 1, (k + kSabStages - 1) % kSabStages);
+    if (step + 1 < s1) convert_row((k + 1) % kSabStages);
     if (k > 0) finish_b(step - 1, (k - 1) & 1, rprev);
-    if (kUsesB && tid < p.ncol && step + 1 < s1) {
-      // Convert step k+1's b row now; it is read after the next barrier.
-      if (mbar_wait(&s_bar[(k + 1) % kSabStages], parity_of(k + 1))) convert_row((k + 1) % kSabStages);
-      else s_abort = 1;
-    }
-    if (!mbar_wait(&s_bar[k % kSabStages], parity_of(k))) {
-      s_abort = 1;
-      continue;
-    }
+    issue(step + kSabStages - 1, (k + kSabStages - 1) % kSabStages);
 
     const uint32_t tile = fd_div(p.n_beta_div, static_cast<uint32_t>(step));
     const uint32_t beta = static_cast<uint32_t>(step) - tile * p.n_beta;
@@ -280,18 +202,17 @@ k_sab(const __grid_constant__ SabPlan p) {
     for (int j = 0; j < RPT; ++j) {
       const uint32_t row = ty + j * lanes;
       const float4 g4 = *reinterpret_cast<const float4*>(st + row * p.ncol + tx * 4);
-      blk[j].x = __fmaf_rn(g4.x, ca.x, blk[j].x);
-      blk[j].y = __fmaf_rn(g4.y, ca.y, blk[j].y);
-      blk[j].z = __fmaf_rn(g4.z, ca.z, blk[j].z);
-      blk[j].w = __fmaf_rn(g4.w, ca.w, blk[j].w);
-      if (kUsesA) {
+      if (OP == OP_ADD || OP == OP_SUB) {
+        acc[j][0].add(g4.x); acc[j][1].add(g4.y); acc[j][2].add(g4.z); acc[j][3].add(g4.w);
+        sb.x = __fadd_rn(sb.x, g4.x); sb.y = __fadd_rn(sb.y, g4.y);
+        sb.z = __fadd_rn(sb.z, g4.z); sb.w = __fadd_rn(sb.w, g4.w);
+      } else {
+        acc[j][0].add_prod(g4.x, ca.x); acc[j][1].add_prod(g4.y, ca.y);
+        acc[j][2].add_prod(g4.z, ca.z); acc[j][3].add_prod(g4.w, ca.w);
         sb.x = __fmaf_rn(g4.x, areg[j].x, sb.x);
         sb.y = __fmaf_rn(g4.y, areg[j].y, sb.y);
         sb.z = __fmaf_rn(g4.z, areg[j].z, sb.z);
         sb.w = __fmaf_rn(g4.w, areg[j].w, sb.w);
-      } else {
-        sb.x = __fadd_rn(sb.x, g4.x); sb.y = __fadd_rn(sb.y, g4.y);
-        sb.z = __fadd_rn(sb.z, g4.z); sb.w = __fadd_rn(sb.w, g4.w);
       }
     }
     // Lanes of a warp that share tx hold different rows: butterfly over them.
@@ -305,51 +226,29 @@ k_sab(const __grid_constant__ SabPlan p) {
       *reinterpret_cast<float4*>(s_sb + (k & 1) * kWarps * p.ncol + warp * p.ncol + tx * 4) = sb;
 
     // Leaving this tile (its last beta, or the end of this CTA's range):
-    // fold, then write grad_a's partial to this CTA's slot for the tile.
+    // write grad_a's partial to this CTA's slot for the tile.
     const bool tile_done = beta == p.n_beta - 1;
-    const bool leave = tile_done || step == s1 - 1;
-    if (++since_fold == kSabFold || leave) {
-      sab_fold<RPT>(blk, s_ks, s_kc, tid);
-      since_fold = 0;
-    }
-    if (leave) {
+    if (tile_done || step == s1 - 1) {
       const uint32_t slot = cta - sab_owner(p, uint64_t(tile) * p.n_beta);
 #pragma unroll
       for (int j = 0; j < RPT; ++j) {
         const uint32_t row = ty + j * lanes;
         const uint64_t x = (uint64_t(tile) * p.ta + row) * p.ncol + tx * 4;
-        float v[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const uint32_t idx = (j * 4 + i) * kSabThreads + tid;
-          v[i] = s_ks[idx];
-          s_ks[idx] = 0.f;
-          s_kc[idx] = 0.f;
-        }
-        *reinterpret_cast<float4*>(p.ws_a + uint64_t(slot) * p.n_a + x) = make_float4(v[0], v[1], v[2], v[3]);
+        const float4 v = make_float4(acc[j][0].s, acc[j][1].s, acc[j][2].s, acc[j][3].s);
+        *reinterpret_cast<float4*>(p.ws_a + uint64_t(slot) * p.n_a + x) = v;
         if (tile_done) {
           // Slots no CTA reaches for this tile hold zeros.
           for (uint32_t s = slot + 1; s < p.slots_a; ++s)
             *reinterpret_cast<float4*>(p.ws_a + uint64_t(s) * p.n_a + x) =
                 make_float4(0.f, 0.f, 0.f, 0.f);
         }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[j][i].init();
       }
     }
   }
+  cp_async_wait<0>();
   __syncthreads();
-  if (s_abort) {
-    // Record the failure, and let every copy this CTA issued land before
-    // its shared memory is released (each wait bounded again).
-    if (tid == 0) {
-      *p.status = 1;
-      const uint64_t issued_end = s0 + k + kSabStages - 1 < s1 ? s0 + k + kSabStages - 1 : s1;
-      for (uint64_t st = s0 + k; st < issued_end; ++st) {
-        const uint32_t kk = static_cast<uint32_t>(st - s0);
-        mbar_wait(&s_bar[kk % kSabStages], parity_of(kk));
-      }
-    }
-    return;
-  }
   if (s1 > s0) finish_b(s1 - 1, static_cast<uint32_t>(s1 - s0 - 1) & 1, rprev);
 }
 
