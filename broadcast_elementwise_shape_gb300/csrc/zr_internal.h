@@ -230,6 +230,9 @@ struct SabPlan {
   uint32_t grid;            // CTAs (persistent)
   uint32_t slots_a;         // grad_a partial slots (max CTAs covering a tile)
   uint64_t n_a, n_b;        // elements of grad_a / grad_b
+  uint32_t ring;            // steps whose grad_b partials wait in shared memory
+                            // before one pass sums them (power of two,
+                            // ring * ncol <= kSabThreads)
   uint32_t smem_bytes;
 };
 
@@ -253,6 +256,7 @@ struct SabFPlan {
 };
 
 constexpr int kSabStages = 5;
+constexpr int kSabFold = 8;   // steps summed plainly before a Kahan fold
 constexpr int kSabThreads = 512;
 constexpr uint32_t kSabGrid = 152;  // one CTA per SM of a GB300; fixed so that
                                     // the partition depends on the shape only

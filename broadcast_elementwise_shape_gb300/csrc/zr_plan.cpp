@@ -620,9 +620,17 @@ int build_sab(const Prob& P, const float* g, const float* a, const float* b, flo
     smax = std::max(smax, c1 - c0 + 1);
   }
   p.slots_a = smax;
-  const uint64_t smem = uint64_t(kSabStages) * (ta + 1) * ncol * 4 + 2 * ta * 8 +
-                        2 * n_beta * 8 + 2 * (kSabThreads / 32) * ncol * 4;
-  if (smem > 220 * 1024) return 1;
+  // grad_b's per-warp partials wait in a ring of (ring + 1) steps, each
+  // [warps][ncol] plus the step's b factors [ncol]; the largest ring that
+  // fits (at most one column-step per thread per pass) is taken.
+  const uint64_t fixed = uint64_t(kSabStages) * (ta + 1) * ncol * 4 + 2 * ta * 8 + 2 * n_beta * 8;
+  uint64_t ring = kSabThreads / ncol, smem = 0;
+  for (; ring >= 1; ring /= 2) {
+    smem = fixed + (ring + 1) * (kSabThreads / 32 + 1) * ncol * 4;
+    if (smem <= 220 * 1024) break;
+  }
+  if (ring < 1) return 1;
+  p.ring = uint32_t(ring);
   p.smem_bytes = uint32_t(smem);
   sb->rpt = int(rows_x_vec / kSabThreads);
   sb->ws_a_bytes = ((uint64_t(p.slots_a) * p.n_a * 4 + 255) / 256) * 256;
@@ -751,10 +759,10 @@ std::string describe_sab(const SabBuild& sb) {
                 "{\"kernel\":\"sab\",\"ncol\":%u,\"ta\":%u,\"rpt\":%d,\"n_tiles\":%u,"
                 "\"n_beta\":%u,\"grid\":%u,\"slots_a\":%u,\"slots_b\":%u,\"n_a\":%llu,"
                 "\"n_b\":%llu,\"ws_bytes\":%zu,\"smem\":%u,\"outer_dims\":%d,\"inner_dims\":%d,"
-                "\"beta_dims\":%d}",
+                "\"beta_dims\":%d,\"ring\":%u}",
                 p.ncol, p.ta, sb.rpt, p.n_tiles, p.n_beta, p.grid, p.slots_a, p.n_tiles,
                 (unsigned long long)p.n_a, (unsigned long long)p.n_b,
-                sb.ws_a_bytes + sb.ws_b_bytes, p.smem_bytes, p.a_outer.n, p.a_inner.n, p.beta.n);
+                sb.ws_a_bytes + sb.ws_b_bytes, p.smem_bytes, p.a_outer.n, p.a_inner.n, p.beta.n, p.ring);
   return buf;
 }
 

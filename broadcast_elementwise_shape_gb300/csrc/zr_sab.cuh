@@ -67,10 +67,11 @@ k_sab(const __grid_constant__ SabPlan p) {
   // to the per-element factor one step before use).
   const uint32_t tile_floats = p.ta * p.ncol;
   const uint32_t stage_floats = tile_floats + p.ncol;
+  const uint32_t ring_floats = (kWarps + 1) * p.ncol;  // [warps][ncol] + factors [ncol]
   float* s_stage = reinterpret_cast<float*>(s_raw);
   int64_t* s_row = reinterpret_cast<int64_t*>(s_stage + kSabStages * stage_floats);  // [ta][2]
   int64_t* s_beta = s_row + 2 * p.ta;                                                 // [n_beta][2]
-  float* s_sb = reinterpret_cast<float*>(s_beta + 2 * p.n_beta);                      // [2][warps][ncol]
+  float* s_ring = reinterpret_cast<float*>(s_beta + 2 * p.n_beta);                    // [ring+1][...]
 
   const uint32_t tid = threadIdx.x;
   for (uint32_t i = tid; i < p.ta; i += blockDim.x) {
@@ -89,13 +90,15 @@ k_sab(const __grid_constant__ SabPlan p) {
 
   const uint32_t cta = blockIdx.x;
   const uint64_t s0 = sab_start(p, cta);
-  const uint64_t s1 = sab_start(p, cta + 1);
+  const uint32_t n_steps = static_cast<uint32_t>(sab_start(p, cta + 1) - s0);
   const uint32_t nvc = p.nvc;  // power of two
   const uint32_t nvc_shift = __ffs(nvc) - 1;
+  const uint32_t ncol_shift = nvc_shift + 2;
   const uint32_t lanes = kSabThreads >> nvc_shift;  // row lanes
   const uint32_t tx = tid & (nvc - 1);
   const uint32_t ty = tid >> nvc_shift;
   const uint32_t warp = tid >> 5, lane = tid & 31;
+  const uint32_t R = p.ring;  // power of two
 
   // This thread's RPT 16-byte chunks of every tile: fixed rows and columns,
   // so their source offsets (within a tile) and destinations are fixed too.
@@ -109,25 +112,32 @@ k_sab(const __grid_constant__ SabPlan p) {
     chunk_src[k] = s_row[2 * row] + c4 * 4;
     chunk_dst[k] = row * p.ncol + c4 * 4;
   }
-  uint32_t iss_tile = 0xffffffffu;
-  int64_t iss_base = 0;
+  const uint32_t tile0 = fd_div(p.n_beta_div, static_cast<uint32_t>(s0));
+  const uint32_t beta0 = static_cast<uint32_t>(s0) - tile0 * p.n_beta;
+  auto g_base = [&](uint32_t tile) {
+    int64_t ob[kMaxOperands];
+    decomp_offsets(p.a_outer, tile, ob);
+    return ob[0];
+  };
 
-  // Stage the tile (and b's row) of `step` if in range; close one group.
-  auto issue = [&](uint64_t step, uint32_t stage) {
-    if (step < s1) {
-      const uint32_t tile = fd_div(p.n_beta_div, static_cast<uint32_t>(step));
-      const uint32_t beta = static_cast<uint32_t>(step) - tile * p.n_beta;
-      if (tile != iss_tile) {
-        int64_t ob[kMaxOperands];
-        decomp_offsets(p.a_outer, tile, ob);
-        iss_tile = tile;
-        iss_base = ob[0];
-      }
-      const float* src = p.g + iss_base + s_beta[2 * beta];
+  // Loads are issued in step order; (tile, beta) of the next one to issue.
+  uint32_t iss_k = 0, iss_tile = tile0, iss_beta = beta0;
+  int64_t iss_base = n_steps ? g_base(tile0) : 0;
+  // Stage the next step's tile (and b's row) if in range; close one group.
+  auto issue = [&](uint32_t stage) {
+    if (iss_k < n_steps) {
+      const float* src = p.g + iss_base + s_beta[2 * iss_beta];
       float* dst = s_stage + stage * stage_floats;
-      if (kUsesB && tid < nvc) cp_async16(dst + tile_floats + tid * 4, p.b + s_beta[2 * beta + 1] + tid * 4);
+      if (kUsesB && tid < nvc)
+        cp_async16(dst + tile_floats + tid * 4, p.b + s_beta[2 * iss_beta + 1] + tid * 4);
 #pragma unroll
       for (int k = 0; k < RPT; ++k) cp_async16(dst + chunk_dst[k], src + chunk_src[k]);
+      ++iss_k;
+      if (++iss_beta == p.n_beta) {
+        iss_beta = 0;
+        ++iss_tile;
+        if (iss_k < n_steps) iss_base = g_base(iss_tile);
+      }
     }
     cp_async_commit();
   };
@@ -138,49 +148,62 @@ k_sab(const __grid_constant__ SabPlan p) {
       r[tid] = sab_row<OP>(r[tid]);
     }
   };
-  // grad_b of a finished step: per column, the warps' partials in warp order,
-  // times b's factor; stored to slot `tile` of the workspace.
-  auto finish_b = [&](uint64_t step, uint32_t buf, float rv) {
-    if (tid < p.ncol) {
-      const uint32_t tile = fd_div(p.n_beta_div, static_cast<uint32_t>(step));
-      const uint32_t beta = static_cast<uint32_t>(step) - tile * p.n_beta;
-      const float* src = s_sb + buf * kWarps * p.ncol + tid;
+  // grad_b of `cnt` finished steps k0.. (ring entries rb0..): thread
+  // (r, col) adds step k0+r's warp partials of column col in warp order,
+  // scales by b's factor and stores to slot `tile` of the workspace.
+  auto finish_b = [&](uint32_t k0, uint32_t cnt, uint32_t rb0) {
+    const uint32_t r = tid >> ncol_shift, col = tid & (p.ncol - 1);
+    if (r < cnt) {
+      uint32_t rb = rb0 + r;
+      if (rb > R) rb -= R + 1;
+      const float* src = s_ring + rb * ring_floats + col;
       float v = src[0];
 #pragma unroll
       for (uint32_t w = 1; w < kWarps; ++w) v = __fadd_rn(v, src[w * p.ncol]);
-      p.ws_b[uint64_t(tile) * p.n_b + uint64_t(beta) * p.ncol + tid] = __fmul_rn(v, sab_scale<OP>(rv));
+      const float rv = src[kWarps * p.ncol];
+      const uint32_t step = static_cast<uint32_t>(s0) + k0 + r;
+      const uint32_t tile = fd_div(p.n_beta_div, step);
+      const uint32_t beta = step - tile * p.n_beta;
+      p.ws_b[uint64_t(tile) * p.n_b + uint64_t(beta) * p.ncol + col] =
+          __fmul_rn(v, sab_scale<OP>(rv));
     }
   };
 
-  for (int k = 0; k < kSabStages - 1; ++k) issue(s0 + k, k);
+  for (int k = 0; k < kSabStages - 1; ++k) issue(k);
   cp_async_wait<kSabStages - 2>();
   __syncthreads();
   convert_row(0);
 
+  // grad_a: per step a plain FMA into blk; every kSabFold steps (and when a
+  // tile's partial is written) blk is added into the Kahan total acc.
   Kahan acc[RPT][4];
+  float4 blk[RPT];
 #pragma unroll
-  for (int j = 0; j < RPT; ++j)
+  for (int j = 0; j < RPT; ++j) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) acc[j][i].init();
+    blk[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
   float4 areg[RPT];
 #pragma unroll
   for (int j = 0; j < RPT; ++j) areg[j] = make_float4(1.f, 1.f, 1.f, 1.f);
-  uint32_t cur_tile = 0xffffffffu;
-  float rprev = 1.0f;  // factor of column tid at the previous step (tid < ncol)
+  uint32_t tile = tile0, beta = beta0;
+  uint32_t sc = 0;       // stage of step k
+  uint32_t wr = 0;       // ring entry of step k (k mod (R + 1))
+  uint32_t nfold = 0;    // steps in blk
 
-  for (uint64_t step = s0; step < s1; ++step) {
-    const uint32_t k = static_cast<uint32_t>(step - s0);
+  for (uint32_t k = 0; k < n_steps; ++k) {
     // Steps k and k+1 have landed (for this thread's copies); the barrier
     // makes every thread's copies visible and frees stage (k-1).
     cp_async_wait<kSabStages - 3>();
     __syncthreads();
-    if (step + 1 < s1) convert_row((k + 1) % kSabStages);
-    if (k > 0) finish_b(step - 1, (k - 1) & 1, rprev);
-    issue(step + kSabStages - 1, (k + kSabStages - 1) % kSabStages);
+    const uint32_t s_next = sc + 1 == kSabStages ? 0 : sc + 1;
+    if (k + 1 < n_steps) convert_row(s_next);
+    // Ring entries of steps k-R .. k-1 are complete (k-R sits at wr+1).
+    if (k != 0 && (k & (R - 1)) == 0) finish_b(k - R, R, wr == R ? 0 : wr + 1);
+    issue(sc == 0 ? kSabStages - 1 : sc - 1);
 
-    const uint32_t tile = fd_div(p.n_beta_div, static_cast<uint32_t>(step));
-    const uint32_t beta = static_cast<uint32_t>(step) - tile * p.n_beta;
-    if (kUsesA && tile != cur_tile) {
+    if (kUsesA && (k == 0 || beta == 0)) {
       int64_t ob[kMaxOperands];
       decomp_offsets(p.a_outer, tile, ob);
 #pragma unroll
@@ -189,12 +212,12 @@ k_sab(const __grid_constant__ SabPlan p) {
         areg[j] = __ldg(reinterpret_cast<const float4*>(p.a + ob[1] + s_row[2 * row + 1] + tx * 4));
       }
     }
-    cur_tile = tile;
-    const float* st = s_stage + (k % kSabStages) * stage_floats;
+    const float* st = s_stage + sc * stage_floats;
+    float* ring = s_ring + wr * ring_floats;
     float4 ca = make_float4(1.f, 1.f, 1.f, 1.f);
     if (kUsesB) {
       ca = *reinterpret_cast<const float4*>(st + tile_floats + tx * 4);
-      if (tid < p.ncol) rprev = st[tile_floats + tid];
+      if (tid < p.ncol) ring[kWarps * p.ncol + tid] = st[tile_floats + tid];
     }
 
     float4 sb = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -203,12 +226,13 @@ k_sab(const __grid_constant__ SabPlan p) {
       const uint32_t row = ty + j * lanes;
       const float4 g4 = *reinterpret_cast<const float4*>(st + row * p.ncol + tx * 4);
       if (OP == OP_ADD || OP == OP_SUB) {
-        acc[j][0].add(g4.x); acc[j][1].add(g4.y); acc[j][2].add(g4.z); acc[j][3].add(g4.w);
+        blk[j].x = __fadd_rn(blk[j].x, g4.x); blk[j].y = __fadd_rn(blk[j].y, g4.y);
+        blk[j].z = __fadd_rn(blk[j].z, g4.z); blk[j].w = __fadd_rn(blk[j].w, g4.w);
         sb.x = __fadd_rn(sb.x, g4.x); sb.y = __fadd_rn(sb.y, g4.y);
         sb.z = __fadd_rn(sb.z, g4.z); sb.w = __fadd_rn(sb.w, g4.w);
       } else {
-        acc[j][0].add_prod(g4.x, ca.x); acc[j][1].add_prod(g4.y, ca.y);
-        acc[j][2].add_prod(g4.z, ca.z); acc[j][3].add_prod(g4.w, ca.w);
+        blk[j].x = __fmaf_rn(g4.x, ca.x, blk[j].x); blk[j].y = __fmaf_rn(g4.y, ca.y, blk[j].y);
+        blk[j].z = __fmaf_rn(g4.z, ca.z, blk[j].z); blk[j].w = __fmaf_rn(g4.w, ca.w, blk[j].w);
         sb.x = __fmaf_rn(g4.x, areg[j].x, sb.x);
         sb.y = __fmaf_rn(g4.y, areg[j].y, sb.y);
         sb.z = __fmaf_rn(g4.z, areg[j].z, sb.z);
@@ -222,13 +246,22 @@ k_sab(const __grid_constant__ SabPlan p) {
       sb.z = __fadd_rn(sb.z, __shfl_xor_sync(0xffffffffu, sb.z, off));
       sb.w = __fadd_rn(sb.w, __shfl_xor_sync(0xffffffffu, sb.w, off));
     }
-    if (lane < nvc)
-      *reinterpret_cast<float4*>(s_sb + (k & 1) * kWarps * p.ncol + warp * p.ncol + tx * 4) = sb;
+    if (lane < nvc) *reinterpret_cast<float4*>(ring + warp * p.ncol + tx * 4) = sb;
 
     // Leaving this tile (its last beta, or the end of this CTA's range):
     // write grad_a's partial to this CTA's slot for the tile.
     const bool tile_done = beta == p.n_beta - 1;
-    if (tile_done || step == s1 - 1) {
+    const bool leave = tile_done || k + 1 == n_steps;
+    if (++nfold == kSabFold || leave) {
+#pragma unroll
+      for (int j = 0; j < RPT; ++j) {
+        acc[j][0].add(blk[j].x); acc[j][1].add(blk[j].y);
+        acc[j][2].add(blk[j].z); acc[j][3].add(blk[j].w);
+        blk[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      nfold = 0;
+    }
+    if (leave) {
       const uint32_t slot = cta - sab_owner(p, uint64_t(tile) * p.n_beta);
 #pragma unroll
       for (int j = 0; j < RPT; ++j) {
@@ -246,10 +279,22 @@ k_sab(const __grid_constant__ SabPlan p) {
         for (int i = 0; i < 4; ++i) acc[j][i].init();
       }
     }
+    if (tile_done) {
+      beta = 0;
+      ++tile;
+    } else {
+      ++beta;
+    }
+    sc = s_next;
+    wr = wr == R ? 0 : wr + 1;
   }
   cp_async_wait<0>();
   __syncthreads();
-  if (s1 > s0) finish_b(s1 - 1, static_cast<uint32_t>(s1 - s0 - 1) & 1, rprev);
+  // Steps left in the ring: from the last multiple of R below n_steps.
+  if (n_steps > 0) {
+    const uint32_t k0 = ((n_steps - 1) / R) * R;
+    finish_b(k0, n_steps - k0, k0 % (R + 1));
+  }
 }
 
 }  // namespace zr
