@@ -65,6 +65,8 @@ def parse():
                    help="JSON size overrides for a single --workload (see workloads.DEFAULT_DIMS), "
                         "e.g. for a smaller profiling case")
     p.add_argument("--e2e-steps", type=int, default=3)
+    p.add_argument("--breakdown-steps", type=int, default=20,
+                   help="steps of the untimed per-op breakdown pass")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     a = p.parse_args()
@@ -326,18 +328,39 @@ def run_zr(args, rank, world, local):
     flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=device)
     stream = torch.cuda.current_stream(device)
 
-    def one_step(events=None):
+    ncalls = len(suite.calls)
+
+    def one_step(events=None, only=None):
         for i, c in enumerate(suite.calls):
-            if events is not None:
-                events[i][0].record(stream)
+            timed = events is not None and (only is None or i == only)
+            if timed:
+                events[i if only is None else 0][0].record(stream)
             c[5]()
-            if events is not None:
-                events[i][1].record(stream)
+            if timed:
+                events[i if only is None else 0][1].record(stream)
+
+    def new_events(n):
+        return [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(n)]
 
     for _ in range(args.warmup):
         flush.fill_(0.0)
         one_step()
     torch.cuda.synchronize()
+
+    # Per-op breakdown (outside the timed region): events around every op.
+    # An event between two ops keeps the second op's first kernel from being
+    # scheduled while the first op's last kernel drains, so these per-op
+    # times add up to a little more than a step of the timed loop.
+    nb = max(1, min(args.steps, args.breakdown_steps))
+    bd_ev = [new_events(ncalls) for _ in range(nb)]
+    for k in range(nb):
+        flush.fill_(0.0)
+        one_step(bd_ev[k])
+    torch.cuda.synchronize()
+    op_ms = [[bd_ev[k][i][0].elapsed_time(bd_ev[k][i][1]) for k in range(nb)]
+             for i in range(ncalls)]
+    dom = max(range(ncalls), key=lambda i: statistics.fmean(op_ms[i]))
 
     uuid = None
     try:
@@ -353,11 +376,10 @@ def run_zr(args, rank, world, local):
             sampler.stop()
             sampler = ClockSampler(None)
             time.sleep(0.35)
-    ncalls = len(suite.calls)
-    steps_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                for _ in range(args.steps)]
-    op_ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(ncalls)] for _ in range(args.steps)]
+    # Timed loop: events around each whole step and around the dominant op
+    # (for its roofline), nothing between the other ops.
+    steps_ev = new_events(args.steps)
+    dom_ev = [new_events(1) for _ in range(args.steps)]
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -365,7 +387,7 @@ def run_zr(args, rank, world, local):
     for k in range(args.steps):
         flush.fill_(0.0)
         steps_ev[k][0].record(stream)
-        one_step(op_ev[k])
+        one_step(dom_ev[k], only=dom)
         steps_ev[k][1].record(stream)
     torch.cuda.synchronize()
     t1 = time.monotonic()
@@ -373,8 +395,7 @@ def run_zr(args, rank, world, local):
         dist.barrier()
     step_ms = [s.elapsed_time(e) for s, e in steps_ev]
     total_ms = sum(step_ms)
-    op_ms = [[op_ev[k][i][0].elapsed_time(op_ev[k][i][1]) for k in range(args.steps)]
-             for i in range(ncalls)]
+    dom_ms = [dom_ev[k][0][0].elapsed_time(dom_ev[k][0][1]) for k in range(args.steps)]
     if world > 1:
         t = torch.tensor([total_ms], dtype=torch.float64, device=device)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -397,8 +418,7 @@ def run_zr(args, rank, world, local):
             per_op.append({"config": c[0], "kind": c[1], "op": c[2], "bytes": c[3],
                            "launches": c[4], "ms_mean": round(mean, 5), "ms_median": round(med, 5),
                            "gbs": round(c[3] / (mean * 1e-3) / 1e9, 1)})
-        dom = max(range(ncalls), key=lambda i: statistics.fmean(op_ms[i]))
-        dom_gbs = suite.calls[dom][3] / (statistics.fmean(op_ms[dom]) * 1e-3) / 1e9
+        dom_gbs = suite.calls[dom][3] / (statistics.fmean(dom_ms) * 1e-3) / 1e9
         traffic = read_traffic(suite.calls[dom])
         roofline = {"bound": "hbm", "achieved": round(dom_gbs, 1), "peak": peak, "unit": "GB/s",
                     "frac": round(dom_gbs / peak, 4), "traffic": traffic,
@@ -420,6 +440,7 @@ def run_zr(args, rank, world, local):
                        "pct_of_nominal_8000": round(value / world / NOMINAL_HBM_GBS, 4)},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": suite.launches() * args.steps, "clocks": clocks, "per_op": per_op,
+            "per_op_pass": f"untimed breakdown, {nb} steps with events around every op",
         }
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -54,6 +54,16 @@ struct Needs {
 // the number of terms (N. J. Higham, "Accuracy and Stability of Numerical
 // Algorithms", 2nd ed., section 4.3).  Explicit _rn intrinsics keep the
 // compiler from reassociating or contracting the compensation away.
+// First statement of every kernel: wait until the grids before this one in
+// the stream have completed and their writes are visible (returns at once
+// when the launch did not ask for programmatic serialization), then let the
+// next kernel in the stream be scheduled; its own wait keeps it from touching
+// memory before this grid has finished.
+__device__ __forceinline__ void grid_dep_sync() {
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+
 struct Kahan {
   float s, c;
   __device__ __forceinline__ void init() { s = 0.f; c = 0.f; }
@@ -170,6 +180,7 @@ struct CopyF {
 template <class F, int VEC, int NOUT>
 __global__ void __launch_bounds__(kThreads, F::kMinBlocks)
 k_elementwise(const __grid_constant__ EwPlan p) {
+  grid_dep_sync();
   extern __shared__ int64_t s_off[];  // [tile_rows][kMaxOperands]
   const EwTile t = ew_tile(p, blockIdx.x);
   for (uint32_t i = threadIdx.x; i < t.nrows; i += blockDim.x) {
@@ -221,6 +232,7 @@ k_elementwise(const __grid_constant__ EwPlan p) {
 template <int OP>
 __global__ void __launch_bounds__(kThreads)
 k_transpose(const __grid_constant__ TrPlan p) {
+  grid_dep_sync();
   __shared__ float tile[kTrTile][kTrP + 1];  // [q][p], padded: no bank conflicts
   const uint32_t t1 = fd_div(p.n_qt_div, blockIdx.x);
   const uint32_t qt = blockIdx.x - t1 * p.n_qt;
@@ -277,6 +289,7 @@ k_transpose(const __grid_constant__ TrPlan p) {
 template <int OP, int RPT>
 __global__ void __launch_bounds__(kThreads)
 k_sabf(const __grid_constant__ SabFPlan p) {
+  grid_dep_sync();
   const uint32_t tile = fd_div(p.n_bc_div, blockIdx.x);
   const uint32_t bc = blockIdx.x - tile * p.n_bc;
   const uint32_t nvc = p.nvc;
@@ -368,6 +381,7 @@ struct RedTerms {
 template <int OP, int WHICH, int VEC, bool INNER_KEPT>
 __global__ void __launch_bounds__(kThreads, (OP == OP_MUL || OP == OP_DIV) ? 3 : 4)
 k_reduce(const __grid_constant__ RedPlan p) {
+  grid_dep_sync();
   using T = RedTerms<OP, WHICH>;
   extern __shared__ int64_t s_dyn[];
   const uint32_t table_rows = p.rows_per_blk < kMaxTileRows ? p.rows_per_blk : kMaxTileRows;
@@ -531,6 +545,7 @@ k_reduce(const __grid_constant__ RedPlan p) {
 // fixed tree over the sy lanes.
 static __global__ void __launch_bounds__(kThreads)
 k_combine(const __grid_constant__ CombinePlan p) {
+  grid_dep_sync();
   __shared__ float s_red[kThreads];
   const uint32_t jl = threadIdx.x % p.jx;
   const uint32_t sl = threadIdx.x / p.jx;
@@ -538,15 +553,18 @@ k_combine(const __grid_constant__ CombinePlan p) {
   Kahan acc;
   acc.init();
   if (j < p.nout && sl < p.sy) {
+    // Eight partials are loaded before any is added, so their loads overlap.
+    const float* src = p.partial + uint64_t(sl) * p.nout + j;
+    const uint64_t step = uint64_t(p.sy) * p.nout;
     uint32_t s = sl;
-    for (; s + 3 * p.sy < p.nslots; s += 4 * p.sy) {
-      const float v0 = __ldg(p.partial + uint64_t(s) * p.nout + j);
-      const float v1 = __ldg(p.partial + uint64_t(s + p.sy) * p.nout + j);
-      const float v2 = __ldg(p.partial + uint64_t(s + 2 * p.sy) * p.nout + j);
-      const float v3 = __ldg(p.partial + uint64_t(s + 3 * p.sy) * p.nout + j);
-      acc.add(v0); acc.add(v1); acc.add(v2); acc.add(v3);
+    for (; s + 7 * p.sy < p.nslots; s += 8 * p.sy, src += 8 * step) {
+      float v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v[u] = __ldg(src + u * step);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) acc.add(v[u]);
     }
-    for (; s < p.nslots; s += p.sy) acc.add(__ldg(p.partial + uint64_t(s) * p.nout + j));
+    for (; s < p.nslots; s += p.sy, src += step) acc.add(__ldg(src));
   }
   const uint32_t syn = blockDim.x / p.jx;  // power of two
   s_red[sl * p.jx + jl] = (sl < p.sy) ? acc.s : 0.f;

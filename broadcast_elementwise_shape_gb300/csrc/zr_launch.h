@@ -7,6 +7,28 @@
 
 namespace zr {
 
+// Launch with programmatic stream serialization: the kernel may be scheduled
+// while the kernel before it in the stream is still running.  Every kernel
+// of this library begins with grid_dep_sync() (griddepcontrol.wait, which
+// returns once the grids before it have completed and their writes are
+// visible), so only launch latency and CTA setup overlap the previous
+// kernel, never a memory access.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_k(void (*kernel)(KArgs...), unsigned grid, unsigned block, size_t smem,
+                            cudaStream_t s, const Args&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // Every launcher first checks that the plan provides each operand its kernel
 // dereferences (cudaErrorInvalidValue otherwise); with dry == true it stops
 // there and launches nothing.

@@ -14,11 +14,8 @@ cudaError_t launch_ew_t(const EwBuild& eb, cudaStream_t s, bool dry) {
     return cudaErrorInvalidValue;
   if (dry) return cudaSuccess;
   const size_t smem = size_t(eb.plan.tile_rows) * kMaxOperands * sizeof(int64_t);
-  if (eb.vec == 4)
-    k_elementwise<F, 4, NOUT><<<eb.plan.n_cta, kThreads, smem, s>>>(eb.plan);
-  else
-    k_elementwise<F, 1, NOUT><<<eb.plan.n_cta, kThreads, smem, s>>>(eb.plan);
-  return cudaGetLastError();
+  if (eb.vec == 4) return launch_k(k_elementwise<F, 4, NOUT>, eb.plan.n_cta, kThreads, smem, s, eb.plan);
+  return launch_k(k_elementwise<F, 1, NOUT>, eb.plan.n_cta, kThreads, smem, s, eb.plan);
 }
 
 template <int OP>
@@ -45,13 +42,12 @@ namespace {
 template <int OP>
 cudaError_t launch_sabf_op(int rpt, const SabFPlan& sp, cudaStream_t s) {
   switch (rpt) {
-    case 1: k_sabf<OP, 1><<<sp.n_cta, kThreads, 0, s>>>(sp); break;
-    case 2: k_sabf<OP, 2><<<sp.n_cta, kThreads, 0, s>>>(sp); break;
-    case 4: k_sabf<OP, 4><<<sp.n_cta, kThreads, 0, s>>>(sp); break;
-    case 8: k_sabf<OP, 8><<<sp.n_cta, kThreads, 0, s>>>(sp); break;
+    case 1: return launch_k(k_sabf<OP, 1>, sp.n_cta, kThreads, 0, s, sp);
+    case 2: return launch_k(k_sabf<OP, 2>, sp.n_cta, kThreads, 0, s, sp);
+    case 4: return launch_k(k_sabf<OP, 4>, sp.n_cta, kThreads, 0, s, sp);
+    case 8: return launch_k(k_sabf<OP, 8>, sp.n_cta, kThreads, 0, s, sp);
     default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 }  // namespace
 
@@ -71,12 +67,11 @@ cudaError_t launch_fwd_tr(int op, const TrPlan& tp, cudaStream_t s, bool dry) {
   if (!tp.x || !tp.y || !tp.out) return cudaErrorInvalidValue;
   if (dry) return cudaSuccess;
   switch (op) {
-    case OP_ADD: k_transpose<OP_ADD><<<tp.n_cta, kThreads, 0, s>>>(tp); break;
-    case OP_SUB: k_transpose<OP_SUB><<<tp.n_cta, kThreads, 0, s>>>(tp); break;
-    case OP_MUL: k_transpose<OP_MUL><<<tp.n_cta, kThreads, 0, s>>>(tp); break;
-    default: k_transpose<OP_DIV><<<tp.n_cta, kThreads, 0, s>>>(tp); break;
+    case OP_ADD: return launch_k(k_transpose<OP_ADD>, tp.n_cta, kThreads, 0, s, tp);
+    case OP_SUB: return launch_k(k_transpose<OP_SUB>, tp.n_cta, kThreads, 0, s, tp);
+    case OP_MUL: return launch_k(k_transpose<OP_MUL>, tp.n_cta, kThreads, 0, s, tp);
+    default: return launch_k(k_transpose<OP_DIV>, tp.n_cta, kThreads, 0, s, tp);
   }
-  return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_direct(int op, int want, const EwBuild& eb, cudaStream_t s, bool dry) {

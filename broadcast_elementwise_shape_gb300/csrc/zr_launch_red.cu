@@ -21,19 +21,18 @@ cudaError_t launch_red_t(const RedBuild& rb, cudaStream_t s, bool dry) {
   const uint32_t table_rows = p.rows_per_blk < kMaxTileRows ? p.rows_per_blk : kMaxTileRows;
   const size_t red_floats = p.inner_kept ? size_t(kThreads) * rb.vec : size_t(kThreads);
   const size_t smem = size_t(table_rows) * kMaxOperands * sizeof(int64_t) + red_floats * sizeof(float);
+  cudaError_t e;
   if (p.inner_kept) {
-    if (rb.vec == 4) k_reduce<OP, WHICH, 4, true><<<p.n_cta, kThreads, smem, s>>>(p);
-    else k_reduce<OP, WHICH, 1, true><<<p.n_cta, kThreads, smem, s>>>(p);
+    e = rb.vec == 4 ? launch_k(k_reduce<OP, WHICH, 4, true>, p.n_cta, kThreads, smem, s, p)
+                    : launch_k(k_reduce<OP, WHICH, 1, true>, p.n_cta, kThreads, smem, s, p);
   } else {
-    if (rb.vec == 4) k_reduce<OP, WHICH, 4, false><<<p.n_cta, kThreads, smem, s>>>(p);
-    else k_reduce<OP, WHICH, 1, false><<<p.n_cta, kThreads, smem, s>>>(p);
+    e = rb.vec == 4 ? launch_k(k_reduce<OP, WHICH, 4, false>, p.n_cta, kThreads, smem, s, p)
+                    : launch_k(k_reduce<OP, WHICH, 1, false>, p.n_cta, kThreads, smem, s, p);
   }
-  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || p.nslots <= 1) return e;
   const CombinePlan& c = rb.comb;
   const uint64_t nblk = (c.nout + c.jx - 1) / c.jx;
-  k_combine<<<static_cast<unsigned>(nblk), kThreads, 0, s>>>(c);
-  return cudaGetLastError();
+  return launch_k(k_combine, static_cast<unsigned>(nblk), kThreads, 0, s, c);
 }
 
 template <int OP>

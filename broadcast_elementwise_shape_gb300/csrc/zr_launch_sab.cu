@@ -18,15 +18,14 @@ cudaError_t launch_sab_t(const SabBuild& sb, cudaStream_t s, bool dry) {
   cudaError_t e = cudaFuncSetAttribute(k_sab<OP, RPT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        int(p.smem_bytes));
   if (e != cudaSuccess) return e;
-  k_sab<OP, RPT><<<p.grid, kSabThreads, p.smem_bytes, s>>>(p);
-  e = cudaGetLastError();
+  e = launch_k(k_sab<OP, RPT>, p.grid, kSabThreads, p.smem_bytes, s, p);
   if (e != cudaSuccess) return e;
   CombinePlan ca = sb.comb_a, cb = sb.comb_b;
   ca.partial = p.ws_a;
   cb.partial = p.ws_b;
-  k_combine<<<static_cast<unsigned>((ca.nout + ca.jx - 1) / ca.jx), kThreads, 0, s>>>(ca);
-  k_combine<<<static_cast<unsigned>((cb.nout + cb.jx - 1) / cb.jx), kThreads, 0, s>>>(cb);
-  return cudaGetLastError();
+  e = launch_k(k_combine, static_cast<unsigned>((ca.nout + ca.jx - 1) / ca.jx), kThreads, 0, s, ca);
+  if (e != cudaSuccess) return e;
+  return launch_k(k_combine, static_cast<unsigned>((cb.nout + cb.jx - 1) / cb.jx), kThreads, 0, s, cb);
 }
 
 template <int OP>

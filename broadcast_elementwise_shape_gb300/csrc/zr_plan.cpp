@@ -48,15 +48,20 @@ uint32_t pick_tx(uint64_t nvcol) {
 }
 
 // Thread layout of the combine pass: jx outputs x sy slot lanes (powers of
-// two, jx * sy = 256).  Few slots: one output per thread, summed serially
-// (no tree).  Many slots: 32 consecutive outputs per row of lanes (coalesced
-// 128-byte loads) and 8 slot lanes, unless there are fewer than 32 outputs,
-// where the lanes go to the slots.
+// two, jx * sy <= 256).  Few slots: one output per thread, summed serially
+// (no tree).  Many slots: rows of jx consecutive outputs (32, or down to 8 =
+// one 32-byte sector, until there are about two CTAs per SM) and the lanes
+// left over go to the slots, so each thread has few partials to load.
 void combine_layout(CombinePlan* c) {
   uint32_t jx;
-  if (c->nslots <= 16) jx = kThreads;
-  else if (c->nout >= 32) jx = 32;
-  else jx = pow2_ceil(c->nout);
+  if (c->nslots <= 16) {
+    jx = kThreads;
+  } else if (c->nout < 8) {
+    jx = pow2_ceil(c->nout);
+  } else {
+    jx = 32;
+    while (jx > 8 && ceil_div(c->nout, jx) < 2 * 152) jx /= 2;
+  }
   if (jx > kThreads) jx = kThreads;
   const uint32_t sy_max = kThreads / jx;
   c->jx = jx;

@@ -59,6 +59,7 @@ __device__ __forceinline__ float sab_scale(float rv) {
 template <int OP, int RPT>
 __global__ void __launch_bounds__(kSabThreads, 1)
 k_sab(const __grid_constant__ SabPlan p) {
+  grid_dep_sync();
   constexpr bool kUsesA = OP == OP_MUL || OP == OP_DIV;
   constexpr bool kUsesB = OP == OP_MUL || OP == OP_DIV;
   constexpr uint32_t kWarps = kSabThreads / 32;
