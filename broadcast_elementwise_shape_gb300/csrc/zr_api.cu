@@ -778,9 +778,13 @@ void walk_tr(const TrPlan& p, Rec rec) {
     const uint32_t pt = t1 - bidx * p.n_pt;
     int64_t base[kMaxOperands];
     decomp_offsets(p.batch, bidx, base);
-    for (uint32_t i = 0; i < kTrP; ++i) {
-      for (uint32_t l = 0; l < kTrTile; ++l) {
-        const uint32_t pp = pt * kTrP + i, q = qt * kTrTile + l;
+    // Thread (warp w, lane) covers p = 16w + 4(lane & 3) + c, q = 4(lane >> 2) + k.
+    for (uint32_t t = 0; t < kThreads; ++t) {
+      const uint32_t w = t >> 5, lane = t & 31;
+      for (uint32_t c = 0; c < 4; ++c)
+      for (uint32_t k = 0; k < 4; ++k) {
+        const uint32_t pp = pt * kTrP + 16 * w + 4 * (lane & 3) + c;
+        const uint32_t q = qt * kTrTile + 4 * (lane >> 2) + k;
         if (q >= p.nq || pp >= p.np) continue;
         int64_t o[kMaxOperands] = {base[0] + pp + int64_t(q) * p.xs_q,
                                    base[1] + int64_t(pp) * p.ys_p + int64_t(q) * p.ys_q, 0,

@@ -126,13 +126,16 @@ struct TrPlan {
   uint32_t n_pt, n_qt;      // tiles along p and q
   FastDiv n_qt_div, n_pt_div;
   uint32_t n_cta;
-  uint32_t vec_ok;          // x's rows start 16-byte aligned: 16-byte loads
+  uint32_t vec_ok;          // x's rows (along p) and out's rows (along q) start
+                            // 16-byte aligned: 16-byte loads and stores
 };
 constexpr uint32_t kTrTile = 32;   // tile extent along q
 constexpr uint32_t kTrP = 128;     // tile extent along p
 
 constexpr uint32_t kMaxTileRows = 512;
 constexpr int kThreads = 256;
+// k_transpose: 8 warps x 16 p rows, 8 lanes x 4 q columns.
+static_assert(kTrP == (kThreads / 32) * 16 && kTrTile == 32, "transpose tile");
 
 // CTA -> (first row, first column vector, rows in tile, vectors in tile).
 struct EwTile {

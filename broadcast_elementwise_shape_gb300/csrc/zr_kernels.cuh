@@ -225,15 +225,19 @@ k_elementwise(const __grid_constant__ EwPlan p) {
   }
 }
 
-// Forward with a transposed input (TrPlan): X's tile (kTrP values along its
-// unit-stride dim p x kTrTile along the output's dim q) is read along p with
-// 16-byte loads into shared memory, then read back along q to write the
-// output along its unit-stride dim, both coalesced.
+// Forward with a transposed input (TrPlan): x has unit stride along p, the
+// output along q.  A CTA covers kTrP p x kTrTile q; warp w its p rows
+// [16w, 16w + 16), lane (pc = lane & 3, qq = lane >> 2) a 4 x 4 block at
+// p = 4 pc, q = 4 qq.  The block is read as four 16-byte loads along p (one
+// per q; a warp's load covers 64 contiguous bytes in each of 8 rows),
+// transposed in registers and written as four 16-byte stores along q (a
+// warp's store covers 128 contiguous bytes in each of 4 rows): no shared
+// memory and no barrier.  Blocks cut by the edge of p or q, or views
+// without 16-byte alignment, use scalar accesses with the same mapping.
 template <int OP>
 __global__ void __launch_bounds__(kThreads)
 k_transpose(const __grid_constant__ TrPlan p) {
   grid_dep_sync();
-  __shared__ float tile[kTrTile][kTrP + 1];  // [q][p], padded: no bank conflicts
   const uint32_t t1 = fd_div(p.n_qt_div, blockIdx.x);
   const uint32_t qt = blockIdx.x - t1 * p.n_qt;
   const uint32_t bidx = fd_div(p.n_pt_div, t1);
@@ -241,44 +245,70 @@ k_transpose(const __grid_constant__ TrPlan p) {
   int64_t base[kMaxOperands];
   decomp_offsets(p.batch, bidx, base);
   const uint32_t lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  constexpr uint32_t kWarps = kThreads / 32;
-  const uint32_t p0 = pt * kTrP, q0 = qt * kTrTile;
-  const bool full_p = p0 + kTrP <= p.np;
-  if (full_p && p.vec_ok) {
-    float4 v[kTrTile / kWarps];
+  const uint32_t ps = pt * kTrP + 16 * w + 4 * (lane & 3);  // this thread's first p
+  const uint32_t qs = qt * kTrTile + 4 * (lane >> 2);       // and first q
+  if (ps >= p.np || qs >= p.nq) return;
+  const float* __restrict__ x = p.x + base[0];
+  const float* __restrict__ y = p.y + base[1];
+  float* __restrict__ out = p.out + base[kSlotOut];
+  const bool fast = p.vec_ok && ps + 4 <= p.np && qs + 4 <= p.nq;
+  const uint32_t np4 = min(4u, p.np - ps), nq4 = min(4u, p.nq - qs);
+
+  float v[4][4];  // [q][p]
+  if (fast) {
 #pragma unroll
-    for (uint32_t k = 0; k < kTrTile / kWarps; ++k) {
-      const uint32_t q = q0 + w + k * kWarps;
-      if (q < p.nq)
-        v[k] = __ldcs(reinterpret_cast<const float4*>(p.x + base[0] + p0 + 4 * lane + int64_t(q) * p.xs_q));
-    }
-#pragma unroll
-    for (uint32_t k = 0; k < kTrTile / kWarps; ++k) {
-      const uint32_t j = w + k * kWarps;
-      tile[j][4 * lane + 0] = v[k].x;
-      tile[j][4 * lane + 1] = v[k].y;
-      tile[j][4 * lane + 2] = v[k].z;
-      tile[j][4 * lane + 3] = v[k].w;
+    for (uint32_t k = 0; k < 4; ++k) {
+      const float4 t = __ldcs(reinterpret_cast<const float4*>(x + ps + int64_t(qs + k) * p.xs_q));
+      v[k][0] = t.x; v[k][1] = t.y; v[k][2] = t.z; v[k][3] = t.w;
     }
   } else {
-    for (uint32_t j = w; j < kTrTile; j += kWarps) {
-      const uint32_t q = q0 + j;
-      for (uint32_t l = lane; l < kTrP; l += 32) {
-        const uint32_t pp = p0 + l;
-        if (q < p.nq && pp < p.np) tile[j][l] = __ldcs(p.x + base[0] + pp + int64_t(q) * p.xs_q);
-      }
-    }
+#pragma unroll
+    for (uint32_t k = 0; k < 4; ++k)
+#pragma unroll
+      for (uint32_t c = 0; c < 4; ++c)
+        v[k][c] = (k < nq4 && c < np4) ? __ldcs(x + ps + c + int64_t(qs + k) * p.xs_q) : 0.f;
   }
-  __syncthreads();
-  const uint32_t q = q0 + lane;
-  if (q < p.nq) {
-    for (uint32_t i = w; i < kTrP; i += kWarps) {
-      const uint32_t pp = p0 + i;
-      if (pp >= p.np) break;
-      const float xv = tile[lane][i];
-      const float yv = __ldg(p.y + base[1] + int64_t(pp) * p.ys_p + int64_t(q) * p.ys_q);
-      p.out[base[kSlotOut] + int64_t(pp) * p.os_p + q] = p.x_is_a ? fwd_op<OP>(xv, yv) : fwd_op<OP>(yv, xv);
+  // y at (p, q); a y broadcast along q or p is loaded once per row/column.
+  float yv[4][4];  // [p][q]
+  if (p.ys_q == 0) {
+#pragma unroll
+    for (uint32_t c = 0; c < 4; ++c) {
+      const float t = c < np4 ? __ldg(y + int64_t(ps + c) * p.ys_p) : 0.f;
+#pragma unroll
+      for (uint32_t k = 0; k < 4; ++k) yv[c][k] = t;
     }
+  } else if (p.ys_p == 0) {
+#pragma unroll
+    for (uint32_t k = 0; k < 4; ++k) {
+      const float t = k < nq4 ? __ldg(y + int64_t(qs + k) * p.ys_q) : 0.f;
+#pragma unroll
+      for (uint32_t c = 0; c < 4; ++c) yv[c][k] = t;
+    }
+  } else {
+#pragma unroll
+    for (uint32_t c = 0; c < 4; ++c)
+#pragma unroll
+      for (uint32_t k = 0; k < 4; ++k)
+        yv[c][k] = (c < np4 && k < nq4)
+                       ? __ldg(y + int64_t(ps + c) * p.ys_p + int64_t(qs + k) * p.ys_q) : 0.f;
+  }
+  float r[4][4];  // [p][q]
+#pragma unroll
+  for (uint32_t c = 0; c < 4; ++c)
+#pragma unroll
+    for (uint32_t k = 0; k < 4; ++k)
+      r[c][k] = p.x_is_a ? fwd_op<OP>(v[k][c], yv[c][k]) : fwd_op<OP>(yv[c][k], v[k][c]);
+  if (fast) {
+#pragma unroll
+    for (uint32_t c = 0; c < 4; ++c)
+      *reinterpret_cast<float4*>(out + int64_t(ps + c) * p.os_p + qs) =
+          make_float4(r[c][0], r[c][1], r[c][2], r[c][3]);
+  } else {
+#pragma unroll
+    for (uint32_t c = 0; c < 4; ++c)
+#pragma unroll
+      for (uint32_t k = 0; k < 4; ++k)
+        if (c < np4 && k < nq4) out[int64_t(ps + c) * p.os_p + qs + k] = r[c][k];
   }
 }
 

@@ -451,8 +451,11 @@ int build_tr(const Prob& P, const float* a, const float* b, float* out, TrPlan* 
   const uint64_t ncta = nbatch * p.n_pt * p.n_qt;
   if (nbatch >= (uint64_t(1) << 32) || ncta >= (uint64_t(1) << 31)) return 1;
   p.n_cta = uint32_t(ncta);
-  bool v = reinterpret_cast<uintptr_t>(p.x) % 16 == 0 && p.xs_q % 4 == 0;
-  for (int i = 0; i < nd; ++i) v = v && p.batch.stride[0][i] % 4 == 0;
+  // 16-byte loads of x along p and stores of out along q.
+  bool v = reinterpret_cast<uintptr_t>(p.x) % 16 == 0 && p.xs_q % 4 == 0 &&
+           reinterpret_cast<uintptr_t>(p.out) % 16 == 0 && p.os_p % 4 == 0;
+  for (int i = 0; i < nd; ++i)
+    v = v && p.batch.stride[0][i] % 4 == 0 && p.batch.stride[kSlotOut][i] % 4 == 0;
   p.vec_ok = v ? 1 : 0;
   return ZR_OK;
 }

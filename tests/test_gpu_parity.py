@@ -289,6 +289,55 @@ def test_rank8_and_ragged():
         within(gb.cpu().numpy(), rb, s2, f"rank8 {op} grad_b")
 
 
+def _fwd_kernel(op, a, b, out):
+    L = zr.lib()
+    L.zr_test_describe_fwd.argtypes = [ctypes.c_int, zr.ZrTensor, zr.ZrTensor, ctypes.c_void_p,
+                                       ctypes.POINTER(ctypes.c_int64), ctypes.c_char_p,
+                                       ctypes.c_size_t]
+    da, ka = zr._desc(a)
+    db, kb = zr._desc(b)
+    ost = zr._i64(out.stride())
+    buf = ctypes.create_string_buffer(4096)
+    assert L.zr_test_describe_fwd(zr.OPS[op], da, db, out.data_ptr(), ost, buf, 4096) == 0
+    import json
+    return json.loads(buf.value.decode())["kernel"]
+
+
+def test_transposed_input_tiles():
+    """Forward with one input stored transposed (unit stride along an outer
+    dim): interior 4x4 blocks with 16-byte accesses, blocks cut by ragged p
+    and q edges, y broadcast along q, along p or not at all, the transposed
+    input on either side of a non-commutative op, and an output whose rows
+    are not 16-byte aligned (scalar path)."""
+    rng = np.random.default_rng(31)
+    # p = M = 130: one full p tile and a 2-wide one (a 4x4 block cut by the
+    # p edge); q = Q = 203 (a block cut by the q edge).  x's storage rows are
+    # padded to 136 floats so that its rows stay 16-byte aligned.
+    P, M, Q = 3, 130, 203
+    st = torch.from_numpy(rng.standard_normal((P, Q, 136)).astype(np.float32)).cuda()
+    xt = st[:, :, :M].transpose(1, 2)  # [P, M, Q], unit stride along M
+    dense = torch.from_numpy(rng.standard_normal((P, M, Q)).astype(np.float32) + 3.0).cuda()
+    ys = {
+        "along_p": torch.from_numpy(rng.standard_normal((1, M, 1)).astype(np.float32) + 3.0).cuda(),
+        "along_q": torch.from_numpy(rng.standard_normal((1, 1, Q)).astype(np.float32) + 3.0).cuda(),
+        "full": dense,
+    }
+    pitched = {n: torch.empty((P, M, n), device="cuda") for n in (204, 205)}
+    outs = {"pitch_204": lambda: pitched[204][:, :, :Q],   # aligned rows: 16-byte stores
+            "pitch_205": lambda: pitched[205][:, :, :Q],   # unaligned rows: scalar
+            "dense": lambda: torch.empty((P, M, Q), device="cuda")}
+    for op in OPS:
+        for yname, y in ys.items():
+            for xa in (True, False):
+                a, b = (xt, y) if xa else (y, xt)
+                for oname, mk in outs.items():
+                    out = mk()
+                    assert _fwd_kernel(op, a, b, out) == "transpose", (op, yname, xa, oname)
+                    zr.zr_binary_fwd(op, a, b, out=out)
+                    bitexact(out.cpu().numpy(), oracle.binary_fwd(op, a.cpu(), b.cpu()),
+                             f"transpose {op} y={yname} x_is_a={xa} out={oname}")
+
+
 def test_strided_output_and_in_place():
     rng = np.random.default_rng(9)
     a = torch.from_numpy(rng.standard_normal((33, 65)).astype(np.float32)).cuda()
