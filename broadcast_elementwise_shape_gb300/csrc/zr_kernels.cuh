@@ -54,14 +54,19 @@ struct Needs {
 // the number of terms (N. J. Higham, "Accuracy and Stability of Numerical
 // Algorithms", 2nd ed., section 4.3).  Explicit _rn intrinsics keep the
 // compiler from reassociating or contracting the compensation away.
-// First statement of every kernel: wait until the grids before this one in
-// the stream have completed and their writes are visible (returns at once
-// when the launch did not ask for programmatic serialization), then let the
-// next kernel in the stream be scheduled; its own wait keeps it from touching
-// memory before this grid has finished.
-__device__ __forceinline__ void grid_dep_sync() {
-  asm volatile("griddepcontrol.wait;\n" ::: "memory");
+// Programmatic dependent launch.  Every kernel starts with pdl_trigger()
+// (the next kernel in the stream may now be scheduled; it runs only its own
+// parameter-only setup before its pdl_wait()), computes what depends on its
+// parameters alone (index decompositions, shared-memory offset tables), and
+// calls pdl_wait() before its first access to global memory: that returns
+// once the grids before it in the stream have completed and their writes are
+// visible (at once when the launch did not ask for programmatic
+// serialization).
+__device__ __forceinline__ void pdl_trigger() {
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() {
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
 }
 
 struct Kahan {
@@ -180,7 +185,7 @@ struct CopyF {
 template <class F, int VEC, int NOUT>
 __global__ void __launch_bounds__(kThreads, F::kMinBlocks)
 k_elementwise(const __grid_constant__ EwPlan p) {
-  grid_dep_sync();
+  pdl_trigger();
   extern __shared__ int64_t s_off[];  // [tile_rows][kMaxOperands]
   const EwTile t = ew_tile(p, blockIdx.x);
   for (uint32_t i = threadIdx.x; i < t.nrows; i += blockDim.x) {
@@ -190,6 +195,7 @@ k_elementwise(const __grid_constant__ EwPlan p) {
     for (int k = 0; k < kMaxOperands; ++k) s_off[i * kMaxOperands + k] = off[k];
   }
   __syncthreads();
+  pdl_wait();
 
   constexpr int U = 4;
   const F f;
@@ -237,7 +243,7 @@ k_elementwise(const __grid_constant__ EwPlan p) {
 template <int OP>
 __global__ void __launch_bounds__(kThreads)
 k_transpose(const __grid_constant__ TrPlan p) {
-  grid_dep_sync();
+  pdl_trigger();
   const uint32_t t1 = fd_div(p.n_qt_div, blockIdx.x);
   const uint32_t qt = blockIdx.x - t1 * p.n_qt;
   const uint32_t bidx = fd_div(p.n_pt_div, t1);
@@ -253,6 +259,7 @@ k_transpose(const __grid_constant__ TrPlan p) {
   float* __restrict__ out = p.out + base[kSlotOut];
   const bool fast = p.vec_ok && ps + 4 <= p.np && qs + 4 <= p.nq;
   const uint32_t np4 = min(4u, p.np - ps), nq4 = min(4u, p.nq - qs);
+  pdl_wait();
 
   float v[4][4];  // [q][p]
   if (fast) {
@@ -319,7 +326,7 @@ k_transpose(const __grid_constant__ TrPlan p) {
 template <int OP, int RPT>
 __global__ void __launch_bounds__(kThreads)
 k_sabf(const __grid_constant__ SabFPlan p) {
-  grid_dep_sync();
+  pdl_trigger();
   const uint32_t tile = fd_div(p.n_bc_div, blockIdx.x);
   const uint32_t bc = blockIdx.x - tile * p.n_bc;
   const uint32_t nvc = p.nvc;
@@ -329,15 +336,18 @@ k_sabf(const __grid_constant__ SabFPlan p) {
   const uint32_t ty = threadIdx.x >> nvc_shift;
   int64_t ob[kMaxOperands];
   decomp_offsets(p.a_outer, tile, ob);
-  float4 areg[RPT];
-  int64_t ooff[RPT];
+  int64_t aoff[RPT], ooff[RPT];
 #pragma unroll
   for (int j = 0; j < RPT; ++j) {
     int64_t ri[kMaxOperands];
     decomp_offsets(p.a_inner, ty + j * lanes, ri);
-    areg[j] = __ldg(reinterpret_cast<const float4*>(p.a + ob[1] + ri[1] + tx * 4));
+    aoff[j] = ob[1] + ri[1] + tx * 4;
     ooff[j] = ob[0] + ri[0] + tx * 4;
   }
+  pdl_wait();
+  float4 areg[RPT];
+#pragma unroll
+  for (int j = 0; j < RPT; ++j) areg[j] = __ldg(reinterpret_cast<const float4*>(p.a + aoff[j]));
   const uint32_t b0 = bc * p.beta_chunk;
   const uint32_t b1 = min(p.n_beta, b0 + p.beta_chunk);
   for (uint32_t beta = b0; beta < b1; ++beta) {
@@ -411,7 +421,7 @@ struct RedTerms {
 template <int OP, int WHICH, int VEC, bool INNER_KEPT>
 __global__ void __launch_bounds__(kThreads, (OP == OP_MUL || OP == OP_DIV) ? 3 : 4)
 k_reduce(const __grid_constant__ RedPlan p) {
-  grid_dep_sync();
+  pdl_trigger();
   using T = RedTerms<OP, WHICH>;
   extern __shared__ int64_t s_dyn[];
   const uint32_t table_rows = p.rows_per_blk < kMaxTileRows ? p.rows_per_blk : kMaxTileRows;
@@ -442,17 +452,11 @@ k_reduce(const __grid_constant__ RedPlan p) {
   const uint32_t ncs = vcol_end > vcol_begin + tx ? (vcol_end - vcol_begin - tx + p.tx - 1) / p.tx : 0;
   // The input of the gradient being reduced (a for grad_a, b for grad_b) is
   // broadcast along every reduced dim, so its value depends only on the kept
-  // index and, when the inner dim is kept, the column: load it once.
+  // index and, when the inner dim is kept, the column: loaded once, after the
+  // first chunk's offset table (parameters only) is built and pdl_wait().
   Vec<VEC> own;
 #pragma unroll
   for (int i = 0; i < VEC; ++i) own.v[i] = 0.f;
-  if (WHICH < 2 && ncs > 0) {
-    const int slot = WHICH == 0 ? 1 : 2;
-    const bool needed = WHICH == 0 ? ((T::kXa || T::kDa) && read_a) : ((T::kXb || T::kDb) && read_b);
-    if (needed)
-      own = load_cols<VEC>(WHICH == 0 ? p.a : p.b, base[slot], p.inner_stride[slot],
-                           (vcol_begin + tx) * VEC, false);
-  }
 
   for (uint32_t ch0 = 0; ch0 < nrows; ch0 += kMaxTileRows) {
     const uint32_t cleft = nrows - ch0;
@@ -465,6 +469,17 @@ k_reduce(const __grid_constant__ RedPlan p) {
       for (int k = 0; k < kMaxOperands; ++k) s_off[i * kMaxOperands + k] = off[k] + base[k];
     }
     __syncthreads();
+    if (ch0 == 0) {
+      pdl_wait();
+      if (WHICH < 2 && ncs > 0) {
+        const int slot = WHICH == 0 ? 1 : 2;
+        const bool needed =
+            WHICH == 0 ? ((T::kXa || T::kDa) && read_a) : ((T::kXb || T::kDb) && read_b);
+        if (needed)
+          own = load_cols<VEC>(WHICH == 0 ? p.a : p.b, base[slot], p.inner_stride[slot],
+                               (vcol_begin + tx) * VEC, false);
+      }
+    }
 
     // This thread's items are (row, column vector) pairs: rows ty, ty + ty_n,
     // ... of the chunk, columns vcol_begin + tx, + tx_n, ... of the block,
@@ -575,7 +590,8 @@ k_reduce(const __grid_constant__ RedPlan p) {
 // fixed tree over the sy lanes.
 static __global__ void __launch_bounds__(kThreads)
 k_combine(const __grid_constant__ CombinePlan p) {
-  grid_dep_sync();
+  pdl_trigger();
+  pdl_wait();
   __shared__ float s_red[kThreads];
   const uint32_t jl = threadIdx.x % p.jx;
   const uint32_t sl = threadIdx.x / p.jx;

@@ -9,10 +9,10 @@ namespace zr {
 
 // Launch with programmatic stream serialization: the kernel may be scheduled
 // while the kernel before it in the stream is still running.  Every kernel
-// of this library begins with grid_dep_sync() (griddepcontrol.wait, which
-// returns once the grids before it have completed and their writes are
-// visible), so only launch latency and CTA setup overlap the previous
-// kernel, never a memory access.
+// of this library calls pdl_wait() (griddepcontrol.wait, which returns once
+// the grids before it have completed and their writes are visible) before
+// its first global memory access, so only launch latency and parameter-only
+// setup overlap the previous kernel, never a memory access.
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_k(void (*kernel)(KArgs...), unsigned grid, unsigned block, size_t smem,
                             cudaStream_t s, const Args&... args) {

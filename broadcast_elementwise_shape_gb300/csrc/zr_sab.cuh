@@ -59,7 +59,7 @@ __device__ __forceinline__ float sab_scale(float rv) {
 template <int OP, int RPT>
 __global__ void __launch_bounds__(kSabThreads, 1)
 k_sab(const __grid_constant__ SabPlan p) {
-  grid_dep_sync();
+  pdl_trigger();
   constexpr bool kUsesA = OP == OP_MUL || OP == OP_DIV;
   constexpr bool kUsesB = OP == OP_MUL || OP == OP_DIV;
   constexpr uint32_t kWarps = kSabThreads / 32;
@@ -113,6 +113,7 @@ k_sab(const __grid_constant__ SabPlan p) {
     chunk_src[k] = s_row[2 * row] + c4 * 4;
     chunk_dst[k] = row * p.ncol + c4 * 4;
   }
+  pdl_wait();
   const uint32_t tile0 = fd_div(p.n_beta_div, static_cast<uint32_t>(s0));
   const uint32_t beta0 = static_cast<uint32_t>(s0) - tile0 * p.n_beta;
   auto g_base = [&](uint32_t tile) {
