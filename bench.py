@@ -65,6 +65,8 @@ def parse():
                    help="JSON size overrides for a single --workload (see workloads.DEFAULT_DIMS), "
                         "e.g. for a smaller profiling case")
     p.add_argument("--e2e-steps", type=int, default=3)
+    p.add_argument("--config-reps", type=int, default=20,
+                   help="timed runs per workload phase in the per-config pass (0: skip)")
     p.add_argument("--breakdown-steps", type=int, default=20,
                    help="steps of the untimed per-op breakdown pass")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -325,7 +327,16 @@ def run_zr(args, rank, world, local):
     suite = Suite(names, device, dims)
     nbytes = suite.step_bytes()
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
-    flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=device)
+    nflush = max(2 * l2, 256 << 20) // 4
+    flush_w = torch.empty(nflush, dtype=torch.float32, device=device)
+    flush_r = torch.zeros(nflush, dtype=torch.float32, device=device)
+
+    def flush():
+        # Write a buffer of 2x L2, then read another one of 2x L2: the second
+        # pass evicts the first one's dirty lines, so their write-back happens
+        # here and not inside the next timed region.
+        flush_w.fill_(0.0)
+        flush_r.sum()
     stream = torch.cuda.current_stream(device)
 
     ncalls = len(suite.calls)
@@ -344,7 +355,7 @@ def run_zr(args, rank, world, local):
                 for _ in range(n)]
 
     for _ in range(args.warmup):
-        flush.fill_(0.0)
+        flush()
         one_step()
     torch.cuda.synchronize()
 
@@ -355,7 +366,7 @@ def run_zr(args, rank, world, local):
     nb = max(1, min(args.steps, args.breakdown_steps))
     bd_ev = [new_events(ncalls) for _ in range(nb)]
     for k in range(nb):
-        flush.fill_(0.0)
+        flush()
         one_step(bd_ev[k])
     torch.cuda.synchronize()
     op_ms = [[bd_ev[k][i][0].elapsed_time(bd_ev[k][i][1]) for k in range(nb)]
@@ -385,7 +396,7 @@ def run_zr(args, rank, world, local):
     torch.cuda.synchronize()
     t0 = time.monotonic()
     for k in range(args.steps):
-        flush.fill_(0.0)
+        flush()
         steps_ev[k][0].record(stream)
         one_step(dom_ev[k], only=dom)
         steps_ev[k][1].record(stream)
@@ -402,6 +413,9 @@ def run_zr(args, rank, world, local):
         total_ms = float(t.item())
     clocks = sampler.summary(t0, t1) if sampler else None
 
+    per_config = None
+    if rank == 0 and args.config_reps > 0:
+        per_config = run_per_config(suite, flush, stream, args.config_reps)
     e2e = None
     if not args.no_e2e and rank == 0:
         e2e = run_e2e(args, suite, flush, stream, nbytes)
@@ -435,16 +449,50 @@ def run_zr(args, rank, world, local):
             "config": {"workload": WORKLOAD_DESC if args.workload == "suite" else
                        (args.workload + (" " + json.dumps(dims) if dims else "")),
                        "bytes_per_step": nbytes,
-                       "l2": "flushed before every step (2x L2 write, outside the timed events)",
+                       "l2": "flushed before every step, outside the timed events: 2x L2 written, "
+                             "then another 2x L2 buffer read (clean, cold L2 at step start)",
                        "pct_of_measured_hbm": round(value / world / peak, 4),
                        "pct_of_nominal_8000": round(value / world / NOMINAL_HBM_GBS, 4)},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": suite.launches() * args.steps, "clocks": clocks, "per_op": per_op,
             "per_op_pass": f"untimed breakdown, {nb} steps with events around every op",
+            "per_config": per_config,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def run_per_config(suite, flush, stream, reps, warm=5):
+    """Each workload's forward chain and backward chain timed on their own:
+    the median of ``reps`` CUDA-event timings after ``warm`` untimed runs,
+    with L2 flushed before every run.  GB/s = the phase's algorithmic bytes
+    over that median."""
+    import torch
+    peak, _ = measured_peak()
+    out = {}
+    for name in dict.fromkeys(c[0] for c in suite.calls):
+        for kind in ("fwd", "bwd"):
+            calls = [c for c in suite.calls if c[0] == name and c[1] == kind]
+            nbytes = sum(c[3] for c in calls)
+            ev = []
+            for r in range(warm + reps):
+                flush()
+                s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                s.record(stream)
+                for c in calls:
+                    c[5]()
+                e.record(stream)
+                if r >= warm:
+                    ev.append((s, e))
+            torch.cuda.synchronize()
+            ms = statistics.median(s.elapsed_time(e) for s, e in ev)
+            gbs = nbytes / (ms * 1e-3) / 1e9
+            out.setdefault(name, {})[kind] = {
+                "bytes": nbytes, "ms_median": round(ms, 5), "gbs": round(gbs, 1),
+                "pct_of_measured_hbm": round(gbs / peak, 4),
+                "pct_of_nominal_8000": round(gbs / NOMINAL_HBM_GBS, 4)}
+    return out
 
 
 def run_e2e(args, suite, flush, stream, nbytes):
@@ -474,7 +522,7 @@ def run_e2e(args, suite, flush, stream, nbytes):
     ev = []
     steps = max(1, args.e2e_steps)
     for k in range(steps + 1):  # first iteration is a warm-up
-        flush.fill_(0.0)
+        flush()
         s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         s.record(stream)
         for dst, src in pinned_in:

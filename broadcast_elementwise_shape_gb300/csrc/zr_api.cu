@@ -173,7 +173,7 @@ int plan_fwd(int op, const zr_tensor& ta, const zr_tensor& tb, const float* out,
     S->sabf = true;
     return ZR_OK;
   }
-  return build_ew(P, in, outs, 0x3u, stream_mask, &S->eb);
+  return build_ew(P, in, outs, 0x3u, stream_mask, kOccEwFwd, &S->eb);
 }
 
 // ------------------------------------------------------------------ backward
@@ -277,7 +277,7 @@ int plan_bwd(int op, const zr_tensor& tg, const zr_tensor& ta, const zr_tensor& 
     if (rc) return rc;
     const float* in[3] = {S->g.ptr, S->a.ptr, S->b.ptr};
     float* outs[2] = {grad_a, grad_b};
-    return build_ew(P, in, outs, read_mask, stream_mask, &S->eb);
+    return build_ew(P, in, outs, read_mask, stream_mask, kOccEwBwd, &S->eb);
   }
 
   // One reduced gradient, the other written densely in the same pass (or
@@ -302,13 +302,14 @@ int plan_bwd(int op, const zr_tensor& tg, const zr_tensor& ta, const zr_tensor& 
     const bool rbb = needs_b(op, w) || (d_out && needs_b(op, 1 - w));
     const uint32_t rm = 1u | (ra ? 2u : 0u) | (rbb ? 4u : 0u);
     RedBuild& rb = S->rb[S->nred];
+    const int occ = (op == OP_MUL || op == OP_DIV) ? kOccRedMulDiv : kOccRedAddSub;
     rc = build_red(P, xslot, S->g.ptr, ra ? S->a.ptr : nullptr, rbb ? S->b.ptr : nullptr, rm,
-                   stream_mask & rm, xo, d_out, 0, &rb);
+                   stream_mask & rm, xo, d_out, 0, occ, &rb);
     if (rc) return rc;
     size_t q = rb.ws_bytes;
     for (int v : {1, 4}) {
       RedBuild tmp;
-      rc = build_red(P, xslot, S->g.ptr, nullptr, nullptr, rm, 0, xo, d_out, v, &tmp);
+      rc = build_red(P, xslot, S->g.ptr, nullptr, nullptr, rm, 0, xo, d_out, v, occ, &tmp);
       if (rc) return rc;
       q = std::max(q, tmp.ws_bytes);
     }
@@ -388,17 +389,19 @@ int plan_sum(const zr_tensor& tin, int32_t ndo, const int64_t* so, float* out, S
     if (rc) return rc;
     const float* in[3] = {S->in.ptr, nullptr, nullptr};
     float* outs[2] = {out, nullptr};
-    return build_ew(P, in, outs, 1u, 1u, &S->eb);
+    return build_ew(P, in, outs, 1u, 1u, kOccEwCopy, &S->eb);
   }
   grad_index_strides(S->out, n, S->in.size, st[kSlotXA]);
   rc = coalesce(n, S->in.size, st, 1u | (1u << kSlotXA), -1, &P);
   if (rc) return rc;
-  rc = build_red(P, kSlotXA, S->in.ptr, nullptr, nullptr, 1u, 1u, out, nullptr, 0, &S->rb);
+  rc = build_red(P, kSlotXA, S->in.ptr, nullptr, nullptr, 1u, 1u, out, nullptr, 0, kOccRedAddSub,
+                 &S->rb);
   if (rc) return rc;
   S->ws_query = S->rb.ws_bytes;
   for (int v : {1, 4}) {
     RedBuild tmp;
-    rc = build_red(P, kSlotXA, S->in.ptr, nullptr, nullptr, 1u, 0, out, nullptr, v, &tmp);
+    rc = build_red(P, kSlotXA, S->in.ptr, nullptr, nullptr, 1u, 0, out, nullptr, v, kOccRedAddSub,
+                   &tmp);
     if (rc) return rc;
     S->ws_query = std::max(S->ws_query, tmp.ws_bytes);
   }
@@ -676,6 +679,16 @@ int zr_test_dry_run_bwd(zr_op op, zr_tensor grad_out, zr_tensor a, zr_tensor b,
   if (rc || S.nothing || S.empty) return rc;
   // A stand-in workspace address: only checked for presence, never touched.
   return launch_bwd_set(S, op, reinterpret_cast<void*>(uintptr_t(1) << 40), nullptr, true);
+}
+
+int zr_test_occupancy(int which, int* planned, int* actual) {
+  if (!planned || !actual) return ZR_ERR_NULL;
+  cudaError_t e;
+  if (which >= 0 && which < 4) e = occupancy_ew(which, planned, actual);
+  else if (which >= 4 && which < 9) e = occupancy_red(which - 4, planned, actual);
+  else if (which >= 9 && which < 11) e = occupancy_other(which - 9, planned, actual);
+  else return ZR_ERR_SIZE;
+  return cuda_status(e);
 }
 
 int zr_test_dry_run_sum(zr_tensor in, int32_t ndim_out, const int64_t* sizes_out,

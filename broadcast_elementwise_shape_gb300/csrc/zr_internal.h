@@ -134,6 +134,17 @@ constexpr uint32_t kTrP = 128;     // tile extent along p
 
 constexpr uint32_t kMaxTileRows = 512;
 constexpr int kThreads = 256;
+constexpr uint32_t kSms = 152;  // SMs of a GB300
+// Resident CTAs per SM the planner sizes grids for (whole waves of
+// kSms * occupancy CTAs); each kernel's __launch_bounds__ asks for at least
+// this many, and a GPU test checks the runtime's occupancy against them.
+constexpr int kOccEwFwd = 4;      // k_elementwise: forward
+constexpr int kOccEwBwd = 3;      // k_elementwise: backward without reduction
+constexpr int kOccEwCopy = 5;     // k_elementwise: copy (sum-to-shape onto the same shape)
+constexpr int kOccRedAddSub = 4;  // k_reduce: add, sub, sum-to-shape
+constexpr int kOccRedMulDiv = 3;  // k_reduce: mul, div
+constexpr int kOccSabf = 3;       // k_sabf
+constexpr int kOccTr = 4;         // k_transpose
 // k_transpose: 8 warps x 16 p rows, 8 lanes x 4 q columns.
 static_assert(kTrP == (kThreads / 32) * 16 && kTrTile == 32, "transpose tile");
 

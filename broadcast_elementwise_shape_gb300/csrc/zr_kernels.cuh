@@ -142,7 +142,7 @@ __device__ __forceinline__ void store_cols(float* __restrict__ base, int64_t row
 template <int OP>
 struct FwdF {
   static constexpr bool kR1 = true, kR2 = false;  // slot 0 = a, slot 1 = b
-  static constexpr int kMinBlocks = 4;  // CTAs per SM the register budget targets
+  static constexpr int kMinBlocks = kOccEwFwd;  // CTAs per SM the register budget targets
   template <int VEC>
   __device__ __forceinline__ void operator()(const Vec<VEC> (&x)[3], Vec<VEC> (&y)[2]) const {
 #pragma unroll
@@ -156,7 +156,7 @@ template <int OP, int WANT>
 struct BwdDirectF {
   static constexpr bool kR1 = ((WANT & 1) && Needs<OP, 0>::a) || ((WANT & 2) && Needs<OP, 1>::a);
   static constexpr bool kR2 = ((WANT & 1) && Needs<OP, 0>::b) || ((WANT & 2) && Needs<OP, 1>::b);
-  static constexpr int kMinBlocks = 3;
+  static constexpr int kMinBlocks = kOccEwBwd;
   template <int VEC>
   __device__ __forceinline__ void operator()(const Vec<VEC> (&x)[3], Vec<VEC> (&y)[2]) const {
 #pragma unroll
@@ -170,7 +170,7 @@ struct BwdDirectF {
 // Copy (sum-to-shape onto the same shape).
 struct CopyF {
   static constexpr bool kR1 = false, kR2 = false;
-  static constexpr int kMinBlocks = 4;
+  static constexpr int kMinBlocks = kOccEwCopy;
   template <int VEC>
   __device__ __forceinline__ void operator()(const Vec<VEC> (&x)[3], Vec<VEC> (&y)[2]) const {
     y[0] = x[0];
@@ -241,7 +241,7 @@ k_elementwise(const __grid_constant__ EwPlan p) {
 // memory and no barrier.  Blocks cut by the edge of p or q, or views
 // without 16-byte alignment, use scalar accesses with the same mapping.
 template <int OP>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, kOccTr)
 k_transpose(const __grid_constant__ TrPlan p) {
   pdl_trigger();
   const uint32_t t1 = fd_div(p.n_qt_div, blockIdx.x);
@@ -324,7 +324,7 @@ k_transpose(const __grid_constant__ TrPlan p) {
 // and writes them against each beta's b row: one load of b per beta, one
 // operation and one 16-byte store per four outputs.
 template <int OP, int RPT>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, kOccSabf)
 k_sabf(const __grid_constant__ SabFPlan p) {
   pdl_trigger();
   const uint32_t tile = fd_div(p.n_bc_div, blockIdx.x);
@@ -419,7 +419,7 @@ struct RedTerms {
 // with a fixed tree.  Per-thread sums are Kahan-compensated, so the error
 // bound does not grow with the number of rows a thread adds.
 template <int OP, int WHICH, int VEC, bool INNER_KEPT>
-__global__ void __launch_bounds__(kThreads, (OP == OP_MUL || OP == OP_DIV) ? 3 : 4)
+__global__ void __launch_bounds__(kThreads, (OP == OP_MUL || OP == OP_DIV) ? kOccRedMulDiv : kOccRedAddSub)
 k_reduce(const __grid_constant__ RedPlan p) {
   pdl_trigger();
   using T = RedTerms<OP, WHICH>;

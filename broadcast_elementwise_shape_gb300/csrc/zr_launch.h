@@ -44,6 +44,16 @@ cudaError_t launch_copy(const EwBuild& eb, cudaStream_t s, bool dry = false);
 // pass and, when it writes partials, the combine pass.
 cudaError_t launch_reduce(int op, int which, const RedBuild& rb, cudaStream_t s, bool dry = false);
 
+// Resident CTAs per SM of one representative instantiation per kernel
+// family (the 16-byte-vector variants the workloads run), as the planner
+// assumes (*planned) and as the runtime reports for the current device
+// (*actual).  ew: 0 fwd add, 1 fwd div, 2 bwd div (both gradients), 3 copy;
+// red: 0 add inner kept, 1 sub inner reduced, 2 mul inner kept, 3 div inner
+// reduced, 4 sum-to-shape; other: 0 k_sabf (8 rows per thread), 1 k_transpose.
+cudaError_t occupancy_ew(int which, int* planned, int* actual);
+cudaError_t occupancy_red(int which, int* planned, int* actual);
+cudaError_t occupancy_other(int which, int* planned, int* actual);
+
 // Fused backward with both gradients reduced: the k_sab pass, then one
 // combine pass per gradient.  sb.plan.ws_a / ws_b must be set.
 cudaError_t launch_sab(int op, const SabBuild& sb, cudaStream_t s, bool dry = false);

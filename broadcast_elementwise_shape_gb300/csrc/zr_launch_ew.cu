@@ -87,4 +87,39 @@ cudaError_t launch_copy(const EwBuild& eb, cudaStream_t s, bool dry) {
   return launch_ew_t<CopyF, 1>(eb, s, dry);
 }
 
+cudaError_t occupancy_ew(int which, int* planned, int* actual) {
+  const size_t smem = size_t(kMaxTileRows) * kMaxOperands * sizeof(int64_t);
+  switch (which) {
+    case 0:
+      *planned = kOccEwFwd;
+      return cudaOccupancyMaxActiveBlocksPerMultiprocessor(actual, k_elementwise<FwdF<OP_ADD>, 4, 1>,
+                                                           kThreads, smem);
+    case 1:
+      *planned = kOccEwFwd;
+      return cudaOccupancyMaxActiveBlocksPerMultiprocessor(actual, k_elementwise<FwdF<OP_DIV>, 4, 1>,
+                                                           kThreads, smem);
+    case 2:
+      *planned = kOccEwBwd;
+      return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+          actual, k_elementwise<BwdDirectF<OP_DIV, 3>, 4, 2>, kThreads, smem);
+    case 3:
+      *planned = kOccEwCopy;
+      return cudaOccupancyMaxActiveBlocksPerMultiprocessor(actual, k_elementwise<CopyF, 4, 1>,
+                                                           kThreads, smem);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t occupancy_other(int which, int* planned, int* actual) {
+  switch (which) {
+    case 0:
+      *planned = kOccSabf;
+      return cudaOccupancyMaxActiveBlocksPerMultiprocessor(actual, k_sabf<OP_DIV, 8>, kThreads, 0);
+    case 1:
+      *planned = kOccTr;
+      return cudaOccupancyMaxActiveBlocksPerMultiprocessor(actual, k_transpose<OP_SUB>, kThreads, 0);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
 }  // namespace zr

@@ -42,6 +42,36 @@ cudaError_t launch_red_op(int which, const RedBuild& rb, cudaStream_t s, bool dr
 
 }  // namespace
 
+cudaError_t occupancy_red(int which, int* planned, int* actual) {
+  // The largest dynamic shared memory a plan asks for: a full offset table
+  // and the column-lane tree.
+  const size_t smem = size_t(kMaxTileRows) * kMaxOperands * sizeof(int64_t) +
+                      size_t(kThreads) * 4 * sizeof(float);
+  switch (which) {
+    case 0:
+      *planned = kOccRedAddSub;
+      return cudaOccupancyMaxActiveBlocksPerMultiprocessor(actual, k_reduce<OP_ADD, 1, 4, true>,
+                                                           kThreads, smem);
+    case 1:
+      *planned = kOccRedAddSub;
+      return cudaOccupancyMaxActiveBlocksPerMultiprocessor(actual, k_reduce<OP_SUB, 1, 4, false>,
+                                                           kThreads, smem);
+    case 2:
+      *planned = kOccRedMulDiv;
+      return cudaOccupancyMaxActiveBlocksPerMultiprocessor(actual, k_reduce<OP_MUL, 1, 4, true>,
+                                                           kThreads, smem);
+    case 3:
+      *planned = kOccRedMulDiv;
+      return cudaOccupancyMaxActiveBlocksPerMultiprocessor(actual, k_reduce<OP_DIV, 1, 4, false>,
+                                                           kThreads, smem);
+    case 4:
+      *planned = kOccRedAddSub;
+      return cudaOccupancyMaxActiveBlocksPerMultiprocessor(actual, k_reduce<OP_ADD, 2, 4, true>,
+                                                           kThreads, smem);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
 cudaError_t launch_reduce(int op, int which, const RedBuild& rb, cudaStream_t s, bool dry) {
   if (which == 2) return launch_red_t<OP_ADD, 2>(rb, s, dry);
   switch (op) {

@@ -47,6 +47,38 @@ uint32_t pick_tx(uint64_t nvcol) {
   return best;
 }
 
+// Fill of the last wave when `ctas` CTAs run `wave` at a time (1 for a whole
+// number of waves).  Grids of 6 waves or more count as full: their CTAs start
+// staggered, and resizing their tiles measured no gain.
+constexpr uint64_t kFullWaves = 6;
+double wave_fill(uint64_t ctas, uint64_t wave) {
+  if (ctas == 0) return 0.0;
+  const uint64_t waves = ceil_div(ctas, wave);
+  if (waves >= kFullWaves) return 1.0;
+  return double(ctas) / double(waves * wave);
+}
+
+// Block count n along one split of a grid with F CTAs per block of that
+// split, within [lo, hi]: either pref, or for k whole waves around pref's,
+// the most blocks that fit in k waves, whichever fills its last wave best
+// (pref on ties).  real(n) is the count the tile size implied by n really
+// gives (tile sizes are rounded).
+template <class Real>
+uint64_t fit_waves(uint64_t pref, uint64_t lo, uint64_t hi, uint64_t F, uint64_t wave, Real real) {
+  uint64_t pick = pref;
+  double best = wave_fill(F * real(pref), wave);
+  const uint64_t k0 = ceil_div(F * real(pref), wave);
+  if (k0 >= kFullWaves || best >= 1.0) return pick;
+  for (uint64_t k = k0 > 2 ? k0 - 2 : 1; k <= k0 + 1; ++k) {
+    uint64_t n = k * wave / F;
+    n = std::min(std::max(n, lo), hi);
+    if (n == 0) continue;
+    const double f = wave_fill(F * real(n), wave);
+    if (f > best + 1e-9) { best = f; pick = n; }
+  }
+  return pick;
+}
+
 // Thread layout of the combine pass: jx outputs x sy slot lanes (powers of
 // two, jx * sy <= 256).  Few slots: one output per thread, summed serially
 // (no tree).  Many slots: rows of jx consecutive outputs (32, or down to 8 =
@@ -248,7 +280,7 @@ int coalesce(int n, const int64_t* size, const int64_t (*st)[kMaxDims], uint32_t
 }
 
 int build_ew(const Prob& P, const float* const in[3], float* const out[2], uint32_t read_mask,
-             uint32_t stream_mask, EwBuild* eb) {
+             uint32_t stream_mask, int occ, EwBuild* eb) {
   EwPlan& p = eb->plan;
   p = EwPlan{};
   const int n = P.n;
@@ -277,9 +309,30 @@ int build_ew(const Prob& P, const float* const in[3], float* const out[2], uint3
   uint64_t ipc = items / 1216;
   ipc = std::max<uint64_t>(256, std::min<uint64_t>(2048, ipc));
   ipc = ceil_div(ipc, 256) * 256;
-  const uint64_t tvc = std::min<uint64_t>(nvcol, ipc);
+  uint64_t tvc = std::min<uint64_t>(nvcol, ipc);
   uint64_t trows = std::max<uint64_t>(1, ipc / tvc);
   trows = std::min<uint64_t>(trows, std::min<uint64_t>(nrow, kMaxTileRows));
+  // Grid: nearby tile sizes whose CTA count fills the last wave best.
+  const uint64_t wave = uint64_t(kSms) * uint64_t(occ);
+  if (trows > 1 || tvc == nvcol) {
+    // Rows per tile in [trows / 2, 2 trows].
+    auto real = [&](uint64_t n) { return ceil_div(nrow, ceil_div(nrow, n)); };
+    const uint64_t lo = ceil_div(nrow, std::min<uint64_t>({2 * trows, nrow, kMaxTileRows}));
+    const uint64_t hi = ceil_div(nrow, std::max<uint64_t>(1, trows / 2));
+    const uint64_t n = fit_waves(ceil_div(nrow, trows), lo, hi, ceil_div(nvcol, tvc), wave, real);
+    trows = ceil_div(nrow, n);
+  } else {
+    // One row per tile: vectors per tile in [tvc / 2, 2 tvc], multiples of
+    // 128 (2 KB of each operand).
+    auto width = [&](uint64_t n) {
+      return std::min<uint64_t>(nvcol, ceil_div(ceil_div(nvcol, n), 128) * 128);
+    };
+    auto real = [&](uint64_t n) { return ceil_div(nvcol, width(n)); };
+    const uint64_t lo = ceil_div(nvcol, std::min<uint64_t>(nvcol, 2 * tvc));
+    const uint64_t hi = ceil_div(nvcol, std::max<uint64_t>(128, tvc / 2));
+    const uint64_t n = fit_waves(ceil_div(nvcol, tvc), lo, hi, nrow, wave, real);
+    tvc = width(n);
+  }
   p.nrow = uint32_t(nrow);
   p.ncol = uint32_t(ncol);
   p.nvcol = uint32_t(nvcol);
@@ -297,7 +350,7 @@ int build_ew(const Prob& P, const float* const in[3], float* const out[2], uint3
 
 int build_red(const Prob& P, int xslot, const float* g, const float* a, const float* b,
               uint32_t read_mask, uint32_t stream_mask, float* x_out, float* d_out,
-              int vec_override, RedBuild* rb) {
+              int vec_override, int occ, RedBuild* rb) {
   RedPlan& p = rb->plan;
   p = RedPlan{};
   const int n = P.n;
@@ -346,8 +399,10 @@ int build_red(const Prob& P, int xslot, const float* g, const float* a, const fl
   uint64_t cap = total / (64 * std::max<uint64_t>(1, p.nout));
   cap = std::max<uint64_t>(1, std::min<uint64_t>(4096, cap));
 
-  uint32_t tx = pick_tx(nvcol);
+  const uint32_t tx_wide = pick_tx(nvcol);
+  uint32_t tx = tx_wide;
   uint64_t rows, vcols;
+  const uint64_t wave = uint64_t(kSms) * uint64_t(occ);
   if (p.inner_kept) {
     // Narrow the column lanes while that adds CTAs the slot cap would
     // otherwise forbid.
@@ -357,10 +412,37 @@ int build_red(const Prob& P, int xslot, const float* g, const float* a, const fl
       if (ctas >= 1216) break;
       tx /= 2;
     }
+    auto rows_for = [&](uint32_t t) {
+      uint64_t r = ceil_div(E, uint64_t(t) * vec);
+      r = std::max<uint64_t>(r, ceil_div(n_red, cap));
+      return std::min<uint64_t>(r, n_red);
+    };
+    rows = rows_for(tx);
+    // Grid: over column-lane widths from 32 to the widest, and row blocks
+    // in [n0 / 2, 2 n0], the shape whose CTA count fills the last wave best;
+    // one partial slot (no combine pass) is worth 0.02 of fill, and a plan
+    // with one slot keeps it.
+    auto real = [&](uint64_t n) { return ceil_div(n_red, ceil_div(n_red, n)); };
+    auto score = [&](uint32_t t, uint64_t n) {
+      const uint64_t nb = real(n);
+      return wave_fill(n_kept * ceil_div(nvcol, t) * nb, wave) - (nb > 1 ? 0.02 : 0.0);
+    };
+    uint32_t best_tx = tx;
+    uint64_t best_n = ceil_div(n_red, rows);
+    double best = score(tx, best_n);
+    for (uint32_t t = tx_wide; t >= 1; t /= 2) {
+      if (t < 32 && t != tx_wide) break;
+      const uint64_t n0 = ceil_div(n_red, rows_for(t));
+      const uint64_t lo = std::max<uint64_t>(1, n0 / 2);
+      const uint64_t hi = n0 == 1 ? 1 : std::min<uint64_t>({2 * n0, cap, n_red});
+      const uint64_t F = n_kept * ceil_div(nvcol, t);
+      const uint64_t n = fit_waves(n0, lo, std::max(hi, lo), F, wave, real);
+      const double sc = score(t, n);
+      if (sc > best + 1e-9) { best = sc; best_tx = t; best_n = n; }
+    }
+    tx = best_tx;
+    rows = ceil_div(n_red, best_n);
     vcols = tx;
-    rows = ceil_div(E, uint64_t(tx) * vec);
-    rows = std::max<uint64_t>(rows, ceil_div(n_red, cap));
-    rows = std::min<uint64_t>(rows, n_red);
   } else {
     if (nvcol * vec >= E) {
       vcols = ceil_div(ceil_div(E, vec), tx) * tx;
@@ -375,6 +457,29 @@ int build_red(const Prob& P, int xslot, const float* g, const float* a, const fl
       if (slots_now <= cap) break;
       if (rows < n_red) rows = std::min<uint64_t>(n_red, rows * 2);
       else vcols *= 2;
+    }
+    // Grid: row blocks (or, with one row per block, column blocks in
+    // multiples of tx vectors) whose CTA count fills the last wave best,
+    // keeping the slots within the cap; a plan with one slot keeps it.
+    const uint64_t n_cb = ceil_div(nvcol, vcols);
+    if (ceil_div(n_red, rows) * n_cb == 1) {
+      // one slot: no combine pass
+    } else if (rows > 1 || n_cb == 1) {
+      auto real = [&](uint64_t n) { return ceil_div(n_red, ceil_div(n_red, n)); };
+      const uint64_t n0 = ceil_div(n_red, rows);
+      const uint64_t lo = std::max<uint64_t>(1, n0 / 2);
+      const uint64_t hi = std::max(lo, std::min<uint64_t>({2 * n0, n_red, cap / n_cb}));
+      const uint64_t n = fit_waves(n0, lo, hi, n_kept * n_cb, wave, real);
+      rows = ceil_div(n_red, n);
+    } else {
+      auto width = [&](uint64_t n) {
+        return std::min<uint64_t>(ceil_div(nvcol, tx) * tx, ceil_div(ceil_div(nvcol, n), tx) * tx);
+      };
+      auto real = [&](uint64_t n) { return ceil_div(nvcol, width(n)); };
+      const uint64_t lo = std::max<uint64_t>(1, n_cb / 2);
+      const uint64_t hi = std::max(lo, std::min<uint64_t>(2 * n_cb, cap / std::max<uint64_t>(1, n_red)));
+      const uint64_t n = fit_waves(n_cb, lo, hi, n_kept * n_red, wave, real);
+      vcols = width(n);
     }
   }
   p.tx = tx;
@@ -741,7 +846,18 @@ int build_sabf(const Prob& P, const float* a, const float* b, float* out, SabFPl
   // About 512 KB written per CTA, and at least ~8 CTAs per SM in total.
   uint64_t chunk = std::max<uint64_t>(1, (512 * 1024) / (ta * ncol * 4));
   while (chunk > 1 && n_tiles * ceil_div(n_beta, chunk) < 1216) chunk /= 2;
-  p.beta_chunk = uint32_t(std::min<uint64_t>(chunk, n_beta));
+  chunk = std::min<uint64_t>(chunk, n_beta);
+  {
+    // Grid: chunks in [chunk / 2, 2 chunk] whose CTA count fills the last
+    // wave best.
+    auto real = [&](uint64_t n) { return ceil_div(n_beta, ceil_div(n_beta, n)); };
+    const uint64_t n0 = ceil_div(n_beta, chunk);
+    const uint64_t lo = ceil_div(n_beta, std::min<uint64_t>(n_beta, 2 * chunk));
+    const uint64_t hi = ceil_div(n_beta, std::max<uint64_t>(1, chunk / 2));
+    const uint64_t n = fit_waves(n0, lo, hi, n_tiles, uint64_t(kSms) * kOccSabf, real);
+    chunk = ceil_div(n_beta, n);
+  }
+  p.beta_chunk = uint32_t(chunk);
   p.n_bc = uint32_t(ceil_div(n_beta, p.beta_chunk));
   p.n_bc_div = make_fastdiv(p.n_bc);
   const uint64_t ncta = n_tiles * p.n_bc;

@@ -59,8 +59,9 @@ struct EwBuild {
   int vec;
 };
 // Elementwise plan over P with input slots 0..2 and output slot 3.
+// occ: resident CTAs per SM of the kernel that will run the plan.
 int build_ew(const Prob& P, const float* const in[3], float* const out[2], uint32_t read_mask,
-             uint32_t stream_mask, EwBuild* eb);
+             uint32_t stream_mask, int occ, EwBuild* eb);
 
 // Transposed-input forward plan; ZR_OK when the layout qualifies, 1 if not.
 int build_tr(const Prob& P, const float* a, const float* b, float* out, TrPlan* tp);
@@ -77,9 +78,10 @@ struct RedBuild {
 // vec_override: 0 = choose VEC from alignment; 1 or 4 = size the tiling as if
 // VEC were that value (used to report a workspace size that holds whatever
 // the alignment of the run-time pointers turns out to be).
+// occ: resident CTAs per SM of the kernel that will run the plan.
 int build_red(const Prob& P, int xslot, const float* g, const float* a, const float* b,
               uint32_t read_mask, uint32_t stream_mask, float* x_out, float* d_out,
-              int vec_override, RedBuild* rb);
+              int vec_override, int occ, RedBuild* rb);
 
 struct SabBuild {
   SabPlan plan;

@@ -338,6 +338,19 @@ def test_transposed_input_tiles():
                              f"transpose {op} y={yname} x_is_a={xa} out={oname}")
 
 
+def test_planner_occupancy_matches_runtime():
+    """The planner sizes grids in whole waves of 152 x (resident CTAs per SM);
+    its per-kernel occupancy must be what the runtime reports on this GPU."""
+    L = zr.lib()
+    L.zr_test_occupancy.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_int),
+                                    ctypes.POINTER(ctypes.c_int)]
+    for which in range(11):
+        planned, actual = ctypes.c_int(0), ctypes.c_int(0)
+        assert L.zr_test_occupancy(which, ctypes.byref(planned), ctypes.byref(actual)) == 0
+        assert planned.value == actual.value, (which, planned.value, actual.value)
+    assert L.zr_test_occupancy(11, ctypes.byref(planned), ctypes.byref(actual)) == -4
+
+
 def test_strided_output_and_in_place():
     rng = np.random.default_rng(9)
     a = torch.from_numpy(rng.standard_normal((33, 65)).astype(np.float32)).cuda()
