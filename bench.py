@@ -207,7 +207,7 @@ class Suite:
         self.L = zr.lib()
         self.torch = torch
         self.device = device
-        self.calls = []       # (config, kind, op, bytes, launches, fn)
+        self.calls = []       # (config, kind, op, bytes, launches, fn, elements)
         self.host = {}
         self.dev = {}
         self.in_names = {}
@@ -275,7 +275,7 @@ class Suite:
                 rc = L.zr_binary_fwd(opc, da, db, ptr, ost, stream_of())
                 if rc:
                     raise zr.ZrError(rc, f"{name} fwd {op}")
-            return (name, "fwd", op, nbytes, launches, fn)
+            return (name, "fwd", op, nbytes, launches, fn, sizes[on])
         _, op, gn, an, bn, gan, gbn = step
         dg, da, db = self._desc(env[gn]), self._desc(env[an]), self._desc(env[bn])
         pa, pb = env[gan].data_ptr(), env[gbn].data_ptr()
@@ -299,7 +299,7 @@ class Suite:
             rc = L.zr_binary_bwd(opc, dg, da, db, pa, pb, wsp, ctypes.byref(n), stream_of())
             if rc:
                 raise zr.ZrError(rc, f"{name} bwd {op}")
-        return (name, "bwd", op, nbytes, launches, fn)
+        return (name, "bwd", op, nbytes, launches, fn, sizes[gn])
 
     def step_bytes(self):
         return sum(c[3] for c in self.calls)
@@ -413,9 +413,10 @@ def run_zr(args, rank, world, local):
         total_ms = float(t.item())
     clocks = sampler.summary(t0, t1) if sampler else None
 
-    per_config = None
+    per_config = per_op_alone = None
     if rank == 0 and args.config_reps > 0:
-        per_config = run_per_config(suite, flush, stream, args.config_reps)
+        extra = [Suite(["x1"], device)] if args.workload == "suite" else []
+        per_config, per_op_alone = run_per_config([suite] + extra, flush, stream, args.config_reps)
     e2e = None
     if not args.no_e2e and rank == 0:
         e2e = run_e2e(args, suite, flush, stream, nbytes)
@@ -457,42 +458,55 @@ def run_zr(args, rank, world, local):
             "gpu_launches": suite.launches() * args.steps, "clocks": clocks, "per_op": per_op,
             "per_op_pass": f"untimed breakdown, {nb} steps with events around every op",
             "per_config": per_config,
+            "per_op_alone": per_op_alone,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
 
 
-def run_per_config(suite, flush, stream, reps, warm=5):
-    """Each workload's forward chain and backward chain timed on their own:
-    the median of ``reps`` CUDA-event timings after ``warm`` untimed runs,
-    with L2 flushed before every run.  GB/s = the phase's algorithmic bytes
-    over that median."""
+def run_per_config(suites, flush, stream, reps, warm=5):
+    """Each workload's forward chain and backward chain, and each op, timed on
+    its own: the median of ``reps`` CUDA-event timings after ``warm`` untimed
+    runs, with L2 flushed before every run.  GB/s = algorithmic bytes over
+    that median; elements/s = elements of the broadcast shape (per op) over
+    it.  The supplementary contiguous add ``x1`` is timed here only."""
     import torch
     peak, _ = measured_peak()
-    out = {}
-    for name in dict.fromkeys(c[0] for c in suite.calls):
-        for kind in ("fwd", "bwd"):
-            calls = [c for c in suite.calls if c[0] == name and c[1] == kind]
-            nbytes = sum(c[3] for c in calls)
-            ev = []
-            for r in range(warm + reps):
-                flush()
-                s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                s.record(stream)
-                for c in calls:
-                    c[5]()
-                e.record(stream)
-                if r >= warm:
-                    ev.append((s, e))
-            torch.cuda.synchronize()
-            ms = statistics.median(s.elapsed_time(e) for s, e in ev)
-            gbs = nbytes / (ms * 1e-3) / 1e9
-            out.setdefault(name, {})[kind] = {
-                "bytes": nbytes, "ms_median": round(ms, 5), "gbs": round(gbs, 1),
+
+    def time_calls(calls):
+        ev = []
+        for r in range(warm + reps):
+            flush()
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record(stream)
+            for c in calls:
+                c[5]()
+            e.record(stream)
+            if r >= warm:
+                ev.append((s, e))
+        torch.cuda.synchronize()
+        return statistics.median(s.elapsed_time(e) for s, e in ev)
+
+    def record(nbytes, nelem, ms):
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        return {"bytes": nbytes, "ms_median": round(ms, 5), "gbs": round(gbs, 1),
+                "elems_per_s": float(f"{nelem / (ms * 1e-3):.4g}"),
                 "pct_of_measured_hbm": round(gbs / peak, 4),
                 "pct_of_nominal_8000": round(gbs / NOMINAL_HBM_GBS, 4)}
-    return out
+
+    per_config, per_op = {}, []
+    for suite in suites:
+        for name in dict.fromkeys(c[0] for c in suite.calls):
+            for kind in ("fwd", "bwd"):
+                calls = [c for c in suite.calls if c[0] == name and c[1] == kind]
+                ms = time_calls(calls)
+                per_config.setdefault(name, {})[kind] = record(
+                    sum(c[3] for c in calls), sum(c[6] for c in calls), ms)
+                for c in calls:
+                    rec = record(c[3], c[6], time_calls([c]) if len(calls) > 1 else ms)
+                    per_op.append({"config": c[0], "kind": c[1], "op": c[2], **rec})
+    return per_config, per_op
 
 
 def run_e2e(args, suite, flush, stream, nbytes):

@@ -22,6 +22,9 @@ cases with the same structure):
 * ``c5b`` 8-d div: a [4,1,8,1,16,1,32,64] N(0,1); b = s*u with
   u U(0.5,1.5) [1,6,1,12,1,10,1,64] and s = 2*randint(0,2)-1 drawn after u;
   g N(0,1) of the broadcast shape [4,6,8,12,16,10,32,64]
+* ``x1`` same-shape contiguous add, a [R,C] N(0,1) + b [R,C] N(0,1), g N(0,1)
+  (4096,4096): a supplementary case for the contiguous path without
+  broadcasting (not one of the five workloads of the benchmark step)
 
 Each workload also lists its op steps (forward chain, then backward in
 reverse) as data: ``("fwd", op, a_name, b_name, out_name)`` and
@@ -31,7 +34,7 @@ from __future__ import annotations
 
 import torch
 
-SEEDS = {"c1": 1001, "c2": 1002, "c3": 1003, "c4": 1004, "c5a": 1005, "c5b": 1006}
+SEEDS = {"c1": 1001, "c2": 1002, "c3": 1003, "c4": 1004, "c5a": 1005, "c5b": 1006, "x1": 1007}
 
 DEFAULT_DIMS = {
     "c1": dict(P=32, M=64, Q=128),
@@ -40,6 +43,7 @@ DEFAULT_DIMS = {
     "c4": dict(N=8, H=12, T=1024),
     "c5a": dict(P=128, M=256, Q=512),
     "c5b": dict(a=(4, 1, 8, 1, 16, 1, 32, 64), b=(1, 6, 1, 12, 1, 10, 1, 64)),
+    "x1": dict(R=4096, C=4096),
 }
 
 # Forward chain then backward steps, in execution order.
@@ -60,6 +64,8 @@ STEPS = {
             ("bwd", "sub", "g", "a", "b", "grad_a", "grad_b")],
     "c5b": [("fwd", "div", "a", "b", "out"),
             ("bwd", "div", "g", "a", "b", "grad_a", "grad_b")],
+    "x1": [("fwd", "add", "a", "b", "out"),
+           ("bwd", "add", "g", "a", "b", "grad_a", "grad_b")],
 }
 
 NAMES = list(STEPS)
@@ -134,6 +140,12 @@ def make_inputs(name: str, seed: int | None = None, **dims) -> dict:
         b = s * u
         g = _normal(gen, _broadcast_dims(sa, sb))
         return dict(a=a, b=b, g=g)
+    if name == "x1":
+        R, C = d["R"], d["C"]
+        a = _normal(gen, (R, C))
+        b = _normal(gen, (R, C))
+        g = _normal(gen, (R, C))
+        return dict(a=a, b=b, g=g)
     raise KeyError(name)
 
 
@@ -147,4 +159,5 @@ def small_dims(name: str) -> dict:
         "c4": dict(N=2, H=3, T=131),
         "c5a": dict(P=5, M=67, Q=203),
         "c5b": dict(a=(3, 1, 5, 1, 4, 1, 7, 12), b=(1, 2, 1, 3, 1, 5, 1, 12)),
+        "x1": dict(R=333, C=1030),
     }[name]
