@@ -303,13 +303,15 @@ int plan_bwd(int op, const zr_tensor& tg, const zr_tensor& ta, const zr_tensor& 
     const uint32_t rm = 1u | (ra ? 2u : 0u) | (rbb ? 4u : 0u);
     RedBuild& rb = S->rb[S->nred];
     const int occ = (op == OP_MUL || op == OP_DIV) ? kOccRedMulDiv : kOccRedAddSub;
+    const int ock = red_cl_occ(op, true), ocr = red_cl_occ(op, false);
     rc = build_red(P, xslot, S->g.ptr, ra ? S->a.ptr : nullptr, rbb ? S->b.ptr : nullptr, rm,
-                   stream_mask & rm, xo, d_out, 0, occ, &rb);
+                   stream_mask & rm, xo, d_out, 0, occ, ock, ocr, &rb);
     if (rc) return rc;
     size_t q = rb.ws_bytes;
     for (int v : {1, 4}) {
       RedBuild tmp;
-      rc = build_red(P, xslot, S->g.ptr, nullptr, nullptr, rm, 0, xo, d_out, v, occ, &tmp);
+      rc = build_red(P, xslot, S->g.ptr, nullptr, nullptr, rm, 0, xo, d_out, v, occ, ock, ocr,
+                     &tmp);
       if (rc) return rc;
       q = std::max(q, tmp.ws_bytes);
     }
@@ -394,14 +396,15 @@ int plan_sum(const zr_tensor& tin, int32_t ndo, const int64_t* so, float* out, S
   grad_index_strides(S->out, n, S->in.size, st[kSlotXA]);
   rc = coalesce(n, S->in.size, st, 1u | (1u << kSlotXA), -1, &P);
   if (rc) return rc;
+  const int ock = red_cl_occ(OP_ADD, true), ocr = red_cl_occ(OP_ADD, false);
   rc = build_red(P, kSlotXA, S->in.ptr, nullptr, nullptr, 1u, 1u, out, nullptr, 0, kOccRedAddSub,
-                 &S->rb);
+                 ock, ocr, &S->rb);
   if (rc) return rc;
   S->ws_query = S->rb.ws_bytes;
   for (int v : {1, 4}) {
     RedBuild tmp;
     rc = build_red(P, kSlotXA, S->in.ptr, nullptr, nullptr, 1u, 0, out, nullptr, v, kOccRedAddSub,
-                   &tmp);
+                   ock, ocr, &tmp);
     if (rc) return rc;
     S->ws_query = std::max(S->ws_query, tmp.ws_bytes);
   }
@@ -687,6 +690,7 @@ int zr_test_occupancy(int which, int* planned, int* actual) {
   if (which >= 0 && which < 4) e = occupancy_ew(which, planned, actual);
   else if (which >= 4 && which < 9) e = occupancy_red(which - 4, planned, actual);
   else if (which >= 9 && which < 11) e = occupancy_other(which - 9, planned, actual);
+  else if (which >= 11 && which < 16) e = occupancy_red(which - 6, planned, actual);
   else return ZR_ERR_SIZE;
   return cuda_status(e);
 }

@@ -12,8 +12,10 @@
 
 #if defined(__CUDACC__)
 #define ZR_HD __host__ __device__ __forceinline__
+#define ZR_CX __host__ __device__ constexpr
 #else
 #define ZR_HD inline
+#define ZR_CX constexpr
 #endif
 
 namespace zr {
@@ -143,6 +145,24 @@ constexpr int kOccEwBwd = 3;      // k_elementwise: backward without reduction
 constexpr int kOccEwCopy = 5;     // k_elementwise: copy (sum-to-shape onto the same shape)
 constexpr int kOccRedAddSub = 4;  // k_reduce: add, sub, sum-to-shape
 constexpr int kOccRedMulDiv = 3;  // k_reduce: mul, div
+// k_reduce, cluster variant (no second pass): loads per item are 1 for add,
+// sub and sum-to-shape, 2 for mul and div (the reduced gradient's own input
+// is loaded once per thread, the other one per item).  Items in flight per
+// thread: 8 with one load each, 4 with two.  Inner-reduced plans with one
+// load per item keep 4 CTAs per SM, the others 3.
+ZR_CX int red_cl_loads(int op) { return (op == OP_MUL || op == OP_DIV) ? 2 : 1; }
+ZR_CX int red_cl_unroll(int op) { return red_cl_loads(op) == 1 ? 8 : 4; }
+ZR_CX int red_cl_occ(int op, bool inner_kept) {
+  return (!inner_kept && red_cl_loads(op) == 1) ? 4 : 3;
+}
+constexpr uint32_t kMaxCluster = 8;   // CTAs per cluster (the portable limit)
+// CTAs of a cluster plan that can be resident at once, out of a full wave of
+// `wave` CTAs: clusters must fit within one GPC, which strands slots as the
+// cluster grows (measured on GB300 at 3 and 4 CTAs per SM: pairs keep the
+// whole wave, up to 4 CTAs about 15/16 of it, up to 8 about 7/8).
+ZR_CX uint64_t cluster_wave(uint64_t wave, uint64_t c) {
+  return c <= 2 ? wave : (c <= 4 ? wave * 15 / 16 : wave * 7 / 8);
+}
 constexpr int kOccSabf = 3;       // k_sabf
 constexpr int kOccTr = 4;         // k_transpose
 // k_transpose: 8 warps x 16 p rows, 8 lanes x 4 q columns.
@@ -200,14 +220,37 @@ struct RedPlan {
   uint32_t nslots;          // partial slots per output (1 = final write)
   uint32_t n_cta;
   float scale;              // multiplies X's final value (1 except as noted)
+  // Cluster plans (cluster > 1): the CTAs that cover one output tile run as
+  // one thread-block cluster of `cluster` CTAs, and the cluster's rank-0 CTA
+  // adds their results in rank order from distributed shared memory, so
+  // there are no partial slots and no second pass.  Inner dim kept: a tile is
+  // (kept index, column block), rank = row block.  Inner dim reduced: a tile
+  // is a kept index, rank = row block * n_cblk + column block.
+  uint32_t cluster;
+  FastDiv cluster_div;
 };
 
 struct RedCta {
   uint32_t kidx, rblk, cblk;
 };
-// CTA order: column blocks fastest, then row blocks, then kept index.
+// CTA order: column blocks fastest, then row blocks, then kept index; in a
+// cluster plan, cluster rank fastest, then tile.
 ZR_HD RedCta red_cta(const RedPlan& p, uint32_t cta) {
   RedCta c;
+  if (p.cluster > 1) {
+    const uint32_t tile = fd_div(p.cluster_div, cta);
+    const uint32_t rank = cta - tile * p.cluster;
+    if (p.inner_kept) {
+      c.rblk = rank;
+      c.kidx = fd_div(p.n_cblk_div, tile);
+      c.cblk = tile - c.kidx * p.n_cblk;
+    } else {
+      c.kidx = tile;
+      c.rblk = fd_div(p.n_cblk_div, rank);
+      c.cblk = rank - c.rblk * p.n_cblk;
+    }
+    return c;
+  }
   const uint32_t t = fd_div(p.n_cblk_div, cta);
   c.cblk = cta - t * p.n_cblk;
   c.kidx = fd_div(p.n_rblk_div, t);

@@ -69,6 +69,30 @@ __device__ __forceinline__ void pdl_wait() {
   asm volatile("griddepcontrol.wait;\n" ::: "memory");
 }
 
+// Thread-block clusters.  cluster_sync(): every thread of every CTA of the
+// cluster arrives (release: this CTA's shared-memory writes become visible
+// to the cluster) and waits for all (acquire).  All CTAs of a cluster are
+// resident together by construction, so the wait always ends.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n"
+               "barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(r));
+  return r;
+}
+// The float at the same shared-memory offset as `local` in CTA `rank` of
+// this cluster (distributed shared memory).
+__device__ __forceinline__ float ld_cluster(const float* local, uint32_t rank) {
+  const uint32_t la = static_cast<uint32_t>(__cvta_generic_to_shared(local));
+  uint32_t ra;
+  float v;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(ra) : "r"(la), "r"(rank));
+  asm volatile("ld.shared::cluster.f32 %0, [%1];\n" : "=f"(v) : "r"(ra) : "memory");
+  return v;
+}
+
 struct Kahan {
   float s, c;
   __device__ __forceinline__ void init() { s = 0.f; c = 0.f; }
@@ -418,8 +442,17 @@ struct RedTerms {
 // thread adds its rows and columns into one value and the CTA reduces them
 // with a fixed tree.  Per-thread sums are Kahan-compensated, so the error
 // bound does not grow with the number of rows a thread adds.
-template <int OP, int WHICH, int VEC, bool INNER_KEPT>
-__global__ void __launch_bounds__(kThreads, (OP == OP_MUL || OP == OP_DIV) ? kOccRedMulDiv : kOccRedAddSub)
+//
+// CL (cluster plans): the CTAs of one output tile form a cluster; each keeps
+// its tree result in shared memory, and after a cluster barrier the rank-0
+// CTA adds the cluster's results in rank order and writes X.  A second
+// barrier keeps every CTA resident until the leader has read it.  CL kernels
+// keep more items in flight per thread (red_cl_unroll).
+template <int OP, int WHICH, int VEC, bool INNER_KEPT, bool CL = false>
+__global__ void __launch_bounds__(kThreads,
+                                  CL ? red_cl_occ(OP, INNER_KEPT)
+                                     : ((OP == OP_MUL || OP == OP_DIV) ? kOccRedMulDiv
+                                                                      : kOccRedAddSub))
 k_reduce(const __grid_constant__ RedPlan p) {
   pdl_trigger();
   using T = RedTerms<OP, WHICH>;
@@ -488,7 +521,7 @@ k_reduce(const __grid_constant__ RedPlan p) {
     const uint32_t nrs = nch > ty ? (nch - ty + p.ty - 1) / p.ty : 0;
     const uint32_t items = ncs * nrs;
     uint32_t rm = 0, cm = 0;
-    constexpr int U = 4;
+    constexpr int U = CL ? red_cl_unroll(OP) : 4;
     for (uint32_t m0 = 0; m0 < items; m0 += U) {
       Vec<VEC> gv[U], av[U], bv[U];
       uint32_t ri[U], cc[U];
@@ -543,6 +576,24 @@ k_reduce(const __grid_constant__ RedPlan p) {
       }
     }
     __syncthreads();
+    if (CL) {
+      // s_red[0, lanes) holds this CTA's column sums; the leader adds the
+      // cluster's in rank order.
+      cluster_sync();
+      if (cluster_rank() == 0) {
+        for (uint32_t v = threadIdx.x; v < lanes; v += blockDim.x) {
+          const uint32_t vcv = vcol_begin + v / VEC;
+          const uint32_t col = vcv * VEC + v % VEC;
+          if (vcv >= vcol_end || col >= p.ncol) continue;
+          float r = ld_cluster(s_red + v, 0);
+          for (uint32_t k = 1; k < p.cluster; ++k) r = __fadd_rn(r, ld_cluster(s_red + v, k));
+          if (T::kPost) r = __fmul_rn(r, T::post(__ldg(p.b + base[2] + int64_t(col) * p.inner_stride[2])));
+          p.x_final[uint64_t(cta.kidx) * p.ncol + col] = __fmul_rn(r, p.scale);
+        }
+      }
+      cluster_sync();
+      return;
+    }
     const uint32_t vc = vcol_begin + tx;
     if (ty == 0 && vc < vcol_end) {
       Vec<VEC> r;
@@ -572,6 +623,17 @@ k_reduce(const __grid_constant__ RedPlan p) {
       __syncthreads();
       if (threadIdx.x < h) s_red[threadIdx.x] = __fadd_rn(s_red[threadIdx.x], s_red[threadIdx.x + h]);
     }
+    if (CL) {
+      cluster_sync();
+      if (cluster_rank() == 0 && threadIdx.x == 0) {
+        float r = ld_cluster(s_red, 0);
+        for (uint32_t k = 1; k < p.cluster; ++k) r = __fadd_rn(r, ld_cluster(s_red, k));
+        if (T::kPost) r = __fmul_rn(r, T::post(__ldg(p.b + base[2])));
+        p.x_final[cta.kidx] = __fmul_rn(r, p.scale);
+      }
+      cluster_sync();
+      return;
+    }
     if (threadIdx.x == 0) {
       float r = s_red[0];
       if (T::kPost) r = __fmul_rn(r, T::post(__ldg(p.b + base[2])));
@@ -599,18 +661,18 @@ k_combine(const __grid_constant__ CombinePlan p) {
   Kahan acc;
   acc.init();
   if (j < p.nout && sl < p.sy) {
-    // Eight partials are loaded before any is added, so their loads overlap.
+    // Up to eight partials are loaded before any is added, so their loads
+    // overlap (a ragged last batch is predicated, not walked one by one).
     const float* src = p.partial + uint64_t(sl) * p.nout + j;
     const uint64_t step = uint64_t(p.sy) * p.nout;
-    uint32_t s = sl;
-    for (; s + 7 * p.sy < p.nslots; s += 8 * p.sy, src += 8 * step) {
+    for (uint32_t s = sl; s < p.nslots; s += 8 * p.sy, src += 8 * step) {
       float v[8];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) v[u] = __ldg(src + u * step);
+      for (int u = 0; u < 8; ++u) v[u] = s + u * p.sy < p.nslots ? __ldg(src + u * step) : 0.f;
 #pragma unroll
-      for (int u = 0; u < 8; ++u) acc.add(v[u]);
+      for (int u = 0; u < 8; ++u)
+        if (s + u * p.sy < p.nslots) acc.add(v[u]);
     }
-    for (; s < p.nslots; s += p.sy, src += step) acc.add(__ldg(src));
   }
   const uint32_t syn = blockDim.x / p.jx;  // power of two
   s_red[sl * p.jx + jl] = (sl < p.sy) ? acc.s : 0.f;

@@ -29,6 +29,35 @@ inline cudaError_t launch_k(void (*kernel)(KArgs...), unsigned grid, unsigned bl
   return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
+// The same launch with the grid split into thread-block clusters of
+// `cluster` CTAs along x.  Sizes above 8 are non-portable and need the
+// kernel's opt-in attribute, which is set on first use.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_k_cluster(void (*kernel)(KArgs...), unsigned grid, unsigned block,
+                                    size_t smem, cudaStream_t s, unsigned cluster,
+                                    const Args&... args) {
+  if (cluster > 8) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = cluster;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // Every launcher first checks that the plan provides each operand its kernel
 // dereferences (cudaErrorInvalidValue otherwise); with dry == true it stops
 // there and launches nothing.
@@ -49,7 +78,7 @@ cudaError_t launch_reduce(int op, int which, const RedBuild& rb, cudaStream_t s,
 // assumes (*planned) and as the runtime reports for the current device
 // (*actual).  ew: 0 fwd add, 1 fwd div, 2 bwd div (both gradients), 3 copy;
 // red: 0 add inner kept, 1 sub inner reduced, 2 mul inner kept, 3 div inner
-// reduced, 4 sum-to-shape; other: 0 k_sabf (8 rows per thread), 1 k_transpose.
+// reduced, 4 sum-to-shape; 5..9 the same five as cluster variants; other: 0 k_sabf (8 rows per thread), 1 k_transpose.
 cudaError_t occupancy_ew(int which, int* planned, int* actual);
 cudaError_t occupancy_red(int which, int* planned, int* actual);
 cudaError_t occupancy_other(int which, int* planned, int* actual);

@@ -17,11 +17,21 @@ cudaError_t launch_red_t(const RedBuild& rb, cudaStream_t s, bool dry) {
       (RedTerms<OP, WHICH>::reads_b(has_d) && !p.b) || !p.x_final ||
       (p.nslots > 1 && !p.partial))
     return cudaErrorInvalidValue;
+  if (p.cluster > 1 && (rb.vec != 4 || p.nslots != 1 || p.n_cta % p.cluster != 0 ||
+                        p.cluster > kMaxCluster))
+    return cudaErrorInvalidValue;
   if (dry) return cudaSuccess;
   const uint32_t table_rows = p.rows_per_blk < kMaxTileRows ? p.rows_per_blk : kMaxTileRows;
   const size_t red_floats = p.inner_kept ? size_t(kThreads) * rb.vec : size_t(kThreads);
   const size_t smem = size_t(table_rows) * kMaxOperands * sizeof(int64_t) + red_floats * sizeof(float);
   cudaError_t e;
+  if (p.cluster > 1) {
+    return p.inner_kept
+               ? launch_k_cluster(k_reduce<OP, WHICH, 4, true, true>, p.n_cta, kThreads, smem, s,
+                                  p.cluster, p)
+               : launch_k_cluster(k_reduce<OP, WHICH, 4, false, true>, p.n_cta, kThreads, smem, s,
+                                  p.cluster, p);
+  }
   if (p.inner_kept) {
     e = rb.vec == 4 ? launch_k(k_reduce<OP, WHICH, 4, true>, p.n_cta, kThreads, smem, s, p)
                     : launch_k(k_reduce<OP, WHICH, 1, true>, p.n_cta, kThreads, smem, s, p);
@@ -68,6 +78,26 @@ cudaError_t occupancy_red(int which, int* planned, int* actual) {
       *planned = kOccRedAddSub;
       return cudaOccupancyMaxActiveBlocksPerMultiprocessor(actual, k_reduce<OP_ADD, 2, 4, true>,
                                                            kThreads, smem);
+    case 5:
+      *planned = red_cl_occ(OP_ADD, true);
+      return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+          actual, k_reduce<OP_ADD, 1, 4, true, true>, kThreads, smem);
+    case 6:
+      *planned = red_cl_occ(OP_SUB, false);
+      return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+          actual, k_reduce<OP_SUB, 1, 4, false, true>, kThreads, smem);
+    case 7:
+      *planned = red_cl_occ(OP_MUL, true);
+      return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+          actual, k_reduce<OP_MUL, 1, 4, true, true>, kThreads, smem);
+    case 8:
+      *planned = red_cl_occ(OP_DIV, false);
+      return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+          actual, k_reduce<OP_DIV, 1, 4, false, true>, kThreads, smem);
+    case 9:
+      *planned = red_cl_occ(OP_ADD, true);
+      return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+          actual, k_reduce<OP_ADD, 2, 4, true, true>, kThreads, smem);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -350,7 +350,7 @@ int build_ew(const Prob& P, const float* const in[3], float* const out[2], uint3
 
 int build_red(const Prob& P, int xslot, const float* g, const float* a, const float* b,
               uint32_t read_mask, uint32_t stream_mask, float* x_out, float* d_out,
-              int vec_override, int occ, RedBuild* rb) {
+              int vec_override, int occ, int occ_cl_kept, int occ_cl_red, RedBuild* rb) {
   RedPlan& p = rb->plan;
   p = RedPlan{};
   const int n = P.n;
@@ -482,6 +482,42 @@ int build_red(const Prob& P, int xslot, const float* g, const float* a, const fl
       vcols = width(n);
     }
   }
+  // Combine-free alternative: when the plan above needs partial slots and
+  // 16-byte vectors apply, let the CTAs of one output tile form a cluster
+  // (at most kMaxCluster CTAs) that covers every reduced row, so the tile's
+  // total is formed on chip and no second pass runs.  Taken, widest column
+  // lanes first, when its grid is resident at once (cluster_wave) and fills
+  // three quarters of a wave or has at least as many CTAs as the plan above.
+  p.cluster = 1;
+  const uint64_t std_slots = p.inner_kept ? ceil_div(n_red, rows)
+                                          : ceil_div(n_red, rows) * ceil_div(nvcol, vcols);
+  const uint64_t std_ctas = n_kept * ceil_div(n_red, rows) * ceil_div(nvcol, vcols);
+  const int occ_cl = p.inner_kept ? occ_cl_kept : occ_cl_red;
+  if (occ_cl > 0 && vec == 4 && std_slots > 1) {
+    const uint64_t wave_cl = uint64_t(kSms) * uint64_t(occ_cl);
+    // Inner dim kept: column lanes from the widest down to 8 (128-byte row
+    // segments), tiles = kept index x column block; reduced: tiles = kept
+    // indices, each CTA covering whole rows.
+    for (uint32_t t = p.inner_kept ? tx_wide : pick_tx(nvcol); t >= 8; t /= 2) {
+      const uint64_t vc = p.inner_kept ? t : ceil_div(nvcol, t) * t;
+      const uint64_t tiles = n_kept * ceil_div(nvcol, vc);
+      uint64_t c_max = std::min<uint64_t>({kMaxCluster, wave_cl / tiles, n_red});
+      while (c_max > 1 && tiles * c_max > cluster_wave(wave_cl, c_max)) --c_max;
+      if (c_max >= 1) {
+        const uint64_t r = ceil_div(n_red, c_max);
+        const uint64_t c = ceil_div(n_red, r);
+        const uint64_t need = std::min<uint64_t>(ceil_div(3 * wave_cl, 4), std_ctas);
+        if (c >= 2 && tiles * c >= need && r >= kThreads / t) {
+          tx = t;
+          vcols = vc;
+          rows = r;
+          p.cluster = uint32_t(c);
+          break;
+        }
+      }
+      if (!p.inner_kept) break;
+    }
+  }
   p.tx = tx;
   p.ty = kThreads / tx;
   p.rows_per_blk = uint32_t(rows);
@@ -490,7 +526,8 @@ int build_red(const Prob& P, int xslot, const float* g, const float* a, const fl
   p.n_cblk = uint32_t(ceil_div(nvcol, vcols));
   p.n_cblk_div = make_fastdiv(p.n_cblk);
   p.n_rblk_div = make_fastdiv(p.n_rblk);
-  p.nslots = p.inner_kept ? p.n_rblk : p.n_rblk * p.n_cblk;
+  p.nslots = p.cluster > 1 ? 1 : (p.inner_kept ? p.n_rblk : p.n_rblk * p.n_cblk);
+  p.cluster_div = make_fastdiv(p.cluster);
   const uint64_t ncta = n_kept * p.n_rblk * uint64_t(p.n_cblk);
   if (ncta >= (uint64_t(1) << 31)) return ZR_ERR_SIZE;
   p.n_cta = uint32_t(ncta);
@@ -594,10 +631,11 @@ std::string describe_red(const RedBuild& rb) {
                 "{\"kernel\":\"reduce\",\"vec\":%d,\"inner_kept\":%u,\"n_kept\":%u,\"n_red\":%u,"
                 "\"ncol\":%u,\"kept_dims\":%d,\"red_dims\":%d,\"tx\":%u,\"ty\":%u,"
                 "\"rows_per_blk\":%u,\"vcols_per_blk\":%u,\"n_rblk\":%u,\"n_cblk\":%u,"
-                "\"nslots\":%u,\"nout\":%llu,\"ctas\":%u,\"ws_bytes\":%zu,\"dense_out\":%d}",
+                "\"nslots\":%u,\"nout\":%llu,\"ctas\":%u,\"ws_bytes\":%zu,\"dense_out\":%d,"
+                "\"cluster\":%u}",
                 rb.vec, p.inner_kept, p.n_kept, p.n_red, p.ncol, p.kept.n, p.red.n, p.tx, p.ty,
                 p.rows_per_blk, p.vcols_per_blk, p.n_rblk, p.n_cblk, p.nslots,
-                (unsigned long long)p.nout, p.n_cta, rb.ws_bytes, p.d_out ? 1 : 0);
+                (unsigned long long)p.nout, p.n_cta, rb.ws_bytes, p.d_out ? 1 : 0, p.cluster);
   return buf;
 }
 

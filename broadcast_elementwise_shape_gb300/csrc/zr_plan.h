@@ -78,10 +78,12 @@ struct RedBuild {
 // vec_override: 0 = choose VEC from alignment; 1 or 4 = size the tiling as if
 // VEC were that value (used to report a workspace size that holds whatever
 // the alignment of the run-time pointers turns out to be).
-// occ: resident CTAs per SM of the kernel that will run the plan.
+// occ: resident CTAs per SM of the kernel that will run the plan;
+// occ_cl_kept / occ_cl_red: the same for the cluster variant with the inner
+// dim kept / reduced (0: no cluster plan).
 int build_red(const Prob& P, int xslot, const float* g, const float* a, const float* b,
               uint32_t read_mask, uint32_t stream_mask, float* x_out, float* d_out,
-              int vec_override, int occ, RedBuild* rb);
+              int vec_override, int occ, int occ_cl_kept, int occ_cl_red, RedBuild* rb);
 
 struct SabBuild {
   SabPlan plan;

@@ -252,7 +252,10 @@ def test_emulated_backward_matches_naive(L, op):
             if plan["kernel"] in ("reduce", "sab"):
                 which = desc["which"][pi]
                 np.testing.assert_array_equal(rows[:, 4], (xa if which == 0 else xb)[ref])
-                assert rows[:, 5].min() >= 0 and rows[:, 5].max() < plan["nslots"]
+                # slot: the partial the term goes to (a workspace slot, or
+                # the CTA's rank in a cluster plan)
+                bound = plan["nslots"] if plan.get("cluster", 1) <= 1 else plan["cluster"]
+                assert rows[:, 5].min() >= 0 and rows[:, 5].max() < bound
                 if plan.get("dense_out"):
                     np.testing.assert_array_equal(rows[:, 6], dense[ref])
             else:

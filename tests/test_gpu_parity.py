@@ -10,6 +10,7 @@ inputs, through the C ABI (Python binding).  Needs a CUDA GPU (GB300).
 * bitwise run-to-run determinism and host-side error reporting.
 """
 import ctypes
+import json
 
 import numpy as np
 import pytest
@@ -18,7 +19,8 @@ import torch
 import broadcast_elementwise_shape_gb300 as zr
 import oracle
 import workloads
-from parity import bitexact, compare_workload, run_gpu, run_oracle, to_gpu, within
+from parity import (bitexact, compare_workload, is_single_op_grad, run_gpu, run_oracle, to_gpu,
+                    within)
 
 pytestmark = pytest.mark.gpu
 
@@ -344,11 +346,11 @@ def test_planner_occupancy_matches_runtime():
     L = zr.lib()
     L.zr_test_occupancy.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_int),
                                     ctypes.POINTER(ctypes.c_int)]
-    for which in range(11):
+    for which in range(16):
         planned, actual = ctypes.c_int(0), ctypes.c_int(0)
         assert L.zr_test_occupancy(which, ctypes.byref(planned), ctypes.byref(actual)) == 0
         assert planned.value == actual.value, (which, planned.value, actual.value)
-    assert L.zr_test_occupancy(11, ctypes.byref(planned), ctypes.byref(actual)) == -4
+    assert L.zr_test_occupancy(16, ctypes.byref(planned), ctypes.byref(actual)) == -4
 
 
 def test_strided_output_and_in_place():
@@ -438,6 +440,94 @@ def test_both_reduced_fused_pass(op):
         ga2, gb2 = zr.zr_binary_bwd(op, g.cuda(), a.cuda(), b.cuda())
         assert torch.equal(ga.view(torch.int32), ga2.view(torch.int32))
         assert torch.equal(gb.view(torch.int32), gb2.view(torch.int32))
+
+
+def _bwd_plans(op, g, a, b, ga, gb):
+    L = zr.lib()
+    L.zr_test_describe_bwd.argtypes = [ctypes.c_int, zr.ZrTensor, zr.ZrTensor, zr.ZrTensor,
+                                       ctypes.c_void_p, ctypes.c_void_p, ctypes.c_char_p,
+                                       ctypes.c_size_t]
+    dg, kg = zr._desc(g)
+    da, ka = zr._desc(a)
+    db, kb = zr._desc(b)
+    buf = ctypes.create_string_buffer(16384)
+    assert L.zr_test_describe_bwd(zr.OPS[op], dg, da, db, ga.data_ptr(), gb.data_ptr(), buf,
+                                  16384) == 0
+    return json.loads(buf.value.decode())["plans"]
+
+
+def _sum_plan(x, shape):
+    L = zr.lib()
+    L.zr_test_describe_sum.argtypes = [zr.ZrTensor, ctypes.c_int32,
+                                       ctypes.POINTER(ctypes.c_int64), ctypes.c_void_p,
+                                       ctypes.c_char_p, ctypes.c_size_t]
+    dx, kx = zr._desc(x)
+    out = torch.empty(shape, device="cuda")
+    buf = ctypes.create_string_buffer(16384)
+    assert L.zr_test_describe_sum(dx, len(shape), zr._i64(shape), out.data_ptr(), buf,
+                                  16384) == 0
+    return json.loads(buf.value.decode())["plans"][0]
+
+
+CLUSTER_SHAPES = [
+    ((256, 1024), (1024,)),          # inner dim kept, 2 column blocks
+    ((2048, 1024), (1024,)),
+    ((4096, 1024), (1024,)),         # partial slots (too many tiles for clusters)
+    ((16, 1024, 768), (768,)),
+    ((3, 97, 772), (772,)),
+    ((517, 1028), (1028,)),          # ragged rows and column tiles
+    ((1028,), (517, 1028)),          # grad_a reduced
+    ((128, 256, 512), (1, 256, 1)),  # inner dim reduced
+    ((64, 200, 256), (1, 200, 1)),
+    ((8, 100, 1024), (1, 100, 1)),
+    ((1, 333, 1), (40, 333, 128)),   # too many tiles for a cluster plan
+]
+
+
+@pytest.mark.parametrize("op", OPS)
+def test_cluster_reduction(op):
+    """Backward plans whose reduced gradient is summed by thread-block
+    clusters (no partial slots, no second pass), element by element against
+    the oracle, and bitwise stable across calls."""
+    rng = np.random.default_rng(400 + OPS.index(op))
+    seen = set()
+    for sa, sb in CLUSTER_SHAPES:
+        a = torch.from_numpy(rng.standard_normal(sa).astype(np.float32))
+        b = torch.from_numpy((np.sign(rng.standard_normal(sb)) * (0.5 + rng.random(sb))).astype(np.float32))
+        g = torch.from_numpy(rng.standard_normal(np.broadcast_shapes(sa, sb)).astype(np.float32))
+        ga_d, gb_d = torch.empty(sa, device="cuda"), torch.empty(sb, device="cuda")
+        ad, bd, gd = a.cuda(), b.cuda(), g.cuda()
+        for plan in _bwd_plans(op, gd, ad, bd, ga_d, gb_d):
+            if plan.get("cluster", 1) > 1:
+                assert plan["nslots"] == 1 and plan["ws_bytes"] == 0, plan
+                seen.add(plan["inner_kept"])
+        ga, gb = zr.zr_binary_bwd(op, gd, ad, bd, grad_a=ga_d, grad_b=gb_d)
+        ra, rb, s1, s2 = oracle.binary_bwd(op, g, a, b)
+        for which, got, ref, sabs, shape in ((0, ga, ra, s1, sa), (1, gb, rb, s2, sb)):
+            reduced = int(np.prod(shape)) != g.numel()
+            what = f"cluster {op} grad_{'ab'[which]} {sa} {sb}"
+            if is_single_op_grad(op, which, reduced):
+                bitexact(got.cpu().numpy(), ref, what)
+            else:
+                within(got.cpu().numpy(), ref, sabs, what)
+        ga2, gb2 = zr.zr_binary_bwd(op, gd, ad, bd)
+        assert torch.equal(ga.view(torch.int32), ga2.view(torch.int32))
+        assert torch.equal(gb.view(torch.int32), gb2.view(torch.int32))
+    # Cluster plans with the inner dim kept and with it reduced were covered.
+    assert seen == {0, 1}, seen
+
+
+def test_cluster_sum_to_shape():
+    rng = np.random.default_rng(17)
+    for shape, target in (((2048, 1024), (1024,)), ((517, 1028), (1, 1028)),
+                          ((8, 100, 1024), (1, 100, 1)), ((128, 256, 512), (1, 256, 1))):
+        x = torch.from_numpy(rng.standard_normal(shape).astype(np.float32))
+        xd = x.cuda()
+        plan = _sum_plan(xd, target)
+        assert plan.get("cluster", 1) > 1, plan
+        got = zr.zr_sum_to_shape(xd, target).cpu().numpy()
+        ref, sabs = oracle.sum_to_shape(x, target)
+        within(got, ref, sabs, f"cluster sum_to_shape {shape}->{target}")
 
 
 def _rand_bits(rng, shape):

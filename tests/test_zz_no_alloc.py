@@ -68,9 +68,10 @@ def _check(op, host_g, host_a, host_b, got, ref):
 def test_noalloc_matches_workspace_entry_point_twice(L):
     # First call: 8-d div with both gradients reduced (uses the scratch).
     h1 = workloads.make_inputs("c5b", **workloads.small_dims("c5b"))
-    # Second call: bias-add backward, a column sum over many rows (uses the
-    # scratch too, with a different layout of partials).
-    h2 = workloads.make_inputs("c2", R=4096, C=1024)
+    # Second call: bias-add backward, a column sum over many rows; rows of
+    # 1030 floats rule out 16-byte vectors, so the sum goes through partial
+    # slots in the scratch too, with a different layout of partials.
+    h2 = workloads.make_inputs("c2", R=4096, C=1030)
     cases = [("div", h1["g"], h1["a"], h1["b"]), ("add", h2["g"], h2["x"], h2["bias"])]
     for op, g, a, b in cases:
         dg, da, db = to_gpu(g), to_gpu(a), to_gpu(b)
@@ -81,11 +82,11 @@ def test_noalloc_matches_workspace_entry_point_twice(L):
 
 
 def test_noalloc_rejects_problems_beyond_the_scratch(L):
-    # [4096, 65536] + [65536]: the column sum's partials need more than the
-    # fixed array holds.
-    g = torch.zeros((4096, 65536), device="cuda")
-    x = torch.zeros((4096, 65536), device="cuda")
-    bias = torch.zeros((65536,), device="cuda")
+    # [8192, 65535] + [65535]: the column sum's partials (64 slots of 65535
+    # floats) need more than the fixed array holds.
+    g = torch.zeros((8192, 65535), device="cuda")
+    x = torch.zeros((8192, 65535), device="cuda")
+    bias = torch.zeros((65535,), device="cuda")
     need = ctypes.c_size_t(0)
     dg, kg = zr._desc(g)
     dx, kx = zr._desc(x)
