@@ -11,13 +11,18 @@ Operator page, sections "逐元素算子" (elementwise ops) and "广播"
 (broadcasting, sum back to shape); Tensor page, section "形状与步长"
 (shape and strides); GPU page, section "OpAdd" (add's local derivative).
 sub/div backward use the calculus rules (g, -g) and (g/b, -g*a/b^2), which
-the pages leave unstated.
+the pages leave unstated.  Two-op chains (a op1 b) op2 c are the composition
+of two of these operators (Operator page, section 融合; Autograd page,
+section 链式法则).
 
 Pins (tests/test_oracle_pins.py, all CPU): the pages' printed broadcast,
 stride and transposed-view examples, the worked gradient z = x*y + x at
 x=3, y=2, NumPy broadcasting and float32 arithmetic, float64 central
 finite differences, closed forms of sum-to-shape, and scatter-vs-gather
-agreement.  Every function here is pinned by at least one of them.
+agreement; the chains by the same worked gradient (z = x*y + x is the chain
+(x mul y) add x), NumPy float32 two-step forwards, closed forms of the affine
+and scaled-mask chains, and float64 finite differences of all 16 op pairs.
+Every function here is pinned by at least one of them.
 """
 from __future__ import annotations
 
@@ -227,3 +232,41 @@ def sum_to_shape_at(x, shape, idx):
                                    vals.ctypes.data if vals.size else None,
                                    sabs.ctypes.data if sabs.size else None), "sum_to_shape_at")
     return vals, sabs
+
+
+# ---------------------------------------------------------------- two-op chains
+#
+# out = (a op1 b) op2 c: two of the operators above applied in sequence, each
+# rounded to binary32 — the fused forms the Operator page's section 融合
+# (fusion) motivates (fewer launches, no intermediate round trip through
+# memory), which keep the operators' mathematical definition.  The oracle
+# is that definition: the two forward ops one after the other, and the
+# backward by the chain rule (Autograd page, section 链式法则): op2's local
+# rules give grad_t and grad_c, op1's rules applied to grad_t give grad_a and
+# grad_b.  t and grad_t are rounded to binary32 in between, as the unfused
+# ops would store them.
+
+def chain_fwd(op1, op2, a, b, c):
+    """out = (a op1 b) op2 c, dense float32 of the broadcast of all three."""
+    t = binary_fwd(op1, a, b)
+    return binary_fwd(op2, t, c)
+
+
+def chain_bwd(op1, op2, g, a, b, c):
+    """(grad_a, grad_b, grad_c, abs_a, abs_b, abs_c) of out = (a op1 b) op2 c
+    given grad_out g; abs_* are sum|term| per gradient element (float64),
+    with the terms of grad_a and grad_b taken from the binary32 grad_t."""
+    t = binary_fwd(op1, a, b)
+    gt, gc, _, sc = binary_bwd(op2, g, t, c)
+    ga, gb, sa, sb = binary_bwd(op1, gt, a, b)
+    return ga, gb, gc, sa, sb, sc
+
+
+def chain_bwd_at(op1, op2, which, g, a, b, c, idx):
+    """Values (and sum|term|) of grad_a (which=0), grad_b (1) or grad_c (2)
+    at linear indices ``idx`` of that input's dense row-major shape."""
+    t = binary_fwd(op1, a, b)
+    if which == 2:
+        return binary_bwd_at(op2, 1, g, t, c, idx)
+    gt, _, _, _ = binary_bwd(op2, g, t, c, want_b=False)
+    return binary_bwd_at(op1, which, gt, a, b, idx)

@@ -363,3 +363,128 @@ def test_empty_shapes():
     ga, gb, _, _ = oracle.binary_bwd("mul", np.zeros((0, 3), np.float32), a, b)
     assert ga.shape == (0, 3)
     np.testing.assert_array_equal(gb, np.zeros((1, 3), np.float32))
+
+
+# ---------------------------------------------------------------- two-op chains
+
+def test_chain_worked_gradient_example():
+    """z = x*y + x is the chain (x mul y) add x: the book's worked example."""
+    kv = {}
+    for ln in _golden_lines("worked_gradient.txt"):
+        k, v = (p.strip() for p in ln.split("="))
+        kv[k] = float(v)
+    x = np.array([kv["x"]], np.float32)
+    y = np.array([kv["y"]], np.float32)
+    z = oracle.chain_fwd("mul", "add", x, y, x)
+    assert z[0] == kv["z"]
+    ga, gb, gc, _, _, _ = oracle.chain_bwd("mul", "add", np.ones(1, np.float32), x, y, x)
+    # x enters twice (as a and as c); the caller adds its two gradients.
+    assert ga[0] + gc[0] == kv["dz_dx"]
+    assert gb[0] == kv["dz_dy"]
+
+
+CHAIN_SHAPES = [((3, 4), (4,), (3, 1)), ((2, 1, 3), (4, 1), (3,)), ((2, 3), (2, 3), (1,)),
+                ((4,), (1,), (2, 4)), ((2, 3, 4), (3, 1), (2, 1, 4))]
+
+
+def _chain_inputs(rng, sa, sb, sc, op1, op2):
+    a = rng.standard_normal(sa).astype(np.float32)
+    b = rng.standard_normal(sb).astype(np.float32)
+    c = rng.standard_normal(sc).astype(np.float32)
+    if op1 == "div":
+        b = (np.sign(b) * (0.5 + np.abs(b))).astype(np.float32)
+    if op2 == "div":
+        c = (np.sign(c) * (0.5 + np.abs(c))).astype(np.float32)
+    return a, b, c
+
+
+@pytest.mark.parametrize("op1", OPS)
+def test_chain_forward_matches_numpy_float32_bit_exact(op1):
+    rng = np.random.default_rng(500 + OPS.index(op1))
+    for op2 in OPS:
+        for sa, sb, sc in CHAIN_SHAPES:
+            a, b, c = _chain_inputs(rng, sa, sb, sc, op1, op2)
+            with np.errstate(all="ignore"):
+                ref = NP_OP[op2](NP_OP[op1](a, b), c).astype(np.float32)
+            got = oracle.chain_fwd(op1, op2, a, b, c)
+            assert got.shape == ref.shape
+            assert np.array_equal(got.view(np.uint32), ref.view(np.uint32)), (op1, op2, sa, sb, sc)
+
+
+def _chain_loss64(op1, op2, a64, b64, c64, w64):
+    with np.errstate(all="ignore"):
+        return float(np.sum(w64 * NP_OP[op2](NP_OP[op1](a64, b64), c64)))
+
+
+@pytest.mark.parametrize("op1", OPS)
+def test_chain_backward_matches_finite_differences(op1):
+    rng = np.random.default_rng(600 + OPS.index(op1))
+    for op2 in OPS:
+        for sa, sb, sc in CHAIN_SHAPES:
+            a, b, c = _chain_inputs(rng, sa, sb, sc, op1, op2)
+            out_shape = np.broadcast_shapes(sa, sb, sc)
+            w = rng.standard_normal(out_shape).astype(np.float32)
+            grads = oracle.chain_bwd(op1, op2, w, a, b, c)[:3]
+            xs = [a.astype(np.float64), b.astype(np.float64), c.astype(np.float64)]
+            w64 = w.astype(np.float64)
+            for k in range(3):
+                x64, grad = xs[k], grads[k]
+                fd = np.empty(x64.shape)
+                for i in np.ndindex(x64.shape):
+                    h = 1e-6 * max(1.0, abs(x64[i]))
+                    keep = x64[i]
+                    x64[i] = keep + h
+                    lp = _chain_loss64(op1, op2, *xs, w64)
+                    x64[i] = keep - h
+                    lm = _chain_loss64(op1, op2, *xs, w64)
+                    x64[i] = keep
+                    fd[i] = (lp - lm) / (2 * h)
+                np.testing.assert_allclose(grad, fd, rtol=2e-5, atol=2e-5,
+                                           err_msg=f"{op1} {op2} {sa} {sb} {sc} input {k}")
+
+
+def test_chain_affine_closed_form():
+    """(x * gamma) + beta: grad_x = g*gamma (one binary32 multiply),
+    grad_gamma = column sums of g*x, grad_beta = column sums of g."""
+    host = workloads.make_inputs("c3", **workloads.small_dims("c3"))
+    x, gamma, beta, g = (host[k].numpy() for k in ("x", "gamma", "beta", "g"))
+    ga, gb, gc, sa, sb, sc = oracle.chain_bwd("mul", "add", g, x, gamma, beta)
+    ref_x = (g * gamma).astype(np.float32)
+    assert np.array_equal(ga.view(np.uint32), ref_x.view(np.uint32))
+    g64, x64 = g.astype(np.float64), x.astype(np.float64)
+    col_gx = np.sum(g64 * x64, axis=(0, 1))
+    col_g = np.sum(g64, axis=(0, 1))
+    assert np.all(np.abs(gb - col_gx) <= 1e-6 * np.sum(np.abs(g64 * x64), axis=(0, 1)))
+    assert np.all(np.abs(gc - col_g) <= 1e-6 * np.sum(np.abs(g64), axis=(0, 1)))
+    np.testing.assert_allclose(sb, np.sum(np.abs(g64 * x64), axis=(0, 1)), rtol=1e-6)
+
+
+def test_chain_scaled_mask_closed_form():
+    """(scores + mask) / k: grad_scores = g/k (one binary32 division),
+    grad_mask = sums of g/k over batch and heads, grad_k = -sum(g*t)/k^2
+    with t = fl32(scores + mask)."""
+    host = workloads.make_inputs("c4", **workloads.small_dims("c4"))
+    s, m, k, g = (host[n].numpy() for n in ("scores", "mask", "scalar", "g"))
+    ga, gb, gc, sa, sb, sc = oracle.chain_bwd("add", "div", g, s, m, k)
+    assert np.array_equal(ga.view(np.uint32), (g / k).astype(np.float32).view(np.uint32))
+    g64 = g.astype(np.float64)
+    k64 = float(k[0])
+    mask_ref = np.sum(g64 / k64, axis=(0, 1), keepdims=True)
+    assert np.all(np.abs(gb - mask_ref) <= 1e-6 * np.sum(np.abs(g64 / k64), axis=(0, 1), keepdims=True))
+    t64 = (s + m).astype(np.float32).astype(np.float64)
+    terms = -g64 * t64 / (k64 * k64)
+    assert abs(float(gc[0]) - math.fsum(terms.ravel())) <= 1e-6 * float(np.sum(np.abs(terms)))
+
+
+def test_chain_gather_form_matches_full():
+    rng = np.random.default_rng(700)
+    for op1, op2 in (("mul", "add"), ("add", "div"), ("div", "mul"), ("sub", "sub")):
+        for sa, sb, sc in CHAIN_SHAPES:
+            a, b, c = _chain_inputs(rng, sa, sb, sc, op1, op2)
+            g = rng.standard_normal(np.broadcast_shapes(sa, sb, sc)).astype(np.float32)
+            full = oracle.chain_bwd(op1, op2, g, a, b, c)
+            for which, shape in enumerate((sa, sb, sc)):
+                idx = np.arange(int(np.prod(shape)), dtype=np.int64)
+                vals, sabs = oracle.chain_bwd_at(op1, op2, which, g, a, b, c, idx)
+                assert np.array_equal(vals.view(np.uint32), full[which].ravel().view(np.uint32))
+                np.testing.assert_allclose(sabs, full[3 + which].ravel(), rtol=1e-12)
