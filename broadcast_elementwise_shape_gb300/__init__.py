@@ -60,9 +60,13 @@ def lib() -> ctypes.CDLL:
         L.zr_binary_fwd.argtypes = [c_int, ZrTensor, ZrTensor, vp, i64p, vp]
         L.zr_binary_bwd.argtypes = [c_int, ZrTensor, ZrTensor, ZrTensor, vp, vp, vp, szp, vp]
         L.zr_sum_to_shape.argtypes = [ZrTensor, i32, i64p, vp, vp, szp, vp]
+        L.zr_chain_fwd.argtypes = [c_int, c_int, ZrTensor, ZrTensor, ZrTensor, vp, i64p, vp]
+        L.zr_chain_bwd.argtypes = [c_int, c_int, ZrTensor, ZrTensor, ZrTensor, ZrTensor, vp, vp, vp,
+                                   vp, szp, vp]
         L.zr_status_string.argtypes = [c_int]
         L.zr_status_string.restype = ctypes.c_char_p
-        for f in ("zr_broadcast_shape", "zr_binary_fwd", "zr_binary_bwd", "zr_sum_to_shape"):
+        for f in ("zr_broadcast_shape", "zr_binary_fwd", "zr_binary_bwd", "zr_sum_to_shape",
+                  "zr_chain_fwd", "zr_chain_bwd"):
             getattr(L, f).restype = c_int
         _lib = L
     return _lib
@@ -185,3 +189,49 @@ def zr_sum_to_shape(x, shape, out=None, workspace=None):
                                _stream(x))
     _check(rc, "zr_sum_to_shape")
     return out
+
+
+def zr_chain_fwd(op1, op2, a, b, c, out=None):
+    """out = (a op1 b) op2 c (broadcasting); ``out`` may be a preallocated
+    (strided) tensor of the broadcast shape."""
+    import torch
+    shape = zr_broadcast_shape(zr_broadcast_shape(a.shape, b.shape), c.shape)
+    if out is None:
+        out = torch.empty(shape, dtype=torch.float32, device=a.device)
+    elif tuple(out.shape) != shape:
+        raise ValueError(f"out has shape {tuple(out.shape)}, expected {shape}")
+    da, ka = _desc(a)
+    db, kb = _desc(b)
+    dc, kc = _desc(c)
+    ost = _i64(out.stride())
+    rc = lib().zr_chain_fwd(_op(op1), _op(op2), da, db, dc, out.data_ptr() if out.numel() else None,
+                            ost, _stream(out))
+    _check(rc, "zr_chain_fwd")
+    return out
+
+
+def zr_chain_bwd(op1, op2, grad_out, a, b, c, want=(True, True, True), grads=(None, None, None),
+                 shapes=(None, None, None), workspace=None):
+    """(grad_a, grad_b, grad_c) of out = (a op1 b) op2 c given grad_out.  An
+    operand may be None (with its shape in ``shapes``) when the requested
+    gradients do not read it."""
+    import torch
+    xs = (a, b, c)
+    shp = [tuple(x.shape) if x is not None else tuple(s) for x, s in zip(xs, shapes)]
+    dev = grad_out.device
+    gs = [g if g is not None else (torch.empty(s, dtype=torch.float32, device=dev) if w else None)
+          for g, s, w in zip(grads, shp, want)]
+    dg, kg = _desc(grad_out)
+    descs = [_desc(x, s) for x, s in zip(xs, shp)]
+    ptrs = [g.data_ptr() if (g is not None and g.numel()) else None for g in gs]
+    L = lib()
+    nbytes = ctypes.c_size_t(0)
+    _check(L.zr_chain_bwd(_op(op1), _op(op2), dg, descs[0][0], descs[1][0], descs[2][0], *ptrs,
+                          None, ctypes.byref(nbytes), None), "zr_chain_bwd (workspace query)")
+    if workspace is None or workspace.numel() < nbytes.value:
+        workspace = _workspace(nbytes.value, dev)
+    nbytes = ctypes.c_size_t(workspace.numel())
+    rc = L.zr_chain_bwd(_op(op1), _op(op2), dg, descs[0][0], descs[1][0], descs[2][0], *ptrs,
+                        workspace.data_ptr(), ctypes.byref(nbytes), _stream(grad_out))
+    _check(rc, "zr_chain_bwd")
+    return tuple(gs)

@@ -691,6 +691,7 @@ int zr_test_occupancy(int which, int* planned, int* actual) {
   else if (which >= 4 && which < 9) e = occupancy_red(which - 4, planned, actual);
   else if (which >= 9 && which < 11) e = occupancy_other(which - 9, planned, actual);
   else if (which >= 11 && which < 16) e = occupancy_red(which - 6, planned, actual);
+  else if (which >= 16 && which < 19) e = occupancy_chain(which - 16, planned, actual);
   else return ZR_ERR_SIZE;
   return cuda_status(e);
 }
@@ -1007,6 +1008,400 @@ int zr_test_emulate_bwd(zr_op op, zr_tensor grad_out, zr_tensor a, zr_tensor b,
   }
   *nrec = m;
   return over ? ZR_ERR_SIZE : ZR_OK;
+}
+
+}  // extern "C"
+
+// ------------------------------------------------------------------ two-op chains
+//
+// out = (a op1 b) op2 c (Operator page, section 融合: one launch and no
+// round trip of the intermediate through memory; the mathematics is that of
+// the two operators in sequence).  The forward is one elementwise pass.  The
+// backward runs as one fused pass when a has the output's shape, b is
+// reduced and c either has b's dense layout or one element; any other layout
+// runs the composition: t = a op1 b and grad_t in the workspace, then op2's
+// and op1's backward passes.
+
+namespace zr {
+namespace {
+
+struct ChainFwdSet {
+  bool empty = false;
+  EwBuild eb;
+  TDesc a, b, c, out;
+};
+
+int plan_chain_fwd(int op1, int op2, const zr_tensor& ta, const zr_tensor& tb,
+                   const zr_tensor& tc, const float* out, const int64_t* out_strides,
+                   ChainFwdSet* S) {
+  if (!op_ok(op1) || !op_ok(op2)) return ZR_ERR_NULL;
+  int rc = read_tensor(ta, &S->a);
+  if (rc) return rc;
+  rc = read_tensor(tb, &S->b);
+  if (rc) return rc;
+  rc = read_tensor(tc, &S->c);
+  if (rc) return rc;
+  int nt = 0, n = 0;
+  int64_t szt[kMaxDims], osz[kMaxDims];
+  rc = broadcast_sizes(S->a.nd, S->a.size, S->b.nd, S->b.size, &nt, szt);
+  if (rc) return rc;
+  rc = broadcast_sizes(nt, szt, S->c.nd, S->c.size, &n, osz);
+  if (rc) return rc;
+  zr_tensor to{out, n, osz, out_strides};
+  rc = read_tensor(to, &S->out);
+  if (rc) return rc;
+  if (S->out.numel == 0) {
+    S->empty = true;
+    return ZR_OK;
+  }
+  if (!S->a.ptr || !S->b.ptr || !S->c.ptr || !out) return ZR_ERR_NULL;
+  if (!non_overlapping(S->out)) return ZR_ERR_LAYOUT;
+  const Span so = span_of(out, S->out.extent);
+  for (const TDesc* x : {&S->a, &S->b, &S->c})
+    if (overlaps(so, span_of(x->ptr, x->extent)) && !same_layout(*x, S->out)) return ZR_ERR_LAYOUT;
+  int64_t st[kProbSlots][kMaxDims] = {};
+  align_strides(S->a, n, osz, st[0]);
+  align_strides(S->b, n, osz, st[1]);
+  align_strides(S->c, n, osz, st[2]);
+  for (int d = 0; d < n; ++d) st[kSlotOut][d] = osz[d] == 1 ? 0 : S->out.stride[d];
+  Prob P;
+  rc = coalesce(n, osz, st, 0x7u | (1u << kSlotOut), kSlotOut, &P);
+  if (rc) return rc;
+  const float* in[3] = {S->a.ptr, S->b.ptr, S->c.ptr};
+  float* outs[2] = {const_cast<float*>(out), nullptr};
+  const uint32_t stream_mask = (S->a.numel == S->out.numel ? 1u : 0u) |
+                               (S->b.numel == S->out.numel ? 2u : 0u) |
+                               (S->c.numel == S->out.numel ? 4u : 0u);
+  return build_ew(P, in, outs, 0x7u, stream_mask, kOccEwBwd, &S->eb);
+}
+
+struct ChainBwdSet {
+  bool nothing = false;
+  bool empty = false;
+  float* zero_ptr[3] = {nullptr, nullptr, nullptr};
+  size_t zero_bytes[3] = {0, 0, 0};
+  bool fused = false;
+  ChainBuild cb;
+  size_t off_c = 0;             // fused: grad_c partial region
+  // Composed route: t (when op2's grad_c needs it) and grad_t in the
+  // workspace, then op2's and op1's backward passes sharing one partial
+  // region (they run in stream order).
+  bool need_t = false, need_gt = false;
+  FwdSet tf;
+  BwdSet b2, b1;
+  size_t off_gt = 0, off_p = 0;
+  size_t ws_run = 0, ws_query = 0;
+  TDesc g, a, b, c;
+};
+
+size_t align256(size_t v) { return (v + 255) / 256 * 256; }
+
+bool dense_layout(const TDesc& t) {
+  int64_t want = 1;
+  for (int d = t.nd - 1; d >= 0; --d) {
+    if (t.size[d] != 1 && t.stride[d] != want) return false;
+    want *= t.size[d];
+  }
+  return true;
+}
+
+// Sizes of x right-aligned to rank n (missing dims are 1).
+void aligned_sizes(const TDesc& x, int n, int64_t* out) {
+  for (int d = 0; d < n; ++d) {
+    const int k = d - (n - x.nd);
+    out[d] = k < 0 ? 1 : x.size[k];
+  }
+}
+
+// Plans of the composed route with the workspace at `base` (a real
+// workspace, or at query time an address range above every operand so that
+// the layout checks see no overlap).
+int plan_chain_composed(int op1, int op2, const zr_tensor& tg, const zr_tensor& ta,
+                        const zr_tensor& tb, const zr_tensor& tc, float* grad_a, float* grad_b,
+                        float* grad_c, int nt, const int64_t* szt, int64_t numel_t, char* base,
+                        ChainBwdSet* S, size_t* ws_run, size_t* ws_query) {
+  const size_t t_bytes = S->need_t ? align256(size_t(numel_t) * 4) : 0;
+  const size_t gt_bytes = S->need_gt ? align256(size_t(numel_t) * 4) : 0;
+  S->off_gt = t_bytes;
+  S->off_p = t_bytes + gt_bytes;
+  float* tptr = reinterpret_cast<float*>(base);
+  float* gtptr = reinterpret_cast<float*>(base + S->off_gt);
+  int rc;
+  if (S->need_t) {
+    rc = plan_fwd(op1, ta, tb, tptr, nullptr, &S->tf);
+    if (rc) return rc;
+  }
+  const zr_tensor tt{S->need_t ? tptr : nullptr, nt, szt, nullptr};
+  rc = plan_bwd(op2, tg, tt, tc, S->need_gt ? gtptr : nullptr, grad_c, &S->b2);
+  if (rc) return rc;
+  size_t run = S->b2.ws_run, query = S->b2.ws_query;
+  if (S->need_gt) {
+    const zr_tensor tgt{gtptr, nt, szt, nullptr};
+    rc = plan_bwd(op1, tgt, ta, tb, grad_a, grad_b, &S->b1);
+    if (rc) return rc;
+    run = std::max(run, S->b1.ws_run);
+    query = std::max(query, S->b1.ws_query);
+  }
+  *ws_run = S->off_p + run;
+  *ws_query = S->off_p + query;
+  return ZR_OK;
+}
+
+int plan_chain_bwd(int op1, int op2, const zr_tensor& tg, const zr_tensor& ta, const zr_tensor& tb,
+                   const zr_tensor& tc, float* grad_a, float* grad_b, float* grad_c,
+                   void* workspace, ChainBwdSet* S) {
+  if (!op_ok(op1) || !op_ok(op2)) return ZR_ERR_NULL;
+  int rc = read_tensor(tg, &S->g);
+  if (rc) return rc;
+  rc = read_tensor(ta, &S->a);
+  if (rc) return rc;
+  rc = read_tensor(tb, &S->b);
+  if (rc) return rc;
+  rc = read_tensor(tc, &S->c);
+  if (rc) return rc;
+  int nt = 0, n = 0;
+  int64_t szt[kMaxDims], osz[kMaxDims];
+  rc = broadcast_sizes(S->a.nd, S->a.size, S->b.nd, S->b.size, &nt, szt);
+  if (rc) return rc;
+  rc = broadcast_sizes(nt, szt, S->c.nd, S->c.size, &n, osz);
+  if (rc) return rc;
+  if (S->g.nd != n) return ZR_ERR_SHAPE;
+  for (int d = 0; d < n; ++d)
+    if (S->g.size[d] != osz[d]) return ZR_ERR_SHAPE;
+  if (!grad_a && !grad_b && !grad_c) {
+    S->nothing = true;
+    return ZR_OK;
+  }
+  int64_t numel_t = 1;
+  for (int d = 0; d < nt; ++d) numel_t *= szt[d];
+  // Layout: the gradients are dense in their inputs' shapes, disjoint from
+  // one another and from every input.
+  const TDesc ga = dense_desc(grad_a, S->a.nd, S->a.size);
+  const TDesc gb = dense_desc(grad_b, S->b.nd, S->b.size);
+  const TDesc gc = dense_desc(grad_c, S->c.nd, S->c.size);
+  const Span sg[3] = {span_of(grad_a, ga.extent), span_of(grad_b, gb.extent),
+                      span_of(grad_c, gc.extent)};
+  for (int i = 0; i < 3; ++i) {
+    for (int k = i + 1; k < 3; ++k)
+      if (overlaps(sg[i], sg[k])) return ZR_ERR_LAYOUT;
+    for (const TDesc* x : {&S->g, &S->a, &S->b, &S->c})
+      if (overlaps(sg[i], span_of(x->ptr, x->extent))) return ZR_ERR_LAYOUT;
+  }
+  if (S->g.numel == 0) {
+    S->empty = true;
+    float* gp[3] = {grad_a, grad_b, grad_c};
+    const TDesc* gd[3] = {&ga, &gb, &gc};
+    for (int i = 0; i < 3; ++i)
+      if (gp[i] && gd[i]->numel > 0) { S->zero_ptr[i] = gp[i]; S->zero_bytes[i] = gd[i]->numel * 4; }
+    return ZR_OK;
+  }
+  // Operands the requested gradients read.
+  S->need_t = grad_c && (op2 == OP_MUL || op2 == OP_DIV);
+  S->need_gt = grad_a || grad_b;
+  const bool read_a = S->need_t || (grad_b && needs_a(op1, 1));
+  const bool read_b = S->need_t || (grad_a && needs_b(op1, 0)) || (grad_b && needs_b(op1, 1));
+  const bool read_c = (S->need_gt && needs_b(op2, 0)) || (grad_c && needs_b(op2, 1));
+  if (!S->g.ptr || (read_a && !S->a.ptr) || (read_b && !S->b.ptr) || (read_c && !S->c.ptr))
+    return ZR_ERR_NULL;
+
+  // Fused route: a has the output's shape, b is reduced, and c has b's dense
+  // layout or one element; every gradient requested and every operand given.
+  size_t fused_q = 0;
+  bool shape_ok = grad_a && grad_b && grad_c && S->a.ptr && S->b.ptr && S->c.ptr &&
+                  S->a.numel == S->g.numel && S->b.numel < S->g.numel;
+  bool c_scalar = S->c.numel == 1;
+  if (shape_ok && !c_scalar) {
+    int64_t sb[kMaxDims], sc[kMaxDims];
+    aligned_sizes(S->b, n, sb);
+    aligned_sizes(S->c, n, sc);
+    for (int d = 0; d < n; ++d) shape_ok = shape_ok && sb[d] == sc[d];
+    shape_ok = shape_ok && dense_layout(S->b) && dense_layout(S->c);
+  }
+  if (shape_ok) {
+    int64_t st[kProbSlots][kMaxDims] = {};
+    align_strides(S->g, n, osz, st[0]);
+    align_strides(S->a, n, osz, st[1]);
+    align_strides(S->b, n, osz, st[2]);
+    int64_t dense[kMaxDims];
+    contiguous_strides(n, osz, dense);
+    for (int d = 0; d < n; ++d) st[kSlotOut][d] = osz[d] == 1 ? 0 : dense[d];
+    grad_index_strides(S->b, n, osz, st[kSlotXB]);
+    Prob P;
+    rc = coalesce(n, osz, st, 0x7u | (1u << kSlotOut) | (1u << kSlotXB), -1, &P);
+    if (rc) return rc;
+    const uint32_t stream_mask = 1u | 2u | (S->b.numel == S->g.numel ? 4u : 0u);
+    ChainBuild q;
+    if (build_chain(P, S->g.ptr, S->a.ptr, S->b.ptr, S->c.ptr, c_scalar, grad_a, grad_b, grad_c,
+                    stream_mask, 4, &q) == ZR_OK)
+      fused_q = align256(q.ws_b_bytes) + q.ws_c_bytes;
+    const int r = build_chain(P, S->g.ptr, S->a.ptr, S->b.ptr, S->c.ptr, c_scalar, grad_a,
+                              grad_b, grad_c, stream_mask, 0, &S->cb);
+    if (r == ZR_OK) {
+      S->fused = true;
+      S->off_c = align256(S->cb.ws_b_bytes);
+      S->ws_run = S->off_c + S->cb.ws_c_bytes;
+    } else if (r != 1) {
+      return r;
+    }
+  }
+
+  // Composed route: sized for the query always, planned on the real
+  // workspace when it runs.
+  uintptr_t top = 0;
+  for (const TDesc* x : {&S->g, &S->a, &S->b, &S->c}) {
+    const Span sp = span_of(x->ptr, x->extent);
+    top = std::max(top, sp.hi);
+  }
+  for (const Span& sp : sg) top = std::max(top, sp.hi);
+  char* fake = reinterpret_cast<char*>(align256(top) + 256);
+  ChainBwdSet tmp;
+  tmp.need_t = S->need_t;
+  tmp.need_gt = S->need_gt;
+  size_t run_c = 0, query_c = 0;
+  rc = plan_chain_composed(op1, op2, tg, ta, tb, tc, grad_a, grad_b, grad_c, nt, szt, numel_t,
+                           fake, &tmp, &run_c, &query_c);
+  if (rc) return rc;
+  // The query covers the route these arguments select (for the fused route
+  // whatever pointer alignment; a later call whose pointers select the
+  // composed route instead may need more and is refused before launching).
+  S->ws_query = S->fused ? fused_q : query_c;
+  if (!S->fused) {
+    if (workspace) {
+      rc = plan_chain_composed(op1, op2, tg, ta, tb, tc, grad_a, grad_b, grad_c, nt, szt, numel_t,
+                               static_cast<char*>(workspace), S, &S->ws_run, &query_c);
+      if (rc) return rc;
+    } else {
+      S->ws_run = run_c;
+    }
+  }
+  return ZR_OK;
+}
+
+int launch_fwd_set(const FwdSet& S, int op, cudaStream_t st, bool dry) {
+  if (S.empty) return ZR_OK;
+  if (S.tr) return cuda_status(launch_fwd_tr(op, S.tp, st, dry));
+  if (S.sabf) return cuda_status(launch_fwd_sabf(op, S.sp_rpt, S.sp, st, dry));
+  return cuda_status(launch_fwd(op, S.eb, st, dry));
+}
+
+int launch_chain_set(const ChainBwdSet& S, int op1, int op2, void* workspace, cudaStream_t st,
+                     bool dry) {
+  if (S.fused) {
+    ChainBuild cb = S.cb;
+    char* ws = static_cast<char*>(workspace);
+    cb.plan.r.partial = reinterpret_cast<float*>(ws);
+    cb.comb_b.partial = cb.plan.r.partial;
+    cb.plan.c_partial = reinterpret_cast<float*>(ws + S.off_c);
+    cb.comb_c.partial = cb.plan.c_partial;
+    return cuda_status(launch_chain_bwd(op1, op2, cb, st, dry));
+  }
+  char* p = static_cast<char*>(workspace) + S.off_p;
+  int rc;
+  if (S.need_t) {
+    rc = launch_fwd_set(S.tf, op1, st, dry);
+    if (rc) return rc;
+  }
+  if (!S.b2.nothing) {
+    rc = launch_bwd_set(S.b2, op2, p, st, dry);
+    if (rc) return rc;
+  }
+  if (S.need_gt && !S.b1.nothing) return launch_bwd_set(S.b1, op1, p, st, dry);
+  return ZR_OK;
+}
+
+std::string describe_chain_set(const ChainBwdSet& S) {
+  std::string s;
+  if (S.nothing || S.empty) return "{\"route\":\"none\"}";
+  if (S.fused) {
+    s = "{\"route\":\"fused\",\"plans\":[" + describe_chain(S.cb) + "]";
+  } else {
+    s = "{\"route\":\"composed\",\"need_t\":" + std::to_string(S.need_t ? 1 : 0) +
+        ",\"need_gt\":" + std::to_string(S.need_gt ? 1 : 0);
+  }
+  return s + ",\"ws_run\":" + std::to_string(S.ws_run) + ",\"ws_query\":" +
+         std::to_string(S.ws_query) + "}";
+}
+
+}  // namespace
+}  // namespace zr
+
+extern "C" {
+
+int zr_chain_fwd(zr_op op1, zr_op op2, zr_tensor a, zr_tensor b, zr_tensor c, float* out,
+                 const int64_t* out_strides, zr_stream_t stream) {
+  ChainFwdSet S;
+  int rc = plan_chain_fwd(op1, op2, a, b, c, out, out_strides, &S);
+  if (rc) return rc;
+  if (S.empty) return ZR_OK;
+  for (const void* p : {static_cast<const void*>(S.a.ptr), static_cast<const void*>(S.b.ptr),
+                        static_cast<const void*>(S.c.ptr), static_cast<const void*>(out)}) {
+    rc = check_device_ptr(p);
+    if (rc) return rc;
+  }
+  return cuda_status(launch_chain_fwd(op1, op2, S.eb, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int zr_chain_bwd(zr_op op1, zr_op op2, zr_tensor grad_out, zr_tensor a, zr_tensor b, zr_tensor c,
+                 float* grad_a, float* grad_b, float* grad_c, void* workspace,
+                 size_t* workspace_bytes, zr_stream_t stream) {
+  if (!workspace_bytes) return ZR_ERR_NULL;
+  ChainBwdSet S;
+  int rc = plan_chain_bwd(op1, op2, grad_out, a, b, c, grad_a, grad_b, grad_c, workspace, &S);
+  if (rc) return rc;
+  if (workspace == nullptr) {
+    *workspace_bytes = S.ws_query;
+    return ZR_OK;
+  }
+  if (S.nothing) return ZR_OK;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (S.empty) {
+    for (int w = 0; w < 3; ++w) {
+      if (!S.zero_ptr[w]) continue;
+      rc = check_device_ptr(S.zero_ptr[w]);
+      if (rc) return rc;
+    }
+    for (int w = 0; w < 3; ++w)
+      if (S.zero_ptr[w] && cudaMemsetAsync(S.zero_ptr[w], 0, S.zero_bytes[w], st) != cudaSuccess)
+        return ZR_ERR_CUDA;
+    return ZR_OK;
+  }
+  if (S.ws_run > 0) {
+    if (*workspace_bytes < S.ws_run) return ZR_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(workspace) % 16 != 0) return ZR_ERR_WORKSPACE;
+  }
+  for (const void* p : {static_cast<const void*>(S.g.ptr), static_cast<const void*>(S.a.ptr),
+                        static_cast<const void*>(S.b.ptr), static_cast<const void*>(S.c.ptr),
+                        static_cast<const void*>(grad_a), static_cast<const void*>(grad_b),
+                        static_cast<const void*>(grad_c),
+                        S.ws_run > 0 ? static_cast<const void*>(workspace) : nullptr}) {
+    if (!p) continue;
+    rc = check_device_ptr(p);
+    if (rc) return rc;
+  }
+  return launch_chain_set(S, op1, op2, workspace, st, false);
+}
+
+int zr_test_describe_chain_bwd(zr_op op1, zr_op op2, zr_tensor grad_out, zr_tensor a, zr_tensor b,
+                               zr_tensor c, const float* grad_a, const float* grad_b,
+                               const float* grad_c, char* buf, size_t len) {
+  ChainBwdSet S;
+  const int rc = plan_chain_bwd(op1, op2, grad_out, a, b, c, const_cast<float*>(grad_a),
+                                const_cast<float*>(grad_b), const_cast<float*>(grad_c), nullptr,
+                                &S);
+  if (rc) return rc;
+  return copy_json(describe_chain_set(S), buf, len);
+}
+
+int zr_test_dry_run_chain_bwd(zr_op op1, zr_op op2, zr_tensor grad_out, zr_tensor a, zr_tensor b,
+                              zr_tensor c, const float* grad_a, const float* grad_b,
+                              const float* grad_c) {
+  // A fake workspace far above any operand address the host tests use.
+  void* ws = reinterpret_cast<void*>(uintptr_t(1) << 46);
+  ChainBwdSet S;
+  const int rc = plan_chain_bwd(op1, op2, grad_out, a, b, c, const_cast<float*>(grad_a),
+                                const_cast<float*>(grad_b), const_cast<float*>(grad_c), ws, &S);
+  if (rc || S.nothing || S.empty) return rc;
+  return launch_chain_set(S, op1, op2, ws, nullptr, true);
 }
 
 }  // extern "C"

@@ -326,6 +326,22 @@ ZR_HD uint32_t sab_owner(const SabPlan& p, uint64_t step) {
   return static_cast<uint32_t>(((step + 1) * p.grid - 1) / p.total_steps);
 }
 
+// Fused backward of a two-op chain out = (a op1 b) op2 c in one pass over
+// grad_out, when a has the output's shape and b is reduced: grad_a is the
+// dense gradient (r.d_out), grad_b the reduced one (r's X, inner dim kept,
+// 16-byte vectors), and grad_c is summed in the same pass.  Either c has b's
+// shape and both are dense, so c's offsets are b's and grad_c shares grad_b's
+// tiling and slots (c_scalar = 0); or c has one element and grad_c is the
+// total sum, one partial per CTA (c_scalar = 1).
+struct ChainPlan {
+  RedPlan r;                // g, a, b, grad_b (x_final / partial), grad_a (d_out)
+  const float* c;
+  float* c_final;           // grad_c
+  float* c_partial;         // grad_c partials: [nslots][nout], or [n_cta] when c_scalar
+  uint32_t c_scalar;
+};
+constexpr int kOccChain = 3;  // k_chain_bwd: CTAs per SM
+
 // Second pass: out[j] = sum over s of partial[s * nout + j], s in order.
 struct CombinePlan {
   const float* partial;

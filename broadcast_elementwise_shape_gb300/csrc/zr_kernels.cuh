@@ -191,6 +191,20 @@ struct BwdDirectF {
   }
 };
 
+// Forward of a two-op chain: out = (a op1 b) op2 c, each op one IEEE
+// binary32 operation (the intermediate is rounded as the unfused ops would
+// store it).  Slots 0, 1, 2 = a, b, c.
+template <int OP1, int OP2>
+struct ChainF {
+  static constexpr bool kR1 = true, kR2 = true;
+  static constexpr int kMinBlocks = kOccEwBwd;
+  template <int VEC>
+  __device__ __forceinline__ void operator()(const Vec<VEC> (&x)[3], Vec<VEC> (&y)[2]) const {
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) y[0].v[i] = fwd_op<OP2>(fwd_op<OP1>(x[0].v[i], x[1].v[i]), x[2].v[i]);
+  }
+};
+
 // Copy (sum-to-shape onto the same shape).
 struct CopyF {
   static constexpr bool kR1 = false, kR2 = false;

@@ -83,6 +83,14 @@ cudaError_t occupancy_ew(int which, int* planned, int* actual);
 cudaError_t occupancy_red(int which, int* planned, int* actual);
 cudaError_t occupancy_other(int which, int* planned, int* actual);
 
+// Two-op chains out = (a op1 b) op2 c: the forward (slots 0..2 = a, b, c)
+// and the fused one-pass backward with its second passes.
+cudaError_t launch_chain_fwd(int op1, int op2, const EwBuild& eb, cudaStream_t s, bool dry = false);
+cudaError_t launch_chain_bwd(int op1, int op2, const ChainBuild& cb, cudaStream_t s, bool dry = false);
+// 0: chain forward (mul, add); 1: fused backward (mul, add), c shaped like b;
+// 2: fused backward (add, div), c one element.
+cudaError_t occupancy_chain(int which, int* planned, int* actual);
+
 // Fused backward with both gradients reduced: the k_sab pass, then one
 // combine pass per gradient.  sb.plan.ws_a / ws_b must be set.
 cudaError_t launch_sab(int op, const SabBuild& sb, cudaStream_t s, bool dry = false);

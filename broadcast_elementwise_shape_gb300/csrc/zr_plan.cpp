@@ -543,6 +543,57 @@ int build_red(const Prob& P, int xslot, const float* g, const float* a, const fl
   return ZR_OK;
 }
 
+int build_chain(const Prob& P, const float* g, const float* a, const float* b, const float* c,
+                bool c_scalar, float* grad_a, float* grad_b, float* grad_c, uint32_t stream_mask,
+                int vec_override, ChainBuild* cb) {
+  *cb = ChainBuild{};
+  // c is read with b's offsets (same shape, both dense), so it needs b's
+  // 16-byte alignment; a single-element c is read as a scalar.
+  if (!c_scalar && vec_override == 0 && reinterpret_cast<uintptr_t>(c) % 16 != 0) return 1;
+  RedBuild rb;
+  const int rc = build_red(P, kSlotXB, g, a, b, 7u, stream_mask & 7u, grad_b, grad_a,
+                           vec_override, kOccChain, 0, 0, &rb);
+  if (rc) return rc;
+  if (rb.vec != 4 || !rb.plan.inner_kept) return 1;
+  ChainPlan& cp = cb->plan;
+  cp.r = rb.plan;
+  cp.c = c;
+  cp.c_final = grad_c;
+  cp.c_scalar = c_scalar ? 1 : 0;
+  cb->comb_b = rb.comb;
+  cb->ws_b_bytes = rb.ws_bytes;
+  CombinePlan& cc = cb->comb_c;
+  if (c_scalar) {
+    cc = CombinePlan{};
+    cc.nout = 1;
+    cc.nslots = rb.plan.n_cta;
+    cc.out = grad_c;
+    cc.scale = 1.0f;
+    combine_layout(&cc);
+    cb->ws_c_bytes = rb.plan.n_cta > 1 ? ((uint64_t(rb.plan.n_cta) * 4 + 255) / 256) * 256 : 0;
+  } else {
+    cc = rb.comb;
+    cc.out = grad_c;
+    cb->ws_c_bytes = rb.ws_bytes;
+  }
+  return ZR_OK;
+}
+
+std::string describe_chain(const ChainBuild& cb) {
+  RedBuild rb;
+  rb.plan = cb.plan.r;
+  rb.comb = cb.comb_b;
+  rb.vec = 4;
+  rb.ws_bytes = cb.ws_b_bytes;
+  std::string r = describe_red(rb);
+  char buf[160];
+  std::snprintf(buf, sizeof(buf), ",\"c_scalar\":%u,\"c_slots\":%u,\"ws_c_bytes\":%zu}",
+                cb.plan.c_scalar, cb.comb_c.nslots, cb.ws_c_bytes);
+  r.pop_back();
+  r.replace(r.find("\"kernel\":\"reduce\""), 17, "\"kernel\":\"chain\"");
+  return r + buf;
+}
+
 int build_tr(const Prob& P, const float* a, const float* b, float* out, TrPlan* tp) {
   const int n = P.n;
   const int q = n - 1;

@@ -85,6 +85,20 @@ int build_red(const Prob& P, int xslot, const float* g, const float* a, const fl
               uint32_t read_mask, uint32_t stream_mask, float* x_out, float* d_out,
               int vec_override, int occ, int occ_cl_kept, int occ_cl_red, RedBuild* rb);
 
+struct ChainBuild {
+  ChainPlan plan;
+  CombinePlan comb_b, comb_c;
+  size_t ws_b_bytes, ws_c_bytes;  // grad_b / grad_c partial regions (0: none)
+};
+// Fused chain backward plan over P (slots G, A, B, D = grad_a, XB = grad_b's
+// index map).  Returns ZR_OK when the layout qualifies (16-byte vectors, b
+// reduced with its inner dim kept; c with b's dense layout, or one element),
+// 1 when it does not, or an error code.  vec_override as for build_red.
+int build_chain(const Prob& P, const float* g, const float* a, const float* b, const float* c,
+                bool c_scalar, float* grad_a, float* grad_b, float* grad_c, uint32_t stream_mask,
+                int vec_override, ChainBuild* cb);
+std::string describe_chain(const ChainBuild& cb);
+
 struct SabBuild {
   SabPlan plan;
   CombinePlan comb_a, comb_b;

@@ -199,6 +199,59 @@ int zr_sum_to_shape(zr_tensor in, int32_t ndim_out, const int64_t* sizes_out,
                     float* out, void* workspace, size_t* workspace_bytes,
                     zr_stream_t stream);
 
+/*
+ * zr_chain_fwd — out = (a op1 b) op2 c, all three operands broadcast to one
+ * output shape (broadcast(broadcast(a, b), c)).  The fused form of two of the
+ * operators above in sequence: Operator page, section 融合 (fusion) — one
+ * kernel launch, and the intermediate t = a op1 b never goes through memory,
+ * while the mathematics stays that of the two operators (e.g. OpLayerNorm's
+ * affine tail (x * gamma) + beta, or the GPT page's Attention section's masked
+ * scores, here (scores + mask) / k).  t is rounded to binary32 before op2, so
+ * every element is bit-identical to zr_binary_fwd(op2, zr_binary_fwd(op1, a,
+ * b), c).  Layout, in-place and error rules are those of zr_binary_fwd (c is a
+ * third input).
+ */
+int zr_chain_fwd(zr_op op1, zr_op op2, zr_tensor a, zr_tensor b, zr_tensor c, float* out,
+                 const int64_t* out_strides, zr_stream_t stream);
+
+/*
+ * zr_chain_bwd — gradients of out = (a op1 b) op2 c given grad_out, by the
+ * chain rule (Autograd page, section 链式法则): op2's local rules give
+ * grad_t and grad_c; op1's rules applied to grad_t give grad_a and grad_b;
+ * each gradient is summed back to its input's shape (Operator page, 广播).
+ *
+ *   grad_out  dense or strided, of the output shape (else ZR_ERR_SHAPE).
+ *   a, b, c   the forward inputs.  Values are read only where the requested
+ *             gradients need them: t = a op1 b (so a and b) when grad_c is
+ *             requested and op2 is mul or div; b for grad_a and a for grad_b
+ *             when op1 is mul or div (div's grad_b also b); c when op2 is mul
+ *             or div.  Others may have data == NULL (sizes still required).
+ *   grad_a, grad_b, grad_c
+ *             dense row-major in a's, b's, c's shapes, or NULL to skip.  They
+ *             must not overlap one another or any input (ZR_ERR_LAYOUT).
+ *   workspace, workspace_bytes
+ *             the zr_binary_bwd protocol: workspace == NULL queries the size
+ *             (launches nothing); otherwise at least that many bytes, 16-byte
+ *             aligned, owned by the caller, used in stream order.  The query
+ *             sizes the route (below) that its own arguments select; a call
+ *             whose pointers select the other route and need more workspace
+ *             returns ZR_ERR_WORKSPACE without launching anything.
+ *
+ * When a has the output's shape, b is reduced with its innermost dim kept,
+ * and c either has b's shape (both dense row-major) or one element, and all
+ * three gradients are requested, one pass over grad_out writes grad_a and
+ * sums grad_b and grad_c (plus a second pass over partial sums when the
+ * reduction is split).  Any other layout runs the composition: t (when
+ * needed) and grad_t are formed in the workspace, then op2's and op1's
+ * backward passes, so the query covers numel(t) floats for each.
+ * Numerics: grad_t and a dense grad_a are the binary32 values the two
+ * unfused calls would produce (bit-identical); summed gradients are within
+ * 1e-5 * sum|terms| per element, terms taken from the binary32 grad_t.
+ */
+int zr_chain_bwd(zr_op op1, zr_op op2, zr_tensor grad_out, zr_tensor a, zr_tensor b, zr_tensor c,
+                 float* grad_a, float* grad_b, float* grad_c, void* workspace,
+                 size_t* workspace_bytes, zr_stream_t stream);
+
 /* Static, human-readable name of a status code. */
 const char* zr_status_string(int status);
 

@@ -26,6 +26,17 @@ int zr_test_describe_bwd(zr_op op, zr_tensor grad_out, zr_tensor a, zr_tensor b,
 int zr_test_describe_sum(zr_tensor in, int32_t ndim_out, const int64_t* sizes_out,
                          const float* out, char* buf, size_t len);
 
+/* JSON description of the route zr_chain_bwd would take ("fused" with its
+ * plan, or "composed"), with its workspace sizes. */
+int zr_test_describe_chain_bwd(zr_op op1, zr_op op2, zr_tensor grad_out, zr_tensor a,
+                               zr_tensor b, zr_tensor c, const float* grad_a,
+                               const float* grad_b, const float* grad_c, char* buf, size_t len);
+/* Plan a chain backward and run its launch-time operand checks without
+ * launching (as the zr_test_dry_run_* functions below). */
+int zr_test_dry_run_chain_bwd(zr_op op1, zr_op op2, zr_tensor grad_out, zr_tensor a, zr_tensor b,
+                              zr_tensor c, const float* grad_a, const float* grad_b,
+                              const float* grad_c);
+
 /* Plan a call and run the launch-time operand checks without launching:
  * ZR_OK, an argument error, or ZR_ERR_CUDA if a kernel would read an operand
  * the plan does not provide. */
@@ -36,11 +47,12 @@ int zr_test_dry_run_bwd(zr_op op, zr_tensor grad_out, zr_tensor a, zr_tensor b,
 int zr_test_dry_run_sum(zr_tensor in, int32_t ndim_out, const int64_t* sizes_out,
                         const float* out);
 
-/* Resident CTAs per SM of kernel `which` (0..15: elementwise forward add,
+/* Resident CTAs per SM of kernel `which` (0..18: elementwise forward add,
  * forward div, backward div, copy; reduction add inner-kept, sub
  * inner-reduced, mul inner-kept, div inner-reduced, sum-to-shape; split
  * forward; transpose; then the five reductions again in their cluster
- * variant) as the planner sizes grids for (*planned) and as the
+ * variant; chain forward, fused chain backward with c shaped like b, and
+ * with c one element) as the planner sizes grids for (*planned) and as the
  * CUDA runtime reports for the current device (*actual).  Needs a device:
  * ZR_ERR_CUDA without one; ZR_ERR_SIZE for an unknown `which`. */
 int zr_test_occupancy(int which, int* planned, int* actual);

@@ -455,3 +455,95 @@ def test_emulated_sab_backward(L, op):
         a2 = FakeT(2 * T if need_ab else None, sa)
         b2 = FakeT(3 * T if need_ab else None, sb)
         assert L2.zr_test_dry_run_bwd(op, g.desc, a2.desc, b2.desc, 4 * T, 5 * T) == 0
+
+
+# ---------------------------------------------------------------- two-op chains
+
+def _chain_desc(L, op1, op2, sa, sb, sc, sta=None, off=(0, 0, 0), want=(1, 1, 1)):
+    L.zr_test_describe_chain_bwd.argtypes = [ctypes.c_int, ctypes.c_int, ZrTensor, ZrTensor,
+                                             ZrTensor, ZrTensor, ctypes.c_void_p, ctypes.c_void_p,
+                                             ctypes.c_void_p, ctypes.c_char_p, ctypes.c_size_t]
+    L.zr_test_dry_run_chain_bwd.argtypes = [ctypes.c_int, ctypes.c_int, ZrTensor, ZrTensor,
+                                            ZrTensor, ZrTensor, ctypes.c_void_p, ctypes.c_void_p,
+                                            ctypes.c_void_p]
+    T = 1 << 40
+    out = np.broadcast_shapes(sa, sb, sc)
+    g = FakeT(T, out)
+    a = FakeT(2 * T + 4 * off[0], sa, sta)
+    b = FakeT(3 * T + 4 * off[1], sb)
+    c = FakeT(4 * T + 4 * off[2], sc)
+    grads = [k * T if w else None for k, w in zip((5, 6, 7), want)]
+    buf = ctypes.create_string_buffer(8192)
+    rc = L.zr_test_describe_chain_bwd(ops[op1], ops[op2], g.desc, a.desc, b.desc, c.desc, *grads,
+                                      buf, 8192)
+    assert rc == 0, rc
+    assert L.zr_test_dry_run_chain_bwd(ops[op1], ops[op2], g.desc, a.desc, b.desc, c.desc,
+                                       *grads) == 0
+    return json.loads(buf.value.decode())
+
+
+ops = {"add": 0, "sub": 1, "mul": 2, "div": 3}
+
+
+def test_chain_backward_routes(L):
+    """The two workload chains take the fused one-pass route; other layouts
+    take the composed route, whose workspace holds t and grad_t."""
+    d = _chain_desc(L, "mul", "add", (16, 1024, 768), (768,), (768,))
+    assert d["route"] == "fused"
+    (p,) = d["plans"]
+    assert p["kernel"] == "chain" and p["c_scalar"] == 0 and p["inner_kept"] == 1
+    assert (p["n_red"], p["ncol"]) == (16384, 768)
+    d = _chain_desc(L, "add", "div", (8, 12, 1024, 1024), (1, 1, 1024, 1024), (1,))
+    assert d["route"] == "fused"
+    (p,) = d["plans"]
+    assert p["c_scalar"] == 1 and (p["n_red"], p["ncol"]) == (96, 1024 * 1024)
+    assert p["c_slots"] == p["ctas"] and d["ws_run"] >= 4 * p["ctas"]
+    # The query sizes the fused route these pointers select: partials only.
+    assert d["ws_query"] == d["ws_run"] < 1 << 20
+    # c shaped differently from b: composed.
+    d = _chain_desc(L, "mul", "add", (16, 64, 96), (96,), (64, 1))
+    assert d["route"] == "composed" and d["need_t"] == 0 and d["need_gt"] == 1
+    assert d["ws_run"] >= 4 * 16 * 64 * 96
+    # op2 = mul with grad_c: t is needed too.
+    d = _chain_desc(L, "add", "mul", (16, 64, 96), (64, 96), (16, 1, 1))
+    assert d["route"] == "composed" and d["need_t"] == 1
+    assert d["ws_run"] >= 2 * 4 * 16 * 64 * 96
+    # a broadcast (not of the output's shape): composed.
+    d = _chain_desc(L, "mul", "add", (96,), (32, 96), (32, 96))
+    assert d["route"] == "composed"
+    # c misaligned for 16-byte loads: composed; a gradient not requested: composed.
+    d = _chain_desc(L, "mul", "add", (16, 1024, 768), (768,), (768,), off=(0, 0, 1))
+    assert d["route"] == "composed"
+    d = _chain_desc(L, "mul", "add", (16, 1024, 768), (768,), (768,), want=(1, 1, 0))
+    assert d["route"] == "composed" and d["need_t"] == 0
+
+
+def test_chain_errors_before_any_device_access(L):
+    T = 1 << 40
+    a, b, c = FakeT(T, (4, 8)), FakeT(2 * T, (8,)), FakeT(3 * T, (5,))
+    L.zr_chain_fwd.argtypes = [ctypes.c_int, ctypes.c_int, ZrTensor, ZrTensor, ZrTensor,
+                               ctypes.c_void_p, ctypes.POINTER(ctypes.c_int64), ctypes.c_void_p]
+    assert L.zr_chain_fwd(2, 0, a.desc, b.desc, c.desc, 4 * T, None, None) == -3
+    c1 = FakeT(3 * T, (8,))
+    assert L.zr_chain_fwd(9, 0, a.desc, b.desc, c1.desc, 4 * T, None, None) == -1
+    # Output partially overlapping an input.
+    assert L.zr_chain_fwd(2, 0, a.desc, b.desc, c1.desc, T + 4, None, None) == -5
+    g = FakeT(5 * T, (4, 8))
+    nbytes = ctypes.c_size_t(0)
+    # A gradient overlapping an input.
+    assert L.zr_chain_bwd(2, 0, g.desc, a.desc, b.desc, c1.desc, T, 6 * T, 7 * T, None,
+                          ctypes.byref(nbytes), None) == -5
+    # grad_out of the wrong shape.
+    g2 = FakeT(5 * T, (4, 9))
+    assert L.zr_chain_bwd(2, 0, g2.desc, a.desc, b.desc, c1.desc, 8 * T, 6 * T, 7 * T, None,
+                          ctypes.byref(nbytes), None) == -3
+    # A needed operand without data (op1 = mul: grad_a reads b).
+    bn = ZrTensor(None, 1, _i64([8]), None)
+    assert L.zr_chain_bwd(2, 0, g.desc, a.desc, bn, c1.desc, 8 * T, None, None, None,
+                          ctypes.byref(nbytes), None) == -1
+    # add then add reads no operand values: sizes alone are enough.
+    an = ZrTensor(None, 2, _i64([4, 8]), None)
+    cn = ZrTensor(None, 1, _i64([8]), None)
+    assert L.zr_chain_bwd(0, 0, g.desc, an, bn, cn, 8 * T, 6 * T, 7 * T, None,
+                          ctypes.byref(nbytes), None) == 0
+    assert nbytes.value >= 4 * 32  # grad_t in the workspace
