@@ -60,7 +60,7 @@ def parse():
     p.add_argument("--steps", type=int, default=300)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["zr", "reference"], default="zr")
-    p.add_argument("--workload", default="suite", help="suite or one of " + ",".join(SUITE))
+    p.add_argument("--workload", default="suite", help="suite or one of " + ",".join(workloads.NAMES))
     p.add_argument("--dims", default=None,
                    help="JSON size overrides for a single --workload (see workloads.DEFAULT_DIMS), "
                         "e.g. for a smaller profiling case")
@@ -103,8 +103,27 @@ def measured_peak():
 
 # ------------------------------------------------------------------ op list
 
+def chain_reads(op1, op2):
+    """Inputs (a, b, c) the full chain backward reads: t = a op1 b when op2's
+    grad_c needs it (mul, div); b for grad_a and a for grad_b when op1 is mul
+    or div (div's grad_b also b); c when op2 is mul or div."""
+    need_t = op2 in ("mul", "div")
+    ra = need_t or op1 in ("mul", "div")
+    rb = need_t or op1 in ("mul", "div")
+    rc = op2 in ("mul", "div")
+    return ra, rb, rc
+
+
 def op_bytes(step, shapes):
     """Algorithmic bytes of one op: read each input once, write each output once."""
+    if step[0] == "cfwd":
+        _, op1, op2, an, bn, cn, on = step
+        return 4 * (shapes[an] + shapes[bn] + shapes[cn] + shapes[on])
+    if step[0] == "cbwd":
+        _, op1, op2, gn, an, bn, cn, gan, gbn, gcn = step
+        ra, rb, rc = chain_reads(op1, op2)
+        return 4 * (shapes[gn] + ra * shapes[an] + rb * shapes[bn] + rc * shapes[cn]
+                    + shapes[gan] + shapes[gbn] + shapes[gcn])
     if step[0] == "fwd":
         _, op, an, bn, on = step
         return 4 * (shapes[an] + shapes[bn] + shapes[on])
@@ -126,10 +145,18 @@ def shape_table(name, host):
     """Element counts of every tensor named in a workload's steps."""
     sizes = {k: v.numel() for k, v in host.items()}
     shapes = {k: tuple(v.shape) for k, v in host.items()}
+    import numpy as np
     for step in workloads.STEPS[name]:
-        if step[0] == "fwd":
+        if step[0] == "cfwd":
+            _, op1, op2, an, bn, cn, on = step
+            shapes[on] = tuple(np.broadcast_shapes(shapes[an], shapes[bn], shapes[cn]))
+            sizes[on] = numel(shapes[on])
+        elif step[0] == "cbwd":
+            _, op1, op2, gn, an, bn, cn, gan, gbn, gcn = step
+            for src, dst in ((an, gan), (bn, gbn), (cn, gcn)):
+                shapes[dst], sizes[dst] = shapes[src], sizes[src]
+        elif step[0] == "fwd":
             _, op, an, bn, on = step
-            import numpy as np
             shapes[on] = tuple(np.broadcast_shapes(shapes[an], shapes[bn]))
             sizes[on] = numel(shapes[on])
         else:
@@ -228,12 +255,12 @@ class Suite:
                 env[k] = self._to_dev(v)
             outs = []
             for step in workloads.STEPS[name]:
-                if step[0] == "fwd":
-                    on = step[4]
+                if step[0] in ("fwd", "cfwd"):
+                    on = step[-1]
                     env[on] = torch.empty(shapes[on], dtype=torch.float32, device=device)
                     outs.append(on)
                 else:
-                    for gname in step[5:7]:
+                    for gname in (step[7:10] if step[0] == "cbwd" else step[5:7]):
                         env[gname] = torch.empty(shapes[gname], dtype=torch.float32, device=device)
                         outs.append(gname)
             self.host[name] = host
@@ -255,9 +282,55 @@ class Suite:
         self._keep.append(keep)
         return d
 
+    def _prepare_chain(self, name, step, env, sizes, stream_of):
+        zr, L, torch = self.zr, self.L, self.torch
+        nbytes = op_bytes(step, sizes)
+        op1, op2 = zr.OPS[step[1]], zr.OPS[step[2]]
+        if step[0] == "cfwd":
+            _, _, _, an, bn, cn, on = step
+            da, db, dc = self._desc(env[an]), self._desc(env[bn]), self._desc(env[cn])
+            out = env[on]
+            ost = zr._i64(out.stride())
+            self._keep.append(ost)
+            ptr = out.data_ptr()
+
+            def fn(da=da, db=db, dc=dc, ptr=ptr, ost=ost):
+                rc = L.zr_chain_fwd(op1, op2, da, db, dc, ptr, ost, stream_of())
+                if rc:
+                    raise zr.ZrError(rc, f"{name} chain fwd")
+            return (name, "fwd", f"{step[1]}+{step[2]}", nbytes, 1, fn, sizes[on])
+        _, _, _, gn, an, bn, cn, gan, gbn, gcn = step
+        dg, da, db, dc = (self._desc(env[k]) for k in (gn, an, bn, cn))
+        ptrs = [env[k].data_ptr() for k in (gan, gbn, gcn)]
+        need = ctypes.c_size_t(0)
+        assert L.zr_chain_bwd(op1, op2, dg, da, db, dc, *ptrs, None, ctypes.byref(need), None) == 0
+        ws = torch.empty(max(16, need.value), dtype=torch.uint8, device=self.device)
+        self._keep.append(ws)
+        L.zr_test_describe_chain_bwd.argtypes = [ctypes.c_int, ctypes.c_int] + [type(dg)] * 4 + [
+            ctypes.c_void_p] * 3 + [ctypes.c_char_p, ctypes.c_size_t]
+        buf = ctypes.create_string_buffer(8192)
+        assert L.zr_test_describe_chain_bwd(op1, op2, dg, da, db, dc, *ptrs, buf, 8192) == 0
+        desc = json.loads(buf.value.decode())
+        if desc["route"] == "fused":
+            p = desc["plans"][0]
+            launches = 1 + (p["nslots"] > 1) + ((p["ctas"] > 1) if p["c_scalar"] else (p["nslots"] > 1))
+        else:
+            launches = 0  # composed route: counted as one op of several launches
+        wsz = ws.numel()
+
+        def fn(dg=dg, da=da, db=db, dc=dc, ptrs=ptrs, wsp=ws.data_ptr(), wsz=wsz):
+            n = ctypes.c_size_t(wsz)
+            rc = L.zr_chain_bwd(op1, op2, dg, da, db, dc, *ptrs, wsp, ctypes.byref(n), stream_of())
+            if rc:
+                raise zr.ZrError(rc, f"{name} chain bwd")
+        return (name, "bwd", f"{step[1]}+{step[2]} ({desc['route']})", nbytes, launches, fn,
+                sizes[gn])
+
     def _prepare(self, name, step, env, sizes):
         zr, L, torch = self.zr, self.L, self.torch
         stream_of = lambda: ctypes.c_void_p(torch.cuda.current_stream(self.device).cuda_stream)
+        if step[0] in ("cfwd", "cbwd"):
+            return self._prepare_chain(name, step, env, sizes, stream_of)
         opc = zr.OPS[step[1]]
         nbytes = op_bytes(step, sizes)
         if step[0] == "fwd":
@@ -415,7 +488,7 @@ def run_zr(args, rank, world, local):
 
     per_config = per_op_alone = None
     if rank == 0 and args.config_reps > 0:
-        extra = [Suite(["x1"], device)] if args.workload == "suite" else []
+        extra = [Suite(["x1", "c3f", "c4f"], device)] if args.workload == "suite" else []
         per_config, per_op_alone = run_per_config([suite] + extra, flush, stream, args.config_reps)
     e2e = None
     if not args.no_e2e and rank == 0:

@@ -691,7 +691,7 @@ int zr_test_occupancy(int which, int* planned, int* actual) {
   else if (which >= 4 && which < 9) e = occupancy_red(which - 4, planned, actual);
   else if (which >= 9 && which < 11) e = occupancy_other(which - 9, planned, actual);
   else if (which >= 11 && which < 16) e = occupancy_red(which - 6, planned, actual);
-  else if (which >= 16 && which < 19) e = occupancy_chain(which - 16, planned, actual);
+  else if (which >= 16 && which < 20) e = occupancy_chain(which - 16, planned, actual);
   else return ZR_ERR_SIZE;
   return cuda_status(e);
 }
@@ -1027,6 +1027,7 @@ namespace {
 
 struct ChainFwdSet {
   bool empty = false;
+  bool c_one = false;  // c has one element
   EwBuild eb;
   TDesc a, b, c, out;
 };
@@ -1072,7 +1073,8 @@ int plan_chain_fwd(int op1, int op2, const zr_tensor& ta, const zr_tensor& tb,
   const uint32_t stream_mask = (S->a.numel == S->out.numel ? 1u : 0u) |
                                (S->b.numel == S->out.numel ? 2u : 0u) |
                                (S->c.numel == S->out.numel ? 4u : 0u);
-  return build_ew(P, in, outs, 0x7u, stream_mask, kOccEwBwd, &S->eb);
+  S->c_one = S->c.numel == 1;
+  return build_ew(P, in, outs, 0x7u, stream_mask, S->c_one ? kOccEwFwd : kOccEwBwd, &S->eb);
 }
 
 struct ChainBwdSet {
@@ -1338,7 +1340,8 @@ int zr_chain_fwd(zr_op op1, zr_op op2, zr_tensor a, zr_tensor b, zr_tensor c, fl
     rc = check_device_ptr(p);
     if (rc) return rc;
   }
-  return cuda_status(launch_chain_fwd(op1, op2, S.eb, reinterpret_cast<cudaStream_t>(stream)));
+  return cuda_status(
+      launch_chain_fwd(op1, op2, S.c_one, S.eb, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int zr_chain_bwd(zr_op op1, zr_op op2, zr_tensor grad_out, zr_tensor a, zr_tensor b, zr_tensor c,

@@ -128,7 +128,8 @@ k_chain_bwd(const __grid_constant__ ChainPlan cp) {
   }
 
   // grad_b (and grad_c with b's shape): fixed tree over the ty row lanes of
-  // each column vector, then one value per column to a slot or the output.
+  // each column vector, then one value per column to the output or to its
+  // slot row [grad_b's nout | grad_c's nout] (CSCALAR: grad_b's nout only).
   const uint32_t lanes = p.tx * VEC;
   const uint32_t vc = vcol_begin + tx;
   const uint64_t j = uint64_t(cta.kidx) * p.ncol + uint64_t(vc) * VEC;
@@ -159,7 +160,8 @@ k_chain_bwd(const __grid_constant__ ChainPlan cp) {
       }
       float* dst;
       if (p.nslots == 1) dst = (which == 0 ? p.x_final : cp.c_final) + j;
-      else dst = (which == 0 ? p.partial : cp.c_partial) + uint64_t(cta.rblk) * p.nout + j;
+      else dst = p.partial + uint64_t(cta.rblk) * (CSCALAR ? p.nout : 2 * p.nout) +
+                 (which == 0 ? 0 : p.nout) + j;
       store_cols<VEC>(dst, 0, 1, 0, r);
     }
   }

@@ -331,13 +331,15 @@ ZR_HD uint32_t sab_owner(const SabPlan& p, uint64_t step) {
 // dense gradient (r.d_out), grad_b the reduced one (r's X, inner dim kept,
 // 16-byte vectors), and grad_c is summed in the same pass.  Either c has b's
 // shape and both are dense, so c's offsets are b's and grad_c shares grad_b's
-// tiling and slots (c_scalar = 0); or c has one element and grad_c is the
-// total sum, one partial per CTA (c_scalar = 1).
+// tiling and slots (c_scalar = 0): the partials are r.partial[nslots][2 nout],
+// grad_b's in the first nout of each slot row and grad_c's in the second, so
+// one second pass finishes both.  Or c has one element and grad_c is the total
+// sum, one partial per CTA in c_partial[n_cta] (c_scalar = 1).
 struct ChainPlan {
   RedPlan r;                // g, a, b, grad_b (x_final / partial), grad_a (d_out)
   const float* c;
   float* c_final;           // grad_c
-  float* c_partial;         // grad_c partials: [nslots][nout], or [n_cta] when c_scalar
+  float* c_partial;         // c_scalar: grad_c's per-CTA partials
   uint32_t c_scalar;
 };
 constexpr int kOccChain = 3;  // k_chain_bwd: CTAs per SM
@@ -345,7 +347,9 @@ constexpr int kOccChain = 3;  // k_chain_bwd: CTAs per SM
 // Second pass: out[j] = sum over s of partial[s * nout + j], s in order.
 struct CombinePlan {
   const float* partial;
-  float* out;
+  float* out;               // outputs j < split
+  float* out2;              // outputs j >= split, at out2[j - split]
+  uint64_t split;           // nout when every output goes to out
   uint64_t nout;
   uint32_t nslots;
   uint32_t jx, sy;          // thread layout: jx outputs x sy slot lanes

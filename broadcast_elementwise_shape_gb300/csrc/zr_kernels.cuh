@@ -193,11 +193,13 @@ struct BwdDirectF {
 
 // Forward of a two-op chain: out = (a op1 b) op2 c, each op one IEEE
 // binary32 operation (the intermediate is rounded as the unfused ops would
-// store it).  Slots 0, 1, 2 = a, b, c.
-template <int OP1, int OP2>
+// store it).  Slots 0, 1, 2 = a, b, c.  C_ONE: c has one element, loaded once
+// per thread instead of per item (fewer registers: 4 CTAs per SM).
+template <int OP1, int OP2, bool C_ONE>
 struct ChainF {
   static constexpr bool kR1 = true, kR2 = true;
-  static constexpr int kMinBlocks = kOccEwBwd;
+  static constexpr bool kUniform2 = C_ONE;
+  static constexpr int kMinBlocks = C_ONE ? kOccEwFwd : kOccEwBwd;
   template <int VEC>
   __device__ __forceinline__ void operator()(const Vec<VEC> (&x)[3], Vec<VEC> (&y)[2]) const {
 #pragma unroll
@@ -217,6 +219,13 @@ struct CopyF {
 
 // ---------------------------------------------------------------- elementwise
 
+// Slot 2 holds one value for every element (read once per thread), when the
+// functor says so.
+template <class F, class = void>
+struct Uniform2 { static constexpr bool value = false; };
+template <class F>
+struct Uniform2<F, decltype(void(F::kUniform2))> { static constexpr bool value = F::kUniform2; };
+
 // One CTA = one tile of rows x column vectors.  Each thread takes items
 // threadIdx.x + k * 256; items are processed in batches of U so that U
 // independent loads per operand are in flight before any result is stored.
@@ -234,6 +243,9 @@ k_elementwise(const __grid_constant__ EwPlan p) {
   }
   __syncthreads();
   pdl_wait();
+  constexpr bool kUni2 = Uniform2<F>::value;
+  float uni2 = 0.f;
+  if (kUni2) uni2 = __ldg(p.in[2]);
 
   constexpr int U = 4;
   const F f;
@@ -254,7 +266,12 @@ k_elementwise(const __grid_constant__ EwPlan p) {
         const int64_t* ro = s_off + ri * kMaxOperands;
         x[u][0] = load_cols<VEC>(p.in[0], ro[0], p.inner_stride[0], col[u], p.stream_mask & 1);
         if (F::kR1) x[u][1] = load_cols<VEC>(p.in[1], ro[1], p.inner_stride[1], col[u], p.stream_mask & 2);
-        if (F::kR2) x[u][2] = load_cols<VEC>(p.in[2], ro[2], p.inner_stride[2], col[u], p.stream_mask & 4);
+        if (F::kR2 && kUni2) {
+#pragma unroll
+          for (int i = 0; i < VEC; ++i) x[u][2].v[i] = uni2;
+        } else if (F::kR2) {
+          x[u][2] = load_cols<VEC>(p.in[2], ro[2], p.inner_stride[2], col[u], p.stream_mask & 4);
+        }
         doff[u] = ro[kSlotOut];
       }
     }
@@ -695,7 +712,11 @@ k_combine(const __grid_constant__ CombinePlan p) {
     if (sl < h) s_red[sl * p.jx + jl] = __fadd_rn(s_red[sl * p.jx + jl], s_red[(sl + h) * p.jx + jl]);
   }
   __syncthreads();
-  if (sl == 0 && j < p.nout) p.out[j] = __fmul_rn(s_red[jl], p.scale);
+  if (sl == 0 && j < p.nout) {
+    const float v = __fmul_rn(s_red[jl], p.scale);
+    if (j < p.split) p.out[j] = v;
+    else p.out2[j - p.split] = v;
+  }
 }
 
 }  // namespace zr

@@ -85,10 +85,13 @@ cudaError_t occupancy_other(int which, int* planned, int* actual);
 
 // Two-op chains out = (a op1 b) op2 c: the forward (slots 0..2 = a, b, c)
 // and the fused one-pass backward with its second passes.
-cudaError_t launch_chain_fwd(int op1, int op2, const EwBuild& eb, cudaStream_t s, bool dry = false);
+// c_one: c has one element (read once per thread, 4 CTAs per SM).
+cudaError_t launch_chain_fwd(int op1, int op2, bool c_one, const EwBuild& eb, cudaStream_t s,
+                             bool dry = false);
 cudaError_t launch_chain_bwd(int op1, int op2, const ChainBuild& cb, cudaStream_t s, bool dry = false);
 // 0: chain forward (mul, add); 1: fused backward (mul, add), c shaped like b;
-// 2: fused backward (add, div), c one element.
+// 2: fused backward (add, div), c one element; 3: chain forward (add, div), c
+// one element.
 cudaError_t occupancy_chain(int which, int* planned, int* actual);
 
 // Fused backward with both gradients reduced: the k_sab pass, then one

@@ -8,12 +8,23 @@ namespace zr {
 
 namespace {
 
-template <int OP1, int OP2>
-cudaError_t launch_chain_fwd_t(const EwBuild& eb, cudaStream_t s) {
-  using F = ChainF<OP1, OP2>;
+template <int OP1, int OP2, bool C_ONE>
+cudaError_t launch_chain_fwd_c(const EwBuild& eb, cudaStream_t s) {
+  using F = ChainF<OP1, OP2, C_ONE>;
   const size_t smem = size_t(eb.plan.tile_rows) * kMaxOperands * sizeof(int64_t);
   if (eb.vec == 4) return launch_k(k_elementwise<F, 4, 1>, eb.plan.n_cta, kThreads, smem, s, eb.plan);
   return launch_k(k_elementwise<F, 1, 1>, eb.plan.n_cta, kThreads, smem, s, eb.plan);
+}
+
+// c_one: c has one element (read once per thread).
+struct FwdArg {
+  const EwBuild& eb;
+  bool c_one;
+};
+template <int OP1, int OP2>
+cudaError_t launch_chain_fwd_t(const FwdArg& f, cudaStream_t s) {
+  return f.c_one ? launch_chain_fwd_c<OP1, OP2, true>(f.eb, s)
+                 : launch_chain_fwd_c<OP1, OP2, false>(f.eb, s);
 }
 
 cudaError_t launch_combine(const CombinePlan& c, cudaStream_t s) {
@@ -30,11 +41,8 @@ cudaError_t launch_chain_bwd_t(const ChainBuild& cb, cudaStream_t s) {
   cudaError_t e = cp.c_scalar ? launch_k(k_chain_bwd<OP1, OP2, true>, p.n_cta, kThreads, smem, s, cp)
                               : launch_k(k_chain_bwd<OP1, OP2, false>, p.n_cta, kThreads, smem, s, cp);
   if (e != cudaSuccess) return e;
-  if (p.nslots > 1) {
-    e = launch_combine(cb.comb_b, s);
-    if (e != cudaSuccess) return e;
-    if (!cp.c_scalar) e = launch_combine(cb.comb_c, s);
-  }
+  // With c shaped like b, one second pass finishes grad_b and grad_c.
+  if (p.nslots > 1) e = launch_combine(cb.comb_b, s);
   if (e == cudaSuccess && cp.c_scalar && p.n_cta > 1) e = launch_combine(cb.comb_c, s);
   return e;
 }
@@ -47,12 +55,12 @@ cudaError_t launch_chain_bwd_t(const ChainBuild& cb, cudaStream_t s) {
     default: return FN<OP1, OP_DIV>(ARG, s);                 \
   }
 
-cudaError_t fwd_dispatch(int op1, int op2, const EwBuild& eb, cudaStream_t s) {
+cudaError_t fwd_dispatch(int op1, int op2, const FwdArg& f, cudaStream_t s) {
   switch (op1) {
-    case OP_ADD: ZR_CHAIN_CASES(OP_ADD, launch_chain_fwd_t, eb)
-    case OP_SUB: ZR_CHAIN_CASES(OP_SUB, launch_chain_fwd_t, eb)
-    case OP_MUL: ZR_CHAIN_CASES(OP_MUL, launch_chain_fwd_t, eb)
-    default: ZR_CHAIN_CASES(OP_DIV, launch_chain_fwd_t, eb)
+    case OP_ADD: ZR_CHAIN_CASES(OP_ADD, launch_chain_fwd_t, f)
+    case OP_SUB: ZR_CHAIN_CASES(OP_SUB, launch_chain_fwd_t, f)
+    case OP_MUL: ZR_CHAIN_CASES(OP_MUL, launch_chain_fwd_t, f)
+    default: ZR_CHAIN_CASES(OP_DIV, launch_chain_fwd_t, f)
   }
 }
 
@@ -68,11 +76,12 @@ cudaError_t bwd_dispatch(int op1, int op2, const ChainBuild& cb, cudaStream_t s)
 
 }  // namespace
 
-cudaError_t launch_chain_fwd(int op1, int op2, const EwBuild& eb, cudaStream_t s, bool dry) {
+cudaError_t launch_chain_fwd(int op1, int op2, bool c_one, const EwBuild& eb, cudaStream_t s,
+                             bool dry) {
   if (!eb.plan.in[0] || !eb.plan.in[1] || !eb.plan.in[2] || !eb.plan.out[0])
     return cudaErrorInvalidValue;
   if (dry) return cudaSuccess;
-  return fwd_dispatch(op1, op2, eb, s);
+  return fwd_dispatch(op1, op2, FwdArg{eb, c_one}, s);
 }
 
 cudaError_t launch_chain_bwd(int op1, int op2, const ChainBuild& cb, cudaStream_t s, bool dry) {
@@ -80,7 +89,8 @@ cudaError_t launch_chain_bwd(int op1, int op2, const ChainBuild& cb, cudaStream_
   const RedPlan& p = cp.r;
   // The kernel dereferences every one of these.
   if (!p.g || !p.a || !p.b || !cp.c || !p.d_out || !p.x_final || !cp.c_final ||
-      !p.inner_kept || p.cluster > 1 || (p.nslots > 1 && (!p.partial || !cp.c_partial)) ||
+      !p.inner_kept || p.cluster > 1 || (p.nslots > 1 && !p.partial) ||
+      (!cp.c_scalar && p.nslots > 1 && (cb.comb_b.split != p.nout || !cb.comb_b.out2)) ||
       (cp.c_scalar && p.n_cta > 1 && !cp.c_partial))
     return cudaErrorInvalidValue;
   if (dry) return cudaSuccess;
@@ -94,7 +104,12 @@ cudaError_t occupancy_chain(int which, int* planned, int* actual) {
     case 0:
       *planned = kOccEwBwd;
       return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-          actual, k_elementwise<ChainF<OP_MUL, OP_ADD>, 4, 1>, kThreads,
+          actual, k_elementwise<ChainF<OP_MUL, OP_ADD, false>, 4, 1>, kThreads,
+          size_t(kMaxTileRows) * kMaxOperands * sizeof(int64_t));
+    case 3:
+      *planned = kOccEwFwd;
+      return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+          actual, k_elementwise<ChainF<OP_ADD, OP_DIV, true>, 4, 1>, kThreads,
           size_t(kMaxTileRows) * kMaxOperands * sizeof(int64_t));
     case 1:
       *planned = kOccChain;

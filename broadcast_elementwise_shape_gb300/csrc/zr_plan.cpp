@@ -536,6 +536,7 @@ int build_red(const Prob& P, int xslot, const float* g, const float* a, const fl
   CombinePlan& c = rb->comb;
   c = CombinePlan{};
   c.nout = p.nout;
+  c.split = p.nout;
   c.nslots = p.nslots;
   c.out = x_out;
   c.scale = 1.0f;
@@ -563,18 +564,23 @@ int build_chain(const Prob& P, const float* g, const float* a, const float* b, c
   cb->comb_b = rb.comb;
   cb->ws_b_bytes = rb.ws_bytes;
   CombinePlan& cc = cb->comb_c;
+  cc = CombinePlan{};
   if (c_scalar) {
-    cc = CombinePlan{};
     cc.nout = 1;
+    cc.split = 1;
     cc.nslots = rb.plan.n_cta;
     cc.out = grad_c;
     cc.scale = 1.0f;
     combine_layout(&cc);
     cb->ws_c_bytes = rb.plan.n_cta > 1 ? ((uint64_t(rb.plan.n_cta) * 4 + 255) / 256) * 256 : 0;
-  } else {
-    cc = rb.comb;
-    cc.out = grad_c;
-    cb->ws_c_bytes = rb.ws_bytes;
+  } else if (rb.plan.nslots > 1) {
+    // One second pass over [nslots][2 nout]: grad_b, then grad_c.
+    CombinePlan& c2 = cb->comb_b;
+    c2.nout = 2 * rb.plan.nout;
+    c2.split = rb.plan.nout;
+    c2.out2 = grad_c;
+    combine_layout(&c2);
+    cb->ws_b_bytes = ((uint64_t(rb.plan.nslots) * c2.nout * 4 + 255) / 256) * 256;
   }
   return ZR_OK;
 }
@@ -845,6 +851,7 @@ int build_sab(const Prob& P, const float* g, const float* a, const float* b, flo
     CombinePlan& c = *cs[w];
     c = CombinePlan{};
     c.nout = nouts[w];
+    c.split = nouts[w];
     c.nslots = nsl[w];
     c.out = outs[w];
     c.scale = 1.0f;

@@ -72,7 +72,14 @@ def run_gpu(name: str, host: dict) -> dict:
     """All step outputs of workload ``name`` computed by the CUDA library."""
     env = {k: to_gpu(v) for k, v in host.items()}
     for step in workloads.STEPS[name]:
-        if step[0] == "fwd":
+        if step[0] == "cfwd":
+            _, op1, op2, an, bn, cn, on = step
+            env[on] = zr.zr_chain_fwd(op1, op2, env[an], env[bn], env[cn])
+        elif step[0] == "cbwd":
+            _, op1, op2, gn, an, bn, cn, gan, gbn, gcn = step
+            env[gan], env[gbn], env[gcn] = zr.zr_chain_bwd(op1, op2, env[gn], env[an], env[bn],
+                                                           env[cn])
+        elif step[0] == "fwd":
             _, op, an, bn, on = step
             env[on] = zr.zr_binary_fwd(op, env[an], env[bn])
         else:
@@ -88,7 +95,16 @@ def run_oracle(name: str, host: dict) -> tuple[dict, dict]:
     env = {k: v for k, v in host.items()}
     sums = {}
     for step in workloads.STEPS[name]:
-        if step[0] == "fwd":
+        if step[0] == "cfwd":
+            _, op1, op2, an, bn, cn, on = step
+            env[on] = torch.from_numpy(oracle.chain_fwd(op1, op2, env[an], env[bn], env[cn]))
+        elif step[0] == "cbwd":
+            _, op1, op2, gn, an, bn, cn, gan, gbn, gcn = step
+            r = oracle.chain_bwd(op1, op2, env[gn], env[an], env[bn], env[cn])
+            for k, nm in enumerate((gan, gbn, gcn)):
+                env[nm] = torch.from_numpy(r[k])
+                sums[nm] = r[3 + k]
+        elif step[0] == "fwd":
             _, op, an, bn, on = step
             env[on] = torch.from_numpy(oracle.binary_fwd(op, env[an], env[bn]))
         else:
@@ -102,6 +118,24 @@ def run_oracle(name: str, host: dict) -> tuple[dict, dict]:
 def compare_workload(name: str, host: dict, gpu: dict, ref: dict, sums: dict):
     out_shapes = {}
     for step in workloads.STEPS[name]:
+        if step[0] == "cfwd":
+            on = step[6]
+            bitexact(gpu[on].numpy(), ref[on].numpy(), f"{name} chain fwd -> {on}")
+            continue
+        if step[0] == "cbwd":
+            _, op1, op2, gn, an, bn, cn, gan, gbn, gcn = step
+            n_out = ref[gn].numel()
+            t_full = int(np.prod(np.broadcast_shapes(tuple(ref[an].shape), tuple(ref[bn].shape)))) == n_out
+            for k, (src, gname) in enumerate(((an, gan), (bn, gbn), (cn, gcn))):
+                full = ref[gname].numel() == n_out
+                exact = full and ((k == 0 and t_full) or (k == 1 and t_full and op1 != "div") or
+                                  (k == 2 and op2 != "div"))
+                what = f"{name} chain bwd -> {gname}"
+                if exact:
+                    bitexact(gpu[gname].numpy(), ref[gname].numpy(), what)
+                else:
+                    within(gpu[gname].numpy(), ref[gname].numpy(), sums[gname], what)
+            continue
         if step[0] == "fwd":
             _, op, an, bn, on = step
             bitexact(gpu[on].numpy(), ref[on].numpy(), f"{name} fwd {op} -> {on}")

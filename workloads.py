@@ -25,16 +25,24 @@ cases with the same structure):
 * ``x1`` same-shape contiguous add, a [R,C] N(0,1) + b [R,C] N(0,1), g N(0,1)
   (4096,4096): a supplementary case for the contiguous path without
   broadcasting (not one of the five workloads of the benchmark step)
+* ``c3f`` and ``c4f``: the inputs of ``c3`` and ``c4`` (same seeds and
+  sizes), run as one fused two-op chain each, (x * gamma) + beta and
+  (scores + mask) / scalar (supplementary, outside the benchmark step)
 
 Each workload also lists its op steps (forward chain, then backward in
 reverse) as data: ``("fwd", op, a_name, b_name, out_name)`` and
-``("bwd", op, g_name, a_name, b_name, grad_a_name, grad_b_name)``.
+``("bwd", op, g_name, a_name, b_name, grad_a_name, grad_b_name)``; a fused
+chain is ``("cfwd", op1, op2, a_name, b_name, c_name, out_name)`` and
+``("cbwd", op1, op2, g_name, a_name, b_name, c_name, grad_a_name,
+grad_b_name, grad_c_name)``.
 """
 from __future__ import annotations
 
 import torch
 
 SEEDS = {"c1": 1001, "c2": 1002, "c3": 1003, "c4": 1004, "c5a": 1005, "c5b": 1006, "x1": 1007}
+# Fused-chain workloads draw the inputs of the workload they fuse.
+BASE = {"c3f": "c3", "c4f": "c4"}
 
 DEFAULT_DIMS = {
     "c1": dict(P=32, M=64, Q=128),
@@ -66,6 +74,11 @@ STEPS = {
             ("bwd", "div", "g", "a", "b", "grad_a", "grad_b")],
     "x1": [("fwd", "add", "a", "b", "out"),
            ("bwd", "add", "g", "a", "b", "grad_a", "grad_b")],
+    "c3f": [("cfwd", "mul", "add", "x", "gamma", "beta", "y2"),
+            ("cbwd", "mul", "add", "g", "x", "gamma", "beta", "grad_x", "grad_gamma", "grad_beta")],
+    "c4f": [("cfwd", "add", "div", "scores", "mask", "scalar", "out"),
+            ("cbwd", "add", "div", "g", "scores", "mask", "scalar", "grad_scores", "grad_mask",
+             "grad_scalar")],
 }
 
 NAMES = list(STEPS)
@@ -93,6 +106,7 @@ def make_inputs(name: str, seed: int | None = None, **dims) -> dict:
     ``dims`` overrides the default sizes (see ``DEFAULT_DIMS``) for small
     parity cases; ``seed`` overrides the workload's seed.
     """
+    name = BASE.get(name, name)
     d = dict(DEFAULT_DIMS[name])
     d.update(dims)
     gen = torch.Generator("cpu").manual_seed(SEEDS[name] if seed is None else seed)
@@ -160,4 +174,7 @@ def small_dims(name: str) -> dict:
         "c5a": dict(P=5, M=67, Q=203),
         "c5b": dict(a=(3, 1, 5, 1, 4, 1, 7, 12), b=(1, 2, 1, 3, 1, 5, 1, 12)),
         "x1": dict(R=333, C=1030),
+        "c3f": dict(B=3, T=97, C=772),
+        # 132 columns: 16-byte vectors, so the fused one-pass backward runs.
+        "c4f": dict(N=2, H=3, T=132),
     }[name]
