@@ -44,6 +44,11 @@ class ZrTensor(ctypes.Structure):
                 ("strides", ctypes.POINTER(ctypes.c_int64))]
 
 
+class ZrGrad(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("strides", ctypes.POINTER(ctypes.c_int64)),
+                ("accumulate", ctypes.c_int32)]
+
+
 def lib() -> ctypes.CDLL:
     """The loaded ``libzr.so``; raises if it has not been built."""
     global _lib
@@ -60,13 +65,15 @@ def lib() -> ctypes.CDLL:
         L.zr_binary_fwd.argtypes = [c_int, ZrTensor, ZrTensor, vp, i64p, vp]
         L.zr_binary_bwd.argtypes = [c_int, ZrTensor, ZrTensor, ZrTensor, vp, vp, vp, szp, vp]
         L.zr_sum_to_shape.argtypes = [ZrTensor, i32, i64p, vp, vp, szp, vp]
+        L.zr_binary_bwd_ex.argtypes = [c_int, ZrTensor, ZrTensor, ZrTensor, ZrGrad, ZrGrad, vp, szp,
+                                       vp]
         L.zr_chain_fwd.argtypes = [c_int, c_int, ZrTensor, ZrTensor, ZrTensor, vp, i64p, vp]
         L.zr_chain_bwd.argtypes = [c_int, c_int, ZrTensor, ZrTensor, ZrTensor, ZrTensor, vp, vp, vp,
                                    vp, szp, vp]
         L.zr_status_string.argtypes = [c_int]
         L.zr_status_string.restype = ctypes.c_char_p
         for f in ("zr_broadcast_shape", "zr_binary_fwd", "zr_binary_bwd", "zr_sum_to_shape",
-                  "zr_chain_fwd", "zr_chain_bwd"):
+                  "zr_chain_fwd", "zr_chain_bwd", "zr_binary_bwd_ex"):
             getattr(L, f).restype = c_int
         _lib = L
     return _lib
@@ -235,3 +242,39 @@ def zr_chain_bwd(op1, op2, grad_out, a, b, c, want=(True, True, True), grads=(No
                         workspace.data_ptr(), ctypes.byref(nbytes), _stream(grad_out))
     _check(rc, "zr_chain_bwd")
     return tuple(gs)
+
+
+def _grad(t, acc):
+    """zr_grad for a caller's gradient tensor (any strides) or None."""
+    if t is None:
+        return ZrGrad(None, None, 0), ()
+    st = _i64(t.stride())
+    return ZrGrad(t.data_ptr() if t.numel() else None, st, 1 if acc else 0), (st, t)
+
+
+def zr_binary_bwd_ex(op, grad_out, a, b, grad_a=None, grad_b=None, accumulate=(False, False),
+                     shape_a=None, shape_b=None, workspace=None):
+    """Backward of out = a op b into the caller's gradient tensors, which may
+    be strided views; ``accumulate[k]`` adds to what they hold (grad +=
+    result) instead of overwriting.  Returns (grad_a, grad_b)."""
+    sa = tuple(a.shape) if a is not None else tuple(shape_a)
+    sb = tuple(b.shape) if b is not None else tuple(shape_b)
+    for g, s in ((grad_a, sa), (grad_b, sb)):
+        if g is not None and tuple(g.shape) != s:
+            raise ValueError(f"gradient has shape {tuple(g.shape)}, expected {s}")
+    dg, kg = _desc(grad_out)
+    da, ka = _desc(a, sa)
+    db, kb = _desc(b, sb)
+    gga, kga = _grad(grad_a, accumulate[0])
+    ggb, kgb = _grad(grad_b, accumulate[1])
+    L = lib()
+    nbytes = ctypes.c_size_t(0)
+    _check(L.zr_binary_bwd_ex(_op(op), dg, da, db, gga, ggb, None, ctypes.byref(nbytes), None),
+           "zr_binary_bwd_ex (workspace query)")
+    if workspace is None or workspace.numel() < nbytes.value:
+        workspace = _workspace(nbytes.value, grad_out.device)
+    nbytes = ctypes.c_size_t(workspace.numel())
+    rc = L.zr_binary_bwd_ex(_op(op), dg, da, db, gga, ggb, workspace.data_ptr(),
+                            ctypes.byref(nbytes), _stream(grad_out))
+    _check(rc, "zr_binary_bwd_ex")
+    return grad_a, grad_b

@@ -1408,3 +1408,183 @@ int zr_test_dry_run_chain_bwd(zr_op op1, zr_op op2, zr_tensor grad_out, zr_tenso
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------ backward with gradient layouts
+//
+// zr_binary_bwd_ex: each gradient may be strided and may be accumulated
+// into (AccumulateGrad, Autograd page, section 反向传播: when the gradient
+// slot already holds a value, the new gradient is added in place).  Dense
+// gradients are written (or added to) by the backward kernels themselves; a
+// strided gradient is computed densely into the workspace and then copied
+// (or added) into its layout by one elementwise pass.
+
+namespace zr {
+namespace {
+
+struct BwdExSet {
+  BwdSet S;
+  float* user[2] = {nullptr, nullptr};
+  bool stage[2] = {false, false};
+  bool acc[2] = {false, false};
+  TDesc gd[2];
+  EwBuild copy[2];
+  size_t off_stage[2] = {0, 0};
+  size_t off_ws = 0;
+  size_t ws_run = 0, ws_query = 0;
+};
+
+int plan_bwd_ex(int op, const zr_tensor& tg, const zr_tensor& ta, const zr_tensor& tb,
+                const zr_grad& ga, const zr_grad& gb, void* workspace, BwdExSet* E) {
+  const zr_grad* gs[2] = {&ga, &gb};
+  const zr_tensor* ins[2] = {&ta, &tb};
+  TDesc in_desc[2], g_desc;
+  int rc = read_tensor(tg, &g_desc);
+  if (rc) return rc;
+  for (int w = 0; w < 2; ++w) {
+    rc = read_tensor(*ins[w], &in_desc[w]);
+    if (rc) return rc;
+    E->user[w] = gs[w]->data;
+    E->acc[w] = gs[w]->data && gs[w]->accumulate != 0;
+    if (!gs[w]->data) continue;
+    const zr_tensor t{gs[w]->data, ins[w]->ndim, ins[w]->sizes, gs[w]->strides};
+    rc = read_tensor(t, &E->gd[w]);
+    if (rc) return rc;
+    if (!non_overlapping(E->gd[w])) return ZR_ERR_LAYOUT;
+    E->stage[w] = !dense_layout(E->gd[w]);
+  }
+  // A staged (strided) gradient is checked here against everything else;
+  // dense ones are checked by the backward's own plan.
+  for (int w = 0; w < 2; ++w) {
+    if (!E->stage[w]) continue;
+    const Span sp = span_of(E->gd[w].ptr, E->gd[w].extent);
+    if (E->user[1 - w] && overlaps(sp, span_of(E->gd[1 - w].ptr, E->gd[1 - w].extent)))
+      return ZR_ERR_LAYOUT;
+    for (const TDesc* x : {&g_desc, &in_desc[0], &in_desc[1]})
+      if (overlaps(sp, span_of(x->ptr, x->extent))) return ZR_ERR_LAYOUT;
+  }
+  // Workspace: [staged grad_a][staged grad_b][the backward's partials].
+  size_t off = 0;
+  for (int w = 0; w < 2; ++w) {
+    E->off_stage[w] = off;
+    if (E->stage[w]) off += align256(size_t(E->gd[w].numel) * 4);
+  }
+  E->off_ws = off;
+  char* base = static_cast<char*>(workspace);
+  if (!base) {
+    // Query: staging placed above every operand, so no layout check trips.
+    uintptr_t top = 0;
+    for (const TDesc* x : {&g_desc, &in_desc[0], &in_desc[1], &E->gd[0], &E->gd[1]})
+      top = std::max(top, span_of(x->ptr, x->extent).hi);
+    base = reinterpret_cast<char*>(align256(top) + 256);
+  }
+  float* pg[2];
+  for (int w = 0; w < 2; ++w)
+    pg[w] = E->stage[w] ? reinterpret_cast<float*>(base + E->off_stage[w]) : E->user[w];
+  rc = plan_bwd(op, tg, ta, tb, pg[0], pg[1], &E->S);
+  if (rc) return rc;
+  BwdSet& S = E->S;
+  // Accumulate flags of the gradients the kernels write in place.
+  const bool acc_k[2] = {E->acc[0] && !E->stage[0], E->acc[1] && !E->stage[1]};
+  if (S.direct) {
+    S.eb.plan.acc_mask = (acc_k[0] ? 1u : 0u) | (acc_k[1] ? 2u : 0u);
+  } else if (S.sab) {
+    S.sb.comb_a.accumulate = acc_k[0];
+    S.sb.comb_b.accumulate = acc_k[1];
+  } else {
+    for (int i = 0; i < S.nred; ++i) {
+      const int w = S.which[i];
+      S.rb[i].plan.acc_x = acc_k[w];
+      S.rb[i].comb.accumulate = acc_k[w];
+      S.rb[i].plan.acc_d = acc_k[1 - w];
+    }
+  }
+  // Copy (or add) each staged gradient into its layout.
+  for (int w = 0; w < 2; ++w) {
+    if (!E->stage[w] || E->gd[w].numel == 0) continue;
+    const TDesc& x = E->gd[w];
+    int64_t st[kProbSlots][kMaxDims] = {};
+    int64_t dense[kMaxDims];
+    contiguous_strides(x.nd, x.size, dense);
+    for (int d = 0; d < x.nd; ++d) {
+      st[0][d] = x.size[d] == 1 ? 0 : dense[d];
+      st[kSlotOut][d] = x.size[d] == 1 ? 0 : x.stride[d];
+    }
+    Prob P;
+    rc = coalesce(x.nd, x.size, st, 1u | (1u << kSlotOut), kSlotOut, &P);
+    if (rc) return rc;
+    const float* in[3] = {pg[w], nullptr, nullptr};
+    float* outs[2] = {E->user[w], nullptr};
+    rc = build_ew(P, in, outs, 1u, 1u, kOccEwCopy, &E->copy[w]);
+    if (rc) return rc;
+    E->copy[w].plan.acc_mask = E->acc[w] ? 1u : 0u;
+  }
+  E->ws_run = E->off_ws + S.ws_run;
+  E->ws_query = E->off_ws + S.ws_query;
+  return ZR_OK;
+}
+
+}  // namespace
+}  // namespace zr
+
+extern "C" {
+
+int zr_binary_bwd_ex(zr_op op, zr_tensor grad_out, zr_tensor a, zr_tensor b, zr_grad grad_a,
+                     zr_grad grad_b, void* workspace, size_t* workspace_bytes,
+                     zr_stream_t stream) {
+  if (!workspace_bytes) return ZR_ERR_NULL;
+  BwdExSet E;
+  // Plan once to size the workspace; at run time plan again on it.
+  int rc = plan_bwd_ex(op, grad_out, a, b, grad_a, grad_b, nullptr, &E);
+  if (rc) return rc;
+  if (workspace == nullptr) {
+    *workspace_bytes = E.ws_query;
+    return ZR_OK;
+  }
+  if (E.S.nothing) return ZR_OK;
+  if (E.ws_run > 0) {
+    if (*workspace_bytes < E.ws_run) return ZR_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(workspace) % 16 != 0) return ZR_ERR_WORKSPACE;
+  }
+  BwdExSet R;
+  rc = plan_bwd_ex(op, grad_out, a, b, grad_a, grad_b, workspace, &R);
+  if (rc) return rc;
+  if (*workspace_bytes < R.ws_run) return ZR_ERR_WORKSPACE;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const BwdSet& S = R.S;
+  const bool ra = (grad_a.data && needs_a(op, 0)) || (grad_b.data && needs_a(op, 1));
+  const bool rb = (grad_a.data && needs_b(op, 0)) || (grad_b.data && needs_b(op, 1));
+  const void* ptrs[6] = {S.g.ptr,
+                         ra ? static_cast<const void*>(S.a.ptr) : nullptr,
+                         rb ? static_cast<const void*>(S.b.ptr) : nullptr,
+                         grad_a.data,
+                         grad_b.data,
+                         R.ws_run > 0 ? workspace : nullptr};
+  for (const void* p : ptrs) {
+    if (!p) continue;
+    rc = check_device_ptr(p);
+    if (rc) return rc;
+  }
+  if (S.empty) {
+    // Nothing to add: an accumulated gradient keeps its values; a written
+    // one becomes zero (staged: a zeroed staging buffer copied into place).
+    for (int w = 0; w < 2; ++w) {
+      if (!S.zero_ptr[w] || R.acc[w]) continue;
+      if (cudaMemsetAsync(S.zero_ptr[w], 0, S.zero_bytes[w], st) != cudaSuccess) return ZR_ERR_CUDA;
+      if (R.stage[w]) {
+        rc = cuda_status(launch_copy(R.copy[w], st));
+        if (rc) return rc;
+      }
+    }
+    return ZR_OK;
+  }
+  rc = launch_bwd_set(S, op, static_cast<char*>(workspace) + R.off_ws, st, false);
+  if (rc) return rc;
+  for (int w = 0; w < 2; ++w) {
+    if (!R.stage[w] || R.gd[w].numel == 0) continue;
+    rc = cuda_status(launch_copy(R.copy[w], st));
+    if (rc) return rc;
+  }
+  return ZR_OK;
+}
+
+}  // extern "C"

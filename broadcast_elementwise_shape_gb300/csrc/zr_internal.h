@@ -109,6 +109,7 @@ struct EwPlan {
   FastDiv tile_vcols_div;   // item -> (row in tile, column vector)
   uint32_t items_per_cta;   // tile_rows * tile_vcols
   uint32_t n_cta;
+  uint32_t acc_mask;        // bit k: out[k] += result (AccumulateGrad) instead of =
 };
 
 // Forward with one input read transposed: that input (X) walks the output's
@@ -228,6 +229,7 @@ struct RedPlan {
   // is a kept index, rank = row block * n_cblk + column block.
   uint32_t cluster;
   FastDiv cluster_div;
+  uint32_t acc_x, acc_d;    // X / the dense gradient: += result instead of =
 };
 
 struct RedCta {
@@ -354,6 +356,7 @@ struct CombinePlan {
   uint32_t nslots;
   uint32_t jx, sy;          // thread layout: jx outputs x sy slot lanes
   float scale;
+  uint32_t accumulate;      // outputs += result instead of =
 };
 
 }  // namespace zr

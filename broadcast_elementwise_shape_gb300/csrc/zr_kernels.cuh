@@ -160,6 +160,22 @@ __device__ __forceinline__ void store_cols(float* __restrict__ base, int64_t row
   }
 }
 
+// Store, or with acc add to what is there first (one binary32 addition per
+// element: AccumulateGrad's in-place sum, Autograd page, section 反向传播).
+template <int VEC>
+__device__ __forceinline__ void put_cols(float* __restrict__ base, int64_t row_off, int64_t inner,
+                                         uint32_t c, Vec<VEC> x, bool acc) {
+  if (acc) {
+    const Vec<VEC> old = load_cols<VEC>(base, row_off, inner, c, false);
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) x.v[i] = __fadd_rn(old.v[i], x.v[i]);
+  }
+  store_cols<VEC>(base, row_off, inner, c, x);
+}
+__device__ __forceinline__ void put1(float* p, float v, bool acc) {
+  *p = acc ? __fadd_rn(*p, v) : v;
+}
+
 // ---------------------------------------------------------------- functors
 
 // Forward: out = a op b.
@@ -280,8 +296,9 @@ k_elementwise(const __grid_constant__ EwPlan p) {
       if (!ok[u]) continue;
       Vec<VEC> y[2];
       f(x[u], y);
-      if (p.out[0]) store_cols<VEC>(p.out[0], doff[u], p.inner_stride[kSlotOut], col[u], y[0]);
-      if (NOUT > 1 && p.out[1]) store_cols<VEC>(p.out[1], doff[u], p.inner_stride[kSlotOut], col[u], y[1]);
+      if (p.out[0]) put_cols<VEC>(p.out[0], doff[u], p.inner_stride[kSlotOut], col[u], y[0], p.acc_mask & 1);
+      if (NOUT > 1 && p.out[1])
+        put_cols<VEC>(p.out[1], doff[u], p.inner_stride[kSlotOut], col[u], y[1], p.acc_mask & 2);
     }
   }
 }
@@ -585,7 +602,9 @@ k_reduce(const __grid_constant__ RedPlan p) {
           else acc[0].add_prod(gg, T::m(aa, bb));
           if (has_d) dv.v[i] = T::d(gg, aa, bb);
         }
-        if (has_d) store_cols<VEC>(p.d_out, s_off[ri[u] * kMaxOperands + kSlotOut], 1, cc[u], dv);
+        if (has_d)
+          put_cols<VEC>(p.d_out, s_off[ri[u] * kMaxOperands + kSlotOut], p.inner_stride[kSlotOut],
+                        cc[u], dv, p.acc_d);
       }
     }
   }
@@ -619,7 +638,7 @@ k_reduce(const __grid_constant__ RedPlan p) {
           float r = ld_cluster(s_red + v, 0);
           for (uint32_t k = 1; k < p.cluster; ++k) r = __fadd_rn(r, ld_cluster(s_red + v, k));
           if (T::kPost) r = __fmul_rn(r, T::post(__ldg(p.b + base[2] + int64_t(col) * p.inner_stride[2])));
-          p.x_final[uint64_t(cta.kidx) * p.ncol + col] = __fmul_rn(r, p.scale);
+          put1(p.x_final + uint64_t(cta.kidx) * p.ncol + col, __fmul_rn(r, p.scale), p.acc_x);
         }
       }
       cluster_sync();
@@ -636,15 +655,13 @@ k_reduce(const __grid_constant__ RedPlan p) {
 #pragma unroll
         for (int i = 0; i < VEC; ++i) r.v[i] = __fmul_rn(r.v[i], T::post(bv.v[i]));
       }
-      float* dst;
       if (p.nslots == 1) {
 #pragma unroll
         for (int i = 0; i < VEC; ++i) r.v[i] = __fmul_rn(r.v[i], p.scale);
-        dst = p.x_final + j;
+        put_cols<VEC>(p.x_final + j, 0, 1, 0, r, p.acc_x);
       } else {
-        dst = p.partial + uint64_t(cta.rblk) * p.nout + j;
+        store_cols<VEC>(p.partial + uint64_t(cta.rblk) * p.nout + j, 0, 1, 0, r);
       }
-      store_cols<VEC>(dst, 0, 1, 0, r);
     }
   } else {
     // Whole-CTA fixed tree: one value per kept index.
@@ -660,7 +677,7 @@ k_reduce(const __grid_constant__ RedPlan p) {
         float r = ld_cluster(s_red, 0);
         for (uint32_t k = 1; k < p.cluster; ++k) r = __fadd_rn(r, ld_cluster(s_red, k));
         if (T::kPost) r = __fmul_rn(r, T::post(__ldg(p.b + base[2])));
-        p.x_final[cta.kidx] = __fmul_rn(r, p.scale);
+        put1(p.x_final + cta.kidx, __fmul_rn(r, p.scale), p.acc_x);
       }
       cluster_sync();
       return;
@@ -669,7 +686,7 @@ k_reduce(const __grid_constant__ RedPlan p) {
       float r = s_red[0];
       if (T::kPost) r = __fmul_rn(r, T::post(__ldg(p.b + base[2])));
       if (p.nslots == 1) {
-        p.x_final[cta.kidx] = __fmul_rn(r, p.scale);
+        put1(p.x_final + cta.kidx, __fmul_rn(r, p.scale), p.acc_x);
       } else {
         const uint64_t slot = uint64_t(cta.rblk) * p.n_cblk + cta.cblk;
         p.partial[slot * p.nout + cta.kidx] = r;
@@ -714,8 +731,7 @@ k_combine(const __grid_constant__ CombinePlan p) {
   __syncthreads();
   if (sl == 0 && j < p.nout) {
     const float v = __fmul_rn(s_red[jl], p.scale);
-    if (j < p.split) p.out[j] = v;
-    else p.out2[j - p.split] = v;
+    put1(j < p.split ? p.out + j : p.out2 + (j - p.split), v, p.accumulate);
   }
 }
 

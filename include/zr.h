@@ -200,6 +200,39 @@ int zr_sum_to_shape(zr_tensor in, int32_t ndim_out, const int64_t* sizes_out,
                     zr_stream_t stream);
 
 /*
+ * Where and how zr_binary_bwd_ex writes one gradient.
+ *   data        NULL: the gradient is not computed.
+ *   strides     element strides over the input's shape (any non-negative
+ *               layout that does not overlap itself); NULL: dense row-major.
+ *   accumulate  nonzero: add the new gradient to the values already there,
+ *               one binary32 addition per element (AccumulateGrad, Autograd
+ *               page, section 反向传播: a gradient slot that already holds a
+ *               value is summed in place, so a tensor reached by several
+ *               paths gets the sum of their gradients).
+ */
+typedef struct {
+  float* data;
+  const int64_t* strides;
+  int32_t accumulate;
+} zr_grad;
+
+/*
+ * zr_binary_bwd_ex — zr_binary_bwd with a layout and a write mode per
+ * gradient (zr_grad).  Results, numerics and the workspace protocol are
+ * those of zr_binary_bwd; with accumulate, each element becomes
+ * old + (the value zr_binary_bwd would write), rounded once.  Dense
+ * gradients are written (or added to) by the backward's own kernels; a
+ * strided gradient is formed densely in the workspace and copied (or added)
+ * into its layout by one more pass, so the workspace query includes numel
+ * floats for it.  Layout errors (ZR_ERR_LAYOUT): a gradient that overlaps
+ * itself, the other gradient or any input.  When grad_out is empty, written
+ * gradients become zero and accumulated ones keep their values.
+ */
+int zr_binary_bwd_ex(zr_op op, zr_tensor grad_out, zr_tensor a, zr_tensor b, zr_grad grad_a,
+                     zr_grad grad_b, void* workspace, size_t* workspace_bytes,
+                     zr_stream_t stream);
+
+/*
  * zr_chain_fwd — out = (a op1 b) op2 c, all three operands broadcast to one
  * output shape (broadcast(broadcast(a, b), c)).  The fused form of two of the
  * operators above in sequence: Operator page, section 融合 (fusion) — one

@@ -270,3 +270,13 @@ def chain_bwd_at(op1, op2, which, g, a, b, c, idx):
         return binary_bwd_at(op2, 1, g, t, c, idx)
     gt, _, _, _ = binary_bwd(op2, g, t, c, want_b=False)
     return binary_bwd_at(op1, which, gt, a, b, idx)
+
+
+# ---------------------------------------------------------------- accumulation
+
+def accumulate(old, new):
+    """AccumulateGrad (Autograd page, section 反向传播): a gradient slot that
+    already holds a value gets the new gradient added in place — one binary32
+    addition per element, so a tensor reached by several paths receives the
+    sum of their gradients."""
+    return (np.asarray(old, dtype=np.float32) + np.asarray(new, dtype=np.float32)).astype(np.float32)

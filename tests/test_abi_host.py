@@ -547,3 +547,33 @@ def test_chain_errors_before_any_device_access(L):
     assert L.zr_chain_bwd(0, 0, g.desc, an, bn, cn, 8 * T, 6 * T, 7 * T, None,
                           ctypes.byref(nbytes), None) == 0
     assert nbytes.value >= 4 * 32  # grad_t in the workspace
+
+
+def test_backward_ex_layout_errors_and_query(L):
+    """zr_binary_bwd_ex: gradients that overlap themselves or an input are
+    refused before any device access; a strided gradient adds its staging
+    buffer to the workspace query."""
+    from broadcast_elementwise_shape_gb300 import ZrGrad
+    T = 1 << 40
+    g, x, bias = FakeT(T, (64, 256)), FakeT(2 * T, (64, 256)), FakeT(3 * T, (256,))
+    nb = ctypes.c_size_t(0)
+    dense = ZrGrad(4 * T, None, 0)
+    assert L.zr_binary_bwd_ex(0, g.desc, x.desc, bias.desc, dense, ZrGrad(5 * T, None, 1), None,
+                              ctypes.byref(nb), None) == 0
+    q_dense = nb.value
+    # grad_a as a transposed view of a [256, 64] buffer: staged.
+    st = _i64([1, 64])
+    assert L.zr_binary_bwd_ex(0, g.desc, x.desc, bias.desc, ZrGrad(4 * T, st, 1),
+                              ZrGrad(5 * T, None, 0), None, ctypes.byref(nb), None) == 0
+    assert nb.value >= q_dense + 4 * 64 * 256
+    # A gradient layout that overlaps itself.
+    bad = _i64([0, 1])
+    assert L.zr_binary_bwd_ex(0, g.desc, x.desc, bias.desc, ZrGrad(4 * T, bad, 0), dense, None,
+                              ctypes.byref(nb), None) == -5
+    # A strided gradient overlapping grad_out.
+    assert L.zr_binary_bwd_ex(0, g.desc, x.desc, bias.desc, ZrGrad(T + 4, st, 0),
+                              ZrGrad(5 * T, None, 0), None, ctypes.byref(nb), None) == -5
+    # Negative strides are refused like any tensor's.
+    neg = _i64([-1, 64])
+    assert L.zr_binary_bwd_ex(0, g.desc, x.desc, bias.desc, ZrGrad(4 * T, neg, 0), dense, None,
+                              ctypes.byref(nb), None) == -4

@@ -488,3 +488,36 @@ def test_chain_gather_form_matches_full():
                 vals, sabs = oracle.chain_bwd_at(op1, op2, which, g, a, b, c, idx)
                 assert np.array_equal(vals.view(np.uint32), full[which].ravel().view(np.uint32))
                 np.testing.assert_allclose(sabs, full[3 + which].ravel(), rtol=1e-12)
+
+
+def test_accumulate_worked_gradient_example():
+    """x reaches z = x*y + x along two paths; the book adds their gradients
+    into x's slot: 2 (through Mul) + 1 (through Add) = dz/dx = 3."""
+    kv = {}
+    for ln in _golden_lines("worked_gradient.txt"):
+        k, v = (p.strip() for p in ln.split("="))
+        kv[k] = float(v)
+    x = np.array([kv["x"]], np.float32)
+    y = np.array([kv["y"]], np.float32)
+    xy = oracle.binary_fwd("mul", x, y)
+    one = np.ones(1, np.float32)
+    g_xy, g_x_add, _, _ = oracle.binary_bwd("add", one, xy, x)
+    g_x_mul, _, _, _ = oracle.binary_bwd("mul", g_xy, x, y)
+    slot = np.zeros(1, np.float32)
+    slot = oracle.accumulate(slot, g_x_mul)
+    slot = oracle.accumulate(slot, g_x_add)
+    assert slot[0] == kv["dz_dx"]
+
+
+def test_accumulate_is_one_rounded_addition():
+    """Each element is old + new rounded once: by Figueroa's double-rounding
+    result a binary64 sum of two binary32 values rounded to binary32 is that
+    value; the sign rules of zero follow IEEE (+0 + -0 = +0)."""
+    rng = np.random.default_rng(21)
+    old = (rng.standard_normal(5000) * 10.0 ** rng.integers(-30, 30, 5000)).astype(np.float32)
+    new = (rng.standard_normal(5000) * 10.0 ** rng.integers(-30, 30, 5000)).astype(np.float32)
+    got = oracle.accumulate(old, new)
+    want = (old.astype(np.float64) + new.astype(np.float64)).astype(np.float32)
+    assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+    z = oracle.accumulate(np.array([0.0, -0.0, -0.0], np.float32), np.array([-0.0, 0.0, -0.0], np.float32))
+    assert list(np.signbit(z)) == [False, False, True]
