@@ -74,6 +74,10 @@ def _load():
             _lib.orc_binary_bwd_at.argtypes = [ci, ci] + ten + ten + ten + [ctypes.c_int64, i64p, vp, vp]
             _lib.orc_sum_to_shape.argtypes = ten + [ci, i64p, vp, vp]
             _lib.orc_sum_to_shape_at.argtypes = ten + [ci, i64p, ctypes.c_int64, i64p, vp, vp]
+            _lib.orc_unary_fwd.argtypes = [ci, ctypes.c_float] + ten + [vp]
+            _lib.orc_unary_bwd.argtypes = [ci, ctypes.c_float] + ten + [vp, i64p, vp, vp]
+            for f in ("orc_unary_fwd", "orc_unary_bwd"):
+                getattr(_lib, f).restype = ci
             for f in ("orc_contiguous_strides", "orc_broadcast_shape", "orc_binary_fwd",
                       "orc_binary_fwd_at", "orc_binary_bwd", "orc_binary_bwd_at",
                       "orc_sum_to_shape", "orc_sum_to_shape_at"):
@@ -280,3 +284,39 @@ def accumulate(old, new):
     addition per element, so a tensor reached by several paths receives the
     sum of their gradients."""
     return (np.asarray(old, dtype=np.float32) + np.asarray(new, dtype=np.float32)).astype(np.float32)
+
+
+
+# ---------------------------------------------------------------- unary ops
+#
+# GPU page, section 逐元素运算: GeLU and gradient scaling are elementwise.
+# scale: alpha * x (one binary32 multiply); GeLU: the exact x * Phi(x) (the
+# pages give no formula), evaluated in binary64 and rounded once.
+
+UNARY = {"scale": 0, "gelu": 1}
+
+
+def unary_fwd(op, x, alpha=1.0):
+    """out = op(x), dense float32 of x's shape."""
+    lib = _load()
+    tx = _T(x)
+    out = np.empty(tx.sizes, dtype=np.float32)
+    _check(lib.orc_unary_fwd(UNARY.get(op, op), alpha, *tx.args(), out.ctypes.data if out.size else None),
+           "unary_fwd")
+    return out
+
+
+def unary_bwd(op, g, x, alpha=1.0):
+    """(grad_x, mag): grad_x = g * op'(x) dense float32; mag the size of the
+    terms before rounding (|g| (Phi(x) + |x| phi(x)) for GeLU, float64)."""
+    lib = _load()
+    tg = _T(g)
+    tx = _T(x) if x is not None else _T(None, tg.sizes)
+    if tx.sizes != tg.sizes:
+        raise OracleError("unary_bwd: g and x differ in shape")
+    out = np.empty(tg.sizes, dtype=np.float32)
+    mag = np.empty(tg.sizes, dtype=np.float64)
+    _check(lib.orc_unary_bwd(UNARY.get(op, op), alpha, *tg.args(), tx.ptr, tx._st,
+                             out.ctypes.data if out.size else None,
+                             mag.ctypes.data if mag.size else None), "unary_bwd")
+    return out, mag

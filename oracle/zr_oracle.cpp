@@ -507,3 +507,91 @@ int orc_sum_to_shape_at(const float* x, int ndx, const int64_t* szx, const int64
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------- unary ops
+//
+// GPU page, section 逐元素运算 (elementwise ops): add, mul, GeLU and
+// gradient scaling each compute an output element from the input element at
+// the same position.  The pages name GeLU without a formula; the plainest
+// reading is its exact definition GeLU(x) = x * Phi(x), Phi the standard
+// normal CDF, written Phi(x) = erfc(-x / sqrt(2)) / 2.  Evaluated in binary64
+// and rounded once.  Backward: d/dx GeLU = Phi(x) + x * phi(x) with
+// phi(x) = exp(-x^2 / 2) / sqrt(2 pi).  scale: out = alpha * x, one binary32
+// multiply; its backward alpha * g.  Outputs are dense row-major of x's shape.
+namespace {
+enum Unary { UN_SCALE = 0, UN_GELU = 1 };
+
+double norm_cdf(double x) { return 0.5 * std::erfc(-x / std::sqrt(2.0)); }
+double norm_pdf(double x) { return std::exp(-0.5 * x * x) / std::sqrt(2.0 * 3.14159265358979323846); }
+
+// Visit every element of a strided view in row-major coordinate order.
+template <class F>
+void for_each_elem(const View& v, F f) {
+  const int64_t n = numel(v.sizes);
+  std::vector<int64_t> c(v.ndim, 0);
+  for (int64_t i = 0; i < n; ++i) {
+    int64_t off = 0;
+    for (int d = 0; d < v.ndim; ++d) off += c[d] * v.strides[d];
+    f(i, off);
+    for (int d = v.ndim - 1; d >= 0; --d) {
+      if (++c[d] < v.sizes[d]) break;
+      c[d] = 0;
+    }
+  }
+}
+}  // namespace
+
+extern "C" {
+
+int orc_unary_fwd(int op, float alpha, const float* x, int ndx, const int64_t* szx,
+                  const int64_t* stx, float* out) {
+  if (op != UN_SCALE && op != UN_GELU) return -1;
+  View vx;
+  int rc = make_view(x, ndx, szx, stx, &vx);
+  if (rc) return rc;
+  if (numel(vx.sizes) > 0 && (!x || !out)) return -1;
+  for_each_elem(vx, [&](int64_t i, int64_t off) {
+    const float xv = x[off];
+    if (op == UN_SCALE) {
+      out[i] = alpha * xv;
+    } else {
+      const double xd = xv;
+      out[i] = static_cast<float>(xd * norm_cdf(xd));
+    }
+  });
+  return 0;
+}
+
+// grad_x[i] = g[i] * f'(x[i]); mag[i] = |g| * (Phi(x) + |x| phi(x)) for GeLU
+// (the size of the two terms before they cancel near the minimum at
+// x = -0.75), |alpha * g| for scale.
+int orc_unary_bwd(int op, float alpha, const float* g, int ndg, const int64_t* szg,
+                  const int64_t* stg, const float* x, const int64_t* stx, float* grad_x,
+                  double* mag) {
+  if (op != UN_SCALE && op != UN_GELU) return -1;
+  View vg, vx;
+  int rc = make_view(g, ndg, szg, stg, &vg);
+  if (rc) return rc;
+  rc = make_view(x, ndg, szg, stx, &vx);
+  if (rc) return rc;
+  const int64_t n = numel(vg.sizes);
+  if (n > 0 && (!g || !grad_x || (op == UN_GELU && !x))) return -1;
+  std::vector<int64_t> goff(n), xoff(n);
+  for_each_elem(vg, [&](int64_t i, int64_t off) { goff[i] = off; });
+  for_each_elem(vx, [&](int64_t i, int64_t off) { xoff[i] = off; });
+  for (int64_t i = 0; i < n; ++i) {
+    const float gv = g[goff[i]];
+    if (op == UN_SCALE) {
+      grad_x[i] = alpha * gv;
+      if (mag) mag[i] = std::fabs(static_cast<double>(alpha) * gv);
+    } else {
+      const double xd = x[xoff[i]];
+      const double cdf = norm_cdf(xd), pdf = norm_pdf(xd);
+      grad_x[i] = static_cast<float>(static_cast<double>(gv) * (cdf + xd * pdf));
+      if (mag) mag[i] = std::fabs(static_cast<double>(gv)) * (cdf + std::fabs(xd) * pdf);
+    }
+  }
+  return 0;
+}
+
+}  // extern "C"

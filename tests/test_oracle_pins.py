@@ -521,3 +521,59 @@ def test_accumulate_is_one_rounded_addition():
     assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
     z = oracle.accumulate(np.array([0.0, -0.0, -0.0], np.float32), np.array([-0.0, 0.0, -0.0], np.float32))
     assert list(np.signbit(z)) == [False, False, True]
+
+
+# ---------------------------------------------------------------- unary ops
+
+def test_unary_scale_is_one_float32_multiply():
+    rng = np.random.default_rng(31)
+    base = torch.from_numpy(rng.standard_normal((40, 30)).astype(np.float32))
+    x = base.t()  # strided view
+    for alpha in (0.125, -3.0, 1e-30, 7.5):
+        got = oracle.unary_fwd("scale", x, alpha=alpha)
+        want = (np.float32(alpha) * x.numpy()).astype(np.float32)
+        assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+        g = rng.standard_normal((30, 40)).astype(np.float32)
+        gx, mag = oracle.unary_bwd("scale", g, None, alpha=alpha)
+        assert np.array_equal(gx.view(np.uint32), (np.float32(alpha) * g).astype(np.float32).view(np.uint32))
+
+
+def test_gelu_printed_normal_cdf_values():
+    for ln in _golden_lines("normal_cdf.txt"):
+        xs, ps = (p.strip() for p in ln.split(";"))
+        x, phi = float(xs), float(ps)
+        got = float(oracle.unary_fwd("gelu", np.array([x], np.float32))[0])
+        assert abs(got - x * phi) <= 2.0 ** -24 * abs(x * phi) + 1e-10, (x, got, x * phi)
+    # GeLU'(0) = Phi(0) = 1/2 exactly.
+    gx, _ = oracle.unary_bwd("gelu", np.ones(1, np.float32), np.zeros(1, np.float32))
+    assert gx[0] == 0.5
+
+
+def test_gelu_odd_identity_and_erf_form():
+    """x Phi(x) - (-x) Phi(-x) = x; and the erf form 0.5 x (1 + erf(x/sqrt 2))
+    (a different library function) agrees where it does not cancel."""
+    rng = np.random.default_rng(32)
+    x = (rng.standard_normal(4000) * 3).astype(np.float32)
+    p, m = oracle.unary_fwd("gelu", x), oracle.unary_fwd("gelu", -x)
+    err = np.abs((p.astype(np.float64) - m.astype(np.float64)) - x.astype(np.float64))
+    assert np.all(err <= 2.0 ** -23 * (np.abs(p) + np.abs(m)) + 1e-30)
+    xs = x[np.abs(x) <= 3.0]
+    ref = np.array([0.5 * float(v) * (1.0 + math.erf(float(v) / math.sqrt(2.0))) for v in xs])
+    got = oracle.unary_fwd("gelu", xs).astype(np.float64)
+    assert np.all(np.abs(got - ref) <= 2.0 ** -23 * np.abs(ref) + 1e-12)
+
+
+def test_gelu_backward_matches_finite_differences():
+    rng = np.random.default_rng(33)
+    x = (rng.standard_normal(300) * 2).astype(np.float32)
+    g = rng.standard_normal(300).astype(np.float32)
+    gx, mag = oracle.unary_bwd("gelu", g, x)
+
+    def f(v):
+        return 0.5 * v * (1.0 + math.erf(v / math.sqrt(2.0)))
+    for i in range(x.size):
+        v = float(x[i])
+        h = 1e-6 * max(1.0, abs(v))
+        fd = float(g[i]) * (f(v + h) - f(v - h)) / (2 * h)
+        assert abs(float(gx[i]) - fd) <= 1e-6 * float(mag[i]) + 1e-7, (v, gx[i], fd)
+        assert abs(float(gx[i])) <= float(mag[i]) * (1 + 1e-6)
