@@ -116,6 +116,12 @@ def chain_reads(op1, op2):
 
 def op_bytes(step, shapes):
     """Algorithmic bytes of one op: read each input once, write each output once."""
+    if step[0] == "ufwd":
+        _, op, alpha, xn, on = step
+        return 4 * (shapes[xn] + shapes[on])
+    if step[0] == "ubwd":
+        _, op, alpha, gn, xn, gxn = step
+        return 4 * (shapes[gn] + (shapes[xn] if op == "gelu" else 0) + shapes[gxn])
     if step[0] == "cfwd":
         _, op1, op2, an, bn, cn, on = step
         return 4 * (shapes[an] + shapes[bn] + shapes[cn] + shapes[on])
@@ -147,7 +153,10 @@ def shape_table(name, host):
     shapes = {k: tuple(v.shape) for k, v in host.items()}
     import numpy as np
     for step in workloads.STEPS[name]:
-        if step[0] == "cfwd":
+        if step[0] in ("ufwd", "ubwd"):
+            src, dst = step[-2], step[-1]
+            shapes[dst], sizes[dst] = shapes[src], sizes[src]
+        elif step[0] == "cfwd":
             _, op1, op2, an, bn, cn, on = step
             shapes[on] = tuple(np.broadcast_shapes(shapes[an], shapes[bn], shapes[cn]))
             sizes[on] = numel(shapes[on])
@@ -255,7 +264,7 @@ class Suite:
                 env[k] = self._to_dev(v)
             outs = []
             for step in workloads.STEPS[name]:
-                if step[0] in ("fwd", "cfwd"):
+                if step[0] in ("fwd", "cfwd", "ufwd", "ubwd"):
                     on = step[-1]
                     env[on] = torch.empty(shapes[on], dtype=torch.float32, device=device)
                     outs.append(on)
@@ -326,11 +335,37 @@ class Suite:
         return (name, "bwd", f"{step[1]}+{step[2]} ({desc['route']})", nbytes, launches, fn,
                 sizes[gn])
 
+    def _prepare_unary(self, name, step, env, sizes, stream_of):
+        zr, L = self.zr, self.L
+        nbytes = op_bytes(step, sizes)
+        uop, alpha = zr.UNARY[step[1]], float(step[2])
+        out = env[step[-1]]
+        ost = zr._i64(out.stride())
+        self._keep.append(ost)
+        ptr = out.data_ptr()
+        if step[0] == "ufwd":
+            dx = self._desc(env[step[3]])
+
+            def fn(dx=dx, ptr=ptr, ost=ost):
+                rc = L.zr_unary_fwd(uop, alpha, dx, ptr, ost, stream_of())
+                if rc:
+                    raise zr.ZrError(rc, f"{name} unary fwd")
+            return (name, "fwd", step[1], nbytes, 1, fn, sizes[step[-1]])
+        dg, dx = self._desc(env[step[3]]), self._desc(env[step[4]])
+
+        def fn(dg=dg, dx=dx, ptr=ptr, ost=ost):
+            rc = L.zr_unary_bwd(uop, alpha, dg, dx, ptr, ost, stream_of())
+            if rc:
+                raise zr.ZrError(rc, f"{name} unary bwd")
+        return (name, "bwd", step[1], nbytes, 1, fn, sizes[step[-1]])
+
     def _prepare(self, name, step, env, sizes):
         zr, L, torch = self.zr, self.L, self.torch
         stream_of = lambda: ctypes.c_void_p(torch.cuda.current_stream(self.device).cuda_stream)
         if step[0] in ("cfwd", "cbwd"):
             return self._prepare_chain(name, step, env, sizes, stream_of)
+        if step[0] in ("ufwd", "ubwd"):
+            return self._prepare_unary(name, step, env, sizes, stream_of)
         opc = zr.OPS[step[1]]
         nbytes = op_bytes(step, sizes)
         if step[0] == "fwd":
@@ -488,7 +523,7 @@ def run_zr(args, rank, world, local):
 
     per_config = per_op_alone = None
     if rank == 0 and args.config_reps > 0:
-        extra = [Suite(["x1", "c3f", "c4f"], device)] if args.workload == "suite" else []
+        extra = [Suite(["x1", "c3f", "c4f", "u1"], device)] if args.workload == "suite" else []
         per_config, per_op_alone = run_per_config([suite] + extra, flush, stream, args.config_reps)
     e2e = None
     if not args.no_e2e and rank == 0:

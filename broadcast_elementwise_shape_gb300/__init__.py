@@ -68,12 +68,14 @@ def lib() -> ctypes.CDLL:
         L.zr_binary_bwd_ex.argtypes = [c_int, ZrTensor, ZrTensor, ZrTensor, ZrGrad, ZrGrad, vp, szp,
                                        vp]
         L.zr_chain_fwd.argtypes = [c_int, c_int, ZrTensor, ZrTensor, ZrTensor, vp, i64p, vp]
+        L.zr_unary_fwd.argtypes = [c_int, ctypes.c_float, ZrTensor, vp, i64p, vp]
+        L.zr_unary_bwd.argtypes = [c_int, ctypes.c_float, ZrTensor, ZrTensor, vp, i64p, vp]
         L.zr_chain_bwd.argtypes = [c_int, c_int, ZrTensor, ZrTensor, ZrTensor, ZrTensor, vp, vp, vp,
                                    vp, szp, vp]
         L.zr_status_string.argtypes = [c_int]
         L.zr_status_string.restype = ctypes.c_char_p
         for f in ("zr_broadcast_shape", "zr_binary_fwd", "zr_binary_bwd", "zr_sum_to_shape",
-                  "zr_chain_fwd", "zr_chain_bwd", "zr_binary_bwd_ex"):
+                  "zr_chain_fwd", "zr_chain_bwd", "zr_binary_bwd_ex", "zr_unary_fwd", "zr_unary_bwd"):
             getattr(L, f).restype = c_int
         _lib = L
     return _lib
@@ -278,3 +280,34 @@ def zr_binary_bwd_ex(op, grad_out, a, b, grad_a=None, grad_b=None, accumulate=(F
                             ctypes.byref(nbytes), _stream(grad_out))
     _check(rc, "zr_binary_bwd_ex")
     return grad_a, grad_b
+
+
+UNARY = {"scale": 0, "gelu": 1}
+
+
+def zr_unary_fwd(op, x, alpha=1.0, out=None):
+    """out = op(x) for op in ("scale", "gelu"); ``out`` may be a preallocated
+    (strided) tensor of x's shape, or x itself."""
+    import torch
+    if out is None:
+        out = torch.empty(x.shape, dtype=torch.float32, device=x.device)
+    dx, kx = _desc(x)
+    ost = _i64(out.stride())
+    rc = lib().zr_unary_fwd(UNARY.get(op, op), float(alpha), dx, out.data_ptr() if out.numel() else None,
+                            ost, _stream(out))
+    _check(rc, "zr_unary_fwd")
+    return out
+
+
+def zr_unary_bwd(op, grad_out, x, alpha=1.0, grad_x=None):
+    """grad_x = grad_out * op'(x); ``x`` may be None for "scale"."""
+    import torch
+    if grad_x is None:
+        grad_x = torch.empty(grad_out.shape, dtype=torch.float32, device=grad_out.device)
+    dg, kg = _desc(grad_out)
+    dx, kx = _desc(x, tuple(grad_out.shape))
+    gst = _i64(grad_x.stride())
+    rc = lib().zr_unary_bwd(UNARY.get(op, op), float(alpha), dg, dx,
+                            grad_x.data_ptr() if grad_x.numel() else None, gst, _stream(grad_out))
+    _check(rc, "zr_unary_bwd")
+    return grad_x

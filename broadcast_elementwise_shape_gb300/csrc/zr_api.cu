@@ -692,6 +692,7 @@ int zr_test_occupancy(int which, int* planned, int* actual) {
   else if (which >= 9 && which < 11) e = occupancy_other(which - 9, planned, actual);
   else if (which >= 11 && which < 16) e = occupancy_red(which - 6, planned, actual);
   else if (which >= 16 && which < 20) e = occupancy_chain(which - 16, planned, actual);
+  else if (which >= 20 && which < 22) e = occupancy_ew(which - 16, planned, actual);
   else return ZR_ERR_SIZE;
   return cuda_status(e);
 }
@@ -1585,6 +1586,110 @@ int zr_binary_bwd_ex(zr_op op, zr_tensor grad_out, zr_tensor a, zr_tensor b, zr_
     if (rc) return rc;
   }
   return ZR_OK;
+}
+
+}  // extern "C"
+
+// ------------------------------------------------------------------ unary ops
+//
+// GPU page, section 逐元素运算: GeLU and gradient scaling are elementwise
+// (each output element from the input element at the same position).  One
+// elementwise pass over x's (or grad_out's) layout; any strides, in place
+// allowed with the same layout.
+
+namespace zr {
+namespace {
+
+struct UnarySet {
+  bool empty = false;
+  EwBuild eb;
+  TDesc x, g, out;
+};
+
+// in0: x (forward) or grad_out (backward); in1: x for GeLU's backward.
+int plan_unary(int uop, float alpha, const zr_tensor& t0, const zr_tensor* t1, float* out,
+               const int64_t* out_strides, UnarySet* S) {
+  if (uop != UN_SCALE && uop != UN_GELU) return ZR_ERR_NULL;
+  int rc = read_tensor(t0, &S->g);
+  if (rc) return rc;
+  const bool two = t1 != nullptr;
+  if (two) {
+    rc = read_tensor(*t1, &S->x);
+    if (rc) return rc;
+    if (S->x.nd != S->g.nd) return ZR_ERR_SHAPE;
+    for (int d = 0; d < S->g.nd; ++d)
+      if (S->x.size[d] != S->g.size[d]) return ZR_ERR_SHAPE;
+  }
+  const int n = S->g.nd;
+  zr_tensor to{out, n, S->g.size, out_strides};
+  rc = read_tensor(to, &S->out);
+  if (rc) return rc;
+  if (S->out.numel == 0) {
+    S->empty = true;
+    return ZR_OK;
+  }
+  if (!S->g.ptr || !out || (two && !S->x.ptr)) return ZR_ERR_NULL;
+  if (!non_overlapping(S->out)) return ZR_ERR_LAYOUT;
+  const Span so = span_of(out, S->out.extent);
+  if (overlaps(so, span_of(S->g.ptr, S->g.extent)) && !same_layout(S->g, S->out)) return ZR_ERR_LAYOUT;
+  if (two && overlaps(so, span_of(S->x.ptr, S->x.extent)) && !same_layout(S->x, S->out))
+    return ZR_ERR_LAYOUT;
+  int64_t st[kProbSlots][kMaxDims] = {};
+  for (int d = 0; d < n; ++d) {
+    const bool one = S->g.size[d] == 1;
+    st[0][d] = one ? 0 : S->g.stride[d];
+    st[1][d] = (one || !two) ? 0 : S->x.stride[d];
+    st[kSlotOut][d] = one ? 0 : S->out.stride[d];
+  }
+  Prob P;
+  const uint32_t rmask = two ? 3u : 1u;
+  rc = coalesce(n, S->g.size, st, rmask | (1u << kSlotOut), kSlotOut, &P);
+  if (rc) return rc;
+  const float* in[3] = {S->g.ptr, two ? S->x.ptr : nullptr, nullptr};
+  float* outs[2] = {out, nullptr};
+  rc = build_ew(P, in, outs, rmask, rmask, kOccEwFwd, &S->eb);
+  if (rc) return rc;
+  S->eb.plan.alpha = alpha;
+  return ZR_OK;
+}
+
+}  // namespace
+}  // namespace zr
+
+extern "C" {
+
+int zr_unary_fwd(zr_unary op, float alpha, zr_tensor x, float* out, const int64_t* out_strides,
+                 zr_stream_t stream) {
+  UnarySet S;
+  int rc = plan_unary(op, alpha, x, nullptr, out, out_strides, &S);
+  if (rc || S.empty) return rc;
+  for (const void* p : {static_cast<const void*>(S.g.ptr), static_cast<const void*>(out)}) {
+    rc = check_device_ptr(p);
+    if (rc) return rc;
+  }
+  return cuda_status(launch_unary_fwd(op, S.eb, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int zr_unary_bwd(zr_unary op, float alpha, zr_tensor grad_out, zr_tensor x, float* grad_x,
+                 const int64_t* grad_x_strides, zr_stream_t stream) {
+  UnarySet S;
+  // scale's backward does not read x (its sizes must still match grad_out).
+  int rc = plan_unary(op, alpha, grad_out, op == UN_GELU ? &x : nullptr, grad_x, grad_x_strides,
+                      &S);
+  if (rc || S.empty) return rc;
+  if (op != UN_GELU) {
+    if (x.ndim != grad_out.ndim || (x.ndim > 0 && !x.sizes)) return ZR_ERR_SHAPE;
+    for (int d = 0; d < x.ndim; ++d)
+      if (x.sizes[d] != S.g.size[d]) return ZR_ERR_SHAPE;
+  }
+  for (const void* p : {static_cast<const void*>(S.g.ptr),
+                        op == UN_GELU ? static_cast<const void*>(S.x.ptr) : nullptr,
+                        static_cast<const void*>(grad_x)}) {
+    if (!p) continue;
+    rc = check_device_ptr(p);
+    if (rc) return rc;
+  }
+  return cuda_status(launch_unary_bwd(op, S.eb, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

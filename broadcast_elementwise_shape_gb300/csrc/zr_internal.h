@@ -28,6 +28,7 @@ constexpr int kMaxOperands = 4;
 constexpr int kSlotOut = 3;
 
 enum OpCode : int32_t { OP_ADD = 0, OP_SUB = 1, OP_MUL = 2, OP_DIV = 3 };
+enum UnaryCode : int32_t { UN_SCALE = 0, UN_GELU = 1 };
 
 // ---------------------------------------------------------------------------
 // Division by an invariant unsigned 32-bit integer with one multiply-high,
@@ -110,6 +111,7 @@ struct EwPlan {
   uint32_t items_per_cta;   // tile_rows * tile_vcols
   uint32_t n_cta;
   uint32_t acc_mask;        // bit k: out[k] += result (AccumulateGrad) instead of =
+  float alpha;              // the unary ops' scalar (scale's factor)
 };
 
 // Forward with one input read transposed: that input (X) walks the output's

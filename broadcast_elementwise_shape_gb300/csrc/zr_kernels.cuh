@@ -184,7 +184,7 @@ struct FwdF {
   static constexpr bool kR1 = true, kR2 = false;  // slot 0 = a, slot 1 = b
   static constexpr int kMinBlocks = kOccEwFwd;  // CTAs per SM the register budget targets
   template <int VEC>
-  __device__ __forceinline__ void operator()(const Vec<VEC> (&x)[3], Vec<VEC> (&y)[2]) const {
+  __device__ __forceinline__ void operator()(const Vec<VEC> (&x)[3], Vec<VEC> (&y)[2], float) const {
 #pragma unroll
     for (int i = 0; i < VEC; ++i) y[0].v[i] = fwd_op<OP>(x[0].v[i], x[1].v[i]);
   }
@@ -198,7 +198,7 @@ struct BwdDirectF {
   static constexpr bool kR2 = ((WANT & 1) && Needs<OP, 0>::b) || ((WANT & 2) && Needs<OP, 1>::b);
   static constexpr int kMinBlocks = kOccEwBwd;
   template <int VEC>
-  __device__ __forceinline__ void operator()(const Vec<VEC> (&x)[3], Vec<VEC> (&y)[2]) const {
+  __device__ __forceinline__ void operator()(const Vec<VEC> (&x)[3], Vec<VEC> (&y)[2], float) const {
 #pragma unroll
     for (int i = 0; i < VEC; ++i) {
       if (WANT & 1) y[0].v[i] = term_a<OP>(x[0].v[i], x[1].v[i], x[2].v[i]);
@@ -217,9 +217,52 @@ struct ChainF {
   static constexpr bool kUniform2 = C_ONE;
   static constexpr int kMinBlocks = C_ONE ? kOccEwFwd : kOccEwBwd;
   template <int VEC>
-  __device__ __forceinline__ void operator()(const Vec<VEC> (&x)[3], Vec<VEC> (&y)[2]) const {
+  __device__ __forceinline__ void operator()(const Vec<VEC> (&x)[3], Vec<VEC> (&y)[2], float) const {
 #pragma unroll
     for (int i = 0; i < VEC; ++i) y[0].v[i] = fwd_op<OP2>(fwd_op<OP1>(x[0].v[i], x[1].v[i]), x[2].v[i]);
+  }
+};
+
+// Unary elementwise ops (GPU page, section 逐元素运算: GeLU and gradient
+// scaling compute each output element from the input element at the same
+// position).  scale: alpha * x, one IEEE binary32 multiply.  GeLU: the exact
+// x * Phi(x), Phi(x) = erfc(-x / sqrt(2)) / 2 (erfc avoids the cancellation of
+// 1 + erf for negative x); its derivative Phi(x) + x * phi(x),
+// phi(x) = exp(-x^2 / 2) / sqrt(2 pi).  Slot 0: x (forward) or grad_out
+// (backward); slot 1: x (GeLU backward).
+__device__ __forceinline__ float gelu_cdf(float x) {
+  return __fmul_rn(0.5f, erfcf(__fmul_rn(-x, 0.70710678118654752f)));
+}
+template <int UOP>
+struct UnaryF {
+  static constexpr bool kR1 = false, kR2 = false;
+  static constexpr int kMinBlocks = kOccEwFwd;
+  template <int VEC>
+  __device__ __forceinline__ void operator()(const Vec<VEC> (&x)[3], Vec<VEC> (&y)[2], float alpha) const {
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) {
+      const float v = x[0].v[i];
+      y[0].v[i] = UOP == UN_SCALE ? __fmul_rn(alpha, v) : __fmul_rn(v, gelu_cdf(v));
+    }
+  }
+};
+template <int UOP>
+struct UnaryBwdF {
+  static constexpr bool kR1 = UOP == UN_GELU, kR2 = false;
+  static constexpr int kMinBlocks = kOccEwFwd;
+  template <int VEC>
+  __device__ __forceinline__ void operator()(const Vec<VEC> (&x)[3], Vec<VEC> (&y)[2], float alpha) const {
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) {
+      const float g = x[0].v[i];
+      if (UOP == UN_SCALE) {
+        y[0].v[i] = __fmul_rn(alpha, g);
+      } else {
+        const float v = x[1].v[i];
+        const float pdf = __fmul_rn(expf(__fmul_rn(__fmul_rn(-0.5f, v), v)), 0.39894228040143268f);
+        y[0].v[i] = __fmul_rn(g, __fadd_rn(gelu_cdf(v), __fmul_rn(v, pdf)));
+      }
+    }
   }
 };
 
@@ -228,7 +271,7 @@ struct CopyF {
   static constexpr bool kR1 = false, kR2 = false;
   static constexpr int kMinBlocks = kOccEwCopy;
   template <int VEC>
-  __device__ __forceinline__ void operator()(const Vec<VEC> (&x)[3], Vec<VEC> (&y)[2]) const {
+  __device__ __forceinline__ void operator()(const Vec<VEC> (&x)[3], Vec<VEC> (&y)[2], float) const {
     y[0] = x[0];
   }
 };
@@ -295,7 +338,7 @@ k_elementwise(const __grid_constant__ EwPlan p) {
     for (int u = 0; u < U; ++u) {
       if (!ok[u]) continue;
       Vec<VEC> y[2];
-      f(x[u], y);
+      f(x[u], y, p.alpha);
       if (p.out[0]) put_cols<VEC>(p.out[0], doff[u], p.inner_stride[kSlotOut], col[u], y[0], p.acc_mask & 1);
       if (NOUT > 1 && p.out[1])
         put_cols<VEC>(p.out[1], doff[u], p.inner_stride[kSlotOut], col[u], y[1], p.acc_mask & 2);

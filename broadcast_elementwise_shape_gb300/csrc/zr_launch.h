@@ -69,6 +69,10 @@ cudaError_t launch_fwd_tr(int op, const TrPlan& tp, cudaStream_t s, bool dry = f
 // want: bit 0 grad_a, bit 1 grad_b (no reduction).
 cudaError_t launch_bwd_direct(int op, int want, const EwBuild& eb, cudaStream_t s, bool dry = false);
 cudaError_t launch_copy(const EwBuild& eb, cudaStream_t s, bool dry = false);
+// Unary ops (UnaryCode): forward (slot 0 = x) and backward (slot 0 = grad_out,
+// slot 1 = x); eb.plan.alpha is scale's factor.
+cudaError_t launch_unary_fwd(int uop, const EwBuild& eb, cudaStream_t s, bool dry = false);
+cudaError_t launch_unary_bwd(int uop, const EwBuild& eb, cudaStream_t s, bool dry = false);
 // which: 0 = grad_a, 1 = grad_b, 2 = sum-to-shape.  Launches the reduction
 // pass and, when it writes partials, the combine pass.
 cudaError_t launch_reduce(int op, int which, const RedBuild& rb, cudaStream_t s, bool dry = false);
@@ -76,7 +80,8 @@ cudaError_t launch_reduce(int op, int which, const RedBuild& rb, cudaStream_t s,
 // Resident CTAs per SM of one representative instantiation per kernel
 // family (the 16-byte-vector variants the workloads run), as the planner
 // assumes (*planned) and as the runtime reports for the current device
-// (*actual).  ew: 0 fwd add, 1 fwd div, 2 bwd div (both gradients), 3 copy;
+// (*actual).  ew: 0 fwd add, 1 fwd div, 2 bwd div (both gradients), 3 copy,
+// 4 GeLU forward, 5 GeLU backward;
 // red: 0 add inner kept, 1 sub inner reduced, 2 mul inner kept, 3 div inner
 // reduced, 4 sum-to-shape; 5..9 the same five as cluster variants; other: 0 k_sabf (8 rows per thread), 1 k_transpose.
 cudaError_t occupancy_ew(int which, int* planned, int* actual);

@@ -87,6 +87,16 @@ cudaError_t launch_copy(const EwBuild& eb, cudaStream_t s, bool dry) {
   return launch_ew_t<CopyF, 1>(eb, s, dry);
 }
 
+cudaError_t launch_unary_fwd(int uop, const EwBuild& eb, cudaStream_t s, bool dry) {
+  return uop == UN_SCALE ? launch_ew_t<UnaryF<UN_SCALE>, 1>(eb, s, dry)
+                         : launch_ew_t<UnaryF<UN_GELU>, 1>(eb, s, dry);
+}
+
+cudaError_t launch_unary_bwd(int uop, const EwBuild& eb, cudaStream_t s, bool dry) {
+  return uop == UN_SCALE ? launch_ew_t<UnaryBwdF<UN_SCALE>, 1>(eb, s, dry)
+                         : launch_ew_t<UnaryBwdF<UN_GELU>, 1>(eb, s, dry);
+}
+
 cudaError_t occupancy_ew(int which, int* planned, int* actual) {
   const size_t smem = size_t(kMaxTileRows) * kMaxOperands * sizeof(int64_t);
   switch (which) {
@@ -106,6 +116,14 @@ cudaError_t occupancy_ew(int which, int* planned, int* actual) {
       *planned = kOccEwCopy;
       return cudaOccupancyMaxActiveBlocksPerMultiprocessor(actual, k_elementwise<CopyF, 4, 1>,
                                                            kThreads, smem);
+    case 4:
+      *planned = kOccEwFwd;
+      return cudaOccupancyMaxActiveBlocksPerMultiprocessor(actual, k_elementwise<UnaryF<UN_GELU>, 4, 1>,
+                                                           kThreads, smem);
+    case 5:
+      *planned = kOccEwFwd;
+      return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+          actual, k_elementwise<UnaryBwdF<UN_GELU>, 4, 1>, kThreads, smem);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -285,6 +285,41 @@ int zr_chain_bwd(zr_op op1, zr_op op2, zr_tensor grad_out, zr_tensor a, zr_tenso
                  float* grad_a, float* grad_b, float* grad_c, void* workspace,
                  size_t* workspace_bytes, zr_stream_t stream);
 
+/*
+ * Unary elementwise ops.  The GPU page, section 逐元素运算 (elementwise
+ * ops), lists GeLU and gradient scaling among the ops whose every output
+ * element comes from the input element at the same position.
+ *   ZR_SCALE  out = alpha * x, one IEEE binary32 multiply (bit-identical);
+ *             backward grad_x = alpha * grad_out (bit-identical).
+ *   ZR_GELU   out = x * Phi(x), the exact GeLU (the pages give no formula;
+ *             Phi is the standard normal CDF, computed as erfc(-x/sqrt 2)/2),
+ *             alpha unused; backward grad_x = grad_out * (Phi(x) + x phi(x)),
+ *             phi the standard normal density.  Within
+ *             (16 + 2x^2) * 2^-24 * |exact| + 2^-120 per element forward, and
+ *             (16 + 2x^2) * 2^-24 * |g| (Phi(x) + |x| phi(x)) + 2^-120
+ *             backward (the derivative's two terms cancel near x = -0.75;
+ *             the x^2 term is the binary32 argument of erfc, whose tail
+ *             amplifies relative argument error by about x^2).
+ */
+typedef enum { ZR_SCALE = 0, ZR_GELU = 1 } zr_unary;
+
+/*
+ * zr_unary_fwd — out = op(x), out of x's shape with out_strides (NULL:
+ * dense row-major).  Any input strides; out may alias x exactly (same
+ * layout); other overlap is ZR_ERR_LAYOUT.  Errors and asynchrony as
+ * zr_binary_fwd.
+ */
+int zr_unary_fwd(zr_unary op, float alpha, zr_tensor x, float* out, const int64_t* out_strides,
+                 zr_stream_t stream);
+
+/*
+ * zr_unary_bwd — grad_x = grad_out * op'(x), written in grad_x_strides (NULL:
+ * dense row-major) over x's shape (which must equal grad_out's, else
+ * ZR_ERR_SHAPE).  ZR_SCALE reads no x values (x.data may be NULL).
+ */
+int zr_unary_bwd(zr_unary op, float alpha, zr_tensor grad_out, zr_tensor x, float* grad_x,
+                 const int64_t* grad_x_strides, zr_stream_t stream);
+
 /* Static, human-readable name of a status code. */
 const char* zr_status_string(int status);
 

@@ -50,6 +50,27 @@ def within(gpu: np.ndarray, ref: np.ndarray, abs_sum: np.ndarray, what: str = ""
                            f"{np.max(err / np.maximum(bound, 1e-300)):.3g}")
 
 
+def gelu_close(got, ref, x, mag, what=""):
+    """GeLU results against the oracle: within (16 + 2 x^2) * 2^-24 * mag +
+    2^-120 per element (mag: |exact| forward; |g| (Phi(x) + |x| phi(x))
+    backward), NaN matching NaN and infinities equal.  The x^2 term: binary32
+    rounding of the argument x / sqrt(2) (and of the constant 1/sqrt(2)) moves
+    erfc(z) far in its tail by a relative z^2 * 2u each, z^2 = x^2 / 2."""
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    x = np.asarray(x, np.float64)
+    mag = np.asarray(mag, np.float64)
+    gn, rn = np.isnan(got), np.isnan(ref)
+    assert np.array_equal(gn, rn), f"{what}: NaN positions differ"
+    fin = ~gn & np.isfinite(ref)
+    assert np.array_equal(got[~gn & ~fin], ref[~gn & ~fin]), f"{what}: infinities differ"
+    bound = (16.0 + 2.0 * x[fin] ** 2) * 2.0 ** -24 * mag[fin] + 2.0 ** -120
+    err = np.abs(got[fin] - ref[fin])
+    bad = np.nonzero(err > bound)[0]
+    assert bad.size == 0, (f"{what}: {bad.size} beyond bound; worst at x={x[fin][bad[0]]}: "
+                           f"gpu {got[fin][bad[0]]} ref {ref[fin][bad[0]]}")
+
+
 def is_single_op_grad(op: str, which: int, reduced: bool) -> bool:
     """True if a gradient element is exactly one IEEE op of the inputs."""
     if reduced:
@@ -72,7 +93,13 @@ def run_gpu(name: str, host: dict) -> dict:
     """All step outputs of workload ``name`` computed by the CUDA library."""
     env = {k: to_gpu(v) for k, v in host.items()}
     for step in workloads.STEPS[name]:
-        if step[0] == "cfwd":
+        if step[0] == "ufwd":
+            _, op, alpha, xn, on = step
+            env[on] = zr.zr_unary_fwd(op, env[xn], alpha=alpha)
+        elif step[0] == "ubwd":
+            _, op, alpha, gn, xn, gxn = step
+            env[gxn] = zr.zr_unary_bwd(op, env[gn], env[xn], alpha=alpha)
+        elif step[0] == "cfwd":
             _, op1, op2, an, bn, cn, on = step
             env[on] = zr.zr_chain_fwd(op1, op2, env[an], env[bn], env[cn])
         elif step[0] == "cbwd":
@@ -95,7 +122,16 @@ def run_oracle(name: str, host: dict) -> tuple[dict, dict]:
     env = {k: v for k, v in host.items()}
     sums = {}
     for step in workloads.STEPS[name]:
-        if step[0] == "cfwd":
+        if step[0] == "ufwd":
+            _, op, alpha, xn, on = step
+            env[on] = torch.from_numpy(oracle.unary_fwd(op, env[xn], alpha=alpha))
+            sums[on] = np.abs(env[on].numpy().astype(np.float64))
+        elif step[0] == "ubwd":
+            _, op, alpha, gn, xn, gxn = step
+            r, mag = oracle.unary_bwd(op, env[gn], env[xn], alpha=alpha)
+            env[gxn] = torch.from_numpy(r)
+            sums[gxn] = mag
+        elif step[0] == "cfwd":
             _, op1, op2, an, bn, cn, on = step
             env[on] = torch.from_numpy(oracle.chain_fwd(op1, op2, env[an], env[bn], env[cn]))
         elif step[0] == "cbwd":
@@ -118,6 +154,14 @@ def run_oracle(name: str, host: dict) -> tuple[dict, dict]:
 def compare_workload(name: str, host: dict, gpu: dict, ref: dict, sums: dict):
     out_shapes = {}
     for step in workloads.STEPS[name]:
+        if step[0] in ("ufwd", "ubwd"):
+            op, xn, on = step[1], step[-2], step[-1]
+            what = f"{name} {step[0]} {op} -> {on}"
+            if op == "scale":
+                bitexact(gpu[on].numpy(), ref[on].numpy(), what)
+            else:
+                gelu_close(gpu[on].numpy(), ref[on].numpy(), host[xn].numpy(), sums[on], what)
+            continue
         if step[0] == "cfwd":
             on = step[6]
             bitexact(gpu[on].numpy(), ref[on].numpy(), f"{name} chain fwd -> {on}")

@@ -25,6 +25,9 @@ cases with the same structure):
 * ``x1`` same-shape contiguous add, a [R,C] N(0,1) + b [R,C] N(0,1), g N(0,1)
   (4096,4096): a supplementary case for the contiguous path without
   broadcasting (not one of the five workloads of the benchmark step)
+* ``u1`` unary ops on an FFN hidden activation, x [R,C] N(0,1), g N(0,1)
+  (16384, 3072): GeLU forward and backward, then scale by 0.125 forward and
+  backward (supplementary, outside the benchmark step)
 * ``c3f`` and ``c4f``: the inputs of ``c3`` and ``c4`` (same seeds and
   sizes), run as one fused two-op chain each, (x * gamma) + beta and
   (scores + mask) / scalar (supplementary, outside the benchmark step)
@@ -34,13 +37,15 @@ reverse) as data: ``("fwd", op, a_name, b_name, out_name)`` and
 ``("bwd", op, g_name, a_name, b_name, grad_a_name, grad_b_name)``; a fused
 chain is ``("cfwd", op1, op2, a_name, b_name, c_name, out_name)`` and
 ``("cbwd", op1, op2, g_name, a_name, b_name, c_name, grad_a_name,
-grad_b_name, grad_c_name)``.
+grad_b_name, grad_c_name)``; a unary op ``("ufwd", op, alpha, x_name,
+out_name)`` and ``("ubwd", op, alpha, g_name, x_name, grad_x_name)``.
 """
 from __future__ import annotations
 
 import torch
 
-SEEDS = {"c1": 1001, "c2": 1002, "c3": 1003, "c4": 1004, "c5a": 1005, "c5b": 1006, "x1": 1007}
+SEEDS = {"c1": 1001, "c2": 1002, "c3": 1003, "c4": 1004, "c5a": 1005, "c5b": 1006, "x1": 1007,
+         "u1": 1008}
 # Fused-chain workloads draw the inputs of the workload they fuse.
 BASE = {"c3f": "c3", "c4f": "c4"}
 
@@ -52,6 +57,7 @@ DEFAULT_DIMS = {
     "c5a": dict(P=128, M=256, Q=512),
     "c5b": dict(a=(4, 1, 8, 1, 16, 1, 32, 64), b=(1, 6, 1, 12, 1, 10, 1, 64)),
     "x1": dict(R=4096, C=4096),
+    "u1": dict(R=16384, C=3072),
 }
 
 # Forward chain then backward steps, in execution order.
@@ -74,6 +80,10 @@ STEPS = {
             ("bwd", "div", "g", "a", "b", "grad_a", "grad_b")],
     "x1": [("fwd", "add", "a", "b", "out"),
            ("bwd", "add", "g", "a", "b", "grad_a", "grad_b")],
+    "u1": [("ufwd", "gelu", 1.0, "x", "h"),
+           ("ufwd", "scale", 0.125, "x", "s"),
+           ("ubwd", "scale", 0.125, "g", "x", "grad_s"),
+           ("ubwd", "gelu", 1.0, "g", "x", "grad_x")],
     "c3f": [("cfwd", "mul", "add", "x", "gamma", "beta", "y2"),
             ("cbwd", "mul", "add", "g", "x", "gamma", "beta", "grad_x", "grad_gamma", "grad_beta")],
     "c4f": [("cfwd", "add", "div", "scores", "mask", "scalar", "out"),
@@ -154,6 +164,11 @@ def make_inputs(name: str, seed: int | None = None, **dims) -> dict:
         b = s * u
         g = _normal(gen, _broadcast_dims(sa, sb))
         return dict(a=a, b=b, g=g)
+    if name == "u1":
+        R, C = d["R"], d["C"]
+        x = _normal(gen, (R, C))
+        g = _normal(gen, (R, C))
+        return dict(x=x, g=g)
     if name == "x1":
         R, C = d["R"], d["C"]
         a = _normal(gen, (R, C))
@@ -174,6 +189,7 @@ def small_dims(name: str) -> dict:
         "c5a": dict(P=5, M=67, Q=203),
         "c5b": dict(a=(3, 1, 5, 1, 4, 1, 7, 12), b=(1, 2, 1, 3, 1, 5, 1, 12)),
         "x1": dict(R=333, C=1030),
+        "u1": dict(R=97, C=1031),
         "c3f": dict(B=3, T=97, C=772),
         # 132 columns: 16-byte vectors, so the fused one-pass backward runs.
         "c4f": dict(N=2, H=3, T=132),
