@@ -558,3 +558,18 @@ def test_division_is_ieee_bit_exact():
         ta, tb = torch.from_numpy(a), torch.from_numpy(b)
         got = zr.zr_binary_fwd("div", ta.cuda(), tb.cuda()).cpu().numpy()
         bitexact(got, oracle.binary_fwd("div", ta, tb), f"div {a.shape} / {b.shape}")
+
+
+def test_sum_to_shape_batched_matmul_broadcast_grads():
+    """A weight broadcast over a batched matmul's batch dims gets the sum of
+    the per-batch gradients (Operator page, 广播: SumToSize back to the
+    weight's shape).  The per-batch products are given; the reduction is
+    zr_sum_to_shape: [B, K, N] -> [K, N], [B, H, K, N] -> [1, H, K, N] and
+    [B, H, K, N] -> [K, N]."""
+    rng = np.random.default_rng(60)
+    for shape, target in (((8, 768, 3072), (768, 3072)), ((4, 12, 64, 1024), (1, 12, 64, 1024)),
+                          ((4, 12, 64, 1024), (64, 1024)), ((3, 5, 129, 67), (129, 67))):
+        x = torch.from_numpy(rng.standard_normal(shape).astype(np.float32))
+        got = zr.zr_sum_to_shape(x.cuda(), target).cpu().numpy()
+        ref, sabs = oracle.sum_to_shape(x, target)
+        within(got, ref, sabs, f"batch-broadcast grad {shape}->{target}")
