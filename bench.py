@@ -84,6 +84,24 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(ms, world, device=None):
+    """The slowest rank's timed total: with N replicas (one per GPU, no
+    collective on the data path) the job takes as long as its slowest rank."""
+    if world == 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbs(world, step_bytes, steps, total_ms):
+    """Whole-job throughput: every rank moves step_bytes per step (weak
+    scaling), over the slowest rank's time."""
+    return world * step_bytes * steps / (total_ms * 1e-3) / 1e9
+
+
 def kernel_hash():
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
@@ -513,12 +531,8 @@ def run_zr(args, rank, world, local):
     if world > 1:
         dist.barrier()
     step_ms = [s.elapsed_time(e) for s, e in steps_ev]
-    total_ms = sum(step_ms)
+    total_ms = max_over_ranks(sum(step_ms), world, device)
     dom_ms = [dom_ev[k][0][0].elapsed_time(dom_ev[k][0][1]) for k in range(args.steps)]
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
     clocks = sampler.summary(t0, t1) if sampler else None
 
     per_config = per_op_alone = None
@@ -533,7 +547,7 @@ def run_zr(args, rank, world, local):
 
     if rank == 0:
         peak, peak_kind = measured_peak()
-        value = world * nbytes * args.steps / (total_ms * 1e-3) / 1e9
+        value = job_gbs(world, nbytes, args.steps, total_ms)
         per_op = []
         for i, c in enumerate(suite.calls):
             mean = statistics.fmean(op_ms[i])
