@@ -74,6 +74,8 @@ def _load():
             _lib.orc_binary_bwd_at.argtypes = [ci, ci] + ten + ten + ten + [ctypes.c_int64, i64p, vp, vp]
             _lib.orc_sum_to_shape.argtypes = ten + [ci, i64p, vp, vp]
             _lib.orc_sum_to_shape_at.argtypes = ten + [ci, i64p, ctypes.c_int64, i64p, vp, vp]
+            _lib.orc_round_bf16.argtypes = [vp, ctypes.c_int64, vp]
+            _lib.orc_round_bf16.restype = ci
             _lib.orc_unary_fwd.argtypes = [ci, ctypes.c_float] + ten + [vp]
             _lib.orc_unary_bwd.argtypes = [ci, ctypes.c_float] + ten + [vp, i64p, vp, vp]
             for f in ("orc_unary_fwd", "orc_unary_bwd"):
@@ -320,3 +322,25 @@ def unary_bwd(op, g, x, alpha=1.0):
                              out.ctypes.data if out.size else None,
                              mag.ctypes.data if mag.size else None), "unary_bwd")
     return out, mag
+
+
+
+# ---------------------------------------------------------------- bf16 storage
+#
+# A bfloat16 operator reads bf16 inputs (exact binary32 values), computes as
+# the binary32 operator does, and stores each result rounded once to bf16.
+# For one +, -, *, / the binary32 result rounded to bf16 equals the exact
+# result rounded to bf16 (binary32 has 24 >= 2 * 8 + 2 significand bits, so
+# the double rounding is innocuous; Figueroa), so bf16 outputs of the
+# forward and of one-operation gradients are fixed bit for bit; summed
+# gradients are the binary64 sums rounded to binary32 and then to bf16.
+
+def round_bf16(x):
+    """Round float32 values to the nearest bfloat16 (ties to even), returned
+    as the float32 values they denote."""
+    lib = _load()
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty_like(x)
+    _check(lib.orc_round_bf16(x.ctypes.data if x.size else None, x.size,
+                              out.ctypes.data if out.size else None), "round_bf16")
+    return out

@@ -40,6 +40,7 @@
 #include <cstdint>
 #include <cstddef>
 #include <cmath>
+#include <cstring>
 #include <vector>
 
 namespace {
@@ -507,6 +508,30 @@ int orc_sum_to_shape_at(const float* x, int ndx, const int64_t* szx, const int64
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------- bf16 storage
+//
+// bfloat16 keeps binary32's sign and 8-bit exponent and the top 7 bits of
+// its 23-bit fraction.  Rounding a binary32 value to it, to nearest with
+// ties to even: add 0x7FFF plus the lowest kept bit to the bit pattern and
+// drop the low 16 bits (a carry into the exponent is the correct rounding up,
+// up to infinity); NaN stays NaN (quietened).  Results are returned as the
+// binary32 values they denote.
+extern "C" int orc_round_bf16(const float* x, int64_t n, float* out) {
+  if (n > 0 && (!x || !out)) return -1;
+  for (int64_t i = 0; i < n; ++i) {
+    uint32_t u;
+    std::memcpy(&u, &x[i], 4);
+    uint32_t r;
+    if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu) != 0) {
+      r = (u | 0x00400000u) & 0xFFFF0000u;
+    } else {
+      r = (u + 0x7FFFu + ((u >> 16) & 1u)) & 0xFFFF0000u;
+    }
+    std::memcpy(&out[i], &r, 4);
+  }
+  return 0;
+}
 
 // ---------------------------------------------------------------- unary ops
 //

@@ -577,3 +577,44 @@ def test_gelu_backward_matches_finite_differences():
         fd = float(g[i]) * (f(v + h) - f(v - h)) / (2 * h)
         assert abs(float(gx[i]) - fd) <= 1e-6 * float(mag[i]) + 1e-7, (v, gx[i], fd)
         assert abs(float(gx[i])) <= float(mag[i]) * (1 + 1e-6)
+
+
+# ---------------------------------------------------------------- bf16 rounding
+
+def test_round_bf16_matches_torch_conversion():
+    """The oracle's bf16 rounding against PyTorch's float32 -> bfloat16
+    conversion (round to nearest, ties to even), including ties, overflow to
+    infinity, subnormals, signed zeros, infinities and NaN."""
+    rng = np.random.default_rng(71)
+    bits = rng.integers(0, 2 ** 32, size=200000, dtype=np.uint64).astype(np.uint32)
+    ties = (rng.integers(0, 2 ** 16, size=2000, dtype=np.uint64).astype(np.uint32) << 16) | 0x8000
+    special = np.array([0, 0x80000000, 0x7F800000, 0xFF800000, 0x7F7FFFFF, 0x00000001, 0x00008000,
+                        0x3F808000, 0x3F818000, 0x7F7F8000], np.uint32)
+    for b in (bits, ties, special):
+        x = b.view(np.float32)
+        got = oracle.round_bf16(x)
+        want = torch.from_numpy(x.copy()).to(torch.bfloat16).to(torch.float32).numpy()
+        gn, wn = np.isnan(got), np.isnan(want)
+        assert np.array_equal(gn, wn)
+        assert np.array_equal(got[~gn].view(np.uint32), want[~wn].view(np.uint32))
+
+
+def test_bf16_single_ops_round_once():
+    """bf16 inputs, one binary32 operation, rounded to bf16: equal to the
+    exact (binary64) result rounded to bf16 through binary32 (innocuous
+    double rounding, 24 >= 2*8+2)."""
+    rng = np.random.default_rng(72)
+    a = oracle.round_bf16(rng.standard_normal(50000).astype(np.float32) * 3)
+    b = oracle.round_bf16((0.5 + rng.random(50000)).astype(np.float32))
+    for op in OPS:
+        got = oracle.round_bf16(oracle.binary_fwd(op, a, b))
+        exact64 = NP_OP[op](a.astype(np.float64), b.astype(np.float64))
+        # Round binary64 straight to bf16: nearest representable, ties to even.
+        e = np.frexp(exact64)[1]
+        step = np.ldexp(1.0, e - 8)
+        q = exact64 / step
+        r = np.floor(q)
+        frac = q - r
+        r = np.where((frac > 0.5) | ((frac == 0.5) & (np.mod(r, 2) == 1)), r + 1, r)
+        want = (r * step).astype(np.float32)
+        assert np.array_equal(got.view(np.uint32), want.view(np.uint32)), op
