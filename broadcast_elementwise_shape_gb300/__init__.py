@@ -72,10 +72,14 @@ def lib() -> ctypes.CDLL:
         L.zr_unary_bwd.argtypes = [c_int, ctypes.c_float, ZrTensor, ZrTensor, vp, i64p, vp]
         L.zr_chain_bwd.argtypes = [c_int, c_int, ZrTensor, ZrTensor, ZrTensor, ZrTensor, vp, vp, vp,
                                    vp, szp, vp]
+        L.zr_binary_fwd_t.argtypes = [c_int, c_int, ZrTensor, ZrTensor, vp, i64p, vp]
+        L.zr_binary_bwd_t.argtypes = [c_int, c_int, ZrTensor, ZrTensor, ZrTensor, vp, vp, vp, szp, vp]
+        L.zr_sum_to_shape_t.argtypes = [c_int, ZrTensor, i32, i64p, vp, vp, szp, vp]
         L.zr_status_string.argtypes = [c_int]
         L.zr_status_string.restype = ctypes.c_char_p
         for f in ("zr_broadcast_shape", "zr_binary_fwd", "zr_binary_bwd", "zr_sum_to_shape",
-                  "zr_chain_fwd", "zr_chain_bwd", "zr_binary_bwd_ex", "zr_unary_fwd", "zr_unary_bwd"):
+                  "zr_chain_fwd", "zr_chain_bwd", "zr_binary_bwd_ex", "zr_unary_fwd", "zr_unary_bwd",
+                  "zr_binary_fwd_t", "zr_binary_bwd_t", "zr_sum_to_shape_t"):
             getattr(L, f).restype = c_int
         _lib = L
     return _lib
@@ -93,8 +97,8 @@ def _desc(t, shape=None, need_data=True):
     if need_data and t.numel() > 0 and not t.is_cuda:
         raise ValueError("zr operands must be CUDA tensors")
     import torch
-    if t.dtype != torch.float32:
-        raise TypeError("zr operands must be float32")
+    if t.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("zr operands must be float32 or bfloat16")
     sizes, strides = _i64(t.shape), _i64(t.stride())
     ptr = t.data_ptr() if (t.numel() > 0 and need_data) else None
     return ZrTensor(ptr, t.dim(), sizes, strides), (sizes, strides, t)
@@ -126,18 +130,37 @@ def zr_binary_fwd(op, a, b, out=None):
     """out = a op b (broadcasting).  ``out`` may be a preallocated (strided)
     tensor of the broadcast shape; otherwise a contiguous one is allocated."""
     import torch
+    dt = _dtype_of(a, b)
     shape = zr_broadcast_shape(a.shape, b.shape)
     if out is None:
-        out = torch.empty(shape, dtype=torch.float32, device=a.device)
+        out = torch.empty(shape, dtype=a.dtype, device=a.device)
     elif tuple(out.shape) != shape:
         raise ValueError(f"out has shape {tuple(out.shape)}, expected {shape}")
+    _dtype_of(a, out)
     da, ka = _desc(a)
     db, kb = _desc(b)
     ost = _i64(out.stride())
-    rc = lib().zr_binary_fwd(_op(op), da, db, out.data_ptr() if out.numel() else None, ost,
-                             _stream(out))
+    rc = lib().zr_binary_fwd_t(dt, _op(op), da, db, out.data_ptr() if out.numel() else None, ost,
+                               _stream(out))
     _check(rc, "zr_binary_fwd")
     return out
+
+
+ZR_F32, ZR_BF16 = 0, 1
+
+
+def _dtype_of(*ts):
+    """The zr_dtype of tensors that must share one element type."""
+    import torch
+    dts = {t.dtype for t in ts if t is not None}
+    if len(dts) > 1:
+        raise TypeError(f"operands mix element types {sorted(map(str, dts))}")
+    dt = dts.pop() if dts else torch.float32
+    if dt == torch.float32:
+        return ZR_F32
+    if dt == torch.bfloat16:
+        return ZR_BF16
+    raise TypeError("zr operands must be float32 or bfloat16")
 
 
 def _workspace(nbytes, device):
@@ -151,13 +174,14 @@ def zr_binary_bwd(op, grad_out, a, b, want_a=True, want_b=True, grad_a=None, gra
     None (with ``shape_a``/``shape_b``) when the op does not read them."""
     import torch
     opc = _op(op)
+    dt = _dtype_of(grad_out, a, b, grad_a, grad_b)
     sa = tuple(a.shape) if a is not None else tuple(shape_a)
     sb = tuple(b.shape) if b is not None else tuple(shape_b)
     dev = grad_out.device
     if want_a and grad_a is None:
-        grad_a = torch.empty(sa, dtype=torch.float32, device=dev)
+        grad_a = torch.empty(sa, dtype=grad_out.dtype, device=dev)
     if want_b and grad_b is None:
-        grad_b = torch.empty(sb, dtype=torch.float32, device=dev)
+        grad_b = torch.empty(sb, dtype=grad_out.dtype, device=dev)
     dg, kg = _desc(grad_out)
     da, ka = _desc(a, sa)
     db, kb = _desc(b, sb)
@@ -168,13 +192,13 @@ def zr_binary_bwd(op, grad_out, a, b, want_a=True, want_b=True, grad_a=None, gra
     if grad_b is not None and grad_b.numel() == 0:
         pb = None
     nbytes = ctypes.c_size_t(0)
-    _check(lib().zr_binary_bwd(opc, dg, da, db, pa, pb, None, ctypes.byref(nbytes), None),
+    _check(lib().zr_binary_bwd_t(dt, opc, dg, da, db, pa, pb, None, ctypes.byref(nbytes), None),
            "zr_binary_bwd (workspace query)")
     if workspace is None or workspace.numel() < nbytes.value:
         workspace = _workspace(nbytes.value, dev)
     nbytes = ctypes.c_size_t(workspace.numel())
-    rc = lib().zr_binary_bwd(opc, dg, da, db, pa, pb, workspace.data_ptr(), ctypes.byref(nbytes),
-                             _stream(grad_out))
+    rc = lib().zr_binary_bwd_t(dt, opc, dg, da, db, pa, pb, workspace.data_ptr(),
+                               ctypes.byref(nbytes), _stream(grad_out))
     _check(rc, "zr_binary_bwd")
     return grad_a, grad_b
 
@@ -184,18 +208,19 @@ def zr_sum_to_shape(x, shape, out=None, workspace=None):
     import torch
     shape = tuple(int(s) for s in shape)
     if out is None:
-        out = torch.empty(shape, dtype=torch.float32, device=x.device)
+        out = torch.empty(shape, dtype=x.dtype, device=x.device)
+    dt = _dtype_of(x, out)
     dx, kx = _desc(x)
     so = _i64(shape)
     po = out.data_ptr() if out.numel() else None
     nbytes = ctypes.c_size_t(0)
-    _check(lib().zr_sum_to_shape(dx, len(shape), so, po, None, ctypes.byref(nbytes), None),
+    _check(lib().zr_sum_to_shape_t(dt, dx, len(shape), so, po, None, ctypes.byref(nbytes), None),
            "zr_sum_to_shape (workspace query)")
     if workspace is None or workspace.numel() < nbytes.value:
         workspace = _workspace(nbytes.value, x.device)
     nbytes = ctypes.c_size_t(workspace.numel())
-    rc = lib().zr_sum_to_shape(dx, len(shape), so, po, workspace.data_ptr(), ctypes.byref(nbytes),
-                               _stream(x))
+    rc = lib().zr_sum_to_shape_t(dt, dx, len(shape), so, po, workspace.data_ptr(),
+                                 ctypes.byref(nbytes), _stream(x))
     _check(rc, "zr_sum_to_shape")
     return out
 

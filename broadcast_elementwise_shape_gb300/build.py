@@ -20,7 +20,7 @@ LIB = os.path.join(BUILD, "libzr.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
 SOURCES = ["zr_api.cu", "zr_plan.cpp", "zr_launch_ew.cu", "zr_launch_red.cu", "zr_launch_sab.cu",
-           "zr_launch_chain.cu"]
+           "zr_launch_chain.cu", "zr_launch_bf16.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-fmad=false", "-ftz=false",
          "-prec-div=true", "-prec-sqrt=true", "-I", INCLUDE]

@@ -31,11 +31,11 @@ bool needs_b(int op, int which) {
 struct Span {
   uintptr_t lo = 0, hi = 0;
 };
-Span span_of(const void* p, int64_t extent) {
+Span span_of(const void* p, int64_t extent, int es = 4) {
   Span s;
   if (p && extent > 0) {
     s.lo = reinterpret_cast<uintptr_t>(p);
-    s.hi = s.lo + uintptr_t(extent) * sizeof(float);
+    s.hi = s.lo + uintptr_t(extent) * uintptr_t(es);
   }
   return s;
 }
@@ -116,6 +116,7 @@ int check_device_ptr(const void* p) {
 // ------------------------------------------------------------------ forward
 
 struct FwdSet {
+  int es = 4;                    // bytes per stored element: 4 float, 2 bfloat16
   int op = 0;
   bool empty = false;
   bool tr = false;               // transposed-input tile path
@@ -148,9 +149,10 @@ int plan_fwd(int op, const zr_tensor& ta, const zr_tensor& tb, const float* out,
   }
   if (!S->a.ptr || !S->b.ptr || !out) return ZR_ERR_NULL;
   if (!non_overlapping(S->out)) return ZR_ERR_LAYOUT;
-  const Span so = span_of(out, S->out.extent);
+  const Span so = span_of(out, S->out.extent, S->es);
   for (const TDesc* x : {&S->a, &S->b}) {
-    if (overlaps(so, span_of(x->ptr, x->extent)) && !same_layout(*x, S->out)) return ZR_ERR_LAYOUT;
+    if (overlaps(so, span_of(x->ptr, x->extent, S->es)) && !same_layout(*x, S->out))
+      return ZR_ERR_LAYOUT;
   }
   int64_t st[kProbSlots][kMaxDims] = {};
   align_strides(S->a, n, osz, st[0]);
@@ -159,16 +161,19 @@ int plan_fwd(int op, const zr_tensor& ta, const zr_tensor& tb, const float* out,
   Prob P;
   rc = coalesce(n, osz, st, (1u << 0) | (1u << 1) | (1u << kSlotOut), kSlotOut, &P);
   if (rc) return rc;
+  P.es = S->es;
   const float* in[3] = {S->a.ptr, S->b.ptr, nullptr};
   float* outs[2] = {const_cast<float*>(out), nullptr};
   const uint32_t stream_mask = (S->a.numel == S->out.numel ? 1u : 0u) |
                                (S->b.numel == S->out.numel ? 2u : 0u);
-  rc = build_tr(P, S->a.ptr, S->b.ptr, const_cast<float*>(out), &S->tp);
+  // The transposed-tile and split kernels are built for float storage only.
+  rc = S->es == 4 ? build_tr(P, S->a.ptr, S->b.ptr, const_cast<float*>(out), &S->tp) : 1;
   if (rc == ZR_OK) {
     S->tr = true;
     return ZR_OK;
   }
-  rc = build_sabf(P, S->a.ptr, S->b.ptr, const_cast<float*>(out), &S->sp, &S->sp_rpt);
+  rc = S->es == 4 ? build_sabf(P, S->a.ptr, S->b.ptr, const_cast<float*>(out), &S->sp, &S->sp_rpt)
+                   : 1;
   if (rc == ZR_OK) {
     S->sabf = true;
     return ZR_OK;
@@ -179,6 +184,7 @@ int plan_fwd(int op, const zr_tensor& ta, const zr_tensor& tb, const float* out,
 // ------------------------------------------------------------------ backward
 
 struct BwdSet {
+  int es = 4;                    // bytes per stored element: 4 float, 2 bfloat16
   int op = 0;
   bool nothing = false;          // no gradient requested
   bool empty = false;            // grad_out empty: only zero fills
@@ -231,8 +237,8 @@ int plan_bwd(int op, const zr_tensor& tg, const zr_tensor& ta, const zr_tensor& 
   // exactly only when it has grad_out's shape and grad_out is dense (then each
   // element is read and written by the same thread); any other overlap with
   // an input is refused.
-  const Span sga = span_of(grad_a, S->ga.extent);
-  const Span sgb = span_of(grad_b, S->gb.extent);
+  const Span sga = span_of(grad_a, S->ga.extent, S->es);
+  const Span sgb = span_of(grad_b, S->gb.extent, S->es);
   if (overlaps(sga, sgb)) return ZR_ERR_LAYOUT;
   struct In { const TDesc* t; bool read; };
   const In ins[3] = {{&S->g, true}, {&S->a, read_a}, {&S->b, read_b}};
@@ -243,7 +249,7 @@ int plan_bwd(int op, const zr_tensor& tg, const zr_tensor& ta, const zr_tensor& 
     if (!gd.ptr) continue;
     for (int i = 0; i < 3; ++i) {
       if (!ins[i].read || !ins[i].t->ptr) continue;
-      if (!overlaps(sp, span_of(ins[i].t->ptr, ins[i].t->extent))) continue;
+      if (!overlaps(sp, span_of(ins[i].t->ptr, ins[i].t->extent, S->es))) continue;
       const bool ok = i == 0 && !reduced && same_layout(gd, S->g);
       if (!ok) return ZR_ERR_LAYOUT;
     }
@@ -251,8 +257,8 @@ int plan_bwd(int op, const zr_tensor& tg, const zr_tensor& ta, const zr_tensor& 
 
   if (S->g.numel == 0) {
     S->empty = true;
-    if (grad_a && S->ga.numel > 0) { S->zero_ptr[0] = grad_a; S->zero_bytes[0] = S->ga.numel * 4; }
-    if (grad_b && S->gb.numel > 0) { S->zero_ptr[1] = grad_b; S->zero_bytes[1] = S->gb.numel * 4; }
+    if (grad_a && S->ga.numel > 0) { S->zero_ptr[0] = grad_a; S->zero_bytes[0] = S->ga.numel * S->es; }
+    if (grad_b && S->gb.numel > 0) { S->zero_ptr[1] = grad_b; S->zero_bytes[1] = S->gb.numel * S->es; }
     return ZR_OK;
   }
   if (!S->g.ptr || (read_a && !S->a.ptr) || (read_b && !S->b.ptr)) return ZR_ERR_NULL;
@@ -275,6 +281,7 @@ int plan_bwd(int op, const zr_tensor& tg, const zr_tensor& ta, const zr_tensor& 
     Prob P;
     rc = coalesce(n, osz, st, read_mask | (1u << kSlotOut), -1, &P);
     if (rc) return rc;
+    P.es = S->es;
     const float* in[3] = {S->g.ptr, S->a.ptr, S->b.ptr};
     float* outs[2] = {grad_a, grad_b};
     return build_ew(P, in, outs, read_mask, stream_mask, kOccEwBwd, &S->eb);
@@ -290,6 +297,7 @@ int plan_bwd(int op, const zr_tensor& tg, const zr_tensor& ta, const zr_tensor& 
   Prob P;
   rc = coalesce(n, osz, st, active, -1, &P);
   if (rc) return rc;
+  P.es = S->es;
   size_t off = 0, off_q = 0;
   for (int w = 0; w < 2; ++w) {
     const bool red = w == 0 ? red_a : red_b;
@@ -303,7 +311,9 @@ int plan_bwd(int op, const zr_tensor& tg, const zr_tensor& ta, const zr_tensor& 
     const uint32_t rm = 1u | (ra ? 2u : 0u) | (rbb ? 4u : 0u);
     RedBuild& rb = S->rb[S->nred];
     const int occ = (op == OP_MUL || op == OP_DIV) ? kOccRedMulDiv : kOccRedAddSub;
-    const int ock = red_cl_occ(op, true), ocr = red_cl_occ(op, false);
+    // Cluster plans are built for float storage only.
+    const int ock = S->es == 4 ? red_cl_occ(op, true) : 0;
+    const int ocr = S->es == 4 ? red_cl_occ(op, false) : 0;
     rc = build_red(P, xslot, S->g.ptr, ra ? S->a.ptr : nullptr, rbb ? S->b.ptr : nullptr, rm,
                    stream_mask & rm, xo, d_out, 0, occ, ock, ocr, &rb);
     if (rc) return rc;
@@ -324,7 +334,7 @@ int plan_bwd(int op, const zr_tensor& tg, const zr_tensor& ta, const zr_tensor& 
   S->ws_run = off;
   S->ws_query = off_q;
   // Both gradients reduced: one fused pass when the shape allows it.
-  if (red_a && red_b) {
+  if (red_a && red_b && S->es == 4) {
     const int r = build_sab(P, S->g.ptr, S->a.ptr, S->b.ptr, grad_a, grad_b, read_mask, &S->sb);
     if (r == ZR_OK) {
       S->sab = true;
@@ -344,6 +354,7 @@ int plan_bwd(int op, const zr_tensor& tg, const zr_tensor& ta, const zr_tensor& 
 // ------------------------------------------------------------------ sum to shape
 
 struct SumSet {
+  int es = 4;                    // bytes per stored element: 4 float, 2 bfloat16
   bool empty = false;
   bool copy = false;
   EwBuild eb;
@@ -369,13 +380,13 @@ int plan_sum(const zr_tensor& tin, int32_t ndo, const int64_t* so, float* out, S
   for (int d = 0; d < n; ++d)
     if (bsz[d] != S->in.size[d]) return ZR_ERR_SHAPE;
   const bool reduced = is_reduced(S->out, n, S->in.size);
-  const Span sout = span_of(out, S->out.extent);
-  if (overlaps(sout, span_of(S->in.ptr, S->in.extent)) &&
+  const Span sout = span_of(out, S->out.extent, S->es);
+  if (overlaps(sout, span_of(S->in.ptr, S->in.extent, S->es)) &&
       (reduced || !same_layout(S->out, S->in)))
     return ZR_ERR_LAYOUT;
   if (S->in.numel == 0) {
     S->empty = true;
-    if (S->out.numel > 0) { S->zero_ptr = out; S->zero_bytes = S->out.numel * 4; }
+    if (S->out.numel > 0) { S->zero_ptr = out; S->zero_bytes = S->out.numel * S->es; }
     return ZR_OK;
   }
   if (!S->in.ptr || !out) return ZR_ERR_NULL;
@@ -389,6 +400,7 @@ int plan_sum(const zr_tensor& tin, int32_t ndo, const int64_t* so, float* out, S
     for (int d = 0; d < n; ++d) st[kSlotOut][d] = S->in.size[d] == 1 ? 0 : dense[d];
     rc = coalesce(n, S->in.size, st, 1u | (1u << kSlotOut), -1, &P);
     if (rc) return rc;
+    P.es = S->es;
     const float* in[3] = {S->in.ptr, nullptr, nullptr};
     float* outs[2] = {out, nullptr};
     return build_ew(P, in, outs, 1u, 1u, kOccEwCopy, &S->eb);
@@ -396,7 +408,9 @@ int plan_sum(const zr_tensor& tin, int32_t ndo, const int64_t* so, float* out, S
   grad_index_strides(S->out, n, S->in.size, st[kSlotXA]);
   rc = coalesce(n, S->in.size, st, 1u | (1u << kSlotXA), -1, &P);
   if (rc) return rc;
-  const int ock = red_cl_occ(OP_ADD, true), ocr = red_cl_occ(OP_ADD, false);
+  P.es = S->es;
+  const int ock = S->es == 4 ? red_cl_occ(OP_ADD, true) : 0;
+  const int ocr = S->es == 4 ? red_cl_occ(OP_ADD, false) : 0;
   rc = build_red(P, kSlotXA, S->in.ptr, nullptr, nullptr, 1u, 1u, out, nullptr, 0, kOccRedAddSub,
                  ock, ocr, &S->rb);
   if (rc) return rc;
@@ -469,9 +483,10 @@ int zr_broadcast_shape(int32_t ndim_a, const int64_t* sizes_a, int32_t ndim_b,
   return ZR_OK;
 }
 
-int zr_binary_fwd(zr_op op, zr_tensor a, zr_tensor b, float* out, const int64_t* out_strides,
-                  zr_stream_t stream) {
+static int binary_fwd_es(int es, zr_op op, zr_tensor a, zr_tensor b, float* out,
+                         const int64_t* out_strides, zr_stream_t stream) {
   FwdSet S;
+  S.es = es;
   int rc = plan_fwd(op, a, b, out, out_strides, &S);
   if (rc) return rc;
   if (S.empty) return ZR_OK;
@@ -486,10 +501,12 @@ int zr_binary_fwd(zr_op op, zr_tensor a, zr_tensor b, float* out, const int64_t*
   return cuda_status(launch_fwd(op, S.eb, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-int zr_binary_bwd(zr_op op, zr_tensor grad_out, zr_tensor a, zr_tensor b, float* grad_a,
-                  float* grad_b, void* workspace, size_t* workspace_bytes, zr_stream_t stream) {
+static int binary_bwd_es(int es, zr_op op, zr_tensor grad_out, zr_tensor a, zr_tensor b,
+                         float* grad_a, float* grad_b, void* workspace, size_t* workspace_bytes,
+                         zr_stream_t stream) {
   if (!workspace_bytes) return ZR_ERR_NULL;
   BwdSet S;
+  S.es = es;
   int rc = plan_bwd(op, grad_out, a, b, grad_a, grad_b, &S);
   if (rc) return rc;
   if (workspace == nullptr) {
@@ -610,10 +627,12 @@ int zr_binary_bwd_noalloc(zr_op op, zr_tensor grad_out, zr_tensor a, zr_tensor b
   return launch_bwd_set(S, op, scratch, st, false);
 }
 
-int zr_sum_to_shape(zr_tensor in, int32_t ndim_out, const int64_t* sizes_out, float* out,
-                    void* workspace, size_t* workspace_bytes, zr_stream_t stream) {
+static int sum_to_shape_es(int es, zr_tensor in, int32_t ndim_out, const int64_t* sizes_out,
+                           float* out, void* workspace, size_t* workspace_bytes,
+                           zr_stream_t stream) {
   if (!workspace_bytes) return ZR_ERR_NULL;
   SumSet S;
+  S.es = es;
   int rc = plan_sum(in, ndim_out, sizes_out, out, &S);
   if (rc) return rc;
   if (workspace == nullptr) {
@@ -641,9 +660,51 @@ int zr_sum_to_shape(zr_tensor in, int32_t ndim_out, const int64_t* sizes_out, fl
   return launch_sum_set(S, workspace, st, false);
 }
 
+int zr_binary_fwd(zr_op op, zr_tensor a, zr_tensor b, float* out, const int64_t* out_strides,
+                  zr_stream_t stream) {
+  return binary_fwd_es(4, op, a, b, out, out_strides, stream);
+}
+
+int zr_binary_bwd(zr_op op, zr_tensor grad_out, zr_tensor a, zr_tensor b, float* grad_a,
+                  float* grad_b, void* workspace, size_t* workspace_bytes, zr_stream_t stream) {
+  return binary_bwd_es(4, op, grad_out, a, b, grad_a, grad_b, workspace, workspace_bytes, stream);
+}
+
+int zr_sum_to_shape(zr_tensor in, int32_t ndim_out, const int64_t* sizes_out, float* out,
+                    void* workspace, size_t* workspace_bytes, zr_stream_t stream) {
+  return sum_to_shape_es(4, in, ndim_out, sizes_out, out, workspace, workspace_bytes, stream);
+}
+
+static int dtype_bytes(int dtype) { return dtype == ZR_F32 ? 4 : (dtype == ZR_BF16 ? 2 : 0); }
+
+int zr_binary_fwd_t(zr_dtype dtype, zr_op op, zr_tensor a, zr_tensor b, void* out,
+                    const int64_t* out_strides, zr_stream_t stream) {
+  const int es = dtype_bytes(dtype);
+  if (!es) return ZR_ERR_DTYPE;
+  return binary_fwd_es(es, op, a, b, static_cast<float*>(out), out_strides, stream);
+}
+
+int zr_binary_bwd_t(zr_dtype dtype, zr_op op, zr_tensor grad_out, zr_tensor a, zr_tensor b,
+                    void* grad_a, void* grad_b, void* workspace, size_t* workspace_bytes,
+                    zr_stream_t stream) {
+  const int es = dtype_bytes(dtype);
+  if (!es) return ZR_ERR_DTYPE;
+  return binary_bwd_es(es, op, grad_out, a, b, static_cast<float*>(grad_a),
+                       static_cast<float*>(grad_b), workspace, workspace_bytes, stream);
+}
+
+int zr_sum_to_shape_t(zr_dtype dtype, zr_tensor in, int32_t ndim_out, const int64_t* sizes_out,
+                      void* out, void* workspace, size_t* workspace_bytes, zr_stream_t stream) {
+  const int es = dtype_bytes(dtype);
+  if (!es) return ZR_ERR_DTYPE;
+  return sum_to_shape_es(es, in, ndim_out, sizes_out, static_cast<float*>(out), workspace,
+                         workspace_bytes, stream);
+}
+
 const char* zr_status_string(int status) {
   switch (status) {
     case ZR_OK: return "ZR_OK";
+    case ZR_ERR_DTYPE: return "ZR_ERR_DTYPE: unknown element type";
     case ZR_ERR_NULL: return "ZR_ERR_NULL: required pointer is NULL or op code unknown";
     case ZR_ERR_RANK: return "ZR_ERR_RANK: ndim < 0 or ndim > 8";
     case ZR_ERR_SHAPE: return "ZR_ERR_SHAPE: shapes not broadcastable or wrong grad_out shape";

@@ -9,6 +9,7 @@
 #pragma once
 
 #include <cuda_runtime.h>
+#include <cuda_bf16.h>
 #include "zr_internal.h"
 
 namespace zr {
@@ -117,53 +118,86 @@ struct Kahan {
 template <int VEC>
 struct Vec { float v[VEC]; };
 
+// Storage types E: float, or bfloat16 (binary32's upper 16 bits).  Loads
+// widen to binary32 exactly; stores round to the storage type once, to
+// nearest with ties to even.  All arithmetic is binary32.
+__device__ __forceinline__ float ld1(const float* p, bool streaming) {
+  return streaming ? __ldcs(p) : __ldg(p);
+}
+__device__ __forceinline__ float ld1(const __nv_bfloat16* p, bool streaming) {
+  const unsigned short* q = reinterpret_cast<const unsigned short*>(p);
+  const unsigned short u = streaming ? __ldcs(q) : __ldg(q);
+  return __uint_as_float(uint32_t(u) << 16);
+}
+__device__ __forceinline__ void st1(float* p, float v) { *p = v; }
+__device__ __forceinline__ void st1(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  return uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(lo))) |
+         (uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(hi))) << 16);
+}
+
 // Load VEC consecutive columns of one operand in one row.  inner == 1:
-// contiguous (128-bit load when VEC == 4; the planner guarantees alignment);
-// inner == 0: the column is broadcast, one load; otherwise a strided gather.
-template <int VEC>
-__device__ __forceinline__ Vec<VEC> load_cols(const float* __restrict__ base, int64_t row_off,
+// contiguous (one 16-byte load of 4 floats or one 8-byte load of 4 bf16 when
+// VEC == 4; the planner guarantees alignment); inner == 0: the column is
+// broadcast, one load; otherwise a strided gather.
+template <int VEC, class E>
+__device__ __forceinline__ Vec<VEC> load_cols(const E* __restrict__ base, int64_t row_off,
                                               int64_t inner, uint32_t c, bool streaming) {
   Vec<VEC> r;
   if (inner == 1) {
-    const float* p = base + row_off + c;
+    const E* p = base + row_off + c;
     if (VEC == 4) {
-      const float4 q = streaming ? __ldcs(reinterpret_cast<const float4*>(p))
-                                 : __ldg(reinterpret_cast<const float4*>(p));
-      r.v[0] = q.x; r.v[1] = q.y; r.v[2] = q.z; r.v[VEC - 1] = q.w;
+      if constexpr (sizeof(E) == 4) {
+        const float4 q = streaming ? __ldcs(reinterpret_cast<const float4*>(p))
+                                   : __ldg(reinterpret_cast<const float4*>(p));
+        r.v[0] = q.x; r.v[1] = q.y; r.v[2] = q.z; r.v[VEC - 1] = q.w;
+      } else {
+        const uint2 q = streaming ? __ldcs(reinterpret_cast<const uint2*>(p))
+                                  : __ldg(reinterpret_cast<const uint2*>(p));
+        r.v[0] = __uint_as_float(q.x << 16);
+        r.v[1] = __uint_as_float(q.x & 0xFFFF0000u);
+        r.v[2] = __uint_as_float(q.y << 16);
+        r.v[VEC - 1] = __uint_as_float(q.y & 0xFFFF0000u);
+      }
     } else {
-      r.v[0] = streaming ? __ldcs(p) : __ldg(p);
+      r.v[0] = ld1(p, streaming);
     }
   } else if (inner == 0) {
-    const float s = __ldg(base + row_off);
+    const float s = ld1(base + row_off, false);
 #pragma unroll
     for (int i = 0; i < VEC; ++i) r.v[i] = s;
   } else {
 #pragma unroll
-    for (int i = 0; i < VEC; ++i) r.v[i] = __ldg(base + row_off + int64_t(c + i) * inner);
+    for (int i = 0; i < VEC; ++i) r.v[i] = ld1(base + row_off + int64_t(c + i) * inner, false);
   }
   return r;
 }
 
-template <int VEC>
-__device__ __forceinline__ void store_cols(float* __restrict__ base, int64_t row_off, int64_t inner,
+template <int VEC, class E>
+__device__ __forceinline__ void store_cols(E* __restrict__ base, int64_t row_off, int64_t inner,
                                            uint32_t c, const Vec<VEC>& x) {
   if (inner == 1) {
-    float* p = base + row_off + c;
+    E* p = base + row_off + c;
     if (VEC == 4) {
-      *reinterpret_cast<float4*>(p) = make_float4(x.v[0], x.v[1], x.v[2], x.v[VEC - 1]);
+      if constexpr (sizeof(E) == 4) {
+        *reinterpret_cast<float4*>(p) = make_float4(x.v[0], x.v[1], x.v[2], x.v[VEC - 1]);
+      } else {
+        *reinterpret_cast<uint2*>(p) = make_uint2(pack_bf16x2(x.v[0], x.v[1]),
+                                                  pack_bf16x2(x.v[2], x.v[VEC - 1]));
+      }
     } else {
-      *p = x.v[0];
+      st1(p, x.v[0]);
     }
   } else {
 #pragma unroll
-    for (int i = 0; i < VEC; ++i) base[row_off + int64_t(c + i) * inner] = x.v[i];
+    for (int i = 0; i < VEC; ++i) st1(base + row_off + int64_t(c + i) * inner, x.v[i]);
   }
 }
 
 // Store, or with acc add to what is there first (one binary32 addition per
 // element: AccumulateGrad's in-place sum, Autograd page, section 反向传播).
-template <int VEC>
-__device__ __forceinline__ void put_cols(float* __restrict__ base, int64_t row_off, int64_t inner,
+template <int VEC, class E>
+__device__ __forceinline__ void put_cols(E* __restrict__ base, int64_t row_off, int64_t inner,
                                          uint32_t c, Vec<VEC> x, bool acc) {
   if (acc) {
     const Vec<VEC> old = load_cols<VEC>(base, row_off, inner, c, false);
@@ -172,8 +206,9 @@ __device__ __forceinline__ void put_cols(float* __restrict__ base, int64_t row_o
   }
   store_cols<VEC>(base, row_off, inner, c, x);
 }
-__device__ __forceinline__ void put1(float* p, float v, bool acc) {
-  *p = acc ? __fadd_rn(*p, v) : v;
+template <class E>
+__device__ __forceinline__ void put1(E* p, float v, bool acc) {
+  st1(p, acc ? __fadd_rn(ld1(p, false), v) : v);
 }
 
 // ---------------------------------------------------------------- functors
@@ -325,10 +360,15 @@ struct Uniform2<F, decltype(void(F::kUniform2))> { static constexpr bool value =
 // One CTA = one tile of rows x column vectors.  Each thread takes items
 // threadIdx.x + k * 256; items are processed in batches of U so that U
 // independent loads per operand are in flight before any result is stored.
-template <class F, int VEC, int NOUT>
+template <class F, int VEC, int NOUT, class E = float>
 __global__ void __launch_bounds__(kThreads, F::kMinBlocks)
 k_elementwise(const __grid_constant__ EwPlan p) {
   pdl_trigger();
+  const E* in0 = reinterpret_cast<const E*>(p.in[0]);
+  const E* in1 = reinterpret_cast<const E*>(p.in[1]);
+  const E* in2 = reinterpret_cast<const E*>(p.in[2]);
+  E* out0 = reinterpret_cast<E*>(p.out[0]);
+  E* out1 = reinterpret_cast<E*>(p.out[1]);
   extern __shared__ int64_t s_off[];  // [tile_rows][kMaxOperands]
   const EwTile t = ew_tile(p, blockIdx.x);
   for (uint32_t i = threadIdx.x; i < t.nrows; i += blockDim.x) {
@@ -341,7 +381,7 @@ k_elementwise(const __grid_constant__ EwPlan p) {
   pdl_wait();
   constexpr bool kUni2 = Uniform2<F>::value;
   float uni2 = 0.f;
-  if (kUni2) uni2 = __ldg(p.in[2]);
+  if (kUni2) uni2 = ld1(in2, false);
 
   constexpr int U = 4;
   const F f;
@@ -360,13 +400,13 @@ k_elementwise(const __grid_constant__ EwPlan p) {
       doff[u] = 0;
       if (ok[u]) {
         const int64_t* ro = s_off + ri * kMaxOperands;
-        x[u][0] = load_cols<VEC>(p.in[0], ro[0], p.inner_stride[0], col[u], p.stream_mask & 1);
-        if (F::kR1) x[u][1] = load_cols<VEC>(p.in[1], ro[1], p.inner_stride[1], col[u], p.stream_mask & 2);
+        x[u][0] = load_cols<VEC>(in0, ro[0], p.inner_stride[0], col[u], p.stream_mask & 1);
+        if (F::kR1) x[u][1] = load_cols<VEC>(in1, ro[1], p.inner_stride[1], col[u], p.stream_mask & 2);
         if (F::kR2 && kUni2) {
 #pragma unroll
           for (int i = 0; i < VEC; ++i) x[u][2].v[i] = uni2;
         } else if (F::kR2) {
-          x[u][2] = load_cols<VEC>(p.in[2], ro[2], p.inner_stride[2], col[u], p.stream_mask & 4);
+          x[u][2] = load_cols<VEC>(in2, ro[2], p.inner_stride[2], col[u], p.stream_mask & 4);
         }
         doff[u] = ro[kSlotOut];
       }
@@ -376,9 +416,9 @@ k_elementwise(const __grid_constant__ EwPlan p) {
       if (!ok[u]) continue;
       Vec<VEC> y[2];
       f(x[u], y, p.alpha);
-      if (p.out[0]) put_cols<VEC>(p.out[0], doff[u], p.inner_stride[kSlotOut], col[u], y[0], p.acc_mask & 1);
-      if (NOUT > 1 && p.out[1])
-        put_cols<VEC>(p.out[1], doff[u], p.inner_stride[kSlotOut], col[u], y[1], p.acc_mask & 2);
+      if (out0) put_cols<VEC>(out0, doff[u], p.inner_stride[kSlotOut], col[u], y[0], p.acc_mask & 1);
+      if (NOUT > 1 && out1)
+        put_cols<VEC>(out1, doff[u], p.inner_stride[kSlotOut], col[u], y[1], p.acc_mask & 2);
     }
   }
 }
@@ -576,13 +616,19 @@ struct RedTerms {
 // CTA adds the cluster's results in rank order and writes X.  A second
 // barrier keeps every CTA resident until the leader has read it.  CL kernels
 // keep more items in flight per thread (red_cl_unroll).
-template <int OP, int WHICH, int VEC, bool INNER_KEPT, bool CL = false>
+template <int OP, int WHICH, int VEC, bool INNER_KEPT, bool CL = false, class E = float>
 __global__ void __launch_bounds__(kThreads,
                                   CL ? red_cl_occ(OP, INNER_KEPT)
                                      : ((OP == OP_MUL || OP == OP_DIV) ? kOccRedMulDiv
                                                                       : kOccRedAddSub))
 k_reduce(const __grid_constant__ RedPlan p) {
   pdl_trigger();
+  // Operands and gradients in storage type E; partial slots are binary32.
+  const E* gE = reinterpret_cast<const E*>(p.g);
+  const E* aE = reinterpret_cast<const E*>(p.a);
+  const E* bE = reinterpret_cast<const E*>(p.b);
+  E* xE = reinterpret_cast<E*>(p.x_final);
+  E* dE = reinterpret_cast<E*>(p.d_out);
   using T = RedTerms<OP, WHICH>;
   extern __shared__ int64_t s_dyn[];
   const uint32_t table_rows = p.rows_per_blk < kMaxTileRows ? p.rows_per_blk : kMaxTileRows;
@@ -637,7 +683,7 @@ k_reduce(const __grid_constant__ RedPlan p) {
         const bool needed =
             WHICH == 0 ? ((T::kXa || T::kDa) && read_a) : ((T::kXb || T::kDb) && read_b);
         if (needed)
-          own = load_cols<VEC>(WHICH == 0 ? p.a : p.b, base[slot], p.inner_stride[slot],
+          own = load_cols<VEC>(WHICH == 0 ? aE : bE, base[slot], p.inner_stride[slot],
                                (vcol_begin + tx) * VEC, false);
       }
     }
@@ -661,11 +707,11 @@ k_reduce(const __grid_constant__ RedPlan p) {
         cc[u] = (vcol_begin + tx + cm * p.tx) * VEC;
         if (ok[u]) {
           const int64_t* ro = s_off + ri[u] * kMaxOperands;
-          gv[u] = load_cols<VEC>(p.g, ro[0], p.inner_stride[0], cc[u], p.stream_mask & 1);
+          gv[u] = load_cols<VEC>(gE, ro[0], p.inner_stride[0], cc[u], p.stream_mask & 1);
           if ((T::kXa || T::kDa) && read_a && WHICH != 0)
-            av[u] = load_cols<VEC>(p.a, ro[1], p.inner_stride[1], cc[u], p.stream_mask & 2);
+            av[u] = load_cols<VEC>(aE, ro[1], p.inner_stride[1], cc[u], p.stream_mask & 2);
           if ((T::kXb || T::kDb) && read_b && WHICH != 1)
-            bv[u] = load_cols<VEC>(p.b, ro[2], p.inner_stride[2], cc[u], p.stream_mask & 4);
+            bv[u] = load_cols<VEC>(bE, ro[2], p.inner_stride[2], cc[u], p.stream_mask & 4);
           if (++cm == ncs) { cm = 0; ++rm; }
         }
       }
@@ -683,7 +729,7 @@ k_reduce(const __grid_constant__ RedPlan p) {
           if (has_d) dv.v[i] = T::d(gg, aa, bb);
         }
         if (has_d)
-          put_cols<VEC>(p.d_out, s_off[ri[u] * kMaxOperands + kSlotOut], p.inner_stride[kSlotOut],
+          put_cols<VEC>(dE, s_off[ri[u] * kMaxOperands + kSlotOut], p.inner_stride[kSlotOut],
                         cc[u], dv, p.acc_d);
       }
     }
@@ -717,8 +763,8 @@ k_reduce(const __grid_constant__ RedPlan p) {
           if (vcv >= vcol_end || col >= p.ncol) continue;
           float r = ld_cluster(s_red + v, 0);
           for (uint32_t k = 1; k < p.cluster; ++k) r = __fadd_rn(r, ld_cluster(s_red + v, k));
-          if (T::kPost) r = __fmul_rn(r, T::post(__ldg(p.b + base[2] + int64_t(col) * p.inner_stride[2])));
-          put1(p.x_final + uint64_t(cta.kidx) * p.ncol + col, __fmul_rn(r, p.scale), p.acc_x);
+          if (T::kPost) r = __fmul_rn(r, T::post(ld1(bE + base[2] + int64_t(col) * p.inner_stride[2], false)));
+          put1(xE + uint64_t(cta.kidx) * p.ncol + col, __fmul_rn(r, p.scale), p.acc_x);
         }
       }
       cluster_sync();
@@ -731,14 +777,14 @@ k_reduce(const __grid_constant__ RedPlan p) {
 #pragma unroll
       for (int i = 0; i < VEC; ++i) r.v[i] = s_red[tx * VEC + i];
       if (T::kPost) {
-        const Vec<VEC> bv = load_cols<VEC>(p.b, base[2], p.inner_stride[2], vc * VEC, false);
+        const Vec<VEC> bv = load_cols<VEC>(bE, base[2], p.inner_stride[2], vc * VEC, false);
 #pragma unroll
         for (int i = 0; i < VEC; ++i) r.v[i] = __fmul_rn(r.v[i], T::post(bv.v[i]));
       }
       if (p.nslots == 1) {
 #pragma unroll
         for (int i = 0; i < VEC; ++i) r.v[i] = __fmul_rn(r.v[i], p.scale);
-        put_cols<VEC>(p.x_final + j, 0, 1, 0, r, p.acc_x);
+        put_cols<VEC>(xE + j, 0, 1, 0, r, p.acc_x);
       } else {
         store_cols<VEC>(p.partial + uint64_t(cta.rblk) * p.nout + j, 0, 1, 0, r);
       }
@@ -756,17 +802,17 @@ k_reduce(const __grid_constant__ RedPlan p) {
       if (cluster_rank() == 0 && threadIdx.x == 0) {
         float r = ld_cluster(s_red, 0);
         for (uint32_t k = 1; k < p.cluster; ++k) r = __fadd_rn(r, ld_cluster(s_red, k));
-        if (T::kPost) r = __fmul_rn(r, T::post(__ldg(p.b + base[2])));
-        put1(p.x_final + cta.kidx, __fmul_rn(r, p.scale), p.acc_x);
+        if (T::kPost) r = __fmul_rn(r, T::post(ld1(bE + base[2], false)));
+        put1(xE + cta.kidx, __fmul_rn(r, p.scale), p.acc_x);
       }
       cluster_sync();
       return;
     }
     if (threadIdx.x == 0) {
       float r = s_red[0];
-      if (T::kPost) r = __fmul_rn(r, T::post(__ldg(p.b + base[2])));
+      if (T::kPost) r = __fmul_rn(r, T::post(ld1(bE + base[2], false)));
       if (p.nslots == 1) {
-        put1(p.x_final + cta.kidx, __fmul_rn(r, p.scale), p.acc_x);
+        put1(xE + cta.kidx, __fmul_rn(r, p.scale), p.acc_x);
       } else {
         const uint64_t slot = uint64_t(cta.rblk) * p.n_cblk + cta.cblk;
         p.partial[slot * p.nout + cta.kidx] = r;
@@ -778,6 +824,7 @@ k_reduce(const __grid_constant__ RedPlan p) {
 // Second pass: for each output j, add its nslots partials in slot order.
 // Thread (jx lane, sy lane) adds slots sy, sy + sy_n, ... (Kahan), then a
 // fixed tree over the sy lanes.
+template <class E = float>
 static __global__ void __launch_bounds__(kThreads)
 k_combine(const __grid_constant__ CombinePlan p) {
   pdl_trigger();
@@ -811,7 +858,9 @@ k_combine(const __grid_constant__ CombinePlan p) {
   __syncthreads();
   if (sl == 0 && j < p.nout) {
     const float v = __fmul_rn(s_red[jl], p.scale);
-    put1(j < p.split ? p.out + j : p.out2 + (j - p.split), v, p.accumulate);
+    E* out = reinterpret_cast<E*>(p.out);
+    E* out2 = reinterpret_cast<E*>(p.out2);
+    put1(j < p.split ? out + j : out2 + (j - p.split), v, p.accumulate);
   }
 }
 

@@ -88,6 +88,13 @@ cudaError_t occupancy_ew(int which, int* planned, int* actual);
 cudaError_t occupancy_red(int which, int* planned, int* actual);
 cudaError_t occupancy_other(int which, int* planned, int* actual);
 
+// bfloat16 storage (plans with es == 2): the float launchers above hand
+// those plans to these.
+cudaError_t launch_fwd_bf16(int op, const EwBuild& eb, cudaStream_t s, bool dry);
+cudaError_t launch_bwd_direct_bf16(int op, int want, const EwBuild& eb, cudaStream_t s, bool dry);
+cudaError_t launch_copy_bf16(const EwBuild& eb, cudaStream_t s, bool dry);
+cudaError_t launch_reduce_bf16(int op, int which, const RedBuild& rb, cudaStream_t s, bool dry);
+
 // Two-op chains out = (a op1 b) op2 c: the forward (slots 0..2 = a, b, c)
 // and the fused one-pass backward with its second passes.
 // c_one: c has one element (read once per thread, 4 CTAs per SM).

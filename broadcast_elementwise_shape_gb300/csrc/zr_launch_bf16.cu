@@ -1,0 +1,102 @@
+// zr_launch_bf16.cu — bfloat16-storage instantiations of the elementwise,
+// reduction and combine kernels (binary32 arithmetic, one rounding to bf16
+// per stored element; partial sums stay binary32).  The launchers of the
+// float paths hand plans with es == 2 to these.
+#include <cuda_bf16.h>
+
+#include "zr_launch.h"
+#include "zr_kernels.cuh"
+
+namespace zr {
+
+namespace {
+
+using bf16 = __nv_bfloat16;
+
+template <class F, int NOUT>
+cudaError_t launch_ew_bf16(const EwBuild& eb, cudaStream_t s, bool dry) {
+  if (!eb.plan.in[0] || (F::kR1 && !eb.plan.in[1]) || (F::kR2 && !eb.plan.in[2]) ||
+      (!eb.plan.out[0] && !eb.plan.out[1]))
+    return cudaErrorInvalidValue;
+  if (dry) return cudaSuccess;
+  const size_t smem = size_t(eb.plan.tile_rows) * kMaxOperands * sizeof(int64_t);
+  if (eb.vec == 4)
+    return launch_k(k_elementwise<F, 4, NOUT, bf16>, eb.plan.n_cta, kThreads, smem, s, eb.plan);
+  return launch_k(k_elementwise<F, 1, NOUT, bf16>, eb.plan.n_cta, kThreads, smem, s, eb.plan);
+}
+
+template <int OP>
+cudaError_t direct_bf16(int want, const EwBuild& eb, cudaStream_t s, bool dry) {
+  switch (want) {
+    case 1: return launch_ew_bf16<BwdDirectF<OP, 1>, 2>(eb, s, dry);
+    case 2: return launch_ew_bf16<BwdDirectF<OP, 2>, 2>(eb, s, dry);
+    default: return launch_ew_bf16<BwdDirectF<OP, 3>, 2>(eb, s, dry);
+  }
+}
+
+template <int OP, int WHICH>
+cudaError_t red_bf16(const RedBuild& rb, cudaStream_t s, bool dry) {
+  const RedPlan& p = rb.plan;
+  const bool has_d = p.d_out != nullptr;
+  if (!p.g || (RedTerms<OP, WHICH>::reads_a(has_d) && !p.a) ||
+      (RedTerms<OP, WHICH>::reads_b(has_d) && !p.b) || !p.x_final ||
+      (p.nslots > 1 && !p.partial) || p.cluster > 1)
+    return cudaErrorInvalidValue;
+  if (dry) return cudaSuccess;
+  const uint32_t table_rows = p.rows_per_blk < kMaxTileRows ? p.rows_per_blk : kMaxTileRows;
+  const size_t red_floats = p.inner_kept ? size_t(kThreads) * rb.vec : size_t(kThreads);
+  const size_t smem = size_t(table_rows) * kMaxOperands * sizeof(int64_t) + red_floats * sizeof(float);
+  cudaError_t e;
+  if (p.inner_kept) {
+    e = rb.vec == 4 ? launch_k(k_reduce<OP, WHICH, 4, true, false, bf16>, p.n_cta, kThreads, smem, s, p)
+                    : launch_k(k_reduce<OP, WHICH, 1, true, false, bf16>, p.n_cta, kThreads, smem, s, p);
+  } else {
+    e = rb.vec == 4 ? launch_k(k_reduce<OP, WHICH, 4, false, false, bf16>, p.n_cta, kThreads, smem, s, p)
+                    : launch_k(k_reduce<OP, WHICH, 1, false, false, bf16>, p.n_cta, kThreads, smem, s, p);
+  }
+  if (e != cudaSuccess || p.nslots <= 1) return e;
+  const CombinePlan& c = rb.comb;
+  const uint64_t nblk = (c.nout + c.jx - 1) / c.jx;
+  return launch_k(k_combine<bf16>, static_cast<unsigned>(nblk), kThreads, 0, s, c);
+}
+
+template <int OP>
+cudaError_t red_op_bf16(int which, const RedBuild& rb, cudaStream_t s, bool dry) {
+  return which == 0 ? red_bf16<OP, 0>(rb, s, dry) : red_bf16<OP, 1>(rb, s, dry);
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_bf16(int op, const EwBuild& eb, cudaStream_t s, bool dry) {
+  switch (op) {
+    case OP_ADD: return launch_ew_bf16<FwdF<OP_ADD>, 1>(eb, s, dry);
+    case OP_SUB: return launch_ew_bf16<FwdF<OP_SUB>, 1>(eb, s, dry);
+    case OP_MUL: return launch_ew_bf16<FwdF<OP_MUL>, 1>(eb, s, dry);
+    default: return launch_ew_bf16<FwdF<OP_DIV>, 1>(eb, s, dry);
+  }
+}
+
+cudaError_t launch_bwd_direct_bf16(int op, int want, const EwBuild& eb, cudaStream_t s, bool dry) {
+  switch (op) {
+    case OP_ADD: return direct_bf16<OP_ADD>(want, eb, s, dry);
+    case OP_SUB: return direct_bf16<OP_SUB>(want, eb, s, dry);
+    case OP_MUL: return direct_bf16<OP_MUL>(want, eb, s, dry);
+    default: return direct_bf16<OP_DIV>(want, eb, s, dry);
+  }
+}
+
+cudaError_t launch_copy_bf16(const EwBuild& eb, cudaStream_t s, bool dry) {
+  return launch_ew_bf16<CopyF, 1>(eb, s, dry);
+}
+
+cudaError_t launch_reduce_bf16(int op, int which, const RedBuild& rb, cudaStream_t s, bool dry) {
+  if (which == 2) return red_bf16<OP_ADD, 2>(rb, s, dry);
+  switch (op) {
+    case OP_ADD: return red_op_bf16<OP_ADD>(which, rb, s, dry);
+    case OP_SUB: return red_op_bf16<OP_SUB>(which, rb, s, dry);
+    case OP_MUL: return red_op_bf16<OP_MUL>(which, rb, s, dry);
+    default: return red_op_bf16<OP_DIV>(which, rb, s, dry);
+  }
+}
+
+}  // namespace zr

@@ -29,7 +29,7 @@ cudaError_t launch_chain_fwd_t(const FwdArg& f, cudaStream_t s) {
 
 cudaError_t launch_combine(const CombinePlan& c, cudaStream_t s) {
   const uint64_t nblk = (c.nout + c.jx - 1) / c.jx;
-  return launch_k(k_combine, static_cast<unsigned>(nblk), kThreads, 0, s, c);
+  return launch_k(k_combine<float>, static_cast<unsigned>(nblk), kThreads, 0, s, c);
 }
 
 template <int OP1, int OP2>

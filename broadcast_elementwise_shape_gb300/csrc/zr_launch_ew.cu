@@ -30,6 +30,7 @@ cudaError_t launch_direct_op(int want, const EwBuild& eb, cudaStream_t s, bool d
 }  // namespace
 
 cudaError_t launch_fwd(int op, const EwBuild& eb, cudaStream_t s, bool dry) {
+  if (eb.es == 2) return launch_fwd_bf16(op, eb, s, dry);
   switch (op) {
     case OP_ADD: return launch_ew_t<FwdF<OP_ADD>, 1>(eb, s, dry);
     case OP_SUB: return launch_ew_t<FwdF<OP_SUB>, 1>(eb, s, dry);
@@ -75,6 +76,7 @@ cudaError_t launch_fwd_tr(int op, const TrPlan& tp, cudaStream_t s, bool dry) {
 }
 
 cudaError_t launch_bwd_direct(int op, int want, const EwBuild& eb, cudaStream_t s, bool dry) {
+  if (eb.es == 2) return launch_bwd_direct_bf16(op, want, eb, s, dry);
   switch (op) {
     case OP_ADD: return launch_direct_op<OP_ADD>(want, eb, s, dry);
     case OP_SUB: return launch_direct_op<OP_SUB>(want, eb, s, dry);
@@ -84,6 +86,7 @@ cudaError_t launch_bwd_direct(int op, int want, const EwBuild& eb, cudaStream_t 
 }
 
 cudaError_t launch_copy(const EwBuild& eb, cudaStream_t s, bool dry) {
+  if (eb.es == 2) return launch_copy_bf16(eb, s, dry);
   return launch_ew_t<CopyF, 1>(eb, s, dry);
 }
 

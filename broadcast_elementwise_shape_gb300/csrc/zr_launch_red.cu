@@ -42,7 +42,7 @@ cudaError_t launch_red_t(const RedBuild& rb, cudaStream_t s, bool dry) {
   if (e != cudaSuccess || p.nslots <= 1) return e;
   const CombinePlan& c = rb.comb;
   const uint64_t nblk = (c.nout + c.jx - 1) / c.jx;
-  return launch_k(k_combine, static_cast<unsigned>(nblk), kThreads, 0, s, c);
+  return launch_k(k_combine<float>, static_cast<unsigned>(nblk), kThreads, 0, s, c);
 }
 
 template <int OP>
@@ -103,6 +103,7 @@ cudaError_t occupancy_red(int which, int* planned, int* actual) {
 }
 
 cudaError_t launch_reduce(int op, int which, const RedBuild& rb, cudaStream_t s, bool dry) {
+  if (rb.es == 2) return launch_reduce_bf16(op, which, rb, s, dry);
   if (which == 2) return launch_red_t<OP_ADD, 2>(rb, s, dry);
   switch (op) {
     case OP_ADD: return launch_red_op<OP_ADD>(which, rb, s, dry);

@@ -115,7 +115,8 @@ void fill_decomp(Decomp* dc, const Prob& P, const int* dims, int nd) {
 }
 
 // VEC = 4 is allowed when every slot that is read or written with unit inner
-// stride starts 16-byte aligned and every row start stays aligned.
+// stride starts aligned to 4 elements (16 bytes of float, 8 of bfloat16) and
+// every row start stays aligned.
 bool vec4_ok(const Prob& P, uint32_t slots, const void* const* ptrs) {
   const int n = P.n;
   if (P.size[n - 1] % 4 != 0) return false;
@@ -124,7 +125,7 @@ bool vec4_ok(const Prob& P, uint32_t slots, const void* const* ptrs) {
     if (!(slots & (1u << k))) continue;
     if (P.st[k][n - 1] != 1) continue;
     any_unit = true;
-    if (reinterpret_cast<uintptr_t>(ptrs[k]) % 16 != 0) return false;
+    if (reinterpret_cast<uintptr_t>(ptrs[k]) % uintptr_t(4 * P.es) != 0) return false;
     for (int d = 0; d < n - 1; ++d)
       if (P.st[k][d] % 4 != 0) return false;
   }
@@ -301,8 +302,9 @@ int build_ew(const Prob& P, const float* const in[3], float* const out[2], uint3
   const void* ptrs[kMaxOperands] = {in[0], in[1], in[2], out[0] ? out[0] : out[1]};
   uint32_t slots = read_mask | (1u << kSlotOut);
   bool v4 = vec4_ok(P, slots, ptrs);
-  if (v4 && out[0] && out[1] && reinterpret_cast<uintptr_t>(out[1]) % 16 != 0) v4 = false;
+  if (v4 && out[0] && out[1] && reinterpret_cast<uintptr_t>(out[1]) % uintptr_t(4 * P.es) != 0) v4 = false;
   eb->vec = v4 ? 4 : 1;
+  eb->es = P.es;
 
   const uint64_t nvcol = ceil_div(ncol, eb->vec);
   const uint64_t items = nrow * nvcol;
@@ -384,7 +386,8 @@ int build_red(const Prob& P, int xslot, const float* g, const float* a, const fl
   const void* ptrs[kMaxOperands] = {g, a, b, d_out};
   uint32_t slots = (read_mask & 7u) | (d_out ? (1u << kSlotOut) : 0u);
   bool v4 = vec4_ok(P, slots, ptrs);
-  if (v4 && p.inner_kept && reinterpret_cast<uintptr_t>(x_out) % 16 != 0) v4 = false;
+  if (v4 && p.inner_kept && reinterpret_cast<uintptr_t>(x_out) % uintptr_t(4 * P.es) != 0) v4 = false;
+  rb->es = P.es;
   // The reduced gradient's kept outer strides are multiples of ncol, so its
   // rows stay aligned; the workspace is 16-byte aligned by contract.
   rb->vec = vec_override ? vec_override : (v4 ? 4 : 1);

@@ -41,6 +41,7 @@ struct Prob {
   int64_t size[kMaxDims] = {};
   int64_t st[kProbSlots][kMaxDims] = {};
   uint32_t active = 0;  // bit k: slot k takes part
+  int es = 4;           // bytes per stored element: 4 (float) or 2 (bfloat16)
 };
 
 // Strides of x against an output of rank n: 0 where x is missing or 1.
@@ -57,6 +58,7 @@ int coalesce(int n, const int64_t* size, const int64_t (*st)[kMaxDims], uint32_t
 struct EwBuild {
   EwPlan plan;
   int vec;
+  int es;  // bytes per stored element (Prob::es)
 };
 // Elementwise plan over P with input slots 0..2 and output slot 3.
 // occ: resident CTAs per SM of the kernel that will run the plan.
@@ -71,7 +73,8 @@ struct RedBuild {
   RedPlan plan;
   CombinePlan comb;
   int vec;
-  size_t ws_bytes;  // partial workspace (0 when nslots == 1)
+  size_t ws_bytes;  // partial workspace (0 when nslots == 1); partials are binary32
+  int es;           // bytes per stored element (Prob::es)
 };
 // Reduction plan over P for the gradient whose index map is slot `xslot`.
 // `d_out` (may be null) is written densely from slot 3 offsets.

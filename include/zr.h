@@ -70,7 +70,8 @@ typedef enum {
                             input or another output                           */
   ZR_ERR_DEVICE = -6,    /* pointer not addressable by the current device      */
   ZR_ERR_WORKSPACE = -7, /* workspace smaller than required                    */
-  ZR_ERR_CUDA = -8       /* a CUDA call or kernel launch failed                */
+  ZR_ERR_CUDA = -8,      /* a CUDA call or kernel launch failed                */
+  ZR_ERR_DTYPE = -9      /* unknown element type (the _t entry points)         */
 } zr_status;
 
 /*
@@ -319,6 +320,32 @@ int zr_unary_fwd(zr_unary op, float alpha, zr_tensor x, float* out, const int64_
  */
 int zr_unary_bwd(zr_unary op, float alpha, zr_tensor grad_out, zr_tensor x, float* grad_x,
                  const int64_t* grad_x_strides, zr_stream_t stream);
+
+/*
+ * Element types of the _t entry points below.  ZR_F32 is binary32 (the
+ * entry points above).  ZR_BF16 is bfloat16 storage: every operand and
+ * output is bf16 (2 bytes, strides still in elements), arithmetic is the
+ * binary32 arithmetic above, and each stored element is rounded once to bf16,
+ * to nearest with ties to even.  Because binary32 carries at least
+ * 2 * 8 + 2 significand bits, a forward element or a one-operation gradient
+ * equals the exact result rounded to bf16, bit for bit; a summed gradient is
+ * within 1e-5 * sum|terms| + 2^-8 * |its exact value| (the bf16 rounding).
+ * Partial sums in the workspace stay binary32, so the workspace protocol and
+ * sizes are those of the float entry points.  Same-layout in-place outputs,
+ * errors and asynchrony are as above; unknown dtype: ZR_ERR_DTYPE.
+ */
+typedef enum { ZR_F32 = 0, ZR_BF16 = 1 } zr_dtype;
+
+/* zr_binary_fwd on `dtype` storage. */
+int zr_binary_fwd_t(zr_dtype dtype, zr_op op, zr_tensor a, zr_tensor b, void* out,
+                    const int64_t* out_strides, zr_stream_t stream);
+/* zr_binary_bwd on `dtype` storage. */
+int zr_binary_bwd_t(zr_dtype dtype, zr_op op, zr_tensor grad_out, zr_tensor a, zr_tensor b,
+                    void* grad_a, void* grad_b, void* workspace, size_t* workspace_bytes,
+                    zr_stream_t stream);
+/* zr_sum_to_shape on `dtype` storage. */
+int zr_sum_to_shape_t(zr_dtype dtype, zr_tensor in, int32_t ndim_out, const int64_t* sizes_out,
+                      void* out, void* workspace, size_t* workspace_bytes, zr_stream_t stream);
 
 /* Static, human-readable name of a status code. */
 const char* zr_status_string(int status);

@@ -73,7 +73,7 @@ def test_exports_every_declared_symbol(L):
 
 
 def test_status_strings(L):
-    for code in range(0, -9, -1):
+    for code in range(0, -10, -1):
         assert L.zr_status_string(code).decode().startswith("ZR_")
 
 

@@ -1,0 +1,129 @@
+"""GPU parity of the bfloat16-storage entry points (zr_binary_fwd_t,
+zr_binary_bwd_t, zr_sum_to_shape_t with ZR_BF16) against the CPU oracle.
+
+The oracle reads the same bf16 values (as binary32), computes as for float
+storage and rounds every stored result once to bf16.  Forward outputs and
+one-operation gradients must be bit-identical; summed gradients within
+1e-5 * sum|terms| + 2^-8 * |value| per element (the last term is bf16's
+rounding).  Chained steps read the bf16 intermediate, as the GPU does.
+"""
+import numpy as np
+import pytest
+import torch
+
+import broadcast_elementwise_shape_gb300 as zr
+import oracle
+import workloads
+from parity import bitexact, to_gpu, within
+
+pytestmark = pytest.mark.gpu
+
+OPS = ["add", "sub", "mul", "div"]
+BINARY = ["c1", "c2", "c3", "c4", "c5a", "c5b", "x1"]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    zr.build()
+    zr.lib()
+
+
+def _bf(x):
+    """bf16-rounded copy of a float32 CPU tensor, keeping its strides."""
+    st = x.untyped_storage()
+    flat = torch.empty(0, dtype=x.dtype).set_(st, 0, (st.nbytes() // 4,), (1,))
+    r = torch.from_numpy(oracle.round_bf16(flat.numpy()))
+    return r.as_strided(x.shape, x.stride(), x.storage_offset())
+
+
+def _dev16(x):
+    """Device bf16 tensor with x's values (x already bf16-representable) and strides."""
+    st = x.untyped_storage()
+    flat = torch.empty(0, dtype=x.dtype).set_(st, 0, (st.nbytes() // 4,), (1,))
+    d = flat.to(torch.bfloat16).cuda()
+    return d.as_strided(x.shape, x.stride(), x.storage_offset())
+
+
+def _f32(t):
+    return t.float().cpu().numpy()
+
+
+def _check_grad(got, ref, sabs, exact, what):
+    if exact:
+        bitexact(got, ref, what)
+    else:
+        r64 = np.asarray(ref, np.float64)
+        within(got, ref, sabs + 2.0 ** -8 / 1e-5 * np.abs(r64), what)
+
+
+@pytest.mark.parametrize("name", BINARY)
+def test_bf16_workloads_small(name):
+    host = {k: _bf(v) for k, v in workloads.make_inputs(name, **workloads.small_dims(name)).items()}
+    gpu = {k: _dev16(v) for k, v in host.items()}
+    ref = dict(host)
+    for step in workloads.STEPS[name]:
+        if step[0] == "fwd":
+            _, op, an, bn, on = step
+            gpu[on] = zr.zr_binary_fwd(op, gpu[an], gpu[bn])
+            assert gpu[on].dtype == torch.bfloat16
+            ref[on] = torch.from_numpy(oracle.round_bf16(oracle.binary_fwd(op, ref[an], ref[bn])))
+            bitexact(_f32(gpu[on]), ref[on].numpy(), f"bf16 {name} fwd {op}")
+        else:
+            _, op, gn, an, bn, gan, gbn = step
+            ga, gb = zr.zr_binary_bwd(op, gpu[gn], gpu[an], gpu[bn])
+            ra, rb, sa, sb = oracle.binary_bwd(op, ref[gn], ref[an], ref[bn])
+            n_out = ref[gn].numel()
+            for w, got, r, sab in ((0, ga, ra, sa), (1, gb, rb, sb)):
+                reduced = r.size != n_out
+                exact = not reduced and not (op == "div" and w == 1)
+                _check_grad(_f32(got), oracle.round_bf16(r), sab, exact,
+                            f"bf16 {name} bwd {op} grad_{'ab'[w]}")
+            gpu[gan], gpu[gbn] = ga, gb
+            ref[gan] = torch.from_numpy(oracle.round_bf16(ra))
+            ref[gbn] = torch.from_numpy(oracle.round_bf16(rb))
+
+
+@pytest.mark.parametrize("op", OPS)
+def test_bf16_random_views(op):
+    rng = np.random.default_rng(1500 + OPS.index(op))
+    for it in range(40):
+        nd = int(rng.integers(1, 5))
+        out = tuple(int(v) for v in rng.integers(1, 9, nd))
+        sa = tuple(s if rng.random() < 0.7 else 1 for s in out)
+        sb = tuple(s if rng.random() < 0.5 else 1 for s in out)[int(rng.integers(0, nd)):]
+        # a: sometimes a transposed or offset view
+        base = torch.from_numpy(rng.standard_normal(int(np.prod(sa)) + 3).astype(np.float32))
+        off = int(rng.integers(0, 4))
+        a = base[off:off + int(np.prod(sa))].reshape(sa)
+        if nd >= 2 and rng.random() < 0.5:
+            a = torch.from_numpy(rng.standard_normal(sa[::-1]).astype(np.float32)).permute(
+                *reversed(range(nd)))
+        b = torch.from_numpy(rng.standard_normal(sb).astype(np.float32))
+        if op == "div":
+            b = torch.sign(b) * (0.5 + b.abs())
+        a, b = _bf(a), _bf(b)
+        g = _bf(torch.from_numpy(rng.standard_normal(np.broadcast_shapes(sa, sb)).astype(np.float32)))
+        out_gpu = zr.zr_binary_fwd(op, _dev16(a), _dev16(b))
+        bitexact(_f32(out_gpu), oracle.round_bf16(oracle.binary_fwd(op, a, b)), f"bf16 fwd {op} {sa} {sb}")
+        ga, gb = zr.zr_binary_bwd(op, _dev16(g), _dev16(a), _dev16(b))
+        ra, rb, s1, s2 = oracle.binary_bwd(op, g, a, b)
+        n_out = g.numel()
+        for w, got, r, sab in ((0, ga, ra, s1), (1, gb, rb, s2)):
+            exact = r.size == n_out and not (op == "div" and w == 1)
+            _check_grad(_f32(got), oracle.round_bf16(r), sab, exact, f"bf16 bwd {op} {sa} {sb} {w}")
+
+
+def test_bf16_sum_to_shape_and_mixed_types():
+    rng = np.random.default_rng(1600)
+    for shape, tgt in (((4096, 1024), (1024,)), ((64, 300, 256), (1, 300, 1)), ((33, 65), (33, 65)),
+                       (((1 << 20) + 3,), (1,))):
+        x = _bf(torch.from_numpy(rng.standard_normal(shape).astype(np.float32)))
+        got = zr.zr_sum_to_shape(_dev16(x), tgt)
+        assert got.dtype == torch.bfloat16
+        ref, sabs = oracle.sum_to_shape(x, tgt)
+        _check_grad(_f32(got), oracle.round_bf16(ref), sabs, int(np.prod(tgt)) == x.numel(),
+                    f"bf16 sum {shape}->{tgt}")
+    with pytest.raises(TypeError):
+        zr.zr_binary_fwd("add", torch.ones(4, device="cuda"), torch.ones(4, device="cuda", dtype=torch.bfloat16))
