@@ -132,29 +132,35 @@ def chain_reads(op1, op2):
     return ra, rb, rc
 
 
-def op_bytes(step, shapes):
-    """Algorithmic bytes of one op: read each input once, write each output once."""
+def op_bytes(step, shapes, es=4):
+    """Algorithmic bytes of one op: read each input once, write each output
+    once (es bytes per element)."""
+    return es * op_elems(step, shapes)
+
+
+def op_elems(step, shapes):
+    """Elements the op reads and writes (its algorithmic bytes / element size)."""
     if step[0] == "ufwd":
         _, op, alpha, xn, on = step
-        return 4 * (shapes[xn] + shapes[on])
+        return (shapes[xn] + shapes[on])
     if step[0] == "ubwd":
         _, op, alpha, gn, xn, gxn = step
-        return 4 * (shapes[gn] + (shapes[xn] if op == "gelu" else 0) + shapes[gxn])
+        return (shapes[gn] + (shapes[xn] if op == "gelu" else 0) + shapes[gxn])
     if step[0] == "cfwd":
         _, op1, op2, an, bn, cn, on = step
-        return 4 * (shapes[an] + shapes[bn] + shapes[cn] + shapes[on])
+        return (shapes[an] + shapes[bn] + shapes[cn] + shapes[on])
     if step[0] == "cbwd":
         _, op1, op2, gn, an, bn, cn, gan, gbn, gcn = step
         ra, rb, rc = chain_reads(op1, op2)
-        return 4 * (shapes[gn] + ra * shapes[an] + rb * shapes[bn] + rc * shapes[cn]
+        return (shapes[gn] + ra * shapes[an] + rb * shapes[bn] + rc * shapes[cn]
                     + shapes[gan] + shapes[gbn] + shapes[gcn])
     if step[0] == "fwd":
         _, op, an, bn, on = step
-        return 4 * (shapes[an] + shapes[bn] + shapes[on])
+        return (shapes[an] + shapes[bn] + shapes[on])
     _, op, gn, an, bn, gan, gbn = step
     reads_a = op in ("mul", "div")
     reads_b = op in ("mul", "div")
-    return 4 * (shapes[gn] + (shapes[an] if reads_a else 0) + (shapes[bn] if reads_b else 0)
+    return (shapes[gn] + (shapes[an] if reads_a else 0) + (shapes[bn] if reads_b else 0)
                 + shapes[gan] + shapes[gbn])
 
 
@@ -274,21 +280,24 @@ class Suite:
                                            ctypes.c_size_t]
         L.zr_test_describe_fwd.argtypes = [ctypes.c_int, ZrTensor, ZrTensor, ctypes.c_void_p,
                                            i64p, ctypes.c_char_p, ctypes.c_size_t]
+        self.es = {}
         for name in names:
             host = workloads.make_inputs(name, **(dims or {}))
             sizes, shapes = shape_table(name, host)
+            self.es[name] = 2 if name in workloads.BF16 else 4
+            dt = torch.bfloat16 if self.es[name] == 2 else torch.float32
             env = {}
             for k, v in host.items():
-                env[k] = self._to_dev(v)
+                env[k] = self._to_dev(v).to(dt)
             outs = []
             for step in workloads.STEPS[name]:
                 if step[0] in ("fwd", "cfwd", "ufwd", "ubwd"):
                     on = step[-1]
-                    env[on] = torch.empty(shapes[on], dtype=torch.float32, device=device)
+                    env[on] = torch.empty(shapes[on], dtype=dt, device=device)
                     outs.append(on)
                 else:
                     for gname in (step[7:10] if step[0] == "cbwd" else step[5:7]):
-                        env[gname] = torch.empty(shapes[gname], dtype=torch.float32, device=device)
+                        env[gname] = torch.empty(shapes[gname], dtype=dt, device=device)
                         outs.append(gname)
             self.host[name] = host
             self.dev[name] = env
@@ -385,7 +394,9 @@ class Suite:
         if step[0] in ("ufwd", "ubwd"):
             return self._prepare_unary(name, step, env, sizes, stream_of)
         opc = zr.OPS[step[1]]
-        nbytes = op_bytes(step, sizes)
+        es = self.es[name]
+        dtc = zr.ZR_BF16 if es == 2 else zr.ZR_F32
+        nbytes = op_bytes(step, sizes, es)
         if step[0] == "fwd":
             _, op, an, bn, on = step
             da, db = self._desc(env[an]), self._desc(env[bn])
@@ -393,12 +404,14 @@ class Suite:
             ost = zr._i64(out.stride())
             self._keep.append(ost)
             ptr = out.data_ptr()
-            buf = ctypes.create_string_buffer(2048)
-            assert L.zr_test_describe_fwd(opc, da, db, ptr, ost, buf, 2048) == 0
-            launches = 0 if json.loads(buf.value.decode()).get("kernel") == "none" else 1
+            launches = 1
+            if es == 4:  # the plan description hooks plan float storage
+                buf = ctypes.create_string_buffer(2048)
+                assert L.zr_test_describe_fwd(opc, da, db, ptr, ost, buf, 2048) == 0
+                launches = 0 if json.loads(buf.value.decode()).get("kernel") == "none" else 1
 
             def fn(da=da, db=db, ptr=ptr, ost=ost):
-                rc = L.zr_binary_fwd(opc, da, db, ptr, ost, stream_of())
+                rc = L.zr_binary_fwd_t(dtc, opc, da, db, ptr, ost, stream_of())
                 if rc:
                     raise zr.ZrError(rc, f"{name} fwd {op}")
             return (name, "fwd", op, nbytes, launches, fn, sizes[on])
@@ -406,23 +419,25 @@ class Suite:
         dg, da, db = self._desc(env[gn]), self._desc(env[an]), self._desc(env[bn])
         pa, pb = env[gan].data_ptr(), env[gbn].data_ptr()
         need = ctypes.c_size_t(0)
-        rc = L.zr_binary_bwd(opc, dg, da, db, pa, pb, None, ctypes.byref(need), None)
+        rc = L.zr_binary_bwd_t(dtc, opc, dg, da, db, pa, pb, None, ctypes.byref(need), None)
         assert rc == 0, rc
         ws = torch.empty(max(16, need.value), dtype=torch.uint8, device=self.device)
         self._keep.append(ws)
-        buf = ctypes.create_string_buffer(8192)
-        assert L.zr_test_describe_bwd(opc, dg, da, db, pa, pb, buf, 8192) == 0
-        desc = json.loads(buf.value.decode())
-        plans = desc.get("plans", [])
-        if plans and plans[0].get("kernel") == "sab":
-            launches = 3  # fused pass + one combine per gradient
-        else:
-            launches = sum(1 + (p.get("nslots", 1) > 1) for p in plans)
+        launches = 0
+        if es == 4:
+            buf = ctypes.create_string_buffer(8192)
+            assert L.zr_test_describe_bwd(opc, dg, da, db, pa, pb, buf, 8192) == 0
+            desc = json.loads(buf.value.decode())
+            plans = desc.get("plans", [])
+            if plans and plans[0].get("kernel") == "sab":
+                launches = 3  # fused pass + one combine per gradient
+            else:
+                launches = sum(1 + (p.get("nslots", 1) > 1) for p in plans)
         wsz = ws.numel()
 
         def fn(dg=dg, da=da, db=db, pa=pa, pb=pb, wsp=ws.data_ptr(), wsz=wsz):
             n = ctypes.c_size_t(wsz)
-            rc = L.zr_binary_bwd(opc, dg, da, db, pa, pb, wsp, ctypes.byref(n), stream_of())
+            rc = L.zr_binary_bwd_t(dtc, opc, dg, da, db, pa, pb, wsp, ctypes.byref(n), stream_of())
             if rc:
                 raise zr.ZrError(rc, f"{name} bwd {op}")
         return (name, "bwd", op, nbytes, launches, fn, sizes[gn])
@@ -537,7 +552,7 @@ def run_zr(args, rank, world, local):
 
     per_config = per_op_alone = None
     if rank == 0 and args.config_reps > 0:
-        extra = [Suite(["x1", "c3f", "c4f", "u1"], device)] if args.workload == "suite" else []
+        extra = [Suite(["x1", "c3f", "c4f", "u1", "c4h"], device)] if args.workload == "suite" else []
         per_config, per_op_alone = run_per_config([suite] + extra, flush, stream, args.config_reps)
     e2e = None
     if not args.no_e2e and rank == 0:

@@ -1475,10 +1475,12 @@ int zr_test_dry_run_chain_bwd(zr_op op1, zr_op op2, zr_tensor grad_out, zr_tenso
 //
 // zr_binary_bwd_ex: each gradient may be strided and may be accumulated
 // into (AccumulateGrad, Autograd page, section 反向传播: when the gradient
-// slot already holds a value, the new gradient is added in place).  Dense
-// gradients are written (or added to) by the backward kernels themselves; a
-// strided gradient is computed densely into the workspace and then copied
-// (or added) into its layout by one elementwise pass.
+// slot already holds a value, the new gradient is added in place).  A dense,
+// written gradient is written by the backward kernels themselves.  A strided
+// or accumulated one is computed densely into the workspace and then copied
+// into its layout, or added to it (the elementwise add, in place: old +
+// staged, one binary32 addition), by one more elementwise pass; the backward
+// kernels themselves only ever store.
 
 namespace zr {
 namespace {
@@ -1489,7 +1491,7 @@ struct BwdExSet {
   bool stage[2] = {false, false};
   bool acc[2] = {false, false};
   TDesc gd[2];
-  EwBuild copy[2];
+  EwBuild copy[2];          // staged -> caller's layout: a copy, or (acc) old + staged
   size_t off_stage[2] = {0, 0};
   size_t off_ws = 0;
   size_t ws_run = 0, ws_query = 0;
@@ -1512,7 +1514,7 @@ int plan_bwd_ex(int op, const zr_tensor& tg, const zr_tensor& ta, const zr_tenso
     rc = read_tensor(t, &E->gd[w]);
     if (rc) return rc;
     if (!non_overlapping(E->gd[w])) return ZR_ERR_LAYOUT;
-    E->stage[w] = !dense_layout(E->gd[w]);
+    E->stage[w] = !dense_layout(E->gd[w]) || E->acc[w];
   }
   // A staged (strided) gradient is checked here against everything else;
   // dense ones are checked by the backward's own plan.
@@ -1545,40 +1547,31 @@ int plan_bwd_ex(int op, const zr_tensor& tg, const zr_tensor& ta, const zr_tenso
   rc = plan_bwd(op, tg, ta, tb, pg[0], pg[1], &E->S);
   if (rc) return rc;
   BwdSet& S = E->S;
-  // Accumulate flags of the gradients the kernels write in place.
-  const bool acc_k[2] = {E->acc[0] && !E->stage[0], E->acc[1] && !E->stage[1]};
-  if (S.direct) {
-    S.eb.plan.acc_mask = (acc_k[0] ? 1u : 0u) | (acc_k[1] ? 2u : 0u);
-  } else if (S.sab) {
-    S.sb.comb_a.accumulate = acc_k[0];
-    S.sb.comb_b.accumulate = acc_k[1];
-  } else {
-    for (int i = 0; i < S.nred; ++i) {
-      const int w = S.which[i];
-      S.rb[i].plan.acc_x = acc_k[w];
-      S.rb[i].comb.accumulate = acc_k[w];
-      S.rb[i].plan.acc_d = acc_k[1 - w];
-    }
-  }
-  // Copy (or add) each staged gradient into its layout.
+  // Move each staged gradient into its layout: copy it, or add it to the old
+  // values in place (slot 0: the old values in the caller's layout; slot 1:
+  // the staged gradient, dense; the output aliases slot 0 exactly).
   for (int w = 0; w < 2; ++w) {
     if (!E->stage[w] || E->gd[w].numel == 0) continue;
     const TDesc& x = E->gd[w];
+    const bool acc = E->acc[w];
     int64_t st[kProbSlots][kMaxDims] = {};
     int64_t dense[kMaxDims];
     contiguous_strides(x.nd, x.size, dense);
     for (int d = 0; d < x.nd; ++d) {
-      st[0][d] = x.size[d] == 1 ? 0 : dense[d];
-      st[kSlotOut][d] = x.size[d] == 1 ? 0 : x.stride[d];
+      const int64_t sd = x.size[d] == 1 ? 0 : dense[d];
+      const int64_t su = x.size[d] == 1 ? 0 : x.stride[d];
+      st[0][d] = acc ? su : sd;
+      st[1][d] = acc ? sd : 0;
+      st[kSlotOut][d] = su;
     }
     Prob P;
-    rc = coalesce(x.nd, x.size, st, 1u | (1u << kSlotOut), kSlotOut, &P);
+    const uint32_t rmask = acc ? 3u : 1u;
+    rc = coalesce(x.nd, x.size, st, rmask | (1u << kSlotOut), kSlotOut, &P);
     if (rc) return rc;
-    const float* in[3] = {pg[w], nullptr, nullptr};
+    const float* in[3] = {acc ? E->user[w] : pg[w], acc ? pg[w] : nullptr, nullptr};
     float* outs[2] = {E->user[w], nullptr};
-    rc = build_ew(P, in, outs, 1u, 1u, kOccEwCopy, &E->copy[w]);
+    rc = build_ew(P, in, outs, rmask, rmask, acc ? kOccEwFwd : kOccEwCopy, &E->copy[w]);
     if (rc) return rc;
-    E->copy[w].plan.acc_mask = E->acc[w] ? 1u : 0u;
   }
   E->ws_run = E->off_ws + S.ws_run;
   E->ws_query = E->off_ws + S.ws_query;
@@ -1633,7 +1626,7 @@ int zr_binary_bwd_ex(zr_op op, zr_tensor grad_out, zr_tensor a, zr_tensor b, zr_
       if (!S.zero_ptr[w] || R.acc[w]) continue;
       if (cudaMemsetAsync(S.zero_ptr[w], 0, S.zero_bytes[w], st) != cudaSuccess) return ZR_ERR_CUDA;
       if (R.stage[w]) {
-        rc = cuda_status(launch_copy(R.copy[w], st));
+        rc = cuda_status(launch_copy(R.copy[w], st));  // a written (not accumulated) gradient
         if (rc) return rc;
       }
     }
@@ -1643,7 +1636,7 @@ int zr_binary_bwd_ex(zr_op op, zr_tensor grad_out, zr_tensor a, zr_tensor b, zr_
   if (rc) return rc;
   for (int w = 0; w < 2; ++w) {
     if (!R.stage[w] || R.gd[w].numel == 0) continue;
-    rc = cuda_status(launch_copy(R.copy[w], st));
+    rc = cuda_status(R.acc[w] ? launch_fwd(OP_ADD, R.copy[w], st) : launch_copy(R.copy[w], st));
     if (rc) return rc;
   }
   return ZR_OK;

@@ -110,7 +110,6 @@ struct EwPlan {
   FastDiv tile_vcols_div;   // item -> (row in tile, column vector)
   uint32_t items_per_cta;   // tile_rows * tile_vcols
   uint32_t n_cta;
-  uint32_t acc_mask;        // bit k: out[k] += result (AccumulateGrad) instead of =
   float alpha;              // the unary ops' scalar (scale's factor)
 };
 
@@ -151,10 +150,11 @@ constexpr int kOccRedMulDiv = 3;  // k_reduce: mul, div
 // k_reduce, cluster variant (no second pass): loads per item are 1 for add,
 // sub and sum-to-shape, 2 for mul and div (the reduced gradient's own input
 // is loaded once per thread, the other one per item).  Items in flight per
-// thread: 8 with one load each, 4 with two.  Inner-reduced plans with one
-// load per item keep 4 CTAs per SM, the others 3.
+// thread: 4 (8 measured slower on c5a's backward, 26.7 against 22.8 us: it
+// spilled at the 64-register budget of 4 CTAs per SM).  Inner-reduced plans
+// with one load per item keep 4 CTAs per SM, the others 3.
 ZR_CX int red_cl_loads(int op) { return (op == OP_MUL || op == OP_DIV) ? 2 : 1; }
-ZR_CX int red_cl_unroll(int op) { return red_cl_loads(op) == 1 ? 8 : 4; }
+ZR_CX int red_cl_unroll(int) { return 4; }
 ZR_CX int red_cl_occ(int op, bool inner_kept) {
   return (!inner_kept && red_cl_loads(op) == 1) ? 4 : 3;
 }
@@ -231,7 +231,6 @@ struct RedPlan {
   // is a kept index, rank = row block * n_cblk + column block.
   uint32_t cluster;
   FastDiv cluster_div;
-  uint32_t acc_x, acc_d;    // X / the dense gradient: += result instead of =
 };
 
 struct RedCta {
@@ -358,7 +357,6 @@ struct CombinePlan {
   uint32_t nslots;
   uint32_t jx, sy;          // thread layout: jx outputs x sy slot lanes
   float scale;
-  uint32_t accumulate;      // outputs += result instead of =
 };
 
 }  // namespace zr

@@ -194,23 +194,6 @@ __device__ __forceinline__ void store_cols(E* __restrict__ base, int64_t row_off
   }
 }
 
-// Store, or with acc add to what is there first (one binary32 addition per
-// element: AccumulateGrad's in-place sum, Autograd page, section 反向传播).
-template <int VEC, class E>
-__device__ __forceinline__ void put_cols(E* __restrict__ base, int64_t row_off, int64_t inner,
-                                         uint32_t c, Vec<VEC> x, bool acc) {
-  if (acc) {
-    const Vec<VEC> old = load_cols<VEC>(base, row_off, inner, c, false);
-#pragma unroll
-    for (int i = 0; i < VEC; ++i) x.v[i] = __fadd_rn(old.v[i], x.v[i]);
-  }
-  store_cols<VEC>(base, row_off, inner, c, x);
-}
-template <class E>
-__device__ __forceinline__ void put1(E* p, float v, bool acc) {
-  st1(p, acc ? __fadd_rn(ld1(p, false), v) : v);
-}
-
 // ---------------------------------------------------------------- functors
 
 // Forward: out = a op b.
@@ -416,9 +399,8 @@ k_elementwise(const __grid_constant__ EwPlan p) {
       if (!ok[u]) continue;
       Vec<VEC> y[2];
       f(x[u], y, p.alpha);
-      if (out0) put_cols<VEC>(out0, doff[u], p.inner_stride[kSlotOut], col[u], y[0], p.acc_mask & 1);
-      if (NOUT > 1 && out1)
-        put_cols<VEC>(out1, doff[u], p.inner_stride[kSlotOut], col[u], y[1], p.acc_mask & 2);
+      if (out0) store_cols<VEC>(out0, doff[u], p.inner_stride[kSlotOut], col[u], y[0]);
+      if (NOUT > 1 && out1) store_cols<VEC>(out1, doff[u], p.inner_stride[kSlotOut], col[u], y[1]);
     }
   }
 }
@@ -729,8 +711,8 @@ k_reduce(const __grid_constant__ RedPlan p) {
           if (has_d) dv.v[i] = T::d(gg, aa, bb);
         }
         if (has_d)
-          put_cols<VEC>(dE, s_off[ri[u] * kMaxOperands + kSlotOut], p.inner_stride[kSlotOut],
-                        cc[u], dv, p.acc_d);
+          store_cols<VEC>(dE, s_off[ri[u] * kMaxOperands + kSlotOut], p.inner_stride[kSlotOut],
+                          cc[u], dv);
       }
     }
   }
@@ -764,7 +746,7 @@ k_reduce(const __grid_constant__ RedPlan p) {
           float r = ld_cluster(s_red + v, 0);
           for (uint32_t k = 1; k < p.cluster; ++k) r = __fadd_rn(r, ld_cluster(s_red + v, k));
           if (T::kPost) r = __fmul_rn(r, T::post(ld1(bE + base[2] + int64_t(col) * p.inner_stride[2], false)));
-          put1(xE + uint64_t(cta.kidx) * p.ncol + col, __fmul_rn(r, p.scale), p.acc_x);
+          st1(xE + uint64_t(cta.kidx) * p.ncol + col, __fmul_rn(r, p.scale));
         }
       }
       cluster_sync();
@@ -784,7 +766,7 @@ k_reduce(const __grid_constant__ RedPlan p) {
       if (p.nslots == 1) {
 #pragma unroll
         for (int i = 0; i < VEC; ++i) r.v[i] = __fmul_rn(r.v[i], p.scale);
-        put_cols<VEC>(xE + j, 0, 1, 0, r, p.acc_x);
+        store_cols<VEC>(xE + j, 0, 1, 0, r);
       } else {
         store_cols<VEC>(p.partial + uint64_t(cta.rblk) * p.nout + j, 0, 1, 0, r);
       }
@@ -803,7 +785,7 @@ k_reduce(const __grid_constant__ RedPlan p) {
         float r = ld_cluster(s_red, 0);
         for (uint32_t k = 1; k < p.cluster; ++k) r = __fadd_rn(r, ld_cluster(s_red, k));
         if (T::kPost) r = __fmul_rn(r, T::post(ld1(bE + base[2], false)));
-        put1(xE + cta.kidx, __fmul_rn(r, p.scale), p.acc_x);
+        st1(xE + cta.kidx, __fmul_rn(r, p.scale));
       }
       cluster_sync();
       return;
@@ -812,7 +794,7 @@ k_reduce(const __grid_constant__ RedPlan p) {
       float r = s_red[0];
       if (T::kPost) r = __fmul_rn(r, T::post(ld1(bE + base[2], false)));
       if (p.nslots == 1) {
-        put1(xE + cta.kidx, __fmul_rn(r, p.scale), p.acc_x);
+        st1(xE + cta.kidx, __fmul_rn(r, p.scale));
       } else {
         const uint64_t slot = uint64_t(cta.rblk) * p.n_cblk + cta.cblk;
         p.partial[slot * p.nout + cta.kidx] = r;
@@ -860,7 +842,7 @@ k_combine(const __grid_constant__ CombinePlan p) {
     const float v = __fmul_rn(s_red[jl], p.scale);
     E* out = reinterpret_cast<E*>(p.out);
     E* out2 = reinterpret_cast<E*>(p.out2);
-    put1(j < p.split ? out + j : out2 + (j - p.split), v, p.accumulate);
+    st1(j < p.split ? out + j : out2 + (j - p.split), v);
   }
 }
 

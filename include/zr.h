@@ -221,11 +221,11 @@ typedef struct {
  * zr_binary_bwd_ex — zr_binary_bwd with a layout and a write mode per
  * gradient (zr_grad).  Results, numerics and the workspace protocol are
  * those of zr_binary_bwd; with accumulate, each element becomes
- * old + (the value zr_binary_bwd would write), rounded once.  Dense
- * gradients are written (or added to) by the backward's own kernels; a
- * strided gradient is formed densely in the workspace and copied (or added)
- * into its layout by one more pass, so the workspace query includes numel
- * floats for it.  Layout errors (ZR_ERR_LAYOUT): a gradient that overlaps
+ * old + (the value zr_binary_bwd would write), rounded once.  A dense,
+ * written gradient is written by the backward's own kernels; a strided or
+ * accumulated gradient is formed densely in the workspace and then copied
+ * into its layout, or added to the values there, by one more elementwise
+ * pass, so the workspace query includes numel floats for it.  Layout errors (ZR_ERR_LAYOUT): a gradient that overlaps
  * itself, the other gradient or any input.  When grad_out is empty, written
  * gradients become zero and accumulated ones keep their values.
  */

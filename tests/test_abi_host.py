@@ -551,16 +551,20 @@ def test_chain_errors_before_any_device_access(L):
 
 def test_backward_ex_layout_errors_and_query(L):
     """zr_binary_bwd_ex: gradients that overlap themselves or an input are
-    refused before any device access; a strided gradient adds its staging
-    buffer to the workspace query."""
+    refused before any device access; a strided or accumulated gradient adds
+    its staging buffer to the workspace query."""
     from broadcast_elementwise_shape_gb300 import ZrGrad
     T = 1 << 40
     g, x, bias = FakeT(T, (64, 256)), FakeT(2 * T, (64, 256)), FakeT(3 * T, (256,))
     nb = ctypes.c_size_t(0)
     dense = ZrGrad(4 * T, None, 0)
-    assert L.zr_binary_bwd_ex(0, g.desc, x.desc, bias.desc, dense, ZrGrad(5 * T, None, 1), None,
+    assert L.zr_binary_bwd_ex(0, g.desc, x.desc, bias.desc, dense, ZrGrad(5 * T, None, 0), None,
                               ctypes.byref(nb), None) == 0
     q_dense = nb.value
+    # An accumulated gradient is staged too (then added in place).
+    assert L.zr_binary_bwd_ex(0, g.desc, x.desc, bias.desc, dense, ZrGrad(5 * T, None, 1), None,
+                              ctypes.byref(nb), None) == 0
+    assert nb.value >= q_dense + 4 * 256
     # grad_a as a transposed view of a [256, 64] buffer: staged.
     st = _i64([1, 64])
     assert L.zr_binary_bwd_ex(0, g.desc, x.desc, bias.desc, ZrGrad(4 * T, st, 1),

@@ -28,6 +28,8 @@ cases with the same structure):
 * ``u1`` unary ops on an FFN hidden activation, x [R,C] N(0,1), g N(0,1)
   (16384, 3072): GeLU forward and backward, then scale by 0.125 forward and
   backward (supplementary, outside the benchmark step)
+* ``c4h``: ``c4`` with every tensor stored as bfloat16 (the same draws,
+  rounded to bf16 by the caller; see ``BF16``), supplementary
 * ``c3f`` and ``c4f``: the inputs of ``c3`` and ``c4`` (same seeds and
   sizes), run as one fused two-op chain each, (x * gamma) + beta and
   (scores + mask) / scalar (supplementary, outside the benchmark step)
@@ -46,8 +48,10 @@ import torch
 
 SEEDS = {"c1": 1001, "c2": 1002, "c3": 1003, "c4": 1004, "c5a": 1005, "c5b": 1006, "x1": 1007,
          "u1": 1008}
-# Fused-chain workloads draw the inputs of the workload they fuse.
-BASE = {"c3f": "c3", "c4f": "c4"}
+# Fused-chain and bf16 workloads draw the inputs of the workload they derive from.
+BASE = {"c3f": "c3", "c4f": "c4", "c4h": "c4"}
+# Workloads whose tensors are stored as bfloat16.
+BF16 = {"c4h"}
 
 DEFAULT_DIMS = {
     "c1": dict(P=32, M=64, Q=128),
@@ -84,6 +88,10 @@ STEPS = {
            ("ufwd", "scale", 0.125, "x", "s"),
            ("ubwd", "scale", 0.125, "g", "x", "grad_s"),
            ("ubwd", "gelu", 1.0, "g", "x", "grad_x")],
+    "c4h": [("fwd", "add", "scores", "mask", "t"),
+            ("fwd", "div", "t", "scalar", "out"),
+            ("bwd", "div", "g", "t", "scalar", "grad_t", "grad_scalar"),
+            ("bwd", "add", "grad_t", "scores", "mask", "grad_scores", "grad_mask")],
     "c3f": [("cfwd", "mul", "add", "x", "gamma", "beta", "y2"),
             ("cbwd", "mul", "add", "g", "x", "gamma", "beta", "grad_x", "grad_gamma", "grad_beta")],
     "c4f": [("cfwd", "add", "div", "scores", "mask", "scalar", "out"),
@@ -190,6 +198,7 @@ def small_dims(name: str) -> dict:
         "c5b": dict(a=(3, 1, 5, 1, 4, 1, 7, 12), b=(1, 2, 1, 3, 1, 5, 1, 12)),
         "x1": dict(R=333, C=1030),
         "u1": dict(R=97, C=1031),
+        "c4h": dict(N=2, H=3, T=132),
         "c3f": dict(B=3, T=97, C=772),
         # 132 columns: 16-byte vectors, so the fused one-pass backward runs.
         "c4f": dict(N=2, H=3, T=132),
