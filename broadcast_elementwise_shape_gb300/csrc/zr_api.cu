@@ -318,7 +318,8 @@ int plan_bwd(int op, const zr_tensor& tg, const zr_tensor& ta, const zr_tensor& 
                    stream_mask & rm, xo, d_out, 0, occ, ock, ocr, &rb);
     if (rc) return rc;
     size_t q = rb.ws_bytes;
-    for (int v : {1, 4}) {
+    for (int v : {1, 4, 8}) {
+      if (v == 8 && S->es != 2) continue;  // 8-wide vectors: bfloat16 only
       RedBuild tmp;
       rc = build_red(P, xslot, S->g.ptr, nullptr, nullptr, rm, 0, xo, d_out, v, occ, ock, ocr,
                      &tmp);
@@ -415,7 +416,8 @@ int plan_sum(const zr_tensor& tin, int32_t ndo, const int64_t* so, float* out, S
                  ock, ocr, &S->rb);
   if (rc) return rc;
   S->ws_query = S->rb.ws_bytes;
-  for (int v : {1, 4}) {
+  for (int v : {1, 4, 8}) {
+    if (v == 8 && S->es != 2) continue;  // 8-wide vectors: bfloat16 only
     RedBuild tmp;
     rc = build_red(P, kSlotXA, S->in.ptr, nullptr, nullptr, 1u, 0, out, nullptr, v, kOccRedAddSub,
                    ock, ocr, &tmp);

@@ -158,6 +158,9 @@ ZR_CX int red_cl_unroll(int) { return 4; }
 ZR_CX int red_cl_occ(int op, bool inner_kept) {
   return (!inner_kept && red_cl_loads(op) == 1) ? 4 : 3;
 }
+// CTAs per SM of the 8-wide bfloat16 instantiations (a vector is 8 values,
+// so the same unroll needs more registers): one fewer, or two from 4.
+ZR_CX int wide_occ(int occ) { return occ >= 4 ? 3 : 2; }
 constexpr uint32_t kMaxCluster = 8;   // CTAs per cluster (the portable limit)
 // CTAs of a cluster plan that can be resident at once, out of a full wave of
 // `wave` CTAs: clusters must fit within one GPC, which strands slots as the

@@ -136,6 +136,58 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
          (uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(hi))) << 16);
 }
 
+// What a thread holds between issuing a load and using it: the binary32
+// values themselves for float storage; for bfloat16 the packed 16-bit
+// patterns, two per 32-bit word, so that a 16-byte load of 8 elements takes
+// 4 registers (not 8) until the values are used.
+template <class E, int VEC>
+struct Raw { Vec<VEC> x; };
+template <int VEC>
+struct Raw<__nv_bfloat16, VEC> { uint32_t w[(VEC + 1) / 2]; };
+
+template <int VEC>
+__device__ __forceinline__ Raw<__nv_bfloat16, VEC> load_raw_bf16(const __nv_bfloat16* base,
+                                                                  int64_t row_off, int64_t inner,
+                                                                  uint32_t c, bool streaming) {
+  Raw<__nv_bfloat16, VEC> r;
+  const unsigned short* b = reinterpret_cast<const unsigned short*>(base);
+  if (inner == 1) {
+    const unsigned short* p = b + row_off + c;
+    if constexpr (VEC == 8) {
+      const uint4 q = streaming ? __ldcs(reinterpret_cast<const uint4*>(p))
+                                : __ldg(reinterpret_cast<const uint4*>(p));
+      r.w[0] = q.x; r.w[1] = q.y; r.w[2] = q.z; r.w[3] = q.w;
+    } else if constexpr (VEC == 4) {
+      const uint2 q = streaming ? __ldcs(reinterpret_cast<const uint2*>(p))
+                                : __ldg(reinterpret_cast<const uint2*>(p));
+      r.w[0] = q.x; r.w[1] = q.y;
+    } else {
+      r.w[0] = streaming ? __ldcs(p) : __ldg(p);
+    }
+  } else if (inner == 0) {
+    const uint32_t u = __ldg(b + row_off);
+#pragma unroll
+    for (int i = 0; i < (VEC + 1) / 2; ++i) r.w[i] = u | (u << 16);
+  } else {
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) {
+      const uint32_t u = __ldg(b + row_off + int64_t(c + i) * inner);
+      if (i & 1) r.w[i / 2] |= u << 16;
+      else r.w[i / 2] = u;
+    }
+  }
+  return r;
+}
+
+template <int VEC>
+__device__ __forceinline__ Vec<VEC> unpack_bf16(const Raw<__nv_bfloat16, VEC>& r) {
+  Vec<VEC> v;
+#pragma unroll
+  for (int i = 0; i < VEC; ++i)
+    v.v[i] = __uint_as_float((i & 1) ? (r.w[i / 2] & 0xFFFF0000u) : (r.w[i / 2] << 16));
+  return v;
+}
+
 // Load VEC consecutive columns of one operand in one row.  inner == 1:
 // contiguous (one 16-byte load of 4 floats or one 8-byte load of 4 bf16 when
 // VEC == 4; the planner guarantees alignment); inner == 0: the column is
@@ -143,23 +195,21 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 template <int VEC, class E>
 __device__ __forceinline__ Vec<VEC> load_cols(const E* __restrict__ base, int64_t row_off,
                                               int64_t inner, uint32_t c, bool streaming) {
+  if constexpr (sizeof(E) == 2) {
+    return unpack_bf16<VEC>(load_raw_bf16<VEC>(base, row_off, inner, c, streaming));
+  }
   Vec<VEC> r;
   if (inner == 1) {
     const E* p = base + row_off + c;
-    if (VEC == 4) {
-      if constexpr (sizeof(E) == 4) {
-        const float4 q = streaming ? __ldcs(reinterpret_cast<const float4*>(p))
-                                   : __ldg(reinterpret_cast<const float4*>(p));
-        r.v[0] = q.x; r.v[1] = q.y; r.v[2] = q.z; r.v[VEC - 1] = q.w;
-      } else {
-        const uint2 q = streaming ? __ldcs(reinterpret_cast<const uint2*>(p))
-                                  : __ldg(reinterpret_cast<const uint2*>(p));
-        r.v[0] = __uint_as_float(q.x << 16);
-        r.v[1] = __uint_as_float(q.x & 0xFFFF0000u);
-        r.v[2] = __uint_as_float(q.y << 16);
-        r.v[VEC - 1] = __uint_as_float(q.y & 0xFFFF0000u);
+    if constexpr (VEC % 4 == 0) {
+#pragma unroll
+      for (int k = 0; k < VEC; k += 4) {
+        const float4 q = streaming ? __ldcs(reinterpret_cast<const float4*>(p + k))
+                                   : __ldg(reinterpret_cast<const float4*>(p + k));
+        r.v[k] = q.x; r.v[k + 1] = q.y; r.v[k + 2] = q.z; r.v[k + 3] = q.w;
       }
     } else {
+      static_assert(VEC == 1, "vector width");
       r.v[0] = ld1(p, streaming);
     }
   } else if (inner == 0) {
@@ -174,18 +224,40 @@ __device__ __forceinline__ Vec<VEC> load_cols(const E* __restrict__ base, int64_
 }
 
 template <int VEC, class E>
+__device__ __forceinline__ Raw<E, VEC> load_raw(const E* __restrict__ base, int64_t row_off,
+                                                int64_t inner, uint32_t c, bool streaming) {
+  if constexpr (sizeof(E) == 2) {
+    return load_raw_bf16<VEC>(base, row_off, inner, c, streaming);
+  } else {
+    Raw<E, VEC> r;
+    r.x = load_cols<VEC>(base, row_off, inner, c, streaming);
+    return r;
+  }
+}
+template <int VEC, class E>
+__device__ __forceinline__ Vec<VEC> unpack(const Raw<E, VEC>& r) {
+  if constexpr (sizeof(E) == 2) return unpack_bf16<VEC>(r);
+  else return r.x;
+}
+
+template <int VEC, class E>
 __device__ __forceinline__ void store_cols(E* __restrict__ base, int64_t row_off, int64_t inner,
                                            uint32_t c, const Vec<VEC>& x) {
   if (inner == 1) {
     E* p = base + row_off + c;
-    if (VEC == 4) {
-      if constexpr (sizeof(E) == 4) {
-        *reinterpret_cast<float4*>(p) = make_float4(x.v[0], x.v[1], x.v[2], x.v[VEC - 1]);
-      } else {
-        *reinterpret_cast<uint2*>(p) = make_uint2(pack_bf16x2(x.v[0], x.v[1]),
-                                                  pack_bf16x2(x.v[2], x.v[VEC - 1]));
-      }
+    if constexpr (sizeof(E) == 4 && VEC % 4 == 0) {
+      // 16-byte stores of 4 floats (binary32 partial slots of an 8-wide
+      // bfloat16 reduction take two).
+#pragma unroll
+      for (int k = 0; k < VEC; k += 4)
+        *reinterpret_cast<float4*>(p + k) = make_float4(x.v[k], x.v[k + 1], x.v[k + 2], x.v[k + 3]);
+    } else if constexpr (sizeof(E) == 2 && VEC == 8) {
+      *reinterpret_cast<uint4*>(p) = make_uint4(pack_bf16x2(x.v[0], x.v[1]), pack_bf16x2(x.v[2], x.v[3]),
+                                                pack_bf16x2(x.v[4], x.v[5]), pack_bf16x2(x.v[6], x.v[7]));
+    } else if constexpr (sizeof(E) == 2 && VEC == 4) {
+      *reinterpret_cast<uint2*>(p) = make_uint2(pack_bf16x2(x.v[0], x.v[1]), pack_bf16x2(x.v[2], x.v[3]));
     } else {
+      static_assert(VEC == 1, "vector width");
       st1(p, x.v[0]);
     }
   } else {
@@ -344,7 +416,7 @@ struct Uniform2<F, decltype(void(F::kUniform2))> { static constexpr bool value =
 // threadIdx.x + k * 256; items are processed in batches of U so that U
 // independent loads per operand are in flight before any result is stored.
 template <class F, int VEC, int NOUT, class E = float>
-__global__ void __launch_bounds__(kThreads, F::kMinBlocks)
+__global__ void __launch_bounds__(kThreads, VEC == 8 ? wide_occ(F::kMinBlocks) : F::kMinBlocks)
 k_elementwise(const __grid_constant__ EwPlan p) {
   pdl_trigger();
   const E* in0 = reinterpret_cast<const E*>(p.in[0]);
@@ -369,7 +441,7 @@ k_elementwise(const __grid_constant__ EwPlan p) {
   constexpr int U = 4;
   const F f;
   for (uint32_t it0 = 0; it0 < p.items_per_cta; it0 += U * blockDim.x) {
-    Vec<VEC> x[U][3];
+    Raw<E, VEC> xr[U][3];
     int64_t doff[U];
     uint32_t col[U];
     bool ok[U];
@@ -383,22 +455,26 @@ k_elementwise(const __grid_constant__ EwPlan p) {
       doff[u] = 0;
       if (ok[u]) {
         const int64_t* ro = s_off + ri * kMaxOperands;
-        x[u][0] = load_cols<VEC>(in0, ro[0], p.inner_stride[0], col[u], p.stream_mask & 1);
-        if (F::kR1) x[u][1] = load_cols<VEC>(in1, ro[1], p.inner_stride[1], col[u], p.stream_mask & 2);
-        if (F::kR2 && kUni2) {
-#pragma unroll
-          for (int i = 0; i < VEC; ++i) x[u][2].v[i] = uni2;
-        } else if (F::kR2) {
-          x[u][2] = load_cols<VEC>(in2, ro[2], p.inner_stride[2], col[u], p.stream_mask & 4);
-        }
+        xr[u][0] = load_raw<VEC>(in0, ro[0], p.inner_stride[0], col[u], p.stream_mask & 1);
+        if (F::kR1) xr[u][1] = load_raw<VEC>(in1, ro[1], p.inner_stride[1], col[u], p.stream_mask & 2);
+        if (F::kR2 && !kUni2)
+          xr[u][2] = load_raw<VEC>(in2, ro[2], p.inner_stride[2], col[u], p.stream_mask & 4);
         doff[u] = ro[kSlotOut];
       }
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       if (!ok[u]) continue;
-      Vec<VEC> y[2];
-      f(x[u], y, p.alpha);
+      Vec<VEC> x[3], y[2];
+      x[0] = unpack<VEC>(xr[u][0]);
+      if (F::kR1) x[1] = unpack<VEC>(xr[u][1]);
+      if (F::kR2 && kUni2) {
+#pragma unroll
+        for (int i = 0; i < VEC; ++i) x[2].v[i] = uni2;
+      } else if (F::kR2) {
+        x[2] = unpack<VEC>(xr[u][2]);
+      }
+      f(x, y, p.alpha);
       if (out0) store_cols<VEC>(out0, doff[u], p.inner_stride[kSlotOut], col[u], y[0]);
       if (NOUT > 1 && out1) store_cols<VEC>(out1, doff[u], p.inner_stride[kSlotOut], col[u], y[1]);
     }
@@ -601,8 +677,11 @@ struct RedTerms {
 template <int OP, int WHICH, int VEC, bool INNER_KEPT, bool CL = false, class E = float>
 __global__ void __launch_bounds__(kThreads,
                                   CL ? red_cl_occ(OP, INNER_KEPT)
-                                     : ((OP == OP_MUL || OP == OP_DIV) ? kOccRedMulDiv
-                                                                      : kOccRedAddSub))
+                                     : (VEC == 8 ? wide_occ((OP == OP_MUL || OP == OP_DIV)
+                                                                ? kOccRedMulDiv
+                                                                : kOccRedAddSub)
+                                                 : ((OP == OP_MUL || OP == OP_DIV) ? kOccRedMulDiv
+                                                                                  : kOccRedAddSub)))
 k_reduce(const __grid_constant__ RedPlan p) {
   pdl_trigger();
   // Operands and gradients in storage type E; partial slots are binary32.
@@ -679,7 +758,7 @@ k_reduce(const __grid_constant__ RedPlan p) {
     uint32_t rm = 0, cm = 0;
     constexpr int U = CL ? red_cl_unroll(OP) : 4;
     for (uint32_t m0 = 0; m0 < items; m0 += U) {
-      Vec<VEC> gv[U], av[U], bv[U];
+      Raw<E, VEC> gr[U], ar[U], br[U];
       uint32_t ri[U], cc[U];
       bool ok[U];
 #pragma unroll
@@ -689,23 +768,27 @@ k_reduce(const __grid_constant__ RedPlan p) {
         cc[u] = (vcol_begin + tx + cm * p.tx) * VEC;
         if (ok[u]) {
           const int64_t* ro = s_off + ri[u] * kMaxOperands;
-          gv[u] = load_cols<VEC>(gE, ro[0], p.inner_stride[0], cc[u], p.stream_mask & 1);
+          gr[u] = load_raw<VEC>(gE, ro[0], p.inner_stride[0], cc[u], p.stream_mask & 1);
           if ((T::kXa || T::kDa) && read_a && WHICH != 0)
-            av[u] = load_cols<VEC>(aE, ro[1], p.inner_stride[1], cc[u], p.stream_mask & 2);
+            ar[u] = load_raw<VEC>(aE, ro[1], p.inner_stride[1], cc[u], p.stream_mask & 2);
           if ((T::kXb || T::kDb) && read_b && WHICH != 1)
-            bv[u] = load_cols<VEC>(bE, ro[2], p.inner_stride[2], cc[u], p.stream_mask & 4);
+            br[u] = load_raw<VEC>(bE, ro[2], p.inner_stride[2], cc[u], p.stream_mask & 4);
           if (++cm == ncs) { cm = 0; ++rm; }
         }
       }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         if (!ok[u]) continue;
+        const Vec<VEC> gv = unpack<VEC>(gr[u]);
+        Vec<VEC> av, bv;
+        if ((T::kXa || T::kDa) && read_a && WHICH != 0) av = unpack<VEC>(ar[u]);
+        if ((T::kXb || T::kDb) && read_b && WHICH != 1) bv = unpack<VEC>(br[u]);
         Vec<VEC> dv;
 #pragma unroll
         for (int i = 0; i < VEC; ++i) {
-          const float gg = gv[u].v[i];
-          const float aa = ((T::kXa || T::kDa) && read_a) ? (WHICH == 0 ? own.v[i] : av[u].v[i]) : 0.f;
-          const float bb = ((T::kXb || T::kDb) && read_b) ? (WHICH == 1 ? own.v[i] : bv[u].v[i]) : 0.f;
+          const float gg = gv.v[i];
+          const float aa = ((T::kXa || T::kDa) && read_a) ? (WHICH == 0 ? own.v[i] : av.v[i]) : 0.f;
+          const float bb = ((T::kXb || T::kDb) && read_b) ? (WHICH == 1 ? own.v[i] : bv.v[i]) : 0.f;
           if (INNER_KEPT) acc[i].add_prod(gg, T::m(aa, bb));
           else acc[0].add_prod(gg, T::m(aa, bb));
           if (has_d) dv.v[i] = T::d(gg, aa, bb);

@@ -20,6 +20,8 @@ cudaError_t launch_ew_bf16(const EwBuild& eb, cudaStream_t s, bool dry) {
     return cudaErrorInvalidValue;
   if (dry) return cudaSuccess;
   const size_t smem = size_t(eb.plan.tile_rows) * kMaxOperands * sizeof(int64_t);
+  if (eb.vec == 8)
+    return launch_k(k_elementwise<F, 8, NOUT, bf16>, eb.plan.n_cta, kThreads, smem, s, eb.plan);
   if (eb.vec == 4)
     return launch_k(k_elementwise<F, 4, NOUT, bf16>, eb.plan.n_cta, kThreads, smem, s, eb.plan);
   return launch_k(k_elementwise<F, 1, NOUT, bf16>, eb.plan.n_cta, kThreads, smem, s, eb.plan);
@@ -48,11 +50,13 @@ cudaError_t red_bf16(const RedBuild& rb, cudaStream_t s, bool dry) {
   const size_t smem = size_t(table_rows) * kMaxOperands * sizeof(int64_t) + red_floats * sizeof(float);
   cudaError_t e;
   if (p.inner_kept) {
-    e = rb.vec == 4 ? launch_k(k_reduce<OP, WHICH, 4, true, false, bf16>, p.n_cta, kThreads, smem, s, p)
-                    : launch_k(k_reduce<OP, WHICH, 1, true, false, bf16>, p.n_cta, kThreads, smem, s, p);
+    e = rb.vec == 8   ? launch_k(k_reduce<OP, WHICH, 8, true, false, bf16>, p.n_cta, kThreads, smem, s, p)
+        : rb.vec == 4 ? launch_k(k_reduce<OP, WHICH, 4, true, false, bf16>, p.n_cta, kThreads, smem, s, p)
+                      : launch_k(k_reduce<OP, WHICH, 1, true, false, bf16>, p.n_cta, kThreads, smem, s, p);
   } else {
-    e = rb.vec == 4 ? launch_k(k_reduce<OP, WHICH, 4, false, false, bf16>, p.n_cta, kThreads, smem, s, p)
-                    : launch_k(k_reduce<OP, WHICH, 1, false, false, bf16>, p.n_cta, kThreads, smem, s, p);
+    e = rb.vec == 8   ? launch_k(k_reduce<OP, WHICH, 8, false, false, bf16>, p.n_cta, kThreads, smem, s, p)
+        : rb.vec == 4 ? launch_k(k_reduce<OP, WHICH, 4, false, false, bf16>, p.n_cta, kThreads, smem, s, p)
+                      : launch_k(k_reduce<OP, WHICH, 1, false, false, bf16>, p.n_cta, kThreads, smem, s, p);
   }
   if (e != cudaSuccess || p.nslots <= 1) return e;
   const CombinePlan& c = rb.comb;

@@ -114,22 +114,36 @@ void fill_decomp(Decomp* dc, const Prob& P, const int* dims, int nd) {
   }
 }
 
-// VEC = 4 is allowed when every slot that is read or written with unit inner
-// stride starts aligned to 4 elements (16 bytes of float, 8 of bfloat16) and
-// every row start stays aligned.
-bool vec4_ok(const Prob& P, uint32_t slots, const void* const* ptrs) {
+// VEC = V is allowed when the inner dim is a multiple of V and every slot
+// that is read or written with unit inner stride starts aligned to V elements
+// and every row start stays aligned.
+bool vec_ok(const Prob& P, int V, uint32_t slots, const void* const* ptrs) {
   const int n = P.n;
-  if (P.size[n - 1] % 4 != 0) return false;
+  if (P.size[n - 1] % V != 0) return false;
   bool any_unit = false;
   for (int k = 0; k < kMaxOperands; ++k) {
     if (!(slots & (1u << k))) continue;
     if (P.st[k][n - 1] != 1) continue;
     any_unit = true;
-    if (reinterpret_cast<uintptr_t>(ptrs[k]) % uintptr_t(4 * P.es) != 0) return false;
+    if (reinterpret_cast<uintptr_t>(ptrs[k]) % uintptr_t(V * P.es) != 0) return false;
     for (int d = 0; d < n - 1; ++d)
-      if (P.st[k][d] % 4 != 0) return false;
+      if (P.st[k][d] % V != 0) return false;
   }
   return any_unit;
+}
+
+// Elements per vector access: 16 bytes where alignment allows (4 floats or
+// 8 bfloat16), for bfloat16 else 8 bytes (4 elements), else one element.
+// extra: another pointer that must share the alignment (or null).
+int pick_vec(const Prob& P, uint32_t slots, const void* const* ptrs, const void* extra) {
+  const int cands[2] = {P.es == 2 ? 8 : 4, 4};
+  for (int i = 0; i < (P.es == 2 ? 2 : 1); ++i) {
+    const int V = cands[i];
+    if (vec_ok(P, V, slots, ptrs) &&
+        (!extra || reinterpret_cast<uintptr_t>(extra) % uintptr_t(V * P.es) == 0))
+      return V;
+  }
+  return 1;
 }
 
 }  // namespace
@@ -301,10 +315,9 @@ int build_ew(const Prob& P, const float* const in[3], float* const out[2], uint3
 
   const void* ptrs[kMaxOperands] = {in[0], in[1], in[2], out[0] ? out[0] : out[1]};
   uint32_t slots = read_mask | (1u << kSlotOut);
-  bool v4 = vec4_ok(P, slots, ptrs);
-  if (v4 && out[0] && out[1] && reinterpret_cast<uintptr_t>(out[1]) % uintptr_t(4 * P.es) != 0) v4 = false;
-  eb->vec = v4 ? 4 : 1;
+  eb->vec = pick_vec(P, slots, ptrs, out[0] && out[1] ? out[1] : nullptr);
   eb->es = P.es;
+  if (eb->vec == 8) occ = wide_occ(occ);
 
   const uint64_t nvcol = ceil_div(ncol, eb->vec);
   const uint64_t items = nrow * nvcol;
@@ -385,12 +398,13 @@ int build_red(const Prob& P, int xslot, const float* g, const float* a, const fl
 
   const void* ptrs[kMaxOperands] = {g, a, b, d_out};
   uint32_t slots = (read_mask & 7u) | (d_out ? (1u << kSlotOut) : 0u);
-  bool v4 = vec4_ok(P, slots, ptrs);
-  if (v4 && p.inner_kept && reinterpret_cast<uintptr_t>(x_out) % uintptr_t(4 * P.es) != 0) v4 = false;
   rb->es = P.es;
   // The reduced gradient's kept outer strides are multiples of ncol, so its
   // rows stay aligned; the workspace is 16-byte aligned by contract.
-  rb->vec = vec_override ? vec_override : (v4 ? 4 : 1);
+  rb->vec = vec_override ? vec_override
+                         : pick_vec(P, slots, ptrs, p.inner_kept ? static_cast<const void*>(x_out)
+                                                                 : nullptr);
+  if (rb->vec == 8) occ = wide_occ(occ);
   const uint32_t vec = uint32_t(rb->vec);
   const uint64_t nvcol = ceil_div(ncol, vec);
   p.nvcol = uint32_t(nvcol);
@@ -496,7 +510,7 @@ int build_red(const Prob& P, int xslot, const float* g, const float* a, const fl
                                           : ceil_div(n_red, rows) * ceil_div(nvcol, vcols);
   const uint64_t std_ctas = n_kept * ceil_div(n_red, rows) * ceil_div(nvcol, vcols);
   const int occ_cl = p.inner_kept ? occ_cl_kept : occ_cl_red;
-  if (occ_cl > 0 && vec == 4 && std_slots > 1) {
+  if (occ_cl > 0 && vec == 4 && P.es == 4 && std_slots > 1) {
     const uint64_t wave_cl = uint64_t(kSms) * uint64_t(occ_cl);
     // Inner dim kept: column lanes from the widest down to 8 (128-byte row
     // segments), tiles = kept index x column block; reduced: tiles = kept

@@ -329,7 +329,9 @@ int zr_unary_bwd(zr_unary op, float alpha, zr_tensor grad_out, zr_tensor x, floa
  * to nearest with ties to even.  Because binary32 carries at least
  * 2 * 8 + 2 significand bits, a forward element or a one-operation gradient
  * equals the exact result rounded to bf16, bit for bit; a summed gradient is
- * within 1e-5 * sum|terms| + 2^-8 * |its exact value| (the bf16 rounding).
+ * within 1e-5 * sum|terms| + 2^-7 * |its exact value| (one bf16 unit in the
+ * last place: the binary32 sum and the exact one may round to neighbouring
+ * bf16 values).
  * Partial sums in the workspace stay binary32, so the workspace protocol and
  * sizes are those of the float entry points.  Same-layout in-place outputs,
  * errors and asynchrony are as above; unknown dtype: ZR_ERR_DTYPE.

@@ -4,8 +4,11 @@ zr_binary_bwd_t, zr_sum_to_shape_t with ZR_BF16) against the CPU oracle.
 The oracle reads the same bf16 values (as binary32), computes as for float
 storage and rounds every stored result once to bf16.  Forward outputs and
 one-operation gradients must be bit-identical; summed gradients within
-1e-5 * sum|terms| + 2^-8 * |value| per element (the last term is bf16's
-rounding).  Chained steps read the bf16 intermediate, as the GPU does.
+1e-5 * sum|terms| + 2^-7 * |value| per element: a sum within the float
+tolerance can still round to the bf16 neighbour of the exact sum's rounding
+when the two fall on either side of a rounding boundary, one bf16 unit in
+the last place (at most 2^-7 of the value).  Chained steps read the bf16
+intermediate, as the GPU does.
 """
 import numpy as np
 import pytest
@@ -55,7 +58,7 @@ def _check_grad(got, ref, sabs, exact, what):
         bitexact(got, ref, what)
     else:
         r64 = np.asarray(ref, np.float64)
-        within(got, ref, sabs + 2.0 ** -8 / 1e-5 * np.abs(r64), what)
+        within(got, ref, sabs + 2.0 ** -7 / 1e-5 * np.abs(r64), what)
 
 
 @pytest.mark.parametrize("name", BINARY)
@@ -127,3 +130,28 @@ def test_bf16_sum_to_shape_and_mixed_types():
                     f"bf16 sum {shape}->{tgt}")
     with pytest.raises(TypeError):
         zr.zr_binary_fwd("add", torch.ones(4, device="cuda"), torch.ones(4, device="cuda", dtype=torch.bfloat16))
+
+
+WIDE = [((333, 1024), (1024,)), ((7, 40, 96), (1, 40, 1)), ((24, 1, 64), (1, 16, 64)),
+        ((2, 3, 136, 136), (1, 1, 136, 136)), ((64, 1000), (64, 1000))]
+
+
+@pytest.mark.parametrize("op", OPS)
+def test_bf16_wide_vectors(op):
+    """Shapes whose rows allow 16-byte bf16 vectors (8 elements), against
+    the oracle: forward bit-exact, gradients as above."""
+    rng = np.random.default_rng(1700 + OPS.index(op))
+    for sa, sb in WIDE:
+        a = _bf(torch.from_numpy(rng.standard_normal(sa).astype(np.float32)))
+        b = torch.from_numpy(rng.standard_normal(sb).astype(np.float32))
+        if op == "div":
+            b = torch.sign(b) * (0.5 + b.abs())
+        b = _bf(b)
+        g = _bf(torch.from_numpy(rng.standard_normal(np.broadcast_shapes(sa, sb)).astype(np.float32)))
+        out = zr.zr_binary_fwd(op, _dev16(a), _dev16(b))
+        bitexact(_f32(out), oracle.round_bf16(oracle.binary_fwd(op, a, b)), f"bf16 wide fwd {op} {sa} {sb}")
+        ga, gb = zr.zr_binary_bwd(op, _dev16(g), _dev16(a), _dev16(b))
+        ra, rb, s1, s2 = oracle.binary_bwd(op, g, a, b)
+        for w, got, r, sab in ((0, ga, ra, s1), (1, gb, rb, s2)):
+            exact = r.size == g.numel() and not (op == "div" and w == 1)
+            _check_grad(_f32(got), oracle.round_bf16(r), sab, exact, f"bf16 wide bwd {op} {sa} {sb} {w}")
