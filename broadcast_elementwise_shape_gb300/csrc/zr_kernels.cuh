@@ -273,6 +273,8 @@ template <int OP>
 struct FwdF {
   static constexpr bool kR1 = true, kR2 = false;  // slot 0 = a, slot 1 = b
   static constexpr int kMinBlocks = kOccEwFwd;  // CTAs per SM the register budget targets
+  // 8-wide bfloat16: IEEE division needs more registers than 4 CTAs allow.
+  static constexpr int kMinBlocksWide = OP == OP_DIV ? 3 : kOccEwFwd;
   template <int VEC>
   __device__ __forceinline__ void operator()(const Vec<VEC> (&x)[3], Vec<VEC> (&y)[2], float) const {
 #pragma unroll
@@ -287,6 +289,7 @@ struct BwdDirectF {
   static constexpr bool kR1 = ((WANT & 1) && Needs<OP, 0>::a) || ((WANT & 2) && Needs<OP, 1>::a);
   static constexpr bool kR2 = ((WANT & 1) && Needs<OP, 0>::b) || ((WANT & 2) && Needs<OP, 1>::b);
   static constexpr int kMinBlocks = kOccEwBwd;
+  static constexpr int kMinBlocksWide = (OP == OP_DIV && (WANT & 2)) ? 2 : kOccEwBwd;
   template <int VEC>
   __device__ __forceinline__ void operator()(const Vec<VEC> (&x)[3], Vec<VEC> (&y)[2], float) const {
 #pragma unroll
@@ -397,6 +400,7 @@ struct UnaryBwdF {
 struct CopyF {
   static constexpr bool kR1 = false, kR2 = false;
   static constexpr int kMinBlocks = kOccEwCopy;
+  static constexpr int kMinBlocksWide = kOccEwCopy;
   template <int VEC>
   __device__ __forceinline__ void operator()(const Vec<VEC> (&x)[3], Vec<VEC> (&y)[2], float) const {
     y[0] = x[0];
@@ -415,8 +419,14 @@ struct Uniform2<F, decltype(void(F::kUniform2))> { static constexpr bool value =
 // One CTA = one tile of rows x column vectors.  Each thread takes items
 // threadIdx.x + k * 256; items are processed in batches of U so that U
 // independent loads per operand are in flight before any result is stored.
+// CTAs per SM a functor's 8-wide (bfloat16) instantiation keeps.
+template <class F, class = void>
+struct WideBlocks { static constexpr int value = wide_occ(F::kMinBlocks); };
+template <class F>
+struct WideBlocks<F, decltype(void(F::kMinBlocksWide))> { static constexpr int value = F::kMinBlocksWide; };
+
 template <class F, int VEC, int NOUT, class E = float>
-__global__ void __launch_bounds__(kThreads, VEC == 8 ? wide_occ(F::kMinBlocks) : F::kMinBlocks)
+__global__ void __launch_bounds__(kThreads, VEC == 8 ? WideBlocks<F>::value : F::kMinBlocks)
 k_elementwise(const __grid_constant__ EwPlan p) {
   pdl_trigger();
   const E* in0 = reinterpret_cast<const E*>(p.in[0]);
@@ -677,9 +687,7 @@ struct RedTerms {
 template <int OP, int WHICH, int VEC, bool INNER_KEPT, bool CL = false, class E = float>
 __global__ void __launch_bounds__(kThreads,
                                   CL ? red_cl_occ(OP, INNER_KEPT)
-                                     : (VEC == 8 ? wide_occ((OP == OP_MUL || OP == OP_DIV)
-                                                                ? kOccRedMulDiv
-                                                                : kOccRedAddSub)
+                                     : (VEC == 8 ? red_wide_occ(OP, INNER_KEPT)
                                                  : ((OP == OP_MUL || OP == OP_DIV) ? kOccRedMulDiv
                                                                                   : kOccRedAddSub)))
 k_reduce(const __grid_constant__ RedPlan p) {

@@ -317,7 +317,9 @@ int build_ew(const Prob& P, const float* const in[3], float* const out[2], uint3
   uint32_t slots = read_mask | (1u << kSlotOut);
   eb->vec = pick_vec(P, slots, ptrs, out[0] && out[1] ? out[1] : nullptr);
   eb->es = P.es;
-  if (eb->vec == 8) occ = wide_occ(occ);
+  // 8-wide bfloat16 kernels keep the float budget except IEEE division (one
+  // CTA fewer); grids are sized with the float figure.
+
 
   const uint64_t nvcol = ceil_div(ncol, eb->vec);
   const uint64_t items = nrow * nvcol;
@@ -404,7 +406,9 @@ int build_red(const Prob& P, int xslot, const float* g, const float* a, const fl
   rb->vec = vec_override ? vec_override
                          : pick_vec(P, slots, ptrs, p.inner_kept ? static_cast<const void*>(x_out)
                                                                  : nullptr);
-  if (rb->vec == 8) occ = wide_occ(occ);
+  // 8-wide bfloat16 reductions with the inner dim kept run one CTA per SM
+  // fewer than the float kernel (red_wide_occ).
+  if (rb->vec == 8 && p.inner_kept) occ = wide_occ(occ);
   const uint32_t vec = uint32_t(rb->vec);
   const uint64_t nvcol = ceil_div(ncol, vec);
   p.nvcol = uint32_t(nvcol);
