@@ -273,8 +273,10 @@ template <int OP>
 struct FwdF {
   static constexpr bool kR1 = true, kR2 = false;  // slot 0 = a, slot 1 = b
   static constexpr int kMinBlocks = kOccEwFwd;  // CTAs per SM the register budget targets
-  // 8-wide bfloat16: IEEE division needs more registers than 4 CTAs allow.
-  static constexpr int kMinBlocksWide = OP == OP_DIV ? 3 : kOccEwFwd;
+  // 8-wide bfloat16 keeps 4 CTAs per SM even for IEEE division: its 36 bytes
+  // of spill cost less than the lost memory parallelism at 3 (c4 in bf16,
+  // forward div: 89 against 100 us).
+  static constexpr int kMinBlocksWide = kOccEwFwd;
   template <int VEC>
   __device__ __forceinline__ void operator()(const Vec<VEC> (&x)[3], Vec<VEC> (&y)[2], float) const {
 #pragma unroll

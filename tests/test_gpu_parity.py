@@ -540,11 +540,10 @@ def _log_uniform(rng, shape, lo=-60, hi=60):
 
 
 def test_division_is_ieee_bit_exact():
-    """The forward div computes each quotient from the divisor's reciprocal
-    with remainder corrections; it must equal IEEE division bit for bit
-    (any NaN matching any NaN), including every binade, subnormals,
-    infinities and zeros (random bit patterns) and the reciprocal reuse
-    across rows of a broadcast divisor."""
+    """Forward div, and the dense g/b gradient, must equal IEEE division bit
+    for bit (any NaN matching any NaN): every binade, subnormals, infinities
+    and zeros (random bit patterns), broadcast divisors, and divisors +-2^k
+    at the ends of the exponent range (2^-126, 2^127, the subnormal 2^-127)."""
     rng = np.random.default_rng(2024)
     cases = []
     cases.append((_rand_bits(rng, (4096, 256)), _rand_bits(rng, (256,))))         # row divisor
@@ -554,10 +553,23 @@ def test_division_is_ieee_bit_exact():
     cases.append((_log_uniform(rng, (1 << 20,), -126, 127), _log_uniform(rng, (1 << 20,), -126, 127)))
     for s in (8.0, 3.0, 1e-40, 3e38, -7.5, 0.0, float("inf")):
         cases.append((_log_uniform(rng, (1 << 18,), -80, 80), np.array([s], np.float32)))
+    for s in (2.0 ** -126, 2.0 ** 127, -(2.0 ** -126), 2.0 ** -127, 0.5, -1.0, 1.0, 2.0 ** 64, 0.125):
+        cases.append((_rand_bits(rng, (1 << 18,)), np.array([s], np.float32)))
+    pow2_rows = (np.float32(2.0) ** rng.integers(-126, 128, 256).astype(np.float32)) * np.sign(
+        rng.standard_normal(256)).astype(np.float32)
+    cases.append((_rand_bits(rng, (2048, 256)), pow2_rows.astype(np.float32)))
     for a, b in cases:
         ta, tb = torch.from_numpy(a), torch.from_numpy(b)
         got = zr.zr_binary_fwd("div", ta.cuda(), tb.cuda()).cpu().numpy()
         bitexact(got, oracle.binary_fwd("div", ta, tb), f"div {a.shape} / {b.shape}")
+        if b.size > 1 and b.size == a.size:
+            continue
+        # The dense gradient g / b of the same division (b broadcast: grad_b
+        # is a sum, compared elsewhere).
+        g = torch.from_numpy(_rand_bits(rng, a.shape))
+        ga, _ = zr.zr_binary_bwd("div", g.cuda(), ta.cuda(), tb.cuda(), want_b=False)
+        ra, _, _, _ = oracle.binary_bwd("div", g, ta, tb, want_b=False)
+        bitexact(ga.cpu().numpy(), ra, f"div grad_a {a.shape} / {b.shape}")
 
 
 def test_sum_to_shape_batched_matmul_broadcast_grads():
