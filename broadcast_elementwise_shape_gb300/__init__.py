@@ -149,6 +149,14 @@ def zr_binary_fwd(op, a, b, out=None):
 ZR_F32, ZR_BF16 = 0, 1
 
 
+def _float32_only(where, *ts):
+    """The chain, unary and gradient-layout entry points take float32 only."""
+    import torch
+    for t in ts:
+        if t is not None and t.dtype != torch.float32:
+            raise TypeError(f"{where} takes float32 tensors (got {t.dtype})")
+
+
 def _dtype_of(*ts):
     """The zr_dtype of tensors that must share one element type."""
     import torch
@@ -229,6 +237,7 @@ def zr_chain_fwd(op1, op2, a, b, c, out=None):
     """out = (a op1 b) op2 c (broadcasting); ``out`` may be a preallocated
     (strided) tensor of the broadcast shape."""
     import torch
+    _float32_only("zr_chain_fwd", a, b, c, out)
     shape = zr_broadcast_shape(zr_broadcast_shape(a.shape, b.shape), c.shape)
     if out is None:
         out = torch.empty(shape, dtype=torch.float32, device=a.device)
@@ -250,6 +259,7 @@ def zr_chain_bwd(op1, op2, grad_out, a, b, c, want=(True, True, True), grads=(No
     operand may be None (with its shape in ``shapes``) when the requested
     gradients do not read it."""
     import torch
+    _float32_only("zr_chain_bwd", grad_out, a, b, c, *grads)
     xs = (a, b, c)
     shp = [tuple(x.shape) if x is not None else tuple(s) for x, s in zip(xs, shapes)]
     dev = grad_out.device
@@ -284,6 +294,7 @@ def zr_binary_bwd_ex(op, grad_out, a, b, grad_a=None, grad_b=None, accumulate=(F
     """Backward of out = a op b into the caller's gradient tensors, which may
     be strided views; ``accumulate[k]`` adds to what they hold (grad +=
     result) instead of overwriting.  Returns (grad_a, grad_b)."""
+    _float32_only("zr_binary_bwd_ex", grad_out, a, b, grad_a, grad_b)
     sa = tuple(a.shape) if a is not None else tuple(shape_a)
     sb = tuple(b.shape) if b is not None else tuple(shape_b)
     for g, s in ((grad_a, sa), (grad_b, sb)):
@@ -314,6 +325,7 @@ def zr_unary_fwd(op, x, alpha=1.0, out=None):
     """out = op(x) for op in ("scale", "gelu"); ``out`` may be a preallocated
     (strided) tensor of x's shape, or x itself."""
     import torch
+    _float32_only("zr_unary_fwd", x, out)
     if out is None:
         out = torch.empty(x.shape, dtype=torch.float32, device=x.device)
     dx, kx = _desc(x)
@@ -327,6 +339,7 @@ def zr_unary_fwd(op, x, alpha=1.0, out=None):
 def zr_unary_bwd(op, grad_out, x, alpha=1.0, grad_x=None):
     """grad_x = grad_out * op'(x); ``x`` may be None for "scale"."""
     import torch
+    _float32_only("zr_unary_bwd", grad_out, x, grad_x)
     if grad_x is None:
         grad_x = torch.empty(grad_out.shape, dtype=torch.float32, device=grad_out.device)
     dg, kg = _desc(grad_out)

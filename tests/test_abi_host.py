@@ -581,3 +581,23 @@ def test_backward_ex_layout_errors_and_query(L):
     neg = _i64([-1, 64])
     assert L.zr_binary_bwd_ex(0, g.desc, x.desc, bias.desc, ZrGrad(4 * T, neg, 0), dense, None,
                               ctypes.byref(nb), None) == -4
+
+
+def test_float32_only_entry_points_refuse_bf16():
+    """The chain, unary and gradient-layout entry points compute on float32
+    storage; the binding refuses bfloat16 tensors before any call."""
+    import torch
+    h = torch.ones(4, 8, dtype=torch.bfloat16)
+    v = torch.ones(8, dtype=torch.bfloat16)
+    with pytest.raises(TypeError):
+        zr.zr_chain_fwd("mul", "add", h, v, v)
+    with pytest.raises(TypeError):
+        zr.zr_chain_bwd("mul", "add", h, h, v, v)
+    with pytest.raises(TypeError):
+        zr.zr_unary_fwd("gelu", h)
+    with pytest.raises(TypeError):
+        zr.zr_unary_bwd("scale", h, None)
+    with pytest.raises(TypeError):
+        zr.zr_binary_bwd_ex("add", h, h, v, grad_a=h)
+    with pytest.raises(TypeError):  # mixed element types
+        zr.zr_binary_fwd("add", torch.ones(4), v[:4])
