@@ -70,6 +70,8 @@ def parse():
     p.add_argument("--breakdown-steps", type=int, default=20,
                    help="steps of the untimed per-op breakdown pass")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--ref-procs", type=int, default=0,
+                   help="processes of the reference arm's oracle pool (0: one per host core)")
     p.add_argument("--no-e2e", action="store_true")
     a = p.parse_args()
     if a.warmup < 3:
@@ -646,36 +648,115 @@ def run_per_config(suites, flush, stream, reps, warm=5):
     return per_config, per_op
 
 
-def run_e2e(args, suite, flush, stream, nbytes):
-    """Same metric with host buffers: every step copies each workload's inputs
-    from pinned host memory, runs its ops through the C ABI and copies every
-    output back.  Per workload the uploads run on one stream, the ops on the
-    caller's stream after them and the downloads on a third stream after the
-    ops, so one workload's results travel back while the next one's inputs
-    travel in (the host link carries both directions at once)."""
+def step_io(step):
+    """Names a workload step reads and writes."""
+    kind = step[0]
+    if kind == "fwd":
+        return list(step[2:4]), [step[4]]
+    if kind == "bwd":
+        return list(step[2:5]), list(step[5:7])
+    if kind == "cfwd":
+        return list(step[3:6]), [step[6]]
+    if kind == "cbwd":
+        return list(step[3:7]), list(step[7:10])
+    if kind == "ufwd":
+        return [step[3]], [step[4]]
+    return list(step[3:5]), [step[5]]
+
+
+def link_rates(device, nbytes=1 << 30, reps=5):
+    """Copy rates of the host link in GB/s (median of `reps`): pinned host to
+    device, device to pinned host, and both directions at once on two
+    streams (their total).  The ceiling for the end-to-end measurement."""
     import torch
-    per_name = {}
+    n = nbytes // 4
+    h_src = torch.ones(n, dtype=torch.float32).pin_memory()
+    h_dst = torch.empty(n, dtype=torch.float32).pin_memory()
+    d_dst = torch.empty(n, dtype=torch.float32, device=device)
+    d_src = torch.ones(n, dtype=torch.float32, device=device)
+    cur = torch.cuda.current_stream(device)
+    s1, s2 = torch.cuda.Stream(device=device), torch.cuda.Stream(device=device)
+
+    def up():
+        d_dst.copy_(h_src, non_blocking=True)
+
+    def down():
+        h_dst.copy_(d_src, non_blocking=True)
+
+    def both():
+        e0 = cur.record_event()
+        s1.wait_event(e0)
+        s2.wait_event(e0)
+        with torch.cuda.stream(s1):
+            up()
+        with torch.cuda.stream(s2):
+            down()
+        cur.wait_event(s1.record_event())
+        cur.wait_event(s2.record_event())
+
+    out = {}
+    for key, fn, moved in (("h2d", up, nbytes), ("d2h", down, nbytes), ("both", both, 2 * nbytes)):
+        fn()
+        torch.cuda.synchronize(device)
+        ts = []
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(cur)
+            fn()
+            b.record(cur)
+            torch.cuda.synchronize(device)
+            ts.append(a.elapsed_time(b))
+        out[key] = round(moved / (statistics.median(ts) * 1e-3) / 1e9, 1)
+    del h_src, h_dst, d_dst, d_src
+    return out
+
+
+def run_e2e(args, suite, flush, stream, nbytes):
+    """Same metric with host buffers: every step copies each input from
+    pinned host memory and every output back, inside the timed region.  The
+    copies are scheduled per op: an input is uploaded (on an upload stream)
+    just before the first op that reads it, the op runs on the caller's
+    stream once its uploads are in, and each output is downloaded (on a
+    third stream) as soon as its op has written it.  Uploads thus run ahead
+    of the ops and downloads behind them, so the host link carries both
+    directions at once for most of the step (a forward whose inputs are
+    small starts its large download while the next op's large input is
+    still arriving)."""
+    import torch
     h2d = d2h = 0
+    plan = []  # per op: (uploads [(dst, src)], call, downloads [(dst, src)])
     for name in suite.dev:
         env = suite.dev[name]
-        ins, outs = [], []
-        for k in suite.in_names[name]:
-            t = env[k]
-            src = suite.host[name][k]
-            # Copy the whole storage (views keep their layout).
-            st = src.untyped_storage()
-            hs = torch.empty(0, dtype=src.dtype).set_(st, 0, (st.nbytes() // 4,), (1,))
-            hp = hs.pin_memory()
-            ds = t.untyped_storage()
-            dflat = torch.empty(0, dtype=t.dtype, device=t.device).set_(ds, 0, (ds.nbytes() // 4,), (1,))
-            ins.append((dflat, hp))
-            h2d += hp.numel() * 4
-        for k in suite.out_names[name]:
-            t = env[k]
-            hp = torch.empty(t.shape, dtype=torch.float32).pin_memory()
-            outs.append((hp, t))
-            d2h += hp.numel() * 4
-        per_name[name] = (ins, outs, [c for c in suite.calls if c[0] == name])
+        host_in = set(suite.in_names[name])
+        written = set(suite.out_names[name])
+        calls = [c for c in suite.calls if c[0] == name]
+        steps = workloads.STEPS[name]
+        assert len(calls) == len(steps)
+        uploaded = set()
+        for step, call in zip(steps, calls):
+            reads, writes = step_io(step)
+            ups, downs = [], []
+            for k in reads:
+                if k in host_in and k not in uploaded:
+                    uploaded.add(k)
+                    # Copy the operand's whole storage (views keep their
+                    # layout); the pinned host buffer holds the same bytes
+                    # in the device's element type.
+                    t = env[k]
+                    ds = t.untyped_storage()
+                    dflat = torch.empty(0, dtype=t.dtype, device=t.device).set_(
+                        ds, 0, (ds.nbytes() // t.element_size(),), (1,))
+                    hp = torch.empty(dflat.numel(), dtype=t.dtype).pin_memory()
+                    hp.copy_(dflat)
+                    ups.append((dflat, hp))
+                    h2d += hp.numel() * hp.element_size()
+            for k in writes:
+                if k in written:
+                    t = env[k]
+                    hp = torch.empty(t.shape, dtype=t.dtype).pin_memory()
+                    downs.append((hp, t))
+                    d2h += hp.numel() * hp.element_size()
+            plan.append((ups, call, downs))
     s_in = torch.cuda.Stream(device=stream.device)
     s_out = torch.cuda.Stream(device=stream.device)
     ev = []
@@ -686,17 +767,18 @@ def run_e2e(args, suite, flush, stream, nbytes):
         s.record(stream)
         s_in.wait_event(s)
         s_out.wait_event(s)
-        for name, (ins, outs, calls) in per_name.items():
-            with torch.cuda.stream(s_in):
-                for dst, src in ins:
-                    dst.copy_(src, non_blocking=True)
-            stream.wait_event(s_in.record_event())
-            for c in calls:
-                c[5]()
-            s_out.wait_event(stream.record_event())
-            with torch.cuda.stream(s_out):
-                for dst, src in outs:
-                    dst.copy_(src, non_blocking=True)
+        for ups, call, downs in plan:
+            if ups:
+                with torch.cuda.stream(s_in):
+                    for dst, src in ups:
+                        dst.copy_(src, non_blocking=True)
+                stream.wait_event(s_in.record_event())
+            call[5]()
+            if downs:
+                s_out.wait_event(stream.record_event())
+                with torch.cuda.stream(s_out):
+                    for dst, src in downs:
+                        dst.copy_(src, non_blocking=True)
         stream.wait_event(s_out.record_event())
         stream.wait_event(s_in.record_event())
         e.record(stream)
@@ -704,10 +786,14 @@ def run_e2e(args, suite, flush, stream, nbytes):
             ev.append((s, e))
     torch.cuda.synchronize()
     ms = statistics.fmean(s.elapsed_time(e) for s, e in ev)
+    link = link_rates(stream.device)
+    moved = (h2d + d2h) / (ms * 1e-3) / 1e9
     return {"value": round(nbytes / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 3),
-            "steps": steps,
-            "copies": "per workload: uploads, ops and downloads on three streams, pipelined"}
+            "steps": steps, "link_gbs": link, "copied_gbs": round(moved, 1),
+            "frac_of_link_both": round(moved / link["both"], 3) if link["both"] else None,
+            "copies": "per op: uploads ahead on one stream, ops on the caller's stream, "
+                      "downloads behind on a third stream"}
 
 
 def read_traffic(call):
@@ -729,68 +815,156 @@ def read_traffic(call):
 
 # ------------------------------------------------------------------ oracle (CPU)
 
+def oracle_steps(name, host):
+    """The oracle over every step of one workload (forward chain, then
+    backward); returns (algorithmic bytes, op-elements)."""
+    import oracle
+    sizes, _ = shape_table(name, host)
+    env = dict(host)
+    total_bytes = elems = 0
+    for step in workloads.STEPS[name]:
+        total_bytes += op_bytes(step, sizes)
+        if step[0] == "fwd":
+            _, op, an, bn, on = step
+            env[on] = oracle.binary_fwd(op, env[an], env[bn])
+            elems += sizes[on]
+        else:
+            _, op, gn, an, bn, gan, gbn = step
+            ga, gb, _, _ = oracle.binary_bwd(op, env[gn], env[an], env[bn])
+            env[gan], env[gbn] = ga, gb
+            elems += sizes[gn]
+    return total_bytes, elems
+
+
 def oracle_sample(names):
-    """Run the oracle over the complete fwd+bwd of the named workloads;
-    returns (seconds, algorithmic bytes, output elements)."""
+    """Run the oracle over the complete fwd+bwd of the named workloads in
+    this process; returns (seconds, algorithmic bytes, output elements)."""
     import oracle
     oracle.build()
-    total_bytes = 0
-    elems = 0
+    total_bytes = elems = 0
     t_total = 0.0
     for name in names:
         host = workloads.make_inputs(name)
-        sizes, _ = shape_table(name, host)
-        env = dict(host)
         t = time.perf_counter()
-        for step in workloads.STEPS[name]:
-            total_bytes += op_bytes(step, sizes)
-            if step[0] == "fwd":
-                _, op, an, bn, on = step
-                env[on] = oracle.binary_fwd(op, env[an], env[bn])
-                elems += sizes[on]
-            else:
-                _, op, gn, an, bn, gan, gbn = step
-                ga, gb, _, _ = oracle.binary_bwd(op, env[gn], env[an], env[bn])
-                env[gan], env[gbn] = ga, gb
-                elems += sizes[gn]
+        b, e = oracle_steps(name, host)
         t_total += time.perf_counter() - t
+        total_bytes += b
+        elems += e
     return t_total, total_bytes, elems
 
 
-def cpu_baseline():
-    names = ["c1", "c2", "c3"]
-    secs, nbytes, elems = oracle_sample(names)
-    return {"value": round(nbytes / secs / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": "complete fwd+bwd of c1, c2 and c3 (single-thread C++ oracle, binary64 "
-                      f"accumulation); {elems} op-elements in {secs:.2f} s",
-            "seconds": round(secs, 3)}
+def _oracle_worker(names, dims, cmd, res):
+    """One process of OraclePool: builds its own inputs, reports ready, then
+    runs the whole sample each time it is told to."""
+    import torch
+    torch.set_num_threads(1)  # one core per process; torch only draws the inputs
+    import oracle
+    oracle.build()
+    inputs = {n: workloads.make_inputs(n, **(dims or {})) for n in names}
+    res.put("ready")
+    while cmd.get() is not None:
+        t0 = time.time()
+        nbytes = elems = 0
+        for n in names:
+            b, e = oracle_steps(n, inputs[n])
+            nbytes += b
+            elems += e
+        res.put((t0, time.time(), nbytes, elems))
+
+
+class OraclePool:
+    """The oracle on every host core: one spawned process per core (the
+    oracle itself is single-threaded and unchanged), each with its own copy
+    of the sample's inputs.  Independent problems on separate cores is how
+    the path shards, so the pool's throughput is the processes' total bytes
+    over the wall time from the first start to the last finish.  Spawned,
+    not forked, so that no process inherits a CUDA context."""
+
+    def __init__(self, names, procs=None, dims=None):
+        import multiprocessing as mp
+        import oracle
+        oracle.build()  # once, before the processes load it
+        ctx = mp.get_context("spawn")
+        self.n = procs or len(os.sched_getaffinity(0))
+        self.res = ctx.Queue()
+        self.cmd = [ctx.Queue() for _ in range(self.n)]
+        self.procs = [ctx.Process(target=_oracle_worker, args=(names, dims, q, self.res),
+                                  daemon=True) for q in self.cmd]
+        for p in self.procs:
+            p.start()
+        for _ in range(self.n):
+            assert self.res.get(timeout=600) == "ready"
+
+    def run(self):
+        """One pass of every process; returns (wall seconds, bytes, elements)."""
+        for q in self.cmd:
+            q.put(1)
+        out = [self.res.get(timeout=600) for _ in range(self.n)]
+        span = max(o[1] for o in out) - min(o[0] for o in out)
+        return span, sum(o[2] for o in out), sum(o[3] for o in out)
+
+    def close(self):
+        for q in self.cmd:
+            q.put(None)
+        for p in self.procs:
+            p.join(timeout=60)
+
+
+def cpu_baseline(names=("c1", "c2", "c3"), runs=3, procs=None):
+    """The oracle on the machine's host cores: `runs` passes of the pool (one
+    process per core, each computing the complete fwd+bwd of `names`),
+    median wall time; plus the same sample on one core for reference."""
+    names = list(names)
+    secs1, nbytes1, elems1 = oracle_sample(names)
+    pool = OraclePool(names, procs)
+    try:
+        passes = [pool.run() for _ in range(runs)]
+    finally:
+        pool.close()
+    span = statistics.median(p[0] for p in passes)
+    nbytes, elems = passes[0][1], passes[0][2]
+    return {"value": round(nbytes / span / 1e9, 4), "unit": "GB/s", "cores": pool.n,
+            "kind": "oracle",
+            "sample": f"complete fwd+bwd of {', '.join(names)} in each of {pool.n} processes "
+                      "(single-thread C++ oracle, binary64 accumulation, one process per host "
+                      f"core); {elems} op-elements per pass, median of {runs} passes, "
+                      f"{span:.2f} s",
+            "seconds": round(span, 3),
+            "single_core": {"value": round(nbytes1 / secs1 / 1e9, 4), "cores": 1,
+                            "seconds": round(secs1, 3)}}
 
 
 def run_reference(args, rank, world):
     if rank != 0:
         return
-    # Each step is a bounded sample of the suite, sized so that K + W steps
-    # stay within a few minutes of CPU time.
+    # Each step is one pass of the oracle on every host core over a bounded
+    # sample of the suite, sized so that K + W steps stay within a few
+    # minutes.
     names = ["c1", "c2"] if args.steps + args.warmup <= 40 else ["c1"]
-    for _ in range(args.warmup):
-        oracle_sample(names)
-    times, nbytes = [], 0
-    for _ in range(args.steps):
-        s, b, _ = oracle_sample(names)
-        times.append(s)
-        nbytes = b
+    pool = OraclePool(names, args.ref_procs or None)
+    try:
+        for _ in range(args.warmup):
+            pool.run()
+        times, nbytes = [], 0
+        for _ in range(args.steps):
+            s, b, _ = pool.run()
+            times.append(s)
+            nbytes = b
+    finally:
+        pool.close()
     total = sum(times)
     value = nbytes * len(times) / total / 1e9
+    sample = (f"complete fwd+bwd of {' and '.join(names)} per step in each of {pool.n} "
+              "processes (single-thread C++ oracle, one process per host core)")
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(1e3 * total / len(times), 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": "bounded sample of the suite per step: complete fwd+bwd of "
-                               + " and ".join(names)},
-        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": "complete fwd+bwd of " + " and ".join(names)
-                                   + " per step (single-thread C++ oracle)"},
+                               + " and ".join(names) + f" on {pool.n} host cores"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": pool.n,
+                         "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }

@@ -101,7 +101,9 @@ int check_device_ptr(const void* p) {
     return ZR_ERR_DEVICE;
   }
   if (at.type == cudaMemoryTypeUnregistered) return ZR_ERR_DEVICE;
-  if (at.type == cudaMemoryTypeHost && at.devicePointer == nullptr) return ZR_ERR_DEVICE;
+  // Pinned host memory is used through the same address only (unified
+  // addressing maps it there); a different device alias is refused.
+  if (at.type == cudaMemoryTypeHost && at.devicePointer != p) return ZR_ERR_DEVICE;
   if (at.type == cudaMemoryTypeDevice) {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess) {

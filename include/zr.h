@@ -38,8 +38,12 @@
  *
  * Memory.  The library never allocates, frees or retains caller memory and
  * keeps no state between calls.  All pointers given for data must be device
- * memory (or host memory the device can address: registered/pinned or
- * managed) on the current device; the caller owns them and the stream.
+ * memory of the current device, managed memory, or pinned (page-locked)
+ * host memory that the device addresses at the same pointer (unified
+ * addressing); kernels then read and write that host memory directly over
+ * the host link.  Any other pointer (pageable host memory, another device's
+ * memory, a pinned buffer with a different device alias) is ZR_ERR_DEVICE.
+ * The caller owns the memory and the stream.
  */
 #ifndef ZR_H_
 #define ZR_H_

@@ -1,0 +1,47 @@
+"""Host logic of bench.py that needs no GPU: the per-op copy schedule of the
+end-to-end measurement reads and writes exactly the tensors each step names."""
+import os
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+import workloads  # noqa: E402
+
+
+def _allocated(step):
+    """Outputs bench.Suite allocates for a step."""
+    if step[0] in ("fwd", "cfwd", "ufwd", "ubwd"):
+        return [step[-1]]
+    return list(step[7:10] if step[0] == "cbwd" else step[5:7])
+
+
+def test_step_io_covers_every_workload_step():
+    for name, steps in workloads.STEPS.items():
+        host = workloads.make_inputs(name, **workloads.small_dims(name))
+        known = set(host)
+        for step in steps:
+            reads, writes = bench.step_io(step)
+            names = [x for x in step[1:] if isinstance(x, str) and x not in
+                     ("add", "sub", "mul", "div", "gelu", "scale")]
+            assert sorted(reads + writes) == sorted(names), (name, step)
+            assert writes == _allocated(step), (name, step)
+            # Every operand is a host input or the output of an earlier step,
+            # so uploading inputs before their first reader is a valid order.
+            assert all(k in known for k in reads), (name, step)
+            known.update(writes)
+
+
+def test_oracle_pool_runs_every_process_over_the_whole_sample():
+    """The all-cores CPU baseline: each process computes the complete sample,
+    so one pass moves processes x the sample's bytes."""
+    one_bytes = sum(bench.op_bytes(s, bench.shape_table("c1", workloads.make_inputs("c1"))[0])
+                    for s in workloads.STEPS["c1"])
+    pool = bench.OraclePool(["c1"], procs=2)
+    try:
+        span, nbytes, elems = pool.run()
+    finally:
+        pool.close()
+    assert pool.n == 2 and nbytes == 2 * one_bytes and span > 0
+    assert all(not p.is_alive() for p in pool.procs)
