@@ -180,7 +180,9 @@ int plan_fwd(int op, const zr_tensor& ta, const zr_tensor& tb, const float* out,
     S->sabf = true;
     return ZR_OK;
   }
-  return build_ew(P, in, outs, 0x3u, stream_mask, kOccEwFwd, &S->eb);
+  rc = build_ew(P, in, outs, 0x3u, stream_mask, kOccEwFwd, &S->eb);
+  S->eb.uni1 = S->b.numel == 1;
+  return rc;
 }
 
 // ------------------------------------------------------------------ backward
@@ -760,6 +762,12 @@ int zr_test_occupancy(int which, int* planned, int* actual) {
   else if (which >= 20 && which < 22) e = occupancy_ew(which - 16, planned, actual);
   else return ZR_ERR_SIZE;
   return cuda_status(e);
+}
+
+int zr_test_div_short_check(unsigned long long* out, void* stream) {
+  const int rc = check_device_ptr(out);
+  if (rc) return rc;
+  return cuda_status(launch_div_short_check(out, static_cast<cudaStream_t>(stream)));
 }
 
 int zr_test_dry_run_sum(zr_tensor in, int32_t ndim_out, const int64_t* sizes_out,

@@ -161,11 +161,13 @@ ZR_CX int red_cl_occ(int op, bool inner_kept) {
 // CTAs per SM of the 8-wide bfloat16 instantiations where a vector of 8
 // values needs more registers than the float kernel's budget (measured
 // spills): by default one fewer, or two from 3.  The reduction keeps 4 for
-// add/sub with the inner dim reduced (no per-column sums), 3 for mul/div
-// with it reduced and add/sub with it kept, 2 for mul/div with it kept.
+// add/sub (with the inner dim kept, 8 bytes of spill cost less than the
+// memory parallelism a fourth CTA adds: c4 in bf16, backward add, 88 against
+// 79 us), 3 for mul/div with the inner dim reduced, 2 for mul/div with it
+// kept.
 ZR_CX int wide_occ(int occ) { return occ >= 4 ? 3 : 2; }
 ZR_CX int red_wide_occ(int op, bool inner_kept) {
-  return (op == OP_MUL || op == OP_DIV) ? (inner_kept ? 2 : 3) : (inner_kept ? 3 : 4);
+  return (op == OP_MUL || op == OP_DIV) ? (inner_kept ? 2 : 3) : 4;
 }
 constexpr uint32_t kMaxCluster = 8;   // CTAs per cluster (the portable limit)
 // CTAs of a cluster plan that can be resident at once, out of a full wave of

@@ -16,6 +16,43 @@ namespace zr {
 
 // ---------------------------------------------------------------- arithmetic
 
+// The hardware's approximate reciprocal (relative error about 2^-23).
+__device__ __forceinline__ float rcp_approx(float v) {
+  float r;
+  asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(v));
+  return r;
+}
+
+// x / y correctly rounded to binary32 (round to nearest even) for x and y
+// that bfloat16 can hold (8-bit significands), without the general divide:
+// an approximate quotient and one correction with the exact residual, as in
+// P. W. Markstein, "Computation of elementary functions on the IBM RISC
+// System/6000 processor", IBM J. Res. Develop. 34(1), 1990:
+//   r = approx 1/y,  q0 = x * r,  e = x - y * q0 (one FMA),  q = q0 + e * r.
+// Valid when div_fast_ok: both exponents in [-60, 60], so nothing
+// overflows, underflows or turns subnormal, and q0 + e * r is within 2^-43
+// of x / y (relative).  For 8-bit significands A, B the quotient is never
+// exactly halfway between two binary32 numbers (A = (2m + 1) B with 2m + 1
+// odd and above 2^24 is impossible) and otherwise at least 2^-33 (relative)
+// away from every halfway point, so the FMA's one rounding gives RN(x / y).
+// Every pair of bfloat16 values is checked against the IEEE divide by a GPU
+// test.
+__device__ __forceinline__ float div_fast(float x, float y) {
+  float r;  // y is normal here, so the flush-to-zero form is exact enough
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(y));
+  const float q0 = __fmul_rn(x, r);
+  const float e = __fmaf_rn(-y, q0, x);
+  return __fmaf_rn(e, r, q0);
+}
+// 2^-60 <= |v| < 2^61 (false for zeros, subnormals, infinities and NaNs).
+__device__ __forceinline__ bool div_fast_range(float v) {
+  const float m = fabsf(v);
+  return (m >= 0x1p-60f) & (m < 0x1p61f);
+}
+__device__ __forceinline__ bool div_fast_ok(float x, float y) {
+  return div_fast_range(x) & div_fast_range(y);
+}
+
 template <int OP>
 __device__ __forceinline__ float fwd_op(float x, float y) {
   if (OP == OP_ADD) return __fadd_rn(x, y);
@@ -117,6 +154,91 @@ struct Kahan {
 
 template <int VEC>
 struct Vec { float v[VEC]; };
+
+// Quotients x / y of VEC pairs of bfloat16 values: div_fast for all when
+// every pair is in its range, else the IEEE divide for all (one branch per
+// vector, so the VEC independent reciprocal-and-correction chains
+// interleave).  Bit-identical to __fdiv_rn on every pair either way.
+template <int VEC>
+__device__ __forceinline__ void quot_short(const Vec<VEC>& x, const Vec<VEC>& y, Vec<VEC>& q) {
+  bool ok = true;
+#pragma unroll
+  for (int i = 0; i < VEC; ++i) ok = ok & div_fast_ok(x.v[i], y.v[i]);
+  if (ok) {
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) q.v[i] = div_fast(x.v[i], y.v[i]);
+  } else {
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) q.v[i] = __fdiv_rn(x.v[i], y.v[i]);
+  }
+}
+
+// Quotients x / y of VEC pairs of bfloat16 values whose results are stored
+// as bfloat16: q = x * (approximate 1/y), one rounding.  Its relative error is
+// below 2^-22, and x / y is never exactly halfway between two bfloat16
+// numbers and otherwise more than 2^-18 (relative) away from every halfway
+// point: a halfway point is N 2^t with N odd, 2^8 < N < 2^9, and x = A 2^i,
+// y = B 2^j with A, B below 2^8 give |x/y - N 2^t| >= 2^(t+j) / y, about
+// x / (B N) (A = N B odd-part-wise is impossible).  So q and x / y round to
+// the same bfloat16 number, which is RN(RN(x / y)) by the innocuous double
+// rounding of 24 >= 2 * 8 + 2 bits.  Valid when every pair passes
+// div_fast_ok (q is then a normal number); otherwise the IEEE divide for all.
+template <int VEC>
+__device__ __forceinline__ void quot_bf16(const Vec<VEC>& x, const Vec<VEC>& y, Vec<VEC>& q) {
+  bool ok = true;
+#pragma unroll
+  for (int i = 0; i < VEC; ++i) ok = ok & div_fast_ok(x.v[i], y.v[i]);
+  if (ok) {
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) {
+      float r;
+      asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(y.v[i]));
+      q.v[i] = __fmul_rn(x.v[i], r);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) q.v[i] = __fdiv_rn(x.v[i], y.v[i]);
+  }
+}
+
+// Vector forms of the forward and of the dense gradient terms.  SHORT: the
+// operands are bfloat16 values and the results are stored as bfloat16: a
+// stored quotient takes quot_bf16, a quotient that feeds a product
+// quot_short; otherwise (and for the other ops) the scalar forms above,
+// element by element.
+template <int OP, bool SHORT, int VEC>
+__device__ __forceinline__ void fwd_vec(const Vec<VEC>& x, const Vec<VEC>& y, Vec<VEC>& out) {
+  if (OP == OP_DIV && SHORT) {
+    quot_bf16(x, y, out);
+  } else {
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) out.v[i] = fwd_op<OP>(x.v[i], y.v[i]);
+  }
+}
+template <int OP, bool SHORT, int VEC>
+__device__ __forceinline__ void term_a_vec(const Vec<VEC>& g, const Vec<VEC>& a, const Vec<VEC>& b,
+                                           Vec<VEC>& out) {
+  if (OP == OP_DIV && SHORT) {
+    quot_bf16(g, b, out);
+  } else {
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) out.v[i] = term_a<OP>(g.v[i], a.v[i], b.v[i]);
+  }
+}
+template <int OP, bool SHORT, int VEC>
+__device__ __forceinline__ void term_b_vec(const Vec<VEC>& g, const Vec<VEC>& a, const Vec<VEC>& b,
+                                           Vec<VEC>& out) {
+  if (OP == OP_DIV && SHORT) {
+    Vec<VEC> qg, qa;
+    quot_short(g, b, qg);
+    quot_short(a, b, qa);
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) out.v[i] = -__fmul_rn(qg.v[i], qa.v[i]);
+  } else {
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) out.v[i] = term_b<OP>(g.v[i], a.v[i], b.v[i]);
+  }
+}
 
 // Storage types E: float, or bfloat16 (binary32's upper 16 bits).  Loads
 // widen to binary32 exactly; stores round to the storage type once, to
@@ -268,25 +390,24 @@ __device__ __forceinline__ void store_cols(E* __restrict__ base, int64_t row_off
 
 // ---------------------------------------------------------------- functors
 
-// Forward: out = a op b.
-template <int OP>
+// Forward: out = a op b.  SHORT: operands are bfloat16 values (quot_short).
+// B_ONE: b has one element, read once per thread (its reciprocal and range
+// check are then loop-invariant).
+template <int OP, bool SHORT = false, bool B_ONE = false>
 struct FwdF {
   static constexpr bool kR1 = true, kR2 = false;  // slot 0 = a, slot 1 = b
+  static constexpr bool kUniform1 = B_ONE;
   static constexpr int kMinBlocks = kOccEwFwd;  // CTAs per SM the register budget targets
-  // 8-wide bfloat16 keeps 4 CTAs per SM even for IEEE division: its 36 bytes
-  // of spill cost less than the lost memory parallelism at 3 (c4 in bf16,
-  // forward div: 89 against 100 us).
   static constexpr int kMinBlocksWide = kOccEwFwd;
   template <int VEC>
   __device__ __forceinline__ void operator()(const Vec<VEC> (&x)[3], Vec<VEC> (&y)[2], float) const {
-#pragma unroll
-    for (int i = 0; i < VEC; ++i) y[0].v[i] = fwd_op<OP>(x[0].v[i], x[1].v[i]);
+    fwd_vec<OP, SHORT>(x[0], x[1], y[0]);
   }
 };
 
 // Backward with no reduction: grad_a and/or grad_b elementwise.
 // Inputs: slot 0 = g, 1 = a, 2 = b.  WANT: bit 0 grad_a, bit 1 grad_b.
-template <int OP, int WANT>
+template <int OP, int WANT, bool SHORT = false>
 struct BwdDirectF {
   static constexpr bool kR1 = ((WANT & 1) && Needs<OP, 0>::a) || ((WANT & 2) && Needs<OP, 1>::a);
   static constexpr bool kR2 = ((WANT & 1) && Needs<OP, 0>::b) || ((WANT & 2) && Needs<OP, 1>::b);
@@ -294,11 +415,8 @@ struct BwdDirectF {
   static constexpr int kMinBlocksWide = (OP == OP_DIV && (WANT & 2)) ? 2 : kOccEwBwd;
   template <int VEC>
   __device__ __forceinline__ void operator()(const Vec<VEC> (&x)[3], Vec<VEC> (&y)[2], float) const {
-#pragma unroll
-    for (int i = 0; i < VEC; ++i) {
-      if (WANT & 1) y[0].v[i] = term_a<OP>(x[0].v[i], x[1].v[i], x[2].v[i]);
-      if (WANT & 2) y[1].v[i] = term_b<OP>(x[0].v[i], x[1].v[i], x[2].v[i]);
-    }
+    if (WANT & 1) term_a_vec<OP, SHORT>(x[0], x[1], x[2], y[0]);
+    if (WANT & 2) term_b_vec<OP, SHORT>(x[0], x[1], x[2], y[1]);
   }
 };
 
@@ -337,11 +455,6 @@ struct ChainF {
 __device__ __forceinline__ float ex2_approx(float v) {
   float r;
   asm("ex2.approx.f32 %0, %1;" : "=f"(r) : "f"(v));
-  return r;
-}
-__device__ __forceinline__ float rcp_approx(float v) {
-  float r;
-  asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(v));
   return r;
 }
 __device__ __forceinline__ float erfc_cheb(float v) {
@@ -411,8 +524,12 @@ struct CopyF {
 
 // ---------------------------------------------------------------- elementwise
 
-// Slot 2 holds one value for every element (read once per thread), when the
-// functor says so.
+// Slot 1 or slot 2 holds one value for every element (read once per
+// thread), when the functor says so.
+template <class F, class = void>
+struct Uniform1 { static constexpr bool value = false; };
+template <class F>
+struct Uniform1<F, decltype(void(F::kUniform1))> { static constexpr bool value = F::kUniform1; };
 template <class F, class = void>
 struct Uniform2 { static constexpr bool value = false; };
 template <class F>
@@ -446,8 +563,10 @@ k_elementwise(const __grid_constant__ EwPlan p) {
   }
   __syncthreads();
   pdl_wait();
+  constexpr bool kUni1 = Uniform1<F>::value;
   constexpr bool kUni2 = Uniform2<F>::value;
-  float uni2 = 0.f;
+  float uni1 = 0.f, uni2 = 0.f;
+  if (kUni1) uni1 = ld1(in1, false);
   if (kUni2) uni2 = ld1(in2, false);
 
   constexpr int U = 4;
@@ -468,7 +587,8 @@ k_elementwise(const __grid_constant__ EwPlan p) {
       if (ok[u]) {
         const int64_t* ro = s_off + ri * kMaxOperands;
         xr[u][0] = load_raw<VEC>(in0, ro[0], p.inner_stride[0], col[u], p.stream_mask & 1);
-        if (F::kR1) xr[u][1] = load_raw<VEC>(in1, ro[1], p.inner_stride[1], col[u], p.stream_mask & 2);
+        if (F::kR1 && !kUni1)
+          xr[u][1] = load_raw<VEC>(in1, ro[1], p.inner_stride[1], col[u], p.stream_mask & 2);
         if (F::kR2 && !kUni2)
           xr[u][2] = load_raw<VEC>(in2, ro[2], p.inner_stride[2], col[u], p.stream_mask & 4);
         doff[u] = ro[kSlotOut];
@@ -479,7 +599,12 @@ k_elementwise(const __grid_constant__ EwPlan p) {
       if (!ok[u]) continue;
       Vec<VEC> x[3], y[2];
       x[0] = unpack<VEC>(xr[u][0]);
-      if (F::kR1) x[1] = unpack<VEC>(xr[u][1]);
+      if (F::kR1 && kUni1) {
+#pragma unroll
+        for (int i = 0; i < VEC; ++i) x[1].v[i] = uni1;
+      } else if (F::kR1) {
+        x[1] = unpack<VEC>(xr[u][1]);
+      }
       if (F::kR2 && kUni2) {
 #pragma unroll
         for (int i = 0; i < VEC; ++i) x[2].v[i] = uni2;
@@ -630,7 +755,7 @@ k_sabf(const __grid_constant__ SabFPlan p) {
 // Term of the reduced gradient X (WHICH: 0 = a, 1 = b; 2 = sum-to-shape
 // identity) and, when the other gradient is written densely in the same pass,
 // the other term.
-template <int OP, int WHICH>
+template <int OP, int WHICH, bool SHORT = false>
 struct RedTerms {
   // div with grad_b reduced: b is constant along the reduction (it is the
   // broadcast operand), so sum(-g*a/b^2) = -(1/b^2) * sum(g*a): the kernel adds
@@ -663,9 +788,11 @@ struct RedTerms {
     return -__fmul_rn(r, r);
   }
   // Dense gradient terms stay exact single operations (bit-identical).
-  __device__ __forceinline__ static float d(float g, float a, float b) {
-    if (WHICH == 0) return term_b<OP>(g, a, b);
-    return term_a<OP>(g, a, b);
+  template <int VEC>
+  __device__ __forceinline__ static void d(const Vec<VEC>& g, const Vec<VEC>& a, const Vec<VEC>& b,
+                                           Vec<VEC>& out) {
+    if (WHICH == 0) term_b_vec<OP, SHORT>(g, a, b, out);
+    else term_a_vec<OP, SHORT>(g, a, b, out);
   }
   // The same rule on the host: which pointers the kernel dereferences.
   static bool reads_a(bool has_d) { return kXa || (has_d && kDa); }
@@ -700,7 +827,8 @@ k_reduce(const __grid_constant__ RedPlan p) {
   const E* bE = reinterpret_cast<const E*>(p.b);
   E* xE = reinterpret_cast<E*>(p.x_final);
   E* dE = reinterpret_cast<E*>(p.d_out);
-  using T = RedTerms<OP, WHICH>;
+  // bfloat16 operands divide with quot_short.
+  using T = RedTerms<OP, WHICH, sizeof(E) == 2>;
   extern __shared__ int64_t s_dyn[];
   const uint32_t table_rows = p.rows_per_blk < kMaxTileRows ? p.rows_per_blk : kMaxTileRows;
   int64_t* s_off = s_dyn;  // [table_rows][kMaxOperands]
@@ -793,19 +921,22 @@ k_reduce(const __grid_constant__ RedPlan p) {
         Vec<VEC> av, bv;
         if ((T::kXa || T::kDa) && read_a && WHICH != 0) av = unpack<VEC>(ar[u]);
         if ((T::kXb || T::kDb) && read_b && WHICH != 1) bv = unpack<VEC>(br[u]);
-        Vec<VEC> dv;
+        Vec<VEC> aw, bw;
 #pragma unroll
         for (int i = 0; i < VEC; ++i) {
-          const float gg = gv.v[i];
           const float aa = ((T::kXa || T::kDa) && read_a) ? (WHICH == 0 ? own.v[i] : av.v[i]) : 0.f;
           const float bb = ((T::kXb || T::kDb) && read_b) ? (WHICH == 1 ? own.v[i] : bv.v[i]) : 0.f;
-          if (INNER_KEPT) acc[i].add_prod(gg, T::m(aa, bb));
-          else acc[0].add_prod(gg, T::m(aa, bb));
-          if (has_d) dv.v[i] = T::d(gg, aa, bb);
+          aw.v[i] = aa;
+          bw.v[i] = bb;
+          if (INNER_KEPT) acc[i].add_prod(gv.v[i], T::m(aa, bb));
+          else acc[0].add_prod(gv.v[i], T::m(aa, bb));
         }
-        if (has_d)
+        if (has_d) {
+          Vec<VEC> dv;
+          T::d(gv, aw, bw, dv);
           store_cols<VEC>(dE, s_off[ri[u] * kMaxOperands + kSlotOut], p.inner_stride[kSlotOut],
                           cc[u], dv);
+        }
       }
     }
   }

@@ -30,9 +30,9 @@ cudaError_t launch_ew_bf16(const EwBuild& eb, cudaStream_t s, bool dry) {
 template <int OP>
 cudaError_t direct_bf16(int want, const EwBuild& eb, cudaStream_t s, bool dry) {
   switch (want) {
-    case 1: return launch_ew_bf16<BwdDirectF<OP, 1>, 2>(eb, s, dry);
-    case 2: return launch_ew_bf16<BwdDirectF<OP, 2>, 2>(eb, s, dry);
-    default: return launch_ew_bf16<BwdDirectF<OP, 3>, 2>(eb, s, dry);
+    case 1: return launch_ew_bf16<BwdDirectF<OP, 1, true>, 2>(eb, s, dry);
+    case 2: return launch_ew_bf16<BwdDirectF<OP, 2, true>, 2>(eb, s, dry);
+    default: return launch_ew_bf16<BwdDirectF<OP, 3, true>, 2>(eb, s, dry);
   }
 }
 
@@ -76,7 +76,9 @@ cudaError_t launch_fwd_bf16(int op, const EwBuild& eb, cudaStream_t s, bool dry)
     case OP_ADD: return launch_ew_bf16<FwdF<OP_ADD>, 1>(eb, s, dry);
     case OP_SUB: return launch_ew_bf16<FwdF<OP_SUB>, 1>(eb, s, dry);
     case OP_MUL: return launch_ew_bf16<FwdF<OP_MUL>, 1>(eb, s, dry);
-    default: return launch_ew_bf16<FwdF<OP_DIV>, 1>(eb, s, dry);
+    default:
+      return eb.uni1 ? launch_ew_bf16<FwdF<OP_DIV, true, true>, 1>(eb, s, dry)
+                     : launch_ew_bf16<FwdF<OP_DIV, true>, 1>(eb, s, dry);
   }
 }
 
@@ -101,6 +103,52 @@ cudaError_t launch_reduce_bf16(int op, int which, const RedBuild& rb, cudaStream
     case OP_MUL: return red_op_bf16<OP_MUL>(which, rb, s, dry);
     default: return red_op_bf16<OP_DIV>(which, rb, s, dry);
   }
+}
+
+namespace {
+// One CTA per x bit pattern, threads stride over the y patterns.  out[0],
+// out[1]: quot_short against the IEEE divide (binary32 bits); out[2],
+// out[3]: quot_bf16 against the IEEE divide, both rounded to bfloat16.
+__global__ void __launch_bounds__(kThreads) k_div_short_check(unsigned long long* out) {
+  const uint32_t xb = blockIdx.x;
+  const float x = __uint_as_float(xb << 16);
+  uint32_t bad[2] = {0, 0}, first[2] = {0xffffffffu, 0xffffffffu};
+  for (uint32_t yb = threadIdx.x; yb < 65536u; yb += blockDim.x) {
+    const float y = __uint_as_float(yb << 16);
+    Vec<1> xv, yv, q1, q2;
+    xv.v[0] = x;
+    yv.v[0] = y;
+    quot_short(xv, yv, q1);
+    quot_bf16(xv, yv, q2);
+    const float r = __fdiv_rn(x, y);
+    const uint32_t key = (xb << 16) | yb;
+    const float a = q1.v[0];
+    if (!(__float_as_uint(a) == __float_as_uint(r) || (a != a && r != r))) {
+      ++bad[0];
+      first[0] = key < first[0] ? key : first[0];
+    }
+    const float b16 = __bfloat162float(__float2bfloat16_rn(q2.v[0]));
+    const float r16 = __bfloat162float(__float2bfloat16_rn(r));
+    if (!(__float_as_uint(b16) == __float_as_uint(r16) || (b16 != b16 && r16 != r16))) {
+      ++bad[1];
+      first[1] = key < first[1] ? key : first[1];
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const uint32_t n = __reduce_add_sync(0xffffffffu, bad[k]);
+    const uint32_t f = __reduce_min_sync(0xffffffffu, first[k]);
+    if ((threadIdx.x & 31u) == 0 && n) {
+      atomicAdd(out + 2 * k, static_cast<unsigned long long>(n));
+      atomicMin(out + 2 * k + 1, static_cast<unsigned long long>(f));
+    }
+  }
+}
+}  // namespace
+
+cudaError_t launch_div_short_check(unsigned long long* out, cudaStream_t s) {
+  k_div_short_check<<<65536, kThreads, 0, s>>>(out);
+  return cudaGetLastError();
 }
 
 }  // namespace zr

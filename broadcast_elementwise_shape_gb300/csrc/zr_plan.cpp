@@ -406,9 +406,9 @@ int build_red(const Prob& P, int xslot, const float* g, const float* a, const fl
   rb->vec = vec_override ? vec_override
                          : pick_vec(P, slots, ptrs, p.inner_kept ? static_cast<const void*>(x_out)
                                                                  : nullptr);
-  // 8-wide bfloat16 reductions with the inner dim kept run one CTA per SM
-  // fewer than the float kernel (red_wide_occ).
-  if (rb->vec == 8 && p.inner_kept) occ = wide_occ(occ);
+  // 8-wide bfloat16 mul/div reductions with the inner dim kept run one CTA
+  // per SM fewer than the float kernel (red_wide_occ).
+  if (rb->vec == 8 && p.inner_kept && occ < 4) occ = wide_occ(occ);
   const uint32_t vec = uint32_t(rb->vec);
   const uint64_t nvcol = ceil_div(ncol, vec);
   p.nvcol = uint32_t(nvcol);

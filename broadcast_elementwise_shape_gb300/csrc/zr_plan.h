@@ -58,7 +58,8 @@ int coalesce(int n, const int64_t* size, const int64_t (*st)[kMaxDims], uint32_t
 struct EwBuild {
   EwPlan plan;
   int vec;
-  int es;  // bytes per stored element (Prob::es)
+  int es;             // bytes per stored element (Prob::es)
+  bool uni1 = false;  // input slot 1 is one element (a forward's b with numel 1)
 };
 // Elementwise plan over P with input slots 0..2 and output slot 3.
 // occ: resident CTAs per SM of the kernel that will run the plan.

@@ -73,6 +73,19 @@ int zr_test_emulate_bwd(zr_op op, zr_tensor grad_out, zr_tensor a, zr_tensor b,
                         const float* grad_a, const float* grad_b, int64_t cap, int64_t* rec,
                         int64_t* nrec);
 
+/* The two divisions of bfloat16 operands against the IEEE binary32 divide,
+ * over every ordered pair of bfloat16 bit patterns (2^32 pairs, one kernel
+ * on `stream`): the exact one (binary32 quotient rounded to nearest even,
+ * without the general divide's slow path) bit for bit, and the one for
+ * results stored as bfloat16 after both are rounded to bfloat16.  Two NaNs
+ * count as equal.  out: four device words the caller sets to
+ * {0, UINT64_MAX, 0, UINT64_MAX}; the kernel adds the number of differing
+ * pairs of the first division to out[0] and lowers out[1] to the smallest
+ * (x_bits << 16 | y_bits) among them, and likewise out[2], out[3] for the
+ * second.  Returns ZR_ERR_NULL / ZR_ERR_DEVICE for a bad pointer,
+ * ZR_ERR_CUDA if the launch fails. */
+int zr_test_div_short_check(unsigned long long* out, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -155,3 +155,38 @@ def test_bf16_wide_vectors(op):
         for w, got, r, sab in ((0, ga, ra, s1), (1, gb, rb, s2)):
             exact = r.size == g.numel() and not (op == "div" and w == 1)
             _check_grad(_f32(got), oracle.round_bf16(r), sab, exact, f"bf16 wide bwd {op} {sa} {sb} {w}")
+
+
+def test_bf16_division_equals_ieee_divide_on_every_pair():
+    """The divisions bf16 storage uses, over all 2^32 ordered pairs of
+    bfloat16 bit patterns (normals, subnormals, zeros, infinities, NaNs):
+    the exact one (approximate quotient plus one correction with the exact
+    residual) gives the IEEE binary32 quotient bit for bit; the one for
+    stored results (product with the approximate reciprocal) rounds to the
+    same bfloat16 number as the IEEE quotient."""
+    import ctypes
+    L = zr.lib()
+    L.zr_test_div_short_check.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
+    out = torch.tensor([0, -1, 0, -1], dtype=torch.int64, device="cuda")
+    rc = L.zr_test_div_short_check(out.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    assert rc == 0
+    torch.cuda.synchronize()
+    res = out.tolist()
+    for k, what in enumerate(("exact binary32 quotient", "quotient rounded to bf16")):
+        bad, first = res[2 * k], res[2 * k + 1] & ((1 << 64) - 1)
+        assert bad == 0, (f"{what}: {bad} pairs differ; first x bits 0x{first >> 16:04x}, "
+                          f"y bits 0x{first & 0xffff:04x}")
+
+
+def test_bf16_division_of_the_scores_workload_full_size():
+    """c4's scores [8,12,1024,1024] in bf16 divided by [8.0] at full size (the
+    plan the benchmark times): bit-identical to the oracle on sampled
+    elements."""
+    host = workloads.make_inputs("c4h")
+    t = _bf(host["scores"])
+    d_t, d_s = _dev16(t), _dev16(_bf(host["scalar"]))
+    out = zr.zr_binary_fwd("div", d_t, d_s)
+    rng = np.random.default_rng(1500)
+    idx = np.sort(rng.choice(t.numel(), 4096, replace=False)).astype(np.int64)
+    want = oracle.round_bf16(oracle.binary_fwd_at("div", t, _bf(host["scalar"]), idx))
+    bitexact(_f32(out).reshape(-1)[idx], want, "c4h t / 8")
