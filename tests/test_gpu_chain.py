@@ -226,3 +226,42 @@ def test_chain_workloads_full_sampled(name, op1, op2, keys):
             bitexact(gv, vals, what)
         else:
             within(gv, vals, sabs, what)
+
+
+def _dev_view(x, strides):
+    """Device view of x's values with the given element strides (inside a
+    larger zero-filled buffer)."""
+    span = 1 + sum((n - 1) * s for n, s in zip(x.shape, strides))
+    buf = torch.zeros(span, device="cuda")
+    v = buf.as_strided(x.shape, strides)
+    v.copy_(x.cuda())
+    return v
+
+
+STRIDED = [
+    # grad_out and a stepped along the inner dim: fused route.
+    ("fused", (6, 40, 132), (132,), (132,), {"g": (40 * 264, 264, 2), "a": (40 * 264, 264, 2)}),
+    # a with permuted outer dims: fused route.
+    ("fused", (6, 40, 132), (132,), (132,), {"a": (132, 6 * 132, 1)}),
+    # scaled-mask layout with a stepped a: fused route, one-element c.
+    ("fused", (2, 3, 131, 132), (1, 1, 131, 132), (1,), {"a": (3 * 131 * 264, 131 * 264, 264, 2)}),
+    # b and c stepped: c is not in b's dense layout, composed route.
+    ("composed", (6, 40, 132), (132,), (132,), {"b": (2,), "c": (2,)}),
+]
+
+
+@pytest.mark.parametrize("route,sa,sb,sc,st", STRIDED)
+def test_chain_backward_strided_views(route, sa, sb, sc, st):
+    """Strided and stepped views of grad_out, a, b and c, on both routes:
+    the same results as dense copies of the same values."""
+    rng = np.random.default_rng(996)
+    for op1 in OPS:
+        for op2 in OPS:
+            g, a, b, c = _inputs(rng, op1, op2, sa, sb, sc)
+            dev = []
+            for name, x in zip("gabc", (g, a, b, c)):
+                dev.append(_dev_view(x, st[name]) if name in st else x.cuda())
+            grads = [torch.empty(s, device="cuda") for s in (sa, sb, sc)]
+            assert _route(op1, op2, *dev, grads) == route, (op1, op2, sa, st)
+            got = zr.zr_chain_bwd(op1, op2, *dev, grads=grads)
+            _check_bwd(op1, op2, g, a, b, c, got, f"strided {route} {op1} {op2} {sa} {st}")
