@@ -282,6 +282,9 @@ class Suite:
                                            ctypes.c_size_t]
         L.zr_test_describe_fwd.argtypes = [ctypes.c_int, ZrTensor, ZrTensor, ctypes.c_void_p,
                                            i64p, ctypes.c_char_p, ctypes.c_size_t]
+        L.zr_test_describe_bwd_t.argtypes = [ctypes.c_int, ctypes.c_int, ZrTensor, ZrTensor,
+                                             ZrTensor, ctypes.c_void_p, ctypes.c_void_p,
+                                             ctypes.c_char_p, ctypes.c_size_t]
         self.es = {}
         for name in names:
             host = workloads.make_inputs(name, **(dims or {}))
@@ -425,16 +428,14 @@ class Suite:
         assert rc == 0, rc
         ws = torch.empty(max(16, need.value), dtype=torch.uint8, device=self.device)
         self._keep.append(ws)
-        launches = 0
-        if es == 4:
-            buf = ctypes.create_string_buffer(8192)
-            assert L.zr_test_describe_bwd(opc, dg, da, db, pa, pb, buf, 8192) == 0
-            desc = json.loads(buf.value.decode())
-            plans = desc.get("plans", [])
-            if plans and plans[0].get("kernel") == "sab":
-                launches = 3  # fused pass + one combine per gradient
-            else:
-                launches = sum(1 + (p.get("nslots", 1) > 1) for p in plans)
+        buf = ctypes.create_string_buffer(8192)
+        assert L.zr_test_describe_bwd_t(dtc, opc, dg, da, db, pa, pb, buf, 8192) == 0
+        desc = json.loads(buf.value.decode())
+        plans = desc.get("plans", [])
+        if plans and plans[0].get("kernel") == "sab":
+            launches = 3  # fused pass + one combine per gradient
+        else:
+            launches = sum(1 + (p.get("nslots", 1) > 1) for p in plans)
         wsz = ws.numel()
 
         def fn(dg=dg, da=da, db=db, pa=pa, pb=pb, wsp=ws.data_ptr(), wsz=wsz):

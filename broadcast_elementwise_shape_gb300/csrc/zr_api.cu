@@ -791,9 +791,16 @@ int zr_test_describe_fwd(zr_op op, zr_tensor a, zr_tensor b, const float* out,
 
 int zr_test_describe_bwd(zr_op op, zr_tensor grad_out, zr_tensor a, zr_tensor b,
                          const float* grad_a, const float* grad_b, char* buf, size_t len) {
+  return zr_test_describe_bwd_t(ZR_F32, op, grad_out, a, b, grad_a, grad_b, buf, len);
+}
+
+int zr_test_describe_bwd_t(zr_dtype dtype, zr_op op, zr_tensor grad_out, zr_tensor a, zr_tensor b,
+                           const void* grad_a, const void* grad_b, char* buf, size_t len) {
+  if (dtype != ZR_F32 && dtype != ZR_BF16) return ZR_ERR_DTYPE;
   BwdSet S;
-  const int rc = plan_bwd(op, grad_out, a, b, const_cast<float*>(grad_a),
-                          const_cast<float*>(grad_b), &S);
+  S.es = dtype == ZR_BF16 ? 2 : 4;
+  const int rc = plan_bwd(op, grad_out, a, b, static_cast<float*>(const_cast<void*>(grad_a)),
+                          static_cast<float*>(const_cast<void*>(grad_b)), &S);
   if (rc) return rc;
   std::string s;
   if (S.nothing || S.empty) {

@@ -16,12 +16,6 @@ namespace zr {
 
 // ---------------------------------------------------------------- arithmetic
 
-// The hardware's approximate reciprocal (relative error about 2^-23).
-__device__ __forceinline__ float rcp_approx(float v) {
-  float r;
-  asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(v));
-  return r;
-}
 
 // x / y correctly rounded to binary32 (round to nearest even) for x and y
 // that bfloat16 can hold (8-bit significands), without the general divide:
@@ -452,9 +446,18 @@ struct ChainF {
 // (exp(v) = 2^(v log2 e)).  Their errors (a few ulp, plus the rounding of
 // the exponent's argument, relative |v| u) stay inside the stated bound
 // (16 + 2 x^2) * 2^-24 of the exact value.
+// Both in their flush-to-zero forms, which skip the subnormal handling: the
+// reciprocal's argument is at least 1, and an exponential below 2^-126
+// (erfc or phi in their far tails) becomes 0, an absolute change below the
+// bound's 2^-120 term.
 __device__ __forceinline__ float ex2_approx(float v) {
   float r;
-  asm("ex2.approx.f32 %0, %1;" : "=f"(r) : "f"(v));
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(v));
+  return r;
+}
+__device__ __forceinline__ float rcp_approx(float v) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(v));
   return r;
 }
 __device__ __forceinline__ float erfc_cheb(float v) {

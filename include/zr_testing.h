@@ -23,6 +23,10 @@ int zr_test_describe_fwd(zr_op op, zr_tensor a, zr_tensor b, const float* out,
                          const int64_t* out_strides, char* buf, size_t len);
 int zr_test_describe_bwd(zr_op op, zr_tensor grad_out, zr_tensor a, zr_tensor b,
                          const float* grad_a, const float* grad_b, char* buf, size_t len);
+/* The same for zr_binary_bwd_t with element type `dtype` (ZR_ERR_DTYPE for
+ * an unknown one). */
+int zr_test_describe_bwd_t(zr_dtype dtype, zr_op op, zr_tensor grad_out, zr_tensor a, zr_tensor b,
+                           const void* grad_a, const void* grad_b, char* buf, size_t len);
 int zr_test_describe_sum(zr_tensor in, int32_t ndim_out, const int64_t* sizes_out,
                          const float* out, char* buf, size_t len);
 

@@ -601,3 +601,34 @@ def test_float32_only_entry_points_refuse_bf16():
         zr.zr_binary_bwd_ex("add", h, h, v, grad_a=h)
     with pytest.raises(TypeError):  # mixed element types
         zr.zr_binary_fwd("add", torch.ones(4), v[:4])
+
+
+def test_describe_bwd_bf16_plans(L):
+    """The element-type-aware plan description: bf16 plans take 8-wide
+    vectors where the layout allows and plan the grid for the bf16 kernels'
+    occupancy; an unknown element type is ZR_ERR_DTYPE."""
+    L.zr_test_describe_bwd_t.argtypes = [ctypes.c_int, ctypes.c_int, ZrTensor, ZrTensor, ZrTensor,
+                                         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_char_p,
+                                         ctypes.c_size_t]
+    T = 1 << 40
+
+    def bwd(dtype, op, sa, sb):
+        out = np.broadcast_shapes(sa, sb)
+        g, a, b = FakeT(T, out), FakeT(2 * T, sa), FakeT(3 * T, sb)
+        buf = ctypes.create_string_buffer(4096)
+        rc = L.zr_test_describe_bwd_t(dtype, op, g.desc, a.desc, b.desc, 4 * T, 5 * T, buf, 4096)
+        return rc, (json.loads(buf.value.decode()) if rc == 0 else None)
+
+    # c4 in bf16: add backward with the mask reduced over 96 rows (inner kept).
+    rc, d = bwd(1, 0, (8, 12, 1024, 1024), (1, 1, 1024, 1024))
+    assert rc == 0
+    (p,) = d["plans"]
+    assert p["vec"] == 8 and p["inner_kept"] == 1 and (p["n_red"], p["ncol"]) == (96, 1024 * 1024)
+    assert p["ctas"] % (152 * 4) == 0 or p["ctas"] >= 6 * 152 * 4
+    # The same in float: 4-wide vectors.
+    rc, d = bwd(0, 0, (8, 12, 1024, 1024), (1, 1, 1024, 1024))
+    assert rc == 0 and d["plans"][0]["vec"] == 4
+    # div by a scalar in bf16: full sum of g*a with grad_a written densely.
+    rc, d = bwd(1, 3, (8, 12, 1024, 1024), (1,))
+    assert rc == 0 and d["plans"][0]["vec"] == 8 and d["plans"][0]["dense_out"] == 1
+    assert bwd(7, 0, (4, 4), (4,))[0] == -9
