@@ -369,7 +369,9 @@ class Suite:
 
     def _prepare_unary(self, name, step, env, sizes, stream_of):
         zr, L = self.zr, self.L
-        nbytes = op_bytes(step, sizes)
+        es = self.es[name]
+        dtc = zr.ZR_BF16 if es == 2 else zr.ZR_F32
+        nbytes = op_bytes(step, sizes, es)
         uop, alpha = zr.UNARY[step[1]], float(step[2])
         out = env[step[-1]]
         ost = zr._i64(out.stride())
@@ -379,14 +381,14 @@ class Suite:
             dx = self._desc(env[step[3]])
 
             def fn(dx=dx, ptr=ptr, ost=ost):
-                rc = L.zr_unary_fwd(uop, alpha, dx, ptr, ost, stream_of())
+                rc = L.zr_unary_fwd_t(dtc, uop, alpha, dx, ptr, ost, stream_of())
                 if rc:
                     raise zr.ZrError(rc, f"{name} unary fwd")
             return (name, "fwd", step[1], nbytes, 1, fn, sizes[step[-1]])
         dg, dx = self._desc(env[step[3]]), self._desc(env[step[4]])
 
         def fn(dg=dg, dx=dx, ptr=ptr, ost=ost):
-            rc = L.zr_unary_bwd(uop, alpha, dg, dx, ptr, ost, stream_of())
+            rc = L.zr_unary_bwd_t(dtc, uop, alpha, dg, dx, ptr, ost, stream_of())
             if rc:
                 raise zr.ZrError(rc, f"{name} unary bwd")
         return (name, "bwd", step[1], nbytes, 1, fn, sizes[step[-1]])
@@ -555,7 +557,8 @@ def run_zr(args, rank, world, local):
 
     per_config = per_op_alone = None
     if rank == 0 and args.config_reps > 0:
-        extra = [Suite(["x1", "c3f", "c4f", "u1", "c4h"], device)] if args.workload == "suite" else []
+        extra = ([Suite(["x1", "c3f", "c4f", "u1", "c4h", "u1h"], device)]
+                 if args.workload == "suite" else [])
         per_config, per_op_alone = run_per_config([suite] + extra, flush, stream, args.config_reps)
     e2e = None
     if not args.no_e2e and rank == 0:

@@ -75,11 +75,14 @@ def lib() -> ctypes.CDLL:
         L.zr_binary_fwd_t.argtypes = [c_int, c_int, ZrTensor, ZrTensor, vp, i64p, vp]
         L.zr_binary_bwd_t.argtypes = [c_int, c_int, ZrTensor, ZrTensor, ZrTensor, vp, vp, vp, szp, vp]
         L.zr_sum_to_shape_t.argtypes = [c_int, ZrTensor, i32, i64p, vp, vp, szp, vp]
+        L.zr_unary_fwd_t.argtypes = [c_int, c_int, ctypes.c_float, ZrTensor, vp, i64p, vp]
+        L.zr_unary_bwd_t.argtypes = [c_int, c_int, ctypes.c_float, ZrTensor, ZrTensor, vp, i64p, vp]
         L.zr_status_string.argtypes = [c_int]
         L.zr_status_string.restype = ctypes.c_char_p
         for f in ("zr_broadcast_shape", "zr_binary_fwd", "zr_binary_bwd", "zr_sum_to_shape",
                   "zr_chain_fwd", "zr_chain_bwd", "zr_binary_bwd_ex", "zr_unary_fwd", "zr_unary_bwd",
-                  "zr_binary_fwd_t", "zr_binary_bwd_t", "zr_sum_to_shape_t"):
+                  "zr_binary_fwd_t", "zr_binary_bwd_t", "zr_sum_to_shape_t", "zr_unary_fwd_t",
+                  "zr_unary_bwd_t"):
             getattr(L, f).restype = c_int
         _lib = L
     return _lib
@@ -150,7 +153,7 @@ ZR_F32, ZR_BF16 = 0, 1
 
 
 def _float32_only(where, *ts):
-    """The chain, unary and gradient-layout entry points take float32 only."""
+    """The chain and gradient-layout entry points take float32 only."""
     import torch
     for t in ts:
         if t is not None and t.dtype != torch.float32:
@@ -325,13 +328,13 @@ def zr_unary_fwd(op, x, alpha=1.0, out=None):
     """out = op(x) for op in ("scale", "gelu"); ``out`` may be a preallocated
     (strided) tensor of x's shape, or x itself."""
     import torch
-    _float32_only("zr_unary_fwd", x, out)
+    dt = _dtype_of(x, out)
     if out is None:
-        out = torch.empty(x.shape, dtype=torch.float32, device=x.device)
+        out = torch.empty(x.shape, dtype=x.dtype, device=x.device)
     dx, kx = _desc(x)
     ost = _i64(out.stride())
-    rc = lib().zr_unary_fwd(UNARY.get(op, op), float(alpha), dx, out.data_ptr() if out.numel() else None,
-                            ost, _stream(out))
+    rc = lib().zr_unary_fwd_t(dt, UNARY.get(op, op), float(alpha), dx,
+                              out.data_ptr() if out.numel() else None, ost, _stream(out))
     _check(rc, "zr_unary_fwd")
     return out
 
@@ -339,13 +342,13 @@ def zr_unary_fwd(op, x, alpha=1.0, out=None):
 def zr_unary_bwd(op, grad_out, x, alpha=1.0, grad_x=None):
     """grad_x = grad_out * op'(x); ``x`` may be None for "scale"."""
     import torch
-    _float32_only("zr_unary_bwd", grad_out, x, grad_x)
+    dt = _dtype_of(grad_out, x, grad_x)
     if grad_x is None:
-        grad_x = torch.empty(grad_out.shape, dtype=torch.float32, device=grad_out.device)
+        grad_x = torch.empty(grad_out.shape, dtype=grad_out.dtype, device=grad_out.device)
     dg, kg = _desc(grad_out)
     dx, kx = _desc(x, tuple(grad_out.shape))
     gst = _i64(grad_x.stride())
-    rc = lib().zr_unary_bwd(UNARY.get(op, op), float(alpha), dg, dx,
-                            grad_x.data_ptr() if grad_x.numel() else None, gst, _stream(grad_out))
+    rc = lib().zr_unary_bwd_t(dt, UNARY.get(op, op), float(alpha), dg, dx,
+                              grad_x.data_ptr() if grad_x.numel() else None, gst, _stream(grad_out))
     _check(rc, "zr_unary_bwd")
     return grad_x

@@ -1674,6 +1674,7 @@ namespace zr {
 namespace {
 
 struct UnarySet {
+  int es = 4;  // bytes per stored element: 4 float, 2 bfloat16
   bool empty = false;
   EwBuild eb;
   TDesc x, g, out;
@@ -1703,9 +1704,10 @@ int plan_unary(int uop, float alpha, const zr_tensor& t0, const zr_tensor* t1, f
   }
   if (!S->g.ptr || !out || (two && !S->x.ptr)) return ZR_ERR_NULL;
   if (!non_overlapping(S->out)) return ZR_ERR_LAYOUT;
-  const Span so = span_of(out, S->out.extent);
-  if (overlaps(so, span_of(S->g.ptr, S->g.extent)) && !same_layout(S->g, S->out)) return ZR_ERR_LAYOUT;
-  if (two && overlaps(so, span_of(S->x.ptr, S->x.extent)) && !same_layout(S->x, S->out))
+  const Span so = span_of(out, S->out.extent, S->es);
+  if (overlaps(so, span_of(S->g.ptr, S->g.extent, S->es)) && !same_layout(S->g, S->out))
+    return ZR_ERR_LAYOUT;
+  if (two && overlaps(so, span_of(S->x.ptr, S->x.extent, S->es)) && !same_layout(S->x, S->out))
     return ZR_ERR_LAYOUT;
   int64_t st[kProbSlots][kMaxDims] = {};
   for (int d = 0; d < n; ++d) {
@@ -1718,6 +1720,7 @@ int plan_unary(int uop, float alpha, const zr_tensor& t0, const zr_tensor* t1, f
   const uint32_t rmask = two ? 3u : 1u;
   rc = coalesce(n, S->g.size, st, rmask | (1u << kSlotOut), kSlotOut, &P);
   if (rc) return rc;
+  P.es = S->es;
   const float* in[3] = {S->g.ptr, two ? S->x.ptr : nullptr, nullptr};
   float* outs[2] = {out, nullptr};
   rc = build_ew(P, in, outs, rmask, rmask, kOccEwFwd, &S->eb);
@@ -1733,7 +1736,15 @@ extern "C" {
 
 int zr_unary_fwd(zr_unary op, float alpha, zr_tensor x, float* out, const int64_t* out_strides,
                  zr_stream_t stream) {
+  return zr_unary_fwd_t(ZR_F32, op, alpha, x, out, out_strides, stream);
+}
+
+int zr_unary_fwd_t(zr_dtype dtype, zr_unary op, float alpha, zr_tensor x, void* out_v,
+                   const int64_t* out_strides, zr_stream_t stream) {
+  if (dtype != ZR_F32 && dtype != ZR_BF16) return ZR_ERR_DTYPE;
+  float* out = static_cast<float*>(out_v);
   UnarySet S;
+  S.es = dtype == ZR_BF16 ? 2 : 4;
   int rc = plan_unary(op, alpha, x, nullptr, out, out_strides, &S);
   if (rc || S.empty) return rc;
   for (const void* p : {static_cast<const void*>(S.g.ptr), static_cast<const void*>(out)}) {
@@ -1745,7 +1756,15 @@ int zr_unary_fwd(zr_unary op, float alpha, zr_tensor x, float* out, const int64_
 
 int zr_unary_bwd(zr_unary op, float alpha, zr_tensor grad_out, zr_tensor x, float* grad_x,
                  const int64_t* grad_x_strides, zr_stream_t stream) {
+  return zr_unary_bwd_t(ZR_F32, op, alpha, grad_out, x, grad_x, grad_x_strides, stream);
+}
+
+int zr_unary_bwd_t(zr_dtype dtype, zr_unary op, float alpha, zr_tensor grad_out, zr_tensor x,
+                   void* grad_x_v, const int64_t* grad_x_strides, zr_stream_t stream) {
+  if (dtype != ZR_F32 && dtype != ZR_BF16) return ZR_ERR_DTYPE;
+  float* grad_x = static_cast<float*>(grad_x_v);
   UnarySet S;
+  S.es = dtype == ZR_BF16 ? 2 : 4;
   // scale's backward does not read x (its sizes must still match grad_out).
   int rc = plan_unary(op, alpha, grad_out, op == UN_GELU ? &x : nullptr, grad_x, grad_x_strides,
                       &S);

@@ -483,6 +483,7 @@ template <int UOP>
 struct UnaryF {
   static constexpr bool kR1 = false, kR2 = false;
   static constexpr int kMinBlocks = kOccEwFwd;
+  static constexpr int kMinBlocksWide = kOccEwFwd;  // 8-wide bfloat16: no spill at 4
   template <int VEC>
   __device__ __forceinline__ void operator()(const Vec<VEC> (&x)[3], Vec<VEC> (&y)[2], float alpha) const {
 #pragma unroll
@@ -496,6 +497,8 @@ template <int UOP>
 struct UnaryBwdF {
   static constexpr bool kR1 = UOP == UN_GELU, kR2 = false;
   static constexpr int kMinBlocks = kOccEwFwd;
+  // 8-wide bfloat16 GeLU backward (two operand streams) needs 80 registers.
+  static constexpr int kMinBlocksWide = UOP == UN_GELU ? kOccEwFwd - 1 : kOccEwFwd;
   template <int VEC>
   __device__ __forceinline__ void operator()(const Vec<VEC> (&x)[3], Vec<VEC> (&y)[2], float alpha) const {
 #pragma unroll

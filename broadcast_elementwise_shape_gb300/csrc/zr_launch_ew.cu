@@ -91,11 +91,13 @@ cudaError_t launch_copy(const EwBuild& eb, cudaStream_t s, bool dry) {
 }
 
 cudaError_t launch_unary_fwd(int uop, const EwBuild& eb, cudaStream_t s, bool dry) {
+  if (eb.es == 2) return launch_unary_fwd_bf16(uop, eb, s, dry);
   return uop == UN_SCALE ? launch_ew_t<UnaryF<UN_SCALE>, 1>(eb, s, dry)
                          : launch_ew_t<UnaryF<UN_GELU>, 1>(eb, s, dry);
 }
 
 cudaError_t launch_unary_bwd(int uop, const EwBuild& eb, cudaStream_t s, bool dry) {
+  if (eb.es == 2) return launch_unary_bwd_bf16(uop, eb, s, dry);
   return uop == UN_SCALE ? launch_ew_t<UnaryBwdF<UN_SCALE>, 1>(eb, s, dry)
                          : launch_ew_t<UnaryBwdF<UN_GELU>, 1>(eb, s, dry);
 }

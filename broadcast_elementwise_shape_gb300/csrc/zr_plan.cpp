@@ -317,10 +317,8 @@ int build_ew(const Prob& P, const float* const in[3], float* const out[2], uint3
   uint32_t slots = read_mask | (1u << kSlotOut);
   eb->vec = pick_vec(P, slots, ptrs, out[0] && out[1] ? out[1] : nullptr);
   eb->es = P.es;
-  // 8-wide bfloat16 kernels keep the float budget except IEEE division (one
-  // CTA fewer); grids are sized with the float figure.
-
-
+  // Grids are sized with the float kernels' CTAs per SM; most 8-wide
+  // bfloat16 kernels keep that figure (WideBlocks), the others one fewer.
   const uint64_t nvcol = ceil_div(ncol, eb->vec);
   const uint64_t items = nrow * nvcol;
   uint64_t ipc = items / 1216;

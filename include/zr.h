@@ -352,6 +352,15 @@ int zr_binary_bwd_t(zr_dtype dtype, zr_op op, zr_tensor grad_out, zr_tensor a, z
 /* zr_sum_to_shape on `dtype` storage. */
 int zr_sum_to_shape_t(zr_dtype dtype, zr_tensor in, int32_t ndim_out, const int64_t* sizes_out,
                       void* out, void* workspace, size_t* workspace_bytes, zr_stream_t stream);
+/* zr_unary_fwd on `dtype` storage.  ZR_SCALE is bit-identical to the exact
+ * product rounded to bf16; ZR_GELU is within the binary32 bound above plus
+ * one bf16 unit in the last place (2^-7 of the value), since the binary32
+ * result and the exact one may round to neighbouring bf16 values. */
+int zr_unary_fwd_t(zr_dtype dtype, zr_unary op, float alpha, zr_tensor x, void* out,
+                   const int64_t* out_strides, zr_stream_t stream);
+/* zr_unary_bwd on `dtype` storage, with the same accuracy as zr_unary_fwd_t. */
+int zr_unary_bwd_t(zr_dtype dtype, zr_unary op, float alpha, zr_tensor grad_out, zr_tensor x,
+                   void* grad_x, const int64_t* grad_x_strides, zr_stream_t stream);
 
 /* Static, human-readable name of a status code. */
 const char* zr_status_string(int status);

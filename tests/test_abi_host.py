@@ -584,8 +584,9 @@ def test_backward_ex_layout_errors_and_query(L):
 
 
 def test_float32_only_entry_points_refuse_bf16():
-    """The chain, unary and gradient-layout entry points compute on float32
-    storage; the binding refuses bfloat16 tensors before any call."""
+    """The chain and gradient-layout entry points compute on float32
+    storage; the binding refuses bfloat16 tensors before any call.  The
+    unary ops take either type but not a mix."""
     import torch
     h = torch.ones(4, 8, dtype=torch.bfloat16)
     v = torch.ones(8, dtype=torch.bfloat16)
@@ -594,9 +595,9 @@ def test_float32_only_entry_points_refuse_bf16():
     with pytest.raises(TypeError):
         zr.zr_chain_bwd("mul", "add", h, h, v, v)
     with pytest.raises(TypeError):
-        zr.zr_unary_fwd("gelu", h)
+        zr.zr_unary_fwd("gelu", h, out=torch.ones(4, 8))
     with pytest.raises(TypeError):
-        zr.zr_unary_bwd("scale", h, None)
+        zr.zr_unary_bwd("gelu", h, torch.ones(4, 8))
     with pytest.raises(TypeError):
         zr.zr_binary_bwd_ex("add", h, h, v, grad_a=h)
     with pytest.raises(TypeError):  # mixed element types

@@ -190,3 +190,70 @@ def test_bf16_division_of_the_scores_workload_full_size():
     idx = np.sort(rng.choice(t.numel(), 4096, replace=False)).astype(np.int64)
     want = oracle.round_bf16(oracle.binary_fwd_at("div", t, _bf(host["scalar"]), idx))
     bitexact(_f32(out).reshape(-1)[idx], want, "c4h t / 8")
+
+
+def test_unary_ops_in_bf16():
+    """scale and GeLU on bf16 storage (zr_unary_fwd_t / zr_unary_bwd_t):
+    scale is bit-identical to the exact product rounded to bf16; GeLU is
+    within the binary32 bound plus one bf16 unit (2^-7 of the value).
+    Shapes with 8-wide rows, ragged rows, a strided view, tails and special
+    values."""
+    from parity import gelu_close
+    rng = np.random.default_rng(1600)
+    xs = [rng.standard_normal((96, 1024)) * 3, rng.standard_normal((64, 1031)) * 3,
+          np.linspace(-14, 14, 8000),
+          np.array([0.0, -0.0, 1e-40, -1e-40, -0.7518, 88.0, -88.0, np.inf, -np.inf, np.nan])]
+    for x in xs:
+        xt = _bf(torch.from_numpy(x.astype(np.float32)))
+        g = _bf(torch.from_numpy(rng.standard_normal(x.shape).astype(np.float32)))
+        xd, gd = _dev16(xt), _dev16(g)
+        for alpha in (0.125, -3.0):
+            got = _f32(zr.zr_unary_fwd("scale", xd, alpha=alpha))
+            bitexact(got, oracle.round_bf16(oracle.unary_fwd("scale", xt, alpha=alpha)),
+                     f"bf16 scale fwd {x.shape} {alpha}")
+            got = _f32(zr.zr_unary_bwd("scale", gd, None, alpha=alpha))
+            bitexact(got, oracle.round_bf16(oracle.unary_bwd("scale", g, None, alpha=alpha)[0]),
+                     f"bf16 scale bwd {x.shape} {alpha}")
+        xv = xt.numpy().astype(np.float64)
+        widen = 2.0 ** 17 / (16.0 + 2.0 * xv ** 2)  # 2^-7 |value| in units of the bound
+        ref = oracle.unary_fwd("gelu", xt)
+        got = _f32(zr.zr_unary_fwd("gelu", xd))
+        with np.errstate(all="ignore"):
+            mag = np.abs(ref.astype(np.float64))
+            gelu_close(got, ref, xv, mag * (1.0 + widen), f"bf16 gelu fwd {x.shape}")
+        gref, gmag = oracle.unary_bwd("gelu", g, xt)
+        got = _f32(zr.zr_unary_bwd("gelu", gd, xd))
+        with np.errstate(all="ignore"):
+            gelu_close(got, gref, xv, gmag + np.abs(gref.astype(np.float64)) * widen,
+                       f"bf16 gelu bwd {x.shape}")
+    # A strided bf16 view, written into a strided bf16 output.
+    base = _bf(torch.from_numpy((rng.standard_normal((96, 33, 2)) * 2).astype(np.float32)))
+    xv_t = base[:, :, 1].t()
+    out_store = torch.zeros((96, 33), dtype=torch.bfloat16, device="cuda")
+    zr.zr_unary_fwd("scale", _dev16(xv_t), alpha=0.5, out=out_store.t())
+    bitexact(_f32(out_store.t()), oracle.round_bf16(oracle.unary_fwd("scale", xv_t, alpha=0.5)),
+             "bf16 scale strided")
+
+
+def test_unary_workload_in_bf16_full_size():
+    """u1 in bf16 at full size ([16384, 3072], 8-wide plans): GeLU and scale
+    forward and backward on sampled elements (the ops are elementwise, so the
+    oracle evaluates the sampled inputs alone)."""
+    from parity import gelu_close
+    host = workloads.make_inputs("u1h")
+    x, g = _bf(host["x"]), _bf(host["g"])
+    xd, gd = _dev16(x), _dev16(g)
+    rng = np.random.default_rng(1601)
+    idx = np.unique(rng.integers(0, x.numel(), 8192))
+    xs = torch.from_numpy(x.reshape(-1).numpy()[idx])
+    gs = torch.from_numpy(g.reshape(-1).numpy()[idx])
+    xv = xs.numpy().astype(np.float64)
+    widen = 2.0 ** 17 / (16.0 + 2.0 * xv ** 2)
+    h = _f32(zr.zr_unary_fwd("gelu", xd)).reshape(-1)[idx]
+    ref = oracle.unary_fwd("gelu", xs)
+    gelu_close(h, ref, xv, np.abs(ref.astype(np.float64)) * (1.0 + widen), "u1h gelu fwd")
+    gx = _f32(zr.zr_unary_bwd("gelu", gd, xd)).reshape(-1)[idx]
+    gref, gmag = oracle.unary_bwd("gelu", gs, xs)
+    gelu_close(gx, gref, xv, gmag + np.abs(gref.astype(np.float64)) * widen, "u1h gelu bwd")
+    s = _f32(zr.zr_unary_fwd("scale", xd, alpha=0.125)).reshape(-1)[idx]
+    bitexact(s, oracle.round_bf16(oracle.unary_fwd("scale", xs, alpha=0.125)), "u1h scale fwd")

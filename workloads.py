@@ -30,6 +30,7 @@ cases with the same structure):
   backward (supplementary, outside the benchmark step)
 * ``c4h``: ``c4`` with every tensor stored as bfloat16 (the same draws,
   rounded to bf16 by the caller; see ``BF16``), supplementary
+* ``u1h``: ``u1`` stored as bfloat16 in the same way, supplementary
 * ``c3f`` and ``c4f``: the inputs of ``c3`` and ``c4`` (same seeds and
   sizes), run as one fused two-op chain each, (x * gamma) + beta and
   (scores + mask) / scalar (supplementary, outside the benchmark step)
@@ -49,9 +50,9 @@ import torch
 SEEDS = {"c1": 1001, "c2": 1002, "c3": 1003, "c4": 1004, "c5a": 1005, "c5b": 1006, "x1": 1007,
          "u1": 1008}
 # Fused-chain and bf16 workloads draw the inputs of the workload they derive from.
-BASE = {"c3f": "c3", "c4f": "c4", "c4h": "c4"}
+BASE = {"c3f": "c3", "c4f": "c4", "c4h": "c4", "u1h": "u1"}
 # Workloads whose tensors are stored as bfloat16.
-BF16 = {"c4h"}
+BF16 = {"c4h", "u1h"}
 
 DEFAULT_DIMS = {
     "c1": dict(P=32, M=64, Q=128),
@@ -88,6 +89,10 @@ STEPS = {
            ("ufwd", "scale", 0.125, "x", "s"),
            ("ubwd", "scale", 0.125, "g", "x", "grad_s"),
            ("ubwd", "gelu", 1.0, "g", "x", "grad_x")],
+    "u1h": [("ufwd", "gelu", 1.0, "x", "h"),
+            ("ufwd", "scale", 0.125, "x", "s"),
+            ("ubwd", "scale", 0.125, "g", "x", "grad_s"),
+            ("ubwd", "gelu", 1.0, "g", "x", "grad_x")],
     "c4h": [("fwd", "add", "scores", "mask", "t"),
             ("fwd", "div", "t", "scalar", "out"),
             ("bwd", "div", "g", "t", "scalar", "grad_t", "grad_scalar"),
@@ -199,6 +204,7 @@ def small_dims(name: str) -> dict:
         "x1": dict(R=333, C=1030),
         "u1": dict(R=97, C=1031),
         "c4h": dict(N=2, H=3, T=132),
+        "u1h": dict(R=97, C=1032),
         "c3f": dict(B=3, T=97, C=772),
         # 132 columns: 16-byte vectors, so the fused one-pass backward runs.
         "c4f": dict(N=2, H=3, T=132),
