@@ -17,7 +17,7 @@ import torch
 import broadcast_elementwise_shape_gb300 as zr
 import oracle
 import workloads
-from parity import bitexact, to_gpu, within
+from parity import bitexact, within
 
 pytestmark = pytest.mark.gpu
 
