@@ -561,8 +561,17 @@ def run_zr(args, rank, world, local):
                  if args.workload == "suite" else [])
         per_config, per_op_alone = run_per_config([suite] + extra, flush, stream, args.config_reps)
     e2e = None
-    if not args.no_e2e and rank == 0:
-        e2e = run_e2e(args, suite, flush, stream, nbytes)
+    if not args.no_e2e:
+        # Every rank runs its replica end to end; the job takes as long as the
+        # slowest rank, and moves every rank's bytes.
+        if world > 1:
+            dist.barrier()
+        e2e = run_e2e(args, suite, flush, stream, nbytes, measure_link=rank == 0)
+        ms = max_over_ranks(e2e["ms_per_step"], world, device)
+        e2e["value"] = round(job_gbs(world, nbytes, 1, ms), 1)
+        e2e["ms_per_step"] = round(ms, 3)
+        e2e["h2d_bytes_per_step"] *= world
+        e2e["d2h_bytes_per_step"] *= world
     if sampler:
         sampler.stop()
 
@@ -715,7 +724,7 @@ def link_rates(device, nbytes=1 << 30, reps=5):
     return out
 
 
-def run_e2e(args, suite, flush, stream, nbytes):
+def run_e2e(args, suite, flush, stream, nbytes, measure_link=True):
     """Same metric with host buffers: every step copies each input from
     pinned host memory and every output back, inside the timed region.  The
     copies are scheduled per op: an input is uploaded (on an upload stream)
@@ -790,14 +799,17 @@ def run_e2e(args, suite, flush, stream, nbytes):
             ev.append((s, e))
     torch.cuda.synchronize()
     ms = statistics.fmean(s.elapsed_time(e) for s, e in ev)
-    link = link_rates(stream.device)
     moved = (h2d + d2h) / (ms * 1e-3) / 1e9
-    return {"value": round(nbytes / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 3),
-            "steps": steps, "link_gbs": link, "copied_gbs": round(moved, 1),
-            "frac_of_link_both": round(moved / link["both"], 3) if link["both"] else None,
-            "copies": "per op: uploads ahead on one stream, ops on the caller's stream, "
-                      "downloads behind on a third stream"}
+    out = {"value": round(nbytes / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms,
+           "steps": steps, "copied_gbs": round(moved, 1),
+           "copies": "per op: uploads ahead on one stream, ops on the caller's stream, "
+                     "downloads behind on a third stream"}
+    if measure_link:  # this process's own host link (rank 0's at N > 1)
+        link = link_rates(stream.device)
+        out["link_gbs"] = link
+        out["frac_of_link_both"] = round(moved / link["both"], 3) if link["both"] else None
+    return out
 
 
 def read_traffic(call):
