@@ -84,12 +84,12 @@ cudaError_t launch_fwd_bf16(int op, const EwBuild& eb, cudaStream_t s, bool dry)
 
 cudaError_t launch_unary_fwd_bf16(int uop, const EwBuild& eb, cudaStream_t s, bool dry) {
   return uop == UN_SCALE ? launch_ew_bf16<UnaryF<UN_SCALE>, 1>(eb, s, dry)
-                         : launch_ew_bf16<UnaryF<UN_GELU>, 1>(eb, s, dry);
+                         : launch_ew_bf16<UnaryF<UN_GELU, true>, 1>(eb, s, dry);
 }
 
 cudaError_t launch_unary_bwd_bf16(int uop, const EwBuild& eb, cudaStream_t s, bool dry) {
   return uop == UN_SCALE ? launch_ew_bf16<UnaryBwdF<UN_SCALE>, 1>(eb, s, dry)
-                         : launch_ew_bf16<UnaryBwdF<UN_GELU>, 1>(eb, s, dry);
+                         : launch_ew_bf16<UnaryBwdF<UN_GELU, true>, 1>(eb, s, dry);
 }
 
 cudaError_t launch_bwd_direct_bf16(int op, int want, const EwBuild& eb, cudaStream_t s, bool dry) {

@@ -353,9 +353,12 @@ int zr_binary_bwd_t(zr_dtype dtype, zr_op op, zr_tensor grad_out, zr_tensor a, z
 int zr_sum_to_shape_t(zr_dtype dtype, zr_tensor in, int32_t ndim_out, const int64_t* sizes_out,
                       void* out, void* workspace, size_t* workspace_bytes, zr_stream_t stream);
 /* zr_unary_fwd on `dtype` storage.  ZR_SCALE is bit-identical to the exact
- * product rounded to bf16; ZR_GELU is within the binary32 bound above plus
- * one bf16 unit in the last place (2^-7 of the value), since the binary32
- * result and the exact one may round to neighbouring bf16 values. */
+ * product rounded to bf16.  ZR_GELU on bf16 evaluates erfc with a shorter
+ * polynomial fitted for bf16 results (relative error below 2^-16.3); each
+ * result is within half a bf16 unit in the last place of the exact value plus
+ * 2^-14 of its size plus 2^-120 (backward: 2^-14 of
+ * |g| (Phi(x) + |x| phi(x))), so it is the correctly rounded value except
+ * next to a rounding boundary. */
 int zr_unary_fwd_t(zr_dtype dtype, zr_unary op, float alpha, zr_tensor x, void* out,
                    const int64_t* out_strides, zr_stream_t stream);
 /* zr_unary_bwd on `dtype` storage, with the same accuracy as zr_unary_fwd_t. */

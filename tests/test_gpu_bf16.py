@@ -192,6 +192,51 @@ def test_bf16_division_of_the_scores_workload_full_size():
     bitexact(_f32(out).reshape(-1)[idx], want, "c4h t / 8")
 
 
+# GeLU in bf16 evaluates erfc with a shorter fitted polynomial (relative error
+# below 2^-16.3): the summed terms may carry 2^-14 of their size (in units of
+# the binary32 bound's 2^-24: 2^10).
+_SHORT = 2.0 ** 10
+
+
+def _ulp_bf16(v):
+    """One bf16 unit in the last place of |v| (normal range; subnormal spacing
+    below 2^-126)."""
+    v = np.abs(np.asarray(v, np.float64))
+    _, e = np.frexp(v)
+    return np.where(v >= 2.0 ** -126, np.ldexp(1.0, e - 8), 2.0 ** -133)
+
+
+def test_bf16_gelu_on_every_bf16_input():
+    """GeLU forward and backward (grad_out = 1) on all 65536 bf16 bit
+    patterns: each result is within half a bf16 unit of the exact value plus
+    2^-14 of the terms' size (the shorter erfc and binary32 rounding) plus
+    2^-120, so it is the correctly rounded value except next to a rounding
+    boundary; NaN where the exact result is NaN, infinities equal."""
+    bits = np.arange(65536, dtype=np.uint32) << 16
+    x = torch.from_numpy(bits.view(np.float32).copy())
+    xd = x.to(torch.bfloat16).cuda()
+    ones = torch.ones(65536, dtype=torch.bfloat16, device="cuda")
+    for what, got, ref, mag in (
+            ("fwd", _f32(zr.zr_unary_fwd("gelu", xd)), oracle.unary_fwd("gelu", x), None),
+            ("bwd", _f32(zr.zr_unary_bwd("gelu", ones, xd)), *oracle.unary_bwd("gelu", torch.ones(65536), x))):
+        got = got.astype(np.float64)
+        ref = ref.astype(np.float64)
+        gn, rn = np.isnan(got), np.isnan(ref)
+        assert np.array_equal(gn, rn), f"gelu {what}: NaN positions differ"
+        fin = ~gn & np.isfinite(ref)
+        assert np.array_equal(got[~gn & ~fin], ref[~gn & ~fin]), f"gelu {what}: infinities differ"
+        size = np.abs(ref) if mag is None else np.asarray(mag, np.float64)
+        allowed = 0.5 * _ulp_bf16(ref[fin]) + 2.0 ** -14 * size[fin] + 2.0 ** -120
+        err = np.abs(got[fin] - ref[fin])
+        bad = np.nonzero(err > allowed)[0]
+        assert bad.size == 0, (f"gelu {what}: {bad.size} inputs beyond the bound; first x = "
+                               f"{x.numpy()[fin][bad[0]]!r}: gpu {got[fin][bad[0]]!r} "
+                               f"exact {ref[fin][bad[0]]!r}")
+        # Away from rounding boundaries the result is the correctly rounded one.
+        exact16 = oracle.round_bf16(ref.astype(np.float32)).astype(np.float64)
+        assert np.mean(got[fin] == exact16[fin]) > 0.98, f"gelu {what}: too many off by one unit"
+
+
 def test_unary_ops_in_bf16():
     """scale and GeLU on bf16 storage (zr_unary_fwd_t / zr_unary_bwd_t):
     scale is bit-identical to the exact product rounded to bf16; GeLU is
@@ -224,8 +269,8 @@ def test_unary_ops_in_bf16():
         gref, gmag = oracle.unary_bwd("gelu", g, xt)
         got = _f32(zr.zr_unary_bwd("gelu", gd, xd))
         with np.errstate(all="ignore"):
-            gelu_close(got, gref, xv, gmag + np.abs(gref.astype(np.float64)) * widen,
-                       f"bf16 gelu bwd {x.shape}")
+            gelu_close(got, gref, xv, gmag * (1.0 + _SHORT / (16.0 + 2.0 * xv ** 2))
+                       + np.abs(gref.astype(np.float64)) * widen, f"bf16 gelu bwd {x.shape}")
     # A strided bf16 view, written into a strided bf16 output.
     base = _bf(torch.from_numpy((rng.standard_normal((96, 33, 2)) * 2).astype(np.float32)))
     xv_t = base[:, :, 1].t()
@@ -254,6 +299,7 @@ def test_unary_workload_in_bf16_full_size():
     gelu_close(h, ref, xv, np.abs(ref.astype(np.float64)) * (1.0 + widen), "u1h gelu fwd")
     gx = _f32(zr.zr_unary_bwd("gelu", gd, xd)).reshape(-1)[idx]
     gref, gmag = oracle.unary_bwd("gelu", gs, xs)
-    gelu_close(gx, gref, xv, gmag + np.abs(gref.astype(np.float64)) * widen, "u1h gelu bwd")
+    gelu_close(gx, gref, xv, gmag * (1.0 + _SHORT / (16.0 + 2.0 * xv ** 2))
+               + np.abs(gref.astype(np.float64)) * widen, "u1h gelu bwd")
     s = _f32(zr.zr_unary_fwd("scale", xd, alpha=0.125)).reshape(-1)[idx]
     bitexact(s, oracle.round_bf16(oracle.unary_fwd("scale", xs, alpha=0.125)), "u1h scale fwd")

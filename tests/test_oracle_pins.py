@@ -618,3 +618,4 @@ def test_bf16_single_ops_round_once():
         r = np.where((frac > 0.5) | ((frac == 0.5) & (np.mod(r, 2) == 1)), r + 1, r)
         want = (r * step).astype(np.float32)
         assert np.array_equal(got.view(np.uint32), want.view(np.uint32)), op
+
