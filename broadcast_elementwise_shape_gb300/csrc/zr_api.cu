@@ -1005,9 +1005,16 @@ extern "C" {
 
 int zr_test_emulate_fwd(zr_tensor a, zr_tensor b, const float* out, const int64_t* out_strides,
                         int64_t cap, int64_t* rec, int64_t* nrec) {
+  return zr_test_emulate_fwd_t(ZR_F32, a, b, out, out_strides, cap, rec, nrec);
+}
+
+int zr_test_emulate_fwd_t(zr_dtype dtype, zr_tensor a, zr_tensor b, const void* out,
+                          const int64_t* out_strides, int64_t cap, int64_t* rec, int64_t* nrec) {
   if (!rec || !nrec) return ZR_ERR_NULL;
+  if (dtype != ZR_F32 && dtype != ZR_BF16) return ZR_ERR_DTYPE;
   FwdSet S;
-  const int rc = plan_fwd(OP_ADD, a, b, out, out_strides, &S);
+  S.es = dtype == ZR_BF16 ? 2 : 4;
+  const int rc = plan_fwd(OP_ADD, a, b, static_cast<const float*>(out), out_strides, &S);
   if (rc) return rc;
   int64_t m = 0;
   bool over = false;
@@ -1043,10 +1050,18 @@ int zr_test_emulate_fwd(zr_tensor a, zr_tensor b, const float* out, const int64_
 int zr_test_emulate_bwd(zr_op op, zr_tensor grad_out, zr_tensor a, zr_tensor b,
                         const float* grad_a, const float* grad_b, int64_t cap, int64_t* rec,
                         int64_t* nrec) {
+  return zr_test_emulate_bwd_t(ZR_F32, op, grad_out, a, b, grad_a, grad_b, cap, rec, nrec);
+}
+
+int zr_test_emulate_bwd_t(zr_dtype dtype, zr_op op, zr_tensor grad_out, zr_tensor a, zr_tensor b,
+                          const void* grad_a, const void* grad_b, int64_t cap, int64_t* rec,
+                          int64_t* nrec) {
   if (!rec || !nrec) return ZR_ERR_NULL;
+  if (dtype != ZR_F32 && dtype != ZR_BF16) return ZR_ERR_DTYPE;
   BwdSet S;
-  const int rc = plan_bwd(op, grad_out, a, b, const_cast<float*>(grad_a),
-                          const_cast<float*>(grad_b), &S);
+  S.es = dtype == ZR_BF16 ? 2 : 4;
+  const int rc = plan_bwd(op, grad_out, a, b, static_cast<float*>(const_cast<void*>(grad_a)),
+                          static_cast<float*>(const_cast<void*>(grad_b)), &S);
   if (rc) return rc;
   int64_t m = 0;
   bool over = false;

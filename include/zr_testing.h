@@ -76,6 +76,13 @@ int zr_test_emulate_fwd(zr_tensor a, zr_tensor b, const float* out, const int64_
 int zr_test_emulate_bwd(zr_op op, zr_tensor grad_out, zr_tensor a, zr_tensor b,
                         const float* grad_a, const float* grad_b, int64_t cap, int64_t* rec,
                         int64_t* nrec);
+/* The two walks above for plans on `dtype` storage (ZR_ERR_DTYPE for an
+ * unknown type); offsets stay in elements. */
+int zr_test_emulate_fwd_t(zr_dtype dtype, zr_tensor a, zr_tensor b, const void* out,
+                          const int64_t* out_strides, int64_t cap, int64_t* rec, int64_t* nrec);
+int zr_test_emulate_bwd_t(zr_dtype dtype, zr_op op, zr_tensor grad_out, zr_tensor a, zr_tensor b,
+                          const void* grad_a, const void* grad_b, int64_t cap, int64_t* rec,
+                          int64_t* nrec);
 
 /* The two divisions of bfloat16 operands against the IEEE binary32 divide,
  * over every ordered pair of bfloat16 bit patterns (2^32 pairs, one kernel

@@ -633,3 +633,69 @@ def test_describe_bwd_bf16_plans(L):
     rc, d = bwd(1, 3, (8, 12, 1024, 1024), (1,))
     assert rc == 0 and d["plans"][0]["vec"] == 8 and d["plans"][0]["dense_out"] == 1
     assert bwd(7, 0, (4, 4), (4,))[0] == -9
+
+
+def _bf16_shapes(rng):
+    """Shapes whose inner dim is often a multiple of 8 (16-byte bf16 vectors)."""
+    n = int(rng.integers(1, 5))
+    out = [int(v) for v in rng.choice([1, 2, 3, 5, 8, 16, 24], n)]
+    sa = [s if rng.random() < 0.6 else 1 for s in out]
+    sb = [s if rng.random() < 0.6 else 1 for s in out]
+    sa[-1] = out[-1]
+    return tuple(sa), tuple(sb[int(rng.integers(0, n)):])
+
+
+def test_emulated_bf16_plans_match_naive(L):
+    """bf16 plans (8-wide vectors where rows and 2-byte-element pointers are
+    16-byte aligned, else 4 or 1): the host walk of every planned forward and
+    backward kernel visits each output element once, with the offsets and
+    gradient indices of the definition."""
+    L.zr_test_emulate_fwd_t.argtypes = [ctypes.c_int, ZrTensor, ZrTensor, ctypes.c_void_p,
+                                        ctypes.POINTER(ctypes.c_int64), ctypes.c_int64,
+                                        ctypes.POINTER(ctypes.c_int64),
+                                        ctypes.POINTER(ctypes.c_int64)]
+    L.zr_test_emulate_bwd_t.argtypes = [ctypes.c_int, ctypes.c_int, ZrTensor, ZrTensor, ZrTensor,
+                                        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
+                                        ctypes.POINTER(ctypes.c_int64),
+                                        ctypes.POINTER(ctypes.c_int64)]
+    L.zr_test_describe_bwd_t.argtypes = [ctypes.c_int, ctypes.c_int, ZrTensor, ZrTensor, ZrTensor,
+                                         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_char_p,
+                                         ctypes.c_size_t]
+    rng = np.random.default_rng(77)
+    vecs = set()
+    for it in range(300):
+        sa, sb = _bf16_shapes(rng)
+        out_shape = np.broadcast_shapes(sa, sb)
+        n_out = int(np.prod(out_shape))
+        a = rand_view(rng, sa, 0x100000 + 2 * int(rng.integers(0, 8)))
+        b = rand_view(rng, sb, 0x900000 + 2 * int(rng.integers(0, 2)))
+        ost = dense_strides(out_shape)
+        cap = n_out + 8
+        rec = (ctypes.c_int64 * (3 * cap))()
+        nrec = ctypes.c_int64()
+        assert L.zr_test_emulate_fwd_t(1, a.desc, b.desc, 0x4000000, _i64(ost), cap, rec,
+                                       ctypes.byref(nrec)) == 0
+        r = np.frombuffer(rec, np.int64)[: 3 * nrec.value].reshape(-1, 3)
+        assert r.shape[0] == n_out
+        order = np.argsort(r[:, 0])
+        np.testing.assert_array_equal(r[order, 0], np.arange(n_out))
+        np.testing.assert_array_equal(r[order, 1], naive_offsets(out_shape, sa, a.strides).ravel())
+        np.testing.assert_array_equal(r[order, 2], naive_offsets(out_shape, sb, b.strides).ravel())
+        # Backward of mul (both operands read), both gradients requested.
+        g = rand_view(rng, out_shape, 0x200000 + 2 * int(rng.integers(0, 8)))
+        buf = ctypes.create_string_buffer(8192)
+        assert L.zr_test_describe_bwd_t(1, 2, g.desc, a.desc, b.desc, 0x5000000, 0x6000000, buf,
+                                        8192) == 0
+        desc = json.loads(buf.value.decode())
+        for p in desc.get("plans", []):
+            vecs.add(p.get("vec"))
+        rec = (ctypes.c_int64 * (7 * (2 * n_out + 8)))()
+        assert L.zr_test_emulate_bwd_t(1, 2, g.desc, a.desc, b.desc, 0x5000000, 0x6000000,
+                                       2 * n_out + 8, rec, ctypes.byref(nrec)) == 0
+        rr = np.frombuffer(rec, np.int64)[: 7 * nrec.value].reshape(-1, 7)
+        go = naive_offsets(out_shape, out_shape, g.strides).ravel()
+        for pi in range(len(desc.get("plans", []))):
+            rp = rr[rr[:, 0] == pi]
+            assert rp.shape[0] == n_out
+            np.testing.assert_array_equal(np.sort(rp[:, 1]), np.sort(go))
+    assert 8 in vecs and (4 in vecs or 1 in vecs)
