@@ -104,11 +104,22 @@ def job_gbs(world, step_bytes, steps, total_ms):
     return world * step_bytes * steps / (total_ms * 1e-3) / 1e9
 
 
+def _code_only(text):
+    """C++ source without comments and blank lines (a change to a comment
+    leaves the compiled kernels, and so their measured traffic, as they are)."""
+    import re
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+
+
 def kernel_hash():
+    """Hash of the code of the kernel sources: profiles/traffic.json holds the
+    ncu-measured traffic under the hash of the code it was measured on."""
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, f), encoding="utf-8") as fh:
+            h.update(_code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

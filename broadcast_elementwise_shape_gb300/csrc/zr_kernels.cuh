@@ -384,7 +384,8 @@ __device__ __forceinline__ void store_cols(E* __restrict__ base, int64_t row_off
 
 // ---------------------------------------------------------------- functors
 
-// Forward: out = a op b.  SHORT: operands are bfloat16 values (quot_short).
+// Forward: out = a op b.  SHORT: operands are bfloat16 values (fwd_vec's
+// division for stored bfloat16 results).
 // B_ONE: b has one element, read once per thread (its reciprocal and range
 // check are then loop-invariant).
 template <int OP, bool SHORT = false, bool B_ONE = false>
@@ -853,7 +854,8 @@ k_reduce(const __grid_constant__ RedPlan p) {
   const E* bE = reinterpret_cast<const E*>(p.b);
   E* xE = reinterpret_cast<E*>(p.x_final);
   E* dE = reinterpret_cast<E*>(p.d_out);
-  // bfloat16 operands divide with quot_short.
+  // bfloat16 operands divide by the forms for short operands (term_a_vec,
+  // term_b_vec).
   using T = RedTerms<OP, WHICH, sizeof(E) == 2>;
   extern __shared__ int64_t s_dyn[];
   const uint32_t table_rows = p.rows_per_blk < kMaxTileRows ? p.rows_per_blk : kMaxTileRows;

@@ -95,7 +95,8 @@ cudaError_t launch_bwd_direct_bf16(int op, int want, const EwBuild& eb, cudaStre
 cudaError_t launch_copy_bf16(const EwBuild& eb, cudaStream_t s, bool dry);
 cudaError_t launch_unary_fwd_bf16(int uop, const EwBuild& eb, cudaStream_t s, bool dry);
 cudaError_t launch_unary_bwd_bf16(int uop, const EwBuild& eb, cudaStream_t s, bool dry);
-// Test kernel: quot_short against the IEEE divide over all bfloat16 pairs.
+// Test kernel: the two bfloat16 divisions against the IEEE divide over all
+// bfloat16 pairs.
 cudaError_t launch_div_short_check(unsigned long long* out, cudaStream_t s);
 cudaError_t launch_reduce_bf16(int op, int which, const RedBuild& rb, cudaStream_t s, bool dry);
 
