@@ -45,3 +45,13 @@ def test_oracle_pool_runs_every_process_over_the_whole_sample():
         pool.close()
     assert pool.n == 2 and nbytes == 2 * one_bytes and span > 0
     assert all(not p.is_alive() for p in pool.procs)
+
+
+def test_kernel_hash_covers_code_only():
+    """Comments and blank lines do not change the key of the measured traffic;
+    code does."""
+    a = "int f() {  // one\n  /* two\n three */ return 1;\n\n}\n"
+    b = "int f() {\n  return 1;\n}\n"
+    c = "int f() {\n  return 2;\n}\n"
+    assert bench._code_only(a) == bench._code_only(b) != bench._code_only(c)
+    assert bench.kernel_hash() == bench.kernel_hash()
