@@ -105,12 +105,13 @@ def job_gbs(world, step_bytes, steps, total_ms):
 
 
 def _code_only(text):
-    """C++ source without comments and blank lines (a change to a comment
-    leaves the compiled kernels, and so their measured traffic, as they are)."""
+    """C++ source without comments, blank lines and spacing (a change to a
+    comment or to layout leaves the compiled kernels, and so their measured
+    traffic, as they are)."""
     import re
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     text = re.sub(r"//[^\n]*", "", text)
-    return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+    return "\n".join(" ".join(line.split()) for line in text.splitlines() if line.strip())
 
 
 def kernel_hash():
