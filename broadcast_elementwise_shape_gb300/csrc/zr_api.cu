@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <string>
@@ -468,6 +470,60 @@ int copy_json(const std::string& s, char* buf, size_t len) {
   return ZR_OK;
 }
 
+
+// Plan descriptions (JSON) shared by the test hooks and the trace.
+std::string fwd_json(const FwdSet& S) {
+  if (S.empty) return "{\"kernel\":\"none\"}";
+  if (S.tr) return describe_tr(S.tp);
+  if (S.sabf) return describe_sabf(S.sp, S.sp_rpt);
+  return describe_ew(S.eb);
+}
+
+std::string bwd_json(const BwdSet& S) {
+  if (S.nothing || S.empty)
+    return "{\"kernel\":\"none\",\"ws_query\":" + std::to_string(S.ws_query) + "}";
+  if (S.direct)
+    return "{\"plans\":[" + describe_ew(S.eb) + "],\"ws_run\":0,\"ws_query\":" +
+           std::to_string(S.ws_query) + "}";
+  if (S.sab) {
+    const std::string d = describe_sab(S.sb);
+    return "{\"plans\":[" + d.substr(0, d.size() - 1) + ",\"nslots\":" +
+           std::to_string(S.sb.plan.slots_a) + "}," + d.substr(0, d.size() - 1) + ",\"nslots\":" +
+           std::to_string(S.sb.plan.n_tiles) + "}],\"which\":[0,1],\"ws_run\":" +
+           std::to_string(S.ws_run) + ",\"ws_query\":" + std::to_string(S.ws_query) + "}";
+  }
+  std::string s = "{\"plans\":[";
+  for (int i = 0; i < S.nred; ++i) {
+    if (i) s += ",";
+    s += describe_red(S.rb[i]);
+  }
+  return s + "],\"which\":[" + std::to_string(S.which[0]) +
+         (S.nred > 1 ? "," + std::to_string(S.which[1]) : std::string()) +
+         "],\"ws_run\":" + std::to_string(S.ws_run) + ",\"ws_query\":" + std::to_string(S.ws_query) +
+         "}";
+}
+
+std::string sum_json(const SumSet& S) {
+  if (S.empty) return "{\"kernel\":\"none\"}";
+  if (S.copy) return "{\"plans\":[" + describe_ew(S.eb) + "],\"ws_query\":0}";
+  return "{\"plans\":[" + describe_red(S.rb) + "],\"ws_query\":" + std::to_string(S.ws_query) + "}";
+}
+
+// ZR_TRACE set (and not "0"): every forward, backward and sum-to-shape call
+// that is about to launch writes one line "zr_trace <entry> <plan JSON>" to
+// stderr.  Read once per process.
+bool trace_on() {
+  static const bool on = [] {
+    const char* e = std::getenv("ZR_TRACE");
+    return e != nullptr && e[0] != '\0' && !(e[0] == '0' && e[1] == '\0');
+  }();
+  return on;
+}
+
+void trace(const char* entry, const std::string& json) {
+  std::fprintf(stderr, "zr_trace %s %s\n", entry, json.c_str());
+}
+
 }  // namespace
 }  // namespace zr
 
@@ -495,6 +551,7 @@ static int binary_fwd_es(int es, zr_op op, zr_tensor a, zr_tensor b, float* out,
   S.es = es;
   int rc = plan_fwd(op, a, b, out, out_strides, &S);
   if (rc) return rc;
+  if (trace_on()) trace("zr_binary_fwd", fwd_json(S));
   if (S.empty) return ZR_OK;
   for (const void* p : {static_cast<const void*>(S.a.ptr), static_cast<const void*>(S.b.ptr),
                         static_cast<const void*>(out)}) {
@@ -519,6 +576,7 @@ static int binary_bwd_es(int es, zr_op op, zr_tensor grad_out, zr_tensor a, zr_t
     *workspace_bytes = S.ws_query;
     return ZR_OK;
   }
+  if (trace_on()) trace("zr_binary_bwd", bwd_json(S));
   if (S.nothing) return ZR_OK;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (S.empty) {
@@ -645,6 +703,7 @@ static int sum_to_shape_es(int es, zr_tensor in, int32_t ndim_out, const int64_t
     *workspace_bytes = S.ws_query;
     return ZR_OK;
   }
+  if (trace_on()) trace("zr_sum_to_shape", sum_json(S));
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (S.empty) {
     if (!S.zero_ptr) return ZR_OK;
@@ -783,10 +842,7 @@ int zr_test_describe_fwd(zr_op op, zr_tensor a, zr_tensor b, const float* out,
   FwdSet S;
   const int rc = plan_fwd(op, a, b, out, out_strides, &S);
   if (rc) return rc;
-  return copy_json(S.empty ? std::string("{\"kernel\":\"none\"}")
-                           : (S.tr ? describe_tr(S.tp)
-                                   : (S.sabf ? describe_sabf(S.sp, S.sp_rpt) : describe_ew(S.eb))),
-                   buf, len);
+  return copy_json(fwd_json(S), buf, len);
 }
 
 int zr_test_describe_bwd(zr_op op, zr_tensor grad_out, zr_tensor a, zr_tensor b,
@@ -802,29 +858,7 @@ int zr_test_describe_bwd_t(zr_dtype dtype, zr_op op, zr_tensor grad_out, zr_tens
   const int rc = plan_bwd(op, grad_out, a, b, static_cast<float*>(const_cast<void*>(grad_a)),
                           static_cast<float*>(const_cast<void*>(grad_b)), &S);
   if (rc) return rc;
-  std::string s;
-  if (S.nothing || S.empty) {
-    s = "{\"kernel\":\"none\",\"ws_query\":" + std::to_string(S.ws_query) + "}";
-  } else if (S.direct) {
-    s = "{\"plans\":[" + describe_ew(S.eb) + "],\"ws_run\":0,\"ws_query\":" +
-        std::to_string(S.ws_query) + "}";
-  } else if (S.sab) {
-    const std::string d = describe_sab(S.sb);
-    s = "{\"plans\":[" + d.substr(0, d.size() - 1) + ",\"nslots\":" +
-        std::to_string(S.sb.plan.slots_a) + "}," + d.substr(0, d.size() - 1) + ",\"nslots\":" +
-        std::to_string(S.sb.plan.n_tiles) + "}],\"which\":[0,1],\"ws_run\":" +
-        std::to_string(S.ws_run) + ",\"ws_query\":" + std::to_string(S.ws_query) + "}";
-  } else {
-    s = "{\"plans\":[";
-    for (int i = 0; i < S.nred; ++i) {
-      if (i) s += ",";
-      s += describe_red(S.rb[i]);
-    }
-    s += "],\"which\":[" + std::to_string(S.which[0]) +
-         (S.nred > 1 ? "," + std::to_string(S.which[1]) : std::string()) +
-         "],\"ws_run\":" + std::to_string(S.ws_run) + ",\"ws_query\":" + std::to_string(S.ws_query) + "}";
-  }
-  return copy_json(s, buf, len);
+  return copy_json(bwd_json(S), buf, len);
 }
 
 int zr_test_describe_sum(zr_tensor in, int32_t ndim_out, const int64_t* sizes_out,
@@ -832,11 +866,7 @@ int zr_test_describe_sum(zr_tensor in, int32_t ndim_out, const int64_t* sizes_ou
   SumSet S;
   const int rc = plan_sum(in, ndim_out, sizes_out, const_cast<float*>(out), &S);
   if (rc) return rc;
-  std::string s;
-  if (S.empty) s = "{\"kernel\":\"none\"}";
-  else if (S.copy) s = "{\"plans\":[" + describe_ew(S.eb) + "],\"ws_query\":0}";
-  else s = "{\"plans\":[" + describe_red(S.rb) + "],\"ws_query\":" + std::to_string(S.ws_query) + "}";
-  return copy_json(s, buf, len);
+  return copy_json(sum_json(S), buf, len);
 }
 
 }  // extern "C"

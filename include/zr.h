@@ -44,6 +44,13 @@
  * the host link.  Any other pointer (pageable host memory, another device's
  * memory, a pinned buffer with a different device alias) is ZR_ERR_DEVICE.
  * The caller owns the memory and the stream.
+ *
+ * Tracing.  With the environment variable ZR_TRACE set (and not "0") when
+ * the library is first used, every zr_binary_fwd, zr_binary_bwd and
+ * zr_sum_to_shape call (and their _t forms) that passes planning writes one
+ * line "zr_trace <entry point> <plan as JSON>" to stderr before its device
+ * checks and launches: the kernels, vector width, tiling, grid and
+ * workspace it chose.
  */
 #ifndef ZR_H_
 #define ZR_H_

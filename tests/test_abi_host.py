@@ -699,3 +699,44 @@ def test_emulated_bf16_plans_match_naive(L):
             assert rp.shape[0] == n_out
             np.testing.assert_array_equal(np.sort(rp[:, 1]), np.sort(go))
     assert 8 in vecs and (4 in vecs or 1 in vecs)
+
+
+def test_trace_prints_the_plan_of_each_call():
+    """With ZR_TRACE=1 every forward, backward and sum-to-shape call that
+    passes planning prints its plan to stderr (here the device checks then
+    fail: no GPU, fake pointers); without it nothing is printed."""
+    import subprocess
+    import sys
+    code = r"""
+import ctypes, sys
+sys.path.insert(0, %r)
+import broadcast_elementwise_shape_gb300 as zr
+L = zr.lib()
+def T(addr, shape):
+    st = []; s = 1
+    for d in reversed(shape): st.insert(0, s); s *= d
+    sz, stt = zr._i64(shape), zr._i64(st)
+    T.keep.append((sz, stt))
+    return zr.ZrTensor(addr, len(shape), sz, stt)
+T.keep = []
+a, b = T(1 << 40, (64, 32)), T(2 << 40, (32,))
+rc1 = L.zr_binary_fwd(0, a, b, ctypes.c_void_p(3 << 40), None, None)
+n = ctypes.c_size_t(1 << 20)
+rc2 = L.zr_binary_bwd(2, T(4 << 40, (64, 32)), a, b, ctypes.c_void_p(5 << 40), ctypes.c_void_p(6 << 40),
+                      ctypes.c_void_p(7 << 40), ctypes.byref(n), None)
+print(rc1, rc2)
+""" % ROOT
+    env = dict(os.environ, ZR_TRACE="1")
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env,
+                       timeout=120)
+    assert r.returncode == 0, r.stderr
+    lines = [ln for ln in r.stderr.splitlines() if ln.startswith("zr_trace ")]
+    assert lines[0].startswith('zr_trace zr_binary_fwd {"kernel":"elementwise"'), lines
+    assert lines[1].startswith('zr_trace zr_binary_bwd {"plans":[{"kernel":"reduce"'), lines
+    json.loads(lines[1].split(" ", 2)[2])
+    rcs = [int(v) for v in r.stdout.split()]
+    assert all(rc in (-6, -8) for rc in rcs), rcs  # device checks fail without a GPU
+    env["ZR_TRACE"] = "0"
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env,
+                       timeout=120)
+    assert "zr_trace" not in r.stderr
