@@ -719,8 +719,24 @@ def link_rates(device, nbytes=1 << 30, reps=5):
         cur.wait_event(s1.record_event())
         cur.wait_event(s2.record_event())
 
+    # The library's own forward reading its input straight from pinned host
+    # memory (the C ABI takes a pinned pointer the device addresses as is):
+    # out = h_src + 0 into device memory; rate = host bytes read per second.
+    import broadcast_elementwise_shape_gb300 as zr
+    zero = torch.zeros(1, dtype=torch.float32, device=device)
+    da, ka = zr._desc(h_src.view(1, n), need_data=False)
+    da.data = h_src.data_ptr()
+    db, kb = zr._desc(zero)
+
+    def zero_copy():
+        rc = zr.lib().zr_binary_fwd(0, da, db, ctypes.c_void_p(d_dst.data_ptr()), None,
+                                    ctypes.c_void_p(cur.cuda_stream))
+        if rc:
+            raise zr.ZrError(rc, "zero-copy forward")
+
     out = {}
-    for key, fn, moved in (("h2d", up, nbytes), ("d2h", down, nbytes), ("both", both, 2 * nbytes)):
+    for key, fn, moved in (("h2d", up, nbytes), ("d2h", down, nbytes), ("both", both, 2 * nbytes),
+                           ("kernel_reads_host", zero_copy, nbytes)):
         fn()
         torch.cuda.synchronize(device)
         ts = []
