@@ -16,7 +16,6 @@ namespace zr {
 
 // ---------------------------------------------------------------- arithmetic
 
-
 // x / y correctly rounded to binary32 (round to nearest even) for x and y
 // that bfloat16 can hold (8-bit significands), without the general divide:
 // an approximate quotient and one correction with the exact residual, as in
@@ -172,8 +171,10 @@ __device__ __forceinline__ void quot_short(const Vec<VEC>& x, const Vec<VEC>& y,
 // below 2^-22, and x / y is never exactly halfway between two bfloat16
 // numbers and otherwise more than 2^-18 (relative) away from every halfway
 // point: a halfway point is N 2^t with N odd, 2^8 < N < 2^9, and x = A 2^i,
-// y = B 2^j with A, B below 2^8 give |x/y - N 2^t| >= 2^(t+j) / y, about
-// x / (B N) (A = N B odd-part-wise is impossible).  So q and x / y round to
+// y = B 2^j with A, B below 2^8 make x - N 2^t y a nonzero multiple of
+// 2^min(i, t+j) (A = N B odd-part-wise is impossible), so
+// |x/y - N 2^t| >= 2^min(i, t+j) / y, relatively at least about
+// 1 / (B N) > 2^-17.  So q and x / y round to
 // the same bfloat16 number, which is RN(RN(x / y)) by the innocuous double
 // rounding of 24 >= 2 * 8 + 2 bits.  Valid when every pair passes
 // div_fast_ok (q is then a normal number); otherwise the IEEE divide for all.
