@@ -924,6 +924,11 @@ k_reduce(const __grid_constant__ RedPlan p) {
     const uint32_t items = ncs * nrs;
     uint32_t rm = 0, cm = 0;
     constexpr int U = CL ? red_cl_unroll(OP) : 4;
+    // bfloat16 with the inner dim reduced: a vector's 8 products are added
+    // by a 3-level tree before the per-thread Kahan sum (fewer instructions
+    // for the 2-byte stream; the products' roundings and the tree add at
+    // most 4u of each term's size, far inside the tolerance).
+    constexpr bool kPairwise = !INNER_KEPT && sizeof(E) == 2;
     for (uint32_t m0 = 0; m0 < items; m0 += U) {
       Raw<E, VEC> gr[U], ar[U], br[U];
       uint32_t ri[U], cc[U];
@@ -951,6 +956,7 @@ k_reduce(const __grid_constant__ RedPlan p) {
         if ((T::kXa || T::kDa) && read_a && WHICH != 0) av = unpack<VEC>(ar[u]);
         if ((T::kXb || T::kDb) && read_b && WHICH != 1) bv = unpack<VEC>(br[u]);
         Vec<VEC> aw, bw;
+        float pr[VEC];
 #pragma unroll
         for (int i = 0; i < VEC; ++i) {
           const float aa = ((T::kXa || T::kDa) && read_a) ? (WHICH == 0 ? own.v[i] : av.v[i]) : 0.f;
@@ -958,7 +964,17 @@ k_reduce(const __grid_constant__ RedPlan p) {
           aw.v[i] = aa;
           bw.v[i] = bb;
           if (INNER_KEPT) acc[i].add_prod(gv.v[i], T::m(aa, bb));
+          else if (kPairwise) pr[i] = __fmul_rn(gv.v[i], T::m(aa, bb));
           else acc[0].add_prod(gv.v[i], T::m(aa, bb));
+        }
+        if (kPairwise) {
+          // The vector's products by a fixed pairwise tree, then one
+          // compensated addition.
+#pragma unroll
+          for (int w = 1; w < VEC; w *= 2)
+#pragma unroll
+            for (int i = 0; i + w < VEC; i += 2 * w) pr[i] = __fadd_rn(pr[i], pr[i + w]);
+          acc[0].add(pr[0]);
         }
         if (has_d) {
           Vec<VEC> dv;
