@@ -740,3 +740,44 @@ print(rc1, rc2)
     r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env,
                        timeout=120)
     assert "zr_trace" not in r.stderr
+
+
+def test_emulated_eight_dim_plans_match_naive(L):
+    """Rank 8 (the maximum) with broadcasting on every dim pattern: the host
+    walks of the forward and backward plans visit every element once with
+    the definition's offsets and gradient indices."""
+    rng = np.random.default_rng(88)
+    for it in range(40):
+        out = [int(v) for v in rng.choice([1, 2, 3], 8)]
+        sa = tuple(s if rng.random() < 0.6 else 1 for s in out)
+        sb = tuple(s if rng.random() < 0.6 else 1 for s in out)
+        out_shape = np.broadcast_shapes(sa, sb)
+        n_out = int(np.prod(out_shape))
+        a = rand_view(rng, sa, 0x100000)
+        b = rand_view(rng, sb, 0x900000)
+        rec = (ctypes.c_int64 * (3 * (n_out + 8)))()
+        nrec = ctypes.c_int64()
+        assert L.zr_test_emulate_fwd(a.desc, b.desc, 0x4000000, None, n_out + 8, rec,
+                                     ctypes.byref(nrec)) == 0
+        r = np.frombuffer(rec, np.int64)[: 3 * nrec.value].reshape(-1, 3)
+        order = np.argsort(r[:, 0])
+        np.testing.assert_array_equal(r[order, 0], np.arange(n_out))
+        np.testing.assert_array_equal(r[order, 1], naive_offsets(out_shape, sa, a.strides).ravel())
+        np.testing.assert_array_equal(r[order, 2], naive_offsets(out_shape, sb, b.strides).ravel())
+        g = rand_view(rng, out_shape, 0x200000)
+        rec = (ctypes.c_int64 * (7 * (2 * n_out + 8)))()
+        assert L.zr_test_emulate_bwd(3, g.desc, a.desc, b.desc, 0x5000000, 0x6000000, 2 * n_out + 8,
+                                     rec, ctypes.byref(nrec)) == 0
+        rr = np.frombuffer(rec, np.int64)[: 7 * nrec.value].reshape(-1, 7)
+        go = naive_offsets(out_shape, out_shape, g.strides).ravel()
+        xa = grad_index(out_shape, sa).ravel()
+        xb = grad_index(out_shape, sb).ravel()
+        for pi in np.unique(rr[:, 0]):
+            rp = rr[rr[:, 0] == pi]
+            assert rp.shape[0] == n_out
+            order = np.argsort(rp[:, 1])
+            ref = np.argsort(go)
+            np.testing.assert_array_equal(rp[order, 1], go[ref])
+            x = rp[order, 4]
+            if x[0] != -1:
+                assert np.array_equal(x, xa[ref]) or np.array_equal(x, xb[ref])
