@@ -366,8 +366,9 @@ struct CombinePlan {
   uint64_t split;           // nout when every output goes to out
   uint64_t nout;
   uint32_t nslots;
-  uint32_t jx, sy;          // thread layout: jx outputs x sy slot lanes
+  uint32_t jx, sy;          // thread layout: jx output groups x sy slot lanes
   float scale;
+  uint32_t vec;             // outputs per group (1, or 4 with 16-byte partial loads)
 };
 
 }  // namespace zr

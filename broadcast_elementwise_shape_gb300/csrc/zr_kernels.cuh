@@ -1074,44 +1074,71 @@ k_reduce(const __grid_constant__ RedPlan p) {
 
 // Second pass: for each output j, add its nslots partials in slot order.
 // Thread (jx lane, sy lane) adds slots sy, sy + sy_n, ... (Kahan), then a
-// fixed tree over the sy lanes.
-template <class E = float>
+// fixed tree over the sy lanes.  V = 4: each thread takes 4 consecutive
+// outputs with 16-byte loads of the partials (more bytes in flight per
+// thread; the launcher takes it when the outputs and slots are aligned).
+template <class E = float, int V = 1>
 static __global__ void __launch_bounds__(kThreads)
 k_combine(const __grid_constant__ CombinePlan p) {
   pdl_trigger();
   pdl_wait();
-  __shared__ float s_red[kThreads];
+  __shared__ float s_red[kThreads * V];
   const uint32_t jl = threadIdx.x % p.jx;
   const uint32_t sl = threadIdx.x / p.jx;
-  const uint64_t j = uint64_t(blockIdx.x) * p.jx + jl;
-  Kahan acc;
-  acc.init();
+  const uint64_t j = (uint64_t(blockIdx.x) * p.jx + jl) * V;
+  Kahan acc[V];
+#pragma unroll
+  for (int i = 0; i < V; ++i) acc[i].init();
   if (j < p.nout && sl < p.sy) {
-    // Up to eight partials are loaded before any is added, so their loads
-    // overlap (a ragged last batch is predicated, not walked one by one).
+    // Up to eight partials (vectors) are loaded before any is added, so
+    // their loads overlap (a ragged last batch is predicated, not walked one
+    // by one).
     const float* src = p.partial + uint64_t(sl) * p.nout + j;
     const uint64_t step = uint64_t(p.sy) * p.nout;
     for (uint32_t s = sl; s < p.nslots; s += 8 * p.sy, src += 8 * step) {
-      float v[8];
+      Vec<V> v[8];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) v[u] = s + u * p.sy < p.nslots ? __ldg(src + u * step) : 0.f;
+      for (int u = 0; u < 8; ++u) {
+        const bool in = s + u * p.sy < p.nslots;
+        if constexpr (V == 4) {
+          const float4 q = in ? __ldg(reinterpret_cast<const float4*>(src + u * step))
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+          v[u].v[0] = q.x; v[u].v[1] = q.y; v[u].v[2] = q.z; v[u].v[3] = q.w;
+        } else {
+          v[u].v[0] = in ? __ldg(src + u * step) : 0.f;
+        }
+      }
 #pragma unroll
       for (int u = 0; u < 8; ++u)
-        if (s + u * p.sy < p.nslots) acc.add(v[u]);
+        if (s + u * p.sy < p.nslots) {
+#pragma unroll
+          for (int i = 0; i < V; ++i) acc[i].add(v[u].v[i]);
+        }
     }
   }
   const uint32_t syn = blockDim.x / p.jx;  // power of two
-  s_red[sl * p.jx + jl] = (sl < p.sy) ? acc.s : 0.f;
+#pragma unroll
+  for (int i = 0; i < V; ++i) s_red[(sl * p.jx + jl) * V + i] = (sl < p.sy) ? acc[i].s : 0.f;
   for (uint32_t h = syn >> 1; h > 0; h >>= 1) {
     __syncthreads();
-    if (sl < h) s_red[sl * p.jx + jl] = __fadd_rn(s_red[sl * p.jx + jl], s_red[(sl + h) * p.jx + jl]);
+    if (sl < h) {
+#pragma unroll
+      for (int i = 0; i < V; ++i)
+        s_red[(sl * p.jx + jl) * V + i] =
+            __fadd_rn(s_red[(sl * p.jx + jl) * V + i], s_red[((sl + h) * p.jx + jl) * V + i]);
+    }
   }
   __syncthreads();
   if (sl == 0 && j < p.nout) {
-    const float v = __fmul_rn(s_red[jl], p.scale);
     E* out = reinterpret_cast<E*>(p.out);
     E* out2 = reinterpret_cast<E*>(p.out2);
-    st1(j < p.split ? out + j : out2 + (j - p.split), v);
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+      const uint64_t jj = j + i;
+      if (jj >= p.nout) break;
+      const float v = __fmul_rn(s_red[jl * V + i], p.scale);
+      st1(jj < p.split ? out + jj : out2 + (jj - p.split), v);
+    }
   }
 }
 

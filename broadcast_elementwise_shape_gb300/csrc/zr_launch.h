@@ -93,6 +93,10 @@ cudaError_t occupancy_other(int which, int* planned, int* actual);
 cudaError_t launch_fwd_bf16(int op, const EwBuild& eb, cudaStream_t s, bool dry);
 cudaError_t launch_bwd_direct_bf16(int op, int want, const EwBuild& eb, cudaStream_t s, bool dry);
 cudaError_t launch_copy_bf16(const EwBuild& eb, cudaStream_t s, bool dry);
+// Second pass of a reduction whose partial pointer is set: 4 outputs per
+// thread where combine_vectorize allows it.
+cudaError_t launch_combine_f32(CombinePlan c, cudaStream_t s);
+cudaError_t launch_combine_bf16(CombinePlan c, cudaStream_t s);
 cudaError_t launch_unary_fwd_bf16(int uop, const EwBuild& eb, cudaStream_t s, bool dry);
 cudaError_t launch_unary_bwd_bf16(int uop, const EwBuild& eb, cudaStream_t s, bool dry);
 // Test kernel: the two bfloat16 divisions against the IEEE divide over all

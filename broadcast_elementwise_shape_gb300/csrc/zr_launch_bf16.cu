@@ -59,9 +59,7 @@ cudaError_t red_bf16(const RedBuild& rb, cudaStream_t s, bool dry) {
                       : launch_k(k_reduce<OP, WHICH, 1, false, false, bf16>, p.n_cta, kThreads, smem, s, p);
   }
   if (e != cudaSuccess || p.nslots <= 1) return e;
-  const CombinePlan& c = rb.comb;
-  const uint64_t nblk = (c.nout + c.jx - 1) / c.jx;
-  return launch_k(k_combine<bf16>, static_cast<unsigned>(nblk), kThreads, 0, s, c);
+  return launch_combine_bf16(rb.comb, s);
 }
 
 template <int OP>
@@ -70,6 +68,13 @@ cudaError_t red_op_bf16(int which, const RedBuild& rb, cudaStream_t s, bool dry)
 }
 
 }  // namespace
+
+cudaError_t launch_combine_bf16(CombinePlan c, cudaStream_t s) {
+  combine_vectorize(&c);
+  const unsigned nblk = static_cast<unsigned>(combine_blocks(c));
+  return c.vec == 4 ? launch_k(k_combine<bf16, 4>, nblk, kThreads, 0, s, c)
+                    : launch_k(k_combine<bf16, 1>, nblk, kThreads, 0, s, c);
+}
 
 cudaError_t launch_fwd_bf16(int op, const EwBuild& eb, cudaStream_t s, bool dry) {
   switch (op) {

@@ -27,10 +27,6 @@ cudaError_t launch_chain_fwd_t(const FwdArg& f, cudaStream_t s) {
                  : launch_chain_fwd_c<OP1, OP2, false>(f.eb, s);
 }
 
-cudaError_t launch_combine(const CombinePlan& c, cudaStream_t s) {
-  const uint64_t nblk = (c.nout + c.jx - 1) / c.jx;
-  return launch_k(k_combine<float>, static_cast<unsigned>(nblk), kThreads, 0, s, c);
-}
 
 template <int OP1, int OP2>
 cudaError_t launch_chain_bwd_t(const ChainBuild& cb, cudaStream_t s) {
@@ -42,8 +38,8 @@ cudaError_t launch_chain_bwd_t(const ChainBuild& cb, cudaStream_t s) {
                               : launch_k(k_chain_bwd<OP1, OP2, false>, p.n_cta, kThreads, smem, s, cp);
   if (e != cudaSuccess) return e;
   // With c shaped like b, one second pass finishes grad_b and grad_c.
-  if (p.nslots > 1) e = launch_combine(cb.comb_b, s);
-  if (e == cudaSuccess && cp.c_scalar && p.n_cta > 1) e = launch_combine(cb.comb_c, s);
+  if (p.nslots > 1) e = launch_combine_f32(cb.comb_b, s);
+  if (e == cudaSuccess && cp.c_scalar && p.n_cta > 1) e = launch_combine_f32(cb.comb_c, s);
   return e;
 }
 

@@ -40,9 +40,7 @@ cudaError_t launch_red_t(const RedBuild& rb, cudaStream_t s, bool dry) {
                     : launch_k(k_reduce<OP, WHICH, 1, false>, p.n_cta, kThreads, smem, s, p);
   }
   if (e != cudaSuccess || p.nslots <= 1) return e;
-  const CombinePlan& c = rb.comb;
-  const uint64_t nblk = (c.nout + c.jx - 1) / c.jx;
-  return launch_k(k_combine<float>, static_cast<unsigned>(nblk), kThreads, 0, s, c);
+  return launch_combine_f32(rb.comb, s);
 }
 
 template <int OP>
@@ -51,6 +49,13 @@ cudaError_t launch_red_op(int which, const RedBuild& rb, cudaStream_t s, bool dr
 }
 
 }  // namespace
+
+cudaError_t launch_combine_f32(CombinePlan c, cudaStream_t s) {
+  combine_vectorize(&c);
+  const unsigned nblk = static_cast<unsigned>(combine_blocks(c));
+  return c.vec == 4 ? launch_k(k_combine<float, 4>, nblk, kThreads, 0, s, c)
+                    : launch_k(k_combine<float, 1>, nblk, kThreads, 0, s, c);
+}
 
 cudaError_t occupancy_red(int which, int* planned, int* actual) {
   // The largest dynamic shared memory a plan asks for: a full offset table

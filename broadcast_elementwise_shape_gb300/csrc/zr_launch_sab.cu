@@ -23,9 +23,9 @@ cudaError_t launch_sab_t(const SabBuild& sb, cudaStream_t s, bool dry) {
   CombinePlan ca = sb.comb_a, cb = sb.comb_b;
   ca.partial = p.ws_a;
   cb.partial = p.ws_b;
-  e = launch_k(k_combine<float>, static_cast<unsigned>((ca.nout + ca.jx - 1) / ca.jx), kThreads, 0, s, ca);
+  e = launch_combine_f32(ca, s);
   if (e != cudaSuccess) return e;
-  return launch_k(k_combine<float>, static_cast<unsigned>((cb.nout + cb.jx - 1) / cb.jx), kThreads, 0, s, cb);
+  return launch_combine_f32(cb, s);
 }
 
 template <int OP>

@@ -85,14 +85,16 @@ uint64_t fit_waves(uint64_t pref, uint64_t lo, uint64_t hi, uint64_t F, uint64_t
 // one 32-byte sector, until there are about two CTAs per SM) and the lanes
 // left over go to the slots, so each thread has few partials to load.
 void combine_layout(CombinePlan* c) {
+  if (c->vec == 0) c->vec = 1;
+  const uint64_t units = ceil_div(c->nout, c->vec);  // output groups
   uint32_t jx;
   if (c->nslots <= 16) {
     jx = kThreads;
-  } else if (c->nout < 8) {
-    jx = pow2_ceil(c->nout);
+  } else if (units < 8) {
+    jx = pow2_ceil(units);
   } else {
     jx = 32;
-    while (jx > 8 && ceil_div(c->nout, jx) < 2 * 152) jx /= 2;
+    while (jx > 8 && ceil_div(units, jx) < 2 * 152) jx /= 2;
   }
   if (jx > kThreads) jx = kThreads;
   const uint32_t sy_max = kThreads / jx;
@@ -147,6 +149,17 @@ int pick_vec(const Prob& P, uint32_t slots, const void* const* ptrs, const void*
 }
 
 }  // namespace
+
+void combine_vectorize(CombinePlan* c) {
+  c->vec = 1;
+  if (c->nout % 4 == 0 && c->nout >= 64 * 152 && reinterpret_cast<uintptr_t>(c->partial) % 16 == 0)
+    c->vec = 4;
+  combine_layout(c);
+}
+
+uint64_t combine_blocks(const CombinePlan& c) {
+  return ceil_div(ceil_div(c.nout, c.vec ? c.vec : 1), c.jx);
+}
 
 int read_tensor(const zr_tensor& t, TDesc* d) {
   if (t.ndim < 0 || t.ndim > kMaxDims) return ZR_ERR_RANK;

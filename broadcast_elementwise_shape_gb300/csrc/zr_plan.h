@@ -63,6 +63,13 @@ struct EwBuild {
 };
 // Elementwise plan over P with input slots 0..2 and output slot 3.
 // occ: resident CTAs per SM of the kernel that will run the plan.
+// Second-pass layout for the partial pointer now set in c: 4 outputs per
+// thread with 16-byte partial loads when nout is a multiple of 4, at least
+// 64 per SM (so the groups of 4 still fill the GPU), and the partials are
+// 16-byte aligned.
+void combine_vectorize(CombinePlan* c);
+// Thread blocks of the second pass.
+uint64_t combine_blocks(const CombinePlan& c);
 int build_ew(const Prob& P, const float* const in[3], float* const out[2], uint32_t read_mask,
              uint32_t stream_mask, int occ, EwBuild* eb);
 
