@@ -203,8 +203,11 @@ def test_random_sum_to_shape(seed):
 
 def test_sum_to_shape_large_reductions():
     rng = np.random.default_rng(3)
+    # The last two: many outputs (second pass with 4 outputs per thread) and
+    # a ragged count of them (one per thread).
     cases = [((4096, 1024), (1024,)), ((4096, 1024), (4096, 1)), ((64, 64, 64, 64), (1,)),
-             ((3, 1000, 7, 33), (1000, 1, 1)), ((1 << 20) + 3,), ]
+             ((3, 1000, 7, 33), (1000, 1, 1)), ((1 << 20) + 3,), ((700, 20000), (20000,)),
+             ((1500, 10001), (10001,))]
     for case in cases:
         shape, target = (case if len(case) == 2 else (case[0], (1,)))
         x = torch.from_numpy(rng.standard_normal(shape).astype(np.float32))
