@@ -121,7 +121,7 @@ def test_bf16_random_views(op):
 def test_bf16_sum_to_shape_and_mixed_types():
     rng = np.random.default_rng(1600)
     for shape, tgt in (((4096, 1024), (1024,)), ((64, 300, 256), (1, 300, 1)), ((33, 65), (33, 65)),
-                       (((1 << 20) + 3,), (1,))):
+                       (((1 << 20) + 3,), (1,)), ((700, 20000), (20000,))):
         x = _bf(torch.from_numpy(rng.standard_normal(shape).astype(np.float32)))
         got = zr.zr_sum_to_shape(_dev16(x), tgt)
         assert got.dtype == torch.bfloat16
