@@ -64,7 +64,8 @@ def parse():
     p.add_argument("--dims", default=None,
                    help="JSON size overrides for a single --workload (see workloads.DEFAULT_DIMS), "
                         "e.g. for a smaller profiling case")
-    p.add_argument("--e2e-steps", type=int, default=3)
+    p.add_argument("--e2e-steps", type=int, default=None,
+                   help="timed end-to-end steps (default: --steps, at least 10 and at most 50)")
     p.add_argument("--config-reps", type=int, default=20,
                    help="timed runs per workload phase in the per-config pass (0: skip)")
     p.add_argument("--breakdown-steps", type=int, default=20,
@@ -801,7 +802,8 @@ def run_e2e(args, suite, flush, stream, nbytes, measure_link=True):
     s_in = torch.cuda.Stream(device=stream.device)
     s_out = torch.cuda.Stream(device=stream.device)
     ev = []
-    steps = max(1, args.e2e_steps)
+    steps = args.e2e_steps if args.e2e_steps else min(50, max(10, args.steps))
+    steps = max(1, steps)
     for k in range(steps + 1):  # first iteration is a warm-up
         flush()
         s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -826,7 +828,7 @@ def run_e2e(args, suite, flush, stream, nbytes, measure_link=True):
         if k > 0:
             ev.append((s, e))
     torch.cuda.synchronize()
-    ms = statistics.fmean(s.elapsed_time(e) for s, e in ev)
+    ms = statistics.median(s.elapsed_time(e) for s, e in ev)
     moved = (h2d + d2h) / (ms * 1e-3) / 1e9
     out = {"value": round(nbytes / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms,
@@ -880,15 +882,44 @@ def oracle_steps(name, host):
     return total_bytes, elems
 
 
-def oracle_sample(names):
-    """Run the oracle over the complete fwd+bwd of the named workloads in
+# The host baseline's sample: the complete fwd+bwd of c1, c2 and c3 at full
+# size, and of c5a and c5b at reduced sizes that keep their structure (a
+# transposed view; an 8-d division with both gradients reduced), so that the
+# oracle's strided and 8-d paths are timed too.  (name, size overrides).
+CPU_SAMPLE = (("c1", {}), ("c2", {}), ("c3", {}), ("c5a", {"P": 16}),
+              ("c5b", {"a": (4, 1, 8, 1, 4, 1, 8, 64), "b": (1, 6, 1, 12, 1, 10, 1, 64)}))
+# The reference arm's per-step sample (smaller: K + W steps in minutes).
+REF_SAMPLE = (("c1", {}), ("c2", {}), ("c5a", {"P": 4}),
+              ("c5b", {"a": (4, 1, 8, 1, 4, 1, 2, 64), "b": (1, 6, 1, 12, 1, 10, 1, 64)}))
+
+
+def _items(sample):
+    """(name, dims) pairs from workload names or (name, dims) pairs."""
+    return [(x, {}) if isinstance(x, str) else (x[0], dict(x[1])) for x in sample]
+
+
+def sample_label(sample):
+    """Readable name of a sample: c5a[P=16] for a workload at reduced sizes."""
+    out = []
+    for name, dims in _items(sample):
+        if dims:
+            dd = ",".join(f"{k}={'x'.join(map(str, v)) if isinstance(v, (tuple, list)) else v}"
+                          for k, v in dims.items())
+            out.append(f"{name}[{dd}]")
+        else:
+            out.append(name)
+    return out
+
+
+def oracle_sample(sample):
+    """Run the oracle over the complete fwd+bwd of the sample's workloads in
     this process; returns (seconds, algorithmic bytes, output elements)."""
     import oracle
     oracle.build()
     total_bytes = elems = 0
     t_total = 0.0
-    for name in names:
-        host = workloads.make_inputs(name)
+    for name, dims in _items(sample):
+        host = workloads.make_inputs(name, **dims)
         t = time.perf_counter()
         b, e = oracle_steps(name, host)
         t_total += time.perf_counter() - t
@@ -897,20 +928,21 @@ def oracle_sample(names):
     return t_total, total_bytes, elems
 
 
-def _oracle_worker(names, dims, cmd, res):
+def _oracle_worker(sample, cmd, res):
     """One process of OraclePool: builds its own inputs, reports ready, then
     runs the whole sample each time it is told to."""
     import torch
     torch.set_num_threads(1)  # one core per process; torch only draws the inputs
     import oracle
     oracle.build()
-    inputs = {n: workloads.make_inputs(n, **(dims or {})) for n in names}
+    items = _items(sample)
+    inputs = [workloads.make_inputs(n, **d) for n, d in items]
     res.put("ready")
     while cmd.get() is not None:
         t0 = time.time()
         nbytes = elems = 0
-        for n in names:
-            b, e = oracle_steps(n, inputs[n])
+        for (n, _), host in zip(items, inputs):
+            b, e = oracle_steps(n, host)
             nbytes += b
             elems += e
         res.put((t0, time.time(), nbytes, elems))
@@ -922,9 +954,10 @@ class OraclePool:
     of the sample's inputs.  Independent problems on separate cores is how
     the path shards, so the pool's throughput is the processes' total bytes
     over the wall time from the first start to the last finish.  Spawned,
-    not forked, so that no process inherits a CUDA context."""
+    not forked, so that no process inherits a CUDA context.  ``sample``:
+    workload names, or (name, size overrides) pairs."""
 
-    def __init__(self, names, procs=None, dims=None):
+    def __init__(self, sample, procs=None):
         import multiprocessing as mp
         import oracle
         oracle.build()  # once, before the processes load it
@@ -932,7 +965,8 @@ class OraclePool:
         self.n = procs or len(os.sched_getaffinity(0))
         self.res = ctx.Queue()
         self.cmd = [ctx.Queue() for _ in range(self.n)]
-        self.procs = [ctx.Process(target=_oracle_worker, args=(names, dims, q, self.res),
+        sample = _items(sample)
+        self.procs = [ctx.Process(target=_oracle_worker, args=(sample, q, self.res),
                                   daemon=True) for q in self.cmd]
         for p in self.procs:
             p.start()
@@ -954,13 +988,12 @@ class OraclePool:
             p.join(timeout=60)
 
 
-def cpu_baseline(names=("c1", "c2", "c3"), runs=3, procs=None):
+def cpu_baseline(sample=CPU_SAMPLE, runs=3, procs=None):
     """The oracle on the machine's host cores: `runs` passes of the pool (one
-    process per core, each computing the complete fwd+bwd of `names`),
+    process per core, each computing the complete fwd+bwd of the sample),
     median wall time; plus the same sample on one core for reference."""
-    names = list(names)
-    secs1, nbytes1, elems1 = oracle_sample(names)
-    pool = OraclePool(names, procs)
+    secs1, nbytes1, elems1 = oracle_sample(sample)
+    pool = OraclePool(sample, procs)
     try:
         passes = [pool.run() for _ in range(runs)]
     finally:
@@ -969,10 +1002,11 @@ def cpu_baseline(names=("c1", "c2", "c3"), runs=3, procs=None):
     nbytes, elems = passes[0][1], passes[0][2]
     return {"value": round(nbytes / span / 1e9, 4), "unit": "GB/s", "cores": pool.n,
             "kind": "oracle",
-            "sample": f"complete fwd+bwd of {', '.join(names)} in each of {pool.n} processes "
-                      "(single-thread C++ oracle, binary64 accumulation, one process per host "
-                      f"core); {elems} op-elements per pass, median of {runs} passes, "
-                      f"{span:.2f} s",
+            "sample": f"complete fwd+bwd of {', '.join(sample_label(sample))} in each of "
+                      f"{pool.n} processes (single-thread C++ oracle, binary64 accumulation, one "
+                      f"process per host core; c5a and c5b at the reduced sizes given, with their "
+                      f"transposed-view and 8-d structure); {elems} op-elements per pass, median "
+                      f"of {runs} passes, {span:.2f} s",
             "seconds": round(span, 3),
             "single_core": {"value": round(nbytes1 / secs1 / 1e9, 4), "cores": 1,
                             "seconds": round(secs1, 3)}}
@@ -984,8 +1018,9 @@ def run_reference(args, rank, world):
     # Each step is one pass of the oracle on every host core over a bounded
     # sample of the suite, sized so that K + W steps stay within a few
     # minutes.
-    names = ["c1", "c2"] if args.steps + args.warmup <= 40 else ["c1"]
-    pool = OraclePool(names, args.ref_procs or None)
+    sample = list(REF_SAMPLE) if args.steps + args.warmup <= 40 else [("c1", {})]
+    names = sample_label(sample)
+    pool = OraclePool(sample, args.ref_procs or None)
     try:
         for _ in range(args.warmup):
             pool.run()
@@ -1005,8 +1040,9 @@ def run_reference(args, rank, world):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(1e3 * total / len(times), 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": "bounded sample of the suite per step: complete fwd+bwd of "
-                               + " and ".join(names) + f" on {pool.n} host cores"},
+        "config": {"workload": "a sample of the suite by design (the oracle is a deliberately "
+                               "plain CPU program): complete fwd+bwd of " + ", ".join(names)
+                               + f" per step on {pool.n} host cores"},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": pool.n,
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,

@@ -55,3 +55,23 @@ def test_kernel_hash_covers_code_only():
     c = "int f() {\n  return 2;\n}\n"
     assert bench._code_only(a) == bench._code_only(b) != bench._code_only(c)
     assert bench.kernel_hash() == bench.kernel_hash()
+
+
+def test_oracle_pool_takes_reduced_size_workloads():
+    """The host baseline also times the strided workloads at reduced sizes:
+    (name, size overrides) pairs are drawn at those sizes, and the baseline's
+    default sample names c5a and c5b."""
+    sample = [("c5a", dict(P=2, M=8, Q=16)), ("c5b", workloads.small_dims("c5b"))]
+    want = 0
+    for name, dims in sample:
+        sizes = bench.shape_table(name, workloads.make_inputs(name, **dims))[0]
+        want += sum(bench.op_bytes(s, sizes) for s in workloads.STEPS[name])
+    pool = bench.OraclePool(sample, procs=1)
+    try:
+        span, nbytes, elems = pool.run()
+    finally:
+        pool.close()
+    assert nbytes == want and span > 0
+    labels = bench.sample_label(bench.CPU_SAMPLE)
+    assert any(x.startswith("c5a[") for x in labels) and any(x.startswith("c5b[") for x in labels)
+    assert bench.sample_label(sample)[0] == "c5a[P=2,M=8,Q=16]"
