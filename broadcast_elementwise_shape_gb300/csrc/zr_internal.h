@@ -108,9 +108,17 @@ struct EwPlan {
   uint32_t col_tiles;       // tiles along a row
   FastDiv col_tiles_div;    // blockIdx -> (row tile, column tile)
   FastDiv tile_vcols_div;   // item -> (row in tile, column vector)
-  uint32_t items_per_cta;   // tile_rows * tile_vcols
+  uint32_t items_per_cta;   // tile_rows * tile_vcols (flat: items per CTA)
   uint32_t n_cta;
   float alpha;              // the unary ops' scalar (scale's factor)
+  // Flat plans (at most one outer dim): item i of the nrow x nvcol grid is
+  // row i / nvcol, column vector i % nvcol, and each operand's offset is
+  // row * rows.stride[k][0] + column * inner_stride[k], computed per item
+  // with no offset table; CTA c takes items [c * items_per_cta,
+  // (c + 1) * items_per_cta), a whole number of the kernel's load batches.
+  uint32_t flat;
+  uint32_t nitems;          // nrow * nvcol (flat plans)
+  FastDiv nvcol_div;        // item -> (row, column vector) (flat plans)
 };
 
 // Forward with one input read transposed: that input (X) walks the output's

@@ -11,6 +11,7 @@
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include "zr_internal.h"
+#include "zr_launch.h"
 
 namespace zr {
 
@@ -644,6 +645,90 @@ k_elementwise(const __grid_constant__ EwPlan p) {
       if (NOUT > 1 && out1) store_cols<VEC>(out1, doff[u], p.inner_stride[kSlotOut], col[u], y[1]);
     }
   }
+}
+
+// Flat elementwise kernel (EwPlan with flat = 1): the same functors and loads
+// as k_elementwise for problems with at most one outer dim (same-shape,
+// scalar, bias-like rows), with no offset table, no barrier and no
+// shared memory.  A CTA's items are consecutive in row-major order and come
+// in whole batches of U * 256, so every batch issues U loads per operand
+// from every thread; each batch's u-th group of 256 items is 256
+// consecutive vectors (coalesced).
+template <class F, int VEC, int NOUT, class E = float>
+__global__ void __launch_bounds__(kThreads, VEC == 8 ? WideBlocks<F>::value : F::kMinBlocks)
+k_flat(const __grid_constant__ EwPlan p) {
+  pdl_trigger();
+  const E* in0 = reinterpret_cast<const E*>(p.in[0]);
+  const E* in1 = reinterpret_cast<const E*>(p.in[1]);
+  const E* in2 = reinterpret_cast<const E*>(p.in[2]);
+  E* out0 = reinterpret_cast<E*>(p.out[0]);
+  E* out1 = reinterpret_cast<E*>(p.out[1]);
+  const uint32_t first = blockIdx.x * p.items_per_cta;
+  const uint32_t left = p.nitems - first;
+  const uint32_t end = first + (left < p.items_per_cta ? left : p.items_per_cta);
+  pdl_wait();
+  constexpr bool kUni1 = Uniform1<F>::value;
+  constexpr bool kUni2 = Uniform2<F>::value;
+  float uni1 = 0.f, uni2 = 0.f;
+  if (kUni1) uni1 = ld1(in1, false);
+  if (kUni2) uni2 = ld1(in2, false);
+
+  constexpr int U = 4;
+  const F f;
+  for (uint32_t it0 = first; it0 < end; it0 += U * kThreads) {
+    Raw<E, VEC> xr[U][3];
+    int64_t doff[U];
+    uint32_t col[U];
+    bool ok[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const uint32_t item = it0 + u * kThreads + threadIdx.x;
+      ok[u] = item < end;
+      const uint32_t row = fd_div(p.nvcol_div, item);
+      col[u] = (item - row * p.nvcol) * VEC;
+      doff[u] = int64_t(row) * p.rows.stride[kSlotOut][0];
+      if (ok[u]) {
+        xr[u][0] = load_raw<VEC>(in0, int64_t(row) * p.rows.stride[0][0], p.inner_stride[0], col[u],
+                                 p.stream_mask & 1);
+        if (F::kR1 && !kUni1)
+          xr[u][1] = load_raw<VEC>(in1, int64_t(row) * p.rows.stride[1][0], p.inner_stride[1],
+                                   col[u], p.stream_mask & 2);
+        if (F::kR2 && !kUni2)
+          xr[u][2] = load_raw<VEC>(in2, int64_t(row) * p.rows.stride[2][0], p.inner_stride[2],
+                                   col[u], p.stream_mask & 4);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (!ok[u]) continue;
+      Vec<VEC> x[3], y[2];
+      x[0] = unpack<VEC>(xr[u][0]);
+      if (F::kR1 && kUni1) {
+#pragma unroll
+        for (int i = 0; i < VEC; ++i) x[1].v[i] = uni1;
+      } else if (F::kR1) {
+        x[1] = unpack<VEC>(xr[u][1]);
+      }
+      if (F::kR2 && kUni2) {
+#pragma unroll
+        for (int i = 0; i < VEC; ++i) x[2].v[i] = uni2;
+      } else if (F::kR2) {
+        x[2] = unpack<VEC>(xr[u][2]);
+      }
+      f(x, y, p.alpha);
+      if (out0) store_cols<VEC>(out0, doff[u], p.inner_stride[kSlotOut], col[u], y[0]);
+      if (NOUT > 1 && out1) store_cols<VEC>(out1, doff[u], p.inner_stride[kSlotOut], col[u], y[1]);
+    }
+  }
+}
+
+// Launch of an elementwise plan: the flat kernel for flat plans, else the
+// tiled one with its offset table in dynamic shared memory.
+template <class F, int VEC, int NOUT, class E = float>
+cudaError_t launch_ew_kernel(const EwPlan& p, cudaStream_t s) {
+  if (p.flat) return launch_k(k_flat<F, VEC, NOUT, E>, p.n_cta, kThreads, 0, s, p);
+  const size_t smem = size_t(p.tile_rows) * kMaxOperands * sizeof(int64_t);
+  return launch_k(k_elementwise<F, VEC, NOUT, E>, p.n_cta, kThreads, smem, s, p);
 }
 
 // Forward with a transposed input (TrPlan): x has unit stride along p, the

@@ -19,12 +19,9 @@ cudaError_t launch_ew_bf16(const EwBuild& eb, cudaStream_t s, bool dry) {
       (!eb.plan.out[0] && !eb.plan.out[1]))
     return cudaErrorInvalidValue;
   if (dry) return cudaSuccess;
-  const size_t smem = size_t(eb.plan.tile_rows) * kMaxOperands * sizeof(int64_t);
-  if (eb.vec == 8)
-    return launch_k(k_elementwise<F, 8, NOUT, bf16>, eb.plan.n_cta, kThreads, smem, s, eb.plan);
-  if (eb.vec == 4)
-    return launch_k(k_elementwise<F, 4, NOUT, bf16>, eb.plan.n_cta, kThreads, smem, s, eb.plan);
-  return launch_k(k_elementwise<F, 1, NOUT, bf16>, eb.plan.n_cta, kThreads, smem, s, eb.plan);
+  if (eb.vec == 8) return launch_ew_kernel<F, 8, NOUT, bf16>(eb.plan, s);
+  if (eb.vec == 4) return launch_ew_kernel<F, 4, NOUT, bf16>(eb.plan, s);
+  return launch_ew_kernel<F, 1, NOUT, bf16>(eb.plan, s);
 }
 
 template <int OP>

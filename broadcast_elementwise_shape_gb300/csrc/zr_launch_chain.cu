@@ -11,9 +11,8 @@ namespace {
 template <int OP1, int OP2, bool C_ONE>
 cudaError_t launch_chain_fwd_c(const EwBuild& eb, cudaStream_t s) {
   using F = ChainF<OP1, OP2, C_ONE>;
-  const size_t smem = size_t(eb.plan.tile_rows) * kMaxOperands * sizeof(int64_t);
-  if (eb.vec == 4) return launch_k(k_elementwise<F, 4, 1>, eb.plan.n_cta, kThreads, smem, s, eb.plan);
-  return launch_k(k_elementwise<F, 1, 1>, eb.plan.n_cta, kThreads, smem, s, eb.plan);
+  if (eb.vec == 4) return launch_ew_kernel<F, 4, 1>(eb.plan, s);
+  return launch_ew_kernel<F, 1, 1>(eb.plan, s);
 }
 
 // c_one: c has one element (read once per thread).

@@ -13,9 +13,8 @@ cudaError_t launch_ew_t(const EwBuild& eb, cudaStream_t s, bool dry) {
       (!eb.plan.out[0] && !eb.plan.out[1]))
     return cudaErrorInvalidValue;
   if (dry) return cudaSuccess;
-  const size_t smem = size_t(eb.plan.tile_rows) * kMaxOperands * sizeof(int64_t);
-  if (eb.vec == 4) return launch_k(k_elementwise<F, 4, NOUT>, eb.plan.n_cta, kThreads, smem, s, eb.plan);
-  return launch_k(k_elementwise<F, 1, NOUT>, eb.plan.n_cta, kThreads, smem, s, eb.plan);
+  if (eb.vec == 4) return launch_ew_kernel<F, 4, NOUT>(eb.plan, s);
+  return launch_ew_kernel<F, 1, NOUT>(eb.plan, s);
 }
 
 template <int OP>

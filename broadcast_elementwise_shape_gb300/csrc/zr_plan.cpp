@@ -79,6 +79,12 @@ uint64_t fit_waves(uint64_t pref, uint64_t lo, uint64_t hi, uint64_t F, uint64_t
   return pick;
 }
 
+// Flat elementwise plans: items per load batch of the kernel (4 in flight per
+// thread x 256 threads), and the largest item count (item indices and the
+// batch loop stay within 32 bits).
+constexpr uint64_t kFlatBatch = 4 * kThreads;
+constexpr uint64_t kFlatMaxItems = (uint64_t(1) << 32) - (uint64_t(1) << 20);
+
 // Thread layout of the combine pass: jx outputs x sy slot lanes (powers of
 // two, jx * sy <= 256).  Few slots: one output per thread, summed serially
 // (no tree).  Many slots: rows of jx consecutive outputs (32, or down to 8 =
@@ -373,6 +379,21 @@ int build_ew(const Prob& P, const float* const in[3], float* const out[2], uint3
   const uint64_t ncta = ceil_div(nrow, trows) * p.col_tiles;
   if (ncta >= (uint64_t(1) << 31)) return ZR_ERR_SIZE;
   p.n_cta = uint32_t(ncta);
+  // Flat plan for at most one outer dim: no offset table; CTAs of whole
+  // 1024-item batches (the kernel's 4 loads in flight x 256 threads), fewer
+  // per CTA (down to one item per thread) when that is what fills the GPU.
+  if (n <= 2 && items <= kFlatMaxItems) {
+    uint64_t ipc = kFlatBatch;
+    while (ipc > kThreads && ceil_div(items, ipc) < wave) ipc /= 2;
+    p.flat = 1;
+    p.nitems = uint32_t(items);
+    p.nvcol_div = make_fastdiv(p.nvcol);
+    p.items_per_cta = uint32_t(ipc);
+    p.tile_rows = 0;
+    p.tile_vcols = 0;
+    p.col_tiles = 0;
+    p.n_cta = uint32_t(ceil_div(items, ipc));
+  }
   return ZR_OK;
 }
 
@@ -704,12 +725,13 @@ std::string describe_ew(const EwBuild& eb) {
   const EwPlan& p = eb.plan;
   char buf[1024];
   std::snprintf(buf, sizeof(buf),
-                "{\"kernel\":\"elementwise\",\"vec\":%d,\"nrow\":%u,\"ncol\":%u,\"row_dims\":%d,"
+                "{\"kernel\":\"%s\",\"vec\":%d,\"nrow\":%u,\"ncol\":%u,\"row_dims\":%d,"
                 "\"inner_stride\":[%lld,%lld,%lld,%lld],\"tile_rows\":%u,\"tile_vcols\":%u,"
-                "\"ctas\":%u,\"stream_mask\":%u}",
-                eb.vec, p.nrow, p.ncol, p.rows.n, (long long)p.inner_stride[0],
-                (long long)p.inner_stride[1], (long long)p.inner_stride[2],
-                (long long)p.inner_stride[3], p.tile_rows, p.tile_vcols, p.n_cta, p.stream_mask);
+                "\"items_per_cta\":%u,\"ctas\":%u,\"stream_mask\":%u}",
+                p.flat ? "flat" : "elementwise", eb.vec, p.nrow, p.ncol, p.rows.n,
+                (long long)p.inner_stride[0], (long long)p.inner_stride[1],
+                (long long)p.inner_stride[2], (long long)p.inner_stride[3], p.tile_rows,
+                p.tile_vcols, p.items_per_cta, p.n_cta, p.stream_mask);
   return buf;
 }
 

@@ -731,7 +731,7 @@ print(rc1, rc2)
                        timeout=120)
     assert r.returncode == 0, r.stderr
     lines = [ln for ln in r.stderr.splitlines() if ln.startswith("zr_trace ")]
-    assert lines[0].startswith('zr_trace zr_binary_fwd {"kernel":"elementwise"'), lines
+    assert lines[0].startswith('zr_trace zr_binary_fwd {"kernel":"flat"'), lines
     assert lines[1].startswith('zr_trace zr_binary_bwd {"plans":[{"kernel":"reduce"'), lines
     json.loads(lines[1].split(" ", 2)[2])
     rcs = [int(v) for v in r.stdout.split()]
