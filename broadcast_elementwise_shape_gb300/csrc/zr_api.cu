@@ -2,6 +2,7 @@
 // launches.  Every check runs on the host before the first launch (Zero book,
 // Operator page, section 逐元素算子: shape and broadcast checks belong to the
 // operator layer), so an error never leaves a partial write.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -617,15 +618,42 @@ static int binary_bwd_es(int es, zr_op op, zr_tensor grad_out, zr_tensor a, zr_t
 // reduction live here instead of in a caller-provided workspace.  The array
 // exists once per device that loads this library and stays until the process
 // exits.  Host code cannot use the array's name as a device address, so the
-// address is looked up with cudaGetSymbolAddress, once per device, with that
-// device current, on the first call made on it.
+// address is looked up with cudaGetSymbolAddress, with the device current, on
+// the first call made on it.  The lookup is remembered together with the
+// identity of the device's context: a new context (after cudaDeviceReset, for
+// example) reloads the module at another address, and the next call then
+// looks the address up again instead of launching on a freed one.
 static __device__ __align__(256) unsigned char zr_noalloc_scratch[ZR_STATIC_SCRATCH_BYTES];
 
 namespace {
 
 constexpr int kScratchDevices = 256;
+struct ScratchAddr {
+  void* addr = nullptr;
+  unsigned long long ctx = 0;  // context id the address belongs to
+};
 std::mutex g_scratch_mu;
-void* g_scratch_addr[kScratchDevices] = {};
+ScratchAddr g_scratch[kScratchDevices];
+
+// Id of the calling thread's current context (ids are unique for the life of
+// the process), through the driver's cuCtxGetId, found at run time so that
+// the library does not link the driver library.  False when there is no
+// current context or the driver lacks the call.
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+bool current_ctx_id(unsigned long long* id) {
+  static const CtxGetIdFn fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess) {
+      cudaGetLastError();
+      f = nullptr;
+    }
+    return reinterpret_cast<CtxGetIdFn>(f);
+  }();
+  return fn != nullptr && fn(nullptr, id) == CUDA_SUCCESS;
+}
 
 // Device address of the scratch array on the current device.
 int noalloc_scratch(void** out) {
@@ -636,16 +664,27 @@ int noalloc_scratch(void** out) {
   }
   if (dev < 0 || dev >= kScratchDevices) return ZR_ERR_DEVICE;
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (g_scratch_addr[dev] == nullptr) {
+  ScratchAddr& c = g_scratch[dev];
+  unsigned long long id = 0;
+  const bool have_id = current_ctx_id(&id);
+  if (c.addr == nullptr || !have_id || c.ctx != id) {
     void* p = nullptr;
     const cudaError_t e = cudaGetSymbolAddress(&p, zr_noalloc_scratch);
     if (e != cudaSuccess || p == nullptr) {
       cudaGetLastError();
       return ZR_ERR_CUDA;
     }
-    g_scratch_addr[dev] = p;
+    // The lookup makes the device's primary context current if none was.
+    // Without a context id the address is not remembered, so every call
+    // looks it up.
+    c.addr = p;
+    c.ctx = 0;
+    if (current_ctx_id(&id)) c.ctx = id;
+    else c.addr = nullptr;
+    *out = p;
+    return ZR_OK;
   }
-  *out = g_scratch_addr[dev];
+  *out = c.addr;
   return ZR_OK;
 }
 
@@ -658,6 +697,7 @@ int zr_binary_bwd_noalloc(zr_op op, zr_tensor grad_out, zr_tensor a, zr_tensor b
   BwdSet S;
   int rc = plan_bwd(op, grad_out, a, b, grad_a, grad_b, &S);
   if (rc) return rc;
+  if (trace_on()) trace("zr_binary_bwd_noalloc", bwd_json(S));
   if (S.nothing) return ZR_OK;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (S.empty) {
@@ -874,10 +914,35 @@ int zr_test_describe_sum(zr_tensor in, int32_t ndim_out, const int64_t* sizes_ou
 namespace zr {
 namespace {
 
-// Host walk of k_elementwise's (CTA, item, lane) space.
+// Host walk of k_elementwise's (CTA, item, lane) space, or k_flat's for a
+// flat plan.
 template <class Rec>
 void walk_ew(const EwBuild& eb, Rec rec) {
   const EwPlan& p = eb.plan;
+  if (p.flat) {
+    for (uint32_t cta = 0; cta < p.n_cta; ++cta) {
+      const uint32_t first = cta * p.items_per_cta;
+      const uint32_t left = p.nitems - first;
+      const uint32_t end = first + (left < p.items_per_cta ? left : p.items_per_cta);
+      for (uint32_t it0 = first; it0 < end; it0 += 4 * kThreads)
+        for (uint32_t u = 0; u < 4; ++u)
+          for (uint32_t t = 0; t < uint32_t(kThreads); ++t) {
+            const uint32_t item = it0 + u * kThreads + t;
+            if (item >= end) continue;
+            const uint32_t row = fd_div(p.nvcol_div, item);
+            const uint32_t vc = item - row * p.nvcol;
+            for (int i = 0; i < eb.vec; ++i) {
+              const int64_t c = int64_t(vc) * eb.vec + i;
+              if (c >= p.ncol) continue;
+              int64_t o[kMaxOperands];
+              for (int k = 0; k < kMaxOperands; ++k)
+                o[k] = int64_t(row) * p.rows.stride[k][0] + c * p.inner_stride[k];
+              rec(o);
+            }
+          }
+    }
+    return;
+  }
   for (uint32_t cta = 0; cta < p.n_cta; ++cta) {
     const EwTile t = ew_tile(p, cta);
     for (uint32_t item = 0; item < p.items_per_cta; ++item) {

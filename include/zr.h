@@ -194,7 +194,10 @@ int zr_binary_bwd(zr_op op, zr_tensor grad_out, zr_tensor a, zr_tensor b,
  * and may return wrong gradients: order them, for instance by issuing them on
  * one stream.  The first call on each device looks up the array's device
  * address (cudaGetSymbolAddress, with that device current); make that first
- * call before any stream capture.
+ * call before any stream capture.  The address is remembered with the
+ * device's context: after the context is replaced (cudaDeviceReset, for
+ * example) the next call looks it up again, so make that call before any
+ * capture too.
  */
 int zr_binary_bwd_noalloc(zr_op op, zr_tensor grad_out, zr_tensor a, zr_tensor b,
                           float* grad_a, float* grad_b, zr_stream_t stream);
