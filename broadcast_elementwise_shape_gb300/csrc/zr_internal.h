@@ -250,7 +250,19 @@ struct RedPlan {
   // is a kept index, rank = row block * n_cblk + column block.
   uint32_t cluster;
   FastDiv cluster_div;
+  // cp.async staging of the streamed inputs (16-byte vectors with unit inner
+  // stride): a ring of `stages` batches (0 = loads into registers), each
+  // holding stage_ns streams x 4 items x 256 threads of 16 bytes, after the
+  // offset table and the tree in dynamic shared memory.
+  uint32_t stages;
+  uint32_t stage_ns;
 };
+// Bytes of one staged batch per streamed input (4 items x 256 threads x 16).
+constexpr uint32_t kStageBatchBytes = 4 * kThreads * 16;
+// Shared memory the planner lets one SM's resident CTAs use in total, and
+// what each CTA keeps back beyond its own request.
+constexpr uint32_t kSmemPerSm = 228 * 1024;
+constexpr uint32_t kSmemReservedPerCta = 1024;
 
 struct RedCta {
   uint32_t kidx, rblk, cblk;

@@ -125,6 +125,22 @@ __device__ __forceinline__ float ld_cluster(const float* local, uint32_t rank) {
   return v;
 }
 
+// cp.async: 16-byte copies from global to shared memory that complete in the
+// background; a thread waits for its own groups of copies with
+// cp_async_wait<N>() (at most N most recent groups still in flight), after
+// which the copied bytes are visible to that thread.
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc) {
+  const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gsrc) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;\n" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
 struct Kahan {
   float s, c;
   __device__ __forceinline__ void init() { s = 0.f; c = 0.f; }
@@ -306,6 +322,21 @@ __device__ __forceinline__ Vec<VEC> unpack_bf16(const Raw<__nv_bfloat16, VEC>& r
   return v;
 }
 
+// A 16-byte vector staged in shared memory as the register form a load
+// would have produced (4 floats, or 8 bfloat16 kept packed).
+template <class E, int VEC>
+__device__ __forceinline__ Raw<E, VEC> raw_from_u4(const uint4& q) {
+  static_assert(VEC * sizeof(E) == 16, "16-byte vectors only");
+  Raw<E, VEC> r;
+  if constexpr (sizeof(E) == 2) {
+    r.w[0] = q.x; r.w[1] = q.y; r.w[2] = q.z; r.w[3] = q.w;
+  } else {
+    r.x.v[0] = __uint_as_float(q.x); r.x.v[1] = __uint_as_float(q.y);
+    r.x.v[2] = __uint_as_float(q.z); r.x.v[3] = __uint_as_float(q.w);
+  }
+  return r;
+}
+
 // Load VEC consecutive columns of one operand in one row.  inner == 1:
 // contiguous (one 16-byte load of 4 floats or one 8-byte load of 4 bf16 when
 // VEC == 4; the planner guarantees alignment); inner == 0: the column is
@@ -463,19 +494,17 @@ __device__ __forceinline__ float rcp_approx(float v) {
   asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(v));
   return r;
 }
+// P(t) of the degree-9 form, highest coefficient first.
+#define ZR_ERFC_CHEB_P                                                                          \
+  0.17087277f, -0.82215223f, 1.48851587f, -1.13520398f, 0.27886807f, -0.18628806f, 0.09678418f, \
+      0.37409196f, 1.00002368f, -1.26551223f
 __device__ __forceinline__ float erfc_cheb(float v) {
+  constexpr float kP[10] = {ZR_ERFC_CHEB_P};
   const float z = fabsf(v);
   const float t = rcp_approx(__fmaf_rn(0.5f, z, 1.0f));
-  float q = 0.17087277f;  // P(t), Horner from the highest coefficient
-  q = __fmaf_rn(q, t, -0.82215223f);
-  q = __fmaf_rn(q, t, 1.48851587f);
-  q = __fmaf_rn(q, t, -1.13520398f);
-  q = __fmaf_rn(q, t, 0.27886807f);
-  q = __fmaf_rn(q, t, -0.18628806f);
-  q = __fmaf_rn(q, t, 0.09678418f);
-  q = __fmaf_rn(q, t, 0.37409196f);
-  q = __fmaf_rn(q, t, 1.00002368f);
-  q = __fmaf_rn(q, t, -1.26551223f);
+  float q = kP[0];  // P(t), Horner from the highest coefficient
+#pragma unroll
+  for (int k = 1; k < 10; ++k) q = __fmaf_rn(q, t, kP[k]);
   const float y = __fmul_rn(t, ex2_approx(__fmul_rn(__fmaf_rn(-z, z, q), 1.44269504088896341f)));
   return v >= 0.f ? y : __fsub_rn(2.0f, y);
 }
@@ -484,18 +513,87 @@ __device__ __forceinline__ float erfc_cheb(float v) {
 // erfc_fit.py beside this file derives these coefficients and measures the
 // fit).  Relative error below 1.3e-5 (2^-16.3) with binary32 evaluation:
 // far inside bfloat16's half unit of 2^-9, at four fewer multiply-adds.
+// P(t) of the degree-5 form, highest coefficient first.
+#define ZR_ERFC_SHORT_P                                                          \
+  0.22462645173072815f, -0.6965311169624329f, 0.45995479822158813f,              \
+      0.2622242867946625f, 1.0161044597625732f, -1.2663732767105103f
 __device__ __forceinline__ float erfc_short(float v) {
+  constexpr float kP[6] = {ZR_ERFC_SHORT_P};
   const float z = fabsf(v);
   const float t = rcp_approx(__fmaf_rn(0.5f, z, 1.0f));
-  float q = 0.22462645173072815f;  // P(t), Horner from the highest coefficient
-  q = __fmaf_rn(q, t, -0.6965311169624329f);
-  q = __fmaf_rn(q, t, 0.45995479822158813f);
-  q = __fmaf_rn(q, t, 0.2622242867946625f);
-  q = __fmaf_rn(q, t, 1.0161044597625732f);
-  q = __fmaf_rn(q, t, -1.2663732767105103f);
+  float q = kP[0];  // P(t), Horner from the highest coefficient
+#pragma unroll
+  for (int k = 1; k < 6; ++k) q = __fmaf_rn(q, t, kP[k]);
   const float y = __fmul_rn(t, ex2_approx(__fmul_rn(__fmaf_rn(-z, z, q), 1.44269504088896341f)));
   return v >= 0.f ? y : __fsub_rn(2.0f, y);
 }
+// Two binary32 lanes in one 64-bit register, for Blackwell's packed FP32
+// instructions: add/mul/fma.rn.f32x2 round each lane exactly as the scalar
+// __fadd_rn/__fmul_rn/__fmaf_rn do, at one issue slot per pair.  The
+// approximate reciprocal and exponential stay scalar (one per lane).
+struct F2 {
+  unsigned long long v;
+};
+__device__ __forceinline__ F2 f2_pack(float lo, float hi) {
+  F2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r.v) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ F2 f2_splat(float x) { return f2_pack(x, x); }
+__device__ __forceinline__ void f2_unpack(F2 a, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(a.v));
+}
+__device__ __forceinline__ F2 f2_fma(F2 a, F2 b, F2 c) {
+  F2 r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r.v) : "l"(a.v), "l"(b.v), "l"(c.v));
+  return r;
+}
+__device__ __forceinline__ F2 f2_mul(F2 a, F2 b) {
+  F2 r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r.v) : "l"(a.v), "l"(b.v));
+  return r;
+}
+__device__ __forceinline__ F2 f2_add(F2 a, F2 b) {
+  F2 r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r.v) : "l"(a.v), "l"(b.v));
+  return r;
+}
+// Sign operations on both lanes' bit patterns (exact, like fabsf and -x).
+__device__ __forceinline__ F2 f2_abs(F2 a) { return F2{a.v & 0x7FFFFFFF7FFFFFFFull}; }
+__device__ __forceinline__ F2 f2_neg(F2 a) { return F2{a.v ^ 0x8000000080000000ull}; }
+
+// erfc of both lanes: the same operations, in the same order, as erfc_cheb
+// (SHORT = false) or erfc_short (SHORT = true), so each lane's result is
+// bit-identical to theirs.
+template <bool SHORT>
+__device__ __forceinline__ F2 erfc2(F2 v) {
+  const F2 z = f2_abs(v);
+  float d0, d1;
+  f2_unpack(f2_fma(f2_splat(0.5f), z, f2_splat(1.0f)), d0, d1);
+  const F2 t = f2_pack(rcp_approx(d0), rcp_approx(d1));
+  constexpr float kShort[6] = {ZR_ERFC_SHORT_P};
+  constexpr float kCheb[10] = {ZR_ERFC_CHEB_P};
+  constexpr int kN = SHORT ? 6 : 10;
+  F2 q = f2_splat(SHORT ? kShort[0] : kCheb[0]);
+#pragma unroll
+  for (int k = 1; k < kN; ++k) q = f2_fma(q, t, f2_splat(SHORT ? kShort[k] : kCheb[k]));
+  float e0, e1;
+  f2_unpack(f2_mul(f2_fma(f2_neg(z), z, q), f2_splat(1.44269504088896341f)), e0, e1);
+  const F2 y = f2_mul(t, f2_pack(ex2_approx(e0), ex2_approx(e1)));
+  const F2 w = f2_fma(y, f2_splat(-1.0f), f2_splat(2.0f));  // RN(2 - y)
+  float v0, v1, y0, y1, w0, w1;
+  f2_unpack(v, v0, v1);
+  f2_unpack(y, y0, y1);
+  f2_unpack(w, w0, w1);
+  return f2_pack(v0 >= 0.f ? y0 : w0, v1 >= 0.f ? y1 : w1);
+}
+// Phi of both lanes, as gelu_cdf.
+template <bool SHORT>
+__device__ __forceinline__ F2 gelu_cdf2(F2 x) {
+  const F2 v = f2_mul(f2_neg(x), f2_splat(0.70710678118654752f));
+  return f2_mul(f2_splat(0.5f), erfc2<SHORT>(v));
+}
+
 // Phi(x) = erfc(-x / sqrt 2) / 2; SHORT: the result is stored as bfloat16.
 template <bool SHORT = false>
 __device__ __forceinline__ float gelu_cdf(float x) {
@@ -509,6 +607,15 @@ struct UnaryF {
   static constexpr int kMinBlocksWide = kOccEwFwd;  // 8-wide bfloat16: no spill at 4
   template <int VEC>
   __device__ __forceinline__ void operator()(const Vec<VEC> (&x)[3], Vec<VEC> (&y)[2], float alpha) const {
+    if (UOP == UN_GELU && VEC % 2 == 0) {
+      // Pairs of elements through the packed instructions (same results).
+#pragma unroll
+      for (int i = 0; i < VEC; i += 2) {
+        const F2 v = f2_pack(x[0].v[i], x[0].v[i + 1]);
+        f2_unpack(f2_mul(v, gelu_cdf2<SHORT>(v)), y[0].v[i], y[0].v[i + 1]);
+      }
+      return;
+    }
 #pragma unroll
     for (int i = 0; i < VEC; ++i) {
       const float v = x[0].v[i];
@@ -524,6 +631,19 @@ struct UnaryBwdF {
   static constexpr int kMinBlocksWide = UOP == UN_GELU ? kOccEwFwd - 1 : kOccEwFwd;
   template <int VEC>
   __device__ __forceinline__ void operator()(const Vec<VEC> (&x)[3], Vec<VEC> (&y)[2], float alpha) const {
+    if (UOP == UN_GELU && VEC % 2 == 0) {
+      // Pairs of elements through the packed instructions (same results).
+#pragma unroll
+      for (int i = 0; i < VEC; i += 2) {
+        const F2 g = f2_pack(x[0].v[i], x[0].v[i + 1]);
+        const F2 v = f2_pack(x[1].v[i], x[1].v[i + 1]);
+        float a0, a1;
+        f2_unpack(f2_mul(f2_mul(f2_splat(-0.72134752044448170f), v), v), a0, a1);
+        const F2 pdf = f2_mul(f2_pack(ex2_approx(a0), ex2_approx(a1)), f2_splat(0.39894228040143268f));
+        f2_unpack(f2_mul(g, f2_add(gelu_cdf2<SHORT>(v), f2_mul(v, pdf))), y[0].v[i], y[0].v[i + 1]);
+      }
+      return;
+    }
 #pragma unroll
     for (int i = 0; i < VEC; ++i) {
       const float g = x[0].v[i];
@@ -947,6 +1067,10 @@ k_reduce(const __grid_constant__ RedPlan p) {
   const uint32_t table_rows = p.rows_per_blk < kMaxTileRows ? p.rows_per_blk : kMaxTileRows;
   int64_t* s_off = s_dyn;  // [table_rows][kMaxOperands]
   float* s_red = reinterpret_cast<float*>(s_dyn + kMaxOperands * table_rows);
+  // Staging ring (p.stages > 0): [stages][stage_ns][4][kThreads] 16-byte
+  // slots.  It shares its memory with the tree (s_red), which is written
+  // only after every thread has finished its loads and passed a barrier.
+  uint4* s_stage = reinterpret_cast<uint4*>(s_red);
 
   const RedCta cta = red_cta(p, blockIdx.x);
   int64_t base[kMaxOperands];
@@ -1014,6 +1138,97 @@ k_reduce(const __grid_constant__ RedPlan p) {
     // for the 2-byte stream; the products' roundings and the tree add at
     // most 4u of each term's size, far inside the tolerance).
     constexpr bool kPairwise = !INNER_KEPT && sizeof(E) == 2;
+    // Inputs streamed per item besides g: a (when X is grad_b or the dense
+    // gradient needs it) or b (likewise).
+    constexpr bool kSA = (T::kXa || T::kDa) && WHICH != 0;
+    constexpr bool kSB = (T::kXb || T::kDb) && WHICH != 1;
+    const bool sa = kSA && read_a, sb = kSB && read_b;
+    // One item: row ri of the chunk, columns cc .. cc + VEC - 1.
+    auto proc = [&](const Raw<E, VEC>& gr, const Raw<E, VEC>& ar, const Raw<E, VEC>& br, uint32_t ri,
+                    uint32_t cc) {
+      const Vec<VEC> gv = unpack<VEC>(gr);
+      Vec<VEC> av, bv;
+      if (kSA && sa) av = unpack<VEC>(ar);
+      if (kSB && sb) bv = unpack<VEC>(br);
+      Vec<VEC> aw, bw;
+      float pr[VEC];
+#pragma unroll
+      for (int i = 0; i < VEC; ++i) {
+        const float aa = ((T::kXa || T::kDa) && read_a) ? (WHICH == 0 ? own.v[i] : av.v[i]) : 0.f;
+        const float bb = ((T::kXb || T::kDb) && read_b) ? (WHICH == 1 ? own.v[i] : bv.v[i]) : 0.f;
+        aw.v[i] = aa;
+        bw.v[i] = bb;
+        if (INNER_KEPT) acc[i].add_prod(gv.v[i], T::m(aa, bb));
+        else if (kPairwise) pr[i] = __fmul_rn(gv.v[i], T::m(aa, bb));
+        else acc[0].add_prod(gv.v[i], T::m(aa, bb));
+      }
+      if (kPairwise) {
+        // The vector's products by a fixed pairwise tree, then one
+        // compensated addition.
+#pragma unroll
+        for (int w = 1; w < VEC; w *= 2)
+#pragma unroll
+          for (int i = 0; i + w < VEC; i += 2 * w) pr[i] = __fadd_rn(pr[i], pr[i + w]);
+        acc[0].add(pr[0]);
+      }
+      if (has_d) {
+        Vec<VEC> dv;
+        T::d(gv, aw, bw, dv);
+        store_cols<VEC>(dE, s_off[ri * kMaxOperands + kSlotOut], p.inner_stride[kSlotOut], cc, dv);
+      }
+    };
+    if constexpr (VEC * sizeof(E) == 16) {
+      if (p.stages >= 2 && 1u + ((sa || sb) ? 1u : 0u) <= p.stage_ns) {
+        // Staged: each thread copies the 16-byte vectors of its items into
+        // its own slots of a ring of p.stages batches in shared memory
+        // (cp.async) and reads them back once its copies of that batch have
+        // landed, so p.stages - 1 further batches stay in flight while one
+        // is summed, without holding registers.  Same items, same order,
+        // same arithmetic as the loop below.
+        const uint32_t S = p.stages, NSL = p.stage_ns;
+        auto slot = [&](uint32_t st, uint32_t k, int u) {
+          return s_stage + ((st * NSL + k) * U + u) * kThreads + threadIdx.x;
+        };
+        uint32_t irm = 0, icm = 0, im = 0;
+        auto issue = [&](uint32_t st) {
+#pragma unroll
+          for (int u = 0; u < U; ++u) {
+            if (im < items) {
+              const uint32_t ri = ty + irm * p.ty;
+              const uint32_t cc = (vcol_begin + tx + icm * p.tx) * VEC;
+              const int64_t* ro = s_off + ri * kMaxOperands;
+              cp_async16(slot(st, 0, u), gE + ro[0] + cc);
+              if (kSA && sa) cp_async16(slot(st, 1, u), aE + ro[1] + cc);
+              if (kSB && sb) cp_async16(slot(st, 1, u), bE + ro[2] + cc);
+              if (++icm == ncs) { icm = 0; ++irm; }
+              ++im;
+            }
+          }
+          cp_async_commit();
+        };
+        for (uint32_t st = 0; st + 1 < S; ++st) issue(st);
+        uint32_t st = 0;
+        for (uint32_t m0 = 0; m0 < items; m0 += U) {
+          issue(st == 0 ? S - 1 : st - 1);  // the slot the previous batch used
+          if (S >= 3) cp_async_wait<2>();
+          else cp_async_wait<1>();
+#pragma unroll
+          for (int u = 0; u < U; ++u) {
+            if (m0 + u >= items) continue;
+            const uint32_t ri = ty + rm * p.ty;
+            const uint32_t cc = (vcol_begin + tx + cm * p.tx) * VEC;
+            if (++cm == ncs) { cm = 0; ++rm; }
+            Raw<E, VEC> gr = raw_from_u4<E, VEC>(*slot(st, 0, u)), ar, br;
+            if (kSA && sa) ar = raw_from_u4<E, VEC>(*slot(st, 1, u));
+            if (kSB && sb) br = raw_from_u4<E, VEC>(*slot(st, 1, u));
+            proc(gr, ar, br, ri, cc);
+          }
+          st = st + 1 == S ? 0 : st + 1;
+        }
+        cp_async_wait<0>();
+        continue;  // next chunk of rows
+      }
+    }
     for (uint32_t m0 = 0; m0 < items; m0 += U) {
       Raw<E, VEC> gr[U], ar[U], br[U];
       uint32_t ri[U], cc[U];
@@ -1026,48 +1241,14 @@ k_reduce(const __grid_constant__ RedPlan p) {
         if (ok[u]) {
           const int64_t* ro = s_off + ri[u] * kMaxOperands;
           gr[u] = load_raw<VEC>(gE, ro[0], p.inner_stride[0], cc[u], p.stream_mask & 1);
-          if ((T::kXa || T::kDa) && read_a && WHICH != 0)
-            ar[u] = load_raw<VEC>(aE, ro[1], p.inner_stride[1], cc[u], p.stream_mask & 2);
-          if ((T::kXb || T::kDb) && read_b && WHICH != 1)
-            br[u] = load_raw<VEC>(bE, ro[2], p.inner_stride[2], cc[u], p.stream_mask & 4);
+          if (kSA && sa) ar[u] = load_raw<VEC>(aE, ro[1], p.inner_stride[1], cc[u], p.stream_mask & 2);
+          if (kSB && sb) br[u] = load_raw<VEC>(bE, ro[2], p.inner_stride[2], cc[u], p.stream_mask & 4);
           if (++cm == ncs) { cm = 0; ++rm; }
         }
       }
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        if (!ok[u]) continue;
-        const Vec<VEC> gv = unpack<VEC>(gr[u]);
-        Vec<VEC> av, bv;
-        if ((T::kXa || T::kDa) && read_a && WHICH != 0) av = unpack<VEC>(ar[u]);
-        if ((T::kXb || T::kDb) && read_b && WHICH != 1) bv = unpack<VEC>(br[u]);
-        Vec<VEC> aw, bw;
-        float pr[VEC];
-#pragma unroll
-        for (int i = 0; i < VEC; ++i) {
-          const float aa = ((T::kXa || T::kDa) && read_a) ? (WHICH == 0 ? own.v[i] : av.v[i]) : 0.f;
-          const float bb = ((T::kXb || T::kDb) && read_b) ? (WHICH == 1 ? own.v[i] : bv.v[i]) : 0.f;
-          aw.v[i] = aa;
-          bw.v[i] = bb;
-          if (INNER_KEPT) acc[i].add_prod(gv.v[i], T::m(aa, bb));
-          else if (kPairwise) pr[i] = __fmul_rn(gv.v[i], T::m(aa, bb));
-          else acc[0].add_prod(gv.v[i], T::m(aa, bb));
-        }
-        if (kPairwise) {
-          // The vector's products by a fixed pairwise tree, then one
-          // compensated addition.
-#pragma unroll
-          for (int w = 1; w < VEC; w *= 2)
-#pragma unroll
-            for (int i = 0; i + w < VEC; i += 2 * w) pr[i] = __fadd_rn(pr[i], pr[i + w]);
-          acc[0].add(pr[0]);
-        }
-        if (has_d) {
-          Vec<VEC> dv;
-          T::d(gv, aw, bw, dv);
-          store_cols<VEC>(dE, s_off[ri[u] * kMaxOperands + kSlotOut], p.inner_stride[kSlotOut],
-                          cc[u], dv);
-        }
-      }
+      for (int u = 0; u < U; ++u)
+        if (ok[u]) proc(gr[u], ar[u], br[u], ri[u], cc[u]);
     }
   }
 

@@ -3,6 +3,11 @@
 #pragma once
 
 #include <cuda_runtime.h>
+
+#include <mutex>
+#include <utility>
+#include <vector>
+
 #include "zr_plan.h"
 
 namespace zr {
@@ -56,6 +61,30 @@ inline cudaError_t launch_k_cluster(void (*kernel)(KArgs...), unsigned grid, uns
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+// Kernels whose dynamic shared memory may exceed the default 48 KB limit:
+// raise_smem_limit sets the kernel's limit to the most a CTA may use, once
+// per kernel and device (remembered in a small table under a lock).
+inline cudaError_t raise_smem_limit(const void* kernel) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  static std::mutex mu;
+  static std::vector<std::pair<const void*, int>> done;
+  std::lock_guard<std::mutex> lock(mu);
+  for (const auto& d : done)
+    if (d.first == kernel && d.second == dev) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+  if (e == cudaSuccess) done.emplace_back(kernel, dev);
+  return e;
+}
+// The kernel itself when `smem` bytes are allowed for it, null otherwise (the
+// launch then fails with an error instead of running short of memory).
+template <typename... KArgs>
+inline auto with_smem(void (*kernel)(KArgs...), size_t smem) -> void (*)(KArgs...) {
+  if (smem <= 48 * 1024) return kernel;
+  return raise_smem_limit(reinterpret_cast<const void*>(kernel)) == cudaSuccess ? kernel : nullptr;
 }
 
 // Every launcher first checks that the plan provides each operand its kernel

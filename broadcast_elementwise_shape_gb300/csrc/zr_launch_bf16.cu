@@ -41,17 +41,20 @@ cudaError_t red_bf16(const RedBuild& rb, cudaStream_t s, bool dry) {
       (RedTerms<OP, WHICH>::reads_b(has_d) && !p.b) || !p.x_final ||
       (p.nslots > 1 && !p.partial) || p.cluster > 1)
     return cudaErrorInvalidValue;
+  if (p.stages != 0 && (rb.vec * sizeof(bf16) != 16 || p.stages < 2 || p.stages > 3 ||
+                        p.stage_ns < 1 || p.stage_ns > 2))
+    return cudaErrorInvalidValue;
   if (dry) return cudaSuccess;
-  const uint32_t table_rows = p.rows_per_blk < kMaxTileRows ? p.rows_per_blk : kMaxTileRows;
-  const size_t red_floats = p.inner_kept ? size_t(kThreads) * rb.vec : size_t(kThreads);
-  const size_t smem = size_t(table_rows) * kMaxOperands * sizeof(int64_t) + red_floats * sizeof(float);
+  const size_t smem = red_smem_bytes(p, rb.vec, p.stages, p.stage_ns);
   cudaError_t e;
   if (p.inner_kept) {
-    e = rb.vec == 8   ? launch_k(k_reduce<OP, WHICH, 8, true, false, bf16>, p.n_cta, kThreads, smem, s, p)
+    e = rb.vec == 8   ? launch_k(with_smem(k_reduce<OP, WHICH, 8, true, false, bf16>, smem), p.n_cta,
+                                 kThreads, smem, s, p)
         : rb.vec == 4 ? launch_k(k_reduce<OP, WHICH, 4, true, false, bf16>, p.n_cta, kThreads, smem, s, p)
                       : launch_k(k_reduce<OP, WHICH, 1, true, false, bf16>, p.n_cta, kThreads, smem, s, p);
   } else {
-    e = rb.vec == 8   ? launch_k(k_reduce<OP, WHICH, 8, false, false, bf16>, p.n_cta, kThreads, smem, s, p)
+    e = rb.vec == 8   ? launch_k(with_smem(k_reduce<OP, WHICH, 8, false, false, bf16>, smem), p.n_cta,
+                                 kThreads, smem, s, p)
         : rb.vec == 4 ? launch_k(k_reduce<OP, WHICH, 4, false, false, bf16>, p.n_cta, kThreads, smem, s, p)
                       : launch_k(k_reduce<OP, WHICH, 1, false, false, bf16>, p.n_cta, kThreads, smem, s, p);
   }

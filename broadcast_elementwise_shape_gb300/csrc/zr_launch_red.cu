@@ -20,24 +20,27 @@ cudaError_t launch_red_t(const RedBuild& rb, cudaStream_t s, bool dry) {
   if (p.cluster > 1 && (rb.vec != 4 || p.nslots != 1 || p.n_cta % p.cluster != 0 ||
                         p.cluster > kMaxCluster))
     return cudaErrorInvalidValue;
+  if (p.stages != 0 && (rb.vec * sizeof(float) != 16 || p.stages < 2 || p.stages > 3 ||
+                        p.stage_ns < 1 || p.stage_ns > 2))
+    return cudaErrorInvalidValue;
   if (dry) return cudaSuccess;
-  const uint32_t table_rows = p.rows_per_blk < kMaxTileRows ? p.rows_per_blk : kMaxTileRows;
-  const size_t red_floats = p.inner_kept ? size_t(kThreads) * rb.vec : size_t(kThreads);
-  const size_t smem = size_t(table_rows) * kMaxOperands * sizeof(int64_t) + red_floats * sizeof(float);
+  const size_t smem = red_smem_bytes(p, rb.vec, p.stages, p.stage_ns);
   cudaError_t e;
   if (p.cluster > 1) {
     return p.inner_kept
-               ? launch_k_cluster(k_reduce<OP, WHICH, 4, true, true>, p.n_cta, kThreads, smem, s,
-                                  p.cluster, p)
-               : launch_k_cluster(k_reduce<OP, WHICH, 4, false, true>, p.n_cta, kThreads, smem, s,
-                                  p.cluster, p);
+               ? launch_k_cluster(with_smem(k_reduce<OP, WHICH, 4, true, true>, smem), p.n_cta,
+                                  kThreads, smem, s, p.cluster, p)
+               : launch_k_cluster(with_smem(k_reduce<OP, WHICH, 4, false, true>, smem), p.n_cta,
+                                  kThreads, smem, s, p.cluster, p);
   }
   if (p.inner_kept) {
-    e = rb.vec == 4 ? launch_k(k_reduce<OP, WHICH, 4, true>, p.n_cta, kThreads, smem, s, p)
-                    : launch_k(k_reduce<OP, WHICH, 1, true>, p.n_cta, kThreads, smem, s, p);
+    e = rb.vec == 4
+            ? launch_k(with_smem(k_reduce<OP, WHICH, 4, true>, smem), p.n_cta, kThreads, smem, s, p)
+            : launch_k(k_reduce<OP, WHICH, 1, true>, p.n_cta, kThreads, smem, s, p);
   } else {
-    e = rb.vec == 4 ? launch_k(k_reduce<OP, WHICH, 4, false>, p.n_cta, kThreads, smem, s, p)
-                    : launch_k(k_reduce<OP, WHICH, 1, false>, p.n_cta, kThreads, smem, s, p);
+    e = rb.vec == 4
+            ? launch_k(with_smem(k_reduce<OP, WHICH, 4, false>, smem), p.n_cta, kThreads, smem, s, p)
+            : launch_k(k_reduce<OP, WHICH, 1, false>, p.n_cta, kThreads, smem, s, p);
   }
   if (e != cudaSuccess || p.nslots <= 1) return e;
   return launch_combine_f32(rb.comb, s);

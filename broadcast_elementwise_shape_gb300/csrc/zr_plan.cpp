@@ -156,6 +156,13 @@ int pick_vec(const Prob& P, uint32_t slots, const void* const* ptrs, const void*
 
 }  // namespace
 
+uint64_t red_smem_bytes(const RedPlan& p, int vec, uint32_t stages, uint32_t stage_ns) {
+  const uint64_t table_rows = std::min<uint64_t>(p.rows_per_blk, kMaxTileRows);
+  const uint64_t red_floats = p.inner_kept ? uint64_t(kThreads) * vec : uint64_t(kThreads);
+  return table_rows * kMaxOperands * sizeof(int64_t) +
+         std::max<uint64_t>(red_floats * sizeof(float), uint64_t(stages) * stage_ns * kStageBatchBytes);
+}
+
 void combine_vectorize(CombinePlan* c) {
   c->vec = 1;
   if (c->nout % 4 == 0 && c->nout >= 64 * 152 && reinterpret_cast<uintptr_t>(c->partial) % 16 == 0)
@@ -586,6 +593,40 @@ int build_red(const Prob& P, int xslot, const float* g, const float* a, const fl
   p.n_cta = uint32_t(ncta);
   rb->ws_bytes = p.nslots > 1 ? ((p.nslots * p.nout * sizeof(float) + 255) / 256) * 256 : 0;
 
+  // cp.async staging when every streamed input (g, and a or b unless it is
+  // the reduced gradient's own input, read once per thread) is read in
+  // 16-byte vectors with unit inner stride, and the grid runs at least two
+  // waves: three batches in flight where the CTAs per SM of the kernel still
+  // fit in shared memory, else two.  (Measured on GB300: c4's backward
+  // 186 -> 178 us and 121 -> 118 us, c4 in bf16 111 -> 102 us and
+  // 77 -> 71 us; single-wave grids, whose CTAs each stream one long range,
+  // measured slower staged: c5a's backward 22.9 -> 24.3 us.)
+  p.stages = 0;
+  p.stage_ns = 0;
+  const uint64_t cta_wave = uint64_t(kSms) * uint64_t(p.cluster > 1 ? occ_cl : occ);
+  if (uint32_t(rb->vec) * uint32_t(P.es) == 16 && uint64_t(p.n_cta) >= 2 * cta_wave) {
+    const uint32_t own = xslot == kSlotXA ? 2u : (xslot == kSlotXB ? 4u : 0u);  // a's or b's slot
+    const uint32_t streamed = ((read_mask & 7u) & ~own) | 1u;
+    bool unit = true;
+    uint32_t ns = 0;
+    for (int k = 0; k < 3; ++k)
+      if (streamed & (1u << k)) {
+        ++ns;
+        if (P.st[k][n - 1] != 1) unit = false;
+      }
+    const uint32_t cta_occ = p.cluster > 1 ? uint32_t(occ_cl) : uint32_t(occ);
+    if (unit && ns <= 2) {
+      for (uint32_t st = 3; st >= 2; --st) {
+        const uint64_t bytes = red_smem_bytes(p, rb->vec, st, ns);
+        if (cta_occ * (bytes + kSmemReservedPerCta) <= kSmemPerSm) {
+          p.stages = st;
+          p.stage_ns = ns;
+          break;
+        }
+      }
+    }
+  }
+
   CombinePlan& c = rb->comb;
   c = CombinePlan{};
   c.nout = p.nout;
@@ -743,10 +784,11 @@ std::string describe_red(const RedBuild& rb) {
                 "\"ncol\":%u,\"kept_dims\":%d,\"red_dims\":%d,\"tx\":%u,\"ty\":%u,"
                 "\"rows_per_blk\":%u,\"vcols_per_blk\":%u,\"n_rblk\":%u,\"n_cblk\":%u,"
                 "\"nslots\":%u,\"nout\":%llu,\"ctas\":%u,\"ws_bytes\":%zu,\"dense_out\":%d,"
-                "\"cluster\":%u}",
+                "\"cluster\":%u,\"stages\":%u,\"stage_ns\":%u}",
                 rb.vec, p.inner_kept, p.n_kept, p.n_red, p.ncol, p.kept.n, p.red.n, p.tx, p.ty,
                 p.rows_per_blk, p.vcols_per_blk, p.n_rblk, p.n_cblk, p.nslots,
-                (unsigned long long)p.nout, p.n_cta, rb.ws_bytes, p.d_out ? 1 : 0, p.cluster);
+                (unsigned long long)p.nout, p.n_cta, rb.ws_bytes, p.d_out ? 1 : 0, p.cluster,
+                p.stages, p.stage_ns);
   return buf;
 }
 

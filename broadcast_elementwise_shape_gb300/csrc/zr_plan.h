@@ -70,6 +70,9 @@ struct EwBuild {
 void combine_vectorize(CombinePlan* c);
 // Thread blocks of the second pass.
 uint64_t combine_blocks(const CombinePlan& c);
+// Dynamic shared memory of a reduction pass: its row-offset table, its tree
+// and `stages` staged batches of `stage_ns` streamed inputs.
+uint64_t red_smem_bytes(const RedPlan& p, int vec, uint32_t stages, uint32_t stage_ns);
 int build_ew(const Prob& P, const float* const in[3], float* const out[2], uint32_t read_mask,
              uint32_t stream_mask, int occ, EwBuild* eb);
 
