@@ -859,6 +859,9 @@ int zr_test_occupancy(int which, int* planned, int* actual) {
   else if (which >= 11 && which < 16) e = occupancy_red(which - 6, planned, actual);
   else if (which >= 16 && which < 20) e = occupancy_chain(which - 16, planned, actual);
   else if (which >= 20 && which < 22) e = occupancy_ew(which - 16, planned, actual);
+  else if (which >= 22 && which < 24) e = occupancy_ew(which - 16, planned, actual);
+  else if (which == 24) e = occupancy_bf16(0, planned, actual);
+  else if (which == 25) e = occupancy_red(10, planned, actual);
   else return ZR_ERR_SIZE;
   return cuda_status(e);
 }

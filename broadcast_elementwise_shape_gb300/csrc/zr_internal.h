@@ -153,6 +153,8 @@ constexpr uint32_t kSms = 152;  // SMs of a GB300
 constexpr int kOccEwFwd = 4;      // k_elementwise: forward
 constexpr int kOccEwBwd = 3;      // k_elementwise: backward without reduction
 constexpr int kOccEwCopy = 5;     // k_elementwise: copy (sum-to-shape onto the same shape)
+constexpr int kOccGeluFwd = 5;     // GeLU forward, float
+constexpr int kOccGeluFwdWide = 6; // GeLU forward, 8-wide bfloat16 (2 items per batch)
 constexpr int kOccRedAddSub = 4;  // k_reduce: add, sub, sum-to-shape
 constexpr int kOccRedMulDiv = 3;  // k_reduce: mul, div
 // k_reduce, cluster variant (no second pass): loads per item are 1 for add,

@@ -603,8 +603,14 @@ __device__ __forceinline__ float gelu_cdf(float x) {
 template <int UOP, bool SHORT = false>
 struct UnaryF {
   static constexpr bool kR1 = false, kR2 = false;
-  static constexpr int kMinBlocks = kOccEwFwd;
-  static constexpr int kMinBlocksWide = kOccEwFwd;  // 8-wide bfloat16: no spill at 4
+  // GeLU's arithmetic per load is long, so it gains from more resident warps
+  // rather than more loads in flight per thread: float GeLU at 5 CTAs per SM
+  // (u1 forward 64.2 -> 61.4 us), the 8-wide bfloat16 one at 6 CTAs per SM
+  // with 2 items per batch in the flat kernel (u1h forward 45.1 -> 43.1 us);
+  // neither spills.
+  static constexpr int kMinBlocks = UOP == UN_GELU ? kOccGeluFwd : kOccEwFwd;
+  static constexpr int kMinBlocksWide = UOP == UN_GELU ? kOccGeluFwdWide : kOccEwFwd;
+  static constexpr int kUnroll = (UOP == UN_GELU && SHORT) ? 2 : 4;
   template <int VEC>
   __device__ __forceinline__ void operator()(const Vec<VEC> (&x)[3], Vec<VEC> (&y)[2], float alpha) const {
     if (UOP == UN_GELU && VEC % 2 == 0) {
@@ -684,6 +690,13 @@ struct Uniform2 { static constexpr bool value = false; };
 template <class F>
 struct Uniform2<F, decltype(void(F::kUniform2))> { static constexpr bool value = F::kUniform2; };
 
+// Items each thread loads before it computes any (per pass of the elementwise
+// kernels' loops): 4, or the functor's kUnroll.
+template <class F, class = void>
+struct ItemsPerPass { static constexpr int value = 4; };
+template <class F>
+struct ItemsPerPass<F, decltype(void(F::kUnroll))> { static constexpr int value = F::kUnroll; };
+
 // One CTA = one tile of rows x column vectors.  Each thread takes items
 // threadIdx.x + k * 256; items are processed in batches of U so that U
 // independent loads per operand are in flight before any result is stored.
@@ -718,7 +731,7 @@ k_elementwise(const __grid_constant__ EwPlan p) {
   if (kUni1) uni1 = ld1(in1, false);
   if (kUni2) uni2 = ld1(in2, false);
 
-  constexpr int U = 4;
+  constexpr int U = ItemsPerPass<F>::value;
   const F f;
   for (uint32_t it0 = 0; it0 < p.items_per_cta; it0 += U * blockDim.x) {
     Raw<E, VEC> xr[U][3];
@@ -771,9 +784,9 @@ k_elementwise(const __grid_constant__ EwPlan p) {
 // as k_elementwise for problems with at most one outer dim (same-shape,
 // scalar, bias-like rows), with no offset table, no barrier and no
 // shared memory.  A CTA's items are consecutive in row-major order and come
-// in whole batches of U * 256, so every batch issues U loads per operand
-// from every thread; each batch's u-th group of 256 items is 256
-// consecutive vectors (coalesced).
+// in whole batches of 1024 (U * 256 each pass of the loop), so every pass
+// issues U loads per operand from every thread; each pass's u-th group of
+// 256 items is 256 consecutive vectors (coalesced).
 template <class F, int VEC, int NOUT, class E = float>
 __global__ void __launch_bounds__(kThreads, VEC == 8 ? WideBlocks<F>::value : F::kMinBlocks)
 k_flat(const __grid_constant__ EwPlan p) {
@@ -793,7 +806,7 @@ k_flat(const __grid_constant__ EwPlan p) {
   if (kUni1) uni1 = ld1(in1, false);
   if (kUni2) uni2 = ld1(in2, false);
 
-  constexpr int U = 4;
+  constexpr int U = ItemsPerPass<F>::value;
   const F f;
   for (uint32_t it0 = first; it0 < end; it0 += U * kThreads) {
     Raw<E, VEC> xr[U][3];
@@ -978,7 +991,10 @@ k_sabf(const __grid_constant__ SabFPlan p) {
     for (int j = 0; j < RPT; ++j) {
       const float4 r = make_float4(fwd_op<OP>(areg[j].x, b4.x), fwd_op<OP>(areg[j].y, b4.y),
                                    fwd_op<OP>(areg[j].z, b4.z), fwd_op<OP>(areg[j].w, b4.w));
-      *reinterpret_cast<float4*>(p.out + ooff[j] + bo[0]) = r;
+      // Evict-first stores: the 3 GB written here is never read back by
+      // this kernel (c5b's forward 466.9 -> 440.1 us; the same hint on the
+      // flat and reduction kernels measured no faster).
+      __stcs(reinterpret_cast<float4*>(p.out + ooff[j] + bo[0]), r);
     }
   }
 }

@@ -110,10 +110,14 @@ cudaError_t launch_reduce(int op, int which, const RedBuild& rb, cudaStream_t s,
 // family (the 16-byte-vector variants the workloads run), as the planner
 // assumes (*planned) and as the runtime reports for the current device
 // (*actual).  ew: 0 fwd add, 1 fwd div, 2 bwd div (both gradients), 3 copy,
-// 4 GeLU forward, 5 GeLU backward;
+// 4 GeLU forward, 5 GeLU backward, 6 flat fwd add, 7 flat GeLU forward;
+// bf16: 0 flat 8-wide GeLU forward;
 // red: 0 add inner kept, 1 sub inner reduced, 2 mul inner kept, 3 div inner
-// reduced, 4 sum-to-shape; 5..9 the same five as cluster variants; other: 0 k_sabf (8 rows per thread), 1 k_transpose.
+// reduced, 4 sum-to-shape; 5..9 the same five as cluster variants; 10 add
+// inner kept with a three-batch staging ring; other: 0 k_sabf (8 rows per
+// thread), 1 k_transpose.
 cudaError_t occupancy_ew(int which, int* planned, int* actual);
+cudaError_t occupancy_bf16(int which, int* planned, int* actual);
 cudaError_t occupancy_red(int which, int* planned, int* actual);
 cudaError_t occupancy_other(int which, int* planned, int* actual);
 

@@ -106,6 +106,16 @@ cudaError_t launch_bwd_direct_bf16(int op, int want, const EwBuild& eb, cudaStre
   }
 }
 
+cudaError_t occupancy_bf16(int which, int* planned, int* actual) {
+  switch (which) {
+    case 0:  // the flat kernel's 8-wide GeLU forward
+      *planned = kOccGeluFwdWide;
+      return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+          actual, k_flat<UnaryF<UN_GELU, true>, 8, 1, bf16>, kThreads, 0);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
 cudaError_t launch_copy_bf16(const EwBuild& eb, cudaStream_t s, bool dry) {
   return launch_ew_bf16<CopyF, 1>(eb, s, dry);
 }

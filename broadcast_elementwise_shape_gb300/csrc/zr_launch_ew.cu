@@ -121,13 +121,22 @@ cudaError_t occupancy_ew(int which, int* planned, int* actual) {
       return cudaOccupancyMaxActiveBlocksPerMultiprocessor(actual, k_elementwise<CopyF, 4, 1>,
                                                            kThreads, smem);
     case 4:
-      *planned = kOccEwFwd;
+      *planned = kOccGeluFwd;
       return cudaOccupancyMaxActiveBlocksPerMultiprocessor(actual, k_elementwise<UnaryF<UN_GELU>, 4, 1>,
                                                            kThreads, smem);
     case 5:
       *planned = kOccEwFwd;
       return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
           actual, k_elementwise<UnaryBwdF<UN_GELU>, 4, 1>, kThreads, smem);
+    // The flat kernel (no shared memory): forward add, float GeLU forward.
+    case 6:
+      *planned = kOccEwFwd;
+      return cudaOccupancyMaxActiveBlocksPerMultiprocessor(actual, k_flat<FwdF<OP_ADD>, 4, 1>,
+                                                           kThreads, 0);
+    case 7:
+      *planned = kOccGeluFwd;
+      return cudaOccupancyMaxActiveBlocksPerMultiprocessor(actual, k_flat<UnaryF<UN_GELU>, 4, 1>,
+                                                           kThreads, 0);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -106,6 +106,15 @@ cudaError_t occupancy_red(int which, int* planned, int* actual) {
       *planned = red_cl_occ(OP_ADD, true);
       return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
           actual, k_reduce<OP_ADD, 2, 4, true, true>, kThreads, smem);
+    case 10: {
+      // Staged: c4's mask gradient (96 rows per CTA, three 16 KB batches).
+      *planned = kOccRedAddSub;
+      const size_t staged = size_t(96) * kMaxOperands * sizeof(int64_t) + 3 * kStageBatchBytes;
+      const cudaError_t e = raise_smem_limit(reinterpret_cast<const void*>(k_reduce<OP_ADD, 1, 4, true>));
+      if (e != cudaSuccess) return e;
+      return cudaOccupancyMaxActiveBlocksPerMultiprocessor(actual, k_reduce<OP_ADD, 1, 4, true>,
+                                                           kThreads, staged);
+    }
     default: return cudaErrorInvalidValue;
   }
 }

@@ -51,13 +51,15 @@ int zr_test_dry_run_bwd(zr_op op, zr_tensor grad_out, zr_tensor a, zr_tensor b,
 int zr_test_dry_run_sum(zr_tensor in, int32_t ndim_out, const int64_t* sizes_out,
                         const float* out);
 
-/* Resident CTAs per SM of kernel `which` (0..21: elementwise forward add,
+/* Resident CTAs per SM of kernel `which` (0..25: elementwise forward add,
  * forward div, backward div, copy; reduction add inner-kept, sub
  * inner-reduced, mul inner-kept, div inner-reduced, sum-to-shape; split
  * forward; transpose; then the five reductions again in their cluster
  * variant; chain forward, fused chain backward with c shaped like b, the
  * same with c one element, chain forward with c one element; GeLU forward,
- * GeLU backward) as the planner sizes grids for (*planned) and as the
+ * GeLU backward; flat forward add, flat GeLU forward, flat bfloat16 GeLU
+ * forward; reduction add inner-kept with a three-batch staging ring in
+ * shared memory) as the planner sizes grids for (*planned) and as the
  * CUDA runtime reports for the current device (*actual).  Needs a device:
  * ZR_ERR_CUDA without one; ZR_ERR_SIZE for an unknown `which`. */
 int zr_test_occupancy(int which, int* planned, int* actual);
