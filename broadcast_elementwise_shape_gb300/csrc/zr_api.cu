@@ -321,15 +321,17 @@ int plan_bwd(int op, const zr_tensor& tg, const zr_tensor& ta, const zr_tensor& 
     // Cluster plans are built for float storage only.
     const int ock = S->es == 4 ? red_cl_occ(op, true) : 0;
     const int ocr = S->es == 4 ? red_cl_occ(op, false) : 0;
+    // div's grad_b carries the factor -1/b^2, applied once to each total.
+    const bool post = op == OP_DIV && w == 1;
     rc = build_red(P, xslot, S->g.ptr, ra ? S->a.ptr : nullptr, rbb ? S->b.ptr : nullptr, rm,
-                   stream_mask & rm, xo, d_out, 0, occ, ock, ocr, &rb);
+                   stream_mask & rm, xo, d_out, 0, occ, ock, ocr, &rb, post);
     if (rc) return rc;
     size_t q = rb.ws_bytes;
     for (int v : {1, 4, 8}) {
       if (v == 8 && S->es != 2) continue;  // 8-wide vectors: bfloat16 only
       RedBuild tmp;
       rc = build_red(P, xslot, S->g.ptr, nullptr, nullptr, rm, 0, xo, d_out, v, occ, ock, ocr,
-                     &tmp);
+                     &tmp, post);
       if (rc) return rc;
       q = std::max(q, tmp.ws_bytes);
     }
@@ -343,7 +345,8 @@ int plan_bwd(int op, const zr_tensor& tg, const zr_tensor& ta, const zr_tensor& 
   S->ws_query = off_q;
   // Both gradients reduced: one fused pass when the shape allows it.
   if (red_a && red_b && S->es == 4) {
-    const int r = build_sab(P, S->g.ptr, S->a.ptr, S->b.ptr, grad_a, grad_b, read_mask, &S->sb);
+    const int r = build_sab(P, S->g.ptr, S->a.ptr, S->b.ptr, grad_a, grad_b, read_mask, &S->sb,
+                            op == OP_DIV);
     if (r == ZR_OK) {
       S->sab = true;
       S->ws_run = S->sb.ws_a_bytes + S->sb.ws_b_bytes;
@@ -353,7 +356,7 @@ int plan_bwd(int op, const zr_tensor& tg, const zr_tensor& ta, const zr_tensor& 
     // The query covers whichever route the run-time pointers select.
     SabBuild any;
     const float* fake = reinterpret_cast<const float*>(uintptr_t(256));
-    if (build_sab(P, fake, fake, fake, grad_a, grad_b, read_mask, &any) == ZR_OK)
+    if (build_sab(P, fake, fake, fake, grad_a, grad_b, read_mask, &any, op == OP_DIV) == ZR_OK)
       S->ws_query = std::max(S->ws_query, any.ws_a_bytes + any.ws_b_bytes);
   }
   return ZR_OK;
@@ -1427,11 +1430,12 @@ int plan_chain_bwd(int op1, int op2, const zr_tensor& tg, const zr_tensor& ta, c
     if (rc) return rc;
     const uint32_t stream_mask = 1u | 2u | (S->b.numel == S->g.numel ? 4u : 0u);
     ChainBuild q;
+    const bool div1 = op1 == OP_DIV, div2 = op2 == OP_DIV;
     if (build_chain(P, S->g.ptr, S->a.ptr, S->b.ptr, S->c.ptr, c_scalar, grad_a, grad_b, grad_c,
-                    stream_mask, 4, &q) == ZR_OK)
+                    stream_mask, 4, &q, div1, div2) == ZR_OK)
       fused_q = align256(q.ws_b_bytes) + q.ws_c_bytes;
     const int r = build_chain(P, S->g.ptr, S->a.ptr, S->b.ptr, S->c.ptr, c_scalar, grad_a,
-                              grad_b, grad_c, stream_mask, 0, &S->cb);
+                              grad_b, grad_c, stream_mask, 0, &S->cb, div1, div2);
     if (r == ZR_OK) {
       S->fused = true;
       S->off_c = align256(S->cb.ws_b_bytes);

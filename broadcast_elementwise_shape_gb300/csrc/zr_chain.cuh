@@ -148,21 +148,34 @@ k_chain_bwd(const __grid_constant__ ChainPlan cp) {
     }
     __syncthreads();
     if (ty == 0 && vc < vcol_end) {
-      Vec<VEC> r;
+      Vec<VEC> r, f;  // sums, and div's -1/b^2 (-1/c^2) factors (1 otherwise)
       const bool div = which == 0 ? OP1 == OP_DIV : OP2 == OP_DIV;
 #pragma unroll
       for (int i = 0; i < VEC; ++i) {
         r.v[i] = s_red[tx * VEC + i];
+        f.v[i] = 1.0f;
         if (div) {
           const float rc = __frcp_rn(which == 0 ? bown.v[i] : cown.v[i]);
-          r.v[i] = __fmul_rn(r.v[i], -__fmul_rn(rc, rc));
+          f.v[i] = -__fmul_rn(rc, rc);
         }
       }
-      float* dst;
-      if (p.nslots == 1) dst = (which == 0 ? p.x_final : cp.c_final) + j;
-      else dst = p.partial + uint64_t(cta.rblk) * (CSCALAR ? p.nout : 2 * p.nout) +
-                 (which == 0 ? 0 : p.nout) + j;
-      store_cols<VEC>(dst, 0, 1, 0, r);
+      if (p.nslots == 1) {
+        if (div) {
+#pragma unroll
+          for (int i = 0; i < VEC; ++i) r.v[i] = __fmul_rn(r.v[i], f.v[i]);
+        }
+        store_cols<VEC>((which == 0 ? p.x_final : cp.c_final) + j, 0, 1, 0, r);
+      } else {
+        // Unscaled partials in slot row [grad_b | grad_c]; with a division
+        // in the chain the rblk-0 CTAs also store every output's factor in a
+        // row after the slots, and the second pass multiplies each total by
+        // it (so no partial can overflow on its own).
+        const uint64_t width = CSCALAR ? p.nout : 2 * p.nout;
+        const uint64_t col0 = (which == 0 ? 0 : p.nout) + j;
+        store_cols<VEC>(p.partial + uint64_t(cta.rblk) * width + col0, 0, 1, 0, r);
+        if ((OP1 == OP_DIV || (!CSCALAR && OP2 == OP_DIV)) && cta.rblk == 0)
+          store_cols<VEC>(p.partial + uint64_t(p.nslots) * width + col0, 0, 1, 0, f);
+      }
     }
   }
   if (CSCALAR) {
@@ -175,12 +188,18 @@ k_chain_bwd(const __grid_constant__ ChainPlan cp) {
     }
     if (threadIdx.x == 0) {
       float r = s_red[0];
+      float f = 1.0f;
       if (OP2 == OP_DIV) {
         const float rc = __frcp_rn(c0);
-        r = __fmul_rn(r, -__fmul_rn(rc, rc));
+        f = -__fmul_rn(rc, rc);
       }
-      if (p.n_cta == 1) *cp.c_final = r;
-      else cp.c_partial[blockIdx.x] = r;
+      if (p.n_cta == 1) {
+        *cp.c_final = OP2 == OP_DIV ? __fmul_rn(r, f) : r;
+      } else {
+        // Unscaled per-CTA partial; CTA 0 stores the factor after them.
+        cp.c_partial[blockIdx.x] = r;
+        if (OP2 == OP_DIV && blockIdx.x == 0) cp.c_partial[p.n_cta] = f;
+      }
     }
   }
 }

@@ -391,6 +391,11 @@ struct CombinePlan {
   uint32_t jx, sy;          // thread layout: jx output groups x sy slot lanes
   float scale;
   uint32_t vec;             // outputs per group (1, or 4 with 16-byte partial loads)
+  // post = 1: output j's total is multiplied by partial[nslots * nout + j],
+  // a factor the first pass stored after the slots (division's -1/b^2,
+  // applied once to the whole sum so that no partial can overflow on its
+  // own).
+  uint32_t post;
 };
 
 }  // namespace zr

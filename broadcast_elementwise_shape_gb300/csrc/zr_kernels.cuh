@@ -47,6 +47,19 @@ __device__ __forceinline__ bool div_fast_ok(float x, float y) {
   return div_fast_range(x) & div_fast_range(y);
 }
 
+// Division by a power of two as a multiplication: when d = +-2^k and 1/d are
+// both normal binary32 numbers (k in [-126, 126]), x / d and x * (1/d) are
+// the same real number for every x, so their single roundings agree bit for
+// bit, zeros, infinities, NaNs and results in the subnormal range included.
+// Sets *r = 1/d (exact) and returns true for such d.
+__device__ __forceinline__ bool pow2_reciprocal(float d, float* r) {
+  const uint32_t u = __float_as_uint(d);
+  const uint32_t e = (u >> 23) & 0xFFu;
+  if ((u & 0x7FFFFFu) != 0u || e < 1u || e > 253u) return false;
+  *r = __uint_as_float((u & 0x80000000u) | ((254u - e) << 23));
+  return true;
+}
+
 template <int OP>
 __device__ __forceinline__ float fwd_op(float x, float y) {
   if (OP == OP_ADD) return __fadd_rn(x, y);
@@ -429,6 +442,17 @@ struct FwdF {
   static constexpr int kMinBlocksWide = kOccEwFwd;
   template <int VEC>
   __device__ __forceinline__ void operator()(const Vec<VEC> (&x)[3], Vec<VEC> (&y)[2], float) const {
+    if (OP == OP_DIV && B_ONE) {
+      // One divisor for every element: a power of two divides by one exact
+      // multiplication (pow2_reciprocal; the check depends only on the
+      // divisor, so it is made once per thread).
+      float r;
+      if (pow2_reciprocal(x[1].v[0], &r)) {
+#pragma unroll
+        for (int i = 0; i < VEC; ++i) y[0].v[i] = __fmul_rn(x[0].v[i], r);
+        return;
+      }
+    }
     fwd_vec<OP, SHORT>(x[0], x[1], y[0]);
   }
 };
@@ -613,19 +637,19 @@ struct UnaryF {
   static constexpr int kUnroll = (UOP == UN_GELU && SHORT) ? 2 : 4;
   template <int VEC>
   __device__ __forceinline__ void operator()(const Vec<VEC> (&x)[3], Vec<VEC> (&y)[2], float alpha) const {
-    if (UOP == UN_GELU && VEC % 2 == 0) {
+    if constexpr (UOP == UN_GELU && VEC % 2 == 0) {
       // Pairs of elements through the packed instructions (same results).
 #pragma unroll
       for (int i = 0; i < VEC; i += 2) {
         const F2 v = f2_pack(x[0].v[i], x[0].v[i + 1]);
         f2_unpack(f2_mul(v, gelu_cdf2<SHORT>(v)), y[0].v[i], y[0].v[i + 1]);
       }
-      return;
-    }
+    } else {
 #pragma unroll
-    for (int i = 0; i < VEC; ++i) {
-      const float v = x[0].v[i];
-      y[0].v[i] = UOP == UN_SCALE ? __fmul_rn(alpha, v) : __fmul_rn(v, gelu_cdf<SHORT>(v));
+      for (int i = 0; i < VEC; ++i) {
+        const float v = x[0].v[i];
+        y[0].v[i] = UOP == UN_SCALE ? __fmul_rn(alpha, v) : __fmul_rn(v, gelu_cdf<SHORT>(v));
+      }
     }
   }
 };
@@ -637,7 +661,7 @@ struct UnaryBwdF {
   static constexpr int kMinBlocksWide = UOP == UN_GELU ? kOccEwFwd - 1 : kOccEwFwd;
   template <int VEC>
   __device__ __forceinline__ void operator()(const Vec<VEC> (&x)[3], Vec<VEC> (&y)[2], float alpha) const {
-    if (UOP == UN_GELU && VEC % 2 == 0) {
+    if constexpr (UOP == UN_GELU && VEC % 2 == 0) {
       // Pairs of elements through the packed instructions (same results).
 #pragma unroll
       for (int i = 0; i < VEC; i += 2) {
@@ -648,19 +672,19 @@ struct UnaryBwdF {
         const F2 pdf = f2_mul(f2_pack(ex2_approx(a0), ex2_approx(a1)), f2_splat(0.39894228040143268f));
         f2_unpack(f2_mul(g, f2_add(gelu_cdf2<SHORT>(v), f2_mul(v, pdf))), y[0].v[i], y[0].v[i + 1]);
       }
-      return;
-    }
+    } else {
 #pragma unroll
-    for (int i = 0; i < VEC; ++i) {
-      const float g = x[0].v[i];
-      if (UOP == UN_SCALE) {
-        y[0].v[i] = __fmul_rn(alpha, g);
-      } else {
-        const float v = x[1].v[i];
-        // phi(v) = exp(-v^2 / 2) / sqrt(2 pi) = 2^(-(log2 e / 2) v^2) / sqrt(2 pi)
-        const float pdf = __fmul_rn(ex2_approx(__fmul_rn(__fmul_rn(-0.72134752044448170f, v), v)),
-                                    0.39894228040143268f);
-        y[0].v[i] = __fmul_rn(g, __fadd_rn(gelu_cdf<SHORT>(v), __fmul_rn(v, pdf)));
+      for (int i = 0; i < VEC; ++i) {
+        const float g = x[0].v[i];
+        if (UOP == UN_SCALE) {
+          y[0].v[i] = __fmul_rn(alpha, g);
+        } else {
+          const float v = x[1].v[i];
+          // phi(v) = exp(-v^2 / 2) / sqrt(2 pi) = 2^(-(log2 e / 2) v^2) / sqrt(2 pi)
+          const float pdf = __fmul_rn(ex2_approx(__fmul_rn(__fmul_rn(-0.72134752044448170f, v), v)),
+                                      0.39894228040143268f);
+          y[0].v[i] = __fmul_rn(g, __fadd_rn(gelu_cdf<SHORT>(v), __fmul_rn(v, pdf)));
+        }
       }
     }
   }
@@ -1117,6 +1141,15 @@ k_reduce(const __grid_constant__ RedPlan p) {
   Vec<VEC> own;
 #pragma unroll
   for (int i = 0; i < VEC; ++i) own.v[i] = 0.f;
+  // div with grad_b reduced: the dense gradient is g / b with b = own, and
+  // own serves nothing else (grad_b's own factor is applied once, by post).
+  // For bfloat16 storage, when every lane of own is a power of two, own is
+  // replaced by 1/b and the dense gradient is g * own, bit for bit
+  // (pow2_reciprocal): c4's backward division in bf16 103 -> 96 us.  Float
+  // storage keeps the IEEE division there: it is not what bounds that
+  // kernel, and the flag's registers made it spill.
+  constexpr bool kP2 = OP == OP_DIV && WHICH == 1 && sizeof(E) == 2;
+  bool own_p2 = false;
 
   for (uint32_t ch0 = 0; ch0 < nrows; ch0 += kMaxTileRows) {
     const uint32_t cleft = nrows - ch0;
@@ -1138,6 +1171,16 @@ k_reduce(const __grid_constant__ RedPlan p) {
         if (needed)
           own = load_cols<VEC>(WHICH == 0 ? aE : bE, base[slot], p.inner_stride[slot],
                                (vcol_begin + tx) * VEC, false);
+        if (kP2 && needed) {
+          Vec<VEC> r;
+          bool p2 = true;
+#pragma unroll
+          for (int i = 0; i < VEC; ++i) p2 = pow2_reciprocal(own.v[i], &r.v[i]) && p2;
+          if (p2) {
+            own = r;
+            own_p2 = true;
+          }
+        }
       }
     }
 
@@ -1189,7 +1232,12 @@ k_reduce(const __grid_constant__ RedPlan p) {
       }
       if (has_d) {
         Vec<VEC> dv;
-        T::d(gv, aw, bw, dv);
+        if (kP2 && own_p2) {
+#pragma unroll
+          for (int i = 0; i < VEC; ++i) dv.v[i] = __fmul_rn(gv.v[i], own.v[i]);
+        } else {
+          T::d(gv, aw, bw, dv);
+        }
         store_cols<VEC>(dE, s_off[ri * kMaxOperands + kSlotOut], p.inner_stride[kSlotOut], cc, dv);
       }
     };
@@ -1309,17 +1357,25 @@ k_reduce(const __grid_constant__ RedPlan p) {
       const uint64_t j = uint64_t(cta.kidx) * p.ncol + uint64_t(vc) * VEC;
 #pragma unroll
       for (int i = 0; i < VEC; ++i) r.v[i] = s_red[tx * VEC + i];
+      Vec<VEC> f;  // div's -1/b^2 per output
       if (T::kPost) {
         const Vec<VEC> bv = load_cols<VEC>(bE, base[2], p.inner_stride[2], vc * VEC, false);
 #pragma unroll
-        for (int i = 0; i < VEC; ++i) r.v[i] = __fmul_rn(r.v[i], T::post(bv.v[i]));
+        for (int i = 0; i < VEC; ++i) f.v[i] = T::post(bv.v[i]);
       }
       if (p.nslots == 1) {
 #pragma unroll
-        for (int i = 0; i < VEC; ++i) r.v[i] = __fmul_rn(r.v[i], p.scale);
+        for (int i = 0; i < VEC; ++i) {
+          if (T::kPost) r.v[i] = __fmul_rn(r.v[i], f.v[i]);
+          r.v[i] = __fmul_rn(r.v[i], p.scale);
+        }
         store_cols<VEC>(xE + j, 0, 1, 0, r);
       } else {
+        // Partials stay unscaled: the second pass multiplies each total by
+        // its factor, stored after the slots by the slot-0 CTAs.
         store_cols<VEC>(p.partial + uint64_t(cta.rblk) * p.nout + j, 0, 1, 0, r);
+        if (T::kPost && cta.rblk == 0)
+          store_cols<VEC>(p.partial + uint64_t(p.nslots) * p.nout + j, 0, 1, 0, f);
       }
     }
   } else {
@@ -1343,18 +1399,22 @@ k_reduce(const __grid_constant__ RedPlan p) {
     }
     if (threadIdx.x == 0) {
       float r = s_red[0];
-      if (T::kPost) r = __fmul_rn(r, T::post(ld1(bE + base[2], false)));
+      const float f = T::kPost ? T::post(ld1(bE + base[2], false)) : 1.0f;
       if (p.nslots == 1) {
+        if (T::kPost) r = __fmul_rn(r, f);
         st1(xE + cta.kidx, __fmul_rn(r, p.scale));
       } else {
+        // Unscaled partial; slot 0 also stores the factor for the second pass.
         const uint64_t slot = uint64_t(cta.rblk) * p.n_cblk + cta.cblk;
         p.partial[slot * p.nout + cta.kidx] = r;
+        if (T::kPost && slot == 0) p.partial[uint64_t(p.nslots) * p.nout + cta.kidx] = f;
       }
     }
   }
 }
 
-// Second pass: for each output j, add its nslots partials in slot order.
+// Second pass: for each output j, add its nslots partials in slot order (and
+// multiply the total by its factor when p.post is set).
 // Thread (jx lane, sy lane) adds slots sy, sy + sy_n, ... (Kahan), then a
 // fixed tree over the sy lanes.  V = 4: each thread takes 4 consecutive
 // outputs with 16-byte loads of the partials (more bytes in flight per
@@ -1418,7 +1478,9 @@ k_combine(const __grid_constant__ CombinePlan p) {
     for (int i = 0; i < V; ++i) {
       const uint64_t jj = j + i;
       if (jj >= p.nout) break;
-      const float v = __fmul_rn(s_red[jl * V + i], p.scale);
+      float v = s_red[jl * V + i];
+      if (p.post) v = __fmul_rn(v, __ldg(p.partial + uint64_t(p.nslots) * p.nout + jj));
+      v = __fmul_rn(v, p.scale);
       st1(jj < p.split ? out + jj : out2 + (jj - p.split), v);
     }
   }

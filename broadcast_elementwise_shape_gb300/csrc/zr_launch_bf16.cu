@@ -41,6 +41,9 @@ cudaError_t red_bf16(const RedBuild& rb, cudaStream_t s, bool dry) {
       (RedTerms<OP, WHICH>::reads_b(has_d) && !p.b) || !p.x_final ||
       (p.nslots > 1 && !p.partial) || p.cluster > 1)
     return cudaErrorInvalidValue;
+  // With partial slots, division's grad_b stores its factors after the slots:
+  // only a plan whose workspace was sized for them may run.
+  if (RedTerms<OP, WHICH>::kPost && p.nslots > 1 && !rb.comb.post) return cudaErrorInvalidValue;
   if (p.stages != 0 && (rb.vec * sizeof(bf16) != 16 || p.stages < 2 || p.stages > 3 ||
                         p.stage_ns < 1 || p.stage_ns > 2))
     return cudaErrorInvalidValue;

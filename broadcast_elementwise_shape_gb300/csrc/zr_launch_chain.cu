@@ -88,6 +88,12 @@ cudaError_t launch_chain_bwd(int op1, int op2, const ChainBuild& cb, cudaStream_
       (!cp.c_scalar && p.nslots > 1 && (cb.comb_b.split != p.nout || !cb.comb_b.out2)) ||
       (cp.c_scalar && p.n_cta > 1 && !cp.c_partial))
     return cudaErrorInvalidValue;
+  // With a division in the chain the kernel stores per-output factors after
+  // the partial slots: only a plan whose workspace holds them may run.
+  const bool rows_post = op1 == OP_DIV || (!cp.c_scalar && op2 == OP_DIV);
+  if ((rows_post && p.nslots > 1 && !cb.comb_b.post) ||
+      (cp.c_scalar && op2 == OP_DIV && p.n_cta > 1 && !cb.comb_c.post))
+    return cudaErrorInvalidValue;
   if (dry) return cudaSuccess;
   return bwd_dispatch(op1, op2, cb, s);
 }

@@ -34,7 +34,9 @@ cudaError_t launch_fwd(int op, const EwBuild& eb, cudaStream_t s, bool dry) {
     case OP_ADD: return launch_ew_t<FwdF<OP_ADD>, 1>(eb, s, dry);
     case OP_SUB: return launch_ew_t<FwdF<OP_SUB>, 1>(eb, s, dry);
     case OP_MUL: return launch_ew_t<FwdF<OP_MUL>, 1>(eb, s, dry);
-    default: return launch_ew_t<FwdF<OP_DIV>, 1>(eb, s, dry);
+    default:
+      return eb.uni1 ? launch_ew_t<FwdF<OP_DIV, false, true>, 1>(eb, s, dry)
+                     : launch_ew_t<FwdF<OP_DIV>, 1>(eb, s, dry);
   }
 }
 

@@ -20,6 +20,9 @@ cudaError_t launch_red_t(const RedBuild& rb, cudaStream_t s, bool dry) {
   if (p.cluster > 1 && (rb.vec != 4 || p.nslots != 1 || p.n_cta % p.cluster != 0 ||
                         p.cluster > kMaxCluster))
     return cudaErrorInvalidValue;
+  // With partial slots, division's grad_b stores its factors after the slots:
+  // only a plan whose workspace was sized for them may run.
+  if (RedTerms<OP, WHICH>::kPost && p.nslots > 1 && !rb.comb.post) return cudaErrorInvalidValue;
   if (p.stages != 0 && (rb.vec * sizeof(float) != 16 || p.stages < 2 || p.stages > 3 ||
                         p.stage_ns < 1 || p.stage_ns > 2))
     return cudaErrorInvalidValue;

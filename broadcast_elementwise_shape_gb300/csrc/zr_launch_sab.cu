@@ -14,6 +14,9 @@ cudaError_t launch_sab_t(const SabBuild& sb, cudaStream_t s, bool dry) {
   if (!p.g || (kUses && (!p.a || !p.b)) || !p.ws_a || !p.ws_b || !sb.comb_a.out ||
       !sb.comb_b.out)
     return cudaErrorInvalidValue;
+  // Division stores grad_b's factors after its slots: only a plan sized for
+  // them may run.
+  if (OP == OP_DIV && !sb.comb_b.post) return cudaErrorInvalidValue;
   if (dry) return cudaSuccess;
   cudaError_t e = cudaFuncSetAttribute(k_sab<OP, RPT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        int(p.smem_bytes));

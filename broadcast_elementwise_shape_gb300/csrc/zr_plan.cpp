@@ -406,7 +406,8 @@ int build_ew(const Prob& P, const float* const in[3], float* const out[2], uint3
 
 int build_red(const Prob& P, int xslot, const float* g, const float* a, const float* b,
               uint32_t read_mask, uint32_t stream_mask, float* x_out, float* d_out,
-              int vec_override, int occ, int occ_cl_kept, int occ_cl_red, RedBuild* rb) {
+              int vec_override, int occ, int occ_cl_kept, int occ_cl_red, RedBuild* rb,
+              bool post) {
   RedPlan& p = rb->plan;
   p = RedPlan{};
   const int n = P.n;
@@ -591,7 +592,8 @@ int build_red(const Prob& P, int xslot, const float* g, const float* a, const fl
   const uint64_t ncta = n_kept * p.n_rblk * uint64_t(p.n_cblk);
   if (ncta >= (uint64_t(1) << 31)) return ZR_ERR_SIZE;
   p.n_cta = uint32_t(ncta);
-  rb->ws_bytes = p.nslots > 1 ? ((p.nslots * p.nout * sizeof(float) + 255) / 256) * 256 : 0;
+  const uint64_t ws_floats = uint64_t(p.nslots) * p.nout + (post ? p.nout : 0);
+  rb->ws_bytes = p.nslots > 1 ? ((ws_floats * sizeof(float) + 255) / 256) * 256 : 0;
 
   // cp.async staging when every streamed input (g, and a or b unless it is
   // the reduced gradient's own input, read once per thread) is read in
@@ -634,20 +636,21 @@ int build_red(const Prob& P, int xslot, const float* g, const float* a, const fl
   c.nslots = p.nslots;
   c.out = x_out;
   c.scale = 1.0f;
+  c.post = post && p.nslots > 1 ? 1u : 0u;
   combine_layout(&c);
   return ZR_OK;
 }
 
 int build_chain(const Prob& P, const float* g, const float* a, const float* b, const float* c,
                 bool c_scalar, float* grad_a, float* grad_b, float* grad_c, uint32_t stream_mask,
-                int vec_override, ChainBuild* cb) {
+                int vec_override, ChainBuild* cb, bool div1, bool div2) {
   *cb = ChainBuild{};
   // c is read with b's offsets (same shape, both dense), so it needs b's
   // 16-byte alignment; a single-element c is read as a scalar.
   if (!c_scalar && vec_override == 0 && reinterpret_cast<uintptr_t>(c) % 16 != 0) return 1;
   RedBuild rb;
   const int rc = build_red(P, kSlotXB, g, a, b, 7u, stream_mask & 7u, grad_b, grad_a,
-                           vec_override, kOccChain, 0, 0, &rb);
+                           vec_override, kOccChain, 0, 0, &rb, div1);
   if (rc) return rc;
   if (rb.vec != 4 || !rb.plan.inner_kept) return 1;
   ChainPlan& cp = cb->plan;
@@ -665,16 +668,23 @@ int build_chain(const Prob& P, const float* g, const float* a, const float* b, c
     cc.nslots = rb.plan.n_cta;
     cc.out = grad_c;
     cc.scale = 1.0f;
+    // Division by c: the per-CTA partials are followed by the factor -1/c^2.
+    cc.post = div2 && rb.plan.n_cta > 1 ? 1u : 0u;
     combine_layout(&cc);
-    cb->ws_c_bytes = rb.plan.n_cta > 1 ? ((uint64_t(rb.plan.n_cta) * 4 + 255) / 256) * 256 : 0;
+    cb->ws_c_bytes = rb.plan.n_cta > 1
+                         ? ((uint64_t(rb.plan.n_cta + (div2 ? 1 : 0)) * 4 + 255) / 256) * 256
+                         : 0;
   } else if (rb.plan.nslots > 1) {
-    // One second pass over [nslots][2 nout]: grad_b, then grad_c.
+    // One second pass over [nslots][2 nout]: grad_b, then grad_c; with a
+    // division in the chain, a row of per-output factors follows the slots.
     CombinePlan& c2 = cb->comb_b;
     c2.nout = 2 * rb.plan.nout;
     c2.split = rb.plan.nout;
     c2.out2 = grad_c;
+    c2.post = (div1 || div2) ? 1u : 0u;
     combine_layout(&c2);
-    cb->ws_b_bytes = ((uint64_t(rb.plan.nslots) * c2.nout * 4 + 255) / 256) * 256;
+    cb->ws_b_bytes =
+        ((uint64_t(rb.plan.nslots + c2.post) * c2.nout * 4 + 255) / 256) * 256;
   }
   return ZR_OK;
 }
@@ -820,7 +830,7 @@ void fill_from_specs(Decomp* dc, const DimSpec* dims, int nd) {
 }  // namespace
 
 int build_sab(const Prob& P, const float* g, const float* a, const float* b, float* grad_a,
-              float* grad_b, uint32_t read_mask, SabBuild* sb) {
+              float* grad_b, uint32_t read_mask, SabBuild* sb, bool post) {
   const int n = P.n;
   if (n < 2 || !grad_a || !grad_b) return 1;
   const int I = n - 1;
@@ -938,7 +948,8 @@ int build_sab(const Prob& P, const float* g, const float* a, const float* b, flo
   p.smem_bytes = uint32_t(smem);
   sb->rpt = int(rows_x_vec / kSabThreads);
   sb->ws_a_bytes = ((uint64_t(p.slots_a) * p.n_a * 4 + 255) / 256) * 256;
-  sb->ws_b_bytes = ((uint64_t(p.n_tiles) * p.n_b * 4 + 255) / 256) * 256;
+  // grad_b's region: its partial slots, then (post) one factor per output.
+  sb->ws_b_bytes = ((uint64_t(p.n_tiles + (post ? 1 : 0)) * p.n_b * 4 + 255) / 256) * 256;
   CombinePlan* cs[2] = {&sb->comb_a, &sb->comb_b};
   const uint64_t nouts[2] = {p.n_a, p.n_b};
   const uint32_t nsl[2] = {p.slots_a, p.n_tiles};
@@ -951,6 +962,7 @@ int build_sab(const Prob& P, const float* g, const float* a, const float* b, flo
     c.nslots = nsl[w];
     c.out = outs[w];
     c.scale = 1.0f;
+    c.post = (w == 1 && post) ? 1u : 0u;
     combine_layout(&c);
   }
   return ZR_OK;

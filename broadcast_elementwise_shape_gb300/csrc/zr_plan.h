@@ -95,9 +95,13 @@ struct RedBuild {
 // occ: resident CTAs per SM of the kernel that will run the plan;
 // occ_cl_kept / occ_cl_red: the same for the cluster variant with the inner
 // dim kept / reduced (0: no cluster plan).
+// post: X's total is multiplied by a per-output factor (division's -1/b^2
+// for grad_b); with partial slots the workspace also holds those factors,
+// one per output after the slots, and the second pass applies them.
 int build_red(const Prob& P, int xslot, const float* g, const float* a, const float* b,
               uint32_t read_mask, uint32_t stream_mask, float* x_out, float* d_out,
-              int vec_override, int occ, int occ_cl_kept, int occ_cl_red, RedBuild* rb);
+              int vec_override, int occ, int occ_cl_kept, int occ_cl_red, RedBuild* rb,
+              bool post = false);
 
 struct ChainBuild {
   ChainPlan plan;
@@ -108,9 +112,11 @@ struct ChainBuild {
 // index map).  Returns ZR_OK when the layout qualifies (16-byte vectors, b
 // reduced with its inner dim kept; c with b's dense layout, or one element),
 // 1 when it does not, or an error code.  vec_override as for build_red.
+// div1 / div2: op1 / op2 is a division, whose -1/b^2 (-1/c^2) factor the
+// second passes apply to each total (the workspace holds the factors).
 int build_chain(const Prob& P, const float* g, const float* a, const float* b, const float* c,
                 bool c_scalar, float* grad_a, float* grad_b, float* grad_c, uint32_t stream_mask,
-                int vec_override, ChainBuild* cb);
+                int vec_override, ChainBuild* cb, bool div1, bool div2);
 std::string describe_chain(const ChainBuild& cb);
 
 struct SabBuild {
@@ -121,9 +127,10 @@ struct SabBuild {
 };
 // Fused both-reduced plan; returns ZR_OK when the shape qualifies, 1 when it
 // does not (the caller then runs one reduction pass per gradient), or an
-// error code.
+// error code.  post: grad_b's totals carry a per-output factor (division),
+// stored after grad_b's slots and applied by its second pass.
 int build_sab(const Prob& P, const float* g, const float* a, const float* b, float* grad_a,
-              float* grad_b, uint32_t read_mask, SabBuild* sb);
+              float* grad_b, uint32_t read_mask, SabBuild* sb, bool post);
 
 // Split forward plan (SabFPlan); ZR_OK when the layout qualifies, 1 if not.
 // Slots of P: 0 = a, 1 = b, 3 = out.

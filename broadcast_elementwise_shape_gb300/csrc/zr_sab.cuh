@@ -154,8 +154,16 @@ k_sab(const __grid_constant__ SabPlan p) {
       const uint32_t step = static_cast<uint32_t>(s0) + k0 + r;
       const uint32_t tile = fd_div(p.n_beta_div, step);
       const uint32_t beta = step - tile * p.n_beta;
-      p.ws_b[uint64_t(tile) * p.n_b + uint64_t(beta) * p.ncol + col] =
-          __fmul_rn(v, sab_scale<OP>(rv));
+      const uint64_t jb = uint64_t(beta) * p.ncol + col;
+      if (OP == OP_DIV) {
+        // Unscaled partial; the tile-0 step (exactly one per beta) stores the
+        // factor -1/b^2 after the slots, and the second pass multiplies each
+        // total by it, so no partial can overflow on its own.
+        p.ws_b[uint64_t(tile) * p.n_b + jb] = v;
+        if (tile == 0) p.ws_b[uint64_t(p.n_tiles) * p.n_b + jb] = sab_scale<OP>(rv);
+      } else {
+        p.ws_b[uint64_t(tile) * p.n_b + jb] = __fmul_rn(v, sab_scale<OP>(rv));
+      }
     }
   };
 

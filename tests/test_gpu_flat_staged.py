@@ -186,3 +186,155 @@ def test_staged_reductions_bf16(L, op):
     for i, (gs, bs) in enumerate(STAGED):
         staged = _staged_case(L, op, gs, bs, torch.bfloat16, 5050 + 10 * i + OPS[op])
         assert staged, (op, gs, bs)
+
+
+def _special_dividends(gen, n):
+    x = torch.randn(n, generator=gen, dtype=torch.float32)
+    specials = torch.tensor([0.0, -0.0, float("inf"), -float("inf"), float("nan"), 1e-40, -3e-42,
+                             1.2e-38, -1.1754944e-38, 3.0e38, -3.4e38, 1.0, -2.5, 6e-39, 2.0 ** -149],
+                            dtype=torch.float32)
+    x[: specials.numel()] = specials
+    x[-specials.numel():] = specials
+    return x
+
+
+# One-element divisors: powers of two whose reciprocal is normal take one
+# multiplication by the exact reciprocal; the rest (2^127, a subnormal,
+# zeros, infinities, NaN, non-powers of two) the IEEE division.
+DIVISORS = [8.0, -0.25, 2.0 ** -126, 2.0 ** 126, 1.0, -1.0, 2.0 ** 127, 2.0 ** -127, 3.0, -0.0,
+            float("inf"), float("nan"), 0.1]
+
+
+@pytest.mark.parametrize("bf16", [False, True])
+def test_division_by_one_element_divisors_forward(L, bf16):
+    gen = torch.Generator().manual_seed(6060)
+    for shape in [(7, 1031), (96, 4096)]:  # a ragged tail; 16-byte vectors
+        a = _special_dividends(gen, int(np.prod(shape))).view(shape)
+        if bf16:
+            a = _bf(a)
+        for d in DIVISORS:
+            b = torch.tensor([d], dtype=torch.float32)
+            if bf16:
+                b = _bf(b)
+            dt = torch.bfloat16 if bf16 else torch.float32
+            got = zr.zr_binary_fwd("div", _to_dev(a, dt), _to_dev(b, dt))
+            torch.cuda.synchronize()
+            ref = oracle.binary_fwd("div", a, b)
+            if bf16:
+                ref = oracle.round_bf16(ref)
+            bitexact(got.float().cpu().numpy(), ref, f"x / {d!r} {shape} {'bf16' if bf16 else 'f32'}")
+
+
+@pytest.mark.parametrize("bf16", [False, True])
+def test_division_by_one_element_divisors_backward(L, bf16):
+    """grad_a = g / b is dense (bit-exact); grad_b = -sum(g * a) / b^2 is summed."""
+    gen = torch.Generator().manual_seed(7070)
+    dt = torch.bfloat16 if bf16 else torch.float32
+    for shape in [(7, 1031), (3, 700, 4096)]:  # register loads; a staged grid
+        n = int(np.prod(shape))
+        # Moderate values with signed zeros and subnormals (huge ones would
+        # overflow the binary32 sums that the binary64 oracle keeps finite).
+        g = torch.randn(n, generator=gen, dtype=torch.float32)
+        g[:6] = torch.tensor([0.0, -0.0, 1e-40, -3e-42, 1.2e-38, 2.0 ** -149])
+        g = g.view(shape)
+        a = torch.randn(shape, generator=gen, dtype=torch.float32)
+        if bf16:
+            g, a = _bf(g), _bf(a)
+        for d in [8.0, -0.25, 2.0 ** -60, 2.0 ** 60, 3.0, 2.0 ** 127]:
+            b = torch.tensor([d], dtype=torch.float32)
+            if bf16:
+                b = _bf(b)
+            ga, gb = zr.zr_binary_bwd("div", _to_dev(g, dt), _to_dev(a, dt), _to_dev(b, dt))
+            torch.cuda.synchronize()
+            ra, rb, sa, sb = oracle.binary_bwd("div", g, a, b)
+            what = f"g / {d!r} {shape} {'bf16' if bf16 else 'f32'}"
+            if bf16:
+                ra, rb = oracle.round_bf16(ra), oracle.round_bf16(rb)
+            bitexact(ga.float().cpu().numpy(), ra, what + " grad_a")
+            extra = (2.0 ** -7 / 1e-5) * np.abs(np.asarray(rb, np.float64)) if bf16 else 0.0
+            within(gb.float().cpu().numpy(), rb, sb + extra, what + " grad_b")
+
+
+def _halves(shape, axis, big=1000.0):
+    """+big in the first half along `axis`, -big in the second: every sum
+    over that axis cancels exactly to 0 while each half alone is large."""
+    g = torch.full(shape, big, dtype=torch.float32)
+    idx = [slice(None)] * len(shape)
+    idx[axis] = slice(shape[axis] // 2, None)
+    g[tuple(idx)] = -big
+    return g
+
+
+def _chain_plan(L, op1, op2, g, a, b, c, grads):
+    L.zr_test_describe_chain_bwd.argtypes = [ctypes.c_int, ctypes.c_int, zr.ZrTensor, zr.ZrTensor,
+                                             zr.ZrTensor, zr.ZrTensor, ctypes.c_void_p,
+                                             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_char_p,
+                                             ctypes.c_size_t]
+    keep = [zr._desc(x) for x in (g, a, b, c)]
+    buf = ctypes.create_string_buffer(8192)
+    rc = L.zr_test_describe_chain_bwd(OPS[op1], OPS[op2], *[k[0] for k in keep],
+                                      *[x.data_ptr() for x in grads], buf, len(buf))
+    assert rc == 0, L.zr_status_string(rc)
+    return json.loads(buf.value)
+
+
+def test_division_factor_applies_to_each_total(L):
+    """Division's summed gradient is -sum(g * a) / b^2: the factor 1/b^2
+    multiplies the whole sum once.  With b = 2^-60 and sums whose halves are
+    large and cancel exactly, the factor times any partial sum overflows
+    binary32 while the true gradient is 0; every route with partial sums
+    must still give 0 (the oracle's binary64 value), not inf - inf = NaN."""
+    tiny = 2.0 ** -60
+    # Reductions with partial slots: inner dim kept, and reduced.
+    for gshape, bshape, axis in [((4096, 1024), (1024,), 0), ((3, 700, 4096), (1, 700, 1), 0)]:
+        g = _halves(gshape, axis)
+        if gshape[0] == 3:
+            g[2] = 0.0
+        a = torch.ones(gshape)
+        b = torch.full(bshape, tiny)
+        dg, da, db = _to_dev(g), _to_dev(a), _to_dev(b)
+        ga = torch.empty(gshape, device="cuda")
+        gb = torch.empty(bshape, device="cuda")
+        plan = _bwd_plan(L, "div", dg, da, db, ga, gb)
+        assert plan["plans"][0]["nslots"] > 1, plan
+        zr.zr_binary_bwd("div", dg, da, db, grad_a=ga, grad_b=gb)
+        torch.cuda.synchronize()
+        ra, rb, sa, sb = oracle.binary_bwd("div", g, a, b)
+        bitexact(ga.cpu().numpy(), ra, f"div {gshape} grad_a")
+        within(gb.cpu().numpy(), rb, sb, f"div {gshape} grad_b")
+        assert np.all(rb == 0.0) and np.all(gb.cpu().numpy() == 0.0)
+    # Both gradients reduced (the two-gradient pass): grad_b's slots are
+    # a's outer tiles, so halves along a's outermost dim cancel.
+    sa_, sb_ = (2, 1, 4, 1, 8, 1, 16, 32), (1, 3, 1, 5, 1, 6, 1, 32)
+    gshape = tuple(np.broadcast_shapes(sa_, sb_))
+    g, a, b = _halves(gshape, 0), torch.ones(sa_), torch.full(sb_, tiny)
+    dg, da, db = _to_dev(g), _to_dev(a), _to_dev(b)
+    ga, gb = torch.empty(sa_, device="cuda"), torch.empty(sb_, device="cuda")
+    assert _bwd_plan(L, "div", dg, da, db, ga, gb)["plans"][0]["kernel"] == "sab"
+    zr.zr_binary_bwd("div", dg, da, db, grad_a=ga, grad_b=gb)
+    torch.cuda.synchronize()
+    ra, rb, sa, sb = oracle.binary_bwd("div", g, a, b)
+    within(ga.cpu().numpy(), ra, sa, "sab div grad_a")
+    within(gb.cpu().numpy(), rb, sb, "sab div grad_b")
+    assert np.all(rb == 0.0) and np.all(gb.cpu().numpy() == 0.0)
+    # Fused chains: (a + b) / c with c one element (per-CTA partials), and
+    # (a * b) / c with c shaped like b (slot rows of grad_b and grad_c).
+    R, C = 4096, 1024
+    for op1, cshape in [("add", (1,)), ("mul", (C,))]:
+        g = _halves((R, C), 0)
+        a = torch.ones((R, C))
+        b = torch.zeros((C,)) if op1 == "add" else torch.ones((C,))
+        c = torch.full(cshape, tiny)
+        dg, da, db, dc = _to_dev(g), _to_dev(a), _to_dev(b), _to_dev(c)
+        grads = [torch.empty((R, C), device="cuda"), torch.empty((C,), device="cuda"),
+                 torch.empty(cshape, device="cuda")]
+        plan = _chain_plan(L, op1, "div", dg, da, db, dc, grads)
+        assert plan["route"] == "fused", plan
+        zr.zr_chain_bwd(op1, "div", dg, da, db, dc, grads=tuple(grads))
+        torch.cuda.synchronize()
+        refs = oracle.chain_bwd(op1, "div", g, a, b, c)
+        what = f"chain ({op1}, div) c {cshape}"
+        bitexact(grads[0].cpu().numpy(), refs[0], what + " grad_a")
+        for k in (1, 2):
+            within(grads[k].cpu().numpy(), refs[k], refs[k + 3], what + f" grad_{'abc'[k]}")
+            assert np.all(grads[k].cpu().numpy() == 0.0), what
