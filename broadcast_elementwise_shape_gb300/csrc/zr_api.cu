@@ -513,8 +513,8 @@ std::string sum_json(const SumSet& S) {
   return "{\"plans\":[" + describe_red(S.rb) + "],\"ws_query\":" + std::to_string(S.ws_query) + "}";
 }
 
-// ZR_TRACE set (and not "0"): every forward, backward and sum-to-shape call
-// that is about to launch writes one line "zr_trace <entry> <plan JSON>" to
+// ZR_TRACE set (and not "0"): every forward, backward, sum-to-shape and
+// unary call that is about to launch writes one line "zr_trace <entry> <plan JSON>" to
 // stderr.  Read once per process.
 bool trace_on() {
   static const bool on = [] {
@@ -865,6 +865,7 @@ int zr_test_occupancy(int which, int* planned, int* actual) {
   else if (which >= 22 && which < 24) e = occupancy_ew(which - 16, planned, actual);
   else if (which == 24) e = occupancy_bf16(0, planned, actual);
   else if (which == 25) e = occupancy_red(10, planned, actual);
+  else if (which >= 26 && which < 28) e = occupancy_bf16(which - 25, planned, actual);
   else return ZR_ERR_SIZE;
   return cuda_status(e);
 }
@@ -1843,6 +1844,15 @@ int plan_unary(int uop, float alpha, const zr_tensor& t0, const zr_tensor* t1, f
   rc = build_ew(P, in, outs, rmask, rmask, kOccEwFwd, &S->eb);
   if (rc) return rc;
   S->eb.plan.alpha = alpha;
+  // bfloat16 GeLU over a flat layout large enough to amortise the table:
+  // one CTA per SM (fewer if there are fewer passes of the kernel's loads).
+  EwPlan& ep = S->eb.plan;
+  if (uop == UN_GELU && S->es == 2 && ep.flat &&
+      uint64_t(ep.nitems) * uint64_t(S->eb.vec) >= kGeluTabMinElems) {
+    const uint64_t pass = uint64_t(two ? kGeluTabUnrollBwd : kGeluTabUnrollFwd) * kGeluTabThreads;
+    S->eb.gelu_tab = true;
+    ep.n_cta = uint32_t(std::min<uint64_t>(kSms, (uint64_t(ep.nitems) + pass - 1) / pass));
+  }
   return ZR_OK;
 }
 
@@ -1864,6 +1874,7 @@ int zr_unary_fwd_t(zr_dtype dtype, zr_unary op, float alpha, zr_tensor x, void* 
   S.es = dtype == ZR_BF16 ? 2 : 4;
   int rc = plan_unary(op, alpha, x, nullptr, out, out_strides, &S);
   if (rc || S.empty) return rc;
+  if (trace_on()) trace("zr_unary_fwd", describe_ew(S.eb));
   for (const void* p : {static_cast<const void*>(S.g.ptr), static_cast<const void*>(out)}) {
     rc = check_device_ptr(p);
     if (rc) return rc;
@@ -1886,6 +1897,7 @@ int zr_unary_bwd_t(zr_dtype dtype, zr_unary op, float alpha, zr_tensor grad_out,
   int rc = plan_unary(op, alpha, grad_out, op == UN_GELU ? &x : nullptr, grad_x, grad_x_strides,
                       &S);
   if (rc || S.empty) return rc;
+  if (trace_on()) trace("zr_unary_bwd", describe_ew(S.eb));
   if (op != UN_GELU) {
     if (x.ndim != grad_out.ndim || (x.ndim > 0 && !x.sizes)) return ZR_ERR_SHAPE;
     for (int d = 0; d < x.ndim; ++d)
@@ -1899,6 +1911,17 @@ int zr_unary_bwd_t(zr_dtype dtype, zr_unary op, float alpha, zr_tensor grad_out,
     if (rc) return rc;
   }
   return cuda_status(launch_unary_bwd(op, S.eb, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int zr_test_describe_unary_t(zr_dtype dtype, zr_unary op, zr_tensor in0, const zr_tensor* x,
+                             const void* out, const int64_t* out_strides, char* buf, size_t len) {
+  if (dtype != ZR_F32 && dtype != ZR_BF16) return ZR_ERR_DTYPE;
+  UnarySet S;
+  S.es = dtype == ZR_BF16 ? 2 : 4;
+  const int rc = plan_unary(op, 1.f, in0, x, static_cast<float*>(const_cast<void*>(out)),
+                            out_strides, &S);
+  if (rc) return rc;
+  return copy_json(S.empty ? std::string("{\"kernel\":\"none\"}") : describe_ew(S.eb), buf, len);
 }
 
 }  // extern "C"

@@ -155,6 +155,15 @@ constexpr int kOccEwBwd = 3;      // k_elementwise: backward without reduction
 constexpr int kOccEwCopy = 5;     // k_elementwise: copy (sum-to-shape onto the same shape)
 constexpr int kOccGeluFwd = 5;     // GeLU forward, float
 constexpr int kOccGeluFwdWide = 6; // GeLU forward, 8-wide bfloat16 (2 items per batch)
+// GeLU on bfloat16 storage by table (k_gelu_bf16): one CTA of 1024 threads
+// per SM, items per pass 3 (forward) or 2 (backward, two operands) with the
+// next pass's loads in flight (the most that fit in 64 registers without
+// spilling), taken for flat plans of at least 65,536 elements per SM, where
+// each CTA's fill of its tables is small beside its share of the stream.
+constexpr int kGeluTabThreads = 1024;
+constexpr int kGeluTabUnrollFwd = 3;
+constexpr int kGeluTabUnrollBwd = 2;
+constexpr uint64_t kGeluTabMinElems = uint64_t(kSms) << 16;
 constexpr int kOccRedAddSub = 4;  // k_reduce: add, sub, sum-to-shape
 constexpr int kOccRedMulDiv = 3;  // k_reduce: mul, div
 // k_reduce, cluster variant (no second pass): loads per item are 1 for add,

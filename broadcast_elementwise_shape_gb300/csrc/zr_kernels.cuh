@@ -888,6 +888,213 @@ cudaError_t launch_ew_kernel(const EwPlan& p, cudaStream_t s) {
   return launch_k(k_elementwise<F, VEC, NOUT, E>, p.n_cta, kThreads, smem, s, p);
 }
 
+// ------------------------------------------------ bfloat16 GeLU by table
+//
+// A bfloat16 operand takes at most 2^16 values.  On 2^-24 <= |x| < 2^8 (32
+// binades of 128 values for each sign: 8192 values) GeLU on bfloat16
+// storage reads its result from a table in shared memory instead of
+// evaluating erfc per element: the forward's bfloat16 result, or the
+// backward's derivative Phi(x) + x phi(x) in binary32, which the kernel
+// multiplies by g (the product the arithmetic path rounds).  Each CTA fills
+// the table with the functors themselves (the backward's with g = 1, an
+// exact product), so every result is bit for bit the arithmetic path's.
+// Elements outside the range (|x| < 2^-24, |x| >= 256, infinities, NaN) are
+// evaluated again through the functors, in a branch taken only by warps
+// that hold one.  One CTA of 1024 threads per SM, each taking an equal
+// contiguous run of the items; the loads of the next pass are issued before
+// the lookups of the current one.
+//
+// Table slot of a bfloat16 pattern b: t = (b - pattern of 2^-24) mod 2^16 is
+// in [0, 4096) for 2^-24 <= x < 256 and in [32768, 36864) for their
+// negatives; the slot is t & 0x8FFF, one mask.  Slots [4096, 32768) are
+// never filled: a pattern outside the range reads one of them, or a filled
+// slot, and is replaced.
+constexpr uint32_t kGeluTabLo = (127u - 24u) << 7;  // bfloat16 pattern of 2^-24
+constexpr uint32_t kGeluTabSlots = 0x9000u;
+template <bool BWD>
+struct GeluTab {
+  static constexpr size_t kSmemBytes = size_t(kGeluTabSlots) * (BWD ? 4 : 2);
+};
+__device__ __forceinline__ uint32_t gelu_tab_t(uint32_t bits) { return (bits - kGeluTabLo) & 0xFFFFu; }
+__device__ __forceinline__ bool gelu_tab_in(uint32_t t) { return (t & 0x7000u) == 0; }
+// The k-th of the 8192 filled slots, and the value it holds the result for.
+__device__ __forceinline__ uint32_t gelu_nth_slot(uint32_t k) {
+  return k < 4096u ? k : k - 4096u + 0x8000u;
+}
+__device__ __forceinline__ float gelu_slot_value(uint32_t slot) {
+  return __uint_as_float(((slot + kGeluTabLo) & 0xFFFFu) << 16);
+}
+
+// Elements outside the table, one at a time through the functors.
+__device__ __forceinline__ uint32_t gelu_fwd_bf16_slow(uint32_t bits) {
+  Vec<1> x[3], y[2];
+  x[0].v[0] = __uint_as_float(bits << 16);
+  UnaryF<UN_GELU, true>{}(x, y, 0.f);
+  return __bfloat16_as_ushort(__float2bfloat16_rn(y[0].v[0]));
+}
+__device__ __forceinline__ float gelu_bwd_bf16_slow(float g, uint32_t bits) {
+  Vec<1> x[3], y[2];
+  x[0].v[0] = g;
+  x[1].v[0] = __uint_as_float(bits << 16);
+  UnaryBwdF<UN_GELU, true>{}(x, y, 0.f);
+  return y[0].v[0];
+}
+
+template <bool BWD>
+__device__ __forceinline__ void gelu_fill(uint32_t* tab) {
+  for (uint32_t k = threadIdx.x; k < 4096u; k += kGeluTabThreads) {
+    const uint32_t s = gelu_nth_slot(2 * k);  // slots s, s + 1
+    Vec<2> x[3], y[2];
+    if constexpr (BWD) {
+      x[0].v[0] = x[0].v[1] = 1.f;
+      x[1].v[0] = gelu_slot_value(s);
+      x[1].v[1] = gelu_slot_value(s + 1);
+      UnaryBwdF<UN_GELU, true>{}(x, y, 0.f);
+      *reinterpret_cast<uint2*>(tab + s) = make_uint2(__float_as_uint(y[0].v[0]), __float_as_uint(y[0].v[1]));
+    } else {
+      x[0].v[0] = gelu_slot_value(s);
+      x[0].v[1] = gelu_slot_value(s + 1);
+      UnaryF<UN_GELU, true>{}(x, y, 0.f);
+      tab[s / 2] = pack_bf16x2(y[0].v[0], y[0].v[1]);
+    }
+  }
+}
+
+template <int VEC>
+__device__ __forceinline__ uint32_t raw_bits(const Raw<__nv_bfloat16, VEC>& r, int i) {
+  return (i & 1) ? r.w[i / 2] >> 16 : r.w[i / 2] & 0xFFFFu;
+}
+
+// The results of one item: forward bfloat16 patterns, backward values.
+template <int VEC>
+__device__ __forceinline__ void gelu_item_fwd(const uint32_t* tab, const Raw<__nv_bfloat16, VEC>& xr,
+                                              uint32_t (&w)[(VEC + 1) / 2]) {
+  const unsigned short* th = reinterpret_cast<const unsigned short*>(tab);
+  uint32_t bad = 0;
+#pragma unroll
+  for (int i = 0; i < VEC; ++i) {
+    const uint32_t t = gelu_tab_t(raw_bits<VEC>(xr, i));
+    bad |= t & 0x7000u;
+    const uint32_t r = th[t & 0x8FFFu];
+    if (i & 1) w[i / 2] |= r << 16;
+    else w[i / 2] = r;
+  }
+  if (__any_sync(0xffffffffu, bad != 0)) {
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) {
+      const uint32_t bits = raw_bits<VEC>(xr, i);
+      if (!gelu_tab_in(gelu_tab_t(bits))) {
+        const uint32_t r = gelu_fwd_bf16_slow(bits);
+        w[i / 2] = (i & 1) ? (w[i / 2] & 0xFFFFu) | (r << 16) : (w[i / 2] & 0xFFFF0000u) | r;
+      }
+    }
+  }
+}
+template <int VEC>
+__device__ __forceinline__ void gelu_item_bwd(const uint32_t* gsm, const Raw<__nv_bfloat16, VEC>& xr,
+                                              const Raw<__nv_bfloat16, VEC>& gr, Vec<VEC>& y) {
+  const float* tf = reinterpret_cast<const float*>(gsm);
+  uint32_t bad = 0;
+#pragma unroll
+  for (int i = 0; i < VEC; ++i) {
+    const uint32_t t = gelu_tab_t(raw_bits<VEC>(xr, i));
+    bad |= t & 0x7000u;
+    y.v[i] = __fmul_rn(__uint_as_float(raw_bits<VEC>(gr, i) << 16), tf[t & 0x8FFFu]);
+  }
+  if (__any_sync(0xffffffffu, bad != 0)) {
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) {
+      const uint32_t bits = raw_bits<VEC>(xr, i);
+      if (!gelu_tab_in(gelu_tab_t(bits)))
+        y.v[i] = gelu_bwd_bf16_slow(__uint_as_float(raw_bits<VEC>(gr, i) << 16), bits);
+    }
+  }
+}
+
+// Store VEC bfloat16 patterns, two per word, as store_cols stores values.
+template <int VEC>
+__device__ __forceinline__ void store_raw_bf16(__nv_bfloat16* base, int64_t row_off, int64_t inner,
+                                               uint32_t c, const uint32_t (&w)[(VEC + 1) / 2]) {
+  unsigned short* b = reinterpret_cast<unsigned short*>(base) + row_off;
+  if (inner == 1) {
+    if constexpr (VEC == 8) {
+      *reinterpret_cast<uint4*>(b + c) = make_uint4(w[0], w[1], w[2], w[3]);
+    } else if constexpr (VEC == 4) {
+      *reinterpret_cast<uint2*>(b + c) = make_uint2(w[0], w[1]);
+    } else {
+      static_assert(VEC == 1, "vector width");
+      b[c] = static_cast<unsigned short>(w[0]);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < VEC; ++i)
+      b[int64_t(c + i) * inner] = static_cast<unsigned short>((i & 1) ? w[i / 2] >> 16 : w[i / 2]);
+  }
+}
+
+// in0: x (forward) or g (backward), in1: x (backward); a flat plan; dynamic
+// shared memory GeluTab<BWD>::kSmemBytes.  U items per pass.
+template <bool BWD, int VEC>
+__global__ void __launch_bounds__(kGeluTabThreads, 1)
+k_gelu_bf16(const __grid_constant__ EwPlan p) {
+  using E = __nv_bfloat16;
+  extern __shared__ __align__(16) uint32_t gsm[];
+  constexpr int U = BWD ? kGeluTabUnrollBwd : kGeluTabUnrollFwd;
+  constexpr uint32_t kStep = U * kGeluTabThreads;
+  pdl_trigger();
+  const uint32_t first = uint32_t(uint64_t(p.nitems) * blockIdx.x / gridDim.x);
+  const uint32_t end = uint32_t(uint64_t(p.nitems) * (blockIdx.x + 1) / gridDim.x);
+  const int xs = BWD ? 1 : 0;
+  const E* xin = reinterpret_cast<const E*>(p.in[xs]);
+  const E* gin = reinterpret_cast<const E*>(p.in[0]);
+  E* out = reinterpret_cast<E*>(p.out[0]);
+  struct Pass {
+    Raw<E, VEC> xr[U], gr[U];
+  };
+  auto load = [&](uint32_t it0, Pass& q) {
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const uint32_t item = it0 + u * kGeluTabThreads + threadIdx.x;
+      if (item < end) {
+        const uint32_t row = fd_div(p.nvcol_div, item);
+        const uint32_t col = (item - row * p.nvcol) * VEC;
+        q.xr[u] = load_raw<VEC>(xin, int64_t(row) * p.rows.stride[xs][0], p.inner_stride[xs], col,
+                                p.stream_mask & (1u << xs));
+        if (BWD)
+          q.gr[u] = load_raw<VEC>(gin, int64_t(row) * p.rows.stride[0][0], p.inner_stride[0], col,
+                                  p.stream_mask & 1);
+      }
+    }
+  };
+  pdl_wait();
+  // The first pass's loads are in flight while the table is filled.
+  Pass cur, nxt;
+  load(first, cur);
+  gelu_fill<BWD>(gsm);
+  __syncthreads();
+  for (uint32_t it0 = first; it0 < end; it0 += kStep) {
+    if (it0 + kStep < end) load(it0 + kStep, nxt);
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const uint32_t item = it0 + u * kGeluTabThreads + threadIdx.x;
+      if (item >= end) continue;
+      const uint32_t row = fd_div(p.nvcol_div, item);
+      const uint32_t col = (item - row * p.nvcol) * VEC;
+      const int64_t doff = int64_t(row) * p.rows.stride[kSlotOut][0];
+      if constexpr (BWD) {
+        Vec<VEC> y;
+        gelu_item_bwd<VEC>(gsm, cur.xr[u], cur.gr[u], y);
+        store_cols<VEC>(out, doff, p.inner_stride[kSlotOut], col, y);
+      } else {
+        uint32_t w[(VEC + 1) / 2];
+        gelu_item_fwd<VEC>(gsm, cur.xr[u], w);
+        store_raw_bf16<VEC>(out, doff, p.inner_stride[kSlotOut], col, w);
+      }
+    }
+    cur = nxt;
+  }
+}
+
 // Forward with a transposed input (TrPlan): x has unit stride along p, the
 // output along q.  A CTA covers kTrP p x kTrTile q; warp w its p rows
 // [16w, 16w + 16), lane (pc = lane & 3, qq = lane >> 2) a 4 x 4 block at

@@ -24,6 +24,20 @@ cudaError_t launch_ew_bf16(const EwBuild& eb, cudaStream_t s, bool dry) {
   return launch_ew_kernel<F, 1, NOUT, bf16>(eb.plan, s);
 }
 
+// GeLU by table: a flat plan, grid (at most one CTA per SM) in plan.n_cta.
+template <bool BWD>
+cudaError_t gelu_table_bf16(const EwBuild& eb, cudaStream_t s, bool dry) {
+  const EwPlan& p = eb.plan;
+  if (!p.flat || !p.in[0] || (BWD && !p.in[1]) || !p.out[0] || p.n_cta == 0 || p.n_cta > kSms)
+    return cudaErrorInvalidValue;
+  if (dry) return cudaSuccess;
+  constexpr size_t smem = GeluTab<BWD>::kSmemBytes;
+  auto kern = eb.vec == 8 ? k_gelu_bf16<BWD, 8> : eb.vec == 4 ? k_gelu_bf16<BWD, 4> : k_gelu_bf16<BWD, 1>;
+  kern = with_smem(kern, smem);
+  if (!kern) return cudaErrorInvalidValue;
+  return launch_k(kern, p.n_cta, kGeluTabThreads, smem, s, p);
+}
+
 template <int OP>
 cudaError_t direct_bf16(int want, const EwBuild& eb, cudaStream_t s, bool dry) {
   switch (want) {
@@ -91,11 +105,13 @@ cudaError_t launch_fwd_bf16(int op, const EwBuild& eb, cudaStream_t s, bool dry)
 }
 
 cudaError_t launch_unary_fwd_bf16(int uop, const EwBuild& eb, cudaStream_t s, bool dry) {
+  if (uop == UN_GELU && eb.gelu_tab) return gelu_table_bf16<false>(eb, s, dry);
   return uop == UN_SCALE ? launch_ew_bf16<UnaryF<UN_SCALE>, 1>(eb, s, dry)
                          : launch_ew_bf16<UnaryF<UN_GELU, true>, 1>(eb, s, dry);
 }
 
 cudaError_t launch_unary_bwd_bf16(int uop, const EwBuild& eb, cudaStream_t s, bool dry) {
+  if (uop == UN_GELU && eb.gelu_tab) return gelu_table_bf16<true>(eb, s, dry);
   return uop == UN_SCALE ? launch_ew_bf16<UnaryBwdF<UN_SCALE>, 1>(eb, s, dry)
                          : launch_ew_bf16<UnaryBwdF<UN_GELU, true>, 1>(eb, s, dry);
 }
@@ -115,6 +131,15 @@ cudaError_t occupancy_bf16(int which, int* planned, int* actual) {
       *planned = kOccGeluFwdWide;
       return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
           actual, k_flat<UnaryF<UN_GELU, true>, 8, 1, bf16>, kThreads, 0);
+    case 1:  // GeLU by table, forward and backward, 8-wide: one CTA per SM
+    case 2: {
+      *planned = 1;
+      const bool bwd = which == 2;
+      const size_t smem = bwd ? GeluTab<true>::kSmemBytes : GeluTab<false>::kSmemBytes;
+      auto kern = with_smem(bwd ? k_gelu_bf16<true, 8> : k_gelu_bf16<false, 8>, smem);
+      if (!kern) return cudaErrorInvalidValue;
+      return cudaOccupancyMaxActiveBlocksPerMultiprocessor(actual, kern, kGeluTabThreads, smem);
+    }
     default: return cudaErrorInvalidValue;
   }
 }

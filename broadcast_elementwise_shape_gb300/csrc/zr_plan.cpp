@@ -779,7 +779,7 @@ std::string describe_ew(const EwBuild& eb) {
                 "{\"kernel\":\"%s\",\"vec\":%d,\"nrow\":%u,\"ncol\":%u,\"row_dims\":%d,"
                 "\"inner_stride\":[%lld,%lld,%lld,%lld],\"tile_rows\":%u,\"tile_vcols\":%u,"
                 "\"items_per_cta\":%u,\"ctas\":%u,\"stream_mask\":%u}",
-                p.flat ? "flat" : "elementwise", eb.vec, p.nrow, p.ncol, p.rows.n,
+                eb.gelu_tab ? "gelu_table" : p.flat ? "flat" : "elementwise", eb.vec, p.nrow, p.ncol, p.rows.n,
                 (long long)p.inner_stride[0], (long long)p.inner_stride[1],
                 (long long)p.inner_stride[2], (long long)p.inner_stride[3], p.tile_rows,
                 p.tile_vcols, p.items_per_cta, p.n_cta, p.stream_mask);

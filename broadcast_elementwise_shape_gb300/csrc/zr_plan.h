@@ -60,6 +60,7 @@ struct EwBuild {
   int vec;
   int es;             // bytes per stored element (Prob::es)
   bool uni1 = false;  // input slot 1 is one element (a forward's b with numel 1)
+  bool gelu_tab = false;  // bfloat16 GeLU by table (k_gelu_bf16, grid in plan.n_cta)
 };
 // Elementwise plan over P with input slots 0..2 and output slot 3.
 // occ: resident CTAs per SM of the kernel that will run the plan.

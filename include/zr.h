@@ -46,8 +46,9 @@
  * The caller owns the memory and the stream.
  *
  * Tracing.  With the environment variable ZR_TRACE set (and not "0") when
- * the library is first used, every zr_binary_fwd, zr_binary_bwd and
- * zr_sum_to_shape call (and their _t forms) that passes planning writes one
+ * the library is first used, every zr_binary_fwd, zr_binary_bwd,
+ * zr_binary_bwd_noalloc, zr_sum_to_shape, zr_unary_fwd and zr_unary_bwd call
+ * (and their _t forms) that passes planning writes one
  * line "zr_trace <entry point> <plan as JSON>" to stderr before its device
  * checks and launches: the kernels, vector width, tiling, grid and
  * workspace it chose.

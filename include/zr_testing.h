@@ -30,6 +30,14 @@ int zr_test_describe_bwd_t(zr_dtype dtype, zr_op op, zr_tensor grad_out, zr_tens
 int zr_test_describe_sum(zr_tensor in, int32_t ndim_out, const int64_t* sizes_out,
                          const float* out, char* buf, size_t len);
 
+/* The same for zr_unary_fwd_t (x == NULL: in0 is x) and zr_unary_bwd_t
+ * (in0 is grad_out, x is x) on `dtype` storage: "kernel" is "gelu_table" for
+ * bfloat16 GeLU read from its table (k_gelu_bf16), else "flat" or
+ * "elementwise".  `out` is the output (grad_x) with strides out_strides
+ * (NULL: contiguous). */
+int zr_test_describe_unary_t(zr_dtype dtype, zr_unary op, zr_tensor in0, const zr_tensor* x,
+                             const void* out, const int64_t* out_strides, char* buf, size_t len);
+
 /* JSON description of the route zr_chain_bwd would take ("fused" with its
  * plan, or "composed"), with its workspace sizes. */
 int zr_test_describe_chain_bwd(zr_op op1, zr_op op2, zr_tensor grad_out, zr_tensor a,
@@ -51,7 +59,7 @@ int zr_test_dry_run_bwd(zr_op op, zr_tensor grad_out, zr_tensor a, zr_tensor b,
 int zr_test_dry_run_sum(zr_tensor in, int32_t ndim_out, const int64_t* sizes_out,
                         const float* out);
 
-/* Resident CTAs per SM of kernel `which` (0..25: elementwise forward add,
+/* Resident CTAs per SM of kernel `which` (0..27: elementwise forward add,
  * forward div, backward div, copy; reduction add inner-kept, sub
  * inner-reduced, mul inner-kept, div inner-reduced, sum-to-shape; split
  * forward; transpose; then the five reductions again in their cluster
@@ -59,7 +67,7 @@ int zr_test_dry_run_sum(zr_tensor in, int32_t ndim_out, const int64_t* sizes_out
  * same with c one element, chain forward with c one element; GeLU forward,
  * GeLU backward; flat forward add, flat GeLU forward, flat bfloat16 GeLU
  * forward; reduction add inner-kept with a three-batch staging ring in
- * shared memory) as the planner sizes grids for (*planned) and as the
+ * shared memory; bfloat16 GeLU forward and backward by table) as the planner sizes grids for (*planned) and as the
  * CUDA runtime reports for the current device (*actual).  Needs a device:
  * ZR_ERR_CUDA without one; ZR_ERR_SIZE for an unknown `which`. */
 int zr_test_occupancy(int which, int* planned, int* actual);

@@ -781,3 +781,49 @@ def test_emulated_eight_dim_plans_match_naive(L):
             x = rp[order, 4]
             if x[0] != -1:
                 assert np.array_equal(x, xa[ref]) or np.array_equal(x, xb[ref])
+
+
+def test_describe_unary_routes_bf16_gelu_to_its_table(L):
+    """bfloat16 GeLU over a flat layout of at least 65,536 elements per SM
+    (152 SMs) reads its results from a table (k_gelu_bf16, one CTA per SM,
+    fewer when there are fewer passes of 1024 threads); smaller calls, float
+    GeLU, scale and non-flat layouts keep the arithmetic kernels."""
+    L.zr_test_describe_unary_t.argtypes = [ctypes.c_int, ctypes.c_int, ZrTensor,
+                                           ctypes.c_void_p, ctypes.c_void_p,
+                                           ctypes.c_void_p, ctypes.c_char_p, ctypes.c_size_t]
+    T = 1 << 40
+
+    def desc(dtype, op, shape, strides=None, bwd=False, out_strides=None):
+        x = FakeT(T, shape, strides)
+        g = FakeT(2 * T, shape, strides)
+        ost = _i64(out_strides) if out_strides is not None else None
+        buf = ctypes.create_string_buffer(4096)
+        if bwd:
+            rc = L.zr_test_describe_unary_t(dtype, op, g.desc, ctypes.addressof(x.desc), 3 * T,
+                                            ctypes.cast(ost, ctypes.c_void_p) if ost else None,
+                                            buf, 4096)
+        else:
+            rc = L.zr_test_describe_unary_t(dtype, op, x.desc, None, 3 * T,
+                                            ctypes.cast(ost, ctypes.c_void_p) if ost else None,
+                                            buf, 4096)
+        assert rc == 0, rc
+        return json.loads(buf.value.decode())
+
+    BF16, F32, SCALE, GELU = 1, 0, 0, 1
+    for bwd in (False, True):
+        d = desc(BF16, GELU, (16384, 3072), bwd=bwd)  # a [16384, 3072] activation
+        assert d["kernel"] == "gelu_table" and d["vec"] == 8 and d["ctas"] == 152, d
+        assert desc(F32, GELU, (16384, 3072), bwd=bwd)["kernel"] == "flat"
+        assert desc(BF16, SCALE, (16384, 3072), bwd=bwd)["kernel"] == "flat"
+        # Just below and at the size limit.
+        assert desc(BF16, GELU, (152 * 65536 - 8,), bwd=bwd)["kernel"] == "flat"
+        assert desc(BF16, GELU, (152 * 65536,), bwd=bwd)["kernel"] == "gelu_table"
+    # Odd sizes take 1-element items, row-strided views rows of 8.
+    d = desc(BF16, GELU, (152 * 65536 + 1,))
+    assert d["kernel"] == "gelu_table" and d["vec"] == 1 and d["ctas"] == 152
+    d = desc(BF16, GELU, (2048, 8192), strides=(8200, 1))
+    assert d["kernel"] == "gelu_table" and d["vec"] == 8 and d["row_dims"] == 1
+    # A layout that does not flatten to two dims keeps the tiled kernel.
+    d = desc(BF16, GELU, (64, 64, 4096), strides=(64 * 4104, 4104, 1),
+             out_strides=(64 * 4096 + 8, 4096, 1))
+    assert d["kernel"] == "elementwise"

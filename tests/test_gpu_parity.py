@@ -349,11 +349,11 @@ def test_planner_occupancy_matches_runtime():
     L = zr.lib()
     L.zr_test_occupancy.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_int),
                                     ctypes.POINTER(ctypes.c_int)]
-    for which in range(26):
+    for which in range(28):
         planned, actual = ctypes.c_int(0), ctypes.c_int(0)
         assert L.zr_test_occupancy(which, ctypes.byref(planned), ctypes.byref(actual)) == 0
         assert planned.value == actual.value, (which, planned.value, actual.value)
-    assert L.zr_test_occupancy(26, ctypes.byref(planned), ctypes.byref(actual)) == -4
+    assert L.zr_test_occupancy(28, ctypes.byref(planned), ctypes.byref(actual)) == -4
 
 
 def test_strided_output_and_in_place():
