@@ -503,6 +503,12 @@ int build_red(const Prob& P, int xslot, const float* g, const float* a, const fl
     }
     tx = best_tx;
     rows = ceil_div(n_red, best_n);
+    // 8-wide vectors with every reduced row in one block: 64 column lanes
+    // (4 row lanes), so that each thread streams a quarter of the rows, as
+    // the 4-wide plans do, and a staged CTA's pipeline runs for more passes
+    // than it takes to fill (c4 in bf16, backward add: 69.2 -> 66.3 us, with
+    // half the CTAs).
+    if (vec == 8 && best_n == 1 && tx < 64 && tx_wide >= 64) tx = 64;
     vcols = tx;
   } else {
     if (nvcol * vec >= E) {

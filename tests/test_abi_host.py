@@ -625,7 +625,10 @@ def test_describe_bwd_bf16_plans(L):
     assert rc == 0
     (p,) = d["plans"]
     assert p["vec"] == 8 and p["inner_kept"] == 1 and (p["n_red"], p["ncol"]) == (96, 1024 * 1024)
-    assert p["ctas"] % (152 * 4) == 0 or p["ctas"] >= 6 * 152 * 4
+    # Every reduced row in one block, 64 column lanes of 8 (each thread a
+    # quarter of the rows), no partial slots.
+    assert (p["tx"], p["ty"], p["rows_per_blk"], p["nslots"]) == (64, 4, 96, 1)
+    assert p["ctas"] == 1024 * 1024 // 512
     # The same in float: 4-wide vectors.
     rc, d = bwd(0, 0, (8, 12, 1024, 1024), (1, 1, 1024, 1024))
     assert rc == 0 and d["plans"][0]["vec"] == 4
