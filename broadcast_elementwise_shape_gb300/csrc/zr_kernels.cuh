@@ -966,8 +966,11 @@ __device__ __forceinline__ uint32_t raw_bits(const Raw<__nv_bfloat16, VEC>& r, i
 }
 
 // The results of one item: forward bfloat16 patterns, backward values.
+// `lanes`: the lanes of the warp that call it for this item (the vote names
+// exactly them).
 template <int VEC>
-__device__ __forceinline__ void gelu_item_fwd(const uint32_t* tab, const Raw<__nv_bfloat16, VEC>& xr,
+__device__ __forceinline__ void gelu_item_fwd(const uint32_t* tab, unsigned lanes,
+                                              const Raw<__nv_bfloat16, VEC>& xr,
                                               uint32_t (&w)[(VEC + 1) / 2]) {
   const unsigned short* th = reinterpret_cast<const unsigned short*>(tab);
   uint32_t bad = 0;
@@ -979,7 +982,7 @@ __device__ __forceinline__ void gelu_item_fwd(const uint32_t* tab, const Raw<__n
     if (i & 1) w[i / 2] |= r << 16;
     else w[i / 2] = r;
   }
-  if (__any_sync(0xffffffffu, bad != 0)) {
+  if (__any_sync(lanes, bad != 0)) {
 #pragma unroll
     for (int i = 0; i < VEC; ++i) {
       const uint32_t bits = raw_bits<VEC>(xr, i);
@@ -991,7 +994,8 @@ __device__ __forceinline__ void gelu_item_fwd(const uint32_t* tab, const Raw<__n
   }
 }
 template <int VEC>
-__device__ __forceinline__ void gelu_item_bwd(const uint32_t* gsm, const Raw<__nv_bfloat16, VEC>& xr,
+__device__ __forceinline__ void gelu_item_bwd(const uint32_t* gsm, unsigned lanes,
+                                              const Raw<__nv_bfloat16, VEC>& xr,
                                               const Raw<__nv_bfloat16, VEC>& gr, Vec<VEC>& y) {
   const float* tf = reinterpret_cast<const float*>(gsm);
   uint32_t bad = 0;
@@ -1001,7 +1005,7 @@ __device__ __forceinline__ void gelu_item_bwd(const uint32_t* gsm, const Raw<__n
     bad |= t & 0x7000u;
     y.v[i] = __fmul_rn(__uint_as_float(raw_bits<VEC>(gr, i) << 16), tf[t & 0x8FFFu]);
   }
-  if (__any_sync(0xffffffffu, bad != 0)) {
+  if (__any_sync(lanes, bad != 0)) {
 #pragma unroll
     for (int i = 0; i < VEC; ++i) {
       const uint32_t bits = raw_bits<VEC>(xr, i);
@@ -1077,17 +1081,18 @@ k_gelu_bf16(const __grid_constant__ EwPlan p) {
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const uint32_t item = it0 + u * kGeluTabThreads + threadIdx.x;
+      const unsigned lanes = __ballot_sync(0xffffffffu, item < end);
       if (item >= end) continue;
       const uint32_t row = fd_div(p.nvcol_div, item);
       const uint32_t col = (item - row * p.nvcol) * VEC;
       const int64_t doff = int64_t(row) * p.rows.stride[kSlotOut][0];
       if constexpr (BWD) {
         Vec<VEC> y;
-        gelu_item_bwd<VEC>(gsm, cur.xr[u], cur.gr[u], y);
+        gelu_item_bwd<VEC>(gsm, lanes, cur.xr[u], cur.gr[u], y);
         store_cols<VEC>(out, doff, p.inner_stride[kSlotOut], col, y);
       } else {
         uint32_t w[(VEC + 1) / 2];
-        gelu_item_fwd<VEC>(gsm, cur.xr[u], w);
+        gelu_item_fwd<VEC>(gsm, lanes, cur.xr[u], w);
         store_raw_bf16<VEC>(out, doff, p.inner_stride[kSlotOut], col, w);
       }
     }
