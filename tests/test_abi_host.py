@@ -705,9 +705,9 @@ def test_emulated_bf16_plans_match_naive(L):
 
 
 def test_trace_prints_the_plan_of_each_call():
-    """With ZR_TRACE=1 every forward, backward and sum-to-shape call that
-    passes planning prints its plan to stderr (here the device checks then
-    fail: no GPU, fake pointers); without it nothing is printed."""
+    """With ZR_TRACE=1 every forward, backward, sum-to-shape and unary call
+    that passes planning prints its plan to stderr (here the device checks
+    then fail: no GPU, fake pointers); without it nothing is printed."""
     import subprocess
     import sys
     code = r"""
@@ -727,7 +727,15 @@ rc1 = L.zr_binary_fwd(0, a, b, ctypes.c_void_p(3 << 40), None, None)
 n = ctypes.c_size_t(1 << 20)
 rc2 = L.zr_binary_bwd(2, T(4 << 40, (64, 32)), a, b, ctypes.c_void_p(5 << 40), ctypes.c_void_p(6 << 40),
                       ctypes.c_void_p(7 << 40), ctypes.byref(n), None)
-print(rc1, rc2)
+L.zr_unary_fwd_t.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_float, zr.ZrTensor,
+                             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+L.zr_unary_bwd_t.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_float, zr.ZrTensor, zr.ZrTensor,
+                             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+big = (16384, 3072)
+rc3 = L.zr_unary_fwd_t(1, 1, 1.0, T(8 << 40, big), ctypes.c_void_p(9 << 40), None, None)
+rc4 = L.zr_unary_bwd_t(1, 1, 1.0, T(10 << 40, big), T(11 << 40, big), ctypes.c_void_p(12 << 40),
+                       None, None)
+print(rc1, rc2, rc3, rc4)
 """ % ROOT
     env = dict(os.environ, ZR_TRACE="1")
     r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env,
@@ -737,6 +745,11 @@ print(rc1, rc2)
     assert lines[0].startswith('zr_trace zr_binary_fwd {"kernel":"flat"'), lines
     assert lines[1].startswith('zr_trace zr_binary_bwd {"plans":[{"kernel":"reduce"'), lines
     json.loads(lines[1].split(" ", 2)[2])
+    # bf16 GeLU on a [16384, 3072] activation: the table kernel, one CTA per SM.
+    for ln, entry in ((lines[2], "zr_unary_fwd"), (lines[3], "zr_unary_bwd")):
+        assert ln.startswith("zr_trace %s " % entry), lines
+        d = json.loads(ln.split(" ", 2)[2])
+        assert d["kernel"] == "gelu_table" and d["ctas"] == 152, d
     rcs = [int(v) for v in r.stdout.split()]
     assert all(rc in (-6, -8) for rc in rcs), rcs  # device checks fail without a GPU
     env["ZR_TRACE"] = "0"
