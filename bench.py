@@ -763,10 +763,17 @@ def run_e2e(args, suite, flush, stream, nbytes, measure_link=True):
     of the ops and downloads behind them, so the host link carries both
     directions at once for most of the step (a forward whose inputs are
     small starts its large download while the next op's large input is
-    still arriving)."""
+    still arriving).  Steps follow one another as a training loop's would:
+    the next step's uploads start while this step's last downloads are still
+    running, each waiting only for what it overwrites (an input buffer for
+    the previous step's last op that read it, an op's outputs for the
+    previous step's download of them).  The inputs (4 GB) are far larger
+    than L2, so no flush is needed between the steps; the value is the steps'
+    bytes over the time from the first step's start to the last step's
+    end."""
     import torch
     h2d = d2h = 0
-    plan = []  # per op: (uploads [(dst, src)], call, downloads [(dst, src)])
+    plan = []  # per op: (uploads [(dst, src)], call, downloads [(dst, src)], last readers)
     for name in suite.dev:
         env = suite.dev[name]
         host_in = set(suite.in_names[name])
@@ -774,13 +781,14 @@ def run_e2e(args, suite, flush, stream, nbytes, measure_link=True):
         calls = [c for c in suite.calls if c[0] == name]
         steps = workloads.STEPS[name]
         assert len(calls) == len(steps)
-        uploaded = set()
-        for step, call in zip(steps, calls):
+        uploaded = {}
+        first = len(plan)
+        for i, (step, call) in enumerate(zip(steps, calls)):
             reads, writes = step_io(step)
             ups, downs = [], []
             for k in reads:
                 if k in host_in and k not in uploaded:
-                    uploaded.add(k)
+                    uploaded[k] = len(ups)
                     # Copy the operand's whole storage (views keep their
                     # layout); the pinned host buffer holds the same bytes
                     # in the device's element type.
@@ -790,7 +798,7 @@ def run_e2e(args, suite, flush, stream, nbytes, measure_link=True):
                         ds, 0, (ds.nbytes() // t.element_size(),), (1,))
                     hp = torch.empty(dflat.numel(), dtype=t.dtype).pin_memory()
                     hp.copy_(dflat)
-                    ups.append((dflat, hp))
+                    ups.append((dflat, hp, k))
                     h2d += hp.numel() * hp.element_size()
             for k in writes:
                 if k in written:
@@ -798,43 +806,66 @@ def run_e2e(args, suite, flush, stream, nbytes, measure_link=True):
                     hp = torch.empty(t.shape, dtype=t.dtype).pin_memory()
                     downs.append((hp, t))
                     d2h += hp.numel() * hp.element_size()
-            plan.append((ups, call, downs))
+            plan.append([ups, call, downs, reads])
+        # For each upload: the op of this workload that reads it last.
+        reads_of = [set(plan[j][3]) for j in range(first, len(plan))]
+        for i in range(first, len(plan)):
+            plan[i][3] = [first + max(j for j, r in enumerate(reads_of) if k in r)
+                          for _dst, _src, k in plan[i][0]]
     s_in = torch.cuda.Stream(device=stream.device)
     s_out = torch.cuda.Stream(device=stream.device)
-    ev = []
     steps = args.e2e_steps if args.e2e_steps else min(50, max(10, args.steps))
     steps = max(1, steps)
-    for k in range(steps + 1):  # first iteration is a warm-up
-        flush()
+    n = len(plan)
+
+    def run(nsteps):
+        """nsteps pipelined steps; returns their start and end events."""
         s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         s.record(stream)
         s_in.wait_event(s)
         s_out.wait_event(s)
-        for ups, call, downs in plan:
-            if ups:
-                with torch.cuda.stream(s_in):
-                    for dst, src in ups:
-                        dst.copy_(src, non_blocking=True)
-                stream.wait_event(s_in.record_event())
-            call[5]()
-            if downs:
-                s_out.wait_event(stream.record_event())
-                with torch.cuda.stream(s_out):
-                    for dst, src in downs:
-                        dst.copy_(src, non_blocking=True)
+        done_call = [None] * n  # previous step's events, per op
+        done_down = [None] * n
+        for _ in range(nsteps):
+            call_ev, down_ev = [None] * n, [None] * n
+            for i, (ups, call, downs, last) in enumerate(plan):
+                if ups:
+                    for j in set(last):
+                        if done_call[j] is not None:
+                            s_in.wait_event(done_call[j])
+                    with torch.cuda.stream(s_in):
+                        for dst, src, _k in ups:
+                            dst.copy_(src, non_blocking=True)
+                    stream.wait_event(s_in.record_event())
+                if done_down[i] is not None:
+                    stream.wait_event(done_down[i])
+                call[5]()
+                call_ev[i] = stream.record_event()
+                if downs:
+                    s_out.wait_event(call_ev[i])
+                    with torch.cuda.stream(s_out):
+                        for dst, src in downs:
+                            dst.copy_(src, non_blocking=True)
+                    down_ev[i] = s_out.record_event()
+            done_call, done_down = call_ev, down_ev
         stream.wait_event(s_out.record_event())
         stream.wait_event(s_in.record_event())
         e.record(stream)
-        if k > 0:
-            ev.append((s, e))
+        return s, e
+
+    flush()
+    run(1)  # warm-up
     torch.cuda.synchronize()
-    ms = statistics.median(s.elapsed_time(e) for s, e in ev)
+    flush()
+    s, e = run(steps)
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / steps
     moved = (h2d + d2h) / (ms * 1e-3) / 1e9
     out = {"value": round(nbytes / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms,
            "steps": steps, "copied_gbs": round(moved, 1),
            "copies": "per op: uploads ahead on one stream, ops on the caller's stream, "
-                     "downloads behind on a third stream"}
+                     "downloads behind on a third stream; steps pipelined"}
     if measure_link:  # this process's own host link (rank 0's at N > 1)
         link = link_rates(stream.device)
         out["link_gbs"] = link
