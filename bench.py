@@ -768,9 +768,9 @@ def run_e2e(args, suite, flush, stream, nbytes, measure_link=True):
     running, each waiting only for what it overwrites (an input buffer for
     the previous step's last op that read it, an op's outputs for the
     previous step's download of them).  The inputs (4 GB) are far larger
-    than L2, so no flush is needed between the steps; the value is the steps'
-    bytes over the time from the first step's start to the last step's
-    end."""
+    than L2, so no flush is needed between the steps.  The step time is the
+    median interval between consecutive steps' ends, an end being an event
+    recorded after the step's last download."""
     import torch
     h2d = d2h = 0
     plan = []  # per op: (uploads [(dst, src)], call, downloads [(dst, src)], last readers)
@@ -819,11 +819,14 @@ def run_e2e(args, suite, flush, stream, nbytes, measure_link=True):
     n = len(plan)
 
     def run(nsteps):
-        """nsteps pipelined steps; returns their start and end events."""
-        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        """nsteps pipelined steps; returns the start event and, per step, an
+        event on the download stream after its last download (so after all
+        of the step's work)."""
+        s = torch.cuda.Event(enable_timing=True)
         s.record(stream)
         s_in.wait_event(s)
         s_out.wait_event(s)
+        ends = []
         done_call = [None] * n  # previous step's events, per op
         done_down = [None] * n
         for _ in range(nsteps):
@@ -848,18 +851,24 @@ def run_e2e(args, suite, flush, stream, nbytes, measure_link=True):
                             dst.copy_(src, non_blocking=True)
                     down_ev[i] = s_out.record_event()
             done_call, done_down = call_ev, down_ev
-        stream.wait_event(s_out.record_event())
-        stream.wait_event(s_in.record_event())
-        e.record(stream)
-        return s, e
+            s_out.wait_event(stream.record_event())
+            s_out.wait_event(s_in.record_event())
+            e = torch.cuda.Event(enable_timing=True)
+            e.record(s_out)
+            ends.append(e)
+        stream.wait_event(ends[-1])
+        return s, ends
 
     flush()
     run(1)  # warm-up
     torch.cuda.synchronize()
     flush()
-    s, e = run(steps)
+    s, ends = run(steps)
     torch.cuda.synchronize()
-    ms = s.elapsed_time(e) / steps
+    # The step time is the median interval between consecutive steps' ends
+    # (the loop's period once it runs; robust to a late copy in one step).
+    marks = [s] + ends
+    ms = statistics.median(a.elapsed_time(b) for a, b in zip(marks[:-1], marks[1:]))
     moved = (h2d + d2h) / (ms * 1e-3) / 1e9
     out = {"value": round(nbytes / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms,

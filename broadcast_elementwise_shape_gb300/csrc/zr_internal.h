@@ -158,12 +158,15 @@ constexpr int kOccGeluFwdWide = 6; // GeLU forward, 8-wide bfloat16 (2 items per
 // GeLU on bfloat16 storage by table (k_gelu_bf16): one CTA of 1024 threads
 // per SM, items per pass 3 (forward) or 2 (backward, two operands) with the
 // next pass's loads in flight (the most that fit in 64 registers without
-// spilling), taken for flat plans of at least 65,536 elements per SM, where
-// each CTA's fill of its tables is small beside its share of the stream.
+// spilling), taken for flat plans of at least 32,768 elements per SM, where
+// each CTA's fill of its table is small beside its share of the stream (on a
+// [2048, 3072] activation the table took the forward from 12.3 to 10.2 us;
+// at [1024, 3072] both paths took 8.4-8.6 us, below that the arithmetic
+// kernel was faster).
 constexpr int kGeluTabThreads = 1024;
 constexpr int kGeluTabUnrollFwd = 3;
 constexpr int kGeluTabUnrollBwd = 2;
-constexpr uint64_t kGeluTabMinElems = uint64_t(kSms) << 16;
+constexpr uint64_t kGeluTabMinElems = uint64_t(kSms) << 15;
 constexpr int kOccRedAddSub = 4;  // k_reduce: add, sub, sum-to-shape
 constexpr int kOccRedMulDiv = 3;  // k_reduce: mul, div
 // k_reduce, cluster variant (no second pass): loads per item are 1 for add,

@@ -370,7 +370,7 @@ int zr_sum_to_shape_t(zr_dtype dtype, zr_tensor in, int32_t ndim_out, const int6
  * 2^-14 of its size plus 2^-120 (backward: 2^-14 of
  * |g| (Phi(x) + |x| phi(x))), so it is the correctly rounded value except
  * next to a rounding boundary.  Large calls over a layout that flattens to at
- * most two dims (at least 65,536 elements per SM) read the results from a
+ * most two dims (at least 32,768 elements per SM) read the results from a
  * table in shared memory that each thread block fills with the same
  * arithmetic, for the 8192 values 2^-24 <= |x| < 256, and evaluate the others
  * in place: the results do not depend on which path ran. */

@@ -800,7 +800,7 @@ def test_emulated_eight_dim_plans_match_naive(L):
 
 
 def test_describe_unary_routes_bf16_gelu_to_its_table(L):
-    """bfloat16 GeLU over a flat layout of at least 65,536 elements per SM
+    """bfloat16 GeLU over a flat layout of at least 32,768 elements per SM
     (152 SMs) reads its results from a table (k_gelu_bf16, one CTA per SM,
     fewer when there are fewer passes of 1024 threads); smaller calls, float
     GeLU, scale and non-flat layouts keep the arithmetic kernels."""
@@ -832,10 +832,10 @@ def test_describe_unary_routes_bf16_gelu_to_its_table(L):
         assert desc(F32, GELU, (16384, 3072), bwd=bwd)["kernel"] == "flat"
         assert desc(BF16, SCALE, (16384, 3072), bwd=bwd)["kernel"] == "flat"
         # Just below and at the size limit.
-        assert desc(BF16, GELU, (152 * 65536 - 8,), bwd=bwd)["kernel"] == "flat"
-        assert desc(BF16, GELU, (152 * 65536,), bwd=bwd)["kernel"] == "gelu_table"
+        assert desc(BF16, GELU, (152 * 32768 - 8,), bwd=bwd)["kernel"] == "flat"
+        assert desc(BF16, GELU, (152 * 32768,), bwd=bwd)["kernel"] == "gelu_table"
     # Odd sizes take 1-element items, row-strided views rows of 8.
-    d = desc(BF16, GELU, (152 * 65536 + 1,))
+    d = desc(BF16, GELU, (152 * 32768 + 1,))
     assert d["kernel"] == "gelu_table" and d["vec"] == 1 and d["ctas"] == 152
     d = desc(BF16, GELU, (2048, 8192), strides=(8200, 1))
     assert d["kernel"] == "gelu_table" and d["vec"] == 8 and d["row_dims"] == 1

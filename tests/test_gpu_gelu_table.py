@@ -21,7 +21,7 @@ import oracle
 
 pytestmark = pytest.mark.gpu
 
-LIMIT = 152 * 65536  # elements from which flat bfloat16 GeLU reads the table
+LIMIT = 152 * 32768  # elements from which flat bfloat16 GeLU reads the table
 
 
 @pytest.fixture(scope="module")
