@@ -674,6 +674,16 @@ def run_per_config(suites, flush, stream, reps, warm=5):
     return per_config, per_op
 
 
+def last_readers(steps):
+    """For each name a workload's steps read: the index of the last step that
+    reads it (the next step's upload of that buffer must wait for it)."""
+    last = {}
+    for i, step in enumerate(steps):
+        for k in step_io(step)[0]:
+            last[k] = i
+    return last
+
+
 def step_io(step):
     """Names a workload step reads and writes."""
     kind = step[0]
@@ -808,10 +818,9 @@ def run_e2e(args, suite, flush, stream, nbytes, measure_link=True):
                     d2h += hp.numel() * hp.element_size()
             plan.append([ups, call, downs, reads])
         # For each upload: the op of this workload that reads it last.
-        reads_of = [set(plan[j][3]) for j in range(first, len(plan))]
+        last = last_readers(steps)
         for i in range(first, len(plan)):
-            plan[i][3] = [first + max(j for j, r in enumerate(reads_of) if k in r)
-                          for _dst, _src, k in plan[i][0]]
+            plan[i][3] = [first + last[k] for _dst, _src, k in plan[i][0]]
     s_in = torch.cuda.Stream(device=stream.device)
     s_out = torch.cuda.Stream(device=stream.device)
     steps = args.e2e_steps if args.e2e_steps else min(50, max(10, args.steps))

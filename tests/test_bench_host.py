@@ -1,5 +1,7 @@
 """Host logic of bench.py that needs no GPU: the per-op copy schedule of the
-end-to-end measurement reads and writes exactly the tensors each step names."""
+end-to-end measurement reads and writes exactly the tensors each step names,
+and each upload of a pipelined step waits for the previous step's last
+reader of that buffer."""
 import os
 import sys
 
@@ -75,3 +77,17 @@ def test_oracle_pool_takes_reduced_size_workloads():
     labels = bench.sample_label(bench.CPU_SAMPLE)
     assert any(x.startswith("c5a[") for x in labels) and any(x.startswith("c5b[") for x in labels)
     assert bench.sample_label(sample)[0] == "c5a[P=2,M=8,Q=16]"
+
+
+def test_pipelined_uploads_wait_for_the_last_reader():
+    """Brute force over every workload: the step an upload must wait for is
+    the last one that reads the buffer, so no later step of the previous
+    iteration reads it after the next iteration overwrites it."""
+    for name, steps in workloads.STEPS.items():
+        last = bench.last_readers(steps)
+        for k, i in last.items():
+            readers = [j for j, st in enumerate(steps) if k in bench.step_io(st)[0]]
+            assert readers and i == readers[-1], (name, k)
+            assert all(k not in bench.step_io(st)[0] for st in steps[i + 1:]), (name, k)
+    # c3: x is read by the forward mul and again by the backward mul.
+    assert bench.last_readers(workloads.STEPS["c3"])["x"] == 3
